@@ -28,7 +28,8 @@ parity pinned by: tests/test_oracle_model.py (torch scaled_dot_product_attention
 with the same mask, hand-computed attention and SwiGLU cases, RoPE's complex
 form and relative-position property, sparse MoE == dense all-experts MoE with
 zeroed gates, joint canvas permutation and global position-shift invariants,
-zero-weight layers reduce to the identity).
+zero-weight layers reduce to the identity, forced routing accepted only
+within tolerance of the top-k boundary).
 """
 from dataclasses import dataclass, replace
 
@@ -116,11 +117,30 @@ def silu(x):
     return x / (1.0 + np.exp(-x))
 
 
-def route(y, wr, k):
-    """Top-k experts (ties -> lower id) and softmax gates over their logits."""
+ROUTING_TOL = 1e-2
+
+
+def route(y, wr, k, forced=None, tol=ROUTING_TOL):
+    """Top-k experts (ties -> lower id) and softmax gates over their logits.
+
+    `forced` [T, k] replays another implementation's expert choice: top-k is
+    an integer decided by floating point, so where router logits are tied
+    within rounding either side of the tie is a correct result.  A forced set
+    is accepted only if it holds k distinct experts whose logits all reach
+    the k-th largest logit minus `tol`; otherwise ValueError.
+    """
     r = y @ np.asarray(wr, np.float64).T                       # [T, E]
     order = np.argsort(-r, axis=1, kind="stable")
     ids = order[:, :k]
+    if forced is not None:
+        forced = np.asarray(forced).astype(np.int64)
+        kth = np.take_along_axis(r, ids[:, -1:], axis=1)[:, 0]
+        ok = np.take_along_axis(r, forced, axis=1).min(axis=1) >= kth - tol
+        ok &= np.array([len(set(row)) == k for row in forced])
+        if not ok.all():
+            raise ValueError(f"forced routing is not a top-{k} choice within {tol} "
+                             f"(tokens {np.nonzero(~ok)[0][:8].tolist()})")
+        ids = forced
     sel = np.take_along_axis(r, ids, axis=1)
     g = np.exp(sel - sel.max(axis=1, keepdims=True))
     return ids.astype(np.int32), g / g.sum(axis=1, keepdims=True), r
@@ -140,16 +160,17 @@ def moe_given_routing(y, ids, gates, W):
     return out
 
 
-def moe(y, W, k):
-    ids, gates, r = route(y, W["wr"], k)
+def moe(y, W, k, forced=None):
+    ids, gates, r = route(y, W["wr"], k, forced)
     return moe_given_routing(y, ids, gates, W), ids, gates, r
 
 
-def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None):
+def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=None):
     """One decoder layer over new tokens h [T, d] at positions pos.
 
     prefix_k/v [S, Hkv, hd] are the cached (rotated) keys/values visible to
-    every new token.  Returns (h_out, k_new, v_new).
+    every new token; forced_routing (optional [T, k]) as in route().
+    Returns (h_out, k_new, v_new).
     """
     T = h.shape[0]
     hd, Hq, Hkv = cfg.head_dim, cfg.n_q_heads, cfg.n_kv_heads
@@ -164,7 +185,7 @@ def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None):
     o = attention(q, K, V, visibility(prefix_k.shape[0], T, mode))
     h = h + o.reshape(T, Hq * hd) @ np.asarray(W["wo"], np.float64).T
     n2 = rmsnorm(h, W["moe_norm"], cfg.rms_eps)
-    y, ids, gates, r = moe(n2, W, cfg.top_k)
+    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing)
     if trace is not None:
         trace.append(dict(n=n, q=q, k=k, v=v, o=o, n2=n2, ids=ids, gates=gates, router=r, y=y))
     return h + y, k, v
@@ -186,20 +207,22 @@ class KVCache:
         self.v[layer] = np.concatenate([self.v[layer], v], axis=0)
 
 
-def forward(W, cfg, ids, pos, cache, mode, append=False, trace=None):
+def forward(W, cfg, ids, pos, cache, mode, append=False, trace=None, routing=None):
     """Run all layers over tokens `ids` at positions `pos` with `cache` as prefix.
 
     `pos` is an int (first position; the tokens then sit at pos, pos+1, ...)
-    or an explicit array of positions.  Returns the final hidden states
-    [T, d] (fp64).  With append=True the new tokens' K/V are added to the
-    cache after the pass (prefill and commit).
+    or an explicit array of positions.  `routing` (optional) is a per-layer
+    list of forced expert choices (see route()).  Returns the final hidden
+    states [T, d] (fp64).  With append=True the new tokens' K/V are added to
+    the cache after the pass (prefill and commit).
     """
     ids = np.asarray(ids)
     pos = pos + np.arange(len(ids)) if np.ndim(pos) == 0 else np.asarray(pos)
     h = np.asarray(W.embed, np.float64)[ids]
     new_kv = []
     for L, WL in enumerate(W.layers):
-        h, k, v = block(h, pos, WL, cfg, cache.k[L], cache.v[L], mode, trace)
+        forced = None if routing is None else routing[L]
+        h, k, v = block(h, pos, WL, cfg, cache.k[L], cache.v[L], mode, trace, forced)
         new_kv.append((k, v))
     if append:
         for L, (k, v) in enumerate(new_kv):
@@ -213,22 +236,22 @@ def logits(W, cfg, h):
     return n @ np.asarray(W.lm_head, np.float64).T
 
 
-def prefill(W, cfg, prompt, p0=0):
+def prefill(W, cfg, prompt, p0=0, routing=None):
     """Encode the prompt with causal attention and cache its K/V (report §1)."""
     cache = KVCache(cfg)
     if len(prompt):
-        forward(W, cfg, prompt, p0, cache, "causal", append=True)
+        forward(W, cfg, prompt, p0, cache, "causal", append=True, routing=routing)
     return cache
 
 
-def canvas_logits(W, cfg, cache, x, p0, trace=None):
+def canvas_logits(W, cfg, cache, x, p0, trace=None, routing=None):
     """One denoising forward: canvas x at positions p0.. (or an explicit
     position array) sees the whole prefix and the whole canvas; nothing is
     cached.  Returns fp64 logits [C, V]."""
-    return logits(W, cfg, forward(W, cfg, x, p0, cache, "bidir", trace=trace))
+    return logits(W, cfg, forward(W, cfg, x, p0, cache, "bidir", trace=trace, routing=routing))
 
 
-def commit_forward(W, cfg, cache, x, p0, mode="causal"):
+def commit_forward(W, cfg, cache, x, p0, mode="causal", routing=None):
     """The single extra forward between canvases: encodes the finished canvas
     and appends its K/V to the prefix cache (report §3.4, the K-1 term)."""
-    forward(W, cfg, x, p0, cache, mode, append=True)
+    forward(W, cfg, x, p0, cache, mode, append=True, routing=routing)

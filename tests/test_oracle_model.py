@@ -195,3 +195,23 @@ def test_zero_output_projections_make_layers_identity():
     e = W.embed[x].astype(np.float64)
     ref = (e / np.sqrt((e * e).mean(axis=1, keepdims=True) + cfg.rms_eps)) @ W.lm_head.astype(np.float64).T
     assert np.allclose(lg, ref, atol=1e-10)
+
+
+def test_forced_routing_accepts_valid_ties_and_rejects_others(small_weights):
+    W = small_weights.layers[0]
+    rng = np.random.default_rng(17)
+    y = rng.standard_normal((12, SMALL.d_model))
+    out, ids, gates, r = model.moe(y, W, SMALL.top_k)
+    same, _, _, _ = model.moe(y, W, SMALL.top_k, forced=ids[:, ::-1])     # order is irrelevant
+    assert np.allclose(same, out, atol=1e-12)
+    # swap the k-th choice for the (k+1)-th: valid only when their logits are within tol
+    order = np.argsort(-r, axis=1, kind="stable")
+    alt = ids.copy()
+    alt[:, -1] = order[:, SMALL.top_k]
+    gap = np.take_along_axis(r, ids[:, -1:], 1)[:, 0] - np.take_along_axis(r, alt[:, -1:], 1)[:, 0]
+    with pytest.raises(ValueError):
+        model.route(y, W["wr"], SMALL.top_k, forced=alt, tol=float(gap.min()) / 2)
+    ok_ids, ok_g, _ = model.route(y, W["wr"], SMALL.top_k, forced=alt, tol=float(gap.max()) + 1e-9)
+    assert np.array_equal(ok_ids, alt) and np.allclose(ok_g.sum(axis=1), 1.0)
+    with pytest.raises(ValueError):                                   # repeated expert
+        model.route(y, W["wr"], SMALL.top_k, forced=np.repeat(ids[:, :1], SMALL.top_k, 1), tol=10.0)
