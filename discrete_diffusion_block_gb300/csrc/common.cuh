@@ -1,0 +1,209 @@
+// Device-side building blocks shared by the kernels of the GB300 decoder:
+// bf16 helpers, the Philox4x32-10 generator, the sampler's fp32 exp/log and
+// the merge of vocabulary-tile partials of the commit / re-noise sampler.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dg {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of the Philox-4x32 S-box
+//   (c0,c1,c2,c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+// with the key advanced by the Weyl increments after each round.
+// ---------------------------------------------------------------------------
+struct U4 {
+  uint32_t w[4];
+};
+
+__host__ __device__ __forceinline__ U4 philox10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  U4 r;
+  r.w[0] = c0; r.w[1] = c1; r.w[2] = c2; r.w[3] = c3;
+  return r;
+}
+
+// Stream tags of the counter's fourth word.
+constexpr uint32_t kTagWeight = 1, kTagInit = 2, kTagGumbel = 3;
+
+// ---------------------------------------------------------------------------
+// Sampler arithmetic.  Every operation is an explicitly rounded IEEE fp32
+// intrinsic so that no contraction or approximation can change the bits.
+//
+// dg_exp: Cody & Waite (1980) range reduction  k = floor(x log2 e + 1/2),
+// r = (x - k C1) - k C2 with ln 2 = C1 + C2, C1 = 355/512 (9 bits, so k C1
+// is exact); e^r by its degree-7 Taylor polynomial (coefficients 1/j!) in
+// Horner form; times 2^k assembled from the exponent bits.  NaN passes,
+// x < -87 gives 0, x > 88 gives +inf.
+//
+// dg_log: x = 2^e m with m in [sqrt(1/2), sqrt(2)]; log m = 2 atanh(s),
+// s = (m-1)/(m+1), by the odd series s + s^3/3 + ... + s^11/11 (Horner in
+// s^2); log x = (e C2 + log m) + e C1.
+// ---------------------------------------------------------------------------
+constexpr double kLn2d = 0.6931471805599453;
+constexpr float kLog2e = (float)(1.0 / kLn2d);
+constexpr float kLn2Hi = (float)(355.0 / 512.0);
+constexpr float kLn2Lo = (float)(kLn2d - 355.0 / 512.0);
+constexpr float kSqrt2 = (float)1.4142135623730951;
+
+__device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
+
+__device__ __forceinline__ float dg_exp(float x) {
+  if (x != x) return x;
+  if (x < -87.0f) return 0.0f;
+  if (x > 88.0f) return __int_as_float(0x7f800000);
+  const float kf = floorf(fadd(fmul(x, kLog2e), 0.5f));
+  float r = fsub(x, fmul(kf, kLn2Hi));
+  r = fsub(r, fmul(kf, kLn2Lo));
+  float p = (float)(1.0 / 5040.0);
+  p = fadd(fmul(p, r), (float)(1.0 / 720.0));
+  p = fadd(fmul(p, r), (float)(1.0 / 120.0));
+  p = fadd(fmul(p, r), (float)(1.0 / 24.0));
+  p = fadd(fmul(p, r), (float)(1.0 / 6.0));
+  p = fadd(fmul(p, r), 0.5f);
+  p = fadd(fmul(p, r), 1.0f);
+  p = fadd(fmul(p, r), 1.0f);
+  const int k = (int)kf;
+  return fmul(p, __int_as_float((k + 127) << 23));
+}
+
+__device__ __forceinline__ float dg_log(float x) {
+  if (x != x) return x;
+  if (x < 0.0f) return __int_as_float(0x7fc00000);
+  if (x == 0.0f) return __int_as_float(0xff800000);
+  if (x == __int_as_float(0x7f800000)) return x;
+  int eadj = 0;
+  if (x < 1.17549435e-38f) {  // subnormal: scale into the normal range
+    x = fmul(x, 8388608.0f);
+    eadj = -23;
+  }
+  const int bits = __float_as_int(x);
+  int e = ((bits >> 23) & 0xff) - 127 + eadj;
+  float m = __int_as_float((bits & 0x7fffff) | 0x3f800000);
+  if (m > kSqrt2) {
+    m = fmul(m, 0.5f);
+    e += 1;
+  }
+  const float s = __fdiv_rn(fsub(m, 1.0f), fadd(m, 1.0f));
+  const float z = fmul(s, s);
+  float q = (float)(1.0 / 11.0);
+  q = fadd(fmul(q, z), (float)(1.0 / 9.0));
+  q = fadd(fmul(q, z), (float)(1.0 / 7.0));
+  q = fadd(fmul(q, z), (float)(1.0 / 5.0));
+  q = fadd(fmul(q, z), (float)(1.0 / 3.0));
+  q = fmul(q, z);
+  float lm = fadd(s, fmul(s, q));
+  lm = fadd(lm, lm);
+  const float ef = (float)e;
+  const float r = fadd(fmul(ef, kLn2Lo), lm);
+  return fadd(r, fmul(ef, kLn2Hi));
+}
+
+// Open-interval uniform of a Philox word: (2 (w >> 9) + 1) * 2^-24.
+__device__ __forceinline__ float open_uniform(uint32_t w) {
+  return fmul((float)(((w >> 9) << 1) | 1u), 5.9604644775390625e-08f);
+}
+
+__device__ __forceinline__ float gumbel(float u) { return -dg_log(-dg_log(u)); }
+
+// ---------------------------------------------------------------------------
+// Vocabulary-tile partials (tiles of 256 entries) and their merge.
+// m = max, a = first index at the max, s = left-to-right fp32 sum of
+// dg_exp(l - m), (gk, gi) = max / first argmax of l + Gumbel noise.
+// ---------------------------------------------------------------------------
+constexpr int kVocabTile = 256;
+
+struct Partial {
+  float m;
+  int a;
+  float s;
+  float gk;
+  int gi;
+};
+
+__device__ __forceinline__ Partial empty_partial() {
+  Partial p;
+  p.m = __int_as_float(0xff800000);
+  p.a = 0;
+  p.s = 0.0f;
+  p.gk = __int_as_float(0xff800000);
+  p.gi = 0;
+  return p;
+}
+
+// Counter word 2 of the Gumbel stream for step n (1-based) of canvas k.
+__host__ __device__ __forceinline__ uint32_t gumbel_ctr2(int canvas, int step) {
+  return ((uint32_t)canvas << 16) | (uint32_t)step;
+}
+
+// Merge of two adjacent ranges, L the lower vocab range.  An empty right
+// operand (m = -inf) leaves L unchanged.
+__device__ __forceinline__ Partial merge_partials(const Partial &L, const Partial &R) {
+  if (!(R.m > __int_as_float(0xff800000))) return L;
+  Partial o;
+  const float M = fmaxf(L.m, R.m);
+  o.m = M;
+  o.s = fadd(fmul(L.s, dg_exp(fsub(L.m, M))), fmul(R.s, dg_exp(fsub(R.m, M))));
+  o.a = (R.m > L.m) ? R.a : L.a;
+  if (R.gk > L.gk) {
+    o.gk = R.gk;
+    o.gi = R.gi;
+  } else {
+    o.gk = L.gk;
+    o.gi = L.gi;
+  }
+  return o;
+}
+
+// Partials planes: m, a, s, gk, gi, each [rows][tiles].
+struct PartialPlanes {
+  float *m;
+  int *a;
+  float *s;
+  float *gk;
+  int *gi;
+  __host__ __device__ static PartialPlanes at(void *base, int rows, int tiles) {
+    PartialPlanes P;
+    const size_t n = (size_t)rows * tiles;
+    P.m = (float *)base;
+    P.a = (int *)(P.m + n);
+    P.s = (float *)(P.a + n);
+    P.gk = (float *)(P.s + n);
+    P.gi = (int *)(P.gk + n);
+    return P;
+  }
+  __device__ __forceinline__ Partial load(size_t idx) const {
+    Partial p;
+    p.m = m[idx];
+    p.a = a[idx];
+    p.s = s[idx];
+    p.gk = gk[idx];
+    p.gi = gi[idx];
+    return p;
+  }
+};
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace dg

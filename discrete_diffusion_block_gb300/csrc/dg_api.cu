@@ -1,0 +1,917 @@
+// C ABI of the decoder library (declared in include/dg.h): model state, the
+// paged KV cache, the per-layer launch sequence and the canvas loop.
+//
+// Procedure (DiffusionGemma report §1-§4 and §3.4; blog "Once Written, a
+// Prefix Becomes History"): the prompt is encoded once with causal attention
+// and its K/V cached; each canvas of C tokens starts as uniform random ids
+// and is refined by denoising forwards in which the canvas sees the whole
+// cached prefix and itself bidirectionally; the sampler commits confident or
+// stable positions and re-noises the rest until the canvas is finished; one
+// extra forward then encodes the finished canvas and appends its K/V, after
+// which it is read-only prefix.
+//
+// KV layout: per layer, K and V pools [n_pages][Hkv][page_size][hd] bf16 with
+// a page table mapping logical page j (tokens j*page_size ...) to a physical
+// page.  During denoising the canvas K/V of the current layer are written
+// into the slots the canvas will occupy once committed (positions
+// prefix .. prefix + C - 1): attention then treats prefix and canvas keys
+// uniformly, and the KV-append forward overwrites those slots with the
+// clean canvas's K/V.
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using dg::bf16;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CK(call)                                                                          \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return fail(DG_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));              \
+  } while (0)
+
+#define CKR(call)                                                                         \
+  do {                                                                                    \
+    int r_ = (call);                                                                      \
+    if (r_ != DG_OK) return r_;                                                           \
+  } while (0)
+
+constexpr int kPrefillChunk = 2048;
+
+struct Layer {
+  bf16 *wqkv = nullptr, *wo = nullptr, *wr = nullptr, *wgu = nullptr, *wd = nullptr;
+  float *attn_norm = nullptr, *moe_norm = nullptr;
+};
+
+double now_s() {
+  return std::chrono::duration<double>(std::chrono::steady_clock::now().time_since_epoch()).count();
+}
+
+}  // namespace
+
+struct dg_model {
+  dg_config cfg;
+  dg_sampler_config sc;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  std::vector<void *> allocs;
+  // weights
+  bf16 *embed = nullptr, *lm_head = nullptr;
+  float *final_norm = nullptr;
+  std::vector<Layer> layers;
+  // KV cache
+  bf16 *k_pool = nullptr, *v_pool = nullptr;
+  int n_pages = 0;
+  size_t layer_pool_elems = 0;
+  int *page_table = nullptr;
+  std::vector<int> page_table_host;
+  float *cos_t = nullptr, *sin_t = nullptr;
+  // scratch for up to Tmax tokens
+  int Tmax = 0;
+  int *ids = nullptr;
+  float *h = nullptr;
+  bf16 *xn = nullptr, *q = nullptr, *o = nullptr, *act = nullptr;
+  float *router = nullptr, *gates = nullptr, *y = nullptr;
+  int *topk = nullptr, *offs = nullptr, *perm_tok = nullptr, *slot_row = nullptr, *work = nullptr,
+      *n_work = nullptr;
+  int max_work = 0;
+  std::vector<int> routing_rows;  // rows routed by the last forward, per layer
+  void *attn_ws = nullptr;
+  size_t attn_ws_bytes = 0;
+  void *partials = nullptr;
+  // canvas state
+  int *x = nullptr, *last = nullptr, *stable = nullptr, *argmax = nullptr, *gumbel = nullptr,
+      *done_dev = nullptr;
+  uint8_t *committed = nullptr;
+  float *conf = nullptr;
+  int *done_host = nullptr;  // pinned
+  int prompt_len = 0, prefix_len = 0, canvas_index = 0, step = 0;
+  bool prefilled = false, canvas_active = false, canvas_done = false;
+  // profiling: launch counts always, event-timed device ms when prof_on
+  bool prof_on = false;
+  double prof_ms[DG_K_CLASSES] = {};
+  int64_t prof_launches[DG_K_CLASSES] = {};
+  struct ProfRec {
+    int cls;
+    cudaEvent_t a, b;
+  };
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> prof_free;
+
+  template <class T>
+  int alloc(T **p, size_t n) {
+    void *v = nullptr;
+    if (n == 0) n = 1;
+    if (cudaMalloc(&v, n * sizeof(T)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(DG_ENOMEM, "cudaMalloc of %zu bytes failed", n * sizeof(T));
+    }
+    allocs.push_back(v);
+    *p = (T *)v;
+    return DG_OK;
+  }
+  bf16 *kpool(int L) { return k_pool + (size_t)L * layer_pool_elems; }
+  bf16 *vpool(int L) { return v_pool + (size_t)L * layer_pool_elems; }
+};
+
+namespace {
+
+cudaEvent_t prof_event(dg_model *m) {
+  if (!m->prof_free.empty()) {
+    cudaEvent_t e = m->prof_free.back();
+    m->prof_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+cudaEvent_t prof_begin(dg_model *m) {
+  if (!m->prof_on) return nullptr;
+  cudaEvent_t a = prof_event(m);
+  if (a) cudaEventRecord(a, m->stream);
+  return a;
+}
+
+void prof_end(dg_model *m, int cls, int n_kernels, cudaEvent_t a) {
+  m->prof_launches[cls] += n_kernels;
+  if (!a) return;
+  cudaEvent_t b = prof_event(m);
+  if (!b) {
+    m->prof_free.push_back(a);
+    return;
+  }
+  cudaEventRecord(b, m->stream);
+  m->prof_pending.push_back({cls, a, b});
+}
+
+// Fold finished event pairs into the per-class totals (stream already synced).
+void prof_collect(dg_model *m) {
+  for (auto &r : m->prof_pending) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) m->prof_ms[r.cls] += ms;
+    cudaGetLastError();
+    m->prof_free.push_back(r.a);
+    m->prof_free.push_back(r.b);
+  }
+  m->prof_pending.clear();
+}
+
+// Launch `call` (one or more kernels of class `cls`) with profiling brackets.
+#define KL(cls, nk, call)                                                                 \
+  do {                                                                                    \
+    cudaEvent_t a_ = prof_begin(m);                                                       \
+    cudaError_t e_ = (call);                                                              \
+    prof_end(m, (cls), (nk), a_);                                                         \
+    if (e_ != cudaSuccess)                                                                \
+      return fail(DG_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));              \
+  } while (0)
+
+#define SYNC(m)                                                                           \
+  do {                                                                                    \
+    CK(cudaStreamSynchronize((m)->stream));                                               \
+    prof_collect(m);                                                                      \
+  } while (0)
+
+int validate(const dg_config *c, const dg_sampler_config *s) {
+  if (!c || !s) return fail(DG_EINVAL, "null config");
+  if (c->n_layers < 1 || c->d_model < 64 || c->d_model % 64)
+    return fail(DG_EINVAL, "d_model must be a positive multiple of 64");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(DG_EINVAL, "head_dim must be 64 or 128");
+  if (c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads)
+    return fail(DG_EINVAL, "n_q_heads must be a multiple of n_kv_heads");
+  if ((c->n_q_heads * c->head_dim) % 64)
+    return fail(DG_EINVAL, "n_q_heads*head_dim must be a multiple of 64");
+  if (c->n_experts < 1 || c->n_experts > 256) return fail(DG_EINVAL, "n_experts must be in [1, 256]");
+  if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts)
+    return fail(DG_EINVAL, "top_k must be in [1, min(16, n_experts)]");
+  if (c->d_ff < 64 || c->d_ff % 64) return fail(DG_EINVAL, "d_ff must be a positive multiple of 64");
+  if (c->vocab < 256 || c->vocab % 256) return fail(DG_EINVAL, "vocab must be a positive multiple of 256");
+  if (c->page_size < 64 || c->page_size % 64)
+    return fail(DG_EINVAL, "page_size must be a positive multiple of 64");
+  if (s->canvas_len < 1 || s->canvas_len > 1024) return fail(DG_EINVAL, "canvas_len must be in [1, 1024]");
+  if (c->max_context < s->canvas_len) return fail(DG_EINVAL, "max_context smaller than one canvas");
+  if (s->budget_N < 1 || s->budget_N > 65535) return fail(DG_EINVAL, "budget_N must be in [1, 65535]");
+  if (s->stable_steps < 1) return fail(DG_EINVAL, "stable_steps must be >= 1");
+  return DG_OK;
+}
+
+// All layers over T tokens already embedded in m->h at positions pos0..;
+// K/V go to the cache at those positions.  kv_only_last: the last layer only
+// needs its K/V (KV-append and prefill).
+int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
+  const dg_config &c = m->cfg;
+  const int d = c.d_model, qd = c.n_q_heads * c.head_dim;
+  cudaStream_t st = m->stream;
+  for (int L = 0; L < c.n_layers; ++L) {
+    const Layer &W = m->layers[L];
+    KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.attn_norm, T, d, c.rms_eps, st));
+    dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), m->page_table, pos0, c.page_size,
+                  c.n_q_heads, c.n_kv_heads, c.head_dim, m->cos_t, m->sin_t};
+    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xn, W.wqkv, T, d, qo, st));
+    if (kv_only_last && L == c.n_layers - 1) break;
+    dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal};
+    KL(DG_K_ATTENTION, dg::attention_launch_count(as),
+       dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
+                     m->attn_ws_bytes, st));
+    KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, st));
+    KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.moe_norm, T, d, c.rms_eps, st));
+    KL(DG_K_ROUTER, 1, dg::gemm_store_f32(m->xn, W.wr, T, d, c.n_experts, m->router, st));
+    int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
+    m->routing_rows[L] = T;
+    KL(DG_K_TOPK, 1, dg::router_topk(m->router, T, c.n_experts, c.top_k, topk, m->gates, st));
+    KL(DG_K_PERMUTE, 1,
+       dg::moe_permute(topk, T, c.top_k, c.n_experts, dg::kExpertTileRows, m->offs, m->perm_tok,
+                       m->slot_row, m->work, m->n_work, st));
+    KL(DG_K_EXPERT_GATE_UP, 1,
+       dg::gemm_expert_gate_up(m->xn, W.wgu, m->perm_tok, m->offs, m->work, m->n_work,
+                               m->max_work, d, c.d_ff, m->act, st));
+    KL(DG_K_EXPERT_DOWN, 1,
+       dg::gemm_expert_down(m->act, W.wd, m->offs, m->work, m->n_work, m->max_work, d, c.d_ff,
+                            m->y, st));
+    KL(DG_K_COMBINE, 1, dg::moe_combine(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, true, st));
+  }
+  return DG_OK;
+}
+
+int fill_model_weights(dg_model *m) {
+  const dg_config &c = m->cfg;
+  const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+  const uint64_t s = c.weight_seed;
+  const float sd = c.init_std;
+  cudaStream_t st = m->stream;
+  CK(dg::fill_weights(m->embed, (uint64_t)c.vocab * d, s, 1, 0, sd, st));
+  CK(dg::fill_weights(m->lm_head, (uint64_t)c.vocab * d, s, 2, 0, sd, st));
+  CK(dg::fill_const(m->final_norm, d, 1.0f, st));
+  for (int L = 0; L < c.n_layers; ++L) {
+    const uint32_t b = 100u + 16u * (uint32_t)L;
+    Layer &W = m->layers[L];
+    CK(dg::fill_weights(W.wqkv, (uint64_t)qd * d, s, b + 0, 0, sd, st));
+    CK(dg::fill_weights(W.wqkv + (size_t)qd * d, (uint64_t)kd * d, s, b + 1, 0, sd, st));
+    CK(dg::fill_weights(W.wqkv + (size_t)(qd + kd) * d, (uint64_t)kd * d, s, b + 2, 0, sd, st));
+    CK(dg::fill_weights(W.wo, (uint64_t)d * qd, s, b + 3, 0, sd, st));
+    CK(dg::fill_moe_weights(W.wr, W.wgu, W.wd, d, c.n_experts, c.d_ff, L, s, sd, st));
+    CK(dg::fill_const(W.attn_norm, d, 1.0f, st));
+    CK(dg::fill_const(W.moe_norm, d, 1.0f, st));
+  }
+  return DG_OK;
+}
+
+int alloc_model(dg_model *m) {
+  const dg_config &c = m->cfg;
+  const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+  const int E = c.n_experts, F = c.d_ff, k = c.top_k, C = m->sc.canvas_len;
+  CKR(m->alloc(&m->embed, (size_t)c.vocab * d));
+  CKR(m->alloc(&m->lm_head, (size_t)c.vocab * d));
+  CKR(m->alloc(&m->final_norm, d));
+  m->layers.resize(c.n_layers);
+  for (auto &W : m->layers) {
+    CKR(m->alloc(&W.wqkv, (size_t)(qd + 2 * kd) * d));
+    CKR(m->alloc(&W.wo, (size_t)d * qd));
+    CKR(m->alloc(&W.wr, (size_t)E * d));
+    CKR(m->alloc(&W.wgu, (size_t)E * 2 * F * d));
+    CKR(m->alloc(&W.wd, (size_t)E * d * F));
+    CKR(m->alloc(&W.attn_norm, d));
+    CKR(m->alloc(&W.moe_norm, d));
+  }
+  m->n_pages = dg::ceil_div(c.max_context, c.page_size);
+  m->layer_pool_elems = (size_t)m->n_pages * kd * c.page_size;
+  CKR(m->alloc(&m->k_pool, m->layer_pool_elems * c.n_layers));
+  CKR(m->alloc(&m->v_pool, m->layer_pool_elems * c.n_layers));
+  CKR(m->alloc(&m->page_table, m->n_pages));
+  m->page_table_host.resize(m->n_pages);
+  for (int i = 0; i < m->n_pages; ++i) m->page_table_host[i] = i;  // single request: in order
+  CKR(m->alloc(&m->cos_t, (size_t)c.max_context * c.head_dim / 2));
+  CKR(m->alloc(&m->sin_t, (size_t)c.max_context * c.head_dim / 2));
+
+  const int T = m->Tmax = C > kPrefillChunk ? C : kPrefillChunk;
+  CKR(m->alloc(&m->ids, T));
+  CKR(m->alloc(&m->h, (size_t)T * d));
+  CKR(m->alloc(&m->xn, (size_t)T * d));
+  CKR(m->alloc(&m->q, (size_t)T * qd));
+  CKR(m->alloc(&m->o, (size_t)T * qd));
+  CKR(m->alloc(&m->router, (size_t)T * E));
+  CKR(m->alloc(&m->topk, (size_t)c.n_layers * T * k));  // per-layer routing record
+  m->routing_rows.assign(c.n_layers, 0);
+  CKR(m->alloc(&m->gates, (size_t)T * k));
+  m->max_work = (int)dg::moe_max_work(T, k, E, dg::kExpertTileRows);
+  CKR(m->alloc(&m->offs, E + 1));
+  CKR(m->alloc(&m->perm_tok, (size_t)T * k));
+  CKR(m->alloc(&m->slot_row, (size_t)T * k));
+  CKR(m->alloc(&m->work, (size_t)2 * m->max_work + (size_t)T * k));
+  CKR(m->alloc(&m->n_work, 1));
+  CKR(m->alloc(&m->act, (size_t)T * k * F));
+  CKR(m->alloc(&m->y, (size_t)T * k * d));
+  size_t ws = 0;
+  const int shapes[3][2] = {{c.max_context - C, C}, {0, C},
+                            {c.max_context - T > 0 ? c.max_context - T : 0, T}};
+  for (auto &sh : shapes) {
+    dg::AttnShape as{sh[0], sh[1], c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, 0};
+    const size_t b = dg::attention_workspace_bytes(as);
+    if (b > ws) ws = b;
+  }
+  m->attn_ws_bytes = ws;
+  CKR(m->alloc((unsigned char **)&m->attn_ws, ws));
+  CKR(m->alloc((unsigned char **)&m->partials, (size_t)C * (c.vocab / dg::kVocabTile) * 20));
+  CKR(m->alloc(&m->x, C));
+  CKR(m->alloc(&m->last, C));
+  CKR(m->alloc(&m->stable, C));
+  CKR(m->alloc(&m->argmax, C));
+  CKR(m->alloc(&m->gumbel, C));
+  CKR(m->alloc(&m->done_dev, 1));
+  CKR(m->alloc(&m->committed, C));
+  CKR(m->alloc(&m->conf, C));
+  if (cudaMallocHost(&m->done_host, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DG_ENOMEM, "cudaMallocHost failed");
+  }
+  return DG_OK;
+}
+
+int check_model(dg_model *m) {
+  if (!m) return fail(DG_EINVAL, "null model");
+  return DG_OK;
+}
+
+int prefill_impl(dg_model *m, const int32_t *prompt, int32_t n) {
+  const dg_config &c = m->cfg;
+  if (n < 0 || (n > 0 && !prompt)) return fail(DG_EINVAL, "bad prompt");
+  if (n + m->sc.canvas_len > c.max_context)
+    return fail(DG_ECAPACITY, "prompt of %d tokens plus a canvas exceeds max_context %d", n,
+                c.max_context);
+  for (int i = 0; i < n; ++i)
+    if (prompt[i] < 0 || prompt[i] >= c.vocab) return fail(DG_EINVAL, "prompt id %d out of range", prompt[i]);
+  for (int p0 = 0; p0 < n; p0 += m->Tmax) {
+    const int T = n - p0 < m->Tmax ? n - p0 : m->Tmax;
+    CK(cudaMemcpyAsync(m->ids, prompt + p0, sizeof(int) * T, cudaMemcpyHostToDevice, m->stream));
+    KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->ids, T, c.d_model, m->stream));
+    CKR(run_layers(m, T, p0, 1, true));
+    SYNC(m);  // the host prompt buffer and m->ids are reused by the next chunk
+  }
+  m->prompt_len = m->prefix_len = n;
+  m->canvas_index = 0;
+  m->prefilled = true;
+  m->canvas_active = m->canvas_done = false;
+  return DG_OK;
+}
+
+// Denoising forward of the current canvas up to the final norm (in m->xn).
+int canvas_forward(dg_model *m) {
+  const dg_config &c = m->cfg;
+  const int C = m->sc.canvas_len;
+  KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, C, c.d_model, m->stream));
+  CKR(run_layers(m, C, m->prefix_len, 0, false));
+  KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, m->final_norm, C, c.d_model, c.rms_eps, m->stream));
+  return DG_OK;
+}
+
+int begin_canvas(dg_model *m) {
+  if (!m->prefilled) return fail(DG_ESTATE, "dg_prefill must come first");
+  if (m->canvas_done) return fail(DG_ESTATE, "canvas finished: call dg_commit_canvas");
+  if (!m->canvas_active) {
+    if (m->prefix_len + m->sc.canvas_len > m->cfg.max_context)
+      return fail(DG_ECAPACITY, "no room for another canvas (prefix %d, max_context %d)",
+                  m->prefix_len, m->cfg.max_context);
+    KL(DG_K_CANVAS_INIT, 1,
+       dg::canvas_init(m->x, m->committed, m->last, m->stable, m->sc.canvas_len, m->cfg.vocab,
+                       m->sc.sample_seed, m->canvas_index, m->stream));
+    m->step = 0;
+    m->canvas_active = true;
+  }
+  return DG_OK;
+}
+
+int denoise_impl(dg_model *m, int32_t *done) {
+  CKR(begin_canvas(m));
+  const dg_config &c = m->cfg;
+  const dg_sampler_config &s = m->sc;
+  const int C = s.canvas_len;
+  m->step += 1;
+  CKR(canvas_forward(m));
+  KL(DG_K_LM_HEAD, 1,
+     dg::gemm_lm_head_partials(m->xn, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
+                               m->canvas_index, m->step, m->partials, m->stream));
+  KL(DG_K_SAMPLER_MERGE, 1,
+     dg::sampler_merge(m->partials, C, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
+  KL(DG_K_SAMPLER_RULE, 1,
+     dg::sampler_rule(m->argmax, m->conf, m->gumbel, C, m->step, s.budget_N, s.stable_steps,
+                      s.adaptive, s.conf_threshold, m->x, m->committed, m->last, m->stable,
+                      m->done_dev, m->stream));
+  CK(cudaMemcpyAsync(m->done_host, m->done_dev, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  m->canvas_done = *m->done_host != 0;
+  if (done) *done = m->canvas_done ? 1 : 0;
+  return DG_OK;
+}
+
+int valid_tokens(const int32_t *ids, int C, int eos) {
+  if (eos < 0) return C;
+  for (int i = 0; i < C; ++i)
+    if (ids[i] == eos) return i;
+  return C;
+}
+
+int commit_impl(dg_model *m, int32_t *out_ids, int32_t *out_valid, bool append) {
+  if (!m->canvas_active || !m->canvas_done) return fail(DG_ESTATE, "canvas not finished");
+  const int C = m->sc.canvas_len;
+  std::vector<int32_t> ids(C);
+  CK(cudaMemcpyAsync(ids.data(), m->x, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  if (out_ids) memcpy(out_ids, ids.data(), sizeof(int) * C);
+  if (out_valid) *out_valid = valid_tokens(ids.data(), C, m->sc.eos_id);
+  if (append) {
+    KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, C, m->cfg.d_model, m->stream));
+    CKR(run_layers(m, C, m->prefix_len, m->sc.commit_causal ? 1 : 0, true));
+    SYNC(m);
+    m->prefix_len += C;
+    m->canvas_index += 1;
+    m->canvas_active = m->canvas_done = false;
+  }
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dg_last_error(void) { return g_err.c_str(); }
+
+int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, void *cuda_stream,
+                  dg_model **out) {
+  if (!out) return fail(DG_EINVAL, "null out");
+  *out = nullptr;
+  CKR(validate(cfg, scfg));
+  dg_model *m = new dg_model();
+  m->cfg = *cfg;
+  m->sc = *scfg;
+  if (cuda_stream) {
+    m->stream = (cudaStream_t)cuda_stream;
+  } else {
+    if (cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaGetLastError();
+      delete m;
+      return fail(DG_ECUDA, "cudaStreamCreate failed");
+    }
+    m->own_stream = true;
+  }
+  int r = alloc_model(m);
+  if (r == DG_OK) r = fill_model_weights(m);
+  if (r == DG_OK) {
+    cudaError_t e = dg::rope_table(m->cos_t, m->sin_t, cfg->max_context, cfg->head_dim,
+                                   cfg->rope_base, m->stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(m->page_table, m->page_table_host.data(), sizeof(int) * m->n_pages,
+                          cudaMemcpyHostToDevice, m->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+    if (e != cudaSuccess) r = fail(DG_ECUDA, "model set-up: %s", cudaGetErrorString(e));
+  }
+  if (r != DG_OK) {
+    std::string keep = g_err;
+    dg_free_model(m);
+    g_err = keep;
+    return r;
+  }
+  *out = m;
+  return DG_OK;
+}
+
+void dg_free_model(dg_model *m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  prof_collect(m);
+  for (cudaEvent_t e : m->prof_free) cudaEventDestroy(e);
+  for (void *p : m->allocs) cudaFree(p);
+  if (m->done_host) cudaFreeHost(m->done_host);
+  if (m->own_stream) cudaStreamDestroy(m->stream);
+  delete m;
+}
+
+int dg_prefill(dg_model *m, const int32_t *prompt_ids, int32_t n) {
+  CKR(check_model(m));
+  return prefill_impl(m, prompt_ids, n);
+}
+
+int dg_denoise_step(dg_model *m, int32_t *done) {
+  CKR(check_model(m));
+  return denoise_impl(m, done);
+}
+
+int dg_commit_canvas(dg_model *m, int32_t *out_ids, int32_t *out_valid) {
+  CKR(check_model(m));
+  return commit_impl(m, out_ids, out_valid, true);
+}
+
+int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_max,
+                int32_t *out_ids, dg_stats *stats) {
+  CKR(check_model(m));
+  if (K_max < 1 || !out_ids) return fail(DG_EINVAL, "K_max >= 1 and out_ids required");
+  const int C = m->sc.canvas_len;
+  const double t0 = now_s();
+  CKR(prefill_impl(m, prompt, n_prompt));
+  const double t1 = now_s();
+  std::vector<int> Ns, Cs;
+  for (int k = 0; k < K_max; ++k) {
+    int done = 0, n = 0;
+    while (!done) {
+      CKR(denoise_impl(m, &done));
+      ++n;
+    }
+    int valid = 0;
+    const bool last = (k == K_max - 1);
+    CKR(commit_impl(m, out_ids + (size_t)k * C, &valid, false));
+    Ns.push_back(n);
+    Cs.push_back(valid);
+    if (valid < C || last) break;
+    CKR(commit_impl(m, nullptr, nullptr, true));
+  }
+  const double t2 = now_s();
+  if (stats) {
+    const int K = (int)Ns.size();
+    long long tok = 0, steps = 0, wsum = 0;
+    for (int i = 0; i < K; ++i) {
+      tok += Cs[i];
+      steps += Ns[i];
+      wsum += (long long)Ns[i] * Cs[i];
+      if (stats->N_k) stats->N_k[i] = Ns[i];
+      if (stats->C_k) stats->C_k[i] = Cs[i];
+    }
+    stats->K = K;
+    stats->total_tokens = (int)tok;
+    stats->total_steps = (int)steps;
+    stats->n_forwards = (int)(steps + K - 1);
+    stats->effective_steps = tok ? (double)wsum / (double)tok : 0.0;
+    stats->tpf = (double)tok / (double)(steps + K - 1);
+    stats->prefill_seconds = t1 - t0;
+    stats->decode_seconds = t2 - t1;
+  }
+  return DG_OK;
+}
+
+int dg_set_sampler(dg_model *m, const dg_sampler_config *scfg) {
+  CKR(check_model(m));
+  CKR(validate(&m->cfg, scfg));
+  if (scfg->canvas_len != m->sc.canvas_len) return fail(DG_EINVAL, "canvas_len is fixed at init");
+  m->sc = *scfg;
+  return DG_OK;
+}
+
+int dg_rewind(dg_model *m, int32_t n_prefix) {
+  CKR(check_model(m));
+  if (!m->prefilled) return fail(DG_ESTATE, "nothing cached");
+  if (n_prefix < m->prompt_len || n_prefix > m->prefix_len ||
+      (n_prefix - m->prompt_len) % m->sc.canvas_len)
+    return fail(DG_EINVAL, "n_prefix must be the prompt plus whole committed canvases");
+  m->prefix_len = n_prefix;
+  m->canvas_index = (n_prefix - m->prompt_len) / m->sc.canvas_len;
+  m->canvas_active = m->canvas_done = false;
+  return DG_OK;
+}
+
+int dg_read_canvas(dg_model *m, int32_t *ids, uint8_t *committed, int32_t *last_argmax,
+                   int32_t *stable, int32_t *step, int32_t *canvas_index, int32_t *prefix_len) {
+  CKR(check_model(m));
+  const int C = m->sc.canvas_len;
+  if (ids) CK(cudaMemcpyAsync(ids, m->x, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  if (committed) CK(cudaMemcpyAsync(committed, m->committed, C, cudaMemcpyDeviceToHost, m->stream));
+  if (last_argmax)
+    CK(cudaMemcpyAsync(last_argmax, m->last, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  if (stable) CK(cudaMemcpyAsync(stable, m->stable, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  if (step) *step = m->step;
+  if (canvas_index) *canvas_index = m->canvas_index;
+  if (prefix_len) *prefix_len = m->prefix_len;
+  return DG_OK;
+}
+
+int dg_write_canvas(dg_model *m, const int32_t *ids, const uint8_t *committed,
+                    const int32_t *last_argmax, const int32_t *stable, int32_t step,
+                    int32_t canvas_index) {
+  CKR(check_model(m));
+  if (!m->prefilled) return fail(DG_ESTATE, "dg_prefill must come first");
+  if (!ids || !committed || !last_argmax || !stable || step < 0 || canvas_index < 0)
+    return fail(DG_EINVAL, "all state arrays are required");
+  const int C = m->sc.canvas_len;
+  for (int i = 0; i < C; ++i)
+    if (ids[i] < 0 || ids[i] >= m->cfg.vocab) return fail(DG_EINVAL, "id out of range");
+  CK(cudaMemcpyAsync(m->x, ids, sizeof(int) * C, cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(m->committed, committed, C, cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(m->last, last_argmax, sizeof(int) * C, cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(m->stable, stable, sizeof(int) * C, cudaMemcpyHostToDevice, m->stream));
+  SYNC(m);
+  m->step = step;
+  m->canvas_index = canvas_index;
+  m->canvas_active = true;
+  m->canvas_done = false;
+  return DG_OK;
+}
+
+int dg_read_step_outputs(dg_model *m, int32_t *argmax, float *conf, int32_t *gumbel) {
+  CKR(check_model(m));
+  const int C = m->sc.canvas_len;
+  if (argmax) CK(cudaMemcpyAsync(argmax, m->argmax, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  if (conf) CK(cudaMemcpyAsync(conf, m->conf, sizeof(float) * C, cudaMemcpyDeviceToHost, m->stream));
+  if (gumbel) CK(cudaMemcpyAsync(gumbel, m->gumbel, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  return DG_OK;
+}
+
+int dg_canvas_logits(dg_model *m, float *logits_dev) {
+  CKR(check_model(m));
+  if (!logits_dev) return fail(DG_EINVAL, "null logits");
+  CKR(begin_canvas(m));
+  CKR(canvas_forward(m));
+  const dg_config &c = m->cfg;
+  KL(DG_K_LM_HEAD, 1,
+     dg::gemm_store_f32(m->xn, m->lm_head, m->sc.canvas_len, c.d_model, c.vocab, logits_dev,
+                        m->stream));
+  SYNC(m);
+  return DG_OK;
+}
+
+int dg_read_kv(dg_model *m, int32_t layer, int32_t pos0, int32_t n, uint16_t *k_out,
+               uint16_t *v_out) {
+  CKR(check_model(m));
+  const dg_config &c = m->cfg;
+  if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > m->n_pages * c.page_size)
+    return fail(DG_EINVAL, "bad range");
+  const int hd = c.head_dim, Hkv = c.n_kv_heads, pg = c.page_size;
+  for (int t = 0; t < n; ++t) {
+    const int p = pos0 + t;
+    const size_t base = (size_t)m->page_table_host[p / pg] * Hkv * pg * hd + (size_t)(p % pg) * hd;
+    for (int h = 0; h < Hkv; ++h) {
+      const size_t off = base + (size_t)h * pg * hd;
+      const size_t dst = ((size_t)t * Hkv + h) * hd;
+      if (k_out)
+        CK(cudaMemcpyAsync(k_out + dst, m->kpool(layer) + off, hd * 2, cudaMemcpyDeviceToHost, m->stream));
+      if (v_out)
+        CK(cudaMemcpyAsync(v_out + dst, m->vpool(layer) + off, hd * 2, cudaMemcpyDeviceToHost, m->stream));
+    }
+  }
+  SYNC(m);
+  return DG_OK;
+}
+
+int dg_read_routing(dg_model *m, int32_t layer, int32_t *ids, int32_t max_rows, int32_t *n_rows) {
+  CKR(check_model(m));
+  if (layer < 0 || layer >= m->cfg.n_layers) return fail(DG_EINVAL, "bad layer");
+  const int rows = m->routing_rows[layer];
+  if (n_rows) *n_rows = rows;
+  if (ids) {
+    const int n = rows < max_rows ? rows : max_rows;
+    CK(cudaMemcpyAsync(ids, m->topk + (size_t)layer * m->Tmax * m->cfg.top_k,
+                       sizeof(int) * (size_t)n * m->cfg.top_k, cudaMemcpyDeviceToHost, m->stream));
+    SYNC(m);
+  }
+  return DG_OK;
+}
+
+int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t *n_pages) {
+  CKR(check_model(m));
+  const int used = dg::ceil_div(m->prefix_len + (m->canvas_active ? m->sc.canvas_len : 0),
+                                m->cfg.page_size);
+  if (n_pages) *n_pages = used;
+  if (table) {
+    std::vector<int> dev(m->n_pages);
+    CK(cudaMemcpyAsync(dev.data(), m->page_table, sizeof(int) * m->n_pages, cudaMemcpyDeviceToHost,
+                       m->stream));
+    SYNC(m);
+    for (int i = 0; i < used && i < max_entries; ++i) table[i] = dev[i];
+  }
+  return DG_OK;
+}
+
+int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, size_t *bytes) {
+  CKR(check_model(m));
+  const dg_config &c = m->cfg;
+  const size_t d = c.d_model, qd = (size_t)c.n_q_heads * c.head_dim,
+               kd = (size_t)c.n_kv_heads * c.head_dim;
+  const size_t E = c.n_experts, F = c.d_ff;
+  const bool per_layer = which >= DG_W_WQKV;
+  if (per_layer && (layer < 0 || layer >= c.n_layers)) return fail(DG_EINVAL, "bad layer");
+  void *p = nullptr;
+  size_t b = 0;
+  switch (which) {
+    case DG_W_EMBED: p = m->embed; b = (size_t)c.vocab * d * 2; break;
+    case DG_W_LM_HEAD: p = m->lm_head; b = (size_t)c.vocab * d * 2; break;
+    case DG_W_FINAL_NORM: p = m->final_norm; b = d * 4; break;
+    case DG_W_WQKV: p = m->layers[layer].wqkv; b = (qd + 2 * kd) * d * 2; break;
+    case DG_W_WO: p = m->layers[layer].wo; b = d * qd * 2; break;
+    case DG_W_ROUTER: p = m->layers[layer].wr; b = E * d * 2; break;
+    case DG_W_GATE_UP: p = m->layers[layer].wgu; b = E * 2 * F * d * 2; break;
+    case DG_W_DOWN: p = m->layers[layer].wd; b = E * d * F * 2; break;
+    case DG_W_ATTN_NORM: p = m->layers[layer].attn_norm; b = d * 4; break;
+    case DG_W_MOE_NORM: p = m->layers[layer].moe_norm; b = d * 4; break;
+    default: return fail(DG_EINVAL, "unknown weight %d", which);
+  }
+  if (dev_ptr) *dev_ptr = p;
+  if (bytes) *bytes = b;
+  return DG_OK;
+}
+
+const char *dg_kernel_class_name(int32_t cls) {
+  static const char *names[DG_K_CLASSES] = {
+      "embed", "rmsnorm", "qkv_rope", "attention", "o_proj", "router", "topk", "permute",
+      "expert_gate_up", "expert_down", "combine", "lm_head", "sampler_merge", "sampler_rule",
+      "canvas_init"};
+  return (cls >= 0 && cls < DG_K_CLASSES) ? names[cls] : "";
+}
+
+int dg_profile(dg_model *m, int32_t enable) {
+  CKR(check_model(m));
+  SYNC(m);
+  m->prof_on = enable != 0;
+  if (m->prof_on) {
+    for (int i = 0; i < DG_K_CLASSES; ++i) {
+      m->prof_ms[i] = 0.0;
+      m->prof_launches[i] = 0;
+    }
+  }
+  return DG_OK;
+}
+
+int dg_profile_read(dg_model *m, double *ms, int64_t *launches) {
+  CKR(check_model(m));
+  SYNC(m);
+  for (int i = 0; i < DG_K_CLASSES; ++i) {
+    if (ms) ms[i] = m->prof_ms[i];
+    if (launches) launches[i] = m->prof_launches[i];
+  }
+  return DG_OK;
+}
+
+// ---- kernel-level entry points ----------------------------------------------
+
+int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor_id, uint64_t e0,
+                       float std_dev, void *stream) {
+  if (!dst && n) return fail(DG_EINVAL, "null dst");
+  CK(dg::fill_weights((bf16 *)dst, n, seed, tensor_id, e0, std_dev, (cudaStream_t)stream));
+  return DG_OK;
+}
+
+size_t dg_op_attention_workspace_bytes(int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
+                                       int32_t n_kv_heads, int32_t head_dim) {
+  if (n_kv_heads < 1 || n_new < 0 || n_prefix < 0) return 0;
+  dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, 64, 0};
+  return dg::attention_workspace_bytes(as);
+}
+
+int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *page_table, int32_t n_prefix, int32_t n_new,
+                           int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                           int32_t page_size, int32_t causal, uint16_t *out, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  if (!q || !k_pool || !v_pool || !page_table || !out) return fail(DG_EINVAL, "null pointer");
+  if (n_prefix < 0 || n_new < 0 || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
+      (head_dim != 64 && head_dim != 128) || page_size < 64 || page_size % 64)
+    return fail(DG_EINVAL, "unsupported attention shape");
+  dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, page_size, causal ? 1 : 0};
+  if (workspace_bytes < dg::attention_workspace_bytes(as)) return fail(DG_EINVAL, "workspace too small");
+  CK(dg::attention((const bf16 *)q, (const bf16 *)k_pool, (const bf16 *)v_pool, page_table, as,
+                   (bf16 *)out, workspace, workspace_bytes, (cudaStream_t)stream));
+  return DG_OK;
+}
+
+}  // extern "C"
+
+namespace {
+struct MoeWs {
+  float *router;
+  int *offs, *perm_tok, *slot_row, *work, *n_work;
+  bf16 *act;
+  float *y_rows;
+  size_t bytes;
+  int max_work;
+};
+MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
+  MoeWs w{};
+  unsigned char *p = (unsigned char *)base;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    void *r = p ? p + off : nullptr;
+    off += (bytes + 255) & ~(size_t)255;
+    return r;
+  };
+  w.max_work = (int)dg::moe_max_work(T, k, E, dg::kExpertTileRows);
+  w.router = (float *)take((size_t)T * E * 4);
+  w.offs = (int *)take((size_t)(E + 1) * 4);
+  w.perm_tok = (int *)take((size_t)T * k * 4);
+  w.slot_row = (int *)take((size_t)T * k * 4);
+  w.work = (int *)take(((size_t)2 * w.max_work + (size_t)T * k) * 4);
+  w.n_work = (int *)take(4);
+  w.act = (bf16 *)take((size_t)T * k * F * 2);
+  w.y_rows = (float *)take((size_t)T * k * d * 4);
+  w.bytes = off;
+  return w;
+}
+}  // namespace
+
+extern "C" {
+
+size_t dg_op_moe_workspace_bytes(int32_t T, int32_t d, int32_t n_experts, int32_t top_k,
+                                 int32_t d_ff) {
+  if (T < 0 || d < 1 || n_experts < 1 || top_k < 1 || d_ff < 1) return 0;
+  return moe_layout(nullptr, T, d, n_experts, top_k, d_ff).bytes;
+}
+
+int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_gate_up,
+              const uint16_t *w_down, int32_t T, int32_t d, int32_t n_experts, int32_t top_k,
+              int32_t d_ff, float *y, int32_t *expert_ids, float *gates, void *workspace,
+              size_t workspace_bytes, void *stream) {
+  if (!xn || !w_router || !w_gate_up || !w_down || !y || !expert_ids || !gates || !workspace)
+    return fail(DG_EINVAL, "null pointer");
+  if (T < 1 || d % 64 || d_ff % 64 || n_experts < 1 || n_experts > 256 || top_k < 1 ||
+      top_k > 16 || top_k > n_experts)
+    return fail(DG_EINVAL, "unsupported MoE shape");
+  MoeWs w = moe_layout(workspace, T, d, n_experts, top_k, d_ff);
+  if (workspace_bytes < w.bytes) return fail(DG_EINVAL, "workspace too small");
+  cudaStream_t st = (cudaStream_t)stream;
+  CK(dg::gemm_store_f32((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, w.router, st));
+  CK(dg::router_topk(w.router, T, n_experts, top_k, expert_ids, gates, st));
+  CK(dg::moe_permute(expert_ids, T, top_k, n_experts, dg::kExpertTileRows, w.offs, w.perm_tok,
+                     w.slot_row, w.work, w.n_work, st));
+  CK(dg::gemm_expert_gate_up((const bf16 *)xn, (const bf16 *)w_gate_up, w.perm_tok, w.offs, w.work,
+                             w.n_work, w.max_work, d, d_ff, w.act, st));
+  CK(dg::gemm_expert_down(w.act, (const bf16 *)w_down, w.offs, w.work, w.n_work, w.max_work, d,
+                          d_ff, w.y_rows, st));
+  CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));
+  return DG_OK;
+}
+
+int dg_op_fill_moe_weights(uint16_t *w_router, uint16_t *w_gate_up, uint16_t *w_down, int32_t d,
+                           int32_t n_experts, int32_t d_ff, int32_t layer, uint64_t seed,
+                           float std_dev, void *stream) {
+  if (!w_router || !w_gate_up || !w_down || d_ff % 64 || layer < 0) return fail(DG_EINVAL, "bad arguments");
+  CK(dg::fill_moe_weights((bf16 *)w_router, (bf16 *)w_gate_up, (bf16 *)w_down, d, n_experts, d_ff,
+                          layer, seed, std_dev, (cudaStream_t)stream));
+  return DG_OK;
+}
+
+int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *w_out, int32_t rows, int32_t d,
+                           int32_t V, uint64_t sample_seed, int32_t canvas, int32_t step,
+                           void *partials, void *stream) {
+  if (!xn || !w_out || !partials || rows < 1 || d % 64 || V % 256 || V < 256)
+    return fail(DG_EINVAL, "bad arguments");
+  CK(dg::gemm_lm_head_partials((const bf16 *)xn, (const bf16 *)w_out, rows, d, V, sample_seed,
+                               canvas, step, partials, (cudaStream_t)stream));
+  return DG_OK;
+}
+
+int dg_op_logits_partials(const float *logits, int32_t rows, int32_t V, uint64_t sample_seed,
+                          int32_t canvas, int32_t step, void *partials, void *stream) {
+  if (!logits || !partials || rows < 1 || V % 256 || V < 256) return fail(DG_EINVAL, "bad arguments");
+  CK(dg::logits_partials(logits, rows, V, sample_seed, canvas, step, partials, (cudaStream_t)stream));
+  return DG_OK;
+}
+
+int dg_op_sampler_update(const void *partials, int32_t C, int32_t V, int32_t step,
+                         const dg_sampler_config *scfg, int32_t *x, uint8_t *committed,
+                         int32_t *last_argmax, int32_t *stable, int32_t *argmax, float *conf,
+                         int32_t *gumbel, int32_t *done_dev, void *stream) {
+  if (!partials || !scfg || !x || !committed || !last_argmax || !stable || !argmax || !conf ||
+      !gumbel || !done_dev || C < 1 || C > 1024 || V % 256 || V < 256 || step < 1)
+    return fail(DG_EINVAL, "bad arguments");
+  cudaStream_t st = (cudaStream_t)stream;
+  CK(dg::sampler_merge(partials, C, V, argmax, conf, gumbel, st));
+  CK(dg::sampler_rule(argmax, conf, gumbel, C, step, scfg->budget_N, scfg->stable_steps,
+                      scfg->adaptive, scfg->conf_threshold, x, committed, last_argmax, stable,
+                      done_dev, st));
+  return DG_OK;
+}
+
+int dg_op_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool,
+                    uint16_t *v_pool, const int32_t *page_table, int32_t n_layers,
+                    int32_t n_pages, int32_t pos0, int32_t n_new, int32_t n_kv_heads,
+                    int32_t head_dim, int32_t page_size, void *stream) {
+  if (!k_new || !v_new || !k_pool || !v_pool || !page_table || head_dim % 8 || n_layers < 1 ||
+      pos0 < 0 || n_new < 0 || pos0 + n_new > n_pages * page_size)
+    return fail(DG_EINVAL, "bad arguments");
+  CK(dg::kv_append((const bf16 *)k_new, (const bf16 *)v_new, (bf16 *)k_pool, (bf16 *)v_pool,
+                   page_table, n_layers, n_pages, pos0, n_new, n_kv_heads, head_dim, page_size,
+                   (cudaStream_t)stream));
+  return DG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Host-side launchers shared between the translation units of libdg.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dg.h"
+#include "common.cuh"
+
+namespace dg {
+
+// ---- misc kernels (kernels_misc.cu) ---------------------------------------
+cudaError_t fill_weights(bf16 *dst, uint64_t n, uint64_t seed, uint32_t tid, uint64_t e0,
+                         float std_dev, cudaStream_t st);
+cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F, int layer,
+                             uint64_t seed, float std_dev, cudaStream_t st);
+cudaError_t fill_const(float *dst, size_t n, float v, cudaStream_t st);
+cudaError_t rope_table(float *cos_t, float *sin_t, int max_pos, int head_dim, float base,
+                       cudaStream_t st);
+cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
+                        uint64_t seed, int canvas, cudaStream_t st);
+cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st);
+cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
+                         cudaStream_t st);
+cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, float *gates,
+                        cudaStream_t st);
+// Sorts the T*k (token, slot) pairs by expert.  Outputs: offs[E+1], perm_tok[T*k]
+// (token of each sorted row), slot_row[T*k] (sorted row of pair t*k+s),
+// work[2*max_work] = (expert, first row) tiles of `tile_rows`, *n_work.  The
+// per-pair ranks are kept behind the work list: `work` holds
+// 2 * moe_max_work() + T*k ints.
+cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
+                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st);
+size_t moe_max_work(int T, int k, int E, int tile_rows);
+cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
+                        int k, int d, bool accumulate, cudaStream_t st);
+cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
+                      const int *page_table, int L, int n_pages, int pos0, int n, int Hkv, int hd,
+                      int pg, cudaStream_t st);
+
+// ---- GEMM-based layer pieces (kernels_gemm.cu) -----------------------------
+struct QkvOut {
+  bf16 *q;                // [T][Hq*hd]
+  bf16 *k_pool, *v_pool;  // layer slice [n_pages][Hkv][pg][hd]
+  const int *page_table;
+  int pos0, pg, Hq, Hkv, hd;
+  const float *cos_t, *sin_t;  // [max_pos][hd/2]
+};
+cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o,
+                     cudaStream_t st);
+cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h,
+                          cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
+cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out,
+                           cudaStream_t st);  // out[T][N] = act . w^T
+cudaError_t gemm_expert_gate_up(const bf16 *xn, const bf16 *wgu, const int *perm_tok,
+                                const int *offs, const int *work, const int *n_work,
+                                int max_work, int d, int F, bf16 *act, cudaStream_t st);
+cudaError_t gemm_expert_down(const bf16 *act, const bf16 *wd, const int *offs, const int *work,
+                             const int *n_work, int max_work, int d, int F, float *y,
+                             cudaStream_t st);
+constexpr int kExpertTileRows = 32;  // token rows per expert GEMM tile
+cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *w_out, int T, int d, int V,
+                                  uint64_t seed, int canvas, int step, void *partials,
+                                  cudaStream_t st);
+
+// ---- sampler (kernels_sampler.cu) -------------------------------------------
+cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,
+                            int step, void *partials, cudaStream_t st);
+cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,
+                          int *gumbel, cudaStream_t st);
+cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
+                         int budget_N, int stable_steps, int adaptive, float conf_threshold,
+                         int *x, uint8_t *committed, int *last, int *stable, int *done,
+                         cudaStream_t st);
+
+// ---- attention (kernels_attn.cu) -------------------------------------------
+struct AttnShape {
+  int n_prefix, n_new, Hq, Hkv, hd, pg, causal;
+};
+size_t attention_workspace_bytes(const AttnShape &s);
+int attention_launch_count(const AttnShape &s);
+cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const int *page_table,
+                      const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st);
+
+}  // namespace dg

@@ -1,0 +1,350 @@
+// Small kernels of the decoder: seeded weights, canvas initialisation,
+// embedding gather, RMSNorm, RoPE tables, MoE routing / permutation /
+// combination, KV append.
+#include <math.h>
+
+#include "internal.h"
+
+namespace dg {
+
+namespace {
+
+inline int grid_for(size_t n, int threads, int cap = 152 * 32) {
+  size_t b = (n + threads - 1) / threads;
+  if (b < 1) b = 1;
+  return (int)(b < (size_t)cap ? b : (size_t)cap);
+}
+
+// ---- seeded synthetic weights ---------------------------------------------
+// element e of tensor `tid`: Irwin-Hall(4) over one Philox4x32-10 call at
+// counter (e mod 2^32, e div 2^32, tid, 1), scaled to the requested std and
+// rounded to bf16.
+__device__ __forceinline__ bf16 weight_element(uint64_t e, uint32_t tid, uint32_t k0, uint32_t k1,
+                                               float scale) {
+  const U4 w = philox10((uint32_t)e, (uint32_t)(e >> 32), tid, kTagWeight, k0, k1);
+  const int s = (int)(w.w[0] >> 9) + (int)(w.w[1] >> 9) + (int)(w.w[2] >> 9) + (int)(w.w[3] >> 9);
+  return __float2bfloat16_rn(__fmul_rn((float)(s - (1 << 24)), scale));
+}
+
+__global__ void fill_weights_kernel(bf16 *dst, uint64_t n, uint32_t k0, uint32_t k1, uint32_t tid,
+                                    uint64_t e0, float scale) {
+  for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
+       j += (uint64_t)gridDim.x * blockDim.x)
+    dst[j] = weight_element(e0 + j, tid, k0, k1, scale);
+}
+
+// W_gate / W_up (logical [E][F][d]) into the interleaved [E][F/64][2][64][d].
+__global__ void fill_gate_up_kernel(bf16 *dst, int E, int F, int d, uint32_t k0, uint32_t k1,
+                                    uint32_t tid_gate, uint32_t tid_up, float scale) {
+  const uint64_t n = (uint64_t)E * 2 * F * d;
+  for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
+       j += (uint64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(j % d);
+    uint64_t rest = j / d;
+    const int r = (int)(rest % 64);
+    rest /= 64;
+    const int which = (int)(rest % 2);
+    rest /= 2;
+    const int fb = (int)(rest % (F / 64));
+    const int e = (int)(rest / (F / 64));
+    const uint64_t logical = ((uint64_t)e * F + fb * 64 + r) * d + c;
+    dst[j] = weight_element(logical, which ? tid_up : tid_gate, k0, k1, scale);
+  }
+}
+
+__global__ void fill_const_kernel(float *dst, size_t n, float v) {
+  for (size_t j = blockIdx.x * (size_t)blockDim.x + threadIdx.x; j < n;
+       j += (size_t)gridDim.x * blockDim.x)
+    dst[j] = v;
+}
+
+// cos/sin of pos * base^(-2j/hd), evaluated in double, stored fp32.
+__global__ void rope_table_kernel(float *ct, float *stt, int max_pos, int half, int hd,
+                                  double base) {
+  const size_t n = (size_t)max_pos * half;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int p = (int)(i / half), j = (int)(i % half);
+    const double th = pow(base, -2.0 * j / hd);
+    double s, c;
+    sincos((double)p * th, &s, &c);
+    ct[i] = (float)c;
+    stt[i] = (float)s;
+  }
+}
+
+// x_1 ~ Unif(V^C): id = floor(word0 * V / 2^32), word0 of Philox at (i, 0, k, 2).
+__global__ void canvas_init_kernel(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
+                                   uint32_t k0, uint32_t k1, int canvas) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= C) return;
+  const U4 w = philox10((uint32_t)i, 0u, (uint32_t)canvas, kTagInit, k0, k1);
+  x[i] = (int)(((uint64_t)w.w[0] * (uint64_t)V) >> 32);
+  committed[i] = 0;
+  last[i] = -1;
+  stable[i] = 0;
+}
+
+__global__ void embed_kernel(float *h, const bf16 *table, const int *ids, int d) {
+  const int t = blockIdx.x;
+  const bf16 *row = table + (size_t)ids[t] * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) h[(size_t)t * d + c] = __bfloat162float(row[c]);
+}
+
+// y = x / sqrt(mean(x^2) + eps) * g, fp32 statistics, bf16 output.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(bf16 *out, const float *h, const float *g,
+                                                      int d, float eps) {
+  const int t = blockIdx.x;
+  const float *x = h + (size_t)t * d;
+  float ss = 0.0f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) ss += x[c] * x[c];
+  __shared__ float red[8];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / d + eps);
+  for (int c = threadIdx.x; c < d; c += blockDim.x)
+    out[(size_t)t * d + c] = __float2bfloat16_rn(x[c] * inv * g[c]);
+}
+
+// top-k of E router logits per token (value desc, expert id asc), softmax
+// gates over the selected logits.  One warp per token, E <= 256, k <= 16.
+// An unordered logit (NaN) never wins a comparison but a still-unselected
+// expert is always taken over none, so every emitted id is in [0, E).
+__global__ void topk_kernel(const float *logits, int T, int E, int k, int *ids, float *gates) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  float v[8];
+  unsigned taken = 0;  // bit j: expert lane + 32 j already selected
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? logits[(size_t)warp * E + e] : 0.0f;
+  }
+  float sel[16];
+  int sid[16];
+  for (int s = 0; s < k; ++s) {
+    float bv = 0.0f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u) && (bi == 0x7fffffff || v[j] > bv || (v[j] == bv && e < bi))) {
+        bv = v[j];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    sel[s] = bv;
+    sid[s] = bi;
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+  }
+  if (lane == 0) {
+    float sum = 0.0f;
+    for (int s = 0; s < k; ++s) sum += expf(sel[s] - sel[0]);
+    for (int s = 0; s < k; ++s) {
+      ids[(size_t)warp * k + s] = sid[s];
+      gates[(size_t)warp * k + s] = expf(sel[s] - sel[0]) / sum;
+    }
+  }
+}
+
+// Stable counting sort of the T*k (token, slot) pairs by expert, done by one
+// block: warp w owns experts w, w+32, ...; ranks inside an expert follow the
+// pair index (ballot prefix counts), so the order is deterministic.
+constexpr int kPermThreads = 1024;
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, int TK, int k, int E,
+                                                               int tile_rows, int *offs,
+                                                               int *perm_tok, int *slot_row,
+                                                               int *work, int *n_work, int *rank) {
+  __shared__ int cnt[257], toff[257], soff[257];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += kPermThreads / 32) {
+    int c = 0;
+    for (int base = 0; base < TK; base += 32) {
+      const int i = base + lane;
+      const bool hit = i < TK && ids[i] == e;
+      const unsigned b = __ballot_sync(0xffffffffu, hit);
+      if (hit) rank[i] = c + __popc(b & ((1u << lane) - 1u));
+      c += __popc(b);
+    }
+    if (lane == 0) cnt[e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, w = 0;
+    for (int e = 0; e < E; ++e) {
+      offs[e] = o;
+      soff[e] = o;
+      toff[e] = w;
+      o += cnt[e];
+      w += (cnt[e] + tile_rows - 1) / tile_rows;
+    }
+    offs[E] = o;
+    *n_work = w;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < TK; i += kPermThreads) {
+    const int row = soff[ids[i]] + rank[i];
+    perm_tok[row] = i / k;
+    slot_row[i] = row;
+  }
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {
+    const int nt = (cnt[e] + tile_rows - 1) / tile_rows;
+    for (int j = 0; j < nt; ++j) {
+      work[2 * (toff[e] + j)] = e;
+      work[2 * (toff[e] + j) + 1] = j * tile_rows;
+    }
+  }
+}
+
+// h[t] (+)= sum_s gate[t][s] * y[slot_row[t*k+s]], slots in ascending order.
+__global__ void combine_kernel(float *h, const float *y, const float *gates, const int *slot_row,
+                               int k, int d, int accumulate) {
+  const int t = blockIdx.x;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float acc = accumulate ? h[(size_t)t * d + c] : 0.0f;
+    float mo = 0.0f;
+    for (int s = 0; s < k; ++s)
+      mo += gates[(size_t)t * k + s] * y[(size_t)slot_row[(size_t)t * k + s] * d + c];
+    h[(size_t)t * d + c] = acc + mo;
+  }
+}
+
+// 16-byte copies of [L][n][Hkv][hd] rows into the paged pools.
+__global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *k_pool,
+                                 uint4 *v_pool, const int *page_table, int L, int n_pages, int pos0,
+                                 int n, int Hkv, int hd, int pg) {
+  const int vec = hd / 8;  // uint4 per head row
+  const size_t total = (size_t)L * n * Hkv * vec;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % vec);
+    size_t r = i / vec;
+    const int h = (int)(r % Hkv);
+    r /= Hkv;
+    const int t = (int)(r % n);
+    const int l = (int)(r / n);
+    const int p = pos0 + t;
+    const size_t dst =
+        ((((size_t)l * n_pages + page_table[p / pg]) * Hkv + h) * pg + p % pg) * vec + c;
+    k_pool[dst] = k_new[i];
+    v_pool[dst] = v_new[i];
+  }
+}
+
+}  // namespace
+
+static float weight_scale(float std_dev) {
+  return (float)((double)std_dev * sqrt(3.0) / 8388608.0);
+}
+
+cudaError_t fill_weights(bf16 *dst, uint64_t n, uint64_t seed, uint32_t tid, uint64_t e0,
+                         float std_dev, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  fill_weights_kernel<<<grid_for(n, 256), 256, 0, st>>>(dst, n, (uint32_t)seed,
+                                                        (uint32_t)(seed >> 32), tid, e0,
+                                                        weight_scale(std_dev));
+  return cudaGetLastError();
+}
+
+cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F, int layer,
+                             uint64_t seed, float std_dev, cudaStream_t st) {
+  const uint32_t base = 100u + 16u * (uint32_t)layer;
+  cudaError_t e = fill_weights(wr, (uint64_t)E * d, seed, base + 4, 0, std_dev, st);
+  if (e != cudaSuccess) return e;
+  const uint64_t n = (uint64_t)E * 2 * F * d;
+  fill_gate_up_kernel<<<grid_for(n, 256), 256, 0, st>>>(wgu, E, F, d, (uint32_t)seed,
+                                                        (uint32_t)(seed >> 32), base + 5, base + 6,
+                                                        weight_scale(std_dev));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return fill_weights(wd, (uint64_t)E * d * F, seed, base + 7, 0, std_dev, st);
+}
+
+cudaError_t fill_const(float *dst, size_t n, float v, cudaStream_t st) {
+  fill_const_kernel<<<grid_for(n, 256), 256, 0, st>>>(dst, n, v);
+  return cudaGetLastError();
+}
+
+cudaError_t rope_table(float *ct, float *stt, int max_pos, int hd, float base, cudaStream_t st) {
+  const size_t n = (size_t)max_pos * (hd / 2);
+  rope_table_kernel<<<grid_for(n, 256), 256, 0, st>>>(ct, stt, max_pos, hd / 2, hd, (double)base);
+  return cudaGetLastError();
+}
+
+cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
+                        uint64_t seed, int canvas, cudaStream_t st) {
+  canvas_init_kernel<<<ceil_div(C, 256), 256, 0, st>>>(x, committed, last, stable, C, V,
+                                                       (uint32_t)seed, (uint32_t)(seed >> 32),
+                                                       canvas);
+  return cudaGetLastError();
+}
+
+cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  embed_kernel<<<T, 256, 0, st>>>(h, table, ids, d);
+  return cudaGetLastError();
+}
+
+cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
+                         cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  rmsnorm_kernel<<<T, 256, 0, st>>>(out, h, gain, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, float *gates,
+                        cudaStream_t st) {
+  if (E > 256 || k > 16 || k > E) return cudaErrorInvalidValue;
+  topk_kernel<<<ceil_div(T * 32, 256), 256, 0, st>>>(logits, T, E, k, ids, gates);
+  return cudaGetLastError();
+}
+
+size_t moe_max_work(int T, int k, int E, int tile_rows) {
+  return (size_t)(T * k + tile_rows - 1) / tile_rows + E;
+}
+
+cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
+                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st) {
+  if (E > 256) return cudaErrorInvalidValue;
+  int *rank = work + 2 * moe_max_work(T, k, E, tile_rows);
+  permute_kernel<<<1, kPermThreads, 0, st>>>(ids, T * k, k, E, tile_rows, offs, perm_tok, slot_row,
+                                             work, n_work, rank);
+  return cudaGetLastError();
+}
+
+cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
+                        int k, int d, bool accumulate, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<T, 256, 0, st>>>(h, y, gates, slot_row, k, d, accumulate ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
+                      const int *page_table, int L, int n_pages, int pos0, int n, int Hkv, int hd,
+                      int pg, cudaStream_t st) {
+  const size_t total = (size_t)L * n * Hkv * (hd / 8);
+  if (total == 0) return cudaSuccess;
+  kv_append_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, st>>>(
+      (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_pool, (uint4 *)v_pool, page_table, L,
+      n_pages, pos0, n, Hkv, hd, pg);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,160 @@
+// Commit / re-noise / adaptive-stop sampler of one denoising step.
+//
+// Reading of the rule (DiffusionGemma report §3.3 adaptive stopping; blog
+// post "Once Written, a Prefix Becomes History": high-confidence positions
+// lock in first while the rest keep being revised; report §4: multinomial
+// re-noising): per position the argmax a and confidence conf = max softmax
+// probability come from a full-vocabulary reduction; an uncommitted position
+// commits to a when conf >= threshold or when a was unchanged for
+// `stable_steps` consecutive steps, otherwise it is re-noised with a
+// Gumbel-max sample g of its softmax; the canvas is done when every position
+// is committed (adaptive) or at the budget N, where the rest take a.
+//
+// The reduction order is fixed so that results are reproducible bit for bit:
+// 256-wide vocab tiles (sampler.cuh), merged by a balanced binary tree in
+// tile order (left = lower vocab range).
+#include "internal.h"
+#include "sampler.cuh"
+
+namespace dg {
+
+namespace {
+
+constexpr int kLogitRowsPerBlock = 32;
+constexpr int kLdl = kVocabTile + 1;
+
+__global__ void __launch_bounds__(256) logits_partials_kernel(const float *logits, int rows, int V,
+                                                              uint32_t key0, uint32_t key1,
+                                                              uint32_t ctr2, PartialPlanes P) {
+  extern __shared__ float sm[];
+  float *L = sm;
+  float *K = L + kLogitRowsPerBlock * kLdl;
+  float *rm = K + kLogitRowsPerBlock * kLdl;
+  int *ra = (int *)(rm + kLogitRowsPerBlock);
+  const int tile = blockIdx.x, r0 = blockIdx.y * kLogitRowsPerBlock;
+  const int R = min(kLogitRowsPerBlock, rows - r0);
+  const int v0 = tile * kVocabTile;
+  for (int idx = threadIdx.x; idx < R * kVocabTile; idx += blockDim.x) {
+    const int r = idx / kVocabTile, v = idx % kVocabTile;
+    L[r * kLdl + v] = logits[(size_t)(r0 + r) * V + v0 + v];
+  }
+  __syncthreads();
+  PartialScratch sc{K, rm, ra};
+  block_tile_partials(L, kLdl, sc, R, v0, tile, V / kVocabTile, r0, ctr2, key0, key1, P, r0);
+}
+
+// Balanced binary tree over the tiles of one position; one block per position.
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(PartialPlanes P, int tiles,
+                                                              int leaves_per_thread, int *argmax,
+                                                              float *conf, int *gumbel) {
+  const int pos = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // in-thread subtree over leaves [tid*c, tid*c + c), c a power of two
+  Partial stack[12];
+  int level[12];
+  int sp = 0;
+  for (int i = 0; i < leaves_per_thread; ++i) {
+    const int t = tid * leaves_per_thread + i;
+    Partial p = (t < tiles) ? P.load((size_t)pos * tiles + t) : empty_partial();
+    int l = 0;
+    while (sp > 0 && level[sp - 1] == l) {
+      p = merge_partials(stack[sp - 1], p);
+      --sp;
+      ++l;
+    }
+    stack[sp] = p;
+    level[sp] = l;
+    ++sp;
+  }
+  Partial p = stack[0];
+  // across the lanes of a warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    Partial o;
+    o.m = __shfl_down_sync(0xffffffffu, p.m, off);
+    o.a = __shfl_down_sync(0xffffffffu, p.a, off);
+    o.s = __shfl_down_sync(0xffffffffu, p.s, off);
+    o.gk = __shfl_down_sync(0xffffffffu, p.gk, off);
+    o.gi = __shfl_down_sync(0xffffffffu, p.gi, off);
+    if ((lane & (2 * off - 1)) == 0) p = merge_partials(p, o);
+  }
+  __shared__ Partial wres[kMergeThreads / 32];
+  if (lane == 0) wres[warp] = p;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kMergeThreads / 32; w <<= 1)
+      for (int i = 0; i + w < kMergeThreads / 32; i += 2 * w) wres[i] = merge_partials(wres[i], wres[i + w]);
+    argmax[pos] = wres[0].a;
+    conf[pos] = __fdiv_rn(1.0f, wres[0].s);
+    gumbel[pos] = wres[0].gi;
+  }
+}
+
+__global__ void rule_kernel(const int *argmax, const float *conf, const int *gum, int C, int step,
+                            int budget_N, int stable_steps, int adaptive, float thr, int *x,
+                            uint8_t *committed, int *last, int *stable, int *done) {
+  const int i = threadIdx.x;
+  bool com = true;
+  if (i < C) {
+    com = committed[i] != 0;
+    if (!com) {
+      const int a = argmax[i];
+      const int st = (a == last[i]) ? stable[i] + 1 : 0;
+      stable[i] = st;
+      last[i] = a;
+      com = (conf[i] >= thr) || (st >= stable_steps);
+      x[i] = com ? a : gum[i];
+      if (!com && step >= budget_N) {
+        x[i] = a;
+        com = true;
+      }
+      committed[i] = com ? 1 : 0;
+    }
+  }
+  const int n_free = __syncthreads_count(!com);
+  if (i == 0) *done = (step >= budget_N || (adaptive && n_free == 0)) ? 1 : 0;
+}
+
+}  // namespace
+
+cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,
+                            int step, void *partials, cudaStream_t st) {
+  const int tiles = V / kVocabTile;
+  const PartialPlanes P = PartialPlanes::at(partials, rows, tiles);
+  const size_t smem = (size_t)2 * kLogitRowsPerBlock * kLdl * sizeof(float) +
+                      kLogitRowsPerBlock * (sizeof(float) + sizeof(int));
+  cudaError_t e = cudaFuncSetAttribute(logits_partials_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(tiles, ceil_div(rows, kLogitRowsPerBlock));
+  logits_partials_kernel<<<grid, 256, smem, st>>>(logits, rows, V, (uint32_t)seed,
+                                                  (uint32_t)(seed >> 32),
+                                                  gumbel_ctr2(canvas, step), P);
+  return cudaGetLastError();
+}
+
+cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,
+                          int *gumbel, cudaStream_t st) {
+  const int tiles = V / kVocabTile;
+  int width = kMergeThreads;
+  while (width < tiles) width *= 2;
+  const int c = width / kMergeThreads;
+  if (c > 1024) return cudaErrorInvalidValue;  // stack depth of the in-thread tree
+  const PartialPlanes P = PartialPlanes::at(const_cast<void *>(partials), C, tiles);
+  merge_kernel<<<C, kMergeThreads, 0, st>>>(P, tiles, c, argmax, conf, gumbel);
+  return cudaGetLastError();
+}
+
+cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
+                         int budget_N, int stable_steps, int adaptive, float conf_threshold,
+                         int *x, uint8_t *committed, int *last, int *stable, int *done,
+                         cudaStream_t st) {
+  if (C > 1024) return cudaErrorInvalidValue;
+  const int threads = ((C + 31) / 32) * 32;
+  rule_kernel<<<1, threads, 0, st>>>(argmax, conf, gumbel, C, step, budget_N, stable_steps,
+                                     adaptive, conf_threshold, x, committed, last, stable, done);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

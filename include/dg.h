@@ -1,0 +1,324 @@
+/*
+ * dg.h -- C ABI of the GB300 (sm_103a) block text-diffusion decoding library.
+ *
+ * The library runs the hot path of a DiffusionGemma-style decoder on one GPU:
+ * a canvas of C = 256 tokens is refined by repeated denoising forwards that
+ * attend to a read-only, paged bf16 KV cache of the clean prefix and
+ * bidirectionally within the canvas; a top-k mixture-of-experts FFN follows
+ * attention in every layer; an LM head fused with a vocabulary-split softmax
+ * reduction feeds a commit / re-noise / adaptive-stop sampler; one extra
+ * forward per finished canvas appends its K/V to the cache.
+ *
+ * Sources for what each call computes:
+ *   DiffusionGemma Technical Report  -- abstract and §1 (256-token canvases
+ *     refined in parallel; causal attention for context encoding,
+ *     bidirectional attention for diffusion); §2.1 (canvas x_t in V^C,
+ *     fully corrupted start x_1 ~ Unif(V^C)); §3.3 (adaptive stopping under a
+ *     budget N = 48); §3.4 Eq. 7-10 (metrics; one extra forward between
+ *     canvases appends the clean tokens' K/V); §4 (encoder KV cache of the
+ *     prompt and previous canvases; multinomial corruption); §6 (batch-1
+ *     serving; MoE, sampling and attention dominate step time).
+ *   Blog post on the release, "Once Written, a Prefix Becomes History" --
+ *     finished canvases become read-only prefix; high-confidence positions
+ *     lock in first while the rest keep being revised.
+ *
+ * Conventions for every call
+ *   - Return 0 (DG_OK) on success or a negative DG_E* code; the message of
+ *     the last failure on the calling thread is dg_last_error().
+ *   - Pointers documented as "host" are caller-owned host memory, read or
+ *     written only during the call.  Pointers documented as "device" are
+ *     device memory of the current CUDA device; the library never frees them.
+ *   - A model owns its device memory (weights, KV pool, scratch) from
+ *     dg_init_model until dg_free_model.  A model is not thread-safe; all of
+ *     its work is ordered on its CUDA stream.  Calls that return host data
+ *     synchronise that stream before returning.
+ *   - Integer tensors are int32, "bf16" tensors hold IEEE bfloat16 bit
+ *     patterns (uint16), float tensors are IEEE fp32; all row-major.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DG_OK 0
+#define DG_EINVAL (-1)      /* bad argument or unsupported shape               */
+#define DG_ENOMEM (-2)      /* device allocation failed                        */
+#define DG_ECUDA (-3)       /* a CUDA call or kernel launch failed             */
+#define DG_ESTATE (-4)      /* call out of order (e.g. denoise before prefill) */
+#define DG_ECAPACITY (-5)   /* KV pool or position range exhausted             */
+#define DG_ETIMEOUT (-6)    /* a bounded device-side wait gave up              */
+
+/* Model shape.  Supported: head_dim in {64, 128}; d_model, n_q_heads*head_dim,
+ * d_ff multiples of 64; vocab a multiple of 256; n_experts <= 256;
+ * top_k <= 16; n_q_heads a multiple of n_kv_heads. */
+typedef struct dg_config {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t d_ff;          /* expert SwiGLU width F                          */
+    int32_t vocab;
+    int32_t page_size;     /* tokens per KV page (a multiple of 64)          */
+    int32_t max_context;   /* KV pool capacity in tokens (prompt + canvases) */
+    float rope_base;       /* RoPE theta base (10000)                        */
+    float rms_eps;         /* RMSNorm epsilon (1e-6)                         */
+    float init_std;        /* std of the seeded random-init weights (0.02)   */
+    uint64_t weight_seed;  /* seed of the Philox weight stream               */
+} dg_config;
+
+/* Sampler of one canvas.  Commit rule: an uncommitted position commits to its
+ * argmax when conf >= conf_threshold or when its argmax was unchanged for
+ * stable_steps consecutive steps; every other position is re-noised with a
+ * Gumbel-max sample of its softmax; the canvas stops when all positions are
+ * committed (adaptive != 0) or after budget_N steps. */
+typedef struct dg_sampler_config {
+    int32_t canvas_len;      /* C (256 in the method; 1..1024 supported)       */
+    int32_t budget_N;        /* denoising budget N (48)                        */
+    int32_t stable_steps;    /* 2                                              */
+    int32_t adaptive;        /* 1: stop early once all committed               */
+    int32_t eos_id;          /* -1: no end-of-sequence token                   */
+    int32_t commit_causal;   /* 1: causal mask inside the canvas in the KV-append forward */
+    float conf_threshold;    /* 0.9                                             */
+    uint64_t sample_seed;    /* seed of the canvas-init and Gumbel streams     */
+} dg_sampler_config;
+
+/* Eq. 7-10 of the report over one dg_generate call. */
+typedef struct dg_stats {
+    int32_t K;               /* canvases generated                             */
+    int32_t total_tokens;    /* Eq. 7                                          */
+    int32_t total_steps;     /* Eq. 8                                          */
+    int32_t n_forwards;      /* denoise forwards + KV-append forwards          */
+    double effective_steps;  /* Eq. 9                                          */
+    double tpf;              /* Eq. 10                                         */
+    double prefill_seconds;  /* wall time of the prompt encoding               */
+    double decode_seconds;   /* wall time of the canvases (prefill excluded)   */
+    int32_t *N_k;            /* host, caller-owned, >= K_max entries, or NULL  */
+    int32_t *C_k;            /* host, caller-owned, >= K_max entries, or NULL  */
+} dg_stats;
+
+typedef struct dg_model dg_model;
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *dg_last_error(void);
+
+/* Create a model on the current CUDA device: allocate seeded random-init
+ * bf16 weights (Philox4x32-10, see dg_op_fill_weights), the paged KV pool for
+ * cfg->max_context tokens and all scratch.  `cuda_stream` (a cudaStream_t)
+ * orders all of the model's work; NULL creates a private non-blocking stream.
+ * On success *out owns everything until dg_free_model. */
+int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, void *cuda_stream,
+                  dg_model **out);
+void dg_free_model(dg_model *m);
+
+/* Encode prompt_ids[0..n) (host) with causal attention at positions 0..n-1
+ * and write their K/V into the cache (report §1, context encoding).  Resets
+ * any previous generation.  n may be 0.  DG_ECAPACITY if the prompt plus one
+ * canvas does not fit max_context. */
+int dg_prefill(dg_model *m, const int32_t *prompt_ids, int32_t n);
+
+/* One denoising step of the current canvas (the first call after prefill or
+ * commit initialises it to uniform random ids, report §2.1).  All canvas
+ * positions attend to the whole prefix and the whole canvas; the sampler
+ * commits / re-noises and decides whether the canvas is finished.
+ * *done (host) receives 1 when the canvas is finished, else 0. */
+int dg_denoise_step(dg_model *m, int32_t *done);
+
+/* Finish the current canvas: copy its ids to out_ids (host, canvas_len
+ * entries, may be NULL), set *out_valid (host, may be NULL) to C_k (tokens
+ * before the first EOS, report §3.4), then run the single extra forward that
+ * encodes the canvas (causal inside the canvas unless commit_causal == 0)
+ * and appends its K/V to the prefix.  DG_ESTATE if the canvas is not done. */
+int dg_commit_canvas(dg_model *m, int32_t *out_ids, int32_t *out_valid);
+
+/* Prefill + up to K_max canvases (stopping after the canvas holding the first
+ * EOS); no KV-append forward follows the last canvas.  out_ids (host,
+ * K_max * canvas_len entries) receives the canvases; stats (may be NULL)
+ * receives Eq. 7-10.  The per-step done flag is the only device->host
+ * synchronisation inside the canvas loop. */
+int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_max,
+                int32_t *out_ids, dg_stats *stats);
+
+/* ---- helpers: state access for replay tests and benchmarking ------------ */
+
+/* Replace the sampler configuration (e.g. a new sample_seed). */
+int dg_set_sampler(dg_model *m, const dg_sampler_config *scfg);
+
+/* Forget everything after the first n_prefix cached tokens (the prompt plus
+ * whole committed canvases) and drop the current canvas.  The cached K/V of
+ * those tokens are kept, so decoding can restart without a prefill. */
+int dg_rewind(dg_model *m, int32_t n_prefix);
+
+/* Current canvas and sampler state (host outputs, canvas_len entries each;
+ * any pointer may be NULL).  *step = steps taken on this canvas,
+ * *canvas_index = k (0-based), *prefix_len = cached tokens. */
+int dg_read_canvas(dg_model *m, int32_t *ids, uint8_t *committed, int32_t *last_argmax,
+                   int32_t *stable, int32_t *step, int32_t *canvas_index, int32_t *prefix_len);
+
+/* Overwrite the current canvas state (host inputs, canvas_len entries) and its
+ * step counter / canvas index; used to replay a step from recorded state. */
+int dg_write_canvas(dg_model *m, const int32_t *ids, const uint8_t *committed,
+                    const int32_t *last_argmax, const int32_t *stable, int32_t step,
+                    int32_t canvas_index);
+
+/* Per-position outputs of the last denoising step (host, canvas_len each):
+ * argmax a_i, confidence conf_i = max softmax prob, Gumbel-max sample g_i. */
+int dg_read_step_outputs(dg_model *m, int32_t *argmax, float *conf, int32_t *gumbel);
+
+/* Run the denoising forward of the current canvas without sampling and write
+ * its fp32 logits [canvas_len][vocab] to logits_dev (device).  Test hook. */
+int dg_canvas_logits(dg_model *m, float *logits_dev);
+
+/* Cached K/V of `layer` at positions pos0..pos0+n-1, read through the page
+ * table into k_out/v_out (host, bf16 bits, [n][n_kv_heads][head_dim]). */
+int dg_read_kv(dg_model *m, int32_t layer, int32_t pos0, int32_t n, uint16_t *k_out,
+               uint16_t *v_out);
+
+/* Expert choice of the last forward that ran `layer`'s MoE: ids (host,
+ * [rows][top_k], up to max_rows rows, descending router logit), *n_rows =
+ * tokens of that forward.  Lets a replay follow the GPU's top-k decision
+ * where router logits are tied within rounding. */
+int dg_read_routing(dg_model *m, int32_t layer, int32_t *ids, int32_t max_rows, int32_t *n_rows);
+
+/* Page table (logical page -> physical page), host out, up to max_entries;
+ * *n_pages = pages covering the prefix plus the current canvas. */
+int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t *n_pages);
+
+/* Device pointer and size of a weight tensor.  which: DG_W_* below; layer is
+ * ignored for the embedding, LM head and final norm.  Physical layouts:
+ *   EMBED, LM_HEAD   [V][d]
+ *   WQKV             [(Hq + 2 Hkv) * hd][d]   rows: W_q, then W_k, then W_v
+ *   WO               [d][Hq * hd]
+ *   ROUTER           [E][d]
+ *   W_GATE_UP        [E][F/64][2][64][d]      per expert, 64-row blocks of
+ *                                             W_gate then W_up interleaved
+ *   W_DOWN           [E][d][F]
+ *   ATTN_NORM, MOE_NORM, FINAL_NORM  [d] (fp32 gains, initialised to 1) */
+enum {
+    DG_W_EMBED = 0, DG_W_LM_HEAD = 1, DG_W_FINAL_NORM = 2, DG_W_WQKV = 3, DG_W_WO = 4,
+    DG_W_ROUTER = 5, DG_W_GATE_UP = 6, DG_W_DOWN = 7, DG_W_ATTN_NORM = 8, DG_W_MOE_NORM = 9
+};
+int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, size_t *bytes);
+
+/* ---- profiling --------------------------------------------------------- */
+
+/* Kernel classes of the decoder, for per-class timing and launch counts. */
+enum {
+    DG_K_EMBED = 0, DG_K_RMSNORM, DG_K_QKV_ROPE, DG_K_ATTENTION, DG_K_O_PROJ, DG_K_ROUTER,
+    DG_K_TOPK, DG_K_PERMUTE, DG_K_EXPERT_GATE_UP, DG_K_EXPERT_DOWN, DG_K_COMBINE, DG_K_LM_HEAD,
+    DG_K_SAMPLER_MERGE, DG_K_SAMPLER_RULE, DG_K_CANVAS_INIT, DG_K_CLASSES
+};
+const char *dg_kernel_class_name(int32_t cls);
+
+/* Kernel launches are always counted per class.  With enable != 0 every
+ * launch is also bracketed by CUDA events on the model's stream and the
+ * elapsed device time is accumulated per class (read back at each
+ * synchronising call).  Enabling resets counts and times. */
+int dg_profile(dg_model *m, int32_t enable);
+/* ms[DG_K_CLASSES] (host, may be NULL): accumulated device milliseconds;
+ * launches[DG_K_CLASSES] (host, may be NULL): kernels launched per class. */
+int dg_profile_read(dg_model *m, double *ms, int64_t *launches);
+
+/* ---- kernel-level entry points (device pointers, caller's stream) ------- */
+
+/* Seeded synthetic weights: dst[j] (device, bf16) = element e0 + j of tensor
+ * `tensor_id`: an Irwin-Hall(4) sum of the four words of Philox4x32-10
+ * (Salmon et al., SC'11) at counter (e mod 2^32, e div 2^32, tensor_id, 1),
+ * key (seed mod 2^32, seed div 2^32):  s = sum_j (word_j >> 9),
+ * w = fp32(s - 2^24) * fp32(std*sqrt(3)/2^23), rounded to bf16 (nearest even).
+ * Tensor ids: 1 embedding, 2 LM head, 100 + 16*layer + {0 W_q, 1 W_k, 2 W_v,
+ * 3 W_o, 4 router, 5 W_gate, 6 W_up, 7 W_down} (logical row-major shapes as
+ * listed for dg_get_weight, expert tensors [E][F][d] / [E][d][F]). */
+int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor_id,
+                       uint64_t e0, float std_dev, void *stream);
+
+/* Canvas attention (report §1, §4; blog "Once Written..."): for every query
+ * position t < n_new (absolute position n_prefix + t) and query head h,
+ *   out[t][h] = softmax_j(q[t][h] . k_j / sqrt(hd)) v_j
+ * over keys j = 0 .. n_prefix + n_new - 1 of KV head h / (Hq/Hkv), where
+ * causal == 0 lets every query see all keys (denoising) and causal != 0 hides
+ * keys j > n_prefix + t (context encoding / KV append).
+ *   q        device bf16 [n_new][Hq][hd] (already rotated)
+ *   k_pool,
+ *   v_pool   device bf16 [n_pages][Hkv][page_size][hd]; key j lives in physical
+ *            page page_table[j / page_size], slot j % page_size
+ *   page_table device int32, >= ceil((n_prefix + n_new) / page_size) entries
+ *   out      device bf16 [n_new][Hq][hd]
+ * workspace: device scratch of dg_op_attention_workspace_bytes() bytes (the
+ * split-KV partial softmax states; 0 bytes when no split is needed). */
+size_t dg_op_attention_workspace_bytes(int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
+                                       int32_t n_kv_heads, int32_t head_dim);
+int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *page_table, int32_t n_prefix, int32_t n_new,
+                           int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                           int32_t page_size, int32_t causal, uint16_t *out, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* Mixture-of-experts FFN (report §6 "MoE"): for each of T rows of xn
+ * (device bf16 [T][d], already RMS-normalised),
+ *   r = xn W_r^T; S = the top_k largest r (ties -> lower expert id);
+ *   gates = softmax(r_S); y = sum_{e in S} gate_e W_down,e (silu(W_gate,e xn) * W_up,e xn)
+ * Weights in the layouts of dg_get_weight (W_GATE_UP interleaved, W_DOWN).
+ * Outputs (device): y fp32 [T][d]; expert_ids int32 [T][top_k] (descending
+ * router logit); gates fp32 [T][top_k].  workspace: dg_op_moe_workspace_bytes(). */
+size_t dg_op_moe_workspace_bytes(int32_t T, int32_t d, int32_t n_experts, int32_t top_k,
+                                 int32_t d_ff);
+int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_gate_up,
+              const uint16_t *w_down, int32_t T, int32_t d, int32_t n_experts, int32_t top_k,
+              int32_t d_ff, float *y, int32_t *expert_ids, float *gates, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+/* Fill the three MoE weight tensors of `layer` (layouts of dg_get_weight) with
+ * the seeded weights of tensor ids 100 + 16*layer + {4, 5, 6, 7}. */
+int dg_op_fill_moe_weights(uint16_t *w_router, uint16_t *w_gate_up, uint16_t *w_down, int32_t d,
+                           int32_t n_experts, int32_t d_ff, int32_t layer, uint64_t seed,
+                           float std_dev, void *stream);
+
+/* Per-(position, vocab tile) sampler partials.  Tiles are 256 vocab entries;
+ * inside tile t, in ascending v: m = max logit, a = first index reaching it,
+ * s = left-to-right fp32 sum of dg_exp(l_v - m), (gk, gi) = max and first
+ * argmax of l_v + G_v with Gumbel noise G_v = -dg_log(-dg_log(u)) and
+ * u = (2 (w >> 9) + 1) 2^-24, w = word (v mod 4) of Philox4x32-10 at counter
+ * (v div 4, position, (canvas << 16) | step, 3), key = sample seed.
+ * Layout of `partials` (device, rows * V/256 * 20 bytes): 5 planes of
+ * [rows][V/256]: m (f32), a (i32), s (f32), gk (f32), gi (i32).
+ * dg_op_lm_head_partials computes logits = xn W_out^T (fp32 accumulation, the
+ * logits never leave the chip) and their partials; dg_op_logits_partials
+ * does the same for given fp32 logits [rows][V] (device). */
+int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *w_out, int32_t rows, int32_t d,
+                           int32_t V, uint64_t sample_seed, int32_t canvas, int32_t step,
+                           void *partials, void *stream);
+int dg_op_logits_partials(const float *logits, int32_t rows, int32_t V, uint64_t sample_seed,
+                          int32_t canvas, int32_t step, void *partials, void *stream);
+
+/* Merge the partials of each row by a balanced binary tree over the tiles
+ * (left = lower vocab range; M = max; S = sL*exp(mL-M) + sR*exp(mR-M);
+ * argmax / Gumbel winner from the right only if strictly greater) and apply
+ * the commit / re-noise / stop rule to the canvas state (all device, C
+ * entries): x, committed (uint8), last_argmax, stable.  step is 1-based.
+ * Outputs (device): argmax, conf (= 1/S), gumbel, and *done_dev (int32). */
+int dg_op_sampler_update(const void *partials, int32_t C, int32_t V, int32_t step,
+                         const dg_sampler_config *scfg, int32_t *x, uint8_t *committed,
+                         int32_t *last_argmax, int32_t *stable, int32_t *argmax, float *conf,
+                         int32_t *gumbel, int32_t *done_dev, void *stream);
+
+/* KV append, standalone: copy n_layers x n_new tokens of K and V (device bf16
+ * [n_layers][n_new][Hkv][hd]) into the pools (device bf16
+ * [n_layers][n_pages][Hkv][page_size][hd]) at absolute positions
+ * pos0 .. pos0+n_new-1 through page_table (device int32). */
+int dg_op_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool,
+                    uint16_t *v_pool, const int32_t *page_table, int32_t n_layers,
+                    int32_t n_pages, int32_t pos0, int32_t n_new, int32_t n_kv_heads,
+                    int32_t head_dim, int32_t page_size, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DG_H */
