@@ -1,0 +1,368 @@
+"""Benchmark of the GB300 block-diffusion decoder (one JSON line on rank 0).
+
+Workload: the full synthetic decoder (30 layers, d_model 2816, 16/8 heads of
+128, 128 experts top-8 with FFN 704, vocab 262144, seeded random-init bf16
+weights), a 2048-token uniform-random prompt, 4 canvases of 256 tokens,
+denoising budget N = 48, adaptive stopping on, no EOS.
+
+One step = the decode of all 4 canvases from the cached prompt: every
+denoising forward (embed, 30 x {RMSNorm, QKV+RoPE, canvas attention, o-proj,
+RMSNorm, router, top-k, permute, expert SwiGLU GEMMs, combine}, final norm,
+LM head fused with the vocab reduction, sampler) plus the 3 KV-append
+forwards between canvases.  The prompt is encoded once before timing
+(decode-only, as the pages measure); each step rewinds to it and uses a new
+sample seed.  value = denoise steps/s (Eq. 8 total steps / time); output
+tokens/s and TPF (Eq. 7, 10) are reported beside it.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "denoise steps/s and output tokens/s per 256-token canvas on 1 GB300; % roofline"
+PROMPT, CANVASES, BUDGET, C = 2048, 4, 48, 256
+WORKLOAD = ("full synthetic decoder (30 layers, d_model 2816, 16/8 heads x 128, 128 experts top-8, "
+            "FFN 704, vocab 262144), 2048-token random prompt, 4 canvases of 256, N=48, adaptive")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of the SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(os.environ.get("DG_BENCH_BACKEND", "nccl"))
+        pg = dist
+    return world, rank, local, pg
+
+
+def reduce_over_ranks(pg, value, op, device=None):
+    """Barrier, then max or sum of `value` over ranks (identity on one rank)."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.barrier()
+    pg.all_reduce(t, op=pg.ReduceOp.MAX if op == "max" else pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- CPU oracle sample (the reference arm and the cpu_baseline leg) ----------
+
+class OracleSample:
+    """A bounded slice of one denoising step of the workload, run by the oracle.
+
+    One decoder layer over the 256-token canvas with a 2048-token prefix
+    (attention + MoE over all experts the routing touches) and the LM head +
+    sampler for 8 canvas positions.  Estimated step time = 30 x layer +
+    32 x head(8 positions).  Weights are generated before timing.
+    """
+
+    def __init__(self, head_rows=8):
+        import numpy as np
+        from oracle import model as om, weights as ow
+        self.np, self.om = np, om
+        cfg = self.cfg = om.FULL
+        s, std = cfg.weight_seed, cfg.init_std
+        d, E, F = cfg.d_model, cfg.n_experts, cfg.d_ff
+        qd, kd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+        t = lambda w: ow.layer_tid(0, w)
+        self.W = dict(wq=ow.tensor(s, t(ow.WQ), (qd, d), std), wk=ow.tensor(s, t(ow.WK), (kd, d), std),
+                      wv=ow.tensor(s, t(ow.WV), (kd, d), std), wo=ow.tensor(s, t(ow.WO), (d, qd), std),
+                      wr=ow.tensor(s, t(ow.WR), (E, d), std), wg=ow.tensor(s, t(ow.WG), (E, F, d), std),
+                      wu=ow.tensor(s, t(ow.WU), (E, F, d), std), wd=ow.tensor(s, t(ow.WD), (E, d, F), std),
+                      attn_norm=np.ones(d), moe_norm=np.ones(d))
+        self.lm_head = ow.tensor(s, ow.LM_HEAD, (cfg.vocab, d), std)
+        rng = np.random.default_rng(0)
+        ids = rng.integers(0, cfg.vocab, C)
+        self.h = ow.rows(s, ow.EMBED, (cfg.vocab, d), ids, std).astype(np.float64)
+        self.pk = rng.standard_normal((PROMPT, cfg.n_kv_heads, cfg.head_dim)) * 0.5
+        self.pv = rng.standard_normal((PROMPT, cfg.n_kv_heads, cfg.head_dim)) * 0.5
+        self.head_rows = head_rows
+        self.threads = os.cpu_count()
+
+    def run(self):
+        """Returns the estimated seconds of one full denoising step."""
+        np, om, cfg = self.np, self.om, self.cfg
+        from oracle import sampler as osamp
+        pos = PROMPT + np.arange(C)
+        t0 = time.perf_counter()
+        h, _, _ = om.block(self.h, pos, self.W, cfg, self.pk, self.pv, "bidir")
+        t1 = time.perf_counter()
+        n = om.rmsnorm(h[: self.head_rows], 1.0, cfg.rms_eps)
+        l = np.empty((self.head_rows, cfg.vocab), np.float32)
+        for v0 in range(0, cfg.vocab, 32768):
+            l[:, v0:v0 + 32768] = n @ self.lm_head[v0:v0 + 32768].astype(np.float64).T
+        osamp.position_outputs(l, 1, 0, 1)
+        t2 = time.perf_counter()
+        return cfg.n_layers * (t1 - t0) + (C / self.head_rows) * (t2 - t1)
+
+    def describe(self):
+        return (f"oracle (numpy fp64 forward + fp32 sampler) on layer 0 of a denoising step "
+                f"(256-token canvas, {PROMPT}-token prefix, MoE over 128 experts) and the LM head + "
+                f"sampler for {self.head_rows} positions; step time = 30 x layer + "
+                f"{C // self.head_rows} x head")
+
+
+def reference_arm(args):
+    world, rank, local, pg = dist_setup()
+    if rank != 0:
+        return 0
+    smp = OracleSample()
+    for _ in range(args.warmup):
+        smp.run()
+    est = [smp.run() for _ in range(args.steps)]
+    step_s = sum(est) / len(est)
+    v = 1.0 / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "denoise steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "step": "one denoising step, estimated from a bounded sample"},
+            "cpu_baseline": {"value": v, "unit": "denoise steps/s", "cores": smp.threads,
+                             "kind": "oracle", "sample": smp.describe()},
+            "e2e": {"value": v, "unit": "denoise steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the GPU arm -------------------------------------------------------------
+
+def decode_all(dgp, m, seed, scfg):
+    """One bench step: rewind to the prompt and decode all canvases."""
+    dgp.dg_rewind(m, PROMPT)
+    scfg.sample_seed = seed
+    dgp.dg_set_sampler(m, scfg)
+    Ns, Cs = [], []
+    for k in range(CANVASES):
+        n, done = 0, False
+        while not done:
+            done = dgp.dg_denoise_step(m)
+            n += 1
+        Ns.append(n)
+        if k < CANVASES - 1:
+            _, valid = dgp.dg_commit_canvas(m)
+        else:
+            valid = C
+        Cs.append(valid)
+    return Ns, Cs
+
+
+def expert_bytes(cfg):
+    """Algorithmic DRAM bytes of one expert-GEMM launch of a denoising step: every
+    touched expert's weights once (N(0,1)-like routing of 256 x 8 pairs over 128
+    experts touches all of them: P(an expert is idle) = (1 - 8/128)^256 < 1e-7),
+    the gathered token rows once and the outputs once."""
+    d, E, F, k = cfg.d_model, cfg.n_experts, cfg.d_ff, cfg.top_k
+    rows = C * k
+    return {"expert_gate_up": E * 2 * F * d * 2 + rows * d * 2 + rows * F * 2,
+            "expert_down": E * d * F * 2 + rows * F * 2 + rows * d * 4}
+
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+    import discrete_diffusion_block_gb300 as dgp
+    from discrete_diffusion_block_gb300 import build, synth
+
+    world, rank, local, pg = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if pg is not None:
+        pg.barrier()
+    dgp.load()
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+
+    stream = torch.cuda.Stream(device=dev)
+    cfg = dgp.full_config(max_context=PROMPT + CANVASES * C)
+    scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1)
+    m = dgp.dg_init_model(cfg, scfg, stream=stream)
+    prompt = synth.prompt_ids(PROMPT, cfg.vocab, seed=1000 + rank)
+    dgp.dg_prefill(m, prompt)
+
+    for w in range(args.warmup):
+        decode_all(dgp, m, 10_000 + w, scfg)
+
+    dgp.dg_profile(m, 1)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    allN, allC = [], []
+    rdev = dev if pg is not None else None
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ev0.record(stream)
+        for s in range(args.steps):
+            Ns, Cs = decode_all(dgp, m, 20_000 + s, scfg)
+            allN += Ns
+            allC += Cs
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    prof = dgp.dg_profile_read(m)
+    dgp.dg_profile(m, 0)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = reduce_over_ranks(pg, ms, "max", rdev)
+    steps_total = reduce_over_ranks(pg, sum(allN), "sum", rdev)
+    tokens_total = reduce_over_ranks(pg, sum(allC), "sum", rdev)
+    value = steps_total / (ms_max / 1e3)
+    tok_s = tokens_total / (ms_max / 1e3)
+    tpf = sum(allC) / (sum(allN) + args.steps * (CANVASES - 1))
+    eff = sum(n * c for n, c in zip(allN, allC)) / max(sum(allC), 1)
+
+    # ---- roofline of the dominant kernel (events of the timed region) --------
+    per_launch = expert_bytes(cfg)
+    kernels = {}
+    for name, (kms, n) in prof.items():
+        if n:
+            kernels[name] = {"ms_total": round(kms, 3), "launches": n,
+                             "us_per_launch": round(kms / n * 1e3, 2)}
+    for name, b in per_launch.items():
+        if prof[name][1]:
+            a = b / (prof[name][0] / 1e3 / prof[name][1]) / 1e9
+            kernels[name].update(GBps=round(a, 1), frac_hbm=round(a / hbm, 4))
+    if prof["lm_head"][1]:
+        fl = 2.0 * C * cfg.d_model * cfg.vocab
+        a = fl / (prof["lm_head"][0] / 1e3 / prof["lm_head"][1]) / 1e12
+        kernels["lm_head"].update(TFLOPs=round(a, 1), frac_bf16_sustained=round(a / tf_sust, 4))
+    dom = max(per_launch, key=lambda k: prof[k][0])
+    kms, n = prof[dom]
+    achieved = per_launch[dom] / (kms / 1e3 / n) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": args.traffic,
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": per_launch[dom]}
+    launches = int(sum(n for _, n in prof.values()))
+
+    # ---- e2e through the public API: host prompt in, host ids out ----------
+    e2e = None
+    if args.e2e_steps > 0:
+        dgp.dg_set_sampler(m, dgp.SamplerConfig(budget_N=BUDGET, adaptive=1, sample_seed=30_000))
+        host_prompt = np.ascontiguousarray(prompt, dtype=np.int32)
+        t0 = time.perf_counter()
+        e_steps, h2d, d2h = 0, 0, 0
+        for s in range(args.e2e_steps):
+            out, st = dgp.dg_generate(m, host_prompt, CANVASES)
+            e_steps += st["total_steps"]
+            h2d += host_prompt.nbytes
+            d2h += out.nbytes + 4 * st["total_steps"]     # canvases + one done flag per step
+        el = time.perf_counter() - t0
+        e2e = {"value": e_steps / el, "unit": "denoise steps/s",
+               "h2d_bytes_per_step": h2d // args.e2e_steps, "d2h_bytes_per_step": d2h // args.e2e_steps,
+               "includes": "prefill of the 2048-token prompt + decode of 4 canvases per dg_generate call"}
+    m.close()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample()
+        est = smp.run()
+        cpu = {"value": 1.0 / est, "unit": "denoise steps/s", "cores": smp.threads, "kind": "oracle",
+               "sample": smp.describe()}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "denoise steps/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic: seeded random-init weights, uniform random prompt ids",
+                "config": {"workload": WORKLOAD,
+                           "step": "decode of 4 canvases (all denoising steps + 3 KV-append forwards), prompt cached",
+                           "l2": "inputs larger than L2: ~45.7 GB of expert weights streamed per denoising step",
+                           "parallelism": f"replicas x{world}"},
+                "output_tokens_per_s": tok_s, "tpf": tpf, "effective_steps": eff,
+                "N_k_mean": sum(allN) / len(allN),
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clk.summary(), "gpu_launches": launches}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the dominant kernel, if measured for this build")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,248 @@
+"""Kernel-level parity of the CUDA path (through the C ABI) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import discrete_diffusion_block_gb300 as dgp
+from discrete_diffusion_block_gb300 import synth
+from gpu_util import bf16_to_f32, dev, new_partials, partial_planes, rel_err, top2_gap
+from oracle import dgmath, model as om, philox, sampler as osamp, weights as ow
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from discrete_diffusion_block_gb300 import build
+    build.build()
+    dgp.load()
+    torch.cuda.set_device(0)
+
+
+# ---- seeded weights ---------------------------------------------------------
+
+@pytest.mark.parametrize("tid,e0,n", [(1, 0, 100_003), (2, 12345, 4096), (137, (1 << 32) - 7, 64)])
+def test_weight_generator_bit_exact(tid, e0, n):
+    t = torch.empty(n, dtype=torch.bfloat16, device=dev())
+    dgp.dg_op_fill_weights(t, 7, tid, e0, 0.02)
+    got = t.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = (ow.elements(7, tid, e0, n, 0.02).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_moe_weight_layout_matches_logical_tensors():
+    d, E, F, L = 128, 4, 192, 3
+    wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
+    wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
+    wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
+    dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, L, 5, 0.02)
+    base = 100 + 16 * L
+    assert np.array_equal(bf16_to_f32(wr).reshape(E, d), ow.tensor(5, base + 4, (E, d), 0.02))
+    gu = bf16_to_f32(wgu).reshape(E, F // 64, 2, 64, d)
+    g = ow.tensor(5, base + 5, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
+    u = ow.tensor(5, base + 6, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
+    assert np.array_equal(gu[:, :, 0], g) and np.array_equal(gu[:, :, 1], u)
+    assert np.array_equal(bf16_to_f32(wd).reshape(E, d, F), ow.tensor(5, base + 7, (E, d, F), 0.02))
+
+
+# ---- sampler: bit-exact given identical logits --------------------------------
+
+def gpu_sampler(l, scfg, step, canvas, state):
+    C, V = l.shape
+    L = torch.from_numpy(np.ascontiguousarray(l)).to(dev())
+    part = new_partials(C, V)
+    dgp.dg_op_logits_partials(L, C, V, scfg.sample_seed, canvas, step, part)
+    x = torch.from_numpy(state.x.copy()).to(dev())
+    com = torch.from_numpy(state.committed.copy()).to(dev())
+    last = torch.from_numpy(state.last.copy()).to(dev())
+    stab = torch.from_numpy(state.stable.copy()).to(dev())
+    a = torch.zeros(C, dtype=torch.int32, device=dev())
+    conf = torch.zeros(C, dtype=torch.float32, device=dev())
+    g = torch.zeros(C, dtype=torch.int32, device=dev())
+    done = torch.zeros(1, dtype=torch.int32, device=dev())
+    dgp.dg_op_sampler_update(part, C, V, step, scfg, x, com, last, stab, a, conf, g, done)
+    torch.cuda.synchronize()
+    return dict(part=partial_planes(part, C, V), a=a.cpu().numpy(), conf=conf.cpu().numpy(),
+                g=g.cpu().numpy(), x=x.cpu().numpy(), committed=com.cpu().numpy(),
+                last=last.cpu().numpy(), stable=stab.cpu().numpy(), done=bool(done.item()))
+
+
+def oracle_partials(l, seed, canvas, step, positions=None):
+    """Partials of the rows of l, row r being canvas position positions[r]."""
+    positions = np.arange(l.shape[0]) if positions is None else np.asarray(positions)
+    G = dgmath.gumbel_from_uniform(philox.gumbel_uniforms(seed, canvas, step, positions, l.shape[1]))
+    return osamp.tile_partials(l, G)
+
+
+@pytest.mark.parametrize("C,V,seed", [(256, 1024, 0), (40, 768, 3), (32, 262144, 9)])
+def test_sampler_partials_and_outputs_bit_exact(C, V, seed):
+    l = synth.logits(C, V, seed=seed)
+    scfg = dgp.SamplerConfig(canvas_len=C, sample_seed=seed * 7 + 1)
+    st = osamp.CanvasState(philox.canvas_init_ids(scfg.sample_seed, 2, C, V))
+    got = gpu_sampler(l, scfg, 3, 2, st)
+    ref = oracle_partials(l, scfg.sample_seed, 2, 3)
+    for k in ("m", "a", "s", "gk", "gi"):
+        assert np.array_equal(got["part"][k], ref[k]), k
+    a, conf, g, _ = osamp.position_outputs(l, scfg.sample_seed, 2, 3)
+    assert np.array_equal(got["a"], a)
+    assert np.array_equal(got["conf"].view(np.uint32), conf.view(np.uint32))
+    assert np.array_equal(got["g"], g)
+    done = osamp.apply_rule(st, a, conf, g, 3, scfg.budget_N)
+    for k in ("x", "committed", "last", "stable"):
+        assert np.array_equal(got[k], getattr(st, k)), k
+    assert got["done"] == done
+
+
+def test_sampler_full_vocab_full_canvas_sampled_rows():
+    C, V = 256, 262144
+    l = synth.logits(C, V, seed=11, scale=2.0)
+    scfg = dgp.SamplerConfig(sample_seed=5)
+    st = osamp.CanvasState(np.zeros(C, np.int32))
+    got = gpu_sampler(l, scfg, 1, 0, st)
+    rows = np.array([0, 1, 77, 128, 200, 255])
+    ref = oracle_partials(l[rows], 5, 0, 1, rows)
+    for k in ("m", "a", "s", "gk", "gi"):
+        assert np.array_equal(got["part"][k][rows], ref[k]), k
+    r = osamp.reduce_tiles(ref)
+    assert np.array_equal(got["a"][rows], r["a"])
+    assert np.array_equal(got["g"][rows], r["gi"])
+    assert np.array_equal(got["conf"][rows].view(np.uint32),
+                          (np.float32(1) / r["s"]).astype(np.float32).view(np.uint32))
+
+
+def test_sampler_rule_branches_over_scripted_steps():
+    C, V, N = 64, 512, 5
+    rng = np.random.default_rng(4)
+    scfg = dgp.SamplerConfig(canvas_len=C, budget_N=N, sample_seed=21)
+    st = osamp.CanvasState(rng.integers(0, V, C).astype(np.int32))
+    gst = st.copy()
+    target = rng.integers(0, V, C)
+    done = False
+    for n in range(1, N + 1):
+        l = rng.standard_normal((C, V)).astype(np.float32)
+        hot = np.arange(C) < 8 * n                      # more rows spike each step (stable argmax)
+        l[hot, target[hot]] += 6.0
+        l[:4, target[:4]] += 40.0                       # confident: commit at once
+        got = gpu_sampler(l, scfg, n, 1, gst)
+        a, conf, g, _ = osamp.position_outputs(l, 21, 1, n)
+        done = osamp.apply_rule(st, a, conf, g, n, N)
+        for k in ("x", "committed", "last", "stable"):
+            assert np.array_equal(got[k], getattr(st, k)), (n, k)
+        assert got["done"] == done
+        gst = st.copy()
+        if done:
+            break
+    assert done and st.committed.all()
+
+
+# ---- LM head fused with the vocab reduction -------------------------------------
+
+@pytest.mark.parametrize("rows,d,V,sample", [(256, 256, 1024, None), (256, 2816, 262144, [0, 63, 64, 130, 255])])
+def test_lm_head_partials_against_fp64_logits(rows, d, V, sample):
+    xf, xt = synth.normal_bf16((rows, d), seed=2)
+    xn = xt.to(dev())
+    w = torch.empty(V * d, dtype=torch.bfloat16, device=dev())
+    dgp.dg_op_fill_weights(w, 0, 2, 0, 0.02)
+    part = new_partials(rows, V)
+    dgp.dg_op_lm_head_partials(xn, w, rows, d, V, 3, 1, 2, part)
+    got = partial_planes(part, rows, V)
+    sample = np.arange(rows) if sample is None else np.asarray(sample)
+    x64 = xf[sample].astype(np.float64)
+    lo = np.empty((len(sample), V))
+    for v0 in range(0, V, 16384):                     # oracle weights, chunk by chunk
+        nv = min(16384, V - v0)
+        Wc = ow.elements(0, 2, v0 * d, nv * d, 0.02).reshape(nv, d).astype(np.float64)
+        lo[:, v0:v0 + nv] = x64 @ Wc.T
+    ref = oracle_partials(lo.astype(np.float32), 3, 1, 2, sample)
+    assert rel_err(got["m"][sample], ref["m"]) <= TOL
+    tiles = lo.reshape(len(sample), V // 256, 256)
+    clear = top2_gap(tiles) > 1e-2
+    assert np.array_equal(got["a"][sample][clear], ref["a"][clear])
+    assert np.allclose(got["s"][sample], ref["s"], rtol=TOL)
+
+
+# ---- canvas attention -----------------------------------------------------------
+
+def paged(kv, Hkv, hd, pg, n_pages, perm):
+    """Scatter logical keys [S][Hkv][hd] into pages through the page table `perm`."""
+    pool = np.zeros((n_pages, Hkv, pg, hd), np.float32)
+    for j in range(kv.shape[0]):
+        pool[perm[j // pg], :, j % pg, :] = kv[j]
+    return pool
+
+
+@pytest.mark.parametrize("P,causal,Hq,Hkv,hd", [
+    (0, False, 16, 4, 128), (1000, False, 16, 4, 128), (1024, True, 16, 4, 128),
+    (8192, False, 16, 4, 128), (32768, False, 16, 4, 128),
+    (64, False, 4, 2, 64), (200, True, 4, 2, 64), (2048, False, 16, 8, 128)])
+def test_canvas_attention_against_fp64(P, causal, Hq, Hkv, hd):
+    C, pg = 256, 128
+    S = P + C
+    n_pages = (S + pg - 1) // pg + 3
+    perm = np.random.default_rng(P + 1).permutation(n_pages)[: (S + pg - 1) // pg]
+    qf, qt = synth.normal_bf16((C, Hq, hd), seed=10)
+    kf, _ = synth.normal_bf16((S, Hkv, hd), seed=11)
+    vf, _ = synth.normal_bf16((S, Hkv, hd), seed=12)
+    kp = torch.from_numpy(paged(kf, Hkv, hd, pg, n_pages, perm)).to(torch.bfloat16).to(dev())
+    vp = torch.from_numpy(paged(vf, Hkv, hd, pg, n_pages, perm)).to(torch.bfloat16).to(dev())
+    table = torch.from_numpy(perm.astype(np.int32)).to(dev())
+    out = torch.empty(C, Hq, hd, dtype=torch.bfloat16, device=dev())
+    ws = torch.empty(max(dgp.dg_op_attention_workspace_bytes(P, C, Hq, Hkv, hd), 1), dtype=torch.uint8, device=dev())
+    dgp.dg_op_canvas_attention(qt.to(dev()), kp, vp, table, P, C, Hq, Hkv, hd, pg, causal, out, ws)
+    ref = om.attention(qf.astype(np.float64), kf.astype(np.float64), vf.astype(np.float64),
+                       om.visibility(P, C, "causal" if causal else "bidir"))
+    assert rel_err(bf16_to_f32(out), ref) <= TOL
+
+
+# ---- mixture of experts -----------------------------------------------------------
+
+@pytest.mark.parametrize("T,d,E,k,F", [(256, 256, 8, 2, 512), (77, 256, 8, 2, 512), (256, 2816, 128, 8, 704)])
+def test_moe_against_fp64(T, d, E, k, F):
+    wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
+    wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
+    wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
+    dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, 0, 0, 0.02)
+    xf, xt = synth.normal_bf16((T, d), seed=3)
+    y = torch.empty(T, d, dtype=torch.float32, device=dev())
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev())
+    gates = torch.empty(T, k, dtype=torch.float32, device=dev())
+    ws = torch.empty(dgp.dg_op_moe_workspace_bytes(T, d, E, k, F), dtype=torch.uint8, device=dev())
+    dgp.dg_op_moe(xt.to(dev()), wr, wgu, wd, T, d, E, k, F, y, ids, gates, ws)
+    gi = ids.cpu().numpy()
+    W = dict(wr=ow.tensor(0, 104, (E, d), 0.02), wg=ow.tensor(0, 105, (E, F, d), 0.02),
+             wu=ow.tensor(0, 106, (E, F, d), 0.02), wd=ow.tensor(0, 107, (E, d, F), 0.02))
+    x64 = xf.astype(np.float64)
+    ids_o, gates_o, r = om.route(x64, W["wr"], k)
+    # routing: exact where the top-(k+1) logits are separated, valid everywhere
+    srt = -np.sort(-r, axis=1)
+    sep = np.all(np.diff(-srt[:, : k + 1], axis=1) > 1e-2, axis=1)
+    assert np.array_equal(gi[sep], ids_o[sep])
+    _, g_ref, _ = om.route(x64, W["wr"], k, forced=gi)      # raises unless a valid top-k
+    assert np.abs(gates.cpu().numpy() - g_ref).max() <= TOL
+    y_ref = om.moe_given_routing(x64, gi, g_ref, W)
+    assert rel_err(y.cpu().numpy(), y_ref) <= TOL
+
+
+# ---- KV append (bit-exact indexing) ----------------------------------------------
+
+def test_kv_append_bit_exact_with_shuffled_pages():
+    L, n_pages, pg, Hkv, hd, pos0, n = 3, 8, 128, 2, 64, 200, 256
+    perm = np.random.default_rng(0).permutation(n_pages).astype(np.int32)
+    rng = np.random.default_rng(1)
+    kn = rng.integers(0, 65535, (L, n, Hkv, hd), dtype=np.uint16)
+    vn = rng.integers(0, 65535, (L, n, Hkv, hd), dtype=np.uint16)
+    sentinel = 0x7FC1
+    kp = torch.full((L, n_pages, Hkv, pg, hd), sentinel, dtype=torch.int16, device=dev())
+    vp = torch.full((L, n_pages, Hkv, pg, hd), sentinel, dtype=torch.int16, device=dev())
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).to(dev())
+    dgp.dg_op_kv_append(to_dev(kn), to_dev(vn), kp, vp, torch.from_numpy(perm).to(dev()), L, n_pages,
+                        pos0, n, Hkv, hd, pg)
+    kref = np.full((L, n_pages, Hkv, pg, hd), sentinel, np.uint16)
+    vref = kref.copy()
+    for t in range(n):
+        p = pos0 + t
+        kref[:, perm[p // pg], :, p % pg, :] = kn[:, t]
+        vref[:, perm[p // pg], :, p % pg, :] = vn[:, t]
+    assert np.array_equal(kp.cpu().numpy().view(np.uint16), kref)
+    assert np.array_equal(vp.cpu().numpy().view(np.uint16), vref)
