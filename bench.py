@@ -219,15 +219,14 @@ def decode_all(dgp, m, seed, scfg):
     return Ns, Cs
 
 
-def expert_bytes(cfg):
-    """Algorithmic DRAM bytes of one expert-GEMM launch of a denoising step: every
-    touched expert's weights once (N(0,1)-like routing of 256 x 8 pairs over 128
-    experts touches all of them: P(an expert is idle) = (1 - 8/128)^256 < 1e-7),
-    the gathered token rows once and the outputs once."""
-    d, E, F, k = cfg.d_model, cfg.n_experts, cfg.d_ff, cfg.top_k
-    rows = C * k
-    return {"expert_gate_up": E * 2 * F * d * 2 + rows * d * 2 + rows * F * 2,
-            "expert_down": E * d * F * 2 + rows * F * 2 + rows * d * 4}
+def expert_bytes(cfg, experts_per_launch, rows_per_launch):
+    """Algorithmic DRAM bytes of one expert-GEMM launch: the weights of every
+    expert that received a row, once (the count is measured on the device by
+    the permute kernel), the gathered token rows once and the outputs once."""
+    d, F = cfg.d_model, cfg.d_ff
+    e, r = experts_per_launch, rows_per_launch
+    return {"expert_gate_up": e * 2 * F * d * 2 + r * d * 2 + r * F * 2,
+            "expert_down": e * d * F * 2 + r * F * 2 + r * d * 4}
 
 
 def gpu_arm(args):
@@ -272,6 +271,7 @@ def gpu_arm(args):
         ev1.record(stream)
         torch.cuda.synchronize()
     prof = dgp.dg_profile_read(m)
+    touched, routed = dgp.dg_profile_experts(m)
     dgp.dg_profile(m, 0)
     ms = ev0.elapsed_time(ev1)
     ms_max = reduce_over_ranks(pg, ms, "max", rdev)
@@ -283,7 +283,8 @@ def gpu_arm(args):
     eff = sum(n * c for n, c in zip(allN, allC)) / max(sum(allC), 1)
 
     # ---- roofline of the dominant kernel (events of the timed region) --------
-    per_launch = expert_bytes(cfg)
+    n_moe = max(prof["permute"][1], 1)
+    per_launch = expert_bytes(cfg, touched / n_moe, routed / n_moe)
     kernels = {}
     for name, (kms, n) in prof.items():
         if n:
@@ -302,7 +303,8 @@ def gpu_arm(args):
     achieved = per_launch[dom] / (kms / 1e3 / n) / 1e9
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": args.traffic,
-                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": per_launch[dom]}
+                "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_bytes_per_launch": round(per_launch[dom])}
     launches = int(sum(n for _, n in prof.values()))
 
     # ---- e2e through the public API: host prompt in, host ids out ----------
@@ -340,6 +342,7 @@ def gpu_arm(args):
                            "parallelism": f"replicas x{world}"},
                 "output_tokens_per_s": tok_s, "tpf": tpf, "effective_steps": eff,
                 "N_k_mean": sum(allN) / len(allN),
+                "experts_touched_per_moe_launch": touched / n_moe,
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clk.summary(), "gpu_launches": launches}
         print(json.dumps(line), flush=True)

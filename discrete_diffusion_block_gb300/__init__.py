@@ -134,6 +134,7 @@ _SIGS = {
     "dg_kernel_class_name": (ctypes.c_char_p, [_I]),
     "dg_profile": (_I, [_P, _I]),
     "dg_profile_read": (_I, [_P, _P, _P]),
+    "dg_profile_experts": (_I, [_P, _P, _P]),
     "dg_op_fill_weights": (_I, [_P, _U64, _U64, ctypes.c_uint32, _U64, _F, _P]),
     "dg_op_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "dg_op_canvas_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -347,6 +348,13 @@ def dg_profile_read(m):
     ms, n = np.zeros(DG_K_CLASSES, np.float64), np.zeros(DG_K_CLASSES, np.int64)
     _check(load().dg_profile_read(m.handle, _ptr(ms), _ptr(n)))
     return {dg_kernel_class_name(i): (float(ms[i]), int(n[i])) for i in range(DG_K_CLASSES)}
+
+
+def dg_profile_experts(m):
+    """(experts touched, rows routed) summed over MoE launches since dg_profile(m, 1)."""
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().dg_profile_experts(m.handle, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 # ---- kernel-level calls (torch CUDA tensors for device buffers) --------------

@@ -89,7 +89,8 @@ struct dg_model {
   int Tmax = 0;
   int *ids = nullptr;
   float *h = nullptr;
-  bf16 *xn = nullptr, *q = nullptr, *o = nullptr, *act = nullptr;
+  bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr;
+  unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   float *router = nullptr, *gates = nullptr, *y = nullptr;
   int *topk = nullptr, *offs = nullptr, *perm_tok = nullptr, *slot_row = nullptr, *work = nullptr,
       *n_work = nullptr;
@@ -245,7 +246,7 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     KL(DG_K_TOPK, 1, dg::router_topk(m->router, T, c.n_experts, c.top_k, topk, m->gates, st));
     KL(DG_K_PERMUTE, 1,
        dg::moe_permute(topk, T, c.top_k, c.n_experts, dg::kExpertTileRows, m->offs, m->perm_tok,
-                       m->slot_row, m->work, m->n_work, st));
+                       m->slot_row, m->work, m->n_work, st, m->moe_stats));
     KL(DG_K_EXPERT_GATE_UP, 1,
        dg::gemm_expert_gate_up(m->xn, W.wgu, m->perm_tok, m->offs, m->work, m->n_work,
                                m->max_work, d, c.d_ff, m->act, st));
@@ -311,6 +312,8 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->ids, T));
   CKR(m->alloc(&m->h, (size_t)T * d));
   CKR(m->alloc(&m->xn, (size_t)T * d));
+  CKR(m->alloc(&m->xn_lo, (size_t)C * d));
+  CKR(m->alloc(&m->moe_stats, 2));
   CKR(m->alloc(&m->q, (size_t)T * qd));
   CKR(m->alloc(&m->o, (size_t)T * qd));
   CKR(m->alloc(&m->router, (size_t)T * E));
@@ -384,7 +387,9 @@ int canvas_forward(dg_model *m) {
   const int C = m->sc.canvas_len;
   KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, C, c.d_model, m->stream));
   CKR(run_layers(m, C, m->prefix_len, 0, false));
-  KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, m->final_norm, C, c.d_model, c.rms_eps, m->stream));
+  // final norm kept to ~16 bits (hi + lo bf16) for the LM head
+  KL(DG_K_RMSNORM, 1,
+     dg::rmsnorm_rows(m->xn, m->h, m->final_norm, C, c.d_model, c.rms_eps, m->stream, m->xn_lo));
   return DG_OK;
 }
 
@@ -412,7 +417,7 @@ int denoise_impl(dg_model *m, int32_t *done) {
   m->step += 1;
   CKR(canvas_forward(m));
   KL(DG_K_LM_HEAD, 1,
-     dg::gemm_lm_head_partials(m->xn, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
+     dg::gemm_lm_head_partials(m->xn, m->xn_lo, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
                                m->canvas_index, m->step, m->partials, m->stream));
   KL(DG_K_SAMPLER_MERGE, 1,
      dg::sampler_merge(m->partials, C, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
@@ -645,8 +650,8 @@ int dg_canvas_logits(dg_model *m, float *logits_dev) {
   CKR(canvas_forward(m));
   const dg_config &c = m->cfg;
   KL(DG_K_LM_HEAD, 1,
-     dg::gemm_store_f32(m->xn, m->lm_head, m->sc.canvas_len, c.d_model, c.vocab, logits_dev,
-                        m->stream));
+     dg::gemm_lm_head_logits(m->xn, m->xn_lo, m->lm_head, m->sc.canvas_len, c.d_model, c.vocab,
+                             logits_dev, m->stream));
   SYNC(m);
   return DG_OK;
 }
@@ -748,7 +753,19 @@ int dg_profile(dg_model *m, int32_t enable) {
       m->prof_ms[i] = 0.0;
       m->prof_launches[i] = 0;
     }
+    CK(cudaMemsetAsync(m->moe_stats, 0, 2 * sizeof(unsigned long long), m->stream));
+    SYNC(m);
   }
+  return DG_OK;
+}
+
+int dg_profile_experts(dg_model *m, int64_t *experts_touched, int64_t *rows_routed) {
+  CKR(check_model(m));
+  unsigned long long v[2] = {0, 0};
+  CK(cudaMemcpyAsync(v, m->moe_stats, sizeof(v), cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  if (experts_touched) *experts_touched = (int64_t)v[0];
+  if (rows_routed) *rows_routed = (int64_t)v[1];
   return DG_OK;
 }
 
@@ -874,8 +891,8 @@ int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *w_out, int32_t ro
                            void *partials, void *stream) {
   if (!xn || !w_out || !partials || rows < 1 || d % 64 || V % 256 || V < 256)
     return fail(DG_EINVAL, "bad arguments");
-  CK(dg::gemm_lm_head_partials((const bf16 *)xn, (const bf16 *)w_out, rows, d, V, sample_seed,
-                               canvas, step, partials, (cudaStream_t)stream));
+  CK(dg::gemm_lm_head_partials((const bf16 *)xn, nullptr, (const bf16 *)w_out, rows, d, V,
+                               sample_seed, canvas, step, partials, (cudaStream_t)stream));
   return DG_OK;
 }
 

@@ -10,6 +10,7 @@ namespace dg {
 
 struct GemmArgs {
   const bf16 *A;           // [M][lda] (+ group * a_group_stride)
+  const bf16 *A2;          // optional second A ([M][lda]); D += A2 . B^T too (hi/lo split)
   long long lda;
   long long a_group_stride;
   const bf16 *B;           // rows b_row(n)
@@ -51,29 +52,31 @@ __device__ __forceinline__ void mma_bf16_16816(float *c, const uint32_t *a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-template <int BM, int BN, int STAGES>
+template <int BM, int BN, int STAGES, int NA = 1>
 struct GemmSmem {
   static constexpr int BK = 32;
   static constexpr int LDS = BK + 8;  // bf16 per staged row (80 B, conflict-free fragments)
   static constexpr int LDC = BN + 1;  // fp32 per epilogue row (odd: conflict-free columns)
-  static constexpr size_t pipe = (size_t)STAGES * (BM + BN) * LDS * sizeof(bf16);
+  static constexpr size_t pipe = (size_t)STAGES * (NA * BM + BN) * LDS * sizeof(bf16);
   static constexpr size_t tile = (size_t)BM * LDC * sizeof(float);
   static constexpr size_t bytes = pipe > tile ? pipe : tile;
 };
 
 // Epi: struct with `static constexpr size_t extra_smem` and
 //   __device__ void operator()(float *tile, int ldc, const TileCtx &, unsigned char *extra)
-template <int BM, int BN, int WM, int WN, int STAGES, class Epi>
+// NA = 2: A is given as two bf16 matrices whose sum is the operand (hi + lo
+// split of an fp32 activation); both are multiplied with the same B tiles.
+template <int BM, int BN, int WM, int WN, int STAGES, class Epi, int NA = 1>
 __global__ void __launch_bounds__(WM *WN * 32) gemm_kernel(GemmArgs g, Epi epi) {
-  using S = GemmSmem<BM, BN, STAGES>;
+  using S = GemmSmem<BM, BN, STAGES, NA>;
   constexpr int NT = WM * WN * 32;
   constexpr int BK = S::BK, LDS = S::LDS;
   constexpr int TM = BM / WM, TN = BN / WN;
   constexpr int FM = TM / 16, FN = TN / 8;
   static_assert(TM % 16 == 0 && TN % 8 == 0, "warp tile");
   extern __shared__ __align__(16) unsigned char smem[];
-  bf16 *As = (bf16 *)smem;
-  bf16 *Bs = As + STAGES * BM * LDS;
+  bf16 *As = (bf16 *)smem;                 // [STAGES][NA][BM][LDS]
+  bf16 *Bs = As + STAGES * NA * BM * LDS;
 
   TileCtx ctx;
   ctx.m0 = blockIdx.x * BM;
@@ -101,13 +104,15 @@ __global__ void __launch_bounds__(WM *WN * 32) gemm_kernel(GemmArgs g, Epi epi) 
 
   auto load_stage = [&](int st, int kt) {
     const int k0 = kt * BK;
-    bf16 *as = As + st * BM * LDS;
+    bf16 *as = As + st * NA * BM * LDS;
     bf16 *bs = Bs + st * BN * LDS;
-    for (int c = tid; c < BM * 4; c += NT) {
-      const int r = c >> 2, q = c & 3;
+    for (int c = tid; c < NA * BM * 4; c += NT) {
+      const int h = c / (BM * 4), cc = c % (BM * 4);
+      const int r = cc >> 2, q = cc & 3;
       const bool ok = r < ctx.m_valid;
-      const bf16 *src = A + (long long)(ok ? ctx.m0 + r : 0) * g.lda + k0 + q * 8;
-      cp_async16(as + r * LDS + q * 8, src, ok);
+      const bf16 *base = (NA == 2 && h == 1) ? g.A2 : A;
+      const bf16 *src = base + (long long)(ok ? ctx.m0 + r : 0) * g.lda + k0 + q * 8;
+      cp_async16(as + (h * BM + r) * LDS + q * 8, src, ok);
     }
     for (int c = tid; c < BN * 4; c += NT) {
       const int r = c >> 2, q = c & 3;
@@ -140,19 +145,11 @@ __global__ void __launch_bounds__(WM *WN * 32) gemm_kernel(GemmArgs g, Epi epi) 
     const int nk = kt + STAGES - 1;
     if (nk < KT) load_stage(nk % STAGES, nk);
     cp_async_commit();
-    const bf16 *as = As + (kt % STAGES) * BM * LDS;
+    const bf16 *as0 = As + (kt % STAGES) * NA * BM * LDS;
     const bf16 *bs = Bs + (kt % STAGES) * BN * LDS;
 #pragma unroll
     for (int kk = 0; kk < BK; kk += 16) {
-      uint32_t af[FM][4], bfr[FN][2];
-#pragma unroll
-      for (int i = 0; i < FM; ++i) {
-        const bf16 *p = as + (wm * TM + i * 16 + (lane >> 2)) * LDS + kk + 2 * (lane & 3);
-        af[i][0] = *(const uint32_t *)p;
-        af[i][1] = *(const uint32_t *)(p + 8 * LDS);
-        af[i][2] = *(const uint32_t *)(p + 8);
-        af[i][3] = *(const uint32_t *)(p + 8 * LDS + 8);
-      }
+      uint32_t bfr[FN][2];
 #pragma unroll
       for (int j = 0; j < FN; ++j) {
         const bf16 *p = bs + (wn * TN + j * 8 + (lane >> 2)) * LDS + kk + 2 * (lane & 3);
@@ -160,9 +157,22 @@ __global__ void __launch_bounds__(WM *WN * 32) gemm_kernel(GemmArgs g, Epi epi) 
         bfr[j][1] = *(const uint32_t *)(p + 8);
       }
 #pragma unroll
-      for (int i = 0; i < FM; ++i)
+      for (int h = 0; h < NA; ++h) {
+        const bf16 *as = as0 + h * BM * LDS;
+        uint32_t af[FM][4];
 #pragma unroll
-        for (int j = 0; j < FN; ++j) mma_bf16_16816(acc[i][j], af[i], bfr[j]);
+        for (int i = 0; i < FM; ++i) {
+          const bf16 *p = as + (wm * TM + i * 16 + (lane >> 2)) * LDS + kk + 2 * (lane & 3);
+          af[i][0] = *(const uint32_t *)p;
+          af[i][1] = *(const uint32_t *)(p + 8 * LDS);
+          af[i][2] = *(const uint32_t *)(p + 8);
+          af[i][3] = *(const uint32_t *)(p + 8 * LDS + 8);
+        }
+#pragma unroll
+        for (int i = 0; i < FM; ++i)
+#pragma unroll
+          for (int j = 0; j < FN; ++j) mma_bf16_16816(acc[i][j], af[i], bfr[j]);
+      }
     }
   }
   cp_async_wait<0>();
@@ -183,11 +193,11 @@ __global__ void __launch_bounds__(WM *WN * 32) gemm_kernel(GemmArgs g, Epi epi) 
   epi(tile, S::LDC, ctx, smem + S::bytes);
 }
 
-template <int BM, int BN, int WM, int WN, int STAGES, class Epi>
+template <int BM, int BN, int WM, int WN, int STAGES, class Epi, int NA = 1>
 cudaError_t launch_gemm(const GemmArgs &g, const Epi &epi, int grid_y, cudaStream_t st) {
-  using S = GemmSmem<BM, BN, STAGES>;
+  using S = GemmSmem<BM, BN, STAGES, NA>;
   const size_t smem = S::bytes + Epi::extra_smem;
-  auto kern = gemm_kernel<BM, BN, WM, WN, STAGES, Epi>;
+  auto kern = gemm_kernel<BM, BN, WM, WN, STAGES, Epi, NA>;
   static unsigned long long attr_set = 0;  // per device: one attribute call per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -20,7 +20,7 @@ cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int 
                         uint64_t seed, int canvas, cudaStream_t st);
 cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st);
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
-                         cudaStream_t st);
+                         cudaStream_t st, bf16 *out_lo = nullptr);
 cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, float *gates,
                         cudaStream_t st);
 // Sorts the T*k (token, slot) pairs by expert.  Outputs: offs[E+1], perm_tok[T*k]
@@ -28,8 +28,10 @@ cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, floa
 // work[2*max_work] = (expert, first row) tiles of `tile_rows`, *n_work.  The
 // per-pair ranks are kept behind the work list: `work` holds
 // 2 * moe_max_work() + T*k ints.
+// stats (optional, device, 2 x u64): += experts with at least one row, += T*k.
 cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
-                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st);
+                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st,
+                        unsigned long long *stats = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
@@ -58,9 +60,13 @@ cudaError_t gemm_expert_down(const bf16 *act, const bf16 *wd, const int *offs, c
                              const int *n_work, int max_work, int d, int F, float *y,
                              cudaStream_t st);
 constexpr int kExpertTileRows = 32;  // token rows per expert GEMM tile
-cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *w_out, int T, int d, int V,
-                                  uint64_t seed, int canvas, int step, void *partials,
+// xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
+// the logits are then w_out . (xn + xn_lo).
+cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
+                                  int V, uint64_t seed, int canvas, int step, void *partials,
                                   cudaStream_t st);
+cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
+                                int V, float *logits, cudaStream_t st);
 
 // ---- sampler (kernels_sampler.cu) -------------------------------------------
 cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,

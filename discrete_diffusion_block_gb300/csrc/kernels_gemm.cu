@@ -109,6 +109,19 @@ struct EpiLmHead {
   }
 };
 
+// out[row][col] = tile, rows = tokens (A operand), cols = vocab (B operand).
+struct EpiStoreRows {
+  static constexpr size_t extra_smem = 0;
+  float *out;
+  long long ldo;
+  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
+    for (int idx = threadIdx.x; idx < c.m_valid * c.n_valid; idx += blockDim.x) {
+      const int r = idx / c.n_valid, col = idx % c.n_valid;
+      out[(size_t)(c.m0 + r) * ldo + c.n0 + col] = tile[r * ldc + col];
+    }
+  }
+};
+
 GemmArgs plain(const bf16 *A, long long lda, const bf16 *B, long long ldb, int M, int N, int K) {
   GemmArgs g{};
   g.A = A;
@@ -170,17 +183,29 @@ cudaError_t gemm_expert_down(const bf16 *act, const bf16 *wd, const int *offs, c
   return launch_gemm<128, kExpertTileRows, 4, 2, 3>(g, epi, max_work, st);
 }
 
-cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *w_out, int T, int d, int V,
-                                  uint64_t seed, int canvas, int step, void *partials,
+cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
+                                  int V, uint64_t seed, int canvas, int step, void *partials,
                                   cudaStream_t st) {
   constexpr int BM = 64;
   GemmArgs g = plain(xn, d, w_out, d, T, V, d);
+  g.A2 = xn_lo;
   EpiLmHead<BM> epi;
   epi.tiles = V / kVocabTile;
   epi.P = PartialPlanes::at(partials, T, epi.tiles);
   epi.ctr2 = gumbel_ctr2(canvas, step);
   epi.key0 = (uint32_t)seed;
   epi.key1 = (uint32_t)(seed >> 32);
+  if (xn_lo) return launch_gemm<BM, kVocabTile, 2, 4, 3, EpiLmHead<BM>, 2>(g, epi, V / kVocabTile, st);
+  return launch_gemm<BM, kVocabTile, 2, 4, 3>(g, epi, V / kVocabTile, st);
+}
+
+cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
+                                int V, float *logits, cudaStream_t st) {
+  constexpr int BM = 64;
+  GemmArgs g = plain(xn, d, w_out, d, T, V, d);
+  g.A2 = xn_lo;
+  EpiStoreRows epi{logits, V};
+  if (xn_lo) return launch_gemm<BM, kVocabTile, 2, 4, 3, EpiStoreRows, 2>(g, epi, V / kVocabTile, st);
   return launch_gemm<BM, kVocabTile, 2, 4, 3>(g, epi, V / kVocabTile, st);
 }
 

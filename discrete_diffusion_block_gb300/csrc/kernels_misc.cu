@@ -91,9 +91,10 @@ __global__ void embed_kernel(float *h, const bf16 *table, const int *ids, int d)
   for (int c = threadIdx.x; c < d; c += blockDim.x) h[(size_t)t * d + c] = __bfloat162float(row[c]);
 }
 
-// y = x / sqrt(mean(x^2) + eps) * g, fp32 statistics, bf16 output.
-__global__ void __launch_bounds__(256) rmsnorm_kernel(bf16 *out, const float *h, const float *g,
-                                                      int d, float eps) {
+// y = x / sqrt(mean(x^2) + eps) * g, fp32 statistics, bf16 output; with
+// out_lo the residual y - bf16(y) is stored too (hi + lo carries y to ~16 bits).
+__global__ void __launch_bounds__(256) rmsnorm_kernel(bf16 *out, bf16 *out_lo, const float *h,
+                                                      const float *g, int d, float eps) {
   const int t = blockIdx.x;
   const float *x = h + (size_t)t * d;
   float ss = 0.0f;
@@ -111,8 +112,12 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(bf16 *out, const float *h,
   }
   __syncthreads();
   const float inv = rsqrtf(red[0] / d + eps);
-  for (int c = threadIdx.x; c < d; c += blockDim.x)
-    out[(size_t)t * d + c] = __float2bfloat16_rn(x[c] * inv * g[c]);
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float y = x[c] * inv * g[c];
+    const bf16 hi = __float2bfloat16_rn(y);
+    out[(size_t)t * d + c] = hi;
+    if (out_lo) out_lo[(size_t)t * d + c] = __float2bfloat16_rn(y - __bfloat162float(hi));
+  }
 }
 
 // top-k of E router logits per token (value desc, expert id asc), softmax
@@ -172,7 +177,8 @@ constexpr int kPermThreads = 1024;
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, int TK, int k, int E,
                                                                int tile_rows, int *offs,
                                                                int *perm_tok, int *slot_row,
-                                                               int *work, int *n_work, int *rank) {
+                                                               int *work, int *n_work, int *rank,
+                                                               unsigned long long *stats) {
   __shared__ int cnt[257], toff[257], soff[257];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = warp; e < E; e += kPermThreads / 32) {
@@ -198,6 +204,12 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, i
     }
     offs[E] = o;
     *n_work = w;
+    if (stats) {  // experts whose weights this launch's expert GEMMs stream, and their rows
+      unsigned long long touched = 0;
+      for (int e = 0; e < E; ++e) touched += cnt[e] > 0;
+      atomicAdd(&stats[0], touched);
+      atomicAdd(&stats[1], (unsigned long long)TK);
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < TK; i += kPermThreads) {
@@ -303,9 +315,9 @@ cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d
 }
 
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
-                         cudaStream_t st) {
+                         cudaStream_t st, bf16 *out_lo) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<<<T, 256, 0, st>>>(out, h, gain, d, eps);
+  rmsnorm_kernel<<<T, 256, 0, st>>>(out, out_lo, h, gain, d, eps);
   return cudaGetLastError();
 }
 
@@ -321,11 +333,12 @@ size_t moe_max_work(int T, int k, int E, int tile_rows) {
 }
 
 cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
-                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st) {
+                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st,
+                        unsigned long long *stats) {
   if (E > 256) return cudaErrorInvalidValue;
   int *rank = work + 2 * moe_max_work(T, k, E, tile_rows);
   permute_kernel<<<1, kPermThreads, 0, st>>>(ids, T * k, k, E, tile_rows, offs, perm_tok, slot_row,
-                                             work, n_work, rank);
+                                             work, n_work, rank, stats);
   return cudaGetLastError();
 }
 

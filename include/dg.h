@@ -226,6 +226,12 @@ int dg_profile(dg_model *m, int32_t enable);
  * launches[DG_K_CLASSES] (host, may be NULL): kernels launched per class. */
 int dg_profile_read(dg_model *m, double *ms, int64_t *launches);
 
+/* Since the last dg_profile(m, 1): sum over MoE launches of the experts that
+ * received at least one row (each such expert's weights are streamed once
+ * by the expert GEMMs) and of the routed (token, slot) rows.  Host outputs,
+ * may be NULL. */
+int dg_profile_experts(dg_model *m, int64_t *experts_touched, int64_t *rows_routed);
+
 /* ---- kernel-level entry points (device pointers, caller's stream) ------- */
 
 /* Seeded synthetic weights: dst[j] (device, bf16) = element e0 + j of tensor
