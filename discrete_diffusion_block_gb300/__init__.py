@@ -138,6 +138,7 @@ _SIGS = {
     "dg_op_fill_weights": (_I, [_P, _U64, _U64, ctypes.c_uint32, _U64, _F, _P]),
     "dg_op_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "dg_op_canvas_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "dg_op_canvas_attention_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "dg_op_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "dg_op_moe": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "dg_op_fill_moe_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _U64, _F, _P]),
@@ -373,6 +374,15 @@ def dg_op_canvas_attention(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, H
                                          n_prefix, n_new, Hq, Hkv, hd, page_size, int(causal),
                                          _ptr(out), _ptr(workspace), _nbytes(workspace),
                                          _stream(stream)))
+
+
+def dg_op_canvas_attention_noalloc(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, Hkv, hd,
+                                   page_size, causal, out, stream=None):
+    """dg_op_canvas_attention without a workspace: the library's fixed 16 MiB
+    scratch holds the split-KV partials (see include/dg.h)."""
+    _check(load().dg_op_canvas_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                                 _ptr(page_table), n_prefix, n_new, Hq, Hkv, hd,
+                                                 page_size, int(causal), _ptr(out), _stream(stream)))
 
 
 def dg_op_moe_workspace_bytes(T, d, E, k, F):

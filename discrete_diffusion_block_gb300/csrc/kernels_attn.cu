@@ -8,6 +8,8 @@
 // (token t, head h) -> row t*G + (h - g*G), so each K/V tile is read once per
 // block for all of them.  Long key ranges are split across blocks and the
 // partial softmax states combined afterwards (split-KV).
+#include <mutex>
+
 #include "gemm_mma.cuh"
 #include "internal.h"
 
@@ -257,6 +259,32 @@ SplitPlan plan_splits(const AttnShape &s) {
 }
 
 }  // namespace
+
+// Fixed split-KV scratch for the entry point that must not allocate.  It is
+// a file-scope device array, so every GPU that loads the library holds it
+// for the life of the process.  Host code may not pass the symbol itself to
+// a kernel (on the host it only names a stand-in); its device address is
+// looked up once per device, with that device current.
+static __device__ __align__(256) unsigned char g_attention_scratch[kAttentionFixedScratchBytes];
+
+cudaError_t attention_fixed_scratch(void **ptr) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attention_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 int attention_launch_count(const AttnShape &s) {
   if (s.n_new <= 0) return 0;

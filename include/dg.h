@@ -267,6 +267,30 @@ int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint
                            int32_t page_size, int32_t causal, uint16_t *out, void *workspace,
                            size_t workspace_bytes, void *stream);
 
+/* Same computation as dg_op_canvas_attention, for callers that cannot hand
+ * the library a workspace or let it allocate one: code whose device memory
+ * is owned and budgeted entirely by a host framework, plugin interfaces with
+ * a fixed argument list, or latency-critical loops where an allocation (which
+ * may synchronise the device) is not acceptable.  The paper has no
+ * counterpart; this is a property of the library, not of the method.
+ *
+ * The split-KV scratch lives in a fixed 16 MiB device array inside the
+ * library (held by every GPU that loads it until the process exits); no
+ * device memory is allocated or freed by this call.  Shapes whose scratch
+ * (dg_op_attention_workspace_bytes) exceeds 16 MiB return DG_EINVAL with the
+ * required size in dg_last_error().  The first call on a device looks up the
+ * array's device address, with that device current; make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * previous call's contents (every value the kernels read is written earlier
+ * in the same call, so nothing needs clearing); calls whose GPU work overlaps
+ * in time, on any streams, race on it.  Inputs, outputs and errors otherwise
+ * as dg_op_canvas_attention. */
+int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
+                                   const uint16_t *v_pool, const int32_t *page_table,
+                                   int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
+                                   int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                                   int32_t causal, uint16_t *out, void *stream);
+
 /* Mixture-of-experts FFN (report §6 "MoE"): for each of T rows of xn
  * (device bf16 [T][d], already RMS-normalised),
  *   r = xn W_r^T; S = the top_k largest r (ties -> lower expert id);
