@@ -89,7 +89,8 @@ struct dg_model {
   int Tmax = 0;
   int *ids = nullptr;
   float *h = nullptr;
-  bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr;
+  bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr,
+       *x_perm = nullptr;
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   float *router = nullptr, *gates = nullptr, *y = nullptr;
   int *topk = nullptr, *offs = nullptr, *perm_tok = nullptr, *slot_row = nullptr, *work = nullptr,
@@ -104,7 +105,7 @@ struct dg_model {
       *done_dev = nullptr;
   uint8_t *committed = nullptr;
   float *conf = nullptr;
-  int *done_host = nullptr;  // pinned
+  int *done_host = nullptr;  // pinned, 2 ints (done, error word)
   int prompt_len = 0, prefix_len = 0, canvas_index = 0, step = 0;
   bool prefilled = false, canvas_active = false, canvas_done = false;
   // profiling: launch counts always, event-timed device ms when prof_on
@@ -232,27 +233,30 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.attn_norm, T, d, c.rms_eps, st));
     dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), m->page_table, pos0, c.page_size,
                   c.n_q_heads, c.n_kv_heads, c.head_dim, m->cos_t, m->sin_t};
-    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xn, W.wqkv, T, d, qo, st));
+    int *err = m->done_dev + 1;
+    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xn, W.wqkv, T, d, qo, err, st));
     if (kv_only_last && L == c.n_layers - 1) break;
     dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal};
     KL(DG_K_ATTENTION, dg::attention_launch_count(as),
        dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
                      m->attn_ws_bytes, st));
-    KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, st));
+    KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, st));
     KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.moe_norm, T, d, c.rms_eps, st));
-    KL(DG_K_ROUTER, 1, dg::gemm_store_f32(m->xn, W.wr, T, d, c.n_experts, m->router, st));
+    KL(DG_K_ROUTER, 1, dg::gemm_store_f32(m->xn, W.wr, T, d, c.n_experts, m->router, err, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
     KL(DG_K_TOPK, 1, dg::router_topk(m->router, T, c.n_experts, c.top_k, topk, m->gates, st));
     KL(DG_K_PERMUTE, 1,
        dg::moe_permute(topk, T, c.top_k, c.n_experts, dg::kExpertTileRows, m->offs, m->perm_tok,
                        m->slot_row, m->work, m->n_work, st, m->moe_stats));
+    const int rows = T * c.top_k;
+    KL(DG_K_PERMUTE, 1, dg::gather_rows(m->x_perm, m->xn, m->perm_tok, rows, d, st));
     KL(DG_K_EXPERT_GATE_UP, 1,
-       dg::gemm_expert_gate_up(m->xn, W.wgu, m->perm_tok, m->offs, m->work, m->n_work,
-                               m->max_work, d, c.d_ff, m->act, st));
+       dg::gemm_expert_gate_up(m->x_perm, rows, W.wgu, m->offs, m->work, m->n_work, m->max_work,
+                               c.n_experts, d, c.d_ff, m->act, err, st));
     KL(DG_K_EXPERT_DOWN, 1,
-       dg::gemm_expert_down(m->act, W.wd, m->offs, m->work, m->n_work, m->max_work, d, c.d_ff,
-                            m->y, st));
+       dg::gemm_expert_down(m->act, rows, W.wd, m->offs, m->work, m->n_work, m->max_work,
+                            c.n_experts, d, c.d_ff, m->y, err, st));
     KL(DG_K_COMBINE, 1, dg::moe_combine(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, true, st));
   }
   return DG_OK;
@@ -327,6 +331,7 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->work, (size_t)2 * m->max_work + (size_t)T * k));
   CKR(m->alloc(&m->n_work, 1));
   CKR(m->alloc(&m->act, (size_t)T * k * F));
+  CKR(m->alloc(&m->x_perm, (size_t)T * k * d));
   CKR(m->alloc(&m->y, (size_t)T * k * d));
   size_t ws = 0;
   const int shapes[3][2] = {{c.max_context - C, C}, {0, C},
@@ -344,10 +349,11 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->stable, C));
   CKR(m->alloc(&m->argmax, C));
   CKR(m->alloc(&m->gumbel, C));
-  CKR(m->alloc(&m->done_dev, 1));
+  CKR(m->alloc(&m->done_dev, 2));  // [0] canvas done, [1] error word of bounded device waits
+  CK(cudaMemset(m->done_dev, 0, 2 * sizeof(int)));
   CKR(m->alloc(&m->committed, C));
   CKR(m->alloc(&m->conf, C));
-  if (cudaMallocHost(&m->done_host, sizeof(int)) != cudaSuccess) {
+  if (cudaMallocHost(&m->done_host, 2 * sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     return fail(DG_ENOMEM, "cudaMallocHost failed");
   }
@@ -418,16 +424,18 @@ int denoise_impl(dg_model *m, int32_t *done) {
   CKR(canvas_forward(m));
   KL(DG_K_LM_HEAD, 1,
      dg::gemm_lm_head_partials(m->xn, m->xn_lo, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
-                               m->canvas_index, m->step, m->partials, m->stream));
+                               m->canvas_index, m->step, m->partials, m->done_dev + 1, m->stream));
   KL(DG_K_SAMPLER_MERGE, 1,
      dg::sampler_merge(m->partials, C, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
   KL(DG_K_SAMPLER_RULE, 1,
      dg::sampler_rule(m->argmax, m->conf, m->gumbel, C, m->step, s.budget_N, s.stable_steps,
                       s.adaptive, s.conf_threshold, m->x, m->committed, m->last, m->stable,
                       m->done_dev, m->stream));
-  CK(cudaMemcpyAsync(m->done_host, m->done_dev, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaMemcpyAsync(m->done_host, m->done_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, m->stream));
   SYNC(m);
-  m->canvas_done = *m->done_host != 0;
+  if (m->done_host[1])
+    return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", m->done_host[1]);
+  m->canvas_done = m->done_host[0] != 0;
   if (done) *done = m->canvas_done ? 1 : 0;
   return DG_OK;
 }
@@ -651,7 +659,7 @@ int dg_canvas_logits(dg_model *m, float *logits_dev) {
   const dg_config &c = m->cfg;
   KL(DG_K_LM_HEAD, 1,
      dg::gemm_lm_head_logits(m->xn, m->xn_lo, m->lm_head, m->sc.canvas_len, c.d_model, c.vocab,
-                             logits_dev, m->stream));
+                             logits_dev, m->done_dev + 1, m->stream));
   SYNC(m);
   return DG_OK;
 }
@@ -839,7 +847,7 @@ namespace {
 struct MoeWs {
   float *router;
   int *offs, *perm_tok, *slot_row, *work, *n_work;
-  bf16 *act;
+  bf16 *act, *x_perm;
   float *y_rows;
   size_t bytes;
   int max_work;
@@ -861,6 +869,7 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.work = (int *)take(((size_t)2 * w.max_work + (size_t)T * k) * 4);
   w.n_work = (int *)take(4);
   w.act = (bf16 *)take((size_t)T * k * F * 2);
+  w.x_perm = (bf16 *)take((size_t)T * k * d * 2);
   w.y_rows = (float *)take((size_t)T * k * d * 4);
   w.bytes = off;
   return w;
@@ -887,14 +896,17 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   MoeWs w = moe_layout(workspace, T, d, n_experts, top_k, d_ff);
   if (workspace_bytes < w.bytes) return fail(DG_EINVAL, "workspace too small");
   cudaStream_t st = (cudaStream_t)stream;
-  CK(dg::gemm_store_f32((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, w.router, st));
+  CK(dg::gemm_store_f32((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, w.router,
+                        nullptr, st));
   CK(dg::router_topk(w.router, T, n_experts, top_k, expert_ids, gates, st));
   CK(dg::moe_permute(expert_ids, T, top_k, n_experts, dg::kExpertTileRows, w.offs, w.perm_tok,
                      w.slot_row, w.work, w.n_work, st));
-  CK(dg::gemm_expert_gate_up((const bf16 *)xn, (const bf16 *)w_gate_up, w.perm_tok, w.offs, w.work,
-                             w.n_work, w.max_work, d, d_ff, w.act, st));
-  CK(dg::gemm_expert_down(w.act, (const bf16 *)w_down, w.offs, w.work, w.n_work, w.max_work, d,
-                          d_ff, w.y_rows, st));
+  const int rows = T * top_k;
+  CK(dg::gather_rows(w.x_perm, (const bf16 *)xn, w.perm_tok, rows, d, st));
+  CK(dg::gemm_expert_gate_up(w.x_perm, rows, (const bf16 *)w_gate_up, w.offs, w.work, w.n_work,
+                             w.max_work, n_experts, d, d_ff, w.act, nullptr, st));
+  CK(dg::gemm_expert_down(w.act, rows, (const bf16 *)w_down, w.offs, w.work, w.n_work, w.max_work,
+                          n_experts, d, d_ff, w.y_rows, nullptr, st));
   CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));
   return DG_OK;
 }
@@ -914,7 +926,7 @@ int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *w_out, int32_t ro
   if (!xn || !w_out || !partials || rows < 1 || d % 64 || V % 256 || V < 256)
     return fail(DG_EINVAL, "bad arguments");
   CK(dg::gemm_lm_head_partials((const bf16 *)xn, nullptr, (const bf16 *)w_out, rows, d, V,
-                               sample_seed, canvas, step, partials, (cudaStream_t)stream));
+                               sample_seed, canvas, step, partials, nullptr, (cudaStream_t)stream));
   return DG_OK;
 }
 

@@ -47,26 +47,30 @@ struct QkvOut {
   int pos0, pg, Hq, Hkv, hd;
   const float *cos_t, *sin_t;  // [max_pos][hd/2]
 };
-cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o,
+// `err`: device error word set by a tensor-core GEMM whose bounded wait gave up.
+cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o, int *err,
                      cudaStream_t st);
-cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h,
+cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
                           cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
-cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out,
+cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
                            cudaStream_t st);  // out[T][N] = act . w^T
-cudaError_t gemm_expert_gate_up(const bf16 *xn, const bf16 *wgu, const int *perm_tok,
-                                const int *offs, const int *work, const int *n_work,
-                                int max_work, int d, int F, bf16 *act, cudaStream_t st);
-cudaError_t gemm_expert_down(const bf16 *act, const bf16 *wd, const int *offs, const int *work,
-                             const int *n_work, int max_work, int d, int F, float *y,
-                             cudaStream_t st);
-constexpr int kExpertTileRows = 32;  // token rows per expert GEMM tile
+constexpr int kExpertTileRows = 64;  // token rows per expert GEMM tile (MMA N)
+cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, const int *offs,
+                                const int *work, const int *n_work, int max_work, int E, int d,
+                                int F, bf16 *act, int *err, cudaStream_t st);
+cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const int *offs,
+                             const int *work, const int *n_work, int max_work, int E, int d, int F,
+                             float *y, int *err, cudaStream_t st);
 // xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
 // the logits are then w_out . (xn + xn_lo).
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, uint64_t seed, int canvas, int step, void *partials,
-                                  cudaStream_t st);
+                                  int *err, cudaStream_t st);
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
-                                int V, float *logits, cudaStream_t st);
+                                int V, float *logits, int *err, cudaStream_t st);
+// x_perm[j] = xn[perm_tok[j]], j < rows (bf16 rows of d elements).
+cudaError_t gather_rows(bf16 *x_perm, const bf16 *xn, const int *perm_tok, int rows, int d,
+                        cudaStream_t st);
 
 // ---- sampler (kernels_sampler.cu) -------------------------------------------
 cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,

@@ -1,8 +1,11 @@
-// Projection, expert and LM-head GEMMs of the decoder with their fused
-// epilogues.  Weights are the A operand (rows = output features) for every
-// projection (the token count is the short side), except the LM head whose
-// epilogue needs a token's whole 256-wide vocab tile in one row.
-#include "gemm_mma.cuh"
+// Projection, expert and LM-head GEMMs of the decoder (tcgen05, gemm_tc.cuh)
+// with their fused epilogues.  Weights are the A operand (rows = output
+// features, 128 per MMA) for every projection -- the token count is the short
+// side -- except the LM head, whose epilogue needs a token's whole 256-wide
+// vocab tile in one row.
+#include <cudaTypedefs.h>
+
+#include "gemm_tc.cuh"
 #include "internal.h"
 #include "sampler.cuh"
 
@@ -122,91 +125,144 @@ struct EpiStoreRows {
   }
 };
 
-GemmArgs plain(const bf16 *A, long long lda, const bf16 *B, long long ldb, int M, int N, int K) {
-  GemmArgs g{};
-  g.A = A;
-  g.lda = lda;
-  g.B = B;
-  g.ldb = ldb;
+TcArgs targs(int M, int N, int K, int *err) {
+  TcArgs g{};
   g.M = M;
   g.N = N;
   g.K = K;
+  g.err = err;
   return g;
 }
 
 }  // namespace
 
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+cudaError_t make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if (rows == 0) rows = 1;  // an empty operand still needs a valid map; nothing is read
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+#define TMAP(map, ptr, rows, cols, box)                                            \
+  do {                                                                             \
+    cudaError_t e_ = make_tmap_bf16(&(map), (ptr), (rows), (cols), (box));         \
+    if (e_ != cudaSuccess) return e_;                                              \
+  } while (0)
+
+// Projections: A = weights [M][K] (rows = output features), B = activations
+// [T][K]; the tile is [feature][token].
 cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o,
-                     cudaStream_t st) {
+                     int *err, cudaStream_t st) {
   const int M = (o.Hq + 2 * o.Hkv) * o.hd;
-  GemmArgs g = plain(wqkv, d, xn, d, M, T, d);
+  CUtensorMap ta, tb;
+  TMAP(ta, wqkv, M, d, 128);
+  TMAP(tb, xn, T, d, 64);
   EpiQkv epi{o};
-  return launch_gemm<128, 64, 4, 2, 3>(g, epi, ceil_div(T, 64), st);
+  return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(M, T, d, err), epi, ceil_div(T, 64), st);
 }
 
-cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h,
+cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
                           cudaStream_t st) {
-  GemmArgs g = plain(w, K, act, K, N, T, K);
+  CUtensorMap ta, tb;
+  TMAP(ta, w, N, K, 128);
+  TMAP(tb, act, T, K, 64);
   EpiResidual epi{h, N};
-  return launch_gemm<128, 64, 4, 2, 3>(g, epi, ceil_div(T, 64), st);
+  return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(N, T, K, err), epi, ceil_div(T, 64), st);
 }
 
-cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out,
+cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
                            cudaStream_t st) {
-  GemmArgs g = plain(w, K, act, K, N, T, K);
+  CUtensorMap ta, tb;
+  TMAP(ta, w, N, K, 128);
+  TMAP(tb, act, T, K, 64);
   EpiStore epi{out, N};
-  return launch_gemm<128, 64, 4, 2, 3>(g, epi, ceil_div(T, 64), st);
+  return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(N, T, K, err), epi, ceil_div(T, 64), st);
 }
 
-cudaError_t gemm_expert_gate_up(const bf16 *xn, const bf16 *wgu, const int *perm_tok,
-                                const int *offs, const int *work, const int *n_work, int max_work,
-                                int d, int F, bf16 *act, cudaStream_t st) {
-  GemmArgs g = plain(wgu, d, xn, d, 2 * F, 0, d);
-  g.a_group_stride = (long long)2 * F * d;
-  g.b_rows = perm_tok;
+// Experts: A = the expert's weight rows (2-D view over all experts), B = the
+// expert's routed rows, packed contiguously in expert order.
+cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, const int *offs,
+                                const int *work, const int *n_work, int max_work, int E, int d,
+                                int F, bf16 *act, int *err, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  TMAP(ta, wgu, (uint64_t)E * 2 * F, d, 128);
+  TMAP(tb, x_perm, rows, d, kExpertTileRows);
+  TcArgs g = targs(2 * F, 0, d, err);
+  g.a_group_rows = 2 * F;
   g.work = work;
   g.n_work = n_work;
   g.group_offs = offs;
   EpiSwiGlu epi{act, F};
-  return launch_gemm<128, kExpertTileRows, 4, 2, 3>(g, epi, max_work, st);
+  return launch_tc<kExpertTileRows, 4, 1, 128>(ta, ta, tb, g, epi, max_work, st);
 }
 
-cudaError_t gemm_expert_down(const bf16 *act, const bf16 *wd, const int *offs, const int *work,
-                             const int *n_work, int max_work, int d, int F, float *y,
-                             cudaStream_t st) {
-  GemmArgs g = plain(wd, F, act, F, d, 0, F);
-  g.a_group_stride = (long long)d * F;
+cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const int *offs,
+                             const int *work, const int *n_work, int max_work, int E, int d, int F,
+                             float *y, int *err, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  TMAP(ta, wd, (uint64_t)E * d, F, 128);
+  TMAP(tb, act, rows, F, kExpertTileRows);
+  TcArgs g = targs(d, 0, F, err);
+  g.a_group_rows = d;
   g.work = work;
   g.n_work = n_work;
   g.group_offs = offs;
   EpiStore epi{y, d};
-  return launch_gemm<128, kExpertTileRows, 4, 2, 3>(g, epi, max_work, st);
+  return launch_tc<kExpertTileRows, 4, 1, 128>(ta, ta, tb, g, epi, max_work, st);
 }
 
+// LM head: A = normalised token rows (hi, and lo of a hi/lo split), B = the
+// vocab rows of W_out, one 256-wide vocab tile per CTA column.
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, uint64_t seed, int canvas, int step, void *partials,
-                                  cudaStream_t st) {
-  constexpr int BM = 64;
-  GemmArgs g = plain(xn, d, w_out, d, T, V, d);
-  g.A2 = xn_lo;
-  EpiLmHead<BM> epi;
+                                  int *err, cudaStream_t st) {
+  CUtensorMap ta, ta2, tb;
+  TMAP(ta, xn, T, d, 128);
+  TMAP(ta2, xn_lo ? xn_lo : xn, T, d, 128);
+  TMAP(tb, w_out, V, d, 256);
+  EpiLmHead<64> epi;
   epi.tiles = V / kVocabTile;
   epi.P = PartialPlanes::at(partials, T, epi.tiles);
   epi.ctr2 = gumbel_ctr2(canvas, step);
   epi.key0 = (uint32_t)seed;
   epi.key1 = (uint32_t)(seed >> 32);
-  if (xn_lo) return launch_gemm<BM, kVocabTile, 2, 4, 3, EpiLmHead<BM>, 2>(g, epi, V / kVocabTile, st);
-  return launch_gemm<BM, kVocabTile, 2, 4, 3>(g, epi, V / kVocabTile, st);
+  const TcArgs g = targs(T, V, d, err);
+  if (xn_lo) return launch_tc<256, 3, 2, 64>(ta, ta2, tb, g, epi, V / kVocabTile, st);
+  return launch_tc<256, 4, 1, 64>(ta, ta, tb, g, epi, V / kVocabTile, st);
 }
 
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
-                                int V, float *logits, cudaStream_t st) {
-  constexpr int BM = 64;
-  GemmArgs g = plain(xn, d, w_out, d, T, V, d);
-  g.A2 = xn_lo;
+                                int V, float *logits, int *err, cudaStream_t st) {
+  CUtensorMap ta, ta2, tb;
+  TMAP(ta, xn, T, d, 128);
+  TMAP(ta2, xn_lo ? xn_lo : xn, T, d, 128);
+  TMAP(tb, w_out, V, d, 256);
   EpiStoreRows epi{logits, V};
-  if (xn_lo) return launch_gemm<BM, kVocabTile, 2, 4, 3, EpiStoreRows, 2>(g, epi, V / kVocabTile, st);
-  return launch_gemm<BM, kVocabTile, 2, 4, 3>(g, epi, V / kVocabTile, st);
+  const TcArgs g = targs(T, V, d, err);
+  if (xn_lo) return launch_tc<256, 3, 2, 64>(ta, ta2, tb, g, epi, V / kVocabTile, st);
+  return launch_tc<256, 4, 1, 64>(ta, ta, tb, g, epi, V / kVocabTile, st);
 }
 
 }  // namespace dg

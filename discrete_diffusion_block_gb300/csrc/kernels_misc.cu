@@ -239,6 +239,18 @@ __global__ void combine_kernel(float *h, const float *y, const float *gates, con
   }
 }
 
+// x_perm[j] = xn[perm_tok[j]]: the routed rows in expert order, so that each
+// expert's rows are one contiguous TMA box source.
+__global__ void gather_rows_kernel(uint4 *dst, const uint4 *src, const int *perm_tok, int rows,
+                                   int vec) {
+  const size_t total = (size_t)rows * vec;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / vec), c = (int)(i % vec);
+    dst[i] = src[(size_t)perm_tok[r] * vec + c];
+  }
+}
+
 // 16-byte copies of [L][n][Hkv][hd] rows into the paged pools.
 __global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *k_pool,
                                  uint4 *v_pool, const int *page_table, int L, int n_pages, int pos0,
@@ -346,6 +358,15 @@ cudaError_t moe_combine(float *h, const float *y, const float *gates, const int 
                         int k, int d, bool accumulate, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   combine_kernel<<<T, 256, 0, st>>>(h, y, gates, slot_row, k, d, accumulate ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t gather_rows(bf16 *x_perm, const bf16 *xn, const int *perm_tok, int rows, int d,
+                        cudaStream_t st) {
+  const size_t total = (size_t)rows * (d / 8);
+  if (total == 0) return cudaSuccess;
+  gather_rows_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, st>>>(
+      (uint4 *)x_perm, (const uint4 *)xn, perm_tok, rows, d / 8);
   return cudaGetLastError();
 }
 
