@@ -155,6 +155,14 @@ __host__ __device__ __forceinline__ uint32_t gumbel_ctr2(int canvas, int step) {
   return ((uint32_t)canvas << 16) | (uint32_t)step;
 }
 
+// Per-step sampler parameters kept in device memory, so that a captured
+// denoising step can be replayed for every step of a canvas: Gumbel counter
+// word 2, Philox key of the sample seed, 1-based step number.
+struct StepParams {
+  uint32_t ctr2, key0, key1;
+  int step;
+};
+
 // Merge of two adjacent ranges, L the lower vocab range.  An empty right
 // operand (m = -inf) leaves L unchanged.
 __device__ __forceinline__ Partial merge_partials(const Partial &L, const Partial &R) {

@@ -19,6 +19,7 @@
 // clean canvas's K/V.
 #include <chrono>
 #include <cstdarg>
+#include <map>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -118,6 +119,16 @@ struct dg_model {
   };
   std::vector<ProfRec> prof_pending;
   std::vector<cudaEvent_t> prof_free;
+  // CUDA graphs of the denoising step, one per (prefix length, profiling on)
+  struct StepGraph {
+    cudaGraphExec_t exec = nullptr;
+    std::vector<ProfRec> recs;  // event pairs captured as graph nodes
+    int64_t launches[DG_K_CLASSES] = {};
+  };
+  std::map<std::pair<int, int>, StepGraph> graphs;
+  StepGraph *capturing = nullptr;
+  bool eager_step_done = false;  // the first step runs eagerly (sets kernel attributes)
+  dg::StepParams *dyn_dev = nullptr, *dyn_host = nullptr;  // per-step sampler words
 
   template <class T>
   int alloc(T **p, size_t n) {
@@ -151,23 +162,56 @@ cudaEvent_t prof_event(dg_model *m) {
   return e;
 }
 
+// Events of a step being captured belong to its graph (they are replayed with
+// it); other events come from the model's reuse pool.
+cudaEvent_t prof_new_event(dg_model *m) {
+  if (!m->capturing) return prof_event(m);
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
 cudaEvent_t prof_begin(dg_model *m) {
   if (!m->prof_on) return nullptr;
-  cudaEvent_t a = prof_event(m);
+  cudaEvent_t a = prof_new_event(m);
   if (a) cudaEventRecord(a, m->stream);
   return a;
 }
 
 void prof_end(dg_model *m, int cls, int n_kernels, cudaEvent_t a) {
-  m->prof_launches[cls] += n_kernels;
+  (m->capturing ? m->capturing->launches : m->prof_launches)[cls] += n_kernels;
   if (!a) return;
-  cudaEvent_t b = prof_event(m);
+  cudaEvent_t b = prof_new_event(m);
   if (!b) {
-    m->prof_free.push_back(a);
+    if (m->capturing) cudaEventDestroy(a); else m->prof_free.push_back(a);
     return;
   }
   cudaEventRecord(b, m->stream);
-  m->prof_pending.push_back({cls, a, b});
+  (m->capturing ? m->capturing->recs : m->prof_pending).push_back({cls, a, b});
+}
+
+// After a replay has finished: add the graph's launches and event times.
+void prof_collect_graph(dg_model *m, const dg_model::StepGraph &g) {
+  for (int i = 0; i < DG_K_CLASSES; ++i) m->prof_launches[i] += g.launches[i];
+  for (const auto &r : g.recs) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) m->prof_ms[r.cls] += ms;
+    cudaGetLastError();
+  }
+}
+
+void destroy_graphs(dg_model *m) {
+  for (auto &kv : m->graphs) {
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    for (auto &r : kv.second.recs) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+  }
+  m->graphs.clear();
 }
 
 // Fold finished event pairs into the per-class totals (stream already synced).
@@ -353,10 +397,12 @@ int alloc_model(dg_model *m) {
   CK(cudaMemset(m->done_dev, 0, 2 * sizeof(int)));
   CKR(m->alloc(&m->committed, C));
   CKR(m->alloc(&m->conf, C));
-  if (cudaMallocHost(&m->done_host, 2 * sizeof(int)) != cudaSuccess) {
+  if (cudaMallocHost(&m->done_host, 2 * sizeof(int)) != cudaSuccess ||
+      cudaMallocHost(&m->dyn_host, sizeof(dg::StepParams)) != cudaSuccess) {
     cudaGetLastError();
     return fail(DG_ENOMEM, "cudaMallocHost failed");
   }
+  CKR(m->alloc(&m->dyn_dev, 1));
   return DG_OK;
 }
 
@@ -415,24 +461,81 @@ int begin_canvas(dg_model *m) {
   return DG_OK;
 }
 
-int denoise_impl(dg_model *m, int32_t *done) {
-  CKR(begin_canvas(m));
+// The kernels of one denoising step after canvas initialisation: forward,
+// LM head with the fused vocab reduction, merge, commit rule.  Step-varying
+// sampler words are read from m->dyn_dev, so the sequence can be captured.
+int step_launches(dg_model *m) {
   const dg_config &c = m->cfg;
   const dg_sampler_config &s = m->sc;
   const int C = s.canvas_len;
-  m->step += 1;
   CKR(canvas_forward(m));
   KL(DG_K_LM_HEAD, 1,
      dg::gemm_lm_head_partials(m->xn, m->xn_lo, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
-                               m->canvas_index, m->step, m->partials, m->done_dev + 1, m->stream));
+                               m->canvas_index, m->step, m->partials, m->done_dev + 1, m->stream,
+                               m->dyn_dev));
   KL(DG_K_SAMPLER_MERGE, 1,
      dg::sampler_merge(m->partials, C, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
   KL(DG_K_SAMPLER_RULE, 1,
      dg::sampler_rule(m->argmax, m->conf, m->gumbel, C, m->step, s.budget_N, s.stable_steps,
                       s.adaptive, s.conf_threshold, m->x, m->committed, m->last, m->stable,
-                      m->done_dev, m->stream));
+                      m->done_dev, m->stream, m->dyn_dev));
+  return DG_OK;
+}
+
+// Capture step_launches() into a graph for the current prefix length.
+int capture_step(dg_model *m, dg_model::StepGraph *g) {
+  CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+  m->capturing = g;
+  const int r = step_launches(m);
+  m->capturing = nullptr;
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(m->stream, &graph);
+  if (r != DG_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return r;
+  }
+  if (e != cudaSuccess) return fail(DG_ECUDA, "graph capture failed: %s", cudaGetErrorString(e));
+  const cudaError_t ei = cudaGraphInstantiate(&g->exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return fail(DG_ECUDA, "graph instantiation failed: %s", cudaGetErrorString(ei));
+  return DG_OK;
+}
+
+int denoise_impl(dg_model *m, int32_t *done) {
+  CKR(begin_canvas(m));
+  const dg_sampler_config &s = m->sc;
+  m->step += 1;
+  m->dyn_host->ctr2 = dg::gumbel_ctr2(m->canvas_index, m->step);
+  m->dyn_host->key0 = (uint32_t)s.sample_seed;
+  m->dyn_host->key1 = (uint32_t)(s.sample_seed >> 32);
+  m->dyn_host->step = m->step;
+  CK(cudaMemcpyAsync(m->dyn_dev, m->dyn_host, sizeof(dg::StepParams), cudaMemcpyHostToDevice,
+                     m->stream));
+  const dg_model::StepGraph *used = nullptr;
+  if (!m->eager_step_done) {
+    CKR(step_launches(m));
+    m->eager_step_done = true;
+  } else {
+    const auto key = std::make_pair(m->prefix_len, m->prof_on ? 1 : 0);
+    auto it = m->graphs.find(key);
+    if (it == m->graphs.end()) {
+      dg_model::StepGraph g;
+      const int r = capture_step(m, &g);
+      if (r != DG_OK) {
+        for (auto &rec : g.recs) {
+          cudaEventDestroy(rec.a);
+          cudaEventDestroy(rec.b);
+        }
+        return r;
+      }
+      it = m->graphs.emplace(key, std::move(g)).first;
+    }
+    CK(cudaGraphLaunch(it->second.exec, m->stream));
+    used = &it->second;
+  }
   CK(cudaMemcpyAsync(m->done_host, m->done_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, m->stream));
   SYNC(m);
+  if (used) prof_collect_graph(m, *used);
   if (m->done_host[1])
     return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", m->done_host[1]);
   m->canvas_done = m->done_host[0] != 0;
@@ -515,9 +618,11 @@ void dg_free_model(dg_model *m) {
   if (!m) return;
   if (m->stream) cudaStreamSynchronize(m->stream);
   prof_collect(m);
+  destroy_graphs(m);
   for (cudaEvent_t e : m->prof_free) cudaEventDestroy(e);
   for (void *p : m->allocs) cudaFree(p);
   if (m->done_host) cudaFreeHost(m->done_host);
+  if (m->dyn_host) cudaFreeHost(m->dyn_host);
   if (m->own_stream) cudaStreamDestroy(m->stream);
   delete m;
 }
@@ -587,7 +692,13 @@ int dg_set_sampler(dg_model *m, const dg_sampler_config *scfg) {
   CKR(check_model(m));
   CKR(validate(&m->cfg, scfg));
   if (scfg->canvas_len != m->sc.canvas_len) return fail(DG_EINVAL, "canvas_len is fixed at init");
-  m->sc = *scfg;
+  const dg_sampler_config &o = m->sc;
+  if (scfg->budget_N != o.budget_N || scfg->stable_steps != o.stable_steps ||
+      scfg->adaptive != o.adaptive || scfg->conf_threshold != o.conf_threshold) {
+    CK(cudaStreamSynchronize(m->stream));
+    destroy_graphs(m);  // captured steps hold the old rule constants
+  }
+  m->sc = *scfg;  // the sample seed is read per step from device memory
   return DG_OK;
 }
 

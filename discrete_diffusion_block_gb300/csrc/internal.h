@@ -63,9 +63,10 @@ cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const in
                              float *y, int *err, cudaStream_t st);
 // xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
 // the logits are then w_out . (xn + xn_lo).
+// dyn (optional, device): stream words taken from memory instead of seed/canvas/step.
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, uint64_t seed, int canvas, int step, void *partials,
-                                  int *err, cudaStream_t st);
+                                  int *err, cudaStream_t st, const StepParams *dyn = nullptr);
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                 int V, float *logits, int *err, cudaStream_t st);
 // x_perm[j] = xn[perm_tok[j]], j < rows (bf16 rows of d elements).
@@ -77,10 +78,11 @@ cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed,
                             int step, void *partials, cudaStream_t st);
 cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,
                           int *gumbel, cudaStream_t st);
+// dyn (optional, device): the step number is taken from dyn->step.
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
                          int budget_N, int stable_steps, int adaptive, float conf_threshold,
                          int *x, uint8_t *committed, int *last, int *stable, int *done,
-                         cudaStream_t st);
+                         cudaStream_t st, const StepParams *dyn = nullptr);
 
 // ---- attention (kernels_attn.cu) -------------------------------------------
 struct AttnShape {

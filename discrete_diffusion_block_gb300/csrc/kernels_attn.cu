@@ -331,16 +331,21 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   }
   dim3 grid(ceil_div(rows_total, kRowsPerBlock), s.Hkv, pl.splits);
   const size_t smem = (size_t)4 * kKeysPerTile * (s.hd + 8) * sizeof(bf16);
-  cudaError_t e;
-  if (s.hd == 128) {
-    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static unsigned long long attr_set[2] = {0, 0};  // per device, per head size
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int which = s.hd == 128 ? 1 : 0;
+  if (dev >= 64 || !((attr_set[which] >> dev) & 1ull)) {
+    e = which ? cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+              : cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_kernel<128><<<grid, 128, smem, st>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attn_kernel<64><<<grid, 128, smem, st>>>(p);
+    if (dev < 64) attr_set[which] |= 1ull << dev;
   }
+  if (which)
+    attn_kernel<128><<<grid, 128, smem, st>>>(p);
+  else
+    attn_kernel<64><<<grid, 128, smem, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (pl.splits > 1) {
     attn_combine_kernel<<<dim3(rows_total, s.Hkv), 128, 0, st>>>(p.o_part, p.ml_part, pl.splits,

@@ -5,6 +5,9 @@
 // vocab tile in one row.
 #include <cudaTypedefs.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "gemm_tc.cuh"
 #include "internal.h"
 #include "sampler.cuh"
@@ -102,13 +105,15 @@ struct EpiLmHead {
   PartialPlanes P;
   int tiles;
   uint32_t ctr2, key0, key1;
+  const StepParams *dyn;  // when set, the stream words come from device memory
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *extra) const {
     PartialScratch sc;
     sc.kap = (float *)extra;
     sc.rm = sc.kap + BM * ldc;
     sc.ra = (int *)(sc.rm + BM);
-    block_tile_partials(tile, ldc, sc, c.m_valid, c.n0, c.n0 / kVocabTile, tiles, c.m0, ctr2, key0,
-                        key1, P, c.m0);
+    const uint32_t c2 = dyn ? dyn->ctr2 : ctr2, k0 = dyn ? dyn->key0 : key0, k1 = dyn ? dyn->key1 : key1;
+    block_tile_partials(tile, ldc, sc, c.m_valid, c.n0, c.n0 / kVocabTile, tiles, c.m0, c2, k0, k1,
+                        P, c.m0);
   }
 };
 
@@ -165,9 +170,48 @@ cudaError_t make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uin
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Encoded maps depend only on (address, shape, box); the decoder reuses the
+// same weight and activation buffers every step, so each map is encoded once
+// and copied into the launch parameters afterwards.
+namespace {
+struct TmapKey {
+  const void *p;
+  uint64_t rows, cols;
+  uint32_t box;
+  bool operator==(const TmapKey &o) const {
+    return p == o.p && rows == o.rows && cols == o.cols && box == o.box;
+  }
+};
+struct TmapKeyHash {
+  size_t operator()(const TmapKey &k) const {
+    size_t h = std::hash<const void *>()(k.p);
+    h ^= std::hash<uint64_t>()(k.rows * 1000003ull + k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    return h ^ (k.box * 0x85ebca6bu);
+  }
+};
+std::mutex g_tmap_mu;
+std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
+}  // namespace
+
+static cudaError_t tmap_cached(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                               uint32_t box) {
+  const TmapKey key{ptr, rows, cols, box};
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  auto it = g_tmaps.find(key);
+  if (it != g_tmaps.end()) {
+    *map = it->second;
+    return cudaSuccess;
+  }
+  cudaError_t e = make_tmap_bf16(map, ptr, rows, cols, box);
+  if (e != cudaSuccess) return e;
+  if (g_tmaps.size() > 16384) g_tmaps.clear();
+  g_tmaps.emplace(key, *map);
+  return cudaSuccess;
+}
+
 #define TMAP(map, ptr, rows, cols, box)                                            \
   do {                                                                             \
-    cudaError_t e_ = make_tmap_bf16(&(map), (ptr), (rows), (cols), (box));         \
+    cudaError_t e_ = tmap_cached(&(map), (ptr), (rows), (cols), (box));            \
     if (e_ != cudaSuccess) return e_;                                              \
   } while (0)
 
@@ -237,7 +281,7 @@ cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const in
 // vocab rows of W_out, one 256-wide vocab tile per CTA column.
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, uint64_t seed, int canvas, int step, void *partials,
-                                  int *err, cudaStream_t st) {
+                                  int *err, cudaStream_t st, const StepParams *dyn) {
   CUtensorMap ta, ta2, tb;
   TMAP(ta, xn, T, d, 128);
   TMAP(ta2, xn_lo ? xn_lo : xn, T, d, 128);
@@ -248,6 +292,7 @@ cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 
   epi.ctr2 = gumbel_ctr2(canvas, step);
   epi.key0 = (uint32_t)seed;
   epi.key1 = (uint32_t)(seed >> 32);
+  epi.dyn = dyn;
   const TcArgs g = targs(T, V, d, err);
   if (xn_lo) return launch_tc<256, 3, 2, 64>(ta, ta2, tb, g, epi, V / kVocabTile, st);
   return launch_tc<256, 4, 1, 64>(ta, ta, tb, g, epi, V / kVocabTile, st);

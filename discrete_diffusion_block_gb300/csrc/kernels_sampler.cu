@@ -93,8 +93,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(PartialPlanes P, i
 
 __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum, int C, int step,
                             int budget_N, int stable_steps, int adaptive, float thr, int *x,
-                            uint8_t *committed, int *last, int *stable, int *done) {
+                            uint8_t *committed, int *last, int *stable, int *done,
+                            const StepParams *dyn) {
   const int i = threadIdx.x;
+  if (dyn) step = dyn->step;
   bool com = true;
   if (i < C) {
     com = committed[i] != 0;
@@ -149,11 +151,11 @@ cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
                          int budget_N, int stable_steps, int adaptive, float conf_threshold,
                          int *x, uint8_t *committed, int *last, int *stable, int *done,
-                         cudaStream_t st) {
+                         cudaStream_t st, const StepParams *dyn) {
   if (C > 1024) return cudaErrorInvalidValue;
   const int threads = ((C + 31) / 32) * 32;
   rule_kernel<<<1, threads, 0, st>>>(argmax, conf, gumbel, C, step, budget_N, stable_steps,
-                                     adaptive, conf_threshold, x, committed, last, stable, done);
+                                     adaptive, conf_threshold, x, committed, last, stable, done, dyn);
   return cudaGetLastError();
 }
 
