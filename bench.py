@@ -291,10 +291,10 @@ def gpu_arm(args):
             kernels[name] = {"ms_total": round(kms, 3), "launches": n,
                              "us_per_launch": round(kms / n * 1e3, 2)}
     for name, b in per_launch.items():
-        if prof[name][1]:
+        if prof[name][1] and prof[name][0] > 0:
             a = b / (prof[name][0] / 1e3 / prof[name][1]) / 1e9
             kernels[name].update(GBps=round(a, 1), frac_hbm=round(a / hbm, 4))
-    if prof["lm_head"][1]:
+    if prof["lm_head"][1] and prof["lm_head"][0] > 0:
         fl = 2.0 * C * cfg.d_model * cfg.vocab
         a = fl / (prof["lm_head"][0] / 1e3 / prof["lm_head"][1]) / 1e12
         kernels["lm_head"].update(TFLOPs=round(a, 1), frac_bf16_sustained=round(a / tf_sust, 4))

@@ -174,10 +174,19 @@ cudaEvent_t prof_new_event(dg_model *m) {
   return e;
 }
 
+// Inside a capture a plain record only orders the capture; the external
+// flag turns it into an event-record node that timestamps each replay.
+void prof_record(dg_model *m, cudaEvent_t e) {
+  if (m->capturing)
+    cudaEventRecordWithFlags(e, m->stream, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, m->stream);
+}
+
 cudaEvent_t prof_begin(dg_model *m) {
   if (!m->prof_on) return nullptr;
   cudaEvent_t a = prof_new_event(m);
-  if (a) cudaEventRecord(a, m->stream);
+  if (a) prof_record(m, a);
   return a;
 }
 
@@ -189,7 +198,7 @@ void prof_end(dg_model *m, int cls, int n_kernels, cudaEvent_t a) {
     if (m->capturing) cudaEventDestroy(a); else m->prof_free.push_back(a);
     return;
   }
-  cudaEventRecord(b, m->stream);
+  prof_record(m, b);
   (m->capturing ? m->capturing->recs : m->prof_pending).push_back({cls, a, b});
 }
 
