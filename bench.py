@@ -255,7 +255,8 @@ def gpu_arm(args):
     for w in range(args.warmup):
         decode_all(dgp, m, 10_000 + w, scfg)
 
-    dgp.dg_profile(m, 1)
+    # ---- timed region: the value (launch counting only, no per-kernel events)
+    dgp.dg_profile(m, 2)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     allN, allC = [], []
     rdev = dev if pg is not None else None
@@ -270,9 +271,7 @@ def gpu_arm(args):
             allC += Cs
         ev1.record(stream)
         torch.cuda.synchronize()
-    prof = dgp.dg_profile_read(m)
-    touched, routed = dgp.dg_profile_experts(m)
-    dgp.dg_profile(m, 0)
+    launches = int(sum(n for _, n in dgp.dg_profile_read(m).values()))
     ms = ev0.elapsed_time(ev1)
     ms_max = reduce_over_ranks(pg, ms, "max", rdev)
     steps_total = reduce_over_ranks(pg, sum(allN), "sum", rdev)
@@ -282,9 +281,19 @@ def gpu_arm(args):
     tpf = sum(allC) / (sum(allN) + args.steps * (CANVASES - 1))
     eff = sum(n * c for n, c in zip(allN, allC)) / max(sum(allC), 1)
 
-    # ---- roofline of the dominant kernel (events of the timed region) --------
-    n_moe = max(prof["permute"][1], 1)
+    # ---- profiled step: CUDA events around every kernel (graph event nodes) ----
+    dgp.dg_profile(m, 1)
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record(stream)
+    pN, _ = decode_all(dgp, m, 40_000, scfg)
+    pe1.record(stream)
+    torch.cuda.synchronize()
+    prof = dgp.dg_profile_read(m)
+    touched, routed = dgp.dg_profile_experts(m)
+    dgp.dg_profile(m, 0)
+    n_moe = max(prof["permute"][1] // 2, 1)                  # permute + row gather per MoE
     per_launch = expert_bytes(cfg, touched / n_moe, routed / n_moe)
+    hbm, tf_burst, tf_sust, peak_src = peaks()
     kernels = {}
     for name, (kms, n) in prof.items():
         if n:
@@ -295,7 +304,7 @@ def gpu_arm(args):
             a = b / (prof[name][0] / 1e3 / prof[name][1]) / 1e9
             kernels[name].update(GBps=round(a, 1), frac_hbm=round(a / hbm, 4))
     if prof["lm_head"][1] and prof["lm_head"][0] > 0:
-        fl = 2.0 * C * cfg.d_model * cfg.vocab
+        fl = 2 * 2.0 * C * cfg.d_model * cfg.vocab     # hi + lo halves of the split activation
         a = fl / (prof["lm_head"][0] / 1e3 / prof["lm_head"][1]) / 1e12
         kernels["lm_head"].update(TFLOPs=round(a, 1), frac_bf16_sustained=round(a / tf_sust, 4))
     dom = max(per_launch, key=lambda k: prof[k][0])
@@ -304,8 +313,9 @@ def gpu_arm(args):
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": args.traffic,
                 "peak_source": f"{peak_src} hbm_gbs",
-                "algorithmic_bytes_per_launch": round(per_launch[dom])}
-    launches = int(sum(n for _, n in prof.values()))
+                "algorithmic_bytes_per_launch": round(per_launch[dom]),
+                "measured_in": f"profiled step after the timed region ({pe0.elapsed_time(pe1):.0f} ms, "
+                               f"{sum(pN)} denoising steps)"}
 
     # ---- e2e through the public API: host prompt in, host ids out ----------
     e2e = None
@@ -342,12 +352,128 @@ def gpu_arm(args):
                            "parallelism": f"replicas x{world}"},
                 "output_tokens_per_s": tok_s, "tpf": tpf, "effective_steps": eff,
                 "N_k_mean": sum(allN) / len(allN),
-                "experts_touched_per_moe_launch": touched / n_moe,
+                "experts_touched_per_moe_launch": round(touched / n_moe, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clk.summary(), "gpu_launches": launches}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+    return 0
+
+
+# ---- kernel micro-benchmarks (attention and MoE + sampler micro-op shapes) ---
+
+def micro(args):
+    """Per-kernel timings at the micro-op shapes; one JSON line per case."""
+    import numpy as np
+    import torch
+    import discrete_diffusion_block_gb300 as dgp
+    from discrete_diffusion_block_gb300 import build, synth
+    torch.cuda.set_device(0)
+    build.build()
+    dgp.load()
+    hbm, tf_burst, tf_sust, src = peaks()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > L2
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts) / 1e3
+
+    out = []
+    which = args.micro
+    if which in ("moe", "all"):
+        T, d, E, k, F = 256, 2816, 128, 8, 704
+        wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev)
+        wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev)
+        wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev)
+        dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, 0, 0)
+        _, xt = synth.normal_bf16((T, d), seed=3)
+        x = xt.to(dev)
+        y = torch.empty(T, d, dtype=torch.float32, device=dev)
+        ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        gates = torch.empty(T, k, dtype=torch.float32, device=dev)
+        ws = torch.empty(dgp.dg_op_moe_workspace_bytes(T, d, E, k, F), dtype=torch.uint8, device=dev)
+        sec = timed(lambda: dgp.dg_op_moe(x, wr, wgu, wd, T, d, E, k, F, y, ids, gates, ws), args.steps)
+        touched = len(np.unique(ids.cpu().numpy()))
+        byt = touched * 3 * F * d * 2 + E * d * 2
+        fl = 2.0 * T * k * 3 * F * d
+        out.append({"micro": "moe_layer", "shape": f"T={T} d={d} E={E} top{k} F={F}",
+                    "experts_touched": touched, "ms": sec * 1e3, "GBps": byt / sec / 1e9,
+                    "frac_hbm": byt / sec / 1e9 / hbm, "TFLOPs": fl / sec / 1e12})
+    if which in ("lmhead", "all"):
+        T, d, V = 256, 2816, 262144
+        w = torch.empty(V * d, dtype=torch.bfloat16, device=dev)
+        dgp.dg_op_fill_weights(w, 0, 2)
+        _, xt = synth.normal_bf16((T, d), seed=2)
+        x = xt.to(dev)
+        part = torch.empty(dgp.partials_bytes(T, V) // 4, dtype=torch.int32, device=dev)
+        sec = timed(lambda: dgp.dg_op_lm_head_partials(x, w, T, d, V, 1, 0, 1, part), args.steps)
+        fl = 2.0 * T * d * V
+        out.append({"micro": "lm_head_partials", "shape": f"T={T} d={d} V={V}", "ms": sec * 1e3,
+                    "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst,
+                    "GBps_weights": V * d * 2 / sec / 1e9})
+    if which in ("sampler", "all"):
+        C, V = 256, 262144
+        logits = torch.from_numpy(synth.logits(C, V, seed=1)).to(dev)
+        part = torch.empty(dgp.partials_bytes(C, V) // 4, dtype=torch.int32, device=dev)
+        sc = dgp.SamplerConfig()
+        st = [torch.zeros(C, dtype=torch.int32, device=dev) for _ in range(6)]
+        com = torch.zeros(C, dtype=torch.uint8, device=dev)
+        conf = torch.zeros(C, dtype=torch.float32, device=dev)
+        done = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def run():
+            dgp.dg_op_logits_partials(logits, C, V, 1, 0, 1, part)
+            dgp.dg_op_sampler_update(part, C, V, 1, sc, st[0], com, st[1], st[2], st[3], conf, st[4], done)
+        sec = timed(run, args.steps)
+        byt = C * V * 4
+        out.append({"micro": "sampler_materialized_logits", "shape": f"C={C} V={V}", "ms": sec * 1e3,
+                    "GBps": byt / sec / 1e9, "frac_hbm": byt / sec / 1e9 / hbm})
+    if which in ("attention", "all"):
+        Hq, Hkv, hd, C, pg = 16, 4, 128, 256, 128
+        for P in (0, 1024, 8192, 32768):
+            S = P + C
+            n_pages = (S + pg - 1) // pg
+            kp = torch.randn(n_pages, Hkv, pg, hd, device=dev).to(torch.bfloat16)
+            vp = torch.randn(n_pages, Hkv, pg, hd, device=dev).to(torch.bfloat16)
+            q = torch.randn(C, Hq, hd, device=dev).to(torch.bfloat16)
+            table = torch.arange(n_pages, dtype=torch.int32, device=dev)
+            o = torch.empty_like(q)
+            ws = torch.empty(max(dgp.dg_op_attention_workspace_bytes(P, C, Hq, Hkv, hd), 1),
+                             dtype=torch.uint8, device=dev)
+            sec = timed(lambda: dgp.dg_op_canvas_attention(q, kp, vp, table, P, C, Hq, Hkv, hd, pg,
+                                                           False, o, ws), args.steps)
+            fl = 4.0 * C * Hq * S * hd
+            out.append({"micro": "canvas_attention", "shape": f"P={P} C={C} Hq={Hq} Hkv={Hkv} hd={hd}",
+                        "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12,
+                        "frac_bf16": fl / sec / 1e12 / tf_burst})
+    if which in ("kv_append", "all"):
+        L, n, Hkv, hd, pg = 30, 256, 8, 128, 128
+        n_pages = 32
+        kn = torch.randn(L, n, Hkv, hd, device=dev).to(torch.bfloat16)
+        vn = torch.randn(L, n, Hkv, hd, device=dev).to(torch.bfloat16)
+        kp = torch.zeros(L, n_pages, Hkv, pg, hd, dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros_like(kp)
+        table = torch.arange(n_pages, dtype=torch.int32, device=dev)
+        sec = timed(lambda: dgp.dg_op_kv_append(kn, vn, kp, vp, table, L, n_pages, 2048, n, Hkv, hd, pg),
+                    args.steps)
+        byt = 2 * 2 * L * n * Hkv * hd * 2
+        out.append({"micro": "kv_append", "shape": f"layers={L} tokens={n} Hkv={Hkv} hd={hd}",
+                    "ms": sec * 1e3, "GBps": byt / sec / 1e9, "frac_hbm": byt / sec / 1e9 / hbm})
+    for o in out:
+        o["peak_source"] = src
+        print(json.dumps(o), flush=True)
     return 0
 
 
@@ -359,9 +485,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--micro", default=None,
+                    choices=["moe", "lmhead", "sampler", "attention", "kv_append", "all"],
+                    help="kernel micro-benchmarks at the micro-op shapes instead of the decoder")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if measured for this build")
     args = ap.parse_args()
+    if args.micro:
+        return micro(args)
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

@@ -875,8 +875,8 @@ const char *dg_kernel_class_name(int32_t cls) {
 int dg_profile(dg_model *m, int32_t enable) {
   CKR(check_model(m));
   SYNC(m);
-  m->prof_on = enable != 0;
-  if (m->prof_on) {
+  m->prof_on = enable == 1;
+  if (enable != 0) {
     for (int i = 0; i < DG_K_CLASSES; ++i) {
       m->prof_ms[i] = 0.0;
       m->prof_launches[i] = 0;

@@ -18,28 +18,43 @@ namespace {
 
 // q/k/v projection: RoPE (rotate-half pairs (j, j+hd/2)) on q and k at
 // absolute position pos0 + token; q to [T][Hq*hd]; k and v straight into the
-// paged pool slice of this layer.
+// paged pool slice of this layer.  The tile's tokens' cos/sin rows and page
+// slots are first staged in shared memory, so the element loop only reads
+// shared memory and issues stores.
+template <int BN>
 struct EpiQkv {
-  static constexpr size_t extra_smem = 0;
+  static constexpr int kMaxHalf = 64;
+  static constexpr size_t extra_smem = (size_t)BN * kMaxHalf * 2 * sizeof(float) + BN * sizeof(long long);
   QkvOut o;
-  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
+  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *extra) const {
     const int BM = c.m_valid;
     const int half = o.hd / 2, qdim = o.Hq * o.hd, kdim = o.Hkv * o.hd;
+    float *cs = (float *)extra;                  // [BN][half]
+    float *sn = cs + BN * kMaxHalf;              // [BN][half]
+    long long *slot = (long long *)(sn + BN * kMaxHalf);  // element offset of (page, 0, slot, 0)
+    for (int i = threadIdx.x; i < c.n_valid * half; i += blockDim.x) {
+      const int t = i / half, j = i % half;
+      const size_t p = (size_t)(o.pos0 + c.n0 + t);
+      cs[t * half + j] = o.cos_t[p * half + j];
+      sn[t * half + j] = o.sin_t[p * half + j];
+    }
+    for (int t = threadIdx.x; t < c.n_valid; t += blockDim.x) {
+      const int p = o.pos0 + c.n0 + t;
+      slot[t] = ((long long)o.page_table[p / o.pg] * o.Hkv * o.pg + p % o.pg) * o.hd;
+    }
+    __syncthreads();
+#pragma unroll 4
     for (int idx = threadIdx.x; idx < c.n_valid * BM; idx += blockDim.x) {
       const int t = idx / BM, f = idx % BM;
       const int fg = c.m0 + f;
       const int tok = c.n0 + t;
-      const int p = o.pos0 + tok;
       const int j = fg % o.hd;
       float val;
       if (fg < qdim + kdim) {
         const int jj = j % half;
-        const float cs = o.cos_t[(size_t)p * half + jj], sn = o.sin_t[(size_t)p * half + jj];
-        if (j < half) {
-          val = tile[f * ldc + t] * cs - tile[(f + half) * ldc + t] * sn;
-        } else {
-          val = tile[(f - half) * ldc + t] * sn + tile[f * ldc + t] * cs;
-        }
+        const float cv = cs[t * half + jj], sv = sn[t * half + jj];
+        val = j < half ? tile[f * ldc + t] * cv - tile[(f + half) * ldc + t] * sv
+                       : tile[(f - half) * ldc + t] * sv + tile[f * ldc + t] * cv;
       } else {
         val = tile[f * ldc + t];
       }
@@ -49,23 +64,37 @@ struct EpiQkv {
       } else {
         const bool is_k = fg < qdim + kdim;
         const int head = (fg - (is_k ? qdim : qdim + kdim)) / o.hd;
-        const size_t dst =
-            (((size_t)o.page_table[p / o.pg] * o.Hkv + head) * o.pg + p % o.pg) * o.hd + j;
-        (is_k ? o.k_pool : o.v_pool)[dst] = b;
+        (is_k ? o.k_pool : o.v_pool)[slot[t] + (long long)head * o.pg * o.hd + j] = b;
       }
     }
   }
 };
 
-// h[token][feature] += tile
+// h[token][feature] += tile; eight independent loads in flight per thread.
 struct EpiResidual {
   static constexpr size_t extra_smem = 0;
   float *h;
   int ldh;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    for (int idx = threadIdx.x; idx < c.n_valid * c.m_valid; idx += blockDim.x) {
-      const int t = idx / c.m_valid, f = idx % c.m_valid;
-      h[(size_t)(c.n0 + t) * ldh + c.m0 + f] += tile[f * ldc + t];
+    const int n = c.n_valid * c.m_valid;
+    for (int base = threadIdx.x; base < n; base += 8 * blockDim.x) {
+      float v[8];
+      size_t off[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * blockDim.x;
+        const int t = idx / c.m_valid, f = idx % c.m_valid;
+        off[u] = (size_t)(c.n0 + t) * ldh + c.m0 + f;
+        v[u] = idx < n ? h[off[u]] : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < n) {
+          const int t = idx / c.m_valid, f = idx % c.m_valid;
+          h[off[u]] = v[u] + tile[f * ldc + t];
+        }
+      }
     }
   }
 };
@@ -223,7 +252,8 @@ cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOu
   CUtensorMap ta, tb;
   TMAP(ta, wqkv, M, d, 128);
   TMAP(tb, xn, T, d, 64);
-  EpiQkv epi{o};
+  if (o.hd / 2 > EpiQkv<64>::kMaxHalf) return cudaErrorInvalidValue;
+  EpiQkv<64> epi{o};
   return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(M, T, d, err), epi, ceil_div(T, 64), st);
 }
 

@@ -217,10 +217,12 @@ enum {
 };
 const char *dg_kernel_class_name(int32_t cls);
 
-/* Kernel launches are always counted per class.  With enable != 0 every
- * launch is also bracketed by CUDA events on the model's stream and the
- * elapsed device time is accumulated per class (read back at each
- * synchronising call).  Enabling resets counts and times. */
+/* Kernel launches are always counted per class.  enable = 1: every launch is
+ * also bracketed by CUDA events on the model's stream (event-record nodes
+ * inside captured steps) and the elapsed device time is accumulated per
+ * class (read back at each synchronising call); enable = 2: counting only;
+ * enable = 0: stop timing.  1 and 2 reset all counts, times and the expert
+ * counters of dg_profile_experts. */
 int dg_profile(dg_model *m, int32_t enable);
 /* ms[DG_K_CLASSES] (host, may be NULL): accumulated device milliseconds;
  * launches[DG_K_CLASSES] (host, may be NULL): kernels launched per class. */
