@@ -285,6 +285,244 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Split-K GEMM for the decoder's skinny products (weights x a few hundred
+// tokens).  One CTA owns a 128-row A tile, up to 256 B rows (the MMA N is the
+// tile's valid row count rounded up to 16, so a 40-row expert tile costs a
+// 128 x 48 MMA) and 1/SPLIT of the K range.  N = 256 keeps the tensor core
+// busy per instruction: with N = 64 the single-thread MMA issue and the
+// shared-memory operand traffic, not HBM, bounded the mainloop.
+//
+// The SPLIT CTAs of one output tile form a thread-block cluster (1, 1, SPLIT).
+// Each writes its fp32 partial tile into its own shared memory, slice-major
+// ([SPLIT][128][W + 4], W = 256 / SPLIT columns per slice); after a cluster
+// barrier CTA z sums slice z over the cluster in rank order through
+// distributed shared memory (a fixed order, so results are deterministic) and
+// runs the epilogue on that 128 x W slice.  A second cluster barrier keeps
+// every partial alive until its readers are done.
+// ---------------------------------------------------------------------------
+namespace tc {
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
+                   : "memory");
+}
+
+constexpr int kSkBN = 256;           // B rows per tile (MMA N upper bound)
+constexpr int kSkStages = 4;
+constexpr uint32_t kBChunkBytes = 64 * 128;  // one 64-row B box
+
+template <int SPLIT, class Epi>
+struct SkSmem {
+  static constexpr int W = kSkBN / SPLIT;  // epilogue slice width
+  static constexpr uint32_t stage_bytes = kATileBytes + kSkBN * 128;
+  static constexpr size_t ring = (size_t)kSkStages * stage_bytes;
+  static constexpr int part_ld = W + 4;    // float4 rows, 8 consecutive rows on distinct banks
+  static constexpr size_t part = SPLIT > 1 ? (size_t)SPLIT * 128 * part_ld * 4 : 0;
+  static constexpr int red_ld = W + 1;     // odd: column walks are conflict-free
+  static constexpr size_t red = (size_t)128 * red_ld * 4;
+  static constexpr size_t epi = part + red + Epi::extra_smem;
+  static constexpr size_t bars_off = ((ring > epi ? ring : epi) + 15) & ~(size_t)15;
+  static constexpr size_t bytes = bars_off + (2 * kSkStages + 1) * 8 + 16 + 1024;
+};
+
+}  // namespace tc
+
+template <int SPLIT, class Epi>
+__global__ void __launch_bounds__(128, 1)
+    tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                      TcArgs g, Epi epi) {
+  using S = tc::SkSmem<SPLIT, Epi>;
+  constexpr int STAGES = tc::kSkStages, W = S::W;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = (uint64_t *)(base + S::bars_off);
+  uint64_t *empty = full + STAGES;
+  uint64_t *accb = empty + STAGES;
+  uint32_t *tmem_slot = (uint32_t *)(accb + 1);
+  volatile int *abort = (volatile int *)(tmem_slot + 1);
+
+  // Tile decode; the CTAs of a cluster share blockIdx.x/y and so decide alike.
+  TileCtx ctx;
+  ctx.m0 = blockIdx.x * 128;
+  ctx.group = 0;
+  ctx.b_base = 0;
+  int n_total = g.N;
+  if (g.work) {
+    const int w = blockIdx.y;
+    if (w >= *g.n_work) return;
+    ctx.group = g.work[2 * w];
+    ctx.n0 = g.work[2 * w + 1];
+    ctx.b_base = g.group_offs[ctx.group];
+    n_total = g.group_offs[ctx.group + 1] - ctx.b_base;
+  } else {
+    ctx.n0 = blockIdx.y * tc::kSkBN;
+  }
+  ctx.m_valid = min(128, g.M - ctx.m0);
+  ctx.n_valid = min(tc::kSkBN, n_total - ctx.n0);
+  if (ctx.m_valid <= 0 || ctx.n_valid <= 0) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int z = SPLIT > 1 ? (int)blockIdx.z : 0;
+  const int KT = g.K / tc::kBK;
+  const int kb = (int)((long long)KT * z / SPLIT), ke = (int)((long long)KT * (z + 1) / SPLIT);
+  const int nb = (ctx.n_valid + 63) >> 6;                 // 64-row B boxes per stage
+  const int n_mma = (ctx.n_valid + 15) & ~15;             // MMA N
+  const uint32_t tx_bytes = tc::kATileBytes + (uint32_t)nb * tc::kBChunkBytes;
+
+  if (threadIdx.x == 0) {
+    *abort = (g.err && *(volatile int *)g.err) ? 1 : 0;
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    tc::mbar_init(accb, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     tc::smem_u32(tmem_slot)),
+                 "r"((uint32_t)tc::kSkBN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int a_row = ctx.group * g.a_group_rows + ctx.m0;
+  const int b_row = ctx.b_base + ctx.n0;
+  auto a_tile = [&](int s) { return base + (size_t)s * S::stage_bytes; };
+  auto b_tile = [&](int s) { return base + (size_t)s * S::stage_bytes + tc::kATileBytes; };
+
+  if (warp == 0 && lane == 0) {
+    int issued = 0;
+    for (int kt = kb; kt < ke; ++kt, ++issued) {
+      const int i = kt - kb, s = i % STAGES, r = i / STAGES;
+      if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 1, abort);
+      if (*abort) break;
+      tc::mbar_expect_tx(full + s, tx_bytes);
+      tc::tma_load_2d(a_tile(s), &ta, kt * tc::kBK, a_row, full + s);
+      for (int c = 0; c < nb; ++c)
+        tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, &tb, kt * tc::kBK, b_row + 64 * c, full + s);
+    }
+    if (*abort) {
+      // Drain: wait (bounded) for the last copy issued into each stage.
+      for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i) {
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(full + i % STAGES, (i / STAGES) & 1) &&
+               clock64() - t0 < tc::kWaitCycles) {
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = tc::idesc_bf16(128, n_mma);
+    for (int kt = kb; kt < ke; ++kt) {
+      const int i = kt - kb, s = i % STAGES, r = i / STAGES;
+      tc::mbar_wait(full + s, r & 1, g.err, 2, abort);
+      tc::fence_after();
+      const uint64_t adesc = tc::sw128_desc(tc::smem_u32(a_tile(s)));
+      const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(b_tile(s)));
+#pragma unroll
+      for (int kk = 0; kk < tc::kBK / 16; ++kk)
+        tc::mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (i | kk) ? 1u : 0u);
+      tc::mma_commit(empty + s);
+    }
+    tc::mma_commit(accb);
+  }
+  __syncwarp();
+
+  tc::mbar_wait(accb, 0, g.err, 3, abort);
+  tc::fence_after();
+  const int row = warp * 32 + lane;
+  const int nchunks = (ctx.n_valid + 31) >> 5;  // 32-column TMEM chunks holding valid outputs
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  unsigned char *extra = base + S::part + S::red;
+  if (SPLIT == 1) {
+    float *red = (float *)base;
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      uint32_t v[32];
+      tc::tmem_ld32(trow + 32 * c, v);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) red[row * S::red_ld + 32 * c + j] = __uint_as_float(v[j]);
+    }
+    __syncthreads();
+    epi(red, S::red_ld, ctx, extra);
+  } else {
+    float *part = (float *)base;
+    float *red = (float *)(base + S::part);
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      uint32_t v[32];
+      tc::tmem_ld32(trow + 32 * c, v);
+      tc::tmem_ld_wait();
+      const int sl = (32 * c) / W, o = 32 * c - sl * W;
+      float4 *dst = (float4 *)(part + ((size_t)sl * 128 + row) * S::part_ld + o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    }
+    tc::cluster_sync();
+    TileCtx sub = ctx;
+    sub.n0 = ctx.n0 + z * W;
+    sub.n_valid = min(W, ctx.n_valid - z * W);
+    if (sub.n_valid > 0) {
+      const int q4 = (sub.n_valid + 3) >> 2;
+      const uint32_t mine = tc::smem_u32(part + (size_t)z * 128 * S::part_ld);
+      uint32_t src[SPLIT];
+#pragma unroll
+      for (int j = 0; j < SPLIT; ++j) src[j] = tc::cluster_addr(mine, (uint32_t)j);
+      for (int idx = threadIdx.x; idx < 128 * q4; idx += 128) {
+        const int r = idx / q4, q = idx - r * q4;
+        const uint32_t off = (uint32_t)((r * S::part_ld + 4 * q) * 4);
+        float4 acc = tc::ld_cluster_f4(src[0] + off);
+#pragma unroll
+        for (int j = 1; j < SPLIT; ++j) {
+          const float4 v = tc::ld_cluster_f4(src[j] + off);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        float *d = red + r * S::red_ld + 4 * q;
+        d[0] = acc.x;
+        d[1] = acc.y;
+        d[2] = acc.z;
+        d[3] = acc.w;
+      }
+      __syncthreads();
+      epi(red, S::red_ld, sub, extra);
+    }
+    tc::cluster_sync();
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
+                 "r"((uint32_t)tc::kSkBN));
+  }
+}
+
 // ---- host side ---------------------------------------------------------------
 
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix, box = 64 columns x
@@ -310,6 +548,39 @@ cudaError_t launch_tc(const CUtensorMap &ta, const CUtensorMap &ta2, const CUten
   dim3 grid(ceil_div(g.M, 128), grid_y);
   kern<<<grid, 128, S::bytes, st>>>(ta, ta2, tb, g, epi);
   return cudaGetLastError();
+}
+
+// Split-K launch: grid (ceil(M / 128), grid_y, SPLIT), clusters of (1, 1, SPLIT).
+template <int SPLIT, class Epi>
+cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
+                         const Epi &epi, int grid_y, cudaStream_t st) {
+  using S = tc::SkSmem<SPLIT, Epi>;
+  static_assert(S::bytes <= 232448, "shared memory of the split-K GEMM");
+  auto kern = tc_gemm_sk_kernel<SPLIT, Epi>;
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set |= 1ull << dev;
+  }
+  if (g.K % tc::kBK || g.K / tc::kBK < SPLIT) return cudaErrorInvalidValue;
+  if (grid_y <= 0 || g.M <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ceil_div(g.M, 128), grid_y, SPLIT);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = S::bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = SPLIT;
+  cfg.attrs = attr;
+  cfg.numAttrs = SPLIT > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, g, epi);
 }
 
 }  // namespace dg

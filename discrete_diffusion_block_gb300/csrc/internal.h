@@ -54,7 +54,7 @@ cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, f
                           cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
 cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
                            cudaStream_t st);  // out[T][N] = act . w^T
-constexpr int kExpertTileRows = 64;  // token rows per expert GEMM tile (MMA N)
+constexpr int kExpertTileRows = 256;  // token rows per expert GEMM work item (MMA N <= 256)
 cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, const int *offs,
                                 const int *work, const int *n_work, int max_work, int E, int d,
                                 int F, bf16 *act, int *err, cudaStream_t st);

@@ -18,82 +18,115 @@ namespace {
 
 // q/k/v projection: RoPE (rotate-half pairs (j, j+hd/2)) on q and k at
 // absolute position pos0 + token; q to [T][Hq*hd]; k and v straight into the
-// paged pool slice of this layer.  The tile's tokens' cos/sin rows and page
-// slots are first staged in shared memory, so the element loop only reads
-// shared memory and issues stores.
-template <int BN>
+// paged pool slice of this layer.  The tile holds whole heads (128 rows are
+// one head of 128 or two of 64).  Tokens are taken 64 at a time: their
+// cos/sin rows and page slots are staged in shared memory, then each thread
+// rotates two adjacent pairs (j, j+1) and (j+hd/2, j+1+hd/2) of one token and
+// stores them as bf16x2.
 struct EpiQkv {
-  static constexpr int kMaxHalf = 64;
-  static constexpr size_t extra_smem = (size_t)BN * kMaxHalf * 2 * sizeof(float) + BN * sizeof(long long);
+  static constexpr int kTok = 64, kMaxHalf = 64;
+  static constexpr size_t extra_smem = (size_t)kTok * kMaxHalf * 2 * sizeof(float) + kTok * sizeof(long long);
   QkvOut o;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *extra) const {
-    const int BM = c.m_valid;
-    const int half = o.hd / 2, qdim = o.Hq * o.hd, kdim = o.Hkv * o.hd;
-    float *cs = (float *)extra;                  // [BN][half]
-    float *sn = cs + BN * kMaxHalf;              // [BN][half]
-    long long *slot = (long long *)(sn + BN * kMaxHalf);  // element offset of (page, 0, slot, 0)
-    for (int i = threadIdx.x; i < c.n_valid * half; i += blockDim.x) {
-      const int t = i / half, j = i % half;
-      const size_t p = (size_t)(o.pos0 + c.n0 + t);
-      cs[t * half + j] = o.cos_t[p * half + j];
-      sn[t * half + j] = o.sin_t[p * half + j];
-    }
-    for (int t = threadIdx.x; t < c.n_valid; t += blockDim.x) {
-      const int p = o.pos0 + c.n0 + t;
-      slot[t] = ((long long)o.page_table[p / o.pg] * o.Hkv * o.pg + p % o.pg) * o.hd;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int idx = threadIdx.x; idx < c.n_valid * BM; idx += blockDim.x) {
-      const int t = idx / BM, f = idx % BM;
-      const int fg = c.m0 + f;
-      const int tok = c.n0 + t;
-      const int j = fg % o.hd;
-      float val;
-      if (fg < qdim + kdim) {
-        const int jj = j % half;
-        const float cv = cs[t * half + jj], sv = sn[t * half + jj];
-        val = j < half ? tile[f * ldc + t] * cv - tile[(f + half) * ldc + t] * sv
-                       : tile[(f - half) * ldc + t] * sv + tile[f * ldc + t] * cv;
-      } else {
-        val = tile[f * ldc + t];
+    const int hd = o.hd, half = hd >> 1, qdim = o.Hq * hd, kdim = o.Hkv * hd;
+    const int pairs_log = hd == 128 ? 5 : 4;  // half/2 = 32 or 16 pairs of pairs per head
+    const int units = (c.m_valid / hd) << pairs_log;
+    float *cs = (float *)extra;                           // [kTok][half]
+    float *sn = cs + kTok * kMaxHalf;                     // [kTok][half]
+    long long *slot = (long long *)(sn + kTok * kMaxHalf);  // element offset of (page, 0, slot, 0)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t0 = 0; t0 < c.n_valid; t0 += kTok) {
+      const int nt = min(kTok, c.n_valid - t0);
+      __syncthreads();
+      {  // all of this chunk's cos/sin loads in flight at once (blockDim.x == 128)
+        const int q4 = half >> 2, n4 = nt * q4;
+        float4 rc[8], rs[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = threadIdx.x + 128 * u;
+          if (i < n4) {
+            const int t = i / q4, j4 = i - t * q4;
+            const size_t p = (size_t)(o.pos0 + c.n0 + t0 + t);
+            rc[u] = ((const float4 *)(o.cos_t + p * half))[j4];
+            rs[u] = ((const float4 *)(o.sin_t + p * half))[j4];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = threadIdx.x + 128 * u;
+          if (i < n4) {
+            const int t = i / q4, j4 = i - t * q4;
+            ((float4 *)(cs + t * half))[j4] = rc[u];
+            ((float4 *)(sn + t * half))[j4] = rs[u];
+          }
+        }
       }
-      const bf16 b = __float2bfloat16_rn(val);
-      if (fg < qdim) {
-        o.q[(size_t)tok * qdim + fg] = b;
-      } else {
-        const bool is_k = fg < qdim + kdim;
-        const int head = (fg - (is_k ? qdim : qdim + kdim)) / o.hd;
-        (is_k ? o.k_pool : o.v_pool)[slot[t] + (long long)head * o.pg * o.hd + j] = b;
+      for (int t = threadIdx.x; t < nt; t += blockDim.x) {
+        const int p = o.pos0 + c.n0 + t0 + t;
+        slot[t] = ((long long)o.page_table[p / o.pg] * o.Hkv * o.pg + p % o.pg) * hd;
+      }
+      __syncthreads();
+      for (int t = warp; t < nt; t += blockDim.x >> 5) {
+        const int tt = t0 + t, tok = c.n0 + tt;
+        for (int u = lane; u < units; u += 32) {
+          const int hh = u >> pairs_log, j = 2 * (u & ((1 << pairs_log) - 1));
+          const int f = hh * hd + j, fg = c.m0 + f;
+          const float a0 = tile[f * ldc + tt], a1 = tile[(f + 1) * ldc + tt];
+          const float b0 = tile[(f + half) * ldc + tt], b1 = tile[(f + half + 1) * ldc + tt];
+          float lo0 = a0, lo1 = a1, hi0 = b0, hi1 = b1;
+          if (fg < qdim + kdim) {
+            const float c0 = cs[t * half + j], c1 = cs[t * half + j + 1];
+            const float s0 = sn[t * half + j], s1 = sn[t * half + j + 1];
+            lo0 = a0 * c0 - b0 * s0;
+            lo1 = a1 * c1 - b1 * s1;
+            hi0 = b0 * c0 + a0 * s0;
+            hi1 = b1 * c1 + a1 * s1;
+          }
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(lo0, lo1), hi = __floats2bfloat162_rn(hi0, hi1);
+          const int fh = fg - j;  // first feature of the head
+          bf16 *dst;
+          if (fh < qdim) {
+            dst = o.q + (size_t)tok * qdim + fh;
+          } else {
+            const bool is_k = fh < qdim + kdim;
+            const int head = (fh - (is_k ? qdim : qdim + kdim)) / hd;
+            dst = (is_k ? o.k_pool : o.v_pool) + slot[t] + (long long)head * o.pg * hd;
+          }
+          *(__nv_bfloat162 *)(dst + j) = lo;
+          *(__nv_bfloat162 *)(dst + j + half) = hi;
+        }
       }
     }
   }
 };
 
-// h[token][feature] += tile; eight independent loads in flight per thread.
+// h[token][feature] += tile; lanes walk features (coalesced).  A warp takes
+// 16 of its tokens x 4 feature groups of 32 at a time and issues all 64
+// loads before any store.
 struct EpiResidual {
   static constexpr size_t extra_smem = 0;
   float *h;
   int ldh;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    const int n = c.n_valid * c.m_valid;
-    for (int base = threadIdx.x; base < n; base += 8 * blockDim.x) {
-      float v[8];
-      size_t off[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int f0 = 0; f0 < c.m_valid; f0 += 128) {
+      for (int tb = warp; tb < c.n_valid; tb += 16 * nw) {
+        float v[4][16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * blockDim.x;
-        const int t = idx / c.m_valid, f = idx % c.m_valid;
-        off[u] = (size_t)(c.n0 + t) * ldh + c.m0 + f;
-        v[u] = idx < n ? h[off[u]] : 0.0f;
-      }
+        for (int g = 0; g < 4; ++g)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * blockDim.x;
-        if (idx < n) {
-          const int t = idx / c.m_valid, f = idx % c.m_valid;
-          h[off[u]] = v[u] + tile[f * ldc + t];
-        }
+          for (int u = 0; u < 16; ++u) {
+            const int t = tb + u * nw, f = f0 + 32 * g + lane;
+            v[g][u] = (f < c.m_valid && t < c.n_valid) ? h[(size_t)(c.n0 + t) * ldh + c.m0 + f] : 0.0f;
+          }
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int t = tb + u * nw, f = f0 + 32 * g + lane;
+            if (f < c.m_valid && t < c.n_valid)
+              h[(size_t)(c.n0 + t) * ldh + c.m0 + f] = v[g][u] + tile[f * ldc + t];
+          }
       }
     }
   }
@@ -105,24 +138,29 @@ struct EpiStore {
   float *out;
   int ldo;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    for (int idx = threadIdx.x; idx < c.n_valid * c.m_valid; idx += blockDim.x) {
-      const int t = idx / c.m_valid, f = idx % c.m_valid;
-      out[(size_t)(c.b_base + c.n0 + t) * ldo + c.m0 + f] = tile[f * ldc + t];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < c.n_valid; t += blockDim.x >> 5) {
+      float *orow = out + (size_t)(c.b_base + c.n0 + t) * ldo + c.m0;
+      for (int f = lane; f < c.m_valid; f += 32) orow[f] = tile[f * ldc + t];
     }
   }
 };
 
-// SwiGLU on a 128-row tile holding 64 gate rows then the matching 64 up rows.
+// SwiGLU on a 128-row tile holding 64 gate rows then the matching 64 up rows;
+// each lane writes two adjacent outputs as bf16x2.
 struct EpiSwiGlu {
   static constexpr size_t extra_smem = 0;
   bf16 *act;
   int F;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
     const int fb = c.m0 / 128;
-    for (int idx = threadIdx.x; idx < c.n_valid * 64; idx += blockDim.x) {
-      const int t = idx / 64, j = idx % 64;
-      const float g = tile[j * ldc + t], u = tile[(64 + j) * ldc + t];
-      act[(size_t)(c.b_base + c.n0 + t) * F + fb * 64 + j] = __float2bfloat16_rn(silu_f(g) * u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = 2 * lane;
+    for (int t = warp; t < c.n_valid; t += blockDim.x >> 5) {
+      const float g0 = tile[j * ldc + t], g1 = tile[(j + 1) * ldc + t];
+      const float u0 = tile[(64 + j) * ldc + t], u1 = tile[(65 + j) * ldc + t];
+      *(__nv_bfloat162 *)(act + (size_t)(c.b_base + c.n0 + t) * F + fb * 64 + j) =
+          __floats2bfloat162_rn(silu_f(g0) * u0, silu_f(g1) * u1);
     }
   }
 };
@@ -252,9 +290,31 @@ cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOu
   CUtensorMap ta, tb;
   TMAP(ta, wqkv, M, d, 128);
   TMAP(tb, xn, T, d, 64);
-  if (o.hd / 2 > EpiQkv<64>::kMaxHalf) return cudaErrorInvalidValue;
-  EpiQkv<64> epi{o};
-  return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(M, T, d, err), epi, ceil_div(T, 64), st);
+  if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd) return cudaErrorInvalidValue;
+  EpiQkv epi{o};
+  const TcArgs g = targs(M, T, d, err);
+  const int gy = ceil_div(T, tc::kSkBN), kt = d / tc::kBK;
+  if (kt >= 4) return launch_tc_sk<4>(ta, tb, g, epi, gy, st);
+  return launch_tc_sk<1>(ta, tb, g, epi, gy, st);
+}
+
+// Split choice for a plain projection: the largest of 8, 4, 2, 1 that keeps at
+// least two K tiles per split and at most ~one wave of CTAs.
+static int pick_split(int m_tiles, int n_tiles, int kt) {
+  int s = 8;
+  while (s > 1 && (kt < 2 * s || m_tiles * n_tiles * s > 160)) s >>= 1;
+  return s;
+}
+
+template <class Epi>
+static cudaError_t launch_split(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
+                                const Epi &epi, int grid_y, int split, cudaStream_t st) {
+  switch (split) {
+    case 8: return launch_tc_sk<8>(ta, tb, g, epi, grid_y, st);
+    case 4: return launch_tc_sk<4>(ta, tb, g, epi, grid_y, st);
+    case 2: return launch_tc_sk<2>(ta, tb, g, epi, grid_y, st);
+    default: return launch_tc_sk<1>(ta, tb, g, epi, grid_y, st);
+  }
 }
 
 cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
@@ -263,7 +323,8 @@ cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, f
   TMAP(ta, w, N, K, 128);
   TMAP(tb, act, T, K, 64);
   EpiResidual epi{h, N};
-  return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(N, T, K, err), epi, ceil_div(T, 64), st);
+  const int gy = ceil_div(T, tc::kSkBN);
+  return launch_split(ta, tb, targs(N, T, K, err), epi, gy, pick_split(ceil_div(N, 128), gy, K / tc::kBK), st);
 }
 
 cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
@@ -272,24 +333,26 @@ cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, 
   TMAP(ta, w, N, K, 128);
   TMAP(tb, act, T, K, 64);
   EpiStore epi{out, N};
-  return launch_tc<64, 4, 1, 128>(ta, ta, tb, targs(N, T, K, err), epi, ceil_div(T, 64), st);
+  const int gy = ceil_div(T, tc::kSkBN);
+  return launch_split(ta, tb, targs(N, T, K, err), epi, gy, pick_split(ceil_div(N, 128), gy, K / tc::kBK), st);
 }
 
 // Experts: A = the expert's weight rows (2-D view over all experts), B = the
-// expert's routed rows, packed contiguously in expert order.
+// expert's routed rows, packed contiguously in expert order, up to
+// kExpertTileRows per work item.
 cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, const int *offs,
                                 const int *work, const int *n_work, int max_work, int E, int d,
                                 int F, bf16 *act, int *err, cudaStream_t st) {
   CUtensorMap ta, tb;
   TMAP(ta, wgu, (uint64_t)E * 2 * F, d, 128);
-  TMAP(tb, x_perm, rows, d, kExpertTileRows);
+  TMAP(tb, x_perm, rows, d, 64);
   TcArgs g = targs(2 * F, 0, d, err);
   g.a_group_rows = 2 * F;
   g.work = work;
   g.n_work = n_work;
   g.group_offs = offs;
   EpiSwiGlu epi{act, F};
-  return launch_tc<kExpertTileRows, 4, 1, 128>(ta, ta, tb, g, epi, max_work, st);
+  return launch_split(ta, tb, g, epi, max_work, d / tc::kBK >= 8 ? 2 : 1, st);
 }
 
 cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const int *offs,
@@ -297,14 +360,14 @@ cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const in
                              float *y, int *err, cudaStream_t st) {
   CUtensorMap ta, tb;
   TMAP(ta, wd, (uint64_t)E * d, F, 128);
-  TMAP(tb, act, rows, F, kExpertTileRows);
+  TMAP(tb, act, rows, F, 64);
   TcArgs g = targs(d, 0, F, err);
   g.a_group_rows = d;
   g.work = work;
   g.n_work = n_work;
   g.group_offs = offs;
   EpiStore epi{y, d};
-  return launch_tc<kExpertTileRows, 4, 1, 128>(ta, ta, tb, g, epi, max_work, st);
+  return launch_split(ta, tb, g, epi, max_work, 1, st);
 }
 
 // LM head: A = normalised token rows (hi, and lo of a hi/lo split), B = the

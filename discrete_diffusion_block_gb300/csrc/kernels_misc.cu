@@ -93,30 +93,56 @@ __global__ void embed_kernel(float *h, const bf16 *table, const int *ids, int d)
 
 // y = x / sqrt(mean(x^2) + eps) * g, fp32 statistics, bf16 output; with
 // out_lo the residual y - bf16(y) is stored too (hi + lo carries y to ~16 bits).
-__global__ void __launch_bounds__(256) rmsnorm_kernel(bf16 *out, bf16 *out_lo, const float *h,
-                                                      const float *g, int d, float eps) {
-  const int t = blockIdx.x;
-  const float *x = h + (size_t)t * d;
+// One 128-thread block per row; the row is read once as float4 into
+// registers (d <= 4096; longer rows are read twice).
+constexpr int kNormThreads = 128, kNormVec = 8;
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *out_lo, const float *h,
+                                                               const float *g, int d, float eps) {
+  const int t = blockIdx.x, d4 = d >> 2;
+  const float4 *x = (const float4 *)(h + (size_t)t * d);
+  const float4 *g4 = (const float4 *)g;
+  float4 v[kNormVec];
   float ss = 0.0f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) ss += x[c] * x[c];
-  __shared__ float red[8];
+#pragma unroll
+  for (int u = 0; u < kNormVec; ++u) {
+    const int c = threadIdx.x + u * kNormThreads;
+    v[u] = c < d4 ? x[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int u = 0; u < kNormVec; ++u) ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+  for (int c = threadIdx.x + kNormVec * kNormThreads; c < d4; c += kNormThreads) {
+    const float4 a = x[c];
+    ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+  }
+  __shared__ float red[kNormThreads / 32];
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+  float tot = 0.0f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float inv = rsqrtf(red[0] / d + eps);
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    const float y = x[c] * inv * g[c];
-    const bf16 hi = __float2bfloat16_rn(y);
-    out[(size_t)t * d + c] = hi;
-    if (out_lo) out_lo[(size_t)t * d + c] = __float2bfloat16_rn(y - __bfloat162float(hi));
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / d + eps);
+  __nv_bfloat162 *o2 = (__nv_bfloat162 *)(out + (size_t)t * d);
+  __nv_bfloat162 *l2 = out_lo ? (__nv_bfloat162 *)(out_lo + (size_t)t * d) : nullptr;
+  for (int c = threadIdx.x, u = 0; c < d4; c += kNormThreads, ++u) {
+    float4 a;
+    if (u < kNormVec) {
+#pragma unroll
+      for (int q = 0; q < kNormVec; ++q)
+        if (q == u) a = v[q];
+    } else {
+      a = x[c];
+    }
+    const float4 gg = g4[c];
+    const float y0 = a.x * inv * gg.x, y1 = a.y * inv * gg.y, y2 = a.z * inv * gg.z, y3 = a.w * inv * gg.w;
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
+    o2[2 * c] = h01;
+    o2[2 * c + 1] = h23;
+    if (l2) {
+      l2[2 * c] = __floats2bfloat162_rn(y0 - __low2float(h01), y1 - __high2float(h01));
+      l2[2 * c + 1] = __floats2bfloat162_rn(y2 - __low2float(h23), y3 - __high2float(h23));
+    }
   }
 }
 
@@ -171,51 +197,101 @@ __global__ void topk_kernel(const float *logits, int T, int E, int k, int *ids, 
 }
 
 // Stable counting sort of the T*k (token, slot) pairs by expert, done by one
-// block: warp w owns experts w, w+32, ...; ranks inside an expert follow the
-// pair index (ballot prefix counts), so the order is deterministic.
-constexpr int kPermThreads = 1024;
+// block.  Warp w owns the contiguous pair segment w of 32; it counts its
+// segment per expert (__match_any_sync groups lanes holding the same expert),
+// a per-expert prefix over the segments turns the counts into starting ranks,
+// and a second walk of the segment hands out ranks in pair order, so the
+// order inside an expert is the pair order and the result is deterministic.
+constexpr int kPermThreads = 1024, kPermWarps = kPermThreads / 32;
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, int TK, int k, int E,
                                                                int tile_rows, int *offs,
                                                                int *perm_tok, int *slot_row,
-                                                               int *work, int *n_work, int *rank,
+                                                               int *work, int *n_work,
                                                                unsigned long long *stats) {
-  __shared__ int cnt[257], toff[257], soff[257];
+  __shared__ int seg[kPermWarps][257];  // per-segment counts, then running ranks
+  __shared__ int cnt[257], soff[257], toff[257];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e = warp; e < E; e += kPermThreads / 32) {
-    int c = 0;
-    for (int base = 0; base < TK; base += 32) {
-      const int i = base + lane;
-      const bool hit = i < TK && ids[i] == e;
-      const unsigned b = __ballot_sync(0xffffffffu, hit);
-      if (hit) rank[i] = c + __popc(b & ((1u << lane) - 1u));
-      c += __popc(b);
-    }
-    if (lane == 0) cnt[e] = c;
+  for (int i = threadIdx.x; i < kPermWarps * 257; i += kPermThreads) (&seg[0][0])[i] = 0;
+  __syncthreads();
+  const int per = (TK + kPermWarps - 1) / kPermWarps;
+  const int s0 = min(TK, warp * per), s1 = min(TK, s0 + per);
+  for (int base = s0; base < s1; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < s1;
+    const int id = valid ? ids[i] : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, id);
+    if (valid && lane == __ffs(m) - 1) seg[warp][id] += __popc(m);
+    __syncwarp();
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, w = 0;
-    for (int e = 0; e < E; ++e) {
-      offs[e] = o;
-      soff[e] = o;
-      toff[e] = w;
-      o += cnt[e];
-      w += (cnt[e] + tile_rows - 1) / tile_rows;
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {
+    int run = 0;
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = seg[w][e];
+      seg[w][e] = run;
+      run += c;
     }
-    offs[E] = o;
-    *n_work = w;
-    if (stats) {  // experts whose weights this launch's expert GEMMs stream, and their rows
-      unsigned long long touched = 0;
-      for (int e = 0; e < E; ++e) touched += cnt[e] > 0;
-      atomicAdd(&stats[0], touched);
+    cnt[e] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {  // expert and work-tile offsets: lane j scans experts 8j .. 8j+7
+    int c_sum = 0, w_sum = 0, touched = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      if (e < E) {
+        c_sum += cnt[e];
+        w_sum += (cnt[e] + tile_rows - 1) / tile_rows;
+        touched += cnt[e] > 0;
+      }
+    }
+    int c_ex = c_sum, w_ex = w_sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, c_ex, off), b = __shfl_up_sync(0xffffffffu, w_ex, off);
+      if (lane >= off) {
+        c_ex += a;
+        w_ex += b;
+      }
+    }
+    c_ex -= c_sum;
+    w_ex -= w_sum;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      if (e < E) {
+        soff[e] = c_ex;
+        offs[e] = c_ex;
+        toff[e] = w_ex;
+        c_ex += cnt[e];
+        w_ex += (cnt[e] + tile_rows - 1) / tile_rows;
+      }
+    }
+    if (lane == 31) {
+      offs[E] = c_ex;
+      *n_work = w_ex;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) touched += __shfl_xor_sync(0xffffffffu, touched, off);
+    if (stats && lane == 0) {  // experts whose weights this launch's expert GEMMs stream, and their rows
+      atomicAdd(&stats[0], (unsigned long long)touched);
       atomicAdd(&stats[1], (unsigned long long)TK);
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < TK; i += kPermThreads) {
-    const int row = soff[ids[i]] + rank[i];
-    perm_tok[row] = i / k;
-    slot_row[i] = row;
+  for (int base = s0; base < s1; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < s1;
+    const int id = valid ? ids[i] : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, id);
+    if (valid) {
+      const int row = soff[id] + seg[warp][id] + __popc(m & ((1u << lane) - 1u));
+      perm_tok[row] = i / k;
+      slot_row[i] = row;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(m) - 1) seg[warp][id] += __popc(m);
+    __syncwarp();
   }
   for (int e = threadIdx.x; e < E; e += kPermThreads) {
     const int nt = (cnt[e] + tile_rows - 1) / tile_rows;
@@ -227,15 +303,35 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, i
 }
 
 // h[t] (+)= sum_s gate[t][s] * y[slot_row[t*k+s]], slots in ascending order.
-__global__ void combine_kernel(float *h, const float *y, const float *gates, const int *slot_row,
-                               int k, int d, int accumulate) {
+// The token's gates and rows are staged first; each thread then has all k
+// row loads of its float4 column in flight at once.
+__global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y, const float *gates,
+                                                      const int *slot_row, int k, int d4,
+                                                      int accumulate) {
   const int t = blockIdx.x;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float acc = accumulate ? h[(size_t)t * d + c] : 0.0f;
-    float mo = 0.0f;
-    for (int s = 0; s < k; ++s)
-      mo += gates[(size_t)t * k + s] * y[(size_t)slot_row[(size_t)t * k + s] * d + c];
-    h[(size_t)t * d + c] = acc + mo;
+  __shared__ float g_s[16];
+  __shared__ int r_s[16];
+  if (threadIdx.x < k) {
+    g_s[threadIdx.x] = gates[(size_t)t * k + threadIdx.x];
+    r_s[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+    float4 v[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < k) v[s] = y[(size_t)r_s[s] * d4 + c];
+    float4 acc = accumulate ? h[(size_t)t * d4 + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 mo = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < k) {
+        mo.x += g_s[s] * v[s].x;
+        mo.y += g_s[s] * v[s].y;
+        mo.z += g_s[s] * v[s].z;
+        mo.w += g_s[s] * v[s].w;
+      }
+    h[(size_t)t * d4 + c] = make_float4(acc.x + mo.x, acc.y + mo.y, acc.z + mo.z, acc.w + mo.w);
   }
 }
 
@@ -329,7 +425,8 @@ cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
                          cudaStream_t st, bf16 *out_lo) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<<<T, 256, 0, st>>>(out, out_lo, h, gain, d, eps);
+  if (d % 4) return cudaErrorInvalidValue;
+  rmsnorm_kernel<<<T, kNormThreads, 0, st>>>(out, out_lo, h, gain, d, eps);
   return cudaGetLastError();
 }
 
@@ -348,16 +445,17 @@ cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int 
                         int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st,
                         unsigned long long *stats) {
   if (E > 256) return cudaErrorInvalidValue;
-  int *rank = work + 2 * moe_max_work(T, k, E, tile_rows);
   permute_kernel<<<1, kPermThreads, 0, st>>>(ids, T * k, k, E, tile_rows, offs, perm_tok, slot_row,
-                                             work, n_work, rank, stats);
+                                             work, n_work, stats);
   return cudaGetLastError();
 }
 
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 256, 0, st>>>(h, y, gates, slot_row, k, d, accumulate ? 1 : 0);
+  if (k > 16 || d % 4) return cudaErrorInvalidValue;
+  combine_kernel<<<T, 256, 0, st>>>((float4 *)h, (const float4 *)y, gates, slot_row, k, d / 4,
+                                    accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 
