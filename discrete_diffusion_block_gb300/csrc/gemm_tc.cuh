@@ -87,6 +87,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// L2 prefetch of one A box: raises the DRAM requests in flight beyond what
+// the shared-memory ring holds.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"((uint64_t)map),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -174,6 +182,8 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t *tmem_slot = (uint32_t *)(accb + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
+  pdl_wait();
+  pdl_trigger();
   TileCtx ctx;
   ctx.m0 = blockIdx.x * 128;
   ctx.group = 0;
@@ -325,6 +335,7 @@ __device__ __forceinline__ void cluster_sync() {
 
 constexpr int kSkBN = 256;           // B rows per tile (MMA N upper bound)
 constexpr int kSkStages = 4;
+constexpr int kSkPrefetch = 12;      // A boxes kept in flight to L2 ahead of the ring
 constexpr uint32_t kBChunkBytes = 64 * 128;  // one 64-row B box
 
 template <int SPLIT, class Epi>
@@ -357,36 +368,27 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t *tmem_slot = (uint32_t *)(accb + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
-  // Tile decode; the CTAs of a cluster share blockIdx.x/y and so decide alike.
-  TileCtx ctx;
-  ctx.m0 = blockIdx.x * 128;
-  ctx.group = 0;
-  ctx.b_base = 0;
-  int n_total = g.N;
-  if (g.work) {
-    const int w = blockIdx.y;
-    if (w >= *g.n_work) return;
-    ctx.group = g.work[2 * w];
-    ctx.n0 = g.work[2 * w + 1];
-    ctx.b_base = g.group_offs[ctx.group];
-    n_total = g.group_offs[ctx.group + 1] - ctx.b_base;
+  // Grouped launches loop over the device work list (items y, y + gridDim.y,
+  // ...), so the grid is sized to the machine, not to the worst-case list;
+  // plain launches have one n-tile per blockIdx.y.  The CTAs of a cluster
+  // share blockIdx.x/y and so walk the same items.
+  int n_items;
+  if (g.work) {  // the work list is an earlier kernel's output
+    pdl_wait();
+    pdl_trigger();
+    n_items = *g.n_work;
   } else {
-    ctx.n0 = blockIdx.y * tc::kSkBN;
+    n_items = ceil_div(g.N, tc::kSkBN);
   }
-  ctx.m_valid = min(128, g.M - ctx.m0);
-  ctx.n_valid = min(tc::kSkBN, n_total - ctx.n0);
-  if (ctx.m_valid <= 0 || ctx.n_valid <= 0) return;
+  if ((int)blockIdx.y >= n_items) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int z = SPLIT > 1 ? (int)blockIdx.z : 0;
   const int KT = g.K / tc::kBK;
   const int kb = (int)((long long)KT * z / SPLIT), ke = (int)((long long)KT * (z + 1) / SPLIT);
-  const int nb = (ctx.n_valid + 63) >> 6;                 // 64-row B boxes per stage
-  const int n_mma = (ctx.n_valid + 15) & ~15;             // MMA N
-  const uint32_t tx_bytes = tc::kATileBytes + (uint32_t)nb * tc::kBChunkBytes;
 
   if (threadIdx.x == 0) {
-    *abort = (g.err && *(volatile int *)g.err) ? 1 : 0;
+    *abort = 0;
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full + s, 1);
       tc::mbar_init(empty + s, 1);
@@ -405,119 +407,188 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  const int a_row = ctx.group * g.a_group_rows + ctx.m0;
-  const int b_row = ctx.b_base + ctx.n0;
   auto a_tile = [&](int s) { return base + (size_t)s * S::stage_bytes; };
   auto b_tile = [&](int s) { return base + (size_t)s * S::stage_bytes + tc::kATileBytes; };
 
-  if (warp == 0 && lane == 0) {
-    int issued = 0;
-    for (int kt = kb; kt < ke; ++kt, ++issued) {
-      const int i = kt - kb, s = i % STAGES, r = i / STAGES;
-      if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 1, abort);
-      if (*abort) break;
-      tc::mbar_expect_tx(full + s, tx_bytes);
-      tc::tma_load_2d(a_tile(s), &ta, kt * tc::kBK, a_row, full + s);
-      for (int c = 0; c < nb; ++c)
-        tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, &tb, kt * tc::kBK, b_row + 64 * c, full + s);
-    }
-    if (*abort) {
-      // Drain: wait (bounded) for the last copy issued into each stage.
-      for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i) {
-        const long long t0 = clock64();
-        while (!tc::mbar_try_wait(full + i % STAGES, (i / STAGES) & 1) &&
-               clock64() - t0 < tc::kWaitCycles) {
-        }
+  // Weights never change: a plain launch starts streaming its first item's A
+  // boxes before waiting for the kernel that produced B.
+  int pre = 0;
+  if (!g.work) {
+    pre = min(STAGES, ke - kb);
+    if (warp == 0 && lane == 0) {
+      const int nv = min(tc::kSkBN, g.N - (int)blockIdx.y * tc::kSkBN);
+      const uint32_t tx0 = tc::kATileBytes + (uint32_t)((nv + 63) >> 6) * tc::kBChunkBytes;
+      for (int i = 0; i < pre; ++i) {
+        tc::mbar_expect_tx(full + i, tx0);
+        tc::tma_load_2d(a_tile(i), &ta, (kb + i) * tc::kBK, blockIdx.x * 128, full + i);
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = tc::idesc_bf16(128, n_mma);
-    for (int kt = kb; kt < ke; ++kt) {
-      const int i = kt - kb, s = i % STAGES, r = i / STAGES;
-      tc::mbar_wait(full + s, r & 1, g.err, 2, abort);
-      tc::fence_after();
-      const uint64_t adesc = tc::sw128_desc(tc::smem_u32(a_tile(s)));
-      const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(b_tile(s)));
-#pragma unroll
-      for (int kk = 0; kk < tc::kBK / 16; ++kk)
-        tc::mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (i | kk) ? 1u : 0u);
-      tc::mma_commit(empty + s);
-    }
-    tc::mma_commit(accb);
+    pdl_wait();
+    pdl_trigger();
   }
-  __syncwarp();
+  if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;  // an earlier timeout: do not wait again
 
-  tc::mbar_wait(accb, 0, g.err, 3, abort);
-  tc::fence_after();
-  const int row = warp * 32 + lane;
-  const int nchunks = (ctx.n_valid + 31) >> 5;  // 32-column TMEM chunks holding valid outputs
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  unsigned char *extra = base + S::part + S::red;
-  if (SPLIT == 1) {
-    float *red = (float *)base;
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      uint32_t v[32];
-      tc::tmem_ld32(trow + 32 * c, v);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) red[row * S::red_ld + 32 * c + j] = __uint_as_float(v[j]);
+  int it = 0;     // ring position: k-tiles issued (producer) / consumed (MMA) so far
+  int tiles = 0;  // accumulator phase
+  for (int y = blockIdx.y; y < n_items; y += gridDim.y, ++tiles) {
+    TileCtx ctx;
+    ctx.m0 = blockIdx.x * 128;
+    ctx.group = 0;
+    ctx.b_base = 0;
+    int n_total = g.N;
+    if (g.work) {
+      ctx.group = g.work[2 * y];
+      ctx.n0 = g.work[2 * y + 1];
+      ctx.b_base = g.group_offs[ctx.group];
+      n_total = g.group_offs[ctx.group + 1] - ctx.b_base;
+    } else {
+      ctx.n0 = y * tc::kSkBN;
     }
-    __syncthreads();
-    epi(red, S::red_ld, ctx, extra);
-  } else {
-    float *part = (float *)base;
-    float *red = (float *)(base + S::part);
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      uint32_t v[32];
-      tc::tmem_ld32(trow + 32 * c, v);
-      tc::tmem_ld_wait();
-      const int sl = (32 * c) / W, o = 32 * c - sl * W;
-      float4 *dst = (float4 *)(part + ((size_t)sl * 128 + row) * S::part_ld + o);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-    }
-    tc::cluster_sync();
-    TileCtx sub = ctx;
-    sub.n0 = ctx.n0 + z * W;
-    sub.n_valid = min(W, ctx.n_valid - z * W);
-    if (sub.n_valid > 0) {
-      const int q4 = (sub.n_valid + 3) >> 2;
-      const uint32_t mine = tc::smem_u32(part + (size_t)z * 128 * S::part_ld);
-      uint32_t src[SPLIT];
-#pragma unroll
-      for (int j = 0; j < SPLIT; ++j) src[j] = tc::cluster_addr(mine, (uint32_t)j);
-      for (int idx = threadIdx.x; idx < 128 * q4; idx += 128) {
-        const int r = idx / q4, q = idx - r * q4;
-        const uint32_t off = (uint32_t)((r * S::part_ld + 4 * q) * 4);
-        float4 acc = tc::ld_cluster_f4(src[0] + off);
-#pragma unroll
-        for (int j = 1; j < SPLIT; ++j) {
-          const float4 v = tc::ld_cluster_f4(src[j] + off);
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
+    ctx.m_valid = min(128, g.M - ctx.m0);
+    ctx.n_valid = max(0, min(tc::kSkBN, n_total - ctx.n0));
+    const int nb = max(1, (ctx.n_valid + 63) >> 6);     // 64-row B boxes per stage
+    const int n_mma = max(16, (ctx.n_valid + 15) & ~15);  // MMA N
+    const uint32_t tx_bytes = tc::kATileBytes + (uint32_t)nb * tc::kBChunkBytes;
+    const int a_row = ctx.group * g.a_group_rows + ctx.m0;
+    const int b_row = ctx.b_base + ctx.n0;
+
+    if (warp == 0 && lane == 0) {
+      int issued = it;
+      if (y == (int)blockIdx.y)  // first item: nothing was prefetched for it yet
+        for (int kt = kb + STAGES; kt < min(ke, kb + tc::kSkPrefetch); ++kt)
+          tc::tma_prefetch_2d(&ta, kt * tc::kBK, a_row);
+      for (int kt = kb; kt < ke; ++kt, ++issued) {
+        if (kt + tc::kSkPrefetch < ke) tc::tma_prefetch_2d(&ta, (kt + tc::kSkPrefetch) * tc::kBK, a_row);
+        const int s = issued % STAGES, r = issued / STAGES;
+        if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 1, abort);
+        if (*abort) break;
+        if (issued >= pre) {  // else this stage's A box is already on its way
+          tc::mbar_expect_tx(full + s, tx_bytes);
+          tc::tma_load_2d(a_tile(s), &ta, kt * tc::kBK, a_row, full + s);
         }
-        float *d = red + r * S::red_ld + 4 * q;
-        d[0] = acc.x;
-        d[1] = acc.y;
-        d[2] = acc.z;
-        d[3] = acc.w;
+        for (int c = 0; c < nb; ++c)
+          tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, &tb, kt * tc::kBK, b_row + 64 * c, full + s);
+      }
+      if (g.work && y + (int)gridDim.y < n_items && !*abort) {
+        // The next item's first A boxes go to L2 while this item finishes.
+        const int ny = y + gridDim.y;
+        const int na_row = g.work[2 * ny] * g.a_group_rows + ctx.m0;
+        for (int kt = kb; kt < min(ke, kb + tc::kSkPrefetch); ++kt) tc::tma_prefetch_2d(&ta, kt * tc::kBK, na_row);
+      }
+      if (*abort) {
+        // Drain: wait (bounded) for the last copy issued into each stage.
+        for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(full + i % STAGES, (i / STAGES) & 1) &&
+                 clock64() - t0 < tc::kWaitCycles) {
+          }
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(128, n_mma);
+      for (int kt = kb; kt < ke; ++kt) {
+        const int i = it + kt - kb, s = i % STAGES, r = i / STAGES;
+        tc::mbar_wait(full + s, r & 1, g.err, 2, abort);
+        tc::fence_after();
+        const uint64_t adesc = tc::sw128_desc(tc::smem_u32(a_tile(s)));
+        const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(b_tile(s)));
+#pragma unroll
+        for (int kk = 0; kk < tc::kBK / 16; ++kk)
+          tc::mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kt > kb || kk) ? 1u : 0u);
+        tc::mma_commit(empty + s);
+      }
+      tc::mma_commit(accb);
+    }
+    it += ke - kb;
+    __syncwarp();
+
+    tc::mbar_wait(accb, tiles & 1, g.err, 3, abort);
+    tc::fence_after();
+    const int row = warp * 32 + lane;
+    const int nchunks = (ctx.n_valid + 31) >> 5;  // 32-column TMEM chunks holding valid outputs
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    unsigned char *extra = base + S::part + S::red;
+    if (SPLIT == 1) {
+      float *red = (float *)base;
+#pragma unroll 1
+      for (int c = 0; c < nchunks; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(trow + 32 * c, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) red[row * S::red_ld + 32 * c + j] = __uint_as_float(v[j]);
       }
       __syncthreads();
-      epi(red, S::red_ld, sub, extra);
+      if (ctx.n_valid > 0) epi(red, S::red_ld, ctx, extra);
+    } else {
+      float *part = (float *)base;
+      float *red = (float *)(base + S::part);
+#pragma unroll 1
+      for (int c = 0; c < nchunks; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(trow + 32 * c, v);
+        tc::tmem_ld_wait();
+        const int sl = (32 * c) / W, o = 32 * c - sl * W;
+        float4 *dst = (float4 *)(part + ((size_t)sl * 128 + row) * S::part_ld + o);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+      tc::cluster_sync();
+      TileCtx sub = ctx;
+      sub.n0 = ctx.n0 + z * W;
+      sub.n_valid = min(W, ctx.n_valid - z * W);
+      if (sub.n_valid > 0) {
+        const int q4 = (sub.n_valid + 3) >> 2;
+        const uint32_t mine = tc::smem_u32(part + (size_t)z * 128 * S::part_ld);
+        uint32_t src[SPLIT];
+#pragma unroll
+        for (int j = 0; j < SPLIT; ++j) src[j] = tc::cluster_addr(mine, (uint32_t)j);
+        // four float4 columns per thread per step, all remote reads in flight
+        for (int i0 = threadIdx.x; i0 < 128 * q4; i0 += 4 * 128) {
+          float4 v[4][SPLIT];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int idx = min(i0 + 128 * u, 128 * q4 - 1);
+            const int r = idx / q4, q = idx - r * q4;
+            const uint32_t off = (uint32_t)((r * S::part_ld + 4 * q) * 4);
+#pragma unroll
+            for (int j = 0; j < SPLIT; ++j) v[u][j] = tc::ld_cluster_f4(src[j] + off);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int idx = i0 + 128 * u;
+            if (idx < 128 * q4) {
+              const int r = idx / q4, q = idx - r * q4;
+              float4 acc = v[u][0];
+#pragma unroll
+              for (int j = 1; j < SPLIT; ++j) {
+                acc.x += v[u][j].x;
+                acc.y += v[u][j].y;
+                acc.z += v[u][j].z;
+                acc.w += v[u][j].w;
+              }
+              float *d = red + r * S::red_ld + 4 * q;
+              d[0] = acc.x;
+              d[1] = acc.y;
+              d[2] = acc.z;
+              d[3] = acc.w;
+            }
+          }
+        }
+        __syncthreads();
+        epi(red, S::red_ld, sub, extra);
+      }
+      tc::cluster_sync();
     }
-    tc::cluster_sync();
-  }
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 1) {
+    // The next item's MMAs overwrite the accumulator and its copies the
+    // shared memory the epilogue used.
+    tc::fence_before();
+    __syncthreads();
     tc::fence_after();
+  }
+  if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
                  "r"((uint32_t)tc::kSkBN));
   }
@@ -545,12 +616,11 @@ cudaError_t launch_tc(const CUtensorMap &ta, const CUtensorMap &ta2, const CUten
     if (dev < 64) attr_set |= 1ull << dev;
   }
   if (grid_y <= 0 || g.M <= 0 || g.K % tc::kBK) return g.K % tc::kBK ? cudaErrorInvalidValue : cudaSuccess;
-  dim3 grid(ceil_div(g.M, 128), grid_y);
-  kern<<<grid, 128, S::bytes, st>>>(ta, ta2, tb, g, epi);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(ceil_div(g.M, 128), grid_y), dim3(128), S::bytes, st, ta, ta2, tb, g, epi);
 }
 
 // Split-K launch: grid (ceil(M / 128), grid_y, SPLIT), clusters of (1, 1, SPLIT).
+// Grouped launches (g.work set) walk the work list with stride grid_y.
 template <int SPLIT, class Epi>
 cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
                          const Epi &epi, int grid_y, cudaStream_t st) {
@@ -573,13 +643,22 @@ cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcA
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = S::bytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = SPLIT;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (SPLIT > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = SPLIT;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = SPLIT > 1 ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, g, epi);
 }
 

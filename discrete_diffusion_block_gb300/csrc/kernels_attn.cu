@@ -46,6 +46,8 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t *r, const void *p) {
 
 template <int HD>
 __global__ void __launch_bounds__(128) attn_kernel(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int LDK = HD + 8;
   extern __shared__ __align__(16) unsigned char smem[];
   bf16 *Ks = (bf16 *)smem;                 // [2][64][LDK]
@@ -216,6 +218,8 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnParams p) {
 // Merge the split-KV partial states of one (row, KV head): weights 2^(m_s - m*).
 __global__ void attn_combine_kernel(const float *o_part, const float *ml_part, int splits, int Hkv,
                                     int rows_total, int G, int Hq, int HD, bf16 *out) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x, g = blockIdx.y;
   const float NEG = __int_as_float(0xff800000);
   float mx = NEG;
@@ -342,17 +346,12 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[which] |= 1ull << dev;
   }
-  if (which)
-    attn_kernel<128><<<grid, 128, smem, st>>>(p);
-  else
-    attn_kernel<64><<<grid, 128, smem, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (pl.splits > 1) {
-    attn_combine_kernel<<<dim3(rows_total, s.Hkv), 128, 0, st>>>(p.o_part, p.ml_part, pl.splits,
-                                                                 s.Hkv, rows_total, p.G, s.Hq, s.hd,
-                                                                 out);
-    e = cudaGetLastError();
-  }
+  e = which ? launch_pdl(attn_kernel<128>, grid, dim3(128), smem, st, p)
+            : launch_pdl(attn_kernel<64>, grid, dim3(128), smem, st, p);
+  if (e != cudaSuccess) return e;
+  if (pl.splits > 1)
+    e = launch_pdl(attn_combine_kernel, dim3(rows_total, s.Hkv), dim3(128), 0, st, (const float *)p.o_part,
+                   (const float *)p.ml_part, pl.splits, s.Hkv, rows_total, p.G, s.Hq, s.hd, out);
   return e;
 }
 

@@ -66,34 +66,50 @@ struct EpiQkv {
         slot[t] = ((long long)o.page_table[p / o.pg] * o.Hkv * o.pg + p % o.pg) * hd;
       }
       __syncthreads();
-      for (int t = warp; t < nt; t += blockDim.x >> 5) {
-        const int tt = t0 + t, tok = c.n0 + tt;
-        for (int u = lane; u < units; u += 32) {
-          const int hh = u >> pairs_log, j = 2 * (u & ((1 << pairs_log) - 1));
-          const int f = hh * hd + j, fg = c.m0 + f;
-          const float a0 = tile[f * ldc + tt], a1 = tile[(f + 1) * ldc + tt];
-          const float b0 = tile[(f + half) * ldc + tt], b1 = tile[(f + half + 1) * ldc + tt];
-          float lo0 = a0, lo1 = a1, hi0 = b0, hi1 = b1;
-          if (fg < qdim + kdim) {
-            const float c0 = cs[t * half + j], c1 = cs[t * half + j + 1];
-            const float s0 = sn[t * half + j], s1 = sn[t * half + j + 1];
-            lo0 = a0 * c0 - b0 * s0;
-            lo1 = a1 * c1 - b1 * s1;
-            hi0 = b0 * c0 + a0 * s0;
-            hi1 = b1 * c1 + a1 * s1;
+      const int nw = blockDim.x >> 5;
+      for (int u = lane; u < units; u += 32) {
+        const int hh = u >> pairs_log, j = 2 * (u & ((1 << pairs_log) - 1));
+        const int f = hh * hd + j, fg = c.m0 + f;
+        const int fh = fg - j;  // first feature of the head
+        const bool rot = fg < qdim + kdim;
+        bf16 *base_q = nullptr, *base_kv = nullptr;
+        if (fh < qdim) {
+          base_q = o.q + fh + j;
+        } else {
+          const bool is_k = fh < qdim + kdim;
+          const int head = (fh - (is_k ? qdim : qdim + kdim)) / hd;
+          base_kv = (is_k ? o.k_pool : o.v_pool) + (long long)head * o.pg * hd + j;
+        }
+        // four tokens per step: all shared-memory reads first, then math, then stores
+        for (int tb = warp; tb < nt; tb += 4 * nw) {
+          float a0[4], a1[4], b0[4], b1[4], c0[4], c1[4], s0[4], s1[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int t = min(tb + q * nw, nt - 1), tt = t0 + t;
+            a0[q] = tile[f * ldc + tt];
+            a1[q] = tile[(f + 1) * ldc + tt];
+            b0[q] = tile[(f + half) * ldc + tt];
+            b1[q] = tile[(f + half + 1) * ldc + tt];
+            c0[q] = cs[t * half + j];
+            c1[q] = cs[t * half + j + 1];
+            s0[q] = sn[t * half + j];
+            s1[q] = sn[t * half + j + 1];
           }
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(lo0, lo1), hi = __floats2bfloat162_rn(hi0, hi1);
-          const int fh = fg - j;  // first feature of the head
-          bf16 *dst;
-          if (fh < qdim) {
-            dst = o.q + (size_t)tok * qdim + fh;
-          } else {
-            const bool is_k = fh < qdim + kdim;
-            const int head = (fh - (is_k ? qdim : qdim + kdim)) / hd;
-            dst = (is_k ? o.k_pool : o.v_pool) + slot[t] + (long long)head * o.pg * hd;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int t = tb + q * nw;
+            if (t >= nt) break;
+            float lo0 = a0[q], lo1 = a1[q], hi0 = b0[q], hi1 = b1[q];
+            if (rot) {
+              lo0 = a0[q] * c0[q] - b0[q] * s0[q];
+              lo1 = a1[q] * c1[q] - b1[q] * s1[q];
+              hi0 = b0[q] * c0[q] + a0[q] * s0[q];
+              hi1 = b1[q] * c1[q] + a1[q] * s1[q];
+            }
+            bf16 *dst = base_q ? base_q + (size_t)(c.n0 + t0 + t) * qdim : base_kv + slot[t];
+            *(__nv_bfloat162 *)dst = __floats2bfloat162_rn(lo0, lo1);
+            *(__nv_bfloat162 *)(dst + half) = __floats2bfloat162_rn(hi0, hi1);
           }
-          *(__nv_bfloat162 *)(dst + j) = lo;
-          *(__nv_bfloat162 *)(dst + j + half) = hi;
         }
       }
     }
@@ -132,35 +148,73 @@ struct EpiResidual {
   }
 };
 
-// out[token][feature] = tile (grouped launches address rows from b_base)
+// out[token][feature] = tile (grouped launches address rows from b_base).
+// Four tokens x four feature groups per step, reads before writes.
 struct EpiStore {
   static constexpr size_t extra_smem = 0;
   float *out;
   int ldo;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = warp; t < c.n_valid; t += blockDim.x >> 5) {
-      float *orow = out + (size_t)(c.b_base + c.n0 + t) * ldo + c.m0;
-      for (int f = lane; f < c.m_valid; f += 32) orow[f] = tile[f * ldc + t];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int f0 = 0; f0 < c.m_valid; f0 += 128) {
+      for (int tb = warp; tb < c.n_valid; tb += 4 * nw) {
+        float v[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int t = min(tb + q * nw, c.n_valid - 1), f = min(f0 + 32 * g + lane, c.m_valid - 1);
+            v[q][g] = tile[f * ldc + t];
+          }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int t = tb + q * nw;
+          if (t < c.n_valid) {
+            float *orow = out + (size_t)(c.b_base + c.n0 + t) * ldo + c.m0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const int f = f0 + 32 * g + lane;
+              if (f < c.m_valid) orow[f] = v[q][g];
+            }
+          }
+        }
+      }
     }
   }
 };
 
+// silu(g) * u with the hardware exp and a fast divide; the product is rounded
+// to bf16 right after, far coarser than either approximation.
+__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 // SwiGLU on a 128-row tile holding 64 gate rows then the matching 64 up rows;
-// each lane writes two adjacent outputs as bf16x2.
+// each lane writes two adjacent outputs as bf16x2, four tokens per step.
 struct EpiSwiGlu {
   static constexpr size_t extra_smem = 0;
   bf16 *act;
   int F;
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
     const int fb = c.m0 / 128;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int j = 2 * lane;
-    for (int t = warp; t < c.n_valid; t += blockDim.x >> 5) {
-      const float g0 = tile[j * ldc + t], g1 = tile[(j + 1) * ldc + t];
-      const float u0 = tile[(64 + j) * ldc + t], u1 = tile[(65 + j) * ldc + t];
-      *(__nv_bfloat162 *)(act + (size_t)(c.b_base + c.n0 + t) * F + fb * 64 + j) =
-          __floats2bfloat162_rn(silu_f(g0) * u0, silu_f(g1) * u1);
+    bf16 *base = act + (size_t)(c.b_base + c.n0) * F + fb * 64 + j;
+    for (int tb = warp; tb < c.n_valid; tb += 4 * nw) {
+      float g0[4], g1[4], u0[4], u1[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int t = min(tb + q * nw, c.n_valid - 1);
+        g0[q] = tile[j * ldc + t];
+        g1[q] = tile[(j + 1) * ldc + t];
+        u0[q] = tile[(64 + j) * ldc + t];
+        u1[q] = tile[(65 + j) * ldc + t];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int t = tb + q * nw;
+        if (t < c.n_valid)
+          *(__nv_bfloat162 *)(base + (size_t)t * F) =
+              __floats2bfloat162_rn(swiglu(g0[q], u0[q]), swiglu(g1[q], u1[q]));
+      }
     }
   }
 };
@@ -306,6 +360,27 @@ static int pick_split(int m_tiles, int n_tiles, int kt) {
   return s;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+static int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Clusters along y of a grouped launch: at most one CTA per SM in total, so
+// that every CTA is resident from the start.
+static int grouped_grid_y(int ctas_per_item, int max_work) {
+  int gy = num_sms() / ctas_per_item;
+  if (gy > max_work) gy = max_work;
+  return gy < 1 ? 1 : gy;
+}
+
 template <class Epi>
 static cudaError_t launch_split(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
                                 const Epi &epi, int grid_y, int split, cudaStream_t st) {
@@ -352,7 +427,8 @@ cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, c
   g.n_work = n_work;
   g.group_offs = offs;
   EpiSwiGlu epi{act, F};
-  return launch_split(ta, tb, g, epi, max_work, d / tc::kBK >= 8 ? 2 : 1, st);
+  const int split = d / tc::kBK >= 8 ? 2 : 1;
+  return launch_split(ta, tb, g, epi, grouped_grid_y(ceil_div(2 * F, 128) * split, max_work), split, st);
 }
 
 cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const int *offs,
@@ -367,7 +443,7 @@ cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const in
   g.n_work = n_work;
   g.group_offs = offs;
   EpiStore epi{y, d};
-  return launch_split(ta, tb, g, epi, max_work, 1, st);
+  return launch_split(ta, tb, g, epi, grouped_grid_y(ceil_div(d, 128), max_work), 1, st);
 }
 
 // LM head: A = normalised token rows (hi, and lo of a hi/lo split), B = the

@@ -2,6 +2,7 @@
 // embedding gather, RMSNorm, RoPE tables, MoE routing / permutation /
 // combination, KV append.
 #include <math.h>
+#include <stdlib.h>
 
 #include "internal.h"
 
@@ -76,6 +77,8 @@ __global__ void rope_table_kernel(float *ct, float *stt, int max_pos, int half, 
 // x_1 ~ Unif(V^C): id = floor(word0 * V / 2^32), word0 of Philox at (i, 0, k, 2).
 __global__ void canvas_init_kernel(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
                                    uint32_t k0, uint32_t k1, int canvas) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= C) return;
   const U4 w = philox10((uint32_t)i, 0u, (uint32_t)canvas, kTagInit, k0, k1);
@@ -86,6 +89,8 @@ __global__ void canvas_init_kernel(int *x, uint8_t *committed, int *last, int *s
 }
 
 __global__ void embed_kernel(float *h, const bf16 *table, const int *ids, int d) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const bf16 *row = table + (size_t)ids[t] * d;
   for (int c = threadIdx.x; c < d; c += blockDim.x) h[(size_t)t * d + c] = __bfloat162float(row[c]);
@@ -98,6 +103,8 @@ __global__ void embed_kernel(float *h, const bf16 *table, const int *ids, int d)
 constexpr int kNormThreads = 128, kNormVec = 8;
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *out_lo, const float *h,
                                                                const float *g, int d, float eps) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x, d4 = d >> 2;
   const float4 *x = (const float4 *)(h + (size_t)t * d);
   const float4 *g4 = (const float4 *)g;
@@ -151,6 +158,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *
 // An unordered logit (NaN) never wins a comparison but a still-unselected
 // expert is always taken over none, so every emitted id is in [0, E).
 __global__ void topk_kernel(const float *logits, int T, int E, int k, int *ids, float *gates) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= T) return;
   float v[8];
@@ -208,6 +217,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, i
                                                                int *perm_tok, int *slot_row,
                                                                int *work, int *n_work,
                                                                unsigned long long *stats) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int seg[kPermWarps][257];  // per-segment counts, then running ranks
   __shared__ int cnt[257], soff[257], toff[257];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -308,6 +319,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, i
 __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y, const float *gates,
                                                       const int *slot_row, int k, int d4,
                                                       int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   __shared__ float g_s[16];
   __shared__ int r_s[16];
@@ -339,6 +352,8 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
 // expert's rows are one contiguous TMA box source.
 __global__ void gather_rows_kernel(uint4 *dst, const uint4 *src, const int *perm_tok, int rows,
                                    int vec) {
+  pdl_wait();
+  pdl_trigger();
   const size_t total = (size_t)rows * vec;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -351,6 +366,8 @@ __global__ void gather_rows_kernel(uint4 *dst, const uint4 *src, const int *perm
 __global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *k_pool,
                                  uint4 *v_pool, const int *page_table, int L, int n_pages, int pos0,
                                  int n, int Hkv, int hd, int pg) {
+  pdl_wait();
+  pdl_trigger();
   const int vec = hd / 8;  // uint4 per head row
   const size_t total = (size_t)L * n * Hkv * vec;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
@@ -370,6 +387,15 @@ __global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *
 }
 
 }  // namespace
+
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char *v = getenv("DG_PDL");
+    on = (v && v[0] == '0') ? 0 : 1;
+  }
+  return on == 1;
+}
 
 static float weight_scale(float std_dev) {
   return (float)((double)std_dev * sqrt(3.0) / 8388608.0);
@@ -410,31 +436,26 @@ cudaError_t rope_table(float *ct, float *stt, int max_pos, int hd, float base, c
 
 cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
                         uint64_t seed, int canvas, cudaStream_t st) {
-  canvas_init_kernel<<<ceil_div(C, 256), 256, 0, st>>>(x, committed, last, stable, C, V,
-                                                       (uint32_t)seed, (uint32_t)(seed >> 32),
-                                                       canvas);
-  return cudaGetLastError();
+  return launch_pdl(canvas_init_kernel, dim3(ceil_div(C, 256)), dim3(256), 0, st, x, committed, last, stable, C, V,
+                    (uint32_t)seed, (uint32_t)(seed >> 32), canvas);
 }
 
 cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  embed_kernel<<<T, 256, 0, st>>>(h, table, ids, d);
-  return cudaGetLastError();
+  return launch_pdl(embed_kernel, dim3(T), dim3(256), 0, st, h, table, ids, d);
 }
 
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
                          cudaStream_t st, bf16 *out_lo) {
   if (T == 0) return cudaSuccess;
   if (d % 4) return cudaErrorInvalidValue;
-  rmsnorm_kernel<<<T, kNormThreads, 0, st>>>(out, out_lo, h, gain, d, eps);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, out, out_lo, h, gain, d, eps);
 }
 
 cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, float *gates,
                         cudaStream_t st) {
   if (E > 256 || k > 16 || k > E) return cudaErrorInvalidValue;
-  topk_kernel<<<ceil_div(T * 32, 256), 256, 0, st>>>(logits, T, E, k, ids, gates);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(ceil_div(T * 32, 256)), dim3(256), 0, st, logits, T, E, k, ids, gates);
 }
 
 size_t moe_max_work(int T, int k, int E, int tile_rows) {
@@ -445,27 +466,24 @@ cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int 
                         int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st,
                         unsigned long long *stats) {
   if (E > 256) return cudaErrorInvalidValue;
-  permute_kernel<<<1, kPermThreads, 0, st>>>(ids, T * k, k, E, tile_rows, offs, perm_tok, slot_row,
-                                             work, n_work, stats);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), 0, st, ids, T * k, k, E, tile_rows, offs,
+                    perm_tok, slot_row, work, n_work, stats);
 }
 
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   if (k > 16 || d % 4) return cudaErrorInvalidValue;
-  combine_kernel<<<T, 256, 0, st>>>((float4 *)h, (const float4 *)y, gates, slot_row, k, d / 4,
-                                    accumulate ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const float4 *)y, gates, slot_row, k,
+                    d / 4, accumulate ? 1 : 0);
 }
 
 cudaError_t gather_rows(bf16 *x_perm, const bf16 *xn, const int *perm_tok, int rows, int d,
                         cudaStream_t st) {
   const size_t total = (size_t)rows * (d / 8);
   if (total == 0) return cudaSuccess;
-  gather_rows_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, st>>>(
-      (uint4 *)x_perm, (const uint4 *)xn, perm_tok, rows, d / 8);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(grid_for(total, 256, 152 * 16)), dim3(256), 0, st, (uint4 *)x_perm,
+                    (const uint4 *)xn, perm_tok, rows, d / 8);
 }
 
 cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
@@ -473,10 +491,9 @@ cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *
                       int pg, cudaStream_t st) {
   const size_t total = (size_t)L * n * Hkv * (hd / 8);
   if (total == 0) return cudaSuccess;
-  kv_append_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, st>>>(
-      (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_pool, (uint4 *)v_pool, page_table, L,
-      n_pages, pos0, n, Hkv, hd, pg);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(grid_for(total, 256, 152 * 16)), dim3(256), 0, st,
+                    (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_pool, (uint4 *)v_pool, page_table, L,
+                    n_pages, pos0, n, Hkv, hd, pg);
 }
 
 }  // namespace dg

@@ -26,6 +26,8 @@ constexpr int kLdl = kVocabTile + 1;
 __global__ void __launch_bounds__(256) logits_partials_kernel(const float *logits, int rows, int V,
                                                               uint32_t key0, uint32_t key1,
                                                               uint32_t ctr2, PartialPlanes P) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float sm[];
   float *L = sm;
   float *K = L + kLogitRowsPerBlock * kLdl;
@@ -49,6 +51,8 @@ constexpr int kMergeThreads = 256;
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(PartialPlanes P, int tiles,
                                                               int leaves_per_thread, int *argmax,
                                                               float *conf, int *gumbel) {
+  pdl_wait();
+  pdl_trigger();
   const int pos = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // in-thread subtree over leaves [tid*c, tid*c + c), c a power of two
   Partial stack[12];
@@ -95,6 +99,8 @@ __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum
                             int budget_N, int stable_steps, int adaptive, float thr, int *x,
                             uint8_t *committed, int *last, int *stable, int *done,
                             const StepParams *dyn) {
+  pdl_wait();
+  pdl_trigger();
   const int i = threadIdx.x;
   if (dyn) step = dyn->step;
   bool com = true;
@@ -130,10 +136,8 @@ cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(tiles, ceil_div(rows, kLogitRowsPerBlock));
-  logits_partials_kernel<<<grid, 256, smem, st>>>(logits, rows, V, (uint32_t)seed,
-                                                  (uint32_t)(seed >> 32),
-                                                  gumbel_ctr2(canvas, step), P);
-  return cudaGetLastError();
+  return launch_pdl(logits_partials_kernel, grid, dim3(256), smem, st, logits, rows, V, (uint32_t)seed,
+                    (uint32_t)(seed >> 32), gumbel_ctr2(canvas, step), P);
 }
 
 cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,
@@ -144,8 +148,7 @@ cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float
   const int c = width / kMergeThreads;
   if (c > 1024) return cudaErrorInvalidValue;  // stack depth of the in-thread tree
   const PartialPlanes P = PartialPlanes::at(const_cast<void *>(partials), C, tiles);
-  merge_kernel<<<C, kMergeThreads, 0, st>>>(P, tiles, c, argmax, conf, gumbel);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(C), dim3(kMergeThreads), 0, st, P, tiles, c, argmax, conf, gumbel);
 }
 
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
@@ -154,9 +157,8 @@ cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel
                          cudaStream_t st, const StepParams *dyn) {
   if (C > 1024) return cudaErrorInvalidValue;
   const int threads = ((C + 31) / 32) * 32;
-  rule_kernel<<<1, threads, 0, st>>>(argmax, conf, gumbel, C, step, budget_N, stable_steps,
-                                     adaptive, conf_threshold, x, committed, last, stable, done, dyn);
-  return cudaGetLastError();
+  return launch_pdl(rule_kernel, dim3(1), dim3(threads), 0, st, argmax, conf, gumbel, C, step, budget_N,
+                    stable_steps, adaptive, conf_threshold, x, committed, last, stable, done, dyn);
 }
 
 }  // namespace dg
