@@ -69,12 +69,14 @@ __device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b)
 __device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
 __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
 
+// Both are written without branches: the special cases are selected after
+// the main path, so a warp evaluating many entries keeps them interleaved.
+// The results are those of the branching form bit for bit (checked over all
+// 2^32 inputs).
 __device__ __forceinline__ float dg_exp(float x) {
-  if (x != x) return x;
-  if (x < -87.0f) return 0.0f;
-  if (x > 88.0f) return __int_as_float(0x7f800000);
-  const float kf = floorf(fadd(fmul(x, kLog2e), 0.5f));
-  float r = fsub(x, fmul(kf, kLn2Hi));
+  const float xc = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float kf = floorf(fadd(fmul(xc, kLog2e), 0.5f));
+  float r = fsub(xc, fmul(kf, kLn2Hi));
   r = fsub(r, fmul(kf, kLn2Lo));
   float p = (float)(1.0 / 5040.0);
   p = fadd(fmul(p, r), (float)(1.0 / 720.0));
@@ -85,26 +87,21 @@ __device__ __forceinline__ float dg_exp(float x) {
   p = fadd(fmul(p, r), 1.0f);
   p = fadd(fmul(p, r), 1.0f);
   const int k = (int)kf;
-  return fmul(p, __int_as_float((k + 127) << 23));
+  float y = fmul(p, __int_as_float((k + 127) << 23));
+  y = x < -87.0f ? 0.0f : y;
+  y = x > 88.0f ? __int_as_float(0x7f800000) : y;
+  return x != x ? x : y;
 }
 
 __device__ __forceinline__ float dg_log(float x) {
-  if (x != x) return x;
-  if (x < 0.0f) return __int_as_float(0x7fc00000);
-  if (x == 0.0f) return __int_as_float(0xff800000);
-  if (x == __int_as_float(0x7f800000)) return x;
-  int eadj = 0;
-  if (x < 1.17549435e-38f) {  // subnormal: scale into the normal range
-    x = fmul(x, 8388608.0f);
-    eadj = -23;
-  }
-  const int bits = __float_as_int(x);
-  int e = ((bits >> 23) & 0xff) - 127 + eadj;
+  const bool sub = x < 1.17549435e-38f;  // subnormal: scale into the normal range
+  const float xs = sub ? fmul(x, 8388608.0f) : x;
+  const int bits = __float_as_int(xs);
+  int e = ((bits >> 23) & 0xff) - 127 - (sub ? 23 : 0);
   float m = __int_as_float((bits & 0x7fffff) | 0x3f800000);
-  if (m > kSqrt2) {
-    m = fmul(m, 0.5f);
-    e += 1;
-  }
+  const bool big = m > kSqrt2;
+  m = big ? fmul(m, 0.5f) : m;
+  e += big ? 1 : 0;
   const float s = __fdiv_rn(fsub(m, 1.0f), fadd(m, 1.0f));
   const float z = fmul(s, s);
   float q = (float)(1.0 / 11.0);
@@ -116,8 +113,11 @@ __device__ __forceinline__ float dg_log(float x) {
   float lm = fadd(s, fmul(s, q));
   lm = fadd(lm, lm);
   const float ef = (float)e;
-  const float r = fadd(fmul(ef, kLn2Lo), lm);
-  return fadd(r, fmul(ef, kLn2Hi));
+  float r = fadd(fadd(fmul(ef, kLn2Lo), lm), fmul(ef, kLn2Hi));
+  r = x == 0.0f ? __int_as_float(0xff800000) : r;
+  r = x < 0.0f ? __int_as_float(0x7fc00000) : r;
+  r = x == __int_as_float(0x7f800000) ? x : r;
+  return x != x ? x : r;
 }
 
 // Open-interval uniform of a Philox word: (2 (w >> 9) + 1) * 2^-24.

@@ -1,17 +1,19 @@
-// Blackwell (sm_103a) tensor-core GEMM  D[M][N] = A[M][K] . B[N][K]^T with fp32
-// accumulation in tensor memory, for the decoder's dense contractions.
+// Blackwell (sm_103a) tensor-core building blocks: mbarrier waits, TMA
+// loads and L2 prefetches, shared-memory matrix descriptors, tcgen05.mma /
+// commit / ld, and the split-K GEMM  D[M][N] = A[M][K] . B[N][K]^T  (fp32
+// accumulation in tensor memory) used for every projection and expert GEMM
+// of the decoder.  The LM head has its own persistent kernel built from the
+// same pieces (kernels_lmhead.cu).
 //
-// One CTA computes one 128 x BN output tile with 4 warps:
-//   warp 0, one thread  -- TMA producer: 128-row A tiles (and the second A of a
-//                          hi/lo split) and BN-row B tiles, 64 K-elements each,
-//                          128-byte swizzled, into a STAGES-deep smem ring;
-//   warp 1, one thread  -- allocates BN TMEM columns and issues
-//                          tcgen05.mma (M = 128, N = BN, K = 16) per stage,
+// Roles inside a GEMM CTA (128 threads):
+//   warp 0, one thread  -- TMA producer: 128-row A boxes and 64-row B boxes,
+//                          64 K-elements each, 128-byte swizzled, into a
+//                          4-stage shared-memory ring;
+//   warp 1, one thread  -- allocates the TMEM accumulator and issues
+//                          tcgen05.mma (M = 128, N <= 256, K = 16) per stage,
 //                          releasing each stage with tcgen05.commit;
-//   warps 0-3           -- after the last commit, read the accumulator out of
-//                          TMEM (each warp its 32-lane quarter) into an fp32
-//                          smem tile and run the same cooperative epilogues as
-//                          the warp-level GEMM (gemm_mma.cuh).
+//   warps 0-3           -- read the accumulator out of TMEM (each warp its
+//                          32-lane quarter) and run the fused epilogue.
 // Every mbarrier wait is bounded; a wait that gives up records an error word
 // and lets the CTA finish, so a fault can never hang the GPU.
 #pragma once
@@ -152,148 +154,21 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
-template <int BN, int STAGES, int NA, int EPI_ROWS, class Epi>
-struct TcSmem {
-  static constexpr uint32_t b_bytes = BN * 128;
-  static constexpr uint32_t stage_bytes = NA * kATileBytes + b_bytes;
-  static constexpr size_t ring = (size_t)STAGES * stage_bytes;
-  static constexpr size_t bars = (2 * STAGES + 1) * 8 + 16;  // + TMEM address + abort flag
-  static constexpr int ldc = BN + 1;
-  static constexpr size_t epi = (size_t)EPI_ROWS * ldc * 4 + Epi::extra_smem;
-  static constexpr size_t main_bytes = ring + bars;
-  static constexpr size_t bytes = (main_bytes > epi ? main_bytes : epi) + 1024;  // + alignment slack
-  static constexpr int tmem_cols = BN < 32 ? 32 : BN;
-};
+// The same wait with the loaded registers as in/out operands, so that no use
+// of them can be scheduled before it (for code placed between load and wait).
+__device__ __forceinline__ void tmem_ld_wait(uint32_t *r) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
 
 }  // namespace tc
-
-template <int BN, int STAGES, int NA, int EPI_ROWS, class Epi>
-__global__ void __launch_bounds__(128, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap ta2,
-                   const __grid_constant__ CUtensorMap tb, TcArgs g, Epi epi) {
-  using S = tc::TcSmem<BN, STAGES, NA, EPI_ROWS, Epi>;
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert(128 % EPI_ROWS == 0 && EPI_ROWS % 32 == 0, "EPI_ROWS");
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t *full = (uint64_t *)(base + S::ring);
-  uint64_t *empty = full + STAGES;
-  uint64_t *accb = empty + STAGES;
-  uint32_t *tmem_slot = (uint32_t *)(accb + 1);
-  volatile int *abort = (volatile int *)(tmem_slot + 1);
-
-  pdl_wait();
-  pdl_trigger();
-  TileCtx ctx;
-  ctx.m0 = blockIdx.x * 128;
-  ctx.group = 0;
-  ctx.b_base = 0;
-  int n_total = g.N;
-  if (g.work) {
-    const int w = blockIdx.y;
-    if (w >= *g.n_work) return;
-    ctx.group = g.work[2 * w];
-    ctx.n0 = g.work[2 * w + 1];
-    ctx.b_base = g.group_offs[ctx.group];
-    n_total = g.group_offs[ctx.group + 1] - ctx.b_base;
-  } else {
-    ctx.n0 = blockIdx.y * BN;
-  }
-  ctx.m_valid = min(128, g.M - ctx.m0);
-  ctx.n_valid = min(BN, n_total - ctx.n0);
-  if (ctx.m_valid <= 0 || ctx.n_valid <= 0) return;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KT = g.K / tc::kBK;
-  if (threadIdx.x == 0) {
-    *abort = (g.err && *(volatile int *)g.err) ? 1 : 0;  // an earlier timeout: do not wait again
-    for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
-    }
-    tc::mbar_init(accb, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     tc::smem_u32(tmem_slot)),
-                 "r"((uint32_t)S::tmem_cols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  const int a_row = ctx.group * g.a_group_rows + ctx.m0;
-  const int b_row = ctx.b_base + ctx.n0;
-  auto a_tile = [&](int s, int h) { return base + (size_t)s * S::stage_bytes + h * tc::kATileBytes; };
-  auto b_tile = [&](int s) { return base + (size_t)s * S::stage_bytes + NA * tc::kATileBytes; };
-
-  if (warp == 0 && lane == 0) {
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % STAGES, r = kt / STAGES;
-      if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 1, abort);
-      if (*abort) break;  // no new copies once the CTA has given up
-      tc::mbar_expect_tx(full + s, S::stage_bytes);
-      tc::tma_load_2d(a_tile(s, 0), &ta, kt * tc::kBK, a_row, full + s);
-      if (NA == 2) tc::tma_load_2d(a_tile(s, 1), &ta2, kt * tc::kBK, a_row, full + s);
-      tc::tma_load_2d(b_tile(s), &tb, kt * tc::kBK, b_row, full + s);
-    }
-  } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = tc::idesc_bf16(128, BN);
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % STAGES, r = kt / STAGES;
-      tc::mbar_wait(full + s, r & 1, g.err, 2, abort);
-      tc::fence_after();
-      const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(b_tile(s)));
-#pragma unroll
-      for (int h = 0; h < NA; ++h) {
-        const uint64_t adesc = tc::sw128_desc(tc::smem_u32(a_tile(s, h)));
-#pragma unroll
-        for (int kk = 0; kk < tc::kBK / 16; ++kk)  // +32 bytes of K per MMA: +2 in the address field
-          tc::mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk | h) ? 1u : 0u);
-      }
-      tc::mma_commit(empty + s);
-    }
-    tc::mma_commit(accb);
-  }
-  __syncwarp();
-
-  // ---- epilogue: TMEM -> fp32 smem tile -> cooperative epilogue --------------
-  tc::mbar_wait(accb, 0, g.err, 3, abort);
-  tc::fence_after();
-  float *tile = (float *)base;
-  constexpr int ldc = S::ldc;
-  for (int c = 0; c < 128 / EPI_ROWS; ++c) {
-    __syncthreads();
-    const int r0 = c * EPI_ROWS;
-    if (warp * 32 >= r0 && warp * 32 < r0 + EPI_ROWS) {
-      const int row = warp * 32 - r0 + lane;
-#pragma unroll 1
-      for (int col = 0; col < BN; col += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + col, v);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) tile[row * ldc + col + j] = __uint_as_float(v[j]);
-      }
-    }
-    __syncthreads();
-    TileCtx sub = ctx;
-    sub.m0 = ctx.m0 + r0;
-    sub.m_valid = min(EPI_ROWS, ctx.m_valid - r0);
-    if (sub.m_valid > 0) epi(tile, ldc, sub, (unsigned char *)(tile + EPI_ROWS * ldc));
-  }
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc::fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
-                 "r"((uint32_t)S::tmem_cols));
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Split-K GEMM for the decoder's skinny products (weights x a few hundred
@@ -600,24 +475,6 @@ __global__ void __launch_bounds__(128, 1)
 // box_rows rows, 128-byte swizzle, zero fill outside the matrix.
 cudaError_t make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
                            uint32_t box_rows);
-
-template <int BN, int STAGES, int NA, int EPI_ROWS, class Epi>
-cudaError_t launch_tc(const CUtensorMap &ta, const CUtensorMap &ta2, const CUtensorMap &tb,
-                      const TcArgs &g, const Epi &epi, int grid_y, cudaStream_t st) {
-  using S = tc::TcSmem<BN, STAGES, NA, EPI_ROWS, Epi>;
-  auto kern = tc_gemm_kernel<BN, STAGES, NA, EPI_ROWS, Epi>;
-  static unsigned long long attr_set = 0;  // per device: one attribute call per instantiation
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set |= 1ull << dev;
-  }
-  if (grid_y <= 0 || g.M <= 0 || g.K % tc::kBK) return g.K % tc::kBK ? cudaErrorInvalidValue : cudaSuccess;
-  return launch_pdl(kern, dim3(ceil_div(g.M, 128), grid_y), dim3(128), S::bytes, st, ta, ta2, tb, g, epi);
-}
 
 // Split-K launch: grid (ceil(M / 128), grid_y, SPLIT), clusters of (1, 1, SPLIT).
 // Grouped launches (g.work set) walk the work list with stride grid_y.

@@ -10,7 +10,6 @@
 
 #include "gemm_tc.cuh"
 #include "internal.h"
-#include "sampler.cuh"
 
 namespace dg {
 
@@ -219,38 +218,6 @@ struct EpiSwiGlu {
   }
 };
 
-// LM head: the tile is [token][256 vocab]; reduce it to sampler partials.
-template <int BM>
-struct EpiLmHead {
-  static constexpr size_t extra_smem = (size_t)BM * (kVocabTile + 1) * sizeof(float) + BM * 8;
-  PartialPlanes P;
-  int tiles;
-  uint32_t ctr2, key0, key1;
-  const StepParams *dyn;  // when set, the stream words come from device memory
-  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *extra) const {
-    PartialScratch sc;
-    sc.kap = (float *)extra;
-    sc.rm = sc.kap + BM * ldc;
-    sc.ra = (int *)(sc.rm + BM);
-    const uint32_t c2 = dyn ? dyn->ctr2 : ctr2, k0 = dyn ? dyn->key0 : key0, k1 = dyn ? dyn->key1 : key1;
-    block_tile_partials(tile, ldc, sc, c.m_valid, c.n0, c.n0 / kVocabTile, tiles, c.m0, c2, k0, k1,
-                        P, c.m0);
-  }
-};
-
-// out[row][col] = tile, rows = tokens (A operand), cols = vocab (B operand).
-struct EpiStoreRows {
-  static constexpr size_t extra_smem = 0;
-  float *out;
-  long long ldo;
-  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    for (int idx = threadIdx.x; idx < c.m_valid * c.n_valid; idx += blockDim.x) {
-      const int r = idx / c.n_valid, col = idx % c.n_valid;
-      out[(size_t)(c.m0 + r) * ldo + c.n0 + col] = tile[r * ldc + col];
-    }
-  }
-};
-
 TcArgs targs(int M, int N, int K, int *err) {
   TcArgs g{};
   g.M = M;
@@ -328,6 +295,11 @@ static cudaError_t tmap_cached(CUtensorMap *map, const void *ptr, uint64_t rows,
   if (g_tmaps.size() > 16384) g_tmaps.clear();
   g_tmaps.emplace(key, *map);
   return cudaSuccess;
+}
+
+cudaError_t tmap_bf16_cached(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                             uint32_t box) {
+  return tmap_cached(map, ptr, rows, cols, box);
 }
 
 #define TMAP(map, ptr, rows, cols, box)                                            \
@@ -444,39 +416,6 @@ cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const in
   g.group_offs = offs;
   EpiStore epi{y, d};
   return launch_split(ta, tb, g, epi, grouped_grid_y(ceil_div(d, 128), max_work), 1, st);
-}
-
-// LM head: A = normalised token rows (hi, and lo of a hi/lo split), B = the
-// vocab rows of W_out, one 256-wide vocab tile per CTA column.
-cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
-                                  int V, uint64_t seed, int canvas, int step, void *partials,
-                                  int *err, cudaStream_t st, const StepParams *dyn) {
-  CUtensorMap ta, ta2, tb;
-  TMAP(ta, xn, T, d, 128);
-  TMAP(ta2, xn_lo ? xn_lo : xn, T, d, 128);
-  TMAP(tb, w_out, V, d, 256);
-  EpiLmHead<64> epi;
-  epi.tiles = V / kVocabTile;
-  epi.P = PartialPlanes::at(partials, T, epi.tiles);
-  epi.ctr2 = gumbel_ctr2(canvas, step);
-  epi.key0 = (uint32_t)seed;
-  epi.key1 = (uint32_t)(seed >> 32);
-  epi.dyn = dyn;
-  const TcArgs g = targs(T, V, d, err);
-  if (xn_lo) return launch_tc<256, 3, 2, 64>(ta, ta2, tb, g, epi, V / kVocabTile, st);
-  return launch_tc<256, 4, 1, 64>(ta, ta, tb, g, epi, V / kVocabTile, st);
-}
-
-cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
-                                int V, float *logits, int *err, cudaStream_t st) {
-  CUtensorMap ta, ta2, tb;
-  TMAP(ta, xn, T, d, 128);
-  TMAP(ta2, xn_lo ? xn_lo : xn, T, d, 128);
-  TMAP(tb, w_out, V, d, 256);
-  EpiStoreRows epi{logits, V};
-  const TcArgs g = targs(T, V, d, err);
-  if (xn_lo) return launch_tc<256, 3, 2, 64>(ta, ta2, tb, g, epi, V / kVocabTile, st);
-  return launch_tc<256, 4, 1, 64>(ta, ta, tb, g, epi, V / kVocabTile, st);
 }
 
 }  // namespace dg
