@@ -301,15 +301,12 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     KL(DG_K_TOPK, 1, dg::router_topk(m->router, T, c.n_experts, c.top_k, topk, m->gates, st));
     KL(DG_K_PERMUTE, 1,
        dg::moe_permute(topk, T, c.top_k, c.n_experts, dg::kExpertTileRows, m->offs, m->perm_tok,
-                       m->slot_row, m->work, m->n_work, st, m->moe_stats));
+                       m->slot_row, m->work, m->n_work, m->max_work, st, m->moe_stats));
     const int rows = T * c.top_k;
     KL(DG_K_PERMUTE, 1, dg::gather_rows(m->x_perm, m->xn, m->perm_tok, rows, d, st));
-    KL(DG_K_EXPERT_GATE_UP, 1,
-       dg::gemm_expert_gate_up(m->x_perm, rows, W.wgu, m->offs, m->work, m->n_work, m->max_work,
-                               c.n_experts, d, c.d_ff, m->act, err, st));
-    KL(DG_K_EXPERT_DOWN, 1,
-       dg::gemm_expert_down(m->act, rows, W.wd, m->offs, m->work, m->n_work, m->max_work,
-                            c.n_experts, d, c.d_ff, m->y, err, st));
+    KL(DG_K_EXPERT_FFN, 1,
+       dg::moe_ffn(m->x_perm, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
+                   c.n_experts, d, c.d_ff, m->act, m->y, err, st));
     KL(DG_K_COMBINE, 1, dg::moe_combine(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, true, st));
   }
   return DG_OK;
@@ -381,7 +378,7 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->offs, E + 1));
   CKR(m->alloc(&m->perm_tok, (size_t)T * k));
   CKR(m->alloc(&m->slot_row, (size_t)T * k));
-  CKR(m->alloc(&m->work, (size_t)2 * m->max_work + (size_t)T * k));
+  CKR(m->alloc(&m->work, dg::moe_work_ints(T, k, E, dg::kExpertTileRows)));
   CKR(m->alloc(&m->n_work, 1));
   CKR(m->alloc(&m->act, (size_t)T * k * F));
   CKR(m->alloc(&m->x_perm, (size_t)T * k * d));
@@ -867,7 +864,7 @@ int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, siz
 const char *dg_kernel_class_name(int32_t cls) {
   static const char *names[DG_K_CLASSES] = {
       "embed", "rmsnorm", "qkv_rope", "attention", "o_proj", "router", "topk", "permute",
-      "expert_gate_up", "expert_down", "combine", "lm_head", "sampler_merge", "sampler_rule",
+      "expert_ffn", "combine", "lm_head", "sampler_merge", "sampler_rule",
       "canvas_init"};
   return (cls >= 0 && cls < DG_K_CLASSES) ? names[cls] : "";
 }
@@ -986,7 +983,7 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.offs = (int *)take((size_t)(E + 1) * 4);
   w.perm_tok = (int *)take((size_t)T * k * 4);
   w.slot_row = (int *)take((size_t)T * k * 4);
-  w.work = (int *)take(((size_t)2 * w.max_work + (size_t)T * k) * 4);
+  w.work = (int *)take(dg::moe_work_ints(T, k, E, dg::kExpertTileRows) * 4);
   w.n_work = (int *)take(4);
   w.act = (bf16 *)take((size_t)T * k * F * 2);
   w.x_perm = (bf16 *)take((size_t)T * k * d * 2);
@@ -1020,13 +1017,11 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
                         nullptr, st));
   CK(dg::router_topk(w.router, T, n_experts, top_k, expert_ids, gates, st));
   CK(dg::moe_permute(expert_ids, T, top_k, n_experts, dg::kExpertTileRows, w.offs, w.perm_tok,
-                     w.slot_row, w.work, w.n_work, st));
+                     w.slot_row, w.work, w.n_work, w.max_work, st));
   const int rows = T * top_k;
   CK(dg::gather_rows(w.x_perm, (const bf16 *)xn, w.perm_tok, rows, d, st));
-  CK(dg::gemm_expert_gate_up(w.x_perm, rows, (const bf16 *)w_gate_up, w.offs, w.work, w.n_work,
-                             w.max_work, n_experts, d, d_ff, w.act, nullptr, st));
-  CK(dg::gemm_expert_down(w.act, rows, (const bf16 *)w_down, w.offs, w.work, w.n_work, w.max_work,
-                          n_experts, d, d_ff, w.y_rows, nullptr, st));
+  CK(dg::moe_ffn(w.x_perm, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
+                 w.max_work, n_experts, d, d_ff, w.act, w.y_rows, nullptr, st));
   CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));
   return DG_OK;
 }

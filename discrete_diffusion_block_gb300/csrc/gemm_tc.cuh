@@ -203,6 +203,12 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
@@ -243,10 +249,11 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t *tmem_slot = (uint32_t *)(accb + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
-  // Grouped launches loop over the device work list (items y, y + gridDim.y,
-  // ...), so the grid is sized to the machine, not to the worst-case list;
-  // plain launches have one n-tile per blockIdx.y.  The CTAs of a cluster
-  // share blockIdx.x/y and so walk the same items.
+  // Output units are (item, 128-row M tile) pairs; items are the n-tiles of a
+  // plain launch or the device work list of a grouped one.  Cluster c (the
+  // SPLIT CTAs blockIdx.x = c * SPLIT + z, one per K range) takes units c,
+  // c + n_clusters, ..., so the grid is sized to the machine and the units
+  // spread evenly over it.
   int n_items;
   if (g.work) {  // the work list is an earlier kernel's output
     pdl_wait();
@@ -255,10 +262,13 @@ __global__ void __launch_bounds__(128, 1)
   } else {
     n_items = ceil_div(g.N, tc::kSkBN);
   }
-  if ((int)blockIdx.y >= n_items) return;
+  const int m_tiles = ceil_div(g.M, 128);
+  const int n_units = n_items * m_tiles;
+  const int cluster = blockIdx.x / SPLIT, n_clusters = gridDim.x / SPLIT;
+  if (cluster >= n_units) return;  // every CTA of a cluster decides alike
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int z = SPLIT > 1 ? (int)blockIdx.z : 0;
+  const int z = SPLIT > 1 ? (int)(blockIdx.x % SPLIT) : 0;
   const int KT = g.K / tc::kBK;
   const int kb = (int)((long long)KT * z / SPLIT), ke = (int)((long long)KT * (z + 1) / SPLIT);
 
@@ -285,17 +295,18 @@ __global__ void __launch_bounds__(128, 1)
   auto a_tile = [&](int s) { return base + (size_t)s * S::stage_bytes; };
   auto b_tile = [&](int s) { return base + (size_t)s * S::stage_bytes + tc::kATileBytes; };
 
-  // Weights never change: a plain launch starts streaming its first item's A
+  // Weights never change: a plain launch starts streaming its first unit's A
   // boxes before waiting for the kernel that produced B.
   int pre = 0;
   if (!g.work) {
     pre = min(STAGES, ke - kb);
     if (warp == 0 && lane == 0) {
-      const int nv = min(tc::kSkBN, g.N - (int)blockIdx.y * tc::kSkBN);
+      const int y0 = cluster / m_tiles, mt0 = cluster - y0 * m_tiles;
+      const int nv = min(tc::kSkBN, g.N - y0 * tc::kSkBN);
       const uint32_t tx0 = tc::kATileBytes + (uint32_t)((nv + 63) >> 6) * tc::kBChunkBytes;
       for (int i = 0; i < pre; ++i) {
         tc::mbar_expect_tx(full + i, tx0);
-        tc::tma_load_2d(a_tile(i), &ta, (kb + i) * tc::kBK, blockIdx.x * 128, full + i);
+        tc::tma_load_2d(a_tile(i), &ta, (kb + i) * tc::kBK, mt0 * 128, full + i);
       }
     }
     pdl_wait();
@@ -305,9 +316,10 @@ __global__ void __launch_bounds__(128, 1)
 
   int it = 0;     // ring position: k-tiles issued (producer) / consumed (MMA) so far
   int tiles = 0;  // accumulator phase
-  for (int y = blockIdx.y; y < n_items; y += gridDim.y, ++tiles) {
+  for (int unit = cluster; unit < n_units; unit += n_clusters, ++tiles) {
+    const int y = unit / m_tiles, mt = unit - y * m_tiles;
     TileCtx ctx;
-    ctx.m0 = blockIdx.x * 128;
+    ctx.m0 = mt * 128;
     ctx.group = 0;
     ctx.b_base = 0;
     int n_total = g.N;
@@ -329,7 +341,7 @@ __global__ void __launch_bounds__(128, 1)
 
     if (warp == 0 && lane == 0) {
       int issued = it;
-      if (y == (int)blockIdx.y)  // first item: nothing was prefetched for it yet
+      if (unit == cluster)  // first unit: nothing was prefetched for it yet
         for (int kt = kb + STAGES; kt < min(ke, kb + tc::kSkPrefetch); ++kt)
           tc::tma_prefetch_2d(&ta, kt * tc::kBK, a_row);
       for (int kt = kb; kt < ke; ++kt, ++issued) {
@@ -344,10 +356,11 @@ __global__ void __launch_bounds__(128, 1)
         for (int c = 0; c < nb; ++c)
           tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, &tb, kt * tc::kBK, b_row + 64 * c, full + s);
       }
-      if (g.work && y + (int)gridDim.y < n_items && !*abort) {
-        // The next item's first A boxes go to L2 while this item finishes.
-        const int ny = y + gridDim.y;
-        const int na_row = g.work[2 * ny] * g.a_group_rows + ctx.m0;
+      const int nu = unit + n_clusters;
+      if (nu < n_units && !*abort) {
+        // The next unit's first A boxes go to L2 while this one finishes.
+        const int ny = nu / m_tiles, nmt = nu - ny * m_tiles;
+        const int na_row = (g.work ? g.work[2 * ny] * g.a_group_rows : 0) + nmt * 128;
         for (int kt = kb; kt < min(ke, kb + tc::kSkPrefetch); ++kt) tc::tma_prefetch_2d(&ta, kt * tc::kBK, na_row);
       }
       if (*abort) {
@@ -389,20 +402,23 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < nchunks; ++c) {
         uint32_t v[32];
         tc::tmem_ld32(trow + 32 * c, v);
-        tc::tmem_ld_wait();
+        tc::tmem_ld_wait(v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) red[row * S::red_ld + 32 * c + j] = __uint_as_float(v[j]);
       }
       __syncthreads();
       if (ctx.n_valid > 0) epi(red, S::red_ld, ctx, extra);
     } else {
+      // Each CTA writes its fp32 partial, slice-major ([SPLIT][128][W + 4]),
+      // into its own shared memory; after a cluster barrier CTA z sums slice
+      // z over the cluster in rank order through distributed shared memory.
       float *part = (float *)base;
       float *red = (float *)(base + S::part);
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
         uint32_t v[32];
         tc::tmem_ld32(trow + 32 * c, v);
-        tc::tmem_ld_wait();
+        tc::tmem_ld_wait(v);
         const int sl = (32 * c) / W, o = 32 * c - sl * W;
         float4 *dst = (float4 *)(part + ((size_t)sl * 128 + row) * S::part_ld + o);
 #pragma unroll
@@ -457,7 +473,7 @@ __global__ void __launch_bounds__(128, 1)
       }
       tc::cluster_sync();
     }
-    // The next item's MMAs overwrite the accumulator and its copies the
+    // The next unit's MMAs overwrite the accumulator and its copies the
     // shared memory the epilogue used.
     tc::fence_before();
     __syncthreads();
@@ -476,11 +492,11 @@ __global__ void __launch_bounds__(128, 1)
 cudaError_t make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
                            uint32_t box_rows);
 
-// Split-K launch: grid (ceil(M / 128), grid_y, SPLIT), clusters of (1, 1, SPLIT).
-// Grouped launches (g.work set) walk the work list with stride grid_y.
+// Split-K launch: n_clusters clusters of SPLIT CTAs (grid.x = n_clusters *
+// SPLIT, cluster dims (SPLIT, 1, 1)); the clusters walk the output units.
 template <int SPLIT, class Epi>
 cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
-                         const Epi &epi, int grid_y, cudaStream_t st) {
+                         const Epi &epi, int n_clusters, cudaStream_t st) {
   using S = tc::SkSmem<SPLIT, Epi>;
   static_assert(S::bytes <= 232448, "shared memory of the split-K GEMM");
   auto kern = tc_gemm_sk_kernel<SPLIT, Epi>;
@@ -494,9 +510,9 @@ cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcA
     if (dev < 64) attr_set |= 1ull << dev;
   }
   if (g.K % tc::kBK || g.K / tc::kBK < SPLIT) return cudaErrorInvalidValue;
-  if (grid_y <= 0 || g.M <= 0) return cudaSuccess;
+  if (n_clusters <= 0 || g.M <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ceil_div(g.M, 128), grid_y, SPLIT);
+  cfg.gridDim = dim3(n_clusters * SPLIT, 1, 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = S::bytes;
   cfg.stream = st;
@@ -509,9 +525,9 @@ cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcA
   }
   if (SPLIT > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.x = SPLIT;
     attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = SPLIT;
+    attr[na].val.clusterDim.z = 1;
     ++na;
   }
   cfg.attrs = attr;

@@ -25,14 +25,22 @@ cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, floa
                         cudaStream_t st);
 // Sorts the T*k (token, slot) pairs by expert.  Outputs: offs[E+1], perm_tok[T*k]
 // (token of each sorted row), slot_row[T*k] (sorted row of pair t*k+s),
-// work[2*max_work] = (expert, first row) tiles of `tile_rows`, *n_work.  The
-// per-pair ranks are kept behind the work list: `work` holds
-// 2 * moe_max_work() + T*k ints.
+// work[2*max_work] = (expert, first row) items of up to `tile_rows` rows,
+// *n_work.  `work` holds moe_work_ints() ints: the item list, then one
+// counter per item and a unit counter used by moe_ffn, all zeroed here.
 // stats (optional, device, 2 x u64): += experts with at least one row, += T*k.
+// max_work: the item capacity the work buffer was sized for (moe_max_work of
+// the largest T it serves); moe_ffn must be given the same value.
 cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
-                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st,
-                        unsigned long long *stats = nullptr);
+                        int *perm_tok, int *slot_row, int *work, int *n_work, int max_work,
+                        cudaStream_t st, unsigned long long *stats = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
+size_t moe_work_ints(int T, int k, int E, int tile_rows);
+// Routed experts of one layer (kernels_moe.cu): act = SwiGLU(x_perm Wg^T, x_perm Wu^T),
+// y = act Wd^T, for every work item of moe_permute; one persistent launch.
+cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
+                    const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act,
+                    float *y, int *err, cudaStream_t st);
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
 cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
@@ -54,13 +62,7 @@ cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, f
                           cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
 cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
                            cudaStream_t st);  // out[T][N] = act . w^T
-constexpr int kExpertTileRows = 256;  // token rows per expert GEMM work item (MMA N <= 256)
-cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, const int *offs,
-                                const int *work, const int *n_work, int max_work, int E, int d,
-                                int F, bf16 *act, int *err, cudaStream_t st);
-cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const int *offs,
-                             const int *work, const int *n_work, int max_work, int E, int d, int F,
-                             float *y, int *err, cudaStream_t st);
+constexpr int kExpertTileRows = 128;  // token rows per expert work item (MMA N <= 128)
 // xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
 // the logits are then w_out . (xn + xn_lo).
 // dyn (optional, device): stream words taken from memory instead of seed/canvas/step.

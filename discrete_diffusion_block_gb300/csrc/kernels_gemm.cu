@@ -182,42 +182,6 @@ struct EpiStore {
   }
 };
 
-// silu(g) * u with the hardware exp and a fast divide; the product is rounded
-// to bf16 right after, far coarser than either approximation.
-__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
-
-// SwiGLU on a 128-row tile holding 64 gate rows then the matching 64 up rows;
-// each lane writes two adjacent outputs as bf16x2, four tokens per step.
-struct EpiSwiGlu {
-  static constexpr size_t extra_smem = 0;
-  bf16 *act;
-  int F;
-  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    const int fb = c.m0 / 128;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int j = 2 * lane;
-    bf16 *base = act + (size_t)(c.b_base + c.n0) * F + fb * 64 + j;
-    for (int tb = warp; tb < c.n_valid; tb += 4 * nw) {
-      float g0[4], g1[4], u0[4], u1[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int t = min(tb + q * nw, c.n_valid - 1);
-        g0[q] = tile[j * ldc + t];
-        g1[q] = tile[(j + 1) * ldc + t];
-        u0[q] = tile[(64 + j) * ldc + t];
-        u1[q] = tile[(65 + j) * ldc + t];
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int t = tb + q * nw;
-        if (t < c.n_valid)
-          *(__nv_bfloat162 *)(base + (size_t)t * F) =
-              __floats2bfloat162_rn(swiglu(g0[q], u0[q]), swiglu(g1[q], u1[q]));
-      }
-    }
-  }
-};
-
 TcArgs targs(int M, int N, int K, int *err) {
   TcArgs g{};
   g.M = M;
@@ -310,28 +274,6 @@ cudaError_t tmap_bf16_cached(CUtensorMap *map, const void *ptr, uint64_t rows, u
 
 // Projections: A = weights [M][K] (rows = output features), B = activations
 // [T][K]; the tile is [feature][token].
-cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o,
-                     int *err, cudaStream_t st) {
-  const int M = (o.Hq + 2 * o.Hkv) * o.hd;
-  CUtensorMap ta, tb;
-  TMAP(ta, wqkv, M, d, 128);
-  TMAP(tb, xn, T, d, 64);
-  if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd) return cudaErrorInvalidValue;
-  EpiQkv epi{o};
-  const TcArgs g = targs(M, T, d, err);
-  const int gy = ceil_div(T, tc::kSkBN), kt = d / tc::kBK;
-  if (kt >= 4) return launch_tc_sk<4>(ta, tb, g, epi, gy, st);
-  return launch_tc_sk<1>(ta, tb, g, epi, gy, st);
-}
-
-// Split choice for a plain projection: the largest of 8, 4, 2, 1 that keeps at
-// least two K tiles per split and at most ~one wave of CTAs.
-static int pick_split(int m_tiles, int n_tiles, int kt) {
-  int s = 8;
-  while (s > 1 && (kt < 2 * s || m_tiles * n_tiles * s > 160)) s >>= 1;
-  return s;
-}
-
 // Streaming multiprocessors of the current device (cached per device).
 static int num_sms() {
   static int cached[64] = {0};
@@ -345,23 +287,45 @@ static int num_sms() {
   return cached[dev];
 }
 
-// Clusters along y of a grouped launch: at most one CTA per SM in total, so
-// that every CTA is resident from the start.
-static int grouped_grid_y(int ctas_per_item, int max_work) {
-  int gy = num_sms() / ctas_per_item;
-  if (gy > max_work) gy = max_work;
-  return gy < 1 ? 1 : gy;
+// Clusters for a launch with a known number of output units: one CTA per SM
+// at most, no more clusters than units.
+static int plain_clusters(int units, int split) {
+  int nc = num_sms() / split;
+  if (nc > units) nc = units;
+  return nc < 1 ? 1 : nc;
+}
+
+// Split for a plain projection: the largest of 8, 4, 2, 1 that keeps at least
+// two K tiles per split and every CTA resident at once.
+static int pick_split(int units, int kt) {
+  int s = 8;
+  while (s > 1 && (kt < 2 * s || units * s > num_sms())) s >>= 1;
+  return s;
 }
 
 template <class Epi>
 static cudaError_t launch_split(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
-                                const Epi &epi, int grid_y, int split, cudaStream_t st) {
+                                const Epi &epi, int n_clusters, int split, cudaStream_t st) {
   switch (split) {
-    case 8: return launch_tc_sk<8>(ta, tb, g, epi, grid_y, st);
-    case 4: return launch_tc_sk<4>(ta, tb, g, epi, grid_y, st);
-    case 2: return launch_tc_sk<2>(ta, tb, g, epi, grid_y, st);
-    default: return launch_tc_sk<1>(ta, tb, g, epi, grid_y, st);
+    case 8: return launch_tc_sk<8>(ta, tb, g, epi, n_clusters, st);
+    case 4: return launch_tc_sk<4>(ta, tb, g, epi, n_clusters, st);
+    case 2: return launch_tc_sk<2>(ta, tb, g, epi, n_clusters, st);
+    default: return launch_tc_sk<1>(ta, tb, g, epi, n_clusters, st);
   }
+}
+
+cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o,
+                     int *err, cudaStream_t st) {
+  const int M = (o.Hq + 2 * o.Hkv) * o.hd;
+  CUtensorMap ta, tb;
+  TMAP(ta, wqkv, M, d, 128);
+  TMAP(tb, xn, T, d, 64);
+  if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd) return cudaErrorInvalidValue;
+  EpiQkv epi{o};
+  const TcArgs g = targs(M, T, d, err);
+  const int units = ceil_div(M, 128) * ceil_div(T, tc::kSkBN), kt = d / tc::kBK;
+  if (kt >= 4) return launch_tc_sk<4>(ta, tb, g, epi, plain_clusters(units, 4), st);
+  return launch_tc_sk<1>(ta, tb, g, epi, plain_clusters(units, 1), st);
 }
 
 cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
@@ -370,8 +334,9 @@ cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, f
   TMAP(ta, w, N, K, 128);
   TMAP(tb, act, T, K, 64);
   EpiResidual epi{h, N};
-  const int gy = ceil_div(T, tc::kSkBN);
-  return launch_split(ta, tb, targs(N, T, K, err), epi, gy, pick_split(ceil_div(N, 128), gy, K / tc::kBK), st);
+  const int units = ceil_div(N, 128) * ceil_div(T, tc::kSkBN);
+  const int split = pick_split(units, K / tc::kBK);
+  return launch_split(ta, tb, targs(N, T, K, err), epi, plain_clusters(units, split), split, st);
 }
 
 cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
@@ -380,42 +345,9 @@ cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, 
   TMAP(ta, w, N, K, 128);
   TMAP(tb, act, T, K, 64);
   EpiStore epi{out, N};
-  const int gy = ceil_div(T, tc::kSkBN);
-  return launch_split(ta, tb, targs(N, T, K, err), epi, gy, pick_split(ceil_div(N, 128), gy, K / tc::kBK), st);
-}
-
-// Experts: A = the expert's weight rows (2-D view over all experts), B = the
-// expert's routed rows, packed contiguously in expert order, up to
-// kExpertTileRows per work item.
-cudaError_t gemm_expert_gate_up(const bf16 *x_perm, int rows, const bf16 *wgu, const int *offs,
-                                const int *work, const int *n_work, int max_work, int E, int d,
-                                int F, bf16 *act, int *err, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  TMAP(ta, wgu, (uint64_t)E * 2 * F, d, 128);
-  TMAP(tb, x_perm, rows, d, 64);
-  TcArgs g = targs(2 * F, 0, d, err);
-  g.a_group_rows = 2 * F;
-  g.work = work;
-  g.n_work = n_work;
-  g.group_offs = offs;
-  EpiSwiGlu epi{act, F};
-  const int split = d / tc::kBK >= 8 ? 2 : 1;
-  return launch_split(ta, tb, g, epi, grouped_grid_y(ceil_div(2 * F, 128) * split, max_work), split, st);
-}
-
-cudaError_t gemm_expert_down(const bf16 *act, int rows, const bf16 *wd, const int *offs,
-                             const int *work, const int *n_work, int max_work, int E, int d, int F,
-                             float *y, int *err, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  TMAP(ta, wd, (uint64_t)E * d, F, 128);
-  TMAP(tb, act, rows, F, 64);
-  TcArgs g = targs(d, 0, F, err);
-  g.a_group_rows = d;
-  g.work = work;
-  g.n_work = n_work;
-  g.group_offs = offs;
-  EpiStore epi{y, d};
-  return launch_split(ta, tb, g, epi, grouped_grid_y(ceil_div(d, 128), max_work), 1, st);
+  const int units = ceil_div(N, 128) * ceil_div(T, tc::kSkBN);
+  const int split = pick_split(units, K / tc::kBK);
+  return launch_split(ta, tb, targs(N, T, K, err), epi, plain_clusters(units, split), split, st);
 }
 
 }  // namespace dg

@@ -215,7 +215,8 @@ constexpr int kPermThreads = 1024, kPermWarps = kPermThreads / 32;
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, int TK, int k, int E,
                                                                int tile_rows, int *offs,
                                                                int *perm_tok, int *slot_row,
-                                                               int *work, int *n_work,
+                                                               int *work, int *n_work, int *sync,
+                                                               int max_work,
                                                                unsigned long long *stats) {
   pdl_wait();
   pdl_trigger();
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, i
       work[2 * (toff[e] + j) + 1] = j * tile_rows;
     }
   }
+  for (int i = threadIdx.x; i <= max_work; i += kPermThreads) sync[i] = 0;  // per-item counters, unit counter
 }
 
 // h[t] (+)= sum_s gate[t][s] * y[slot_row[t*k+s]], slots in ascending order.
@@ -462,12 +464,15 @@ size_t moe_max_work(int T, int k, int E, int tile_rows) {
   return (size_t)(T * k + tile_rows - 1) / tile_rows + E;
 }
 
+size_t moe_work_ints(int T, int k, int E, int tile_rows) { return 3 * moe_max_work(T, k, E, tile_rows) + 1; }
+
 cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
-                        int *perm_tok, int *slot_row, int *work, int *n_work, cudaStream_t st,
-                        unsigned long long *stats) {
+                        int *perm_tok, int *slot_row, int *work, int *n_work, int max_work,
+                        cudaStream_t st, unsigned long long *stats) {
   if (E > 256) return cudaErrorInvalidValue;
+  if ((size_t)max_work < moe_max_work(T, k, E, tile_rows)) return cudaErrorInvalidValue;
   return launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), 0, st, ids, T * k, k, E, tile_rows, offs,
-                    perm_tok, slot_row, work, n_work, stats);
+                    perm_tok, slot_row, work, n_work, work + 2 * max_work, max_work, stats);
 }
 
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,

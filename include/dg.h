@@ -212,7 +212,7 @@ int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, siz
 /* Kernel classes of the decoder, for per-class timing and launch counts. */
 enum {
     DG_K_EMBED = 0, DG_K_RMSNORM, DG_K_QKV_ROPE, DG_K_ATTENTION, DG_K_O_PROJ, DG_K_ROUTER,
-    DG_K_TOPK, DG_K_PERMUTE, DG_K_EXPERT_GATE_UP, DG_K_EXPERT_DOWN, DG_K_COMBINE, DG_K_LM_HEAD,
+    DG_K_TOPK, DG_K_PERMUTE, DG_K_EXPERT_FFN, DG_K_COMBINE, DG_K_LM_HEAD,
     DG_K_SAMPLER_MERGE, DG_K_SAMPLER_RULE, DG_K_CANVAS_INIT, DG_K_CLASSES
 };
 const char *dg_kernel_class_name(int32_t cls);

@@ -196,6 +196,6 @@ def test_profile_counts_launches():
     dgp.dg_profile(m, 1)
     dgp.dg_denoise_step(m)
     prof = dgp.dg_profile_read(m)
-    assert prof["expert_gate_up"][1] == 2 and prof["lm_head"][1] == 1
-    assert all(ms >= 0 for ms, _ in prof.values()) and prof["expert_gate_up"][0] > 0
+    assert prof["expert_ffn"][1] == 2 and prof["lm_head"][1] == 1
+    assert all(ms >= 0 for ms, _ in prof.values()) and prof["expert_ffn"][0] > 0
     m.close()
