@@ -281,9 +281,11 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
   const dg_config &c = m->cfg;
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim;
   cudaStream_t st = m->stream;
+  const bool fuse_norm = d <= 4096;  // the MoE combine also writes the next layer's input norm
   for (int L = 0; L < c.n_layers; ++L) {
     const Layer &W = m->layers[L];
-    KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.attn_norm, T, d, c.rms_eps, st));
+    if (L == 0 || !fuse_norm)
+      KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.attn_norm, T, d, c.rms_eps, st));
     dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), m->page_table, pos0, c.page_size,
                   c.n_q_heads, c.n_kv_heads, c.head_dim, m->cos_t, m->sin_t};
     int *err = m->done_dev + 1;
@@ -295,9 +297,9 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
                      m->attn_ws_bytes, st));
     KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, st));
     KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.moe_norm, T, d, c.rms_eps, st));
-    KL(DG_K_ROUTER, 1, dg::gemm_store_f32(m->xn, W.wr, T, d, c.n_experts, m->router, err, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
+    KL(DG_K_ROUTER, 1, dg::gemm_store_f32(m->xn, W.wr, T, d, c.n_experts, m->router, err, st));
     KL(DG_K_TOPK, 1, dg::router_topk(m->router, T, c.n_experts, c.top_k, topk, m->gates, st));
     KL(DG_K_PERMUTE, 1,
        dg::moe_permute(topk, T, c.top_k, c.n_experts, dg::kExpertTileRows, m->offs, m->perm_tok,
@@ -307,7 +309,13 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     KL(DG_K_EXPERT_FFN, 1,
        dg::moe_ffn(m->x_perm, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
                    c.n_experts, d, c.d_ff, m->act, m->y, err, st));
-    KL(DG_K_COMBINE, 1, dg::moe_combine(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, true, st));
+    if (fuse_norm && L + 1 < c.n_layers) {
+      KL(DG_K_COMBINE, 1,
+         dg::moe_combine_norm(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, m->layers[L + 1].attn_norm,
+                              c.rms_eps, m->xn, st));
+    } else {
+      KL(DG_K_COMBINE, 1, dg::moe_combine(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, true, st));
+    }
   }
   return DG_OK;
 }
@@ -1013,8 +1021,7 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   MoeWs w = moe_layout(workspace, T, d, n_experts, top_k, d_ff);
   if (workspace_bytes < w.bytes) return fail(DG_EINVAL, "workspace too small");
   cudaStream_t st = (cudaStream_t)stream;
-  CK(dg::gemm_store_f32((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, w.router,
-                        nullptr, st));
+  CK(dg::gemm_store_f32((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, w.router, nullptr, st));
   CK(dg::router_topk(w.router, T, n_experts, top_k, expert_ids, gates, st));
   CK(dg::moe_permute(expert_ids, T, top_k, n_experts, dg::kExpertTileRows, w.offs, w.perm_tok,
                      w.slot_row, w.work, w.n_work, w.max_work, st));

@@ -43,6 +43,12 @@ cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *w
                     float *y, int *err, cudaStream_t st);
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
+// h[t] += sum_s gate * y (as moe_combine with accumulate), then the RMSNorm of
+// the updated row with `gain` into xn (bf16): the next layer's input norm.
+// d <= 4096.
+cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const int *slot_row,
+                             int T, int k, int d, const float *gain, float eps, bf16 *xn,
+                             cudaStream_t st);
 cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
                       const int *page_table, int L, int n_pages, int pos0, int n, int Hkv, int hd,
                       int pg, cudaStream_t st);

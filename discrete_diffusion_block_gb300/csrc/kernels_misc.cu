@@ -350,6 +350,71 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
   }
 }
 
+// combine_kernel followed by the RMSNorm of the updated row (the next
+// layer's input norm, same formula as rmsnorm_kernel): the row stays in
+// registers between the two.  d4 <= 4 * 256.
+constexpr int kCombNormVec = 4;
+__global__ void __launch_bounds__(256) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
+                                                           const int *slot_row, int k, int d4,
+                                                           const float *gain, float eps, bf16 *xn) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  __shared__ float g_s[16];
+  __shared__ int r_s[16];
+  __shared__ float red[8];
+  if (threadIdx.x < k) {
+    g_s[threadIdx.x] = gates[(size_t)t * k + threadIdx.x];
+    r_s[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  float4 hv[kCombNormVec];
+  float ss = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kCombNormVec; ++u) {
+    const int c = threadIdx.x + 256 * u;
+    hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < d4) {
+      float4 v[16];
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s < k) v[s] = y[(size_t)r_s[s] * d4 + c];
+      const float4 acc = h[(size_t)t * d4 + c];
+      float4 mo = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s < k) {
+          mo.x += g_s[s] * v[s].x;
+          mo.y += g_s[s] * v[s].y;
+          mo.z += g_s[s] * v[s].z;
+          mo.w += g_s[s] * v[s].w;
+        }
+      hv[u] = make_float4(acc.x + mo.x, acc.y + mo.y, acc.z + mo.z, acc.w + mo.w);
+      h[(size_t)t * d4 + c] = hv[u];
+      ss += hv[u].x * hv[u].x + hv[u].y * hv[u].y + hv[u].z * hv[u].z + hv[u].w * hv[u].w;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (4 * d4) + eps);
+  const float4 *g4 = (const float4 *)gain;
+  __nv_bfloat162 *o2 = (__nv_bfloat162 *)(xn + (size_t)t * 4 * d4);
+#pragma unroll
+  for (int u = 0; u < kCombNormVec; ++u) {
+    const int c = threadIdx.x + 256 * u;
+    if (c < d4) {
+      const float4 gg = g4[c];
+      o2[2 * c] = __floats2bfloat162_rn(hv[u].x * inv * gg.x, hv[u].y * inv * gg.y);
+      o2[2 * c + 1] = __floats2bfloat162_rn(hv[u].z * inv * gg.z, hv[u].w * inv * gg.w);
+    }
+  }
+}
+
 // x_perm[j] = xn[perm_tok[j]]: the routed rows in expert order, so that each
 // expert's rows are one contiguous TMA box source.
 __global__ void gather_rows_kernel(uint4 *dst, const uint4 *src, const int *perm_tok, int rows,
@@ -481,6 +546,15 @@ cudaError_t moe_combine(float *h, const float *y, const float *gates, const int 
   if (k > 16 || d % 4) return cudaErrorInvalidValue;
   return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const float4 *)y, gates, slot_row, k,
                     d / 4, accumulate ? 1 : 0);
+}
+
+cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const int *slot_row,
+                             int T, int k, int d, const float *gain, float eps, bf16 *xn,
+                             cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  if (k > 16 || d % 4 || d > 4 * 256 * kCombNormVec) return cudaErrorInvalidValue;
+  return launch_pdl(combine_norm_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const float4 *)y, gates,
+                    slot_row, k, d / 4, gain, eps, xn);
 }
 
 cudaError_t gather_rows(bf16 *x_perm, const bf16 *xn, const int *perm_tok, int rows, int d,

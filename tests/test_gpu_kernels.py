@@ -197,7 +197,8 @@ def test_canvas_attention_against_fp64(P, causal, Hq, Hkv, hd):
 
 # ---- mixture of experts -----------------------------------------------------------
 
-@pytest.mark.parametrize("T,d,E,k,F", [(256, 256, 8, 2, 512), (77, 256, 8, 2, 512), (256, 2816, 128, 8, 704)])
+@pytest.mark.parametrize("T,d,E,k,F", [(256, 256, 8, 2, 512), (77, 256, 8, 2, 512), (256, 2816, 128, 8, 704),
+                                       (64, 256, 200, 4, 128)])
 def test_moe_against_fp64(T, d, E, k, F):
     wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
     wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
