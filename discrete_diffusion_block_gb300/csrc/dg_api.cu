@@ -291,10 +291,10 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     int *err = m->done_dev + 1;
     KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xn, W.wqkv, T, d, qo, err, st));
     if (kv_only_last && L == c.n_layers - 1) break;
-    dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal};
+    dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal, m->n_pages};
     KL(DG_K_ATTENTION, dg::attention_launch_count(as),
        dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
-                     m->attn_ws_bytes, st));
+                     m->attn_ws_bytes, st, err));
     KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, st));
     KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.moe_norm, T, d, c.rms_eps, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
@@ -364,6 +364,10 @@ int alloc_model(dg_model *m) {
   m->layer_pool_elems = (size_t)m->n_pages * kd * c.page_size;
   CKR(m->alloc(&m->k_pool, m->layer_pool_elems * c.n_layers));
   CKR(m->alloc(&m->v_pool, m->layer_pool_elems * c.n_layers));
+  // cache slots never written yet are read (and weighted by zero) at the tail
+  // of a key tile: they must hold finite values
+  CK(cudaMemset(m->k_pool, 0, m->layer_pool_elems * c.n_layers * sizeof(bf16)));
+  CK(cudaMemset(m->v_pool, 0, m->layer_pool_elems * c.n_layers * sizeof(bf16)));
   CKR(m->alloc(&m->page_table, m->n_pages));
   m->page_table_host.resize(m->n_pages);
   for (int i = 0; i < m->n_pages; ++i) m->page_table_host[i] = i;  // single request: in order

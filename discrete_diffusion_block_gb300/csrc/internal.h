@@ -95,6 +95,7 @@ cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel
 // ---- attention (kernels_attn.cu) -------------------------------------------
 struct AttnShape {
   int n_prefix, n_new, Hq, Hkv, hd, pg, causal;
+  int n_pages = 0;  // physical pages of the pools when known (0: unknown)
 };
 size_t attention_workspace_bytes(const AttnShape &s);
 int attention_launch_count(const AttnShape &s);
@@ -103,7 +104,9 @@ int attention_launch_count(const AttnShape &s);
 // first use per device).
 constexpr size_t kAttentionFixedScratchBytes = (size_t)16 << 20;
 cudaError_t attention_fixed_scratch(void **ptr);
+// err (optional, device): error word set when a bounded wait of the kernel gives up.
 cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const int *page_table,
-                      const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st);
+                      const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st,
+                      int *err = nullptr);
 
 }  // namespace dg

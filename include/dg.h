@@ -256,7 +256,10 @@ int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor
  *   q        device bf16 [n_new][Hq][hd] (already rotated)
  *   k_pool,
  *   v_pool   device bf16 [n_pages][Hkv][page_size][hd]; key j lives in physical
- *            page page_table[j / page_size], slot j % page_size
+ *            page page_table[j / page_size], slot j % page_size.  Keys are
+ *            read in 64-key groups: the slots after the last key in its
+ *            group (same page) are read too, weighted by zero, and must hold
+ *            finite values (e.g. a zero-initialised pool)
  *   page_table device int32, >= ceil((n_prefix + n_new) / page_size) entries
  *   out      device bf16 [n_new][Hq][hd]
  * workspace: device scratch of dg_op_attention_workspace_bytes() bytes (the
@@ -278,9 +281,11 @@ int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint
  *
  * The split-KV scratch lives in a fixed 16 MiB device array inside the
  * library (held by every GPU that loads it until the process exits); no
- * device memory is allocated or freed by this call.  Shapes whose scratch
- * (dg_op_attention_workspace_bytes) exceeds 16 MiB return DG_EINVAL with the
- * required size in dg_last_error().  The first call on a device looks up the
+ * device memory is allocated or freed by this call.  The split plan sizes
+ * the key splits for about one wave of blocks, which keeps the scratch near
+ * 10 MiB at most for any shape; a shape whose scratch
+ * (dg_op_attention_workspace_bytes) exceeded 16 MiB would return DG_EINVAL
+ * with the required size in dg_last_error().  The first call on a device looks up the
  * array's device address, with that device current; make that first call
  * before any stream capture.  All calls share the one array and it keeps the
  * previous call's contents (every value the kernels read is written earlier
