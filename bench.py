@@ -219,6 +219,13 @@ def decode_all(dgp, m, seed, scfg):
     return Ns, Cs
 
 
+# DRAM traffic / algorithmic bytes of the expert-FFN kernel, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 128-expert MoE
+# layer shape of `--micro moe`; the decoder's launches touch fewer experts and
+# their traffic is this ratio times their algorithmic bytes.
+FFN_TRAFFIC_RATIO = 1.5673e9 / 1.5634e9
+
+
 def expert_bytes(cfg, experts_per_launch, rows_per_launch):
     """Algorithmic DRAM bytes of one expert-FFN launch (gate/up, SwiGLU and
     down of every routed expert): the gate/up and down weights of every expert
@@ -324,8 +331,10 @@ def gpu_arm(args):
         dom = "expert_ffn"
         kms, n = prof[dom]
         achieved = per_launch[dom] / (kms / 1e3 / n) / 1e9
+        traffic = args.traffic if args.traffic is not None else round(FFN_TRAFFIC_RATIO * per_launch[dom])
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": args.traffic,
+                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                    "traffic_source": "ncu dram bytes of the 128-expert layer, scaled by experts touched",
                     "peak_source": f"{peak_src} hbm_gbs",
                     "algorithmic_bytes_per_launch": round(per_launch[dom]), "measured_in": measured_in}
 
