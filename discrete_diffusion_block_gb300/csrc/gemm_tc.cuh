@@ -89,14 +89,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
-// L2 prefetch of one A box: raises the DRAM requests in flight beyond what
-// the shared-memory ring holds.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"((uint64_t)map),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -216,7 +208,6 @@ __device__ __forceinline__ void cluster_sync() {
 
 constexpr int kSkBN = 256;           // B rows per tile (MMA N upper bound)
 constexpr int kSkStages = 4;
-constexpr int kSkPrefetch = 12;      // A boxes kept in flight to L2 ahead of the ring
 constexpr uint32_t kBChunkBytes = 64 * 128;  // one 64-row B box
 
 template <int SPLIT, class Epi>
@@ -341,11 +332,7 @@ __global__ void __launch_bounds__(128, 1)
 
     if (warp == 0 && lane == 0) {
       int issued = it;
-      if (unit == cluster)  // first unit: nothing was prefetched for it yet
-        for (int kt = kb + STAGES; kt < min(ke, kb + tc::kSkPrefetch); ++kt)
-          tc::tma_prefetch_2d(&ta, kt * tc::kBK, a_row);
       for (int kt = kb; kt < ke; ++kt, ++issued) {
-        if (kt + tc::kSkPrefetch < ke) tc::tma_prefetch_2d(&ta, (kt + tc::kSkPrefetch) * tc::kBK, a_row);
         const int s = issued % STAGES, r = issued / STAGES;
         if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 1, abort);
         if (*abort) break;
@@ -355,13 +342,6 @@ __global__ void __launch_bounds__(128, 1)
         }
         for (int c = 0; c < nb; ++c)
           tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, &tb, kt * tc::kBK, b_row + 64 * c, full + s);
-      }
-      const int nu = unit + n_clusters;
-      if (nu < n_units && !*abort) {
-        // The next unit's first A boxes go to L2 while this one finishes.
-        const int ny = nu / m_tiles, nmt = nu - ny * m_tiles;
-        const int na_row = (g.work ? g.work[2 * ny] * g.a_group_rows : 0) + nmt * 128;
-        for (int kt = kb; kt < min(ke, kb + tc::kSkPrefetch); ++kt) tc::tma_prefetch_2d(&ta, kt * tc::kBK, na_row);
       }
       if (*abort) {
         // Drain: wait (bounded) for the last copy issued into each stage.

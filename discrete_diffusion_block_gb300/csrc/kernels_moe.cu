@@ -37,18 +37,19 @@ namespace dg {
 
 namespace {
 
-constexpr int kFfnStages = 4;
+constexpr int kFfnStages = 6;
 constexpr int kFfnThreads = 192;
 constexpr int kFfnBN = kExpertTileRows;  // rows per item = MMA N upper bound
 constexpr int kFfnQueue = 4;
 constexpr uint32_t kFfnABytes = 128 * 128;
 constexpr uint32_t kFfnBBytes = kFfnBN * 128;
 constexpr uint32_t kFfnStageBytes = kFfnABytes + kFfnBBytes;
-constexpr int kFfnLdc = kFfnBN + 1;
+constexpr int kFfnEpiCols = 64;            // accumulator columns (rows of the item) per epilogue pass
+constexpr int kFfnLdc = kFfnEpiCols + 1;
 
 struct FfnSmem {
   static constexpr size_t ring = (size_t)kFfnStages * kFfnStageBytes;
-  static constexpr size_t tile = ring;                                   // fp32 [128][kFfnLdc]
+  static constexpr size_t tile = ring;                                   // fp32 [128][kFfnLdc]: 64 columns at a time
   static constexpr size_t queue = tile + (size_t)128 * kFfnLdc * 4;      // UnitInfo [kFfnQueue]
   static constexpr size_t bars = (queue + kFfnQueue * 32 + 15) & ~(size_t)15;
   // full[S], empty[S], acc_full[2], acc_empty[2], q_full[Q], q_empty[Q]; TMEM address; abort flag
@@ -170,7 +171,6 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         const int KT = inf.phase ? KTB : KTA;
         const int nb = (inf.n_valid + 63) >> 6;
         const uint32_t tx = kFfnABytes + (uint32_t)nb * tc::kBChunkBytes;
-        for (int kt = 0; kt < min(KT, tc::kSkPrefetch); ++kt) tc::tma_prefetch_2d(ma, kt * tc::kBK, inf.a_row);
         if (inf.phase) {
           // the item's act rows: every phase A unit of it must have published
           const long long t0 = clock64();
@@ -185,7 +185,6 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           asm volatile("fence.proxy.async.global;\n" ::: "memory");
         }
         for (int kt = 0; kt < KT; ++kt, ++it) {
-          if (kt + tc::kSkPrefetch < KT) tc::tma_prefetch_2d(ma, (kt + tc::kSkPrefetch) * tc::kBK, inf.a_row);
           const int s = it % kFfnStages, r = it / kFfnStages;
           if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 23, abort);
           if (*abort) break;
@@ -244,65 +243,73 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
       const int buf = n & 1;
       tc::mbar_wait(acc_full + buf, (n >> 1) & 1, g.err, 28, abort);
       tc::fence_after();
-      const int nchunks = (inf.n_valid + 31) >> 5;
       const uint32_t trow = tmem + buf * kFfnBN + ((uint32_t)(warp * 32) << 16);
+      // 64 accumulator columns (item rows) per pass through the fp32 tile
+      for (int h0 = 0; h0 < inf.n_valid; h0 += kFfnEpiCols) {
+        const int nh = min(kFfnEpiCols, inf.n_valid - h0);
+        const int nchunks = (nh + 31) >> 5;
 #pragma unroll 1
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld32(trow + 32 * c, v);
-        tc::tmem_ld_wait(v);
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(trow + h0 + 32 * c, v);
+          tc::tmem_ld_wait(v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) tile[row * kFfnLdc + 32 * c + j] = __uint_as_float(v[j]);
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + buf);  // the accumulator is free for unit n + 2
-      epi_sync();
-      if (inf.phase == 0) {
-        // SwiGLU: rows j and 64 + j hold the gate and up projections of
-        // feature 64 * mt + j; each lane writes two adjacent features.
-        const int j = 2 * lane;
-        bf16 *dst = g.act + (size_t)inf.b_row * g.F + inf.mt * 64 + j;
-        for (int tb = warp; tb < inf.n_valid; tb += 16) {
-          float g0[4], g1[4], u0[4], u1[4];
+          for (int j = 0; j < 32; ++j) tile[row * kFfnLdc + 32 * c + j] = __uint_as_float(v[j]);
+        }
+        if (h0 + kFfnEpiCols >= inf.n_valid) {  // last pass: the accumulator is free for unit n + 2
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty + buf);
+        }
+        epi_sync();
+        if (inf.phase == 0) {
+          // SwiGLU: rows j and 64 + j hold the gate and up projections of
+          // feature 64 * mt + j; each lane writes two adjacent features.
+          const int j = 2 * lane;
+          bf16 *dst = g.act + (size_t)(inf.b_row + h0) * g.F + inf.mt * 64 + j;
+          for (int tb = warp; tb < nh; tb += 16) {
+            float g0[4], g1[4], u0[4], u1[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int t = min(tb + 4 * k, inf.n_valid - 1);
-            g0[k] = tile[j * kFfnLdc + t];
-            g1[k] = tile[(j + 1) * kFfnLdc + t];
-            u0[k] = tile[(64 + j) * kFfnLdc + t];
-            u1[k] = tile[(65 + j) * kFfnLdc + t];
+            for (int k = 0; k < 4; ++k) {
+              const int t = min(tb + 4 * k, nh - 1);
+              g0[k] = tile[j * kFfnLdc + t];
+              g1[k] = tile[(j + 1) * kFfnLdc + t];
+              u0[k] = tile[(64 + j) * kFfnLdc + t];
+              u1[k] = tile[(65 + j) * kFfnLdc + t];
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int t = tb + 4 * k;
+              if (t < nh)
+                *(__nv_bfloat162 *)(dst + (size_t)t * g.F) =
+                    __floats2bfloat162_rn(swiglu_f(g0[k], u0[k]), swiglu_f(g1[k], u1[k]));
+            }
           }
+        } else {
+          // y[row][feature] = tile: lanes walk features, four tokens per step
+          float *dst = g.y + (size_t)(inf.b_row + h0) * g.d + inf.mt * 128;
+          for (int tb = warp; tb < nh; tb += 16) {
+            float v[4][4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int t = tb + 4 * k;
-            if (t < inf.n_valid)
-              *(__nv_bfloat162 *)(dst + (size_t)t * g.F) =
-                  __floats2bfloat162_rn(swiglu_f(g0[k], u0[k]), swiglu_f(g1[k], u1[k]));
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int f4 = 0; f4 < 4; ++f4) v[k][f4] = tile[(32 * f4 + lane) * kFfnLdc + min(tb + 4 * k, nh - 1)];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int t = tb + 4 * k;
+              if (t < nh)
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) dst[(size_t)t * g.d + 32 * f4 + lane] = v[k][f4];
+            }
           }
         }
+        epi_sync();  // the tile is free for the next pass
+      }
+      if (inf.phase == 0) {
         __threadfence();
         asm volatile("fence.proxy.async.global;\n" ::: "memory");
         epi_sync();
         if (threadIdx.x == 0) atomicAdd(g.done + inf.item, 1);  // publish after every thread's stores
-      } else {
-        // y[row][feature] = tile: lanes walk features, four tokens per step
-        float *dst = g.y + (size_t)inf.b_row * g.d + inf.mt * 128;
-        for (int tb = warp; tb < inf.n_valid; tb += 16) {
-          float v[4][4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int f4 = 0; f4 < 4; ++f4) v[k][f4] = tile[(32 * f4 + lane) * kFfnLdc + min(tb + 4 * k, inf.n_valid - 1)];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int t = tb + 4 * k;
-            if (t < inf.n_valid)
-#pragma unroll
-              for (int f4 = 0; f4 < 4; ++f4) dst[(size_t)t * g.d + 32 * f4 + lane] = v[k][f4];
-          }
-        }
-        epi_sync();
       }
       if (threadIdx.x == 0) mbar_arrive(q_empty + q);
     }
