@@ -7,7 +7,8 @@ denoising budget N = 48, adaptive stopping on, no EOS.
 
 One step = the decode of all 4 canvases from the cached prompt: every
 denoising forward (embed, 30 x {RMSNorm, QKV+RoPE, canvas attention, o-proj,
-RMSNorm, router, top-k, permute, expert SwiGLU GEMMs, combine}, final norm,
+RMSNorm, router, routing (top-k + sort by expert), row gather, fused expert
+FFN, combine}, final norm,
 LM head fused with the vocab reduction, sampler) plus the 3 KV-append
 forwards between canvases.  The prompt is encoded once before timing
 (decode-only, as the pages measure); each step rewinds to it and uses a new
@@ -230,7 +231,7 @@ def expert_bytes(cfg, experts_per_launch, rows_per_launch):
     """Algorithmic DRAM bytes of one expert-FFN launch (gate/up, SwiGLU and
     down of every routed expert): the gate/up and down weights of every expert
     that received a row, once (the count is measured on the device by the
-    permute kernel), the gathered token rows, the SwiGLU activations written
+    routing kernel), the gathered token rows, the SwiGLU activations written
     and read back, and the fp32 outputs."""
     d, F = cfg.d_model, cfg.d_ff
     e, r = experts_per_launch, rows_per_launch
@@ -299,7 +300,7 @@ def gpu_arm(args):
     prof = dgp.dg_profile_read(m)
     touched, routed = dgp.dg_profile_experts(m)
     dgp.dg_profile(m, 0)
-    n_moe = max(prof["permute"][1] // 2, 1)                  # permute + row gather per MoE
+    n_moe = max(prof["route"][1] // 2, 1)                    # routing + row gather per MoE
     per_launch = expert_bytes(cfg, touched / n_moe, routed / n_moe)
     hbm, tf_burst, tf_sust, peak_src = peaks()
     kernels = {}

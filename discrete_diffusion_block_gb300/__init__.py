@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdg.so")
 
 DG_OK, DG_EINVAL, DG_ENOMEM, DG_ECUDA, DG_ESTATE, DG_ECAPACITY, DG_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
-DG_K_CLASSES = 15
+DG_K_CLASSES = 13
 (DG_W_EMBED, DG_W_LM_HEAD, DG_W_FINAL_NORM, DG_W_WQKV, DG_W_WO, DG_W_ROUTER, DG_W_GATE_UP,
  DG_W_DOWN, DG_W_ATTN_NORM, DG_W_MOE_NORM) = range(10)
 

@@ -15,7 +15,7 @@ LIB = os.path.join(HERE, "libdg.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",
          "-prec-sqrt=true", "-Xptxas", "-warn-spills"]
-SOURCES = ["dg_api.cu", "kernels_misc.cu", "kernels_gemm.cu", "kernels_lmhead.cu", "kernels_moe.cu", "kernels_attn.cu", "kernels_sampler.cu"]
+SOURCES = ["dg_api.cu", "kernels_misc.cu", "kernels_gemm.cu", "kernels_lmhead.cu", "kernels_moe.cu", "kernels_route.cu", "kernels_attn.cu", "kernels_sampler.cu"]
 
 
 def nvcc():

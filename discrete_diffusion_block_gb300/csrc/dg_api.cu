@@ -93,8 +93,8 @@ struct dg_model {
   bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr,
        *x_perm = nullptr;
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
-  float *router = nullptr, *gates = nullptr, *y = nullptr;
-  int *topk = nullptr, *offs = nullptr, *perm_tok = nullptr, *slot_row = nullptr, *work = nullptr,
+  float *gates = nullptr, *y = nullptr;
+  int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
       *n_work = nullptr;
   int max_work = 0;
   std::vector<int> routing_rows;  // rows routed by the last forward, per layer
@@ -296,16 +296,15 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
        dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
                      m->attn_ws_bytes, st, err));
     KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, st));
-    KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.moe_norm, T, d, c.rms_eps, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
-    KL(DG_K_ROUTER, 1, dg::gemm_store_f32(m->xn, W.wr, T, d, c.n_experts, m->router, err, st));
-    KL(DG_K_TOPK, 1, dg::router_topk(m->router, T, c.n_experts, c.top_k, topk, m->gates, st));
-    KL(DG_K_PERMUTE, 1,
-       dg::moe_permute(topk, T, c.top_k, c.n_experts, dg::kExpertTileRows, m->offs, m->perm_tok,
-                       m->slot_row, m->work, m->n_work, m->max_work, st, m->moe_stats));
+    KL(DG_K_ROUTE, 1,
+       dg::moe_norm_route(m->h, W.moe_norm, c.rms_eps, m->xn, W.wr, T, d, c.n_experts, c.top_k, topk, m->gates,
+                          m->slot_row, m->gcount, err, st));
+    KL(DG_K_ROUTE, 1,
+       dg::moe_scatter(m->xn, topk, m->gcount, m->slot_row, T, d, c.n_experts, c.top_k, dg::kExpertTileRows,
+                       m->x_perm, m->offs, m->work, m->n_work, m->max_work, st, m->moe_stats));
     const int rows = T * c.top_k;
-    KL(DG_K_PERMUTE, 1, dg::gather_rows(m->x_perm, m->xn, m->perm_tok, rows, d, st));
     KL(DG_K_EXPERT_FFN, 1,
        dg::moe_ffn(m->x_perm, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
                    c.n_experts, d, c.d_ff, m->act, m->y, err, st));
@@ -382,13 +381,12 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->moe_stats, 2));
   CKR(m->alloc(&m->q, (size_t)T * qd));
   CKR(m->alloc(&m->o, (size_t)T * qd));
-  CKR(m->alloc(&m->router, (size_t)T * E));
   CKR(m->alloc(&m->topk, (size_t)c.n_layers * T * k));  // per-layer routing record
   m->routing_rows.assign(c.n_layers, 0);
   CKR(m->alloc(&m->gates, (size_t)T * k));
   m->max_work = (int)dg::moe_max_work(T, k, E, dg::kExpertTileRows);
   CKR(m->alloc(&m->offs, E + 1));
-  CKR(m->alloc(&m->perm_tok, (size_t)T * k));
+  CKR(m->alloc(&m->gcount, dg::moe_group_count_ints(T, E)));
   CKR(m->alloc(&m->slot_row, (size_t)T * k));
   CKR(m->alloc(&m->work, dg::moe_work_ints(T, k, E, dg::kExpertTileRows)));
   CKR(m->alloc(&m->n_work, 1));
@@ -875,7 +873,7 @@ int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, siz
 
 const char *dg_kernel_class_name(int32_t cls) {
   static const char *names[DG_K_CLASSES] = {
-      "embed", "rmsnorm", "qkv_rope", "attention", "o_proj", "router", "topk", "permute",
+      "embed", "rmsnorm", "qkv_rope", "attention", "o_proj", "route",
       "expert_ffn", "combine", "lm_head", "sampler_merge", "sampler_rule",
       "canvas_init"};
   return (cls >= 0 && cls < DG_K_CLASSES) ? names[cls] : "";
@@ -974,8 +972,7 @@ int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
 
 namespace {
 struct MoeWs {
-  float *router;
-  int *offs, *perm_tok, *slot_row, *work, *n_work;
+  int *offs, *gcount, *slot_row, *work, *n_work;
   bf16 *act, *x_perm;
   float *y_rows;
   size_t bytes;
@@ -991,9 +988,8 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
     return r;
   };
   w.max_work = (int)dg::moe_max_work(T, k, E, dg::kExpertTileRows);
-  w.router = (float *)take((size_t)T * E * 4);
   w.offs = (int *)take((size_t)(E + 1) * 4);
-  w.perm_tok = (int *)take((size_t)T * k * 4);
+  w.gcount = (int *)take(dg::moe_group_count_ints(T, E) * 4);
   w.slot_row = (int *)take((size_t)T * k * 4);
   w.work = (int *)take(dg::moe_work_ints(T, k, E, dg::kExpertTileRows) * 4);
   w.n_work = (int *)take(4);
@@ -1025,12 +1021,11 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   MoeWs w = moe_layout(workspace, T, d, n_experts, top_k, d_ff);
   if (workspace_bytes < w.bytes) return fail(DG_EINVAL, "workspace too small");
   cudaStream_t st = (cudaStream_t)stream;
-  CK(dg::gemm_store_f32((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, w.router, nullptr, st));
-  CK(dg::router_topk(w.router, T, n_experts, top_k, expert_ids, gates, st));
-  CK(dg::moe_permute(expert_ids, T, top_k, n_experts, dg::kExpertTileRows, w.offs, w.perm_tok,
-                     w.slot_row, w.work, w.n_work, w.max_work, st));
+  CK(dg::moe_route((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, top_k, expert_ids, gates,
+                   w.slot_row, w.gcount, nullptr, st));
+  CK(dg::moe_scatter((const bf16 *)xn, expert_ids, w.gcount, w.slot_row, T, d, n_experts, top_k,
+                     dg::kExpertTileRows, w.x_perm, w.offs, w.work, w.n_work, w.max_work, st));
   const int rows = T * top_k;
-  CK(dg::gather_rows(w.x_perm, (const bf16 *)xn, w.perm_tok, rows, d, st));
   CK(dg::moe_ffn(w.x_perm, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
                  w.max_work, n_experts, d, d_ff, w.act, w.y_rows, nullptr, st));
   CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));

@@ -21,23 +21,37 @@ cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int 
 cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st);
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
                          cudaStream_t st, bf16 *out_lo = nullptr);
-cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, float *gates,
-                        cudaStream_t st);
-// Sorts the T*k (token, slot) pairs by expert.  Outputs: offs[E+1], perm_tok[T*k]
-// (token of each sorted row), slot_row[T*k] (sorted row of pair t*k+s),
+// Routing of one MoE layer (kernels_route.cu), two launches.
+// moe_route: top-k of the router logits r = xn W_r^T (value desc, expert id
+// asc; softmax gates over the selected logits) into ids / gates [T][k]; for
+// every pair t*k+s its rank among the pairs of its token group (kRouteTok
+// tokens) with the same expert into rank[T*k]; the group's pairs per expert
+// into gcount[moe_group_count_ints(T, E)].  moe_norm_route first forms
+// xn = RMSNorm(h) * gain (fp32 h [T][d]) and writes it.  d: a multiple of 64;
+// E <= 256; k <= 16.
+// moe_scatter: from those, the stable counting sort of the pairs by expert:
+// offs[E+1], slot_row[T*k] (sorted row of pair t*k+s; pass the rank array in
+// as slot_row, it is overwritten), x_perm[row] = xn[token of the row],
 // work[2*max_work] = (expert, first row) items of up to `tile_rows` rows,
 // *n_work.  `work` holds moe_work_ints() ints: the item list, then one
 // counter per item and a unit counter used by moe_ffn, all zeroed here.
-// stats (optional, device, 2 x u64): += experts with at least one row, += T*k.
 // max_work: the item capacity the work buffer was sized for (moe_max_work of
 // the largest T it serves); moe_ffn must be given the same value.
-cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
-                        int *perm_tok, int *slot_row, int *work, int *n_work, int max_work,
+// stats (optional, device, 2 x u64): += experts with at least one row, += T*k.
+constexpr int kRouteTok = 32;
+size_t moe_group_count_ints(int T, int E);
+cudaError_t moe_norm_route(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
+                           int E, int k, int *ids, float *gates, int *rank, int *gcount, int *err,
+                           cudaStream_t st);
+cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k, int *ids, float *gates,
+                      int *rank, int *gcount, int *err, cudaStream_t st);
+cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
+                        int k, int tile_rows, bf16 *x_perm, int *offs, int *work, int *n_work, int max_work,
                         cudaStream_t st, unsigned long long *stats = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
 size_t moe_work_ints(int T, int k, int E, int tile_rows);
 // Routed experts of one layer (kernels_moe.cu): act = SwiGLU(x_perm Wg^T, x_perm Wu^T),
-// y = act Wd^T, for every work item of moe_permute; one persistent launch.
+// y = act Wd^T, for every work item of moe_route; one persistent launch.
 cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act,
                     float *y, int *err, cudaStream_t st);
@@ -77,9 +91,6 @@ cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 
                                   int *err, cudaStream_t st, const StepParams *dyn = nullptr);
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                 int V, float *logits, int *err, cudaStream_t st);
-// x_perm[j] = xn[perm_tok[j]], j < rows (bf16 rows of d elements).
-cudaError_t gather_rows(bf16 *x_perm, const bf16 *xn, const int *perm_tok, int rows, int d,
-                        cudaStream_t st);
 
 // ---- sampler (kernels_sampler.cu) -------------------------------------------
 cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,

@@ -157,163 +157,6 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *
 // gates over the selected logits.  One warp per token, E <= 256, k <= 16.
 // An unordered logit (NaN) never wins a comparison but a still-unselected
 // expert is always taken over none, so every emitted id is in [0, E).
-__global__ void topk_kernel(const float *logits, int T, int E, int k, int *ids, float *gates) {
-  pdl_wait();
-  pdl_trigger();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  float v[8];
-  unsigned taken = 0;  // bit j: expert lane + 32 j already selected
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = e < E ? logits[(size_t)warp * E + e] : 0.0f;
-  }
-  float sel[16];
-  int sid[16];
-  for (int s = 0; s < k; ++s) {
-    float bv = 0.0f;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && (bi == 0x7fffffff || v[j] > bv || (v[j] == bv && e < bi))) {
-        bv = v[j];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    sel[s] = bv;
-    sid[s] = bi;
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-  }
-  if (lane == 0) {
-    float sum = 0.0f;
-    for (int s = 0; s < k; ++s) sum += expf(sel[s] - sel[0]);
-    for (int s = 0; s < k; ++s) {
-      ids[(size_t)warp * k + s] = sid[s];
-      gates[(size_t)warp * k + s] = expf(sel[s] - sel[0]) / sum;
-    }
-  }
-}
-
-// Stable counting sort of the T*k (token, slot) pairs by expert, done by one
-// block.  Warp w owns the contiguous pair segment w of 32; it counts its
-// segment per expert (__match_any_sync groups lanes holding the same expert),
-// a per-expert prefix over the segments turns the counts into starting ranks,
-// and a second walk of the segment hands out ranks in pair order, so the
-// order inside an expert is the pair order and the result is deterministic.
-constexpr int kPermThreads = 1024, kPermWarps = kPermThreads / 32;
-__global__ void __launch_bounds__(kPermThreads) permute_kernel(const int *ids, int TK, int k, int E,
-                                                               int tile_rows, int *offs,
-                                                               int *perm_tok, int *slot_row,
-                                                               int *work, int *n_work, int *sync,
-                                                               int max_work,
-                                                               unsigned long long *stats) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ int seg[kPermWarps][257];  // per-segment counts, then running ranks
-  __shared__ int cnt[257], soff[257], toff[257];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kPermWarps * 257; i += kPermThreads) (&seg[0][0])[i] = 0;
-  __syncthreads();
-  const int per = (TK + kPermWarps - 1) / kPermWarps;
-  const int s0 = min(TK, warp * per), s1 = min(TK, s0 + per);
-  for (int base = s0; base < s1; base += 32) {
-    const int i = base + lane;
-    const bool valid = i < s1;
-    const int id = valid ? ids[i] : -1;
-    const unsigned m = __match_any_sync(0xffffffffu, id);
-    if (valid && lane == __ffs(m) - 1) seg[warp][id] += __popc(m);
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kPermThreads) {
-    int run = 0;
-    for (int w = 0; w < kPermWarps; ++w) {
-      const int c = seg[w][e];
-      seg[w][e] = run;
-      run += c;
-    }
-    cnt[e] = run;
-  }
-  __syncthreads();
-  if (warp == 0) {  // expert and work-tile offsets: lane j scans experts 8j .. 8j+7
-    int c_sum = 0, w_sum = 0, touched = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane * 8 + j;
-      if (e < E) {
-        c_sum += cnt[e];
-        w_sum += (cnt[e] + tile_rows - 1) / tile_rows;
-        touched += cnt[e] > 0;
-      }
-    }
-    int c_ex = c_sum, w_ex = w_sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, c_ex, off), b = __shfl_up_sync(0xffffffffu, w_ex, off);
-      if (lane >= off) {
-        c_ex += a;
-        w_ex += b;
-      }
-    }
-    c_ex -= c_sum;
-    w_ex -= w_sum;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane * 8 + j;
-      if (e < E) {
-        soff[e] = c_ex;
-        offs[e] = c_ex;
-        toff[e] = w_ex;
-        c_ex += cnt[e];
-        w_ex += (cnt[e] + tile_rows - 1) / tile_rows;
-      }
-    }
-    if (lane == 31) {
-      offs[E] = c_ex;
-      *n_work = w_ex;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) touched += __shfl_xor_sync(0xffffffffu, touched, off);
-    if (stats && lane == 0) {  // experts whose weights this launch's expert GEMMs stream, and their rows
-      atomicAdd(&stats[0], (unsigned long long)touched);
-      atomicAdd(&stats[1], (unsigned long long)TK);
-    }
-  }
-  __syncthreads();
-  for (int base = s0; base < s1; base += 32) {
-    const int i = base + lane;
-    const bool valid = i < s1;
-    const int id = valid ? ids[i] : -1;
-    const unsigned m = __match_any_sync(0xffffffffu, id);
-    if (valid) {
-      const int row = soff[id] + seg[warp][id] + __popc(m & ((1u << lane) - 1u));
-      perm_tok[row] = i / k;
-      slot_row[i] = row;
-    }
-    __syncwarp();
-    if (valid && lane == __ffs(m) - 1) seg[warp][id] += __popc(m);
-    __syncwarp();
-  }
-  for (int e = threadIdx.x; e < E; e += kPermThreads) {
-    const int nt = (cnt[e] + tile_rows - 1) / tile_rows;
-    for (int j = 0; j < nt; ++j) {
-      work[2 * (toff[e] + j)] = e;
-      work[2 * (toff[e] + j) + 1] = j * tile_rows;
-    }
-  }
-  for (int i = threadIdx.x; i <= max_work; i += kPermThreads) sync[i] = 0;  // per-item counters, unit counter
-}
 
 // h[t] (+)= sum_s gate[t][s] * y[slot_row[t*k+s]], slots in ascending order.
 // The token's gates and rows are staged first; each thread then has all k
@@ -415,19 +258,6 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(float4 *h, const floa
   }
 }
 
-// x_perm[j] = xn[perm_tok[j]]: the routed rows in expert order, so that each
-// expert's rows are one contiguous TMA box source.
-__global__ void gather_rows_kernel(uint4 *dst, const uint4 *src, const int *perm_tok, int rows,
-                                   int vec) {
-  pdl_wait();
-  pdl_trigger();
-  const size_t total = (size_t)rows * vec;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / vec), c = (int)(i % vec);
-    dst[i] = src[(size_t)perm_tok[r] * vec + c];
-  }
-}
 
 // 16-byte copies of [L][n][Hkv][hd] rows into the paged pools.
 __global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *k_pool,
@@ -519,11 +349,6 @@ cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, in
   return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, out, out_lo, h, gain, d, eps);
 }
 
-cudaError_t router_topk(const float *logits, int T, int E, int k, int *ids, float *gates,
-                        cudaStream_t st) {
-  if (E > 256 || k > 16 || k > E) return cudaErrorInvalidValue;
-  return launch_pdl(topk_kernel, dim3(ceil_div(T * 32, 256)), dim3(256), 0, st, logits, T, E, k, ids, gates);
-}
 
 size_t moe_max_work(int T, int k, int E, int tile_rows) {
   return (size_t)(T * k + tile_rows - 1) / tile_rows + E;
@@ -531,14 +356,6 @@ size_t moe_max_work(int T, int k, int E, int tile_rows) {
 
 size_t moe_work_ints(int T, int k, int E, int tile_rows) { return 3 * moe_max_work(T, k, E, tile_rows) + 1; }
 
-cudaError_t moe_permute(const int *ids, int T, int k, int E, int tile_rows, int *offs,
-                        int *perm_tok, int *slot_row, int *work, int *n_work, int max_work,
-                        cudaStream_t st, unsigned long long *stats) {
-  if (E > 256) return cudaErrorInvalidValue;
-  if ((size_t)max_work < moe_max_work(T, k, E, tile_rows)) return cudaErrorInvalidValue;
-  return launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), 0, st, ids, T * k, k, E, tile_rows, offs,
-                    perm_tok, slot_row, work, n_work, work + 2 * max_work, max_work, stats);
-}
 
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st) {
@@ -557,13 +374,6 @@ cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const
                     slot_row, k, d / 4, gain, eps, xn);
 }
 
-cudaError_t gather_rows(bf16 *x_perm, const bf16 *xn, const int *perm_tok, int rows, int d,
-                        cudaStream_t st) {
-  const size_t total = (size_t)rows * (d / 8);
-  if (total == 0) return cudaSuccess;
-  return launch_pdl(gather_rows_kernel, dim3(grid_for(total, 256, 152 * 16)), dim3(256), 0, st, (uint4 *)x_perm,
-                    (const uint4 *)xn, perm_tok, rows, d / 8);
-}
 
 cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
                       const int *page_table, int L, int n_pages, int pos0, int n, int Hkv, int hd,

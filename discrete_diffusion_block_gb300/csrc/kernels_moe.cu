@@ -364,7 +364,7 @@ cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *w
   g.work = work;
   g.n_work = n_work;
   g.offs = offs;
-  g.done = const_cast<int *>(work) + 2 * max_work;  // zeroed by moe_permute
+  g.done = const_cast<int *>(work) + 2 * max_work;  // zeroed by moe_route
   g.next = g.done + max_work;
   g.E = E;
   g.d = d;

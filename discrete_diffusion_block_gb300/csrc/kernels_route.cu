@@ -1,0 +1,678 @@
+// Routing of one MoE layer (report §6 "MoE"; DiffusionGemma model card,
+// "Architecture": 128 experts, 8 active per token) in two launches.
+//
+// route_kernel: the layer's RMSNorm (optional), the router logits
+// r = xn W_r^T, the top-k experts of every token with their softmax gates,
+// and each routed (token, slot) pair's rank among the pairs of its token
+// group that chose the same expert.  A CTA owns 32 tokens (the MMA N) and 1/S
+// of the model dimension; the S CTAs of one token group form a cluster.
+//   1. (norm) each CTA sums the squares of its slice of the 32 rows; the S
+//      partial sums are exchanged through distributed shared memory and added
+//      in rank order, so every CTA derives the same 1/rms.  It writes its
+//      slice of xn (bf16) to global memory and, 128-byte swizzled, to shared
+//      memory as the MMA B operand.  Without the norm, the B slice is loaded
+//      from xn with TMA.
+//   2. one thread streams the CTA's K-slice of W_r (128-expert x 64 boxes,
+//      issued before the wait on the previous kernel: weights never change)
+//      and one thread issues tcgen05.mma (M = 128 experts, N = 32 tokens) into
+//      a 32-column TMEM accumulator per 128 experts.
+//   3. the partial logits go to shared memory; after a cluster barrier CTA z
+//      adds the S partials of 32/S tokens in rank order (deterministic) and
+//      one warp per token selects the top k.
+//   4. per-CTA expert counts are exchanged in the cluster: each pair gets its
+//      rank within the group, and the group's per-expert counts go to global
+//      memory.
+// scatter_kernel: every block turns the group counts into expert offsets
+// (the stable counting sort's prefix sums: groups, then experts), places its
+// share of the pairs at offs[e] + (pairs of e in earlier groups) + rank, and
+// copies their token rows there; block 0 also writes the work list.  The
+// result is the order of a stable sort of the pairs by expert.
+// Every mbarrier wait is bounded (error word + abort flag); every CTA passes
+// the same cluster barriers whatever happened, so no CTA can be left waiting.
+#include <cuda.h>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace dg {
+
+cudaError_t tmap_bf16_cached(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                             uint32_t box);
+
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kTokThreads = kRouteThreads / kRouteTok;  // threads per token in the norm
+constexpr uint32_t kWBox = 128 * 128;              // 128 experts x 64 bf16
+constexpr uint32_t kXBox = kRouteTok * 128;        // 32 tokens x 64 bf16
+constexpr int kNormRegs = 12;
+constexpr int kPairIters = kRouteTok * 16 / kRouteThreads;  // pairs per thread at most (k <= 16)  // float4 columns per thread held in registers by the norm
+constexpr int kSmemBudget = 200 * 1024;  // dynamic; the expert sort adds 11 KB of static shared memory
+
+struct RouteArgs {
+  const float *h;      // norm: input rows fp32 [T][d]
+  const float *gain;   // norm: RMSNorm gain [d]
+  float eps;
+  bf16 *xn;            // norm: normalised rows out [T][d]
+  int T, d, E, k, tile_rows;
+  int S, nk_max, stages, m_tiles;  // cluster size, k-tiles per CTA (max), ring depth, 128-expert tiles
+  int *ids;
+  float *gates;
+  int *rank;           // [T*k] rank of each pair among its group's pairs of the same expert
+  int *gcount;         // [ceil(T/32)][E] pairs per (token group, expert)
+  int *err;
+};
+
+struct RouteSmem {
+  uint32_t w_off, x_off, part_off, logit_off, ss_off, cnt_off, pid_off, bars_off, bytes;
+};
+
+__host__ __device__ inline RouteSmem route_smem(int S, int nk_max, int stages, int m_tiles) {
+  RouteSmem s;
+  const int ep = m_tiles * 128;
+  s.w_off = 0;
+  s.x_off = s.w_off + (uint32_t)stages * m_tiles * kWBox;
+  s.part_off = s.x_off + (uint32_t)nk_max * kXBox;
+  s.logit_off = s.part_off + (uint32_t)kRouteTok * ep * 4;
+  s.ss_off = s.logit_off + (uint32_t)(kRouteTok / S) * ep * 4;
+  s.cnt_off = s.ss_off + kRouteTok * 4;
+  s.pid_off = s.cnt_off + ep * 4;
+  s.bars_off = (s.pid_off + (uint32_t)(kRouteTok / S) * 16 * 4 + 15) & ~15u;
+  s.bytes = s.bars_off + (8 + 8 + 2) * 8 + 32 + 1024;  // full[8], empty[8], x, acc; words; alignment slack
+  return s;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Order-preserving map of a float onto an unsigned key (larger float, larger
+// key; -0 and +0 equal).  Key 0 is below every non-NaN value.
+__device__ __forceinline__ unsigned float_key(float f) {
+  unsigned u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Top-k of one token's E <= 256 logits (shared memory) by one warp: value
+// descending, lower expert id first among equal values; gates are the softmax
+// of the selected logits.
+__device__ __forceinline__ void topk_warp(const float *lrow, int E, int k, int lane, int *ids_out,
+                                          float *gates_out, int *ids_smem) {
+  unsigned key[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < E ? float_key(lrow[e]) : 0u;
+  }
+  float my_val = 0.0f;
+  int my_id = 0;
+  for (int s = 0; s < k; ++s) {
+    unsigned bk = 0u, be = 0xffffffffu;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)  // ascending expert id: strict > keeps the lowest id of a tie
+      if (key[j] > bk) {
+        bk = key[j];
+        be = (unsigned)(lane + 32 * j);
+      }
+    const unsigned mk = __reduce_max_sync(0xffffffffu, bk);
+    const unsigned me = __reduce_min_sync(0xffffffffu, bk == mk ? be : 0xffffffffu);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (me == (unsigned)(lane + 32 * j)) key[j] = 0u;  // taken
+    if (lane == s) {
+      my_val = key_float(mk);
+      my_id = (int)me;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_val, 0);
+  const float ex = lane < k ? expf(my_val - top) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids_out[lane] = my_id;
+    ids_smem[lane] = my_id;
+    gates_out[lane] = ex / sum;
+  }
+}
+
+template <bool NORM>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, RouteArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const RouteSmem L = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
+  uint64_t *full = (uint64_t *)(base + L.bars_off);
+  uint64_t *empty = full + 8;
+  uint64_t *xbar = empty + 8;  // B operand loaded by TMA (no norm)
+  uint64_t *accb = xbar + 1;
+  uint32_t *tmem_slot = (uint32_t *)(accb + 1);
+  volatile int *abort = (volatile int *)(tmem_slot + 1);
+  int *flag = (int *)(tmem_slot + 2);  // [0] k-tiles multiplied, [2] k-tiles loaded
+  unsigned char *wring = base + L.w_off, *xs = base + L.x_off;
+  float *part = (float *)(base + L.part_off), *logit = (float *)(base + L.logit_off);
+  float *ss = (float *)(base + L.ss_off);
+  int *cnt = (int *)(base + L.cnt_off);  // this CTA's pairs per expert
+  int *pid = (int *)(base + L.pid_off);  // this CTA's pairs' experts
+
+  const int S = a.S, z = (int)(blockIdx.x % S), grp = (int)(blockIdx.x / S);
+  const int t0 = grp * kRouteTok, ep = a.m_tiles * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KT = a.d / 64;
+  const int kb = KT * z / S, ke = KT * (z + 1) / S, nk = ke - kb;
+  const int stages = a.stages;
+  const uint32_t stage_bytes = (uint32_t)a.m_tiles * kWBox;
+  const uint32_t tcols = a.m_tiles * kRouteTok;  // 32 or 64 accumulator columns
+  for (int e = threadIdx.x; e < ep; e += kRouteThreads) cnt[e] = 0;
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    tc::mbar_init(accb, 1);
+    tc::mbar_init(xbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     tc::smem_u32(tmem_slot)),
+                 "r"(tcols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Weights never change: the first ring fill starts before the wait on the
+  // kernel that produced this layer's activations.
+  const int pre = min(stages, nk);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < pre; ++i) {
+      tc::mbar_expect_tx(full + i, stage_bytes);
+      for (int mt = 0; mt < a.m_tiles; ++mt)
+        tc::tma_load_2d(wring + (size_t)i * stage_bytes + mt * kWBox, &tw, (kb + i) * 64, mt * 128, full + i);
+    }
+  }
+  // Norm: kTokThreads threads per token; thread `sub` owns the float4
+  // columns c4b + kTokThreads u of the CTA's slice.  The gain is a weight:
+  // its slice is loaded before the wait as well.
+  const int tt = threadIdx.x / kTokThreads, sub = threadIdx.x % kTokThreads, tn = t0 + tt;
+  const int c4b = kb * 16 + sub, c4e = ke * 16;
+  float4 gv[kNormRegs], hv[kNormRegs];
+  if (NORM) {
+    const float4 *g4 = (const float4 *)a.gain;
+#pragma unroll
+    for (int u = 0; u < kNormRegs; ++u) {
+      const int c = c4b + kTokThreads * u;
+      gv[u] = c < c4e ? g4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0 && a.err && *(volatile int *)a.err) *abort = 1;  // an earlier timeout
+
+  if (NORM) {
+    const float4 *row = (const float4 *)(a.h + (size_t)(tn < a.T ? tn : 0) * a.d);
+    const bool live = tn < a.T;
+#pragma unroll
+    for (int u = 0; u < kNormRegs; ++u) {
+      const int c = c4b + kTokThreads * u;
+      hv[u] = live && c < c4e ? row[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kNormRegs; ++u)
+      acc += hv[u].x * hv[u].x + hv[u].y * hv[u].y + hv[u].z * hv[u].z + hv[u].w * hv[u].w;
+    for (int c = c4b + kTokThreads * kNormRegs; live && c < c4e; c += kTokThreads) {  // wider slices
+      const float4 v = row[c];
+      acc += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int off = kTokThreads / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0) ss[tt] = acc;
+    tc::cluster_sync();
+    float pv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) pv[q] = q < S ? ld_cluster_f32(tc::cluster_addr(tc::smem_u32(ss + tt), q)) : 0.0f;
+    float tot = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tot += pv[q];  // rank order; every CTA of the cluster adds alike
+    const float inv = rsqrtf(tot / a.d + a.eps);
+    const float4 *g4 = (const float4 *)a.gain;
+    for (int c = c4b, u = 0; c < c4e; c += kTokThreads, ++u) {
+      float4 v, g;
+      if (u < kNormRegs) {
+#pragma unroll
+        for (int q = 0; q < kNormRegs; ++q)
+          if (q == u) {
+            v = hv[q];
+            g = gv[q];
+          }
+      } else {
+        v = live ? row[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        g = g4[c];
+      }
+      uint2 packed = make_uint2(0u, 0u);
+      if (live) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
+        packed.x = *(uint32_t *)&p0;
+        packed.y = *(uint32_t *)&p1;
+        *(uint2 *)(a.xn + (size_t)tn * a.d + 4 * c) = packed;
+      }
+      // 128-byte swizzled K-major B tile: row tt, 16-byte chunk (col / 8) ^ (tt % 8)
+      const int cl = 4 * c - kb * 64, kt = cl >> 6, col = cl & 63;
+      const uint32_t off = (uint32_t)kt * kXBox + tt * 128 + ((((col >> 3) ^ (tt & 7)) << 4) | ((col & 7) * 2));
+      *(uint2 *)(xs + off) = packed;
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  } else if (threadIdx.x == 0) {
+    tc::mbar_expect_tx(xbar, (uint32_t)nk * kXBox);
+    for (int i = 0; i < nk; ++i) tc::tma_load_2d(xs + (size_t)i * kXBox, &tx, (kb + i) * 64, t0, xbar);
+  }
+  __syncthreads();
+
+  if (threadIdx.x == 0) {  // producer: the rest of the K slice, if the ring is shorter
+    int i = pre;
+    for (; i < nk; ++i) {
+      const int s = i % stages;
+      if (!tc::mbar_wait(empty + s, ((i / stages) - 1) & 1, a.err, 51, abort)) break;
+      tc::mbar_expect_tx(full + s, stage_bytes);
+      for (int mt = 0; mt < a.m_tiles; ++mt)
+        tc::tma_load_2d(wring + (size_t)s * stage_bytes + mt * kWBox, &tw, (kb + i) * 64, mt * 128, full + s);
+    }
+    flag[2] = i;
+  } else if (threadIdx.x == 32) {  // MMA issuer
+    bool ok = NORM || tc::mbar_wait(xbar, 0, a.err, 52, abort);
+    constexpr uint32_t idesc = tc::idesc_bf16(128, kRouteTok);
+    int issued = 0;
+    for (int i = 0; i < nk && ok; ++i) {
+      const int s = i % stages;
+      if (!tc::mbar_wait(full + s, (i / stages) & 1, a.err, 53, abort)) break;
+      tc::fence_after();
+      const uint32_t xa = tc::smem_u32(xs + (size_t)i * kXBox);
+      for (int mt = 0; mt < a.m_tiles; ++mt) {
+        const uint32_t wa = tc::smem_u32(wring + (size_t)s * stage_bytes + mt * kWBox);
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+          tc::mma_bf16(tmem + mt * kRouteTok, tc::sw128_desc(wa) + 2 * k16, tc::sw128_desc(xa) + 2 * k16, idesc,
+                       (i | k16) != 0);
+      }
+      tc::mma_commit(empty + s);
+      ++issued;
+    }
+    if (issued) tc::mma_commit(accb);
+    flag[0] = issued;
+  }
+  __syncthreads();
+  const int issued = flag[0];
+
+  // Partial logits: warp w drains TMEM lanes 32 (w % 4) .. of 128-expert tile w / 4.
+  {
+    const int mt = warp >> 2, q = warp & 3;
+    const int e = mt * 128 + q * 32 + lane;
+    uint32_t r[kRouteTok];
+    bool have = false;
+    if (mt < a.m_tiles && issued) {
+      // bounded, and waited for even after an abort: TMEM is freed only after the MMAs finished
+      const long long c0 = clock64();
+      while (!tc::mbar_try_wait(accb, 0) && clock64() - c0 < tc::kWaitCycles) {
+      }
+      tc::fence_after();
+      tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + mt * kRouteTok, r);
+      tc::tmem_ld_wait();
+      have = !*abort;
+    }
+    if (mt < a.m_tiles) {
+#pragma unroll
+      for (int t = 0; t < kRouteTok; ++t) part[t * ep + e] = have ? __uint_as_float(r[t]) : 0.0f;
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::cluster_sync();  // every CTA's partials are complete
+
+  const int tpr = kRouteTok / S;  // tokens reduced by this CTA
+  for (int idx = threadIdx.x; idx < tpr * ep; idx += kRouteThreads) {
+    const int j = idx / ep, e = idx - j * ep;
+    const uint32_t src = tc::smem_u32(part + (z * tpr + j) * ep + e);
+    float pv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) pv[q] = q < S ? ld_cluster_f32(tc::cluster_addr(src, q)) : 0.0f;
+    float sum = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sum += pv[q];  // rank order
+    logit[j * ep + e] = sum;
+  }
+  tc::cluster_sync();  // all reads of peers' partials done
+  if (warp == 1) {
+    tc::fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(tcols));
+  }
+  // Bounded drain of weight boxes still in flight after an abort.
+  if (threadIdx.x == 0 && *abort) {
+    for (int i = max(0, flag[2] - stages); i < flag[2]; ++i) {
+      const long long c0 = clock64();
+      while (!tc::mbar_try_wait(full + i % stages, (i / stages) & 1) && clock64() - c0 < tc::kWaitCycles) {
+      }
+    }
+    if (!NORM) {
+      const long long c0 = clock64();
+      while (!tc::mbar_try_wait(xbar, 0) && clock64() - c0 < tc::kWaitCycles) {
+      }
+    }
+  }
+  const int k = a.k, np = tpr * k;  // this CTA's pairs: tokens t0 + z tpr + j, slots s
+  for (int j = warp; j < tpr; j += kRouteWarps) {
+    const int t = t0 + z * tpr + j;
+    if (t < a.T)
+      topk_warp(logit + j * ep, a.E, k, lane, a.ids + (size_t)t * k, a.gates + (size_t)t * k, pid + j * k);
+    else if (lane < k)
+      pid[j * k + lane] = -1;
+  }
+  __syncthreads();
+
+  // Stable ranks: pair p of this CTA ranks after the earlier pairs of the CTA
+  // with the same expert, then after those of the cluster's lower ranks.
+  int my_e[kPairIters], my_rank[kPairIters];
+#pragma unroll
+  for (int u = 0; u < kPairIters; ++u) {
+    const int p = threadIdx.x + u * kRouteThreads;
+    my_e[u] = p < np ? pid[p] : -1;
+    my_rank[u] = 0;
+    if (my_e[u] >= 0) {
+      for (int q = 0; q < p; ++q) my_rank[u] += pid[q] == my_e[u];
+      atomicAdd(cnt + my_e[u], 1);
+    }
+  }
+  tc::cluster_sync();  // every CTA's expert counts are complete
+#pragma unroll
+  for (int u = 0; u < kPairIters; ++u) {
+    if (my_e[u] < 0) continue;
+    const uint32_t src = tc::smem_u32(cnt + my_e[u]);
+    int pv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) pv[q] = q < z ? ld_cluster_s32(tc::cluster_addr(src, q)) : 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) my_rank[u] += pv[q];
+    a.rank[(size_t)(t0 + z * tpr) * k + threadIdx.x + u * kRouteThreads] = my_rank[u];
+  }
+  // The group's pairs per expert: CTA z writes experts z, z + S, ...
+  for (int e = z + S * (int)threadIdx.x; e < a.E; e += S * kRouteThreads) {
+    const uint32_t src = tc::smem_u32(cnt + e);
+    int pv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) pv[q] = q < S ? ld_cluster_s32(tc::cluster_addr(src, q)) : 0;
+    int sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sum += pv[q];
+    a.gcount[(size_t)grp * a.E + e] = sum;
+  }
+  tc::cluster_sync();  // peers' counts stay alive until every read is done
+}
+
+template <bool NORM>
+cudaError_t launch_route(const CUtensorMap &tw, const CUtensorMap &tx, RouteArgs a, cudaStream_t st) {
+  const RouteSmem L = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
+  auto kern = route_kernel<NORM>;
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set |= 1ull << dev;
+  }
+  const int groups = ceil_div(a.T, kRouteTok);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * a.S, 1, 1);
+  cfg.blockDim = dim3(kRouteThreads, 1, 1);
+  cfg.dynamicSmemBytes = L.bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = a.S;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a);
+}
+
+cudaError_t route_common(bool norm, const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr,
+                         int T, int d, int E, int k, int *ids, float *gates, int *rank, int *gcount, int *err,
+                         cudaStream_t st) {
+  if (T < 0 || d < 64 || d % 64 || E < 1 || E > 256 || k < 1 || k > 16 || k > E) return cudaErrorInvalidValue;
+  if (T == 0) return cudaSuccess;
+  RouteArgs a = {};
+  a.h = h;
+  a.gain = gain;
+  a.eps = eps;
+  a.xn = xn;
+  a.T = T;
+  a.d = d;
+  a.E = E;
+  a.k = k;
+  const int KT = d / 64;
+  a.S = KT >= 8 ? 8 : KT >= 4 ? 4 : KT >= 2 ? 2 : 1;
+  a.nk_max = ceil_div(KT, a.S);
+  a.m_tiles = E > 128 ? 2 : 1;
+  const RouteSmem base = route_smem(a.S, a.nk_max, 0, a.m_tiles);
+  const int fit = (int)((kSmemBudget - (int)base.bytes) / (a.m_tiles * (int)kWBox));
+  a.stages = min(8, min(a.nk_max, fit));
+  if (a.stages < 1) return cudaErrorInvalidValue;  // the K slice's B operand does not fit: d too large
+  a.ids = ids;
+  a.gates = gates;
+  a.rank = rank;
+  a.gcount = gcount;
+  a.err = err;
+  CUtensorMap tw, tx;
+  cudaError_t e = tmap_bf16_cached(&tw, wr, (uint64_t)E, (uint64_t)d, 128);
+  if (e != cudaSuccess) return e;
+  if (norm) return launch_route<true>(tw, tw, a, st);
+  e = tmap_bf16_cached(&tx, xn, (uint64_t)T, (uint64_t)d, kRouteTok);
+  if (e != cudaSuccess) return e;
+  return launch_route<false>(tw, tx, a, st);
+}
+
+// ---------------------------------------------------------------------------
+// Placement of the routed pairs and copy of their token rows.
+// ---------------------------------------------------------------------------
+constexpr int kScatThreads = 256;
+
+struct ScatArgs {
+  const bf16 *xn;
+  const int *ids, *gcount;
+  int *slot_row;  // in: rank within the token group; out: sorted row
+  bf16 *x_perm;
+  int T, d, E, k, tile_rows, ng;
+  int *offs, *work, *n_work, *sync;
+  int max_work;
+  unsigned long long *stats;
+};
+
+// Exclusive prefix sum over the block of one value per thread (kScatThreads
+// threads); returns the prefix and stores the block total in *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kScatThreads / 32; ++w) {
+    const int c = warp_tot[w];
+    before += w < warp ? c : 0;
+    all += c;
+  }
+  __syncthreads();  // warp_tot may be reused by the next scan
+  *total = all;
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
+  extern __shared__ int tab[];  // [ng][E]: pairs of e in earlier groups; then offs[E]
+  __shared__ int warp_tot[kScatThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int E = a.E, ng = a.ng, n = ng * E;
+  int *soffs = tab + n;
+  for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
+  __syncthreads();
+  const int e = threadIdx.x;  // E <= kScatThreads
+  int tot = 0;
+  if (e < E)
+    for (int g = 0; g < ng; ++g) {
+      const int c = tab[g * E + e];
+      tab[g * E + e] = tot;
+      tot += c;
+    }
+  int total;
+  const int off = block_exclusive_scan(tot, warp_tot, &total);
+  if (e < E) soffs[e] = off;
+  if (blockIdx.x == 0) {  // the expert segments and the work list of the expert FFN
+    const int tiles = e < E ? (tot + a.tile_rows - 1) / a.tile_rows : 0;
+    int n_items;
+    const int toff = block_exclusive_scan(tiles, warp_tot, &n_items);
+    int touched;
+    block_exclusive_scan(e < E && tot > 0 ? 1 : 0, warp_tot, &touched);
+    if (e < E) {
+      a.offs[e] = off;
+      for (int j = 0; j < tiles; ++j) {
+        a.work[2 * (toff + j)] = e;
+        a.work[2 * (toff + j) + 1] = j * a.tile_rows;
+      }
+    }
+    if (threadIdx.x == 0) {
+      a.offs[E] = total;
+      *a.n_work = n_items;
+      if (a.stats) {  // experts whose weights the expert FFN streams, and their rows
+        atomicAdd(&a.stats[0], (unsigned long long)touched);
+        atomicAdd(&a.stats[1], (unsigned long long)total);
+      }
+    }
+    for (int i = threadIdx.x; i <= a.max_work; i += kScatThreads) a.sync[i] = 0;  // FFN counters
+  }
+  __syncthreads();
+  // Pairs of this block: one warp per pair; the warp copies the token's row.
+  const int TK = a.T * a.k, per = (TK + gridDim.x - 1) / gridDim.x;
+  const int p0 = blockIdx.x * per, p1 = min(TK, p0 + per);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8;
+  for (int p = p0 + warp; p < p1; p += kScatThreads / 32) {
+    const int ex = a.ids[p], t = p / a.k, g = t / kRouteTok;
+    const int row = soffs[ex] + tab[g * E + ex] + a.slot_row[p];
+    __syncwarp();
+    if (lane == 0) a.slot_row[p] = row;
+    const uint4 *src = (const uint4 *)(a.xn + (size_t)t * a.d);
+    uint4 *dst = (uint4 *)(a.x_perm + (size_t)row * a.d);
+    constexpr int U = 4;
+    for (int c = lane; c < vec; c += 32 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = c + 32 * u < vec ? src[c + 32 * u] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (c + 32 * u < vec) dst[c + 32 * u] = v[u];
+    }
+  }
+}
+
+int num_sms_route() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+size_t moe_group_count_ints(int T, int E) { return (size_t)ceil_div(T, kRouteTok) * E; }
+
+cudaError_t moe_norm_route(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
+                           int E, int k, int *ids, float *gates, int *rank, int *gcount, int *err,
+                           cudaStream_t st) {
+  return route_common(true, h, gain, eps, xn, wr, T, d, E, k, ids, gates, rank, gcount, err, st);
+}
+
+cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k, int *ids, float *gates,
+                      int *rank, int *gcount, int *err, cudaStream_t st) {
+  return route_common(false, nullptr, nullptr, 0.0f, const_cast<bf16 *>(xn), wr, T, d, E, k, ids, gates, rank,
+                      gcount, err, st);
+}
+
+cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
+                        int k, int tile_rows, bf16 *x_perm, int *offs, int *work, int *n_work, int max_work,
+                        cudaStream_t st, unsigned long long *stats) {
+  if (T < 0 || d % 8 || E < 1 || E > kScatThreads || k < 1) return cudaErrorInvalidValue;
+  if ((size_t)max_work < moe_max_work(T, k, E, tile_rows)) return cudaErrorInvalidValue;
+  ScatArgs a;
+  a.xn = xn;
+  a.ids = ids;
+  a.gcount = gcount;
+  a.slot_row = slot_row;
+  a.x_perm = x_perm;
+  a.T = T;
+  a.d = d;
+  a.E = E;
+  a.k = k;
+  a.tile_rows = tile_rows;
+  a.ng = ceil_div(T, kRouteTok);
+  a.offs = offs;
+  a.work = work;
+  a.n_work = n_work;
+  a.sync = work + 2 * max_work;
+  a.max_work = max_work;
+  a.stats = stats;
+  const size_t smem = ((size_t)a.ng * E + E) * sizeof(int);
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set |= 1ull << dev;
+  }
+  const int TK = T * k;
+  const int grid = max(1, min(ceil_div(TK, 2 * (kScatThreads / 32)), 2 * num_sms_route()));
+  return launch_pdl(scatter_kernel, dim3(grid), dim3(kScatThreads), smem, st, a);
+}
+
+}  // namespace dg

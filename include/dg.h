@@ -209,10 +209,13 @@ int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, siz
 
 /* ---- profiling --------------------------------------------------------- */
 
-/* Kernel classes of the decoder, for per-class timing and launch counts. */
+/* Kernel classes of the decoder, for per-class timing and launch counts.
+ * DG_K_ROUTE counts two launches per MoE layer: the routing kernel (the MoE
+ * RMSNorm, router logits, top-k and gates, and the sort of the routed rows
+ * by expert) and the row gather. */
 enum {
-    DG_K_EMBED = 0, DG_K_RMSNORM, DG_K_QKV_ROPE, DG_K_ATTENTION, DG_K_O_PROJ, DG_K_ROUTER,
-    DG_K_TOPK, DG_K_PERMUTE, DG_K_EXPERT_FFN, DG_K_COMBINE, DG_K_LM_HEAD,
+    DG_K_EMBED = 0, DG_K_RMSNORM, DG_K_QKV_ROPE, DG_K_ATTENTION, DG_K_O_PROJ,
+    DG_K_ROUTE, DG_K_EXPERT_FFN, DG_K_COMBINE, DG_K_LM_HEAD,
     DG_K_SAMPLER_MERGE, DG_K_SAMPLER_RULE, DG_K_CANVAS_INIT, DG_K_CLASSES
 };
 const char *dg_kernel_class_name(int32_t cls);
