@@ -91,7 +91,7 @@ struct dg_model {
   int *ids = nullptr;
   float *h = nullptr;
   bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr,
-       *x_perm = nullptr;
+       *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   float *gates = nullptr, *y = nullptr;
   int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
@@ -303,10 +303,10 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
                           m->slot_row, m->gcount, err, st));
     KL(DG_K_ROUTE, 1,
        dg::moe_scatter(m->xn, topk, m->gcount, m->slot_row, T, d, c.n_experts, c.top_k, dg::kExpertTileRows,
-                       m->x_perm, m->offs, m->work, m->n_work, m->max_work, st, m->moe_stats));
+                       m->x_tiles, m->offs, m->work, m->n_work, m->max_work, st, m->moe_stats));
     const int rows = T * c.top_k;
     KL(DG_K_EXPERT_FFN, 1,
-       dg::moe_ffn(m->x_perm, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
+       dg::moe_ffn(m->x_tiles, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
                    c.n_experts, d, c.d_ff, m->act, m->y, err, st));
     if (fuse_norm && L + 1 < c.n_layers) {
       KL(DG_K_COMBINE, 1,
@@ -390,8 +390,8 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->slot_row, (size_t)T * k));
   CKR(m->alloc(&m->work, dg::moe_work_ints(T, k, E, dg::kExpertTileRows)));
   CKR(m->alloc(&m->n_work, 1));
-  CKR(m->alloc(&m->act, (size_t)T * k * F));
-  CKR(m->alloc(&m->x_perm, (size_t)T * k * d));
+  CKR(m->alloc(&m->act, dg::moe_item_tile_elems(m->max_work, F)));
+  CKR(m->alloc(&m->x_tiles, dg::moe_item_tile_elems(m->max_work, d)));
   CKR(m->alloc(&m->y, (size_t)T * k * d));
   size_t ws = 0;
   const int shapes[3][2] = {{c.max_context - C, C}, {0, C},
@@ -973,7 +973,7 @@ int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
 namespace {
 struct MoeWs {
   int *offs, *gcount, *slot_row, *work, *n_work;
-  bf16 *act, *x_perm;
+  bf16 *act, *x_tiles;
   float *y_rows;
   size_t bytes;
   int max_work;
@@ -993,8 +993,8 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.slot_row = (int *)take((size_t)T * k * 4);
   w.work = (int *)take(dg::moe_work_ints(T, k, E, dg::kExpertTileRows) * 4);
   w.n_work = (int *)take(4);
-  w.act = (bf16 *)take((size_t)T * k * F * 2);
-  w.x_perm = (bf16 *)take((size_t)T * k * d * 2);
+  w.act = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, F) * 2);
+  w.x_tiles = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, d) * 2);
   w.y_rows = (float *)take((size_t)T * k * d * 4);
   w.bytes = off;
   return w;
@@ -1024,9 +1024,9 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   CK(dg::moe_route((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, top_k, expert_ids, gates,
                    w.slot_row, w.gcount, nullptr, st));
   CK(dg::moe_scatter((const bf16 *)xn, expert_ids, w.gcount, w.slot_row, T, d, n_experts, top_k,
-                     dg::kExpertTileRows, w.x_perm, w.offs, w.work, w.n_work, w.max_work, st));
+                     dg::kExpertTileRows, w.x_tiles, w.offs, w.work, w.n_work, w.max_work, st));
   const int rows = T * top_k;
-  CK(dg::moe_ffn(w.x_perm, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
+  CK(dg::moe_ffn(w.x_tiles, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
                  w.max_work, n_experts, d, d_ff, w.act, w.y_rows, nullptr, st));
   CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));
   return DG_OK;

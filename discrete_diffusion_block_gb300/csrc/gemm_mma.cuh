@@ -12,6 +12,7 @@ struct TileCtx {
   int n_valid;     // columns of the tile inside the group's N
   int group;       // expert (0 if not grouped)
   int b_base;      // first B row of the group
+  int swz;         // tile layout: element (f, t) at f * ldc + (t ^ (f & swz)); 0 or 31
 };
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool pred) {

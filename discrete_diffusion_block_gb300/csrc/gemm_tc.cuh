@@ -170,13 +170,13 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t *r) {
 // busy per instruction: with N = 64 the single-thread MMA issue and the
 // shared-memory operand traffic, not HBM, bounded the mainloop.
 //
-// The SPLIT CTAs of one output tile form a thread-block cluster (1, 1, SPLIT).
-// Each writes its fp32 partial tile into its own shared memory, slice-major
-// ([SPLIT][128][W + 4], W = 256 / SPLIT columns per slice); after a cluster
-// barrier CTA z sums slice z over the cluster in rank order through
-// distributed shared memory (a fixed order, so results are deterministic) and
-// runs the epilogue on that 128 x W slice.  A second cluster barrier keeps
-// every partial alive until its readers are done.
+// The SPLIT CTAs of one output tile form a thread-block cluster.  Each writes
+// its fp32 partial tile into its own shared memory, slice-major (W = 256 /
+// SPLIT columns per slice); after a cluster barrier it sends slice j to CTA j
+// with one bulk shared-to-shared copy (the TMA engine moves the bytes, no
+// register round trip), CTA z sums the SPLIT partials of slice z in rank order
+// (a fixed order, so results are deterministic) and runs the epilogue on that
+// 128 x W slice.  A second cluster barrier ends the unit.
 // ---------------------------------------------------------------------------
 namespace tc {
 
@@ -201,6 +201,15 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, f
                : "memory");
 }
 
+// Bulk copy of `bytes` from this CTA's shared memory to a peer's (cluster
+// addresses dst and bar); completion is signalled on the peer's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
@@ -210,18 +219,27 @@ constexpr int kSkBN = 256;           // B rows per tile (MMA N upper bound)
 constexpr int kSkStages = 4;
 constexpr uint32_t kBChunkBytes = 64 * 128;  // one 64-row B box
 
+// Shared memory of a split-K CTA.  The epilogue area overlays the ring.
+// SPLIT > 1: part = the CTA's fp32 partial tile, slice-major ([SPLIT][128][W],
+// element (f, t) of a slice at f * W + (t ^ (f & 31)), so that row-wise
+// writes and column-wise reads are both conflict-free); recv = the SPLIT - 1
+// peer partials of this CTA's own slice, later the epilogue's scratch.
+// SPLIT == 1: red = the tile, [128][kSkBN + 1], then the epilogue scratch.
 template <int SPLIT, class Epi>
 struct SkSmem {
   static constexpr int W = kSkBN / SPLIT;  // epilogue slice width
   static constexpr uint32_t stage_bytes = kATileBytes + kSkBN * 128;
   static constexpr size_t ring = (size_t)kSkStages * stage_bytes;
-  static constexpr int part_ld = W + 4;    // float4 rows, 8 consecutive rows on distinct banks
-  static constexpr size_t part = SPLIT > 1 ? (size_t)SPLIT * 128 * part_ld * 4 : 0;
-  static constexpr int red_ld = W + 1;     // odd: column walks are conflict-free
-  static constexpr size_t red = (size_t)128 * red_ld * 4;
-  static constexpr size_t epi = part + red + Epi::extra_smem;
+  static constexpr uint32_t slice_bytes = 128u * W * 4u;
+  static constexpr size_t part = SPLIT > 1 ? (size_t)SPLIT * slice_bytes : 0;
+  static constexpr size_t recv = SPLIT > 1 ? (size_t)(SPLIT - 1) * slice_bytes : 0;
+  static constexpr int red_ld = kSkBN + 1;  // odd: column walks are conflict-free
+  static constexpr size_t red = SPLIT > 1 ? 0 : (size_t)128 * red_ld * 4;
+  static constexpr size_t scratch = SPLIT > 1 ? (recv > Epi::extra_smem ? recv : Epi::extra_smem)
+                                              : Epi::extra_smem;
+  static constexpr size_t epi = part + red + scratch;
   static constexpr size_t bars_off = ((ring > epi ? ring : epi) + 15) & ~(size_t)15;
-  static constexpr size_t bytes = bars_off + (2 * kSkStages + 1) * 8 + 16 + 1024;
+  static constexpr size_t bytes = bars_off + (2 * kSkStages + 2) * 8 + 16 + 1024;
 };
 
 }  // namespace tc
@@ -237,7 +255,8 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t *full = (uint64_t *)(base + S::bars_off);
   uint64_t *empty = full + STAGES;
   uint64_t *accb = empty + STAGES;
-  uint32_t *tmem_slot = (uint32_t *)(accb + 1);
+  uint64_t *rbar = accb + 1;  // peer partials received
+  uint32_t *tmem_slot = (uint32_t *)(rbar + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
   // Output units are (item, 128-row M tile) pairs; items are the n-tiles of a
@@ -270,6 +289,7 @@ __global__ void __launch_bounds__(128, 1)
       tc::mbar_init(empty + s, 1);
     }
     tc::mbar_init(accb, 1);
+    tc::mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -322,6 +342,7 @@ __global__ void __launch_bounds__(128, 1)
     } else {
       ctx.n0 = y * tc::kSkBN;
     }
+    ctx.swz = 0;
     ctx.m_valid = min(128, g.M - ctx.m0);
     ctx.n_valid = max(0, min(tc::kSkBN, n_total - ctx.n0));
     const int nb = max(1, (ctx.n_valid + 63) >> 6);     // 64-row B boxes per stage
@@ -389,67 +410,62 @@ __global__ void __launch_bounds__(128, 1)
       __syncthreads();
       if (ctx.n_valid > 0) epi(red, S::red_ld, ctx, extra);
     } else {
-      // Each CTA writes its fp32 partial, slice-major ([SPLIT][128][W + 4]),
-      // into its own shared memory; after a cluster barrier CTA z sums slice
-      // z over the cluster in rank order through distributed shared memory.
+      // Each CTA writes its fp32 partial into its own shared memory (part);
+      // after a cluster barrier it pushes slice j to CTA j with one bulk copy
+      // per peer.  CTA z adds the SPLIT partials of slice z in rank order (a
+      // fixed order: deterministic) and runs the epilogue on that 128 x W
+      // slice.  A second cluster barrier ends the unit: every copy into and
+      // out of this CTA's shared memory is complete past it.
       float *part = (float *)base;
-      float *red = (float *)(base + S::part);
+      float *recv = (float *)(base + S::part);
+      const int sw = row & 31;
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
         uint32_t v[32];
         tc::tmem_ld32(trow + 32 * c, v);
         tc::tmem_ld_wait(v);
         const int sl = (32 * c) / W, o = 32 * c - sl * W;
-        float4 *dst = (float4 *)(part + ((size_t)sl * 128 + row) * S::part_ld + o);
+        float *dst = part + (size_t)sl * 128 * W + (size_t)row * W + o;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        for (int j = 0; j < 32; ++j) dst[j ^ sw] = __uint_as_float(v[j]);
       }
-      tc::cluster_sync();
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the bulk copies read part
+      tc::cluster_sync();  // every CTA staged; every ring is idle
+      if (threadIdx.x == 0) {
+        tc::mbar_expect_tx(rbar, (SPLIT - 1) * S::slice_bytes);
+        for (int q = 1; q < SPLIT; ++q) {
+          const int j = (z + q) % SPLIT, slot = z < j ? z : z - 1;
+          tc::bulk_copy_to_peer(tc::cluster_addr(tc::smem_u32(recv) + slot * S::slice_bytes, (uint32_t)j),
+                                tc::smem_u32(part) + j * S::slice_bytes, S::slice_bytes,
+                                tc::cluster_addr(tc::smem_u32(rbar), (uint32_t)j));
+        }
+      }
+      tc::mbar_wait(rbar, tiles & 1, g.err, 4, abort);
       TileCtx sub = ctx;
       sub.n0 = ctx.n0 + z * W;
       sub.n_valid = min(W, ctx.n_valid - z * W);
-      if (sub.n_valid > 0) {
-        const int q4 = (sub.n_valid + 3) >> 2;
-        const uint32_t mine = tc::smem_u32(part + (size_t)z * 128 * S::part_ld);
-        uint32_t src[SPLIT];
+      sub.swz = 31;
+      float *mine = part + (size_t)z * 128 * W;
+      if (sub.n_valid > 0 && !*abort) {
+        constexpr int n4 = 128 * W / 4;
+        float4 *m4 = (float4 *)mine;
+        for (int i = threadIdx.x; i < n4; i += 128) {
+          float4 v[SPLIT];
 #pragma unroll
-        for (int j = 0; j < SPLIT; ++j) src[j] = tc::cluster_addr(mine, (uint32_t)j);
-        // four float4 columns per thread per step, all remote reads in flight
-        for (int i0 = threadIdx.x; i0 < 128 * q4; i0 += 4 * 128) {
-          float4 v[4][SPLIT];
+          for (int q = 0; q < SPLIT; ++q)
+            v[q] = q == z ? m4[i] : ((const float4 *)(recv + (size_t)(q < z ? q : q - 1) * 128 * W))[i];
+          float4 acc = v[0];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int idx = min(i0 + 128 * u, 128 * q4 - 1);
-            const int r = idx / q4, q = idx - r * q4;
-            const uint32_t off = (uint32_t)((r * S::part_ld + 4 * q) * 4);
-#pragma unroll
-            for (int j = 0; j < SPLIT; ++j) v[u][j] = tc::ld_cluster_f4(src[j] + off);
+          for (int q = 1; q < SPLIT; ++q) {  // rank order
+            acc.x += v[q].x;
+            acc.y += v[q].y;
+            acc.z += v[q].z;
+            acc.w += v[q].w;
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int idx = i0 + 128 * u;
-            if (idx < 128 * q4) {
-              const int r = idx / q4, q = idx - r * q4;
-              float4 acc = v[u][0];
-#pragma unroll
-              for (int j = 1; j < SPLIT; ++j) {
-                acc.x += v[u][j].x;
-                acc.y += v[u][j].y;
-                acc.z += v[u][j].z;
-                acc.w += v[u][j].w;
-              }
-              float *d = red + r * S::red_ld + 4 * q;
-              d[0] = acc.x;
-              d[1] = acc.y;
-              d[2] = acc.z;
-              d[3] = acc.w;
-            }
-          }
+          m4[i] = acc;
         }
         __syncthreads();
-        epi(red, S::red_ld, sub, extra);
+        epi(mine, W, sub, (unsigned char *)recv);
       }
       tc::cluster_sync();
     }

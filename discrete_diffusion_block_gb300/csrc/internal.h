@@ -31,14 +31,18 @@ cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, in
 // E <= 256; k <= 16.
 // moe_scatter: from those, the stable counting sort of the pairs by expert:
 // offs[E+1], slot_row[T*k] (sorted row of pair t*k+s; pass the rank array in
-// as slot_row, it is overwritten), x_perm[row] = xn[token of the row],
-// work[2*max_work] = (expert, first row) items of up to `tile_rows` rows,
+// as slot_row, it is overwritten), the item tiles x_tiles (below), and
+// work[2*max_work] = (expert, first row) items of up to `tile_rows` = 128 rows,
 // *n_work.  `work` holds moe_work_ints() ints: the item list, then one
 // counter per item and a unit counter used by moe_ffn, all zeroed here.
 // max_work: the item capacity the work buffer was sized for (moe_max_work of
 // the largest T it serves); moe_ffn must be given the same value.
 // stats (optional, device, 2 x u64): += experts with at least one row, += T*k.
+// Item tiles: item i's rows as d/64 operand tiles of 128 rows x 64 columns
+// (16 KB each, item-major, row r's 16-byte chunk c at position c ^ (r % 8)),
+// moe_item_tile_elems(max_work, d) elements in all.
 constexpr int kRouteTok = 32;
+inline size_t moe_item_tile_elems(int max_work, int cols) { return (size_t)max_work * 128 * cols; }
 size_t moe_group_count_ints(int T, int E);
 cudaError_t moe_norm_route(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
                            int E, int k, int *ids, float *gates, int *rank, int *gcount, int *err,
@@ -46,14 +50,17 @@ cudaError_t moe_norm_route(const float *h, const float *gain, float eps, bf16 *x
 cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k, int *ids, float *gates,
                       int *rank, int *gcount, int *err, cudaStream_t st);
 cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
-                        int k, int tile_rows, bf16 *x_perm, int *offs, int *work, int *n_work, int max_work,
+                        int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
                         cudaStream_t st, unsigned long long *stats = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
 size_t moe_work_ints(int T, int k, int E, int tile_rows);
-// Routed experts of one layer (kernels_moe.cu): act = SwiGLU(x_perm Wg^T, x_perm Wu^T),
-// y = act Wd^T, for every work item of moe_route; one persistent launch.
-cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
-                    const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act,
+// Routed experts of one layer (kernels_moe.cu): act = SwiGLU(X Wg^T, X Wu^T),
+// y = act Wd^T, for every work item of moe_scatter; one persistent launch.
+// X: the item tiles of moe_scatter; wgu / wd: expert weights as operand tiles
+// (the fill kernels' layout); act_tiles: moe_item_tile_elems(max_work, F)
+// elements of scratch; y: [rows][d] fp32, row = sorted pair row.
+cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
+                    const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
                     float *y, int *err, cudaStream_t st);
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
@@ -80,8 +87,7 @@ cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOu
                      cudaStream_t st);
 cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
                           cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
-cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
-                           cudaStream_t st);  // out[T][N] = act . w^T
+  // out[T][N] = act . w^T
 constexpr int kExpertTileRows = 128;  // token rows per expert work item (MMA N <= 128)
 // xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
 // the logits are then w_out . (xn + xn_lo).

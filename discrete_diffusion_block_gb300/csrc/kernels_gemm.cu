@@ -85,10 +85,10 @@ struct EpiQkv {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int t = min(tb + q * nw, nt - 1), tt = t0 + t;
-            a0[q] = tile[f * ldc + tt];
-            a1[q] = tile[(f + 1) * ldc + tt];
-            b0[q] = tile[(f + half) * ldc + tt];
-            b1[q] = tile[(f + half + 1) * ldc + tt];
+            a0[q] = tile[f * ldc + (tt ^ (f & c.swz))];
+            a1[q] = tile[(f + 1) * ldc + (tt ^ ((f + 1) & c.swz))];
+            b0[q] = tile[(f + half) * ldc + (tt ^ ((f + half) & c.swz))];
+            b1[q] = tile[(f + half + 1) * ldc + (tt ^ ((f + half + 1) & c.swz))];
             c0[q] = cs[t * half + j];
             c1[q] = cs[t * half + j + 1];
             s0[q] = sn[t * half + j];
@@ -140,43 +140,8 @@ struct EpiResidual {
           for (int u = 0; u < 16; ++u) {
             const int t = tb + u * nw, f = f0 + 32 * g + lane;
             if (f < c.m_valid && t < c.n_valid)
-              h[(size_t)(c.n0 + t) * ldh + c.m0 + f] = v[g][u] + tile[f * ldc + t];
+              h[(size_t)(c.n0 + t) * ldh + c.m0 + f] = v[g][u] + tile[f * ldc + (t ^ (f & c.swz))];
           }
-      }
-    }
-  }
-};
-
-// out[token][feature] = tile (grouped launches address rows from b_base).
-// Four tokens x four feature groups per step, reads before writes.
-struct EpiStore {
-  static constexpr size_t extra_smem = 0;
-  float *out;
-  int ldo;
-  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int f0 = 0; f0 < c.m_valid; f0 += 128) {
-      for (int tb = warp; tb < c.n_valid; tb += 4 * nw) {
-        float v[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int t = min(tb + q * nw, c.n_valid - 1), f = min(f0 + 32 * g + lane, c.m_valid - 1);
-            v[q][g] = tile[f * ldc + t];
-          }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int t = tb + q * nw;
-          if (t < c.n_valid) {
-            float *orow = out + (size_t)(c.b_base + c.n0 + t) * ldo + c.m0;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int f = f0 + 32 * g + lane;
-              if (f < c.m_valid) orow[f] = v[q][g];
-            }
-          }
-        }
       }
     }
   }
@@ -295,10 +260,10 @@ static int plain_clusters(int units, int split) {
   return nc < 1 ? 1 : nc;
 }
 
-// Split for a plain projection: the largest of 8, 4, 2, 1 that keeps at least
+// Split for a plain projection: the largest of 4, 2, 1 that keeps at least
 // two K tiles per split and every CTA resident at once.
 static int pick_split(int units, int kt) {
-  int s = 8;
+  int s = 4;
   while (s > 1 && (kt < 2 * s || units * s > num_sms())) s >>= 1;
   return s;
 }
@@ -307,7 +272,6 @@ template <class Epi>
 static cudaError_t launch_split(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
                                 const Epi &epi, int n_clusters, int split, cudaStream_t st) {
   switch (split) {
-    case 8: return launch_tc_sk<8>(ta, tb, g, epi, n_clusters, st);
     case 4: return launch_tc_sk<4>(ta, tb, g, epi, n_clusters, st);
     case 2: return launch_tc_sk<2>(ta, tb, g, epi, n_clusters, st);
     default: return launch_tc_sk<1>(ta, tb, g, epi, n_clusters, st);
@@ -339,15 +303,5 @@ cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, f
   return launch_split(ta, tb, targs(N, T, K, err), epi, plain_clusters(units, split), split, st);
 }
 
-cudaError_t gemm_store_f32(const bf16 *act, const bf16 *w, int T, int K, int N, float *out, int *err,
-                           cudaStream_t st) {
-  CUtensorMap ta, tb;
-  TMAP(ta, w, N, K, 128);
-  TMAP(tb, act, T, K, 64);
-  EpiStore epi{out, N};
-  const int units = ceil_div(N, 128) * ceil_div(T, tc::kSkBN);
-  const int split = pick_split(units, K / tc::kBK);
-  return launch_split(ta, tb, targs(N, T, K, err), epi, plain_clusters(units, split), split, st);
-}
 
 }  // namespace dg

@@ -34,22 +34,52 @@ __global__ void fill_weights_kernel(bf16 *dst, uint64_t n, uint32_t k0, uint32_t
     dst[j] = weight_element(e0 + j, tid, k0, k1, scale);
 }
 
-// W_gate / W_up (logical [E][F][d]) into the interleaved [E][F/64][2][64][d].
+// Expert weights are stored as operand tiles: a matrix with 128-row blocks
+// and K-tiles of 64 columns is laid out [row block][k-tile][128][64], each
+// 16 KB tile in the shared-memory order the tensor core reads (row r's
+// 16-byte chunk c at chunk position c ^ (r % 8)), so that one contiguous bulk
+// copy moves a tile.  Physical element p of a tile: row r = p / 64, logical
+// column 8 ((p / 8 % 8) ^ (r % 8)) + p % 8 of the tile.
+__device__ __forceinline__ void tile_coords(uint64_t j, int KT, uint64_t *blk, int *kt, int *r, int *c) {
+  const int p = (int)(j & 8191);
+  const uint64_t t = j >> 13;
+  *kt = (int)(t % KT);
+  *blk = t / KT;
+  *r = p >> 6;
+  *c = *kt * 64 + ((((p >> 3) & 7) ^ (*r & 7)) << 3) + (p & 7);
+}
+
+// W_gate / W_up (logical [E][F][d]) as tiles of 128-row blocks that hold 64
+// gate rows then the matching 64 up rows (block fb of expert e: features
+// 64 fb .. 64 fb + 63), K = d.
 __global__ void fill_gate_up_kernel(bf16 *dst, int E, int F, int d, uint32_t k0, uint32_t k1,
                                     uint32_t tid_gate, uint32_t tid_up, float scale) {
   const uint64_t n = (uint64_t)E * 2 * F * d;
+  const int KT = d / 64, mA = F / 64;
   for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
        j += (uint64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(j % d);
-    uint64_t rest = j / d;
-    const int r = (int)(rest % 64);
-    rest /= 64;
-    const int which = (int)(rest % 2);
-    rest /= 2;
-    const int fb = (int)(rest % (F / 64));
-    const int e = (int)(rest / (F / 64));
-    const uint64_t logical = ((uint64_t)e * F + fb * 64 + r) * d + c;
-    dst[j] = weight_element(logical, which ? tid_up : tid_gate, k0, k1, scale);
+    uint64_t blk;
+    int kt, r, c;
+    tile_coords(j, KT, &blk, &kt, &r, &c);
+    const int fb = (int)(blk % mA), e = (int)(blk / mA);
+    const uint64_t logical = ((uint64_t)e * F + fb * 64 + (r & 63)) * d + c;
+    dst[j] = weight_element(logical, r >= 64 ? tid_up : tid_gate, k0, k1, scale);
+  }
+}
+
+// W_down (logical [E][d][F]) as tiles of 128-row blocks, K = F.
+__global__ void fill_down_kernel(bf16 *dst, int E, int F, int d, uint32_t k0, uint32_t k1, uint32_t tid,
+                                 float scale) {
+  const uint64_t n = (uint64_t)E * d * F;
+  const int KT = F / 64, mB = d / 128;
+  for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
+       j += (uint64_t)gridDim.x * blockDim.x) {
+    uint64_t blk;
+    int kt, r, c;
+    tile_coords(j, KT, &blk, &kt, &r, &c);
+    const int mb = (int)(blk % mB), e = (int)(blk / mB);
+    const uint64_t logical = ((uint64_t)e * d + mb * 128 + r) * F + c;
+    dst[j] = weight_element(logical, tid, k0, k1, scale);
   }
 }
 
@@ -317,7 +347,9 @@ cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F,
                                                         (uint32_t)(seed >> 32), base + 5, base + 6,
                                                         weight_scale(std_dev));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return fill_weights(wd, (uint64_t)E * d * F, seed, base + 7, 0, std_dev, st);
+  fill_down_kernel<<<grid_for(n, 256), 256, 0, st>>>(wd, E, F, d, (uint32_t)seed, (uint32_t)(seed >> 32), base + 7,
+                                                     weight_scale(std_dev));
+  return cudaGetLastError();
 }
 
 cudaError_t fill_const(float *dst, size_t n, float v, cudaStream_t st) {

@@ -15,11 +15,18 @@
 // published their outputs (per-item counter, release/acquire, then a proxy
 // fence before the TMA reads them).
 //
+// Operands.  Expert weights and the item rows (gathered by moe_scatter, and
+// the SwiGLU output written here by phase A) are stored as 16 KB tiles of 128
+// rows x 64 columns already in the tensor core's swizzled shared-memory order,
+// so each k-step of a unit stages its operands with two contiguous bulk
+// copies (the weight tile, the item's valid rows) instead of row-by-row
+// tensor copies.
+//
 // Roles (192 threads):
 //   warp 4, one thread  -- takes units, hands them to the other roles through
-//                          a 4-deep shared-memory queue, and streams A (the
-//                          expert's weight rows, 128 x 64 boxes) and B (the
-//                          item's rows, 64 x 64 boxes) into a 4-stage ring;
+//                          a 4-deep shared-memory queue, and streams A (one
+//                          weight tile) and B (the item's rows) per k-step
+//                          into a 6-stage ring;
 //   warp 5, one thread  -- owns 2 x 128 TMEM columns and issues tcgen05.mma
 //                          (M = 128, N = rows rounded up to 16), unit n into
 //                          accumulator n & 1;
@@ -59,18 +66,33 @@ struct FfnSmem {
 struct UnitInfo {
   int u;        // unit index, -1 = no more units
   int phase;    // 0: gate/up, 1: down
-  int item, mt, b_row, n_valid, a_row, pad;
+  int item, mt, b_row, n_valid, e, pad;
 };
 
+// Operands are stored as 16 KB tiles (128 rows x 64 columns, in the
+// tensor core's 128-byte swizzled shared-memory order), [row block][k-tile];
+// one contiguous bulk copy moves a weight tile, one moves the valid rows of
+// an item's tile.
 struct FfnArgs {
   const int *work, *n_work, *offs;
+  const bf16 *wgu, *wd;  // [E][2F/128][d/64] and [E][d/128][F/64] tiles
+  const bf16 *x;         // [item][d/64] tiles: the item's token rows
   int *done;   // [max_work] phase A units finished per item
   int *next;   // unit counter
   int E, d, F;
-  bf16 *act;   // [rows][F]
+  bf16 *act;   // [item][F/64] tiles: SwiGLU output rows
   float *y;    // [rows][d]
   int *err;
 };
+
+constexpr int kTileElems = 128 * 64;
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
@@ -86,10 +108,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
 
 __device__ __forceinline__ float swiglu_f(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
-__global__ void __launch_bounds__(kFfnThreads, 1)
-    moe_ffn_kernel(const __grid_constant__ CUtensorMap ta_gu, const __grid_constant__ CUtensorMap tb_x,
-                   const __grid_constant__ CUtensorMap ta_d, const __grid_constant__ CUtensorMap tb_act,
-                   FfnArgs g) {
+__global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   using S = FfnSmem;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -161,16 +180,17 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           const int e0 = g.offs[e];
           inf.b_row = e0 + n0;
           inf.n_valid = min(kFfnBN, g.offs[e + 1] - e0 - n0);
-          inf.a_row = e * (inf.phase ? g.d : 2 * g.F) + inf.mt * 128;
+          inf.e = e;
         }
         queue[q] = inf;
         mbar_arrive(q_full + q);  // release: the entry is visible to the waiting roles
         if (inf.u < 0) break;
-        const CUtensorMap *ma = inf.phase ? &ta_d : &ta_gu;
-        const CUtensorMap *mb = inf.phase ? &tb_act : &tb_x;
         const int KT = inf.phase ? KTB : KTA;
-        const int nb = (inf.n_valid + 63) >> 6;
-        const uint32_t tx = kFfnABytes + (uint32_t)nb * tc::kBChunkBytes;
+        const bf16 *asrc = inf.phase ? g.wd + (size_t)(inf.e * mB + inf.mt) * KTB * kTileElems
+                                     : g.wgu + (size_t)(inf.e * mA + inf.mt) * KTA * kTileElems;
+        const bf16 *bsrc = (inf.phase ? g.act : g.x) + (size_t)inf.item * KT * kTileElems;
+        const uint32_t b_bytes = (uint32_t)((inf.n_valid + 7) & ~7) * 128;  // the item's valid rows
+        const uint32_t tx = kFfnABytes + b_bytes;
         if (inf.phase) {
           // the item's act rows: every phase A unit of it must have published
           const long long t0 = clock64();
@@ -189,9 +209,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 23, abort);
           if (*abort) break;
           tc::mbar_expect_tx(full + s, tx);
-          tc::tma_load_2d(a_tile(s), ma, kt * tc::kBK, inf.a_row, full + s);
-          for (int c = 0; c < nb; ++c)
-            tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, mb, kt * tc::kBK, inf.b_row + 64 * c, full + s);
+          bulk_load(a_tile(s), asrc + (size_t)kt * kTileElems, kFfnABytes, full + s);
+          bulk_load(b_tile(s), bsrc + (size_t)kt * kTileElems, b_bytes, full + s);
         }
         if (*abort) {  // drain the copies in flight (bounded), then hand over the end marker
           for (int i = it - 1; i >= 0 && i >= it - kFfnStages; --i) {
@@ -264,9 +283,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         epi_sync();
         if (inf.phase == 0) {
           // SwiGLU: rows j and 64 + j hold the gate and up projections of
-          // feature 64 * mt + j; each lane writes two adjacent features.
+          // feature 64 * mt + j; each lane writes two adjacent features of an
+          // item row into the act tile (item, k-tile mt) of the down GEMM.
           const int j = 2 * lane;
-          bf16 *dst = g.act + (size_t)(inf.b_row + h0) * g.F + inf.mt * 64 + j;
+          unsigned char *blk = (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + inf.mt) * kTileElems);
           for (int tb = warp; tb < nh; tb += 16) {
             float g0[4], g1[4], u0[4], u1[4];
 #pragma unroll
@@ -279,9 +299,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const int t = tb + 4 * k;
+              const int t = tb + 4 * k, r = h0 + t;
               if (t < nh)
-                *(__nv_bfloat162 *)(dst + (size_t)t * g.F) =
+                *(__nv_bfloat162 *)(blk + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2))) =
                     __floats2bfloat162_rn(swiglu_f(g0[k], u0[k]), swiglu_f(g1[k], u1[k]));
             }
           }
@@ -337,23 +357,15 @@ int ffn_num_sms() {
 
 }  // namespace
 
-cudaError_t tmap_bf16_cached(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
-                             uint32_t box);
-
-cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
-                    const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act,
+cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
+                    const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
                     float *y, int *err, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  if (d % 128 || F % 64 || (2 * F) % 128) return cudaErrorInvalidValue;
+  if (d % 128 || F % 64) return cudaErrorInvalidValue;
   static_assert(FfnSmem::bytes <= 232448, "shared memory of the expert FFN");
-  CUtensorMap ta_gu, tb_x, ta_d, tb_act;
-  cudaError_t e;
-  if ((e = tmap_bf16_cached(&ta_gu, wgu, (uint64_t)E * 2 * F, d, 128)) != cudaSuccess) return e;
-  if ((e = tmap_bf16_cached(&tb_x, x_perm, rows, d, 64)) != cudaSuccess) return e;
-  if ((e = tmap_bf16_cached(&ta_d, wd, (uint64_t)E * d, F, 128)) != cudaSuccess) return e;
-  if ((e = tmap_bf16_cached(&tb_act, act, rows, F, 64)) != cudaSuccess) return e;
   static unsigned long long attr_set = 0;
   int dev = 0;
+  cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
     e = cudaFuncSetAttribute(moe_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FfnSmem::bytes);
@@ -364,16 +376,18 @@ cudaError_t moe_ffn(const bf16 *x_perm, int rows, const bf16 *wgu, const bf16 *w
   g.work = work;
   g.n_work = n_work;
   g.offs = offs;
-  g.done = const_cast<int *>(work) + 2 * max_work;  // zeroed by moe_route
+  g.wgu = wgu;
+  g.wd = wd;
+  g.x = x_tiles;
+  g.done = const_cast<int *>(work) + 2 * max_work;  // zeroed by moe_scatter
   g.next = g.done + max_work;
   g.E = E;
   g.d = d;
   g.F = F;
-  g.act = act;
+  g.act = act_tiles;
   g.y = y;
   g.err = err;
-  return launch_pdl(moe_ffn_kernel, dim3(ffn_num_sms()), dim3(kFfnThreads), FfnSmem::bytes, st, ta_gu, tb_x,
-                    ta_d, tb_act, g);
+  return launch_pdl(moe_ffn_kernel, dim3(ffn_num_sms()), dim3(kFfnThreads), FfnSmem::bytes, st, g);
 }
 
 }  // namespace dg

@@ -510,7 +510,7 @@ struct ScatArgs {
   const bf16 *xn;
   const int *ids, *gcount;
   int *slot_row;  // in: rank within the token group; out: sorted row
-  bf16 *x_perm;
+  bf16 *x_tiles;  // [item][d/64] tiles of 128 rows x 64 columns, swizzled
   int T, d, E, k, tile_rows, ng;
   int *offs, *work, *n_work, *sync;
   int max_work;
@@ -542,12 +542,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
 }
 
 __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
-  extern __shared__ int tab[];  // [ng][E]: pairs of e in earlier groups; then offs[E]
+  extern __shared__ int tab[];  // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]
   __shared__ int warp_tot[kScatThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int E = a.E, ng = a.ng, n = ng * E;
-  int *soffs = tab + n;
+  int *soffs = tab + n, *stoff = soffs + E;
   for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
   __syncthreads();
   const int e = threadIdx.x;  // E <= kScatThreads
@@ -558,13 +558,15 @@ __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
       tab[g * E + e] = tot;
       tot += c;
     }
-  int total;
+  int total, n_items;
   const int off = block_exclusive_scan(tot, warp_tot, &total);
-  if (e < E) soffs[e] = off;
+  const int tiles = e < E ? (tot + a.tile_rows - 1) / a.tile_rows : 0;
+  const int toff = block_exclusive_scan(tiles, warp_tot, &n_items);
+  if (e < E) {
+    soffs[e] = off;
+    stoff[e] = toff;
+  }
   if (blockIdx.x == 0) {  // the expert segments and the work list of the expert FFN
-    const int tiles = e < E ? (tot + a.tile_rows - 1) / a.tile_rows : 0;
-    int n_items;
-    const int toff = block_exclusive_scan(tiles, warp_tot, &n_items);
     int touched;
     block_exclusive_scan(e < E && tot > 0 ? 1 : 0, warp_tot, &touched);
     if (e < E) {
@@ -585,25 +587,31 @@ __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
     for (int i = threadIdx.x; i <= a.max_work; i += kScatThreads) a.sync[i] = 0;  // FFN counters
   }
   __syncthreads();
-  // Pairs of this block: one warp per pair; the warp copies the token's row.
+  // Pairs of this block: one warp per pair; the warp copies the token's row
+  // into row r of its item's tiles (16-byte chunk c of k-tile kt at chunk
+  // position c ^ (r % 8): the tensor core's swizzled operand order).
   const int TK = a.T * a.k, per = (TK + gridDim.x - 1) / gridDim.x;
   const int p0 = blockIdx.x * per, p1 = min(TK, p0 + per);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
   for (int p = p0 + warp; p < p1; p += kScatThreads / 32) {
     const int ex = a.ids[p], t = p / a.k, g = t / kRouteTok;
-    const int row = soffs[ex] + tab[g * E + ex] + a.slot_row[p];
+    const int within = tab[g * E + ex] + a.slot_row[p];  // rank among the expert's rows
+    const int row = soffs[ex] + within;
     __syncwarp();
     if (lane == 0) a.slot_row[p] = row;
+    const int item = stoff[ex] + within / a.tile_rows, r = within % a.tile_rows;
     const uint4 *src = (const uint4 *)(a.xn + (size_t)t * a.d);
-    uint4 *dst = (uint4 *)(a.x_perm + (size_t)row * a.d);
+    uint4 *dst = (uint4 *)(a.x_tiles + (size_t)item * KT * (128 * 64)) + r * 8;
     constexpr int U = 4;
     for (int c = lane; c < vec; c += 32 * U) {
       uint4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) v[u] = c + 32 * u < vec ? src[c + 32 * u] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (c + 32 * u < vec) dst[c + 32 * u] = v[u];
+      for (int u = 0; u < U; ++u) {
+        const int cc = c + 32 * u;
+        if (cc < vec) dst[(cc >> 3) * 1024 + ((cc & 7) ^ (r & 7))] = v[u];
+      }
     }
   }
 }
@@ -637,16 +645,16 @@ cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k
 }
 
 cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
-                        int k, int tile_rows, bf16 *x_perm, int *offs, int *work, int *n_work, int max_work,
+                        int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
                         cudaStream_t st, unsigned long long *stats) {
-  if (T < 0 || d % 8 || E < 1 || E > kScatThreads || k < 1) return cudaErrorInvalidValue;
+  if (T < 0 || d % 64 || E < 1 || E > kScatThreads || k < 1 || tile_rows != 128) return cudaErrorInvalidValue;
   if ((size_t)max_work < moe_max_work(T, k, E, tile_rows)) return cudaErrorInvalidValue;
   ScatArgs a;
   a.xn = xn;
   a.ids = ids;
   a.gcount = gcount;
   a.slot_row = slot_row;
-  a.x_perm = x_perm;
+  a.x_tiles = x_tiles;
   a.T = T;
   a.d = d;
   a.E = E;
@@ -659,7 +667,7 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
   a.sync = work + 2 * max_work;
   a.max_work = max_work;
   a.stats = stats;
-  const size_t smem = ((size_t)a.ng * E + E) * sizeof(int);
+  const size_t smem = ((size_t)a.ng * E + 2 * E) * sizeof(int);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static unsigned long long attr_set = 0;
   int dev = 0;

@@ -197,9 +197,16 @@ int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t
  *   WQKV             [(Hq + 2 Hkv) * hd][d]   rows: W_q, then W_k, then W_v
  *   WO               [d][Hq * hd]
  *   ROUTER           [E][d]
- *   W_GATE_UP        [E][F/64][2][64][d]      per expert, 64-row blocks of
- *                                             W_gate then W_up interleaved
- *   W_DOWN           [E][d][F]
+ *   W_GATE_UP        [E][F/64][d/64] tiles    tile (e, b, j): rows 64 b .. 64 b + 63
+ *                                             of W_gate,e then the same rows of
+ *                                             W_up,e; columns 64 j .. 64 j + 63
+ *   W_DOWN           [E][d/128][F/64] tiles   tile (e, b, j): rows 128 b ..
+ *                                             128 b + 127 of W_down,e; columns
+ *                                             64 j .. 64 j + 63
+ *   A tile is 128 rows x 64 bf16 columns, 16 KB, row-major with 128-byte rows
+ *   in which the 16-byte chunk c of row r sits at chunk position c ^ (r % 8)
+ *   (the tensor core's 128-byte-swizzled operand order, so that one bulk
+ *   copy stages a tile).
  *   ATTN_NORM, MOE_NORM, FINAL_NORM  [d] (fp32 gains, initialised to 1) */
 enum {
     DG_W_EMBED = 0, DG_W_LM_HEAD = 1, DG_W_FINAL_NORM = 2, DG_W_WQKV = 3, DG_W_WO = 4,

@@ -31,19 +31,33 @@ def test_weight_generator_bit_exact(tid, e0, n):
     assert np.array_equal(got, ref)
 
 
+def untile(phys, lead, blocks, kt):
+    """Operand tiles [*lead][blocks][kt][128][64] (16-byte chunk c of row r
+    stored at chunk position c ^ (r % 8)) back to the row-major matrix
+    [*lead][blocks * 128][kt * 64]."""
+    t = phys.reshape(*lead, blocks, kt, 128, 8, 8)
+    r = np.arange(128)[:, None]
+    pos = np.arange(8)[None, :] ^ (r % 8)          # position of logical chunk c in row r
+    t = np.take_along_axis(t, np.broadcast_to(pos[..., None], (128, 8, 8)).reshape((1,) * (t.ndim - 3) + (128, 8, 8)), axis=-2)
+    t = t.reshape(*lead, blocks, kt, 128, 64)
+    return np.moveaxis(t, -3, -2).reshape(*lead, blocks * 128, kt * 64)
+
+
 def test_moe_weight_layout_matches_logical_tensors():
-    d, E, F, L = 128, 4, 192, 3
+    d, E, F, L = 256, 4, 192, 3
     wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
     wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
     wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
     dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, L, 5, 0.02)
     base = 100 + 16 * L
     assert np.array_equal(bf16_to_f32(wr).reshape(E, d), ow.tensor(5, base + 4, (E, d), 0.02))
-    gu = bf16_to_f32(wgu).reshape(E, F // 64, 2, 64, d)
+    # gate/up: 128-row blocks of 64 gate rows then the same 64 up rows
+    gu = untile(bf16_to_f32(wgu), (E,), F // 64, d // 64).reshape(E, F // 64, 2, 64, d)
     g = ow.tensor(5, base + 5, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
     u = ow.tensor(5, base + 6, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
     assert np.array_equal(gu[:, :, 0], g) and np.array_equal(gu[:, :, 1], u)
-    assert np.array_equal(bf16_to_f32(wd).reshape(E, d, F), ow.tensor(5, base + 7, (E, d, F), 0.02))
+    wdl = untile(bf16_to_f32(wd), (E,), d // 128, F // 64)
+    assert np.array_equal(wdl, ow.tensor(5, base + 7, (E, d, F), 0.02))
 
 
 # ---- sampler: bit-exact given identical logits --------------------------------
