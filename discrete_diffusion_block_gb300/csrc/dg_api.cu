@@ -798,19 +798,29 @@ int dg_read_kv(dg_model *m, int32_t layer, int32_t pos0, int32_t n, uint16_t *k_
   if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > m->n_pages * c.page_size)
     return fail(DG_EINVAL, "bad range");
   const int hd = c.head_dim, Hkv = c.n_kv_heads, pg = c.page_size;
-  for (int t = 0; t < n; ++t) {
-    const int p = pos0 + t;
-    const size_t base = (size_t)m->page_table_host[p / pg] * Hkv * pg * hd + (size_t)(p % pg) * hd;
-    for (int h = 0; h < Hkv; ++h) {
-      const size_t off = base + (size_t)h * pg * hd;
-      const size_t dst = ((size_t)t * Hkv + h) * hd;
-      if (k_out)
-        CK(cudaMemcpyAsync(k_out + dst, m->kpool(layer) + off, hd * 2, cudaMemcpyDeviceToHost, m->stream));
-      if (v_out)
-        CK(cudaMemcpyAsync(v_out + dst, m->vpool(layer) + off, hd * 2, cudaMemcpyDeviceToHost, m->stream));
+  if (n == 0) return DG_OK;
+  // whole pages to the host, then slot rows out of the pool's tiled order
+  // (element f of slot s: sub-block f / 64, row s, chunk ((f % 64) / 8) ^ (s % 8))
+  const size_t page_elems = (size_t)Hkv * pg * hd;
+  std::vector<uint16_t> kb(page_elems), vb(page_elems);
+  for (int pl = pos0 / pg; pl <= (pos0 + n - 1) / pg; ++pl) {
+    const size_t off = (size_t)m->page_table_host[pl] * page_elems;
+    if (k_out) CK(cudaMemcpyAsync(kb.data(), m->kpool(layer) + off, page_elems * 2, cudaMemcpyDeviceToHost, m->stream));
+    if (v_out) CK(cudaMemcpyAsync(vb.data(), m->vpool(layer) + off, page_elems * 2, cudaMemcpyDeviceToHost, m->stream));
+    SYNC(m);
+    const int t0 = pl * pg > pos0 ? pl * pg : pos0, t1 = (pl + 1) * pg < pos0 + n ? (pl + 1) * pg : pos0 + n;
+    for (int p = t0; p < t1; ++p) {
+      const int sl = p % pg;
+      for (int h = 0; h < Hkv; ++h)
+        for (int f = 0; f < hd; ++f) {
+          const size_t src = (size_t)h * pg * hd + (size_t)(f / 64) * pg * 64 + (size_t)sl * 64 +
+                             ((((f % 64) / 8) ^ (sl % 8)) * 8) + f % 8;
+          const size_t dst = ((size_t)(p - pos0) * Hkv + h) * hd + f;
+          if (k_out) k_out[dst] = kb[src];
+          if (v_out) v_out[dst] = vb[src];
+        }
     }
   }
-  SYNC(m);
   return DG_OK;
 }
 

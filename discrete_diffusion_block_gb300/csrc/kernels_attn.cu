@@ -9,6 +9,11 @@
 // block for all of them.  Long key ranges are split across blocks and the
 // partial softmax states combined afterwards (split-KV).
 //
+// KV pool layout: a (page, KV head) block of page_size keys is stored as
+// hd/64 sub-blocks [page_size][64] in the tensor core's 128-byte swizzled
+// operand order (16-byte chunk c of slot s at chunk position c ^ (s % 8)), so
+// a 64- or 128-key K or V operand tile is one contiguous bulk copy.
+//
 // The kernel is a tcgen05 tensor-core kernel with two passes over the
 // block's key range:
 //   pass 1  S = Q K^T per 128-key tile (TMEM), running row max m;
@@ -17,11 +22,14 @@
 // The second QK^T costs a third more tensor work and saves the read-modify-
 // write of the accumulator that a one-pass online softmax needs.  Roles:
 // warp 0 streams Q once and the K (and V) tiles of each pass through a
-// two-slot ring with TMA (Q through a 4-D map that packs the G heads of a
-// token as consecutive rows; K and V as 64-key boxes of their pages); warp 1
+// two-slot ring (Q with TMA through a 4-D map that packs the G heads of a
+// token as consecutive rows; K and V with bulk copies of their pages); warp 1
 // issues the MMAs (V is the N-contiguous "MN-major" B operand of P V); warps
 // 2-5 hold one row each and do the softmax on the accumulator rows they read
-// from TMEM.
+// from TMEM.  With the key range split over several blocks, the blocks of
+// one query tile form a cluster: each writes its unnormalised output and
+// softmax state, and after a cluster barrier each block merges a slice of
+// the tile's rows (weights 2^(m_s - m*)).
 #include <cuda.h>
 
 #include <cudaTypedefs.h>
@@ -51,6 +59,7 @@ struct AttnParams {
   float *ml_part;  // [splits][Hkv][rows][2]
   int *err;        // device error word (bounded waits, bad page indices), may be null
   int n_pages;     // physical pages of the pools, 0 when unknown
+  bf16 *final_out; // split launches: where the cluster's merge writes the output
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -62,22 +71,36 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 constexpr int kAttnThreads = 192;
 constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one TMA box)
 
+// Shared memory (bytes from a 1024-aligned base): Q [HB][128 rows][64]; a
+// 3-slot K ring and a 2-slot V ring of 128-key tiles [HB][128 keys][64]; the
+// P tile [2][128 rows][64 keys] (bf16, the A operand of P V); barriers.  After
+// the key loop the K ring holds the fp32 output rows [128][HD] on their way
+// out.
 template <int HD>
 struct AttnSmem {
   static constexpr int HB = HD / 64;                       // 64-wide hd blocks
-  static constexpr size_t q = 0;                           // HB x [128 rows][64] bf16
-  static constexpr size_t q_bytes = (size_t)HB * 16384;
-  static constexpr size_t k_bytes = (size_t)HB * 16384;    // HB x [128 keys][64]
-  static constexpr size_t v_bytes = (size_t)HB * 16384;    // HB x [128 keys][64] (N-contiguous B)
-  static constexpr size_t slot_bytes = k_bytes + v_bytes;
-  static constexpr size_t ring = q + q_bytes;              // 2 slots
-  static constexpr size_t pbuf = ring + 2 * slot_bytes;    // 2 x [128 rows][64 keys] bf16
-  static constexpr size_t pages = pbuf + 32768;            // page of every 64-key half (ints)
-  static constexpr int kMaxHalves = 1024;
-  static constexpr size_t bars = pages + kMaxHalves * 4;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, p_empty, o_full; TMEM slot; abort
-  static constexpr size_t bytes = bars + 12 * 8 + 16 + 1024;
+  static constexpr int kK = 3, kV = 2;                     // ring depths
+  static constexpr size_t tile = (size_t)HB * 16384;       // one 128-key K or V tile, or Q
+  static constexpr size_t q = 0;
+  static constexpr size_t kring = q + tile;
+  static constexpr size_t vring = kring + kK * tile;
+  static constexpr size_t pbuf = vring + kV * tile;        // 2 x [128 rows][64 keys] bf16
+  static constexpr size_t bars = pbuf + 32768;
+  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty, o_full
+  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 3;
+  static constexpr size_t bytes = bars + n_bars * 8 + 16 + 1024;
+  static_assert((size_t)128 * HD * 4 <= kK * tile, "output staging fits the K ring");
 };
+
+// One 64-key half of a K or V operand tile, all zero (keys past the end).
+__device__ __align__(128) unsigned char g_zero_half[kAttnSlotHalfBytes];
+
+__device__ __forceinline__ void attn_bulk(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
 
 __device__ __forceinline__ void attn_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(b)) : "memory");
@@ -95,23 +118,45 @@ __device__ __forceinline__ uint64_t mn_desc(uint32_t saddr) {
   return d;
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Rows whose running maximum grows by more than this (log2 units) rescale
+// their accumulated output; otherwise P = 2^(s - m) stays <= 2^8 and the
+// stale maximum is kept (the final O / l does not depend on m).
+constexpr float kRescaleLog2 = 8.0f;
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, AttnParams p) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tq, AttnParams p) {
   using S = AttnSmem<HD>;
-  constexpr int HB = S::HB;
+  constexpr int HB = S::HB, KK = S::kK, KV = S::kV;
+  constexpr uint32_t kTileBytes = (uint32_t)S::tile;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  int *pages = (int *)(base + S::pages);
   uint64_t *q_full = (uint64_t *)(base + S::bars);
-  uint64_t *kv_full = q_full + 1, *kv_empty = kv_full + 2;
-  uint64_t *s_full = kv_empty + 2, *s_empty = s_full + 2;
+  uint64_t *k_full = q_full + 1, *k_empty = k_full + KK;
+  uint64_t *v_full = k_empty + KK, *v_empty = v_full + KV;
+  uint64_t *s_full = v_empty + KV, *s_empty = s_full + 2;
   uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1, *o_full = p_empty + 1;
   uint32_t *tmem_slot = (uint32_t *)(o_full + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
-  auto k_tile = [&](int slot) { return base + S::ring + (size_t)slot * S::slot_bytes; };
-  auto v_tile = [&](int slot) { return base + S::ring + (size_t)slot * S::slot_bytes + S::k_bytes; };
+  auto k_tile = [&](int slot) { return base + S::kring + (size_t)slot * S::tile; };
+  auto v_tile = [&](int slot) { return base + S::vring + (size_t)slot * S::tile; };
 
   const int g = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,9 +174,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     *abort = 0;
     tc::mbar_init(q_full, 1);
+    for (int i = 0; i < KK; ++i) {
+      tc::mbar_init(k_full + i, 1);
+      tc::mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < KV; ++i) {
+      tc::mbar_init(v_full + i, 1);
+      tc::mbar_init(v_empty + i, 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(kv_full + i, 1);
-      tc::mbar_init(kv_empty + i, 1);
       tc::mbar_init(s_full + i, 1);
       tc::mbar_init(s_empty + i, 4);
     }
@@ -149,17 +200,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   pdl_wait();
   pdl_trigger();
-  // physical page of every 64-key half of this block's range
-  const int n_halves = 2 * n_kt;
-  for (int i = threadIdx.x; i < n_halves && i < S::kMaxHalves; i += blockDim.x) {
-    const int key0 = k_begin + 64 * i;
-    int pg_i = key0 < k_end ? p.page_table[key0 / p.pg] : -1;
-    if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) {  // a page index outside the pool: skip it
-      if (p.err) atomicExch(p.err, 39);
-      pg_i = -1;
-    }
-    pages[i] = pg_i;
-  }
   if (threadIdx.x == 0 && p.err && *(volatile int *)p.err) *abort = 1;
   tc::fence_before();
   __syncthreads();
@@ -169,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (warp == 0) {
     if (lane == 0 && n_kt > 0) {
-      tc::mbar_expect_tx(q_full, (uint32_t)S::q_bytes);
+      tc::mbar_expect_tx(q_full, (uint32_t)(HB * 16384));
       for (int b = 0; b < HB; ++b) {
         asm volatile(
             "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
@@ -177,30 +217,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             "l"((uint64_t)&tq), "r"(64 * b), "r"(0), "r"(g), "r"(r_cta / p.G), "r"(tc::smem_u32(q_full))
             : "memory");
       }
-      // two passes over the tiles; pass 1 loads K only
-      int issued = 0;
-      for (int i = 0; i < 2 * n_kt; ++i, issued = i) {
-        const int pass = i >= n_kt, kt = pass ? i - n_kt : i, slot = i & 1;
-        if (i >= 2) tc::mbar_wait(kv_empty + slot, ((i >> 1) - 1) & 1, p.err, 31, abort);
-        if (*abort) break;
-        tc::mbar_expect_tx(kv_full + slot, (pass ? 4u : 2u) * HB * kAttnSlotHalfBytes);
+      // One 128-key K or V tile: per 64-key half, the page's hd sub-blocks;
+      // two halves of one page that follow each other move as one copy; a
+      // half past the block's last key (or on a bad page index) is a zero
+      // half (its P is zero; V must hold finite values).
+      auto load_tile = [&](const bf16 *pool, unsigned char *dst, int kt, uint64_t *bar) {
+        const int key0 = k_begin + 128 * kt;
+        int pgs[2];
         for (int h = 0; h < 2; ++h) {
-          // a half past the block's last key is fetched from rows before the
-          // tensor's start: the fill value (zero) lands in its slot
-          const int pg_i = pages[2 * kt + h];
-          const int key0 = k_begin + 128 * kt + 64 * h;
-          const int row = pg_i < 0 ? -64 : (pg_i * p.Hkv + g) * p.pg + key0 % p.pg;
-          for (int b = 0; b < HB; ++b) {
-            tc::tma_load_2d(k_tile(slot) + (size_t)b * 16384 + h * kAttnSlotHalfBytes, &tk, 64 * b, row, kv_full + slot);
-            if (pass)
-              tc::tma_load_2d(v_tile(slot) + (size_t)b * 16384 + h * kAttnSlotHalfBytes, &tv, 64 * b, row, kv_full + slot);
+          const int key = key0 + 64 * h;
+          int pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
+          if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) {
+            if (p.err) atomicExch(p.err, 39);
+            pg_i = -1;
           }
+          pgs[h] = pg_i;
         }
+        const bool whole = pgs[0] >= 0 && pgs[1] == pgs[0] && (key0 % p.pg) + 128 <= p.pg;
+        tc::mbar_expect_tx(bar, kTileBytes);
+        for (int h = 0; h < (whole ? 1 : 2); ++h) {
+          const uint32_t bytes = whole ? 2 * kAttnSlotHalfBytes : kAttnSlotHalfBytes;
+          const size_t off = pgs[h] < 0 ? 0
+                                        : ((size_t)pgs[h] * p.Hkv + g) * p.pg * HD + (size_t)((key0 + 64 * h) % p.pg) * 64;
+          for (int b = 0; b < HB; ++b)
+            attn_bulk(dst + (size_t)b * 16384 + h * kAttnSlotHalfBytes,
+                      pgs[h] < 0 ? (const void *)g_zero_half : (const void *)(pool + off + (size_t)b * p.pg * 64), bytes,
+                      bar);
+        }
+      };
+      auto issue_k = [&](int i) {
+        const int slot = i % KK;
+        if (i >= KK) tc::mbar_wait(k_empty + slot, ((i / KK) - 1) & 1, p.err, 31, abort);
+        if (!*abort) load_tile(p.k_pool, k_tile(slot), i, k_full + slot);
+      };
+      auto issue_v = [&](int i) {
+        const int slot = i % KV;
+        if (i >= KV) tc::mbar_wait(v_empty + slot, ((i / KV) - 1) & 1, p.err, 30, abort);
+        if (!*abort) load_tile(p.v_pool, v_tile(slot), i, v_full + slot);
+      };
+      // K runs one tile ahead of V: S of the next tile can start while P V of
+      // this one waits for its V
+      int nk = 0, nv = 0;
+      issue_k(0), ++nk;
+      for (int i = 0; i < n_kt && !*abort; ++i) {
+        if (i + 1 < n_kt) issue_k(i + 1), ++nk;
+        if (*abort) break;
+        issue_v(i), ++nv;
       }
       if (*abort) {  // drain the copies still in flight: the last load of each slot (bounded)
-        for (int i = issued - 1; i >= 0 && i >= issued - 2; --i) {
+        for (int i = nk - 1; i >= 0 && i >= nk - KK; --i) {
           const long long t0 = clock64();
-          while (!tc::mbar_try_wait(kv_full + (i & 1), (i >> 1) & 1) && clock64() - t0 < tc::kWaitCycles) {
+          while (!tc::mbar_try_wait(k_full + i % KK, (i / KK) & 1) && clock64() - t0 < tc::kWaitCycles) {
+          }
+        }
+        for (int i = nv - 1; i >= 0 && i >= nv - KV; --i) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(v_full + i % KV, (i / KV) & 1) && clock64() - t0 < tc::kWaitCycles) {
           }
         }
       }
@@ -210,10 +282,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t idesc_s = tc::idesc_bf16(128, 128);
       const uint32_t idesc_o = tc::idesc_bf16(128, HD) | (1u << 16);  // B (V) N-contiguous
       tc::mbar_wait(q_full, 0, p.err, 32, abort);
-      auto issue_s = [&](int i) {  // S[i & 1] = Q K^T of ring load i
-        const int slot = i & 1, buf = i & 1;
+      auto issue_s = [&](int i) {  // S[i & 1] = Q K_i^T
+        const int slot = i % KK, buf = i & 1;
         if (i >= 2) tc::mbar_wait(s_empty + buf, ((i >> 1) - 1) & 1, p.err, 33, abort);
-        tc::mbar_wait(kv_full + slot, (i >> 1) & 1, p.err, 34, abort);
+        tc::mbar_wait(k_full + slot, (i / KK) & 1, p.err, 34, abort);
         tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -222,42 +294,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc::mma_bf16(t_s + buf * 128, adesc, bdesc, idesc_s, kk ? 1u : 0u);
         }
         tc::mma_commit(s_full + buf);
+        tc::mma_commit(k_empty + slot);
       };
-      for (int i = 0; i < n_kt; ++i) {  // pass 1
-        issue_s(i);
-        tc::mma_commit(kv_empty + (i & 1));
-      }
-      issue_s(n_kt);
-      for (int kt = 0; kt < n_kt; ++kt) {  // pass 2
-        const int i = n_kt + kt, slot = i & 1;
-        if (kt + 1 < n_kt) issue_s(i + 1);
-        tc::mbar_wait(p_full, kt & 1, p.err, 35, abort);
+      issue_s(0);
+      for (int i = 0; i < n_kt; ++i) {
+        if (i + 1 < n_kt) issue_s(i + 1);
+        const int slot = i % KV;
+        tc::mbar_wait(p_full, i & 1, p.err, 35, abort);
+        tc::mbar_wait(v_full + slot, (i / KV) & 1, p.err, 29, abort);
         tc::fence_after();
         const unsigned char *pb = base + S::pbuf;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA
           const uint64_t adesc = tc::sw128_desc(tc::smem_u32(pb + (size_t)(kk >> 2) * 16384)) + 2 * (kk & 3);
           const uint64_t bdesc = mn_desc(tc::smem_u32(v_tile(slot))) + (uint64_t)kk * (2048 >> 4);
-          tc::mma_bf16(t_o, adesc, bdesc, idesc_o, (kt | kk) ? 1u : 0u);
+          tc::mma_bf16(t_o, adesc, bdesc, idesc_o, (i | kk) ? 1u : 0u);
         }
         tc::mma_commit(p_empty);
-        tc::mma_commit(kv_empty + slot);
+        tc::mma_commit(v_empty + slot);
       }
       tc::mma_commit(o_full);
     }
   } else {
-    // ---- softmax warps: thread = query row ----------------------------------
+    // ---- softmax warps: thread = query row, one pass ------------------------
     const int q4 = warp & 3, row = 32 * q4 + lane, r = r_cta + row;
     const bool ok = r < rows_total;
     const int lim = p.causal ? p.n_prefix + (ok ? r / p.G : 0) : n_keys - 1;
+    const int last = min(k_end - 1, lim);  // last key this row sees in the block's range
     const float NEG = __int_as_float(0xff800000);
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     float m = NEG, l = 0.0f;
-    for (int i = 0; i < 2 * n_kt; ++i) {
-      const int pass = i >= n_kt, kt = pass ? i - n_kt : i, buf = i & 1;
+    for (int i = 0; i < n_kt; ++i) {
+      const int buf = i & 1;
       tc::mbar_wait(s_full + buf, (i >> 1) & 1, p.err, 36, abort);
       tc::fence_after();
-      const int key_base = k_begin + 128 * kt;
+      const int key_base = k_begin + 128 * i;
       uint32_t x[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_s + buf * 128 + lane_off + 32 * c, x[c]);
@@ -266,53 +337,74 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::fence_before();
       __syncwarp();
       if (lane == 0) attn_arrive(s_empty + buf);
-      if (!pass) {
+      // scaled scores; keys this row must not see are -inf
+      const int nvalid = min(128, last - key_base + 1);  // <= 0: none
+      float tmax = NEG;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int key = key_base + 32 * c + j;
-            if (key < k_end && key <= lim) m = fmaxf(m, __uint_as_float(x[c][j]) * p.scale_log2);
-          }
-      } else {
-        const float mu = m == NEG ? 0.0f : m;
-        uint32_t pk[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int key = key_base + 32 * c + j;
-            const float p0 = (key < k_end && key <= lim) ? exp2f(__uint_as_float(x[c][j]) * p.scale_log2 - mu) : 0.0f;
-            const float p1 = (key + 1 < k_end && key + 1 <= lim) ? exp2f(__uint_as_float(x[c][j + 1]) * p.scale_log2 - mu) : 0.0f;
-            l += p0 + p1;
-            pk[c][j >> 1] = pack_bf16(p0, p1);
-          }
-        // previous P V done with the buffer?
-        if (kt > 0) tc::mbar_wait(p_empty, (kt - 1) & 1, p.err, 37, abort);
-        unsigned char *prow = base + S::pbuf + (size_t)row * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int h = c >> 1;  // keys 0-63 in box 0, 64-127 in box 1
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {  // 16-byte chunks of this 32-key group
-            const int chunk = (c & 1) * 4 + u;
-            uint4 v = make_uint4(pk[c][4 * u], pk[c][4 * u + 1], pk[c][4 * u + 2], pk[c][4 * u + 3]);
-            *(uint4 *)(prow + (size_t)h * 16384 + ((chunk ^ (row & 7)) << 4)) = v;
-          }
+        for (int j = 0; j < 32; ++j) {
+          float v = __uint_as_float(x[c][j]) * p.scale_log2;
+          if (32 * c + j >= nvalid) v = NEG;
+          x[c][j] = __float_as_uint(v);
+          tmax = fmaxf(tmax, v);
         }
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        __syncwarp();
-        if (lane == 0) attn_arrive(p_full);
+      const float m_new = fmaxf(m, tmax);
+      const bool grow = m_new > m + kRescaleLog2;  // false while both are -inf
+      // P V of the previous tile must be done before P is rewritten and
+      // before O is rescaled
+      if (i > 0) tc::mbar_wait(p_empty, (i - 1) & 1, p.err, 37, abort);
+      if (__any_sync(0xffffffffu, grow) && i > 0) {
+        tc::fence_after();
+        const float f = grow ? ex2(m - m_new) : 1.0f;  // m = -inf: 0 (O holds zeros)
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(t_o + lane_off + 32 * c, o);
+          tc::tmem_ld_wait(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st32(t_o + lane_off + 32 * c, o);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+        l *= f;
       }
+      if (grow) m = m_new;
+      const float mu = m == NEG ? 0.0f : m;
+      uint32_t pk[4][16];
+      float ls = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ex2(__uint_as_float(x[c][j]) - mu), p1 = ex2(__uint_as_float(x[c][j + 1]) - mu);
+          ls += p0 + p1;
+          pk[c][j >> 1] = pack_bf16(p0, p1);
+        }
+      l += ls;
+      unsigned char *prow = base + S::pbuf + (size_t)row * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int h = c >> 1;  // keys 0-63 in box 0, 64-127 in box 1
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {  // 16-byte chunks of this 32-key group
+          const int chunk = (c & 1) * 4 + u;
+          uint4 v = make_uint4(pk[c][4 * u], pk[c][4 * u + 1], pk[c][4 * u + 2], pk[c][4 * u + 3]);
+          *(uint4 *)(prow + (size_t)h * 16384 + ((chunk ^ (row & 7)) << 4)) = v;
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) attn_arrive(p_full);
     }
-    // ---- output -------------------------------------------------------------
+    // ---- output: TMEM -> shared rows -> coalesced stores --------------------
     if (n_kt > 0) {
       tc::mbar_wait(o_full, 0, p.err, 38, abort);
       tc::fence_after();
     }
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    const size_t qrow = ok ? (((size_t)(r / p.G) * p.Hq + g * p.G + r % p.G) * HD) : 0;
-    const size_t prow_o = ((size_t)split * p.Hkv + g) * rows_total + r;
+    float *orow = (float *)(base + S::kring) + (size_t)row * HD;  // the K ring is idle now
 #pragma unroll 1
     for (int c = 0; c < HD / 32; ++c) {
       uint32_t v[32];
@@ -323,28 +415,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0u;
       }
-      if (!ok) continue;
-      if (p.out) {
+      const float sc = p.out ? inv : 1.0f;  // split blocks keep the unnormalised sum
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(v[j + 4]) * inv, __uint_as_float(v[j + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(v[j + 6]) * inv, __uint_as_float(v[j + 7]) * inv);
-          *(uint4 *)(p.out + qrow + 32 * c + j) = w;
-        }
-      } else {
-        float4 *d = (float4 *)(p.o_part + prow_o * HD + 32 * c);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          d[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                             __uint_as_float(v[4 * j + 3]));
+      for (int j = 0; j < 32; j += 4) {  // float4 slot rotated by row: conflict-free
+        const int q = ((32 * c + j) >> 2) ^ (row & 7);
+        *(float4 *)(orow + 4 * q) = make_float4(__uint_as_float(v[j]) * sc, __uint_as_float(v[j + 1]) * sc,
+                                                __uint_as_float(v[j + 2]) * sc, __uint_as_float(v[j + 3]) * sc);
       }
     }
-    if (ok && !p.out) {
-      p.ml_part[prow_o * 2] = m;
-      p.ml_part[prow_o * 2 + 1] = l;
+    if (!p.out && ok) {
+      const size_t prow_o = ((size_t)split * p.Hkv + g) * rows_total + r;
+      *(float2 *)(p.ml_part + prow_o * 2) = make_float2(m, l);
     }
   }
   tc::fence_before();
@@ -353,32 +434,91 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(512u));
   }
-}
-
-// Merge the split-KV partial states of one (row, KV head): weights 2^(m_s - m*).
-__global__ void attn_combine_kernel(const float *o_part, const float *ml_part, int splits, int Hkv,
-                                    int rows_total, int G, int Hq, int HD, bf16 *out) {
-  pdl_wait();
-  pdl_trigger();
-  const int row = blockIdx.x, g = blockIdx.y;
-  const float NEG = __int_as_float(0xff800000);
-  float mx = NEG;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ml_part[(((size_t)s * Hkv + g) * rows_total + row) * 2]);
-  float L = 0.0f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t b = ((size_t)s * Hkv + g) * rows_total + row;
-    const float m = ml_part[b * 2];
-    if (m != NEG) L += exp2f(m - mx) * ml_part[b * 2 + 1];
-  }
-  const int t = row / G, h = g * G + row % G;
-  for (int c = threadIdx.x; c < HD; c += blockDim.x) {
-    float acc = 0.0f;
-    for (int s = 0; s < splits; ++s) {
-      const size_t b = ((size_t)s * Hkv + g) * rows_total + row;
-      const float m = ml_part[b * 2];
-      if (m != NEG) acc += exp2f(m - mx) * o_part[b * HD + c];
+  // Rows out of shared memory, one warp per row, lanes along hd.
+  {
+    const float *stage = (const float *)(base + S::kring);
+    for (int rr = warp; rr < 128; rr += kAttnThreads / 32) {
+      const int r = r_cta + rr;
+      if (r >= rows_total) break;
+      for (int c4 = lane; c4 < HD / 4; c4 += 32) {
+        const float4 v = *(const float4 *)(stage + (size_t)rr * HD + 4 * (c4 ^ (rr & 7)));
+        if (p.out) {
+          const int t = r / p.G, h = g * p.G + r % p.G;
+          uint2 w;
+          w.x = pack_bf16(v.x, v.y);
+          w.y = pack_bf16(v.z, v.w);
+          *(uint2 *)(p.out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = w;
+        } else {
+          *(float4 *)(p.o_part + (((size_t)split * p.Hkv + g) * rows_total + r) * HD + 4 * c4) = v;
+        }
+      }
     }
-    out[((size_t)t * Hq + h) * HD + c] = __float2bfloat16_rn(acc / L);
+  }
+  if (!p.out) {
+    // Split-KV merge inside the cluster of this query tile's blocks: block z
+    // merges rows z, z + S, ... of the tile (every block's partial state is
+    // visible past the barrier); a warp takes up to 4 rows at once with all
+    // their loads in flight, lanes along hd.
+    const int S = gridDim.z;
+    tc::cluster_sync();
+    const float NEG = __int_as_float(0xff800000);
+    constexpr int R = 4;
+    for (int rr0 = split + S * R * warp; rr0 < 128; rr0 += S * R * (kAttnThreads / 32)) {
+      float2 ml[R][8];
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const int r = r_cta + rr0 + S * u;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          ml[u][s] = (s < S && rr0 + S * u < 128 && r < rows_total)
+                         ? *(const float2 *)(p.ml_part + (((size_t)s * p.Hkv + g) * rows_total + r) * 2)
+                         : make_float2(NEG, 0.0f);
+      }
+      float w[R][8], invL[R];
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        float mx = NEG;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mx = fmaxf(mx, ml[u][s].x);
+        float L = 0.0f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          w[u][s] = ml[u][s].x == NEG ? 0.0f : ex2(ml[u][s].x - mx);
+          L += w[u][s] * ml[u][s].y;
+        }
+        invL[u] = L > 0.0f ? 1.0f / L : 0.0f;
+      }
+      for (int c4 = lane; c4 < HD / 4; c4 += 32) {
+        float4 o[R][8];
+#pragma unroll
+        for (int u = 0; u < R; ++u)
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const int r = r_cta + rr0 + S * u;
+            o[u][s] = (s < S && w[u][s] != 0.0f)
+                          ? *(const float4 *)(p.o_part + (((size_t)s * p.Hkv + g) * rows_total + r) * HD + 4 * c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+          const int r = r_cta + rr0 + S * u;
+          if (rr0 + S * u >= 128 || r >= rows_total) continue;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            acc.x += w[u][s] * o[u][s].x;
+            acc.y += w[u][s] * o[u][s].y;
+            acc.z += w[u][s] * o[u][s].z;
+            acc.w += w[u][s] * o[u][s].w;
+          }
+          const int t = r / p.G, h = g * p.G + r % p.G;
+          uint2 v;
+          v.x = pack_bf16(acc.x * invL[u], acc.y * invL[u]);
+          v.y = pack_bf16(acc.z * invL[u], acc.w * invL[u]);
+          *(uint2 *)(p.final_out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = v;
+        }
+      }
+    }
   }
 }
 
@@ -392,6 +532,7 @@ SplitPlan plan_splits(const AttnShape &s) {
   const int n_keys = s.n_prefix + s.n_new;
   const int n_kb = ceil_div(n_keys, kKeysPerTile);
   int splits = 148 / base;  // about one wave: one 192 KB block per SM
+  if (splits > 8) splits = 8;  // the blocks of a query tile form one (portable) cluster
   if (splits > n_kb) splits = n_kb;
   if (splits < 1) splits = 1;
   const int kps = ceil_div(n_kb, splits) * kKeysPerTile;
@@ -430,10 +571,7 @@ cudaError_t attention_fixed_scratch(void **ptr) {
   return cudaSuccess;
 }
 
-int attention_launch_count(const AttnShape &s) {
-  if (s.n_new <= 0) return 0;
-  return plan_splits(s).splits > 1 ? 2 : 1;
-}
+int attention_launch_count(const AttnShape &s) { return s.n_new <= 0 ? 0 : 1; }
 
 size_t attention_workspace_bytes(const AttnShape &s) {
   if (s.n_new <= 0 || s.Hkv < 1) return 0;
@@ -507,8 +645,7 @@ cudaError_t attn_map(CUtensorMap *map, const void *ptr, int rank, const uint64_t
 }
 
 template <int HD>
-cudaError_t launch_attn(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const AttnParams &p, dim3 grid, cudaStream_t st) {
+cudaError_t launch_attn(const CUtensorMap &tq, const AttnParams &p, dim3 grid, cudaStream_t st) {
   using S = AttnSmem<HD>;
   static_assert(S::bytes <= 232448, "shared memory of the attention kernel");
   static unsigned long long attr_set = 0;
@@ -520,7 +657,28 @@ cudaError_t launch_attn(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set |= 1ull << dev;
   }
-  return launch_pdl(attn_tc_kernel<HD>, grid, dim3(kAttnThreads), S::bytes, st, tq, tk, tv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (grid.z > 1) {  // the key splits of a query tile: one cluster
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = grid.z;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, tq, p);
 }
 
 }  // namespace
@@ -533,7 +691,6 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   const int G = s.Hq / s.Hkv;
   if (128 % G) return cudaErrorInvalidValue;
   const SplitPlan pl = plan_splits(s);
-  if (pl.keys_per_split > 64 * AttnSmem<128>::kMaxHalves) return cudaErrorInvalidValue;
   AttnParams p;
   p.q = q;
   p.k_pool = k_pool;
@@ -554,15 +711,17 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   if (pl.splits > 1) {
     if (ws_bytes < attention_workspace_bytes(s) || ws == nullptr) return cudaErrorInvalidValue;
     p.out = nullptr;
+    p.final_out = out;
     p.o_part = (float *)ws;
     p.ml_part = p.o_part + (size_t)pl.splits * s.Hkv * rows_total * s.hd;
   } else {
     p.out = out;
+    p.final_out = out;
     p.o_part = p.ml_part = nullptr;
   }
   // Q [T][Hq][hd] as a 4-D tensor (hd, G, Hkv, T): a box of 64 x G x 1 x 128/G
   // lands as 128 rows (token, head of the group) of 128 bytes.
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq;
   {
     const uint64_t dims[4] = {(uint64_t)s.hd, (uint64_t)G, (uint64_t)s.Hkv, (uint64_t)s.n_new};
     const uint64_t strides[3] = {(uint64_t)s.hd * 2, (uint64_t)G * s.hd * 2, (uint64_t)s.Hq * s.hd * 2};
@@ -570,26 +729,8 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
     cudaError_t e = attn_map(&tq, q, 4, dims, strides, box);
     if (e != cudaSuccess) return e;
   }
-  // K and V pools [pages][Hkv][pg][hd] as [pages * Hkv * pg][hd], 64-key boxes.
-  // The pool size is not part of the call, so the map's row extent is set far
-  // beyond any pool; only rows of pages the page table names are requested.
-  {
-    const uint64_t rows = s.n_pages > 0 ? (uint64_t)s.n_pages * s.Hkv * s.pg : (uint64_t)1 << 28;
-    const uint64_t dims[2] = {(uint64_t)s.hd, rows};
-    const uint64_t strides[1] = {(uint64_t)s.hd * 2};
-    const uint32_t box[2] = {64, 64};
-    cudaError_t e = attn_map(&tk, k_pool, 2, dims, strides, box);
-    if (e != cudaSuccess) return e;
-    e = attn_map(&tv, v_pool, 2, dims, strides, box);
-    if (e != cudaSuccess) return e;
-  }
   const dim3 grid(ceil_div(rows_total, kRowsPerBlock), s.Hkv, pl.splits);
-  cudaError_t e = s.hd == 128 ? launch_attn<128>(tq, tk, tv, p, grid, st) : launch_attn<64>(tq, tk, tv, p, grid, st);
-  if (e != cudaSuccess) return e;
-  if (pl.splits > 1)
-    e = launch_pdl(attn_combine_kernel, dim3(rows_total, s.Hkv), dim3(128), 0, st, (const float *)p.o_part,
-                   (const float *)p.ml_part, pl.splits, s.Hkv, rows_total, p.G, s.Hq, s.hd, out);
-  return e;
+  return s.hd == 128 ? launch_attn<128>(tq, p, grid, st) : launch_attn<64>(tq, p, grid, st);
 }
 
 }  // namespace dg

@@ -32,7 +32,7 @@ struct EpiQkv {
     const int units = (c.m_valid / hd) << pairs_log;
     float *cs = (float *)extra;                           // [kTok][half]
     float *sn = cs + kTok * kMaxHalf;                     // [kTok][half]
-    long long *slot = (long long *)(sn + kTok * kMaxHalf);  // element offset of (page, 0, slot, 0)
+    long long *slot = (long long *)(sn + kTok * kMaxHalf);  // element offset of (page, head 0) + 64 * slot
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t0 = 0; t0 < c.n_valid; t0 += kTok) {
       const int nt = min(kTok, c.n_valid - t0);
@@ -62,7 +62,7 @@ struct EpiQkv {
       }
       for (int t = threadIdx.x; t < nt; t += blockDim.x) {
         const int p = o.pos0 + c.n0 + t0 + t;
-        slot[t] = ((long long)o.page_table[p / o.pg] * o.Hkv * o.pg + p % o.pg) * hd;
+        slot[t] = (long long)o.page_table[p / o.pg] * o.Hkv * o.pg * hd + (long long)(p % o.pg) * 64;
       }
       __syncthreads();
       const int nw = blockDim.x >> 5;
@@ -77,7 +77,7 @@ struct EpiQkv {
         } else {
           const bool is_k = fh < qdim + kdim;
           const int head = (fh - (is_k ? qdim : qdim + kdim)) / hd;
-          base_kv = (is_k ? o.k_pool : o.v_pool) + (long long)head * o.pg * hd + j;
+          base_kv = (is_k ? o.k_pool : o.v_pool) + (long long)head * o.pg * hd;
         }
         // four tokens per step: all shared-memory reads first, then math, then stores
         for (int tb = warp; tb < nt; tb += 4 * nw) {
@@ -105,9 +105,19 @@ struct EpiQkv {
               hi0 = b0[q] * c0[q] + a0[q] * s0[q];
               hi1 = b1[q] * c1[q] + a1[q] * s1[q];
             }
-            bf16 *dst = base_q ? base_q + (size_t)(c.n0 + t0 + t) * qdim : base_kv + slot[t];
-            *(__nv_bfloat162 *)dst = __floats2bfloat162_rn(lo0, lo1);
-            *(__nv_bfloat162 *)(dst + half) = __floats2bfloat162_rn(hi0, hi1);
+            if (base_q) {
+              bf16 *dst = base_q + (size_t)(c.n0 + t0 + t) * qdim;
+              *(__nv_bfloat162 *)dst = __floats2bfloat162_rn(lo0, lo1);
+              *(__nv_bfloat162 *)(dst + half) = __floats2bfloat162_rn(hi0, hi1);
+            } else {  // pool: feature f of slot s in sub-block f/64, chunk ((f%64)/8) ^ (s%8)
+              const int s7 = (o.pos0 + c.n0 + t0 + t) & 7;
+              bf16 *row = base_kv + slot[t];
+              const int f0 = j, f1 = j + half;
+              *(__nv_bfloat162 *)(row + (size_t)(f0 >> 6) * o.pg * 64 + ((((f0 & 63) >> 3) ^ s7) << 3) + (f0 & 7)) =
+                  __floats2bfloat162_rn(lo0, lo1);
+              *(__nv_bfloat162 *)(row + (size_t)(f1 >> 6) * o.pg * 64 + ((((f1 & 63) >> 3) ^ s7) << 3) + (f1 & 7)) =
+                  __floats2bfloat162_rn(hi0, hi1);
+            }
           }
         }
       }

@@ -305,9 +305,11 @@ __global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *
     r /= Hkv;
     const int t = (int)(r % n);
     const int l = (int)(r / n);
-    const int p = pos0 + t;
-    const size_t dst =
-        ((((size_t)l * n_pages + page_table[p / pg]) * Hkv + h) * pg + p % pg) * vec + c;
+    const int p = pos0 + t, s = p % pg;
+    // (page, head) block: hd/64 sub-blocks [pg][64], 16-byte chunk c of slot
+    // s at chunk position c ^ (s % 8)
+    const size_t dst = (((size_t)l * n_pages + page_table[p / pg]) * Hkv + h) * pg * vec +
+                       (size_t)(c >> 3) * pg * 8 + (size_t)s * 8 + ((c & 7) ^ (s & 7));
     k_pool[dst] = k_new[i];
     v_pool[dst] = v_new[i];
   }

@@ -265,8 +265,12 @@ int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor
  * keys j > n_prefix + t (context encoding / KV append).
  *   q        device bf16 [n_new][Hq][hd] (already rotated)
  *   k_pool,
- *   v_pool   device bf16 [n_pages][Hkv][page_size][hd]; key j lives in physical
- *            page page_table[j / page_size], slot j % page_size.  Keys are
+ *   v_pool   device bf16 pools of (page, KV head) blocks, [n_pages][Hkv] blocks
+ *            of page_size * hd elements; key j lives in physical page
+ *            page_table[j / page_size], slot s = j % page_size.  A block is
+ *            hd/64 sub-blocks [page_size][64]: element f of slot s sits in
+ *            sub-block f / 64, row s, at position 8 (((f % 64) / 8) ^ (s % 8))
+ *            + f % 8 (the tensor core's 128-byte-swizzled operand order).  Keys are
  *            read in 64-key groups: the slots after the last key in its
  *            group (same page) are read too, weighted by zero, and must hold
  *            finite values (e.g. a zero-initialised pool)
@@ -357,8 +361,8 @@ int dg_op_sampler_update(const void *partials, int32_t C, int32_t V, int32_t ste
                          int32_t *gumbel, int32_t *done_dev, void *stream);
 
 /* KV append, standalone: copy n_layers x n_new tokens of K and V (device bf16
- * [n_layers][n_new][Hkv][hd]) into the pools (device bf16
- * [n_layers][n_pages][Hkv][page_size][hd]) at absolute positions
+ * [n_layers][n_new][Hkv][hd]) into the pools (device bf16, n_layers pools in
+ * the layout of dg_op_canvas_attention) at absolute positions
  * pos0 .. pos0+n_new-1 through page_table (device int32). */
 int dg_op_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool,
                     uint16_t *v_pool, const int32_t *page_table, int32_t n_layers,

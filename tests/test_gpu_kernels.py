@@ -178,12 +178,25 @@ def test_lm_head_partials_against_fp64_logits(rows, d, V, sample):
 
 # ---- canvas attention -----------------------------------------------------------
 
+def pool_layout(blocks):
+    """(page, head) blocks [..., pg, hd] (slot-major) to the pool's storage
+    order: hd/64 sub-blocks [pg][64] in which the 16-byte chunk c of slot s
+    sits at chunk position c ^ (s % 8)."""
+    *lead, pg, hd = blocks.shape
+    x = blocks.reshape(*lead, pg, hd // 64, 8, 8)
+    s = np.arange(pg)[:, None]
+    src = np.arange(8)[None, :] ^ (s % 8)      # logical chunk stored at position c
+    x = np.take_along_axis(x, np.broadcast_to(src[:, None, :, None], (pg, hd // 64, 8, 8)).reshape(
+        (1,) * len(lead) + (pg, hd // 64, 8, 8)), axis=-2)
+    return np.moveaxis(x, -3, -4).reshape(*lead, pg, hd)
+
+
 def paged(kv, Hkv, hd, pg, n_pages, perm):
     """Scatter logical keys [S][Hkv][hd] into pages through the page table `perm`."""
     pool = np.zeros((n_pages, Hkv, pg, hd), np.float32)
     for j in range(kv.shape[0]):
         pool[perm[j // pg], :, j % pg, :] = kv[j]
-    return pool
+    return pool_layout(pool)
 
 
 @pytest.mark.parametrize("P,causal,Hq,Hkv,hd", [
@@ -259,5 +272,5 @@ def test_kv_append_bit_exact_with_shuffled_pages():
         p = pos0 + t
         kref[:, perm[p // pg], :, p % pg, :] = kn[:, t]
         vref[:, perm[p // pg], :, p % pg, :] = vn[:, t]
-    assert np.array_equal(kp.cpu().numpy().view(np.uint16), kref)
-    assert np.array_equal(vp.cpu().numpy().view(np.uint16), vref)
+    assert np.array_equal(kp.cpu().numpy().view(np.uint16), pool_layout(kref))
+    assert np.array_equal(vp.cpu().numpy().view(np.uint16), pool_layout(vref))
