@@ -378,8 +378,8 @@ def dg_op_canvas_attention(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, H
 
 def dg_op_canvas_attention_noalloc(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, Hkv, hd,
                                    page_size, causal, out, stream=None):
-    """dg_op_canvas_attention without a workspace: the library's fixed 16 MiB
-    scratch holds the split-KV partials (see include/dg.h)."""
+    """dg_op_canvas_attention without a workspace argument (no device scratch
+    is needed: split-KV states are merged on chip)."""
     _check(load().dg_op_canvas_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool),
                                                  _ptr(page_table), n_prefix, n_new, Hq, Hkv, hd,
                                                  page_size, int(causal), _ptr(out), _stream(stream)))

@@ -966,15 +966,8 @@ int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
       (head_dim != 64 && head_dim != 128) || page_size < 64 || page_size % 64)
     return fail(DG_EINVAL, "unsupported attention shape");
   dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, page_size, causal ? 1 : 0};
-  const size_t need = dg::attention_workspace_bytes(as);
-  if (need > dg::kAttentionFixedScratchBytes)
-    return fail(DG_EINVAL,
-                "this shape needs %zu bytes of split-KV scratch; the fixed scratch holds %zu bytes",
-                need, dg::kAttentionFixedScratchBytes);
-  void *scratch = nullptr;
-  CK(dg::attention_fixed_scratch(&scratch));
   CK(dg::attention((const bf16 *)q, (const bf16 *)k_pool, (const bf16 *)v_pool, page_table, as,
-                   (bf16 *)out, scratch, dg::kAttentionFixedScratchBytes, (cudaStream_t)stream));
+                   (bf16 *)out, nullptr, 0, (cudaStream_t)stream));
   return DG_OK;
 }
 

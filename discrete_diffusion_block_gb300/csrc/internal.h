@@ -114,13 +114,10 @@ struct AttnShape {
   int n_prefix, n_new, Hq, Hkv, hd, pg, causal;
   int n_pages = 0;  // physical pages of the pools when known (0: unknown)
 };
+// Device scratch the call needs (none: split-KV states merge on chip); ws and
+// ws_bytes of attention() are accepted and unused.
 size_t attention_workspace_bytes(const AttnShape &s);
 int attention_launch_count(const AttnShape &s);
-// Size of the library-owned split-KV scratch used when the caller cannot
-// allocate, and its device address on the current device (looked up on the
-// first use per device).
-constexpr size_t kAttentionFixedScratchBytes = (size_t)16 << 20;
-cudaError_t attention_fixed_scratch(void **ptr);
 // err (optional, device): error word set when a bounded wait of the kernel gives up.
 cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const int *page_table,
                       const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st,

@@ -54,9 +54,7 @@ struct AttnParams {
   int n_prefix, n_new, Hq, Hkv, G, pg, causal;
   float scale_log2;
   int keys_per_split;
-  bf16 *out;
-  float *o_part;   // [splits][Hkv][rows][HD] (split launches)
-  float *ml_part;  // [splits][Hkv][rows][2]
+  bf16 *out;       // unsplit launches: the output
   int *err;        // device error word (bounded waits, bad page indices), may be null
   int n_pages;     // physical pages of the pools, 0 when unknown
   bf16 *final_out; // split launches: where the cluster's merge writes the output
@@ -68,28 +66,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 224;
+constexpr int kAttnPages = 256;  // 64-key halves whose physical page is looked up before the key loop
 constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one TMA box)
 
 // Shared memory (bytes from a 1024-aligned base): Q [HB][128 rows][64]; a
-// 3-slot K ring and a 2-slot V ring of 128-key tiles [HB][128 keys][64]; the
-// P tile [2][128 rows][64 keys] (bf16, the A operand of P V); barriers.  After
-// the key loop the K ring holds the fp32 output rows [128][HD] on their way
+// 2-slot K ring and a 2-slot V ring of 128-key tiles [HB][128 keys][64]; two
+// P tiles [2][128 rows][64 keys] (bf16, the A operand of P V), so that the
+// softmax of tile i does not wait for P V of tile i - 1; barriers.  After the
+// key loop the K and V rings hold the fp32 output rows [128][HD] on their way
 // out.
 template <int HD>
 struct AttnSmem {
   static constexpr int HB = HD / 64;                       // 64-wide hd blocks
-  static constexpr int kK = 3, kV = 2;                     // ring depths
+  static constexpr int kK = 2, kV = 2;                     // ring depths
   static constexpr size_t tile = (size_t)HB * 16384;       // one 128-key K or V tile, or Q
   static constexpr size_t q = 0;
   static constexpr size_t kring = q + tile;
   static constexpr size_t vring = kring + kK * tile;
-  static constexpr size_t pbuf = vring + kV * tile;        // 2 x [128 rows][64 keys] bf16
-  static constexpr size_t bars = pbuf + 32768;
-  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty, o_full
-  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 3;
+  static constexpr size_t pbuf = vring + kV * tile;        // 2 x 2 x [128 rows][64 keys] bf16
+  static constexpr size_t pages = pbuf + 2 * 32768;          // physical page per 64-key half (ints)
+  static constexpr size_t bars = pages + kAttnPages * 4;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty[2], o_full,
+  // r_full (peer partials received)
+  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 4 + 1;
   static constexpr size_t bytes = bars + n_bars * 8 + 16 + 1024;
-  static_assert((size_t)128 * HD * 4 <= kK * tile, "output staging fits the K ring");
+  static_assert((size_t)128 * HD * 4 <= (kK + kV) * tile, "output staging fits the K and V rings");
 };
 
 // One 64-key half of a K or V operand tile, all zero (keys past the end).
@@ -152,9 +154,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t *k_full = q_full + 1, *k_empty = k_full + KK;
   uint64_t *v_full = k_empty + KK, *v_empty = v_full + KV;
   uint64_t *s_full = v_empty + KV, *s_empty = s_full + 2;
-  uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1, *o_full = p_empty + 1;
-  uint32_t *tmem_slot = (uint32_t *)(o_full + 1);
+  uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1, *o_full = p_empty + 2, *r_full = o_full + 1;
+  uint32_t *tmem_slot = (uint32_t *)(r_full + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
+  int *pages = (int *)(base + S::pages);
   auto k_tile = [&](int slot) { return base + S::kring + (size_t)slot * S::tile; };
   auto v_tile = [&](int slot) { return base + S::vring + (size_t)slot * S::tile; };
 
@@ -188,7 +191,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     tc::mbar_init(p_full, 4);
     tc::mbar_init(p_empty, 1);
+    tc::mbar_init(p_empty + 1, 1);
     tc::mbar_init(o_full, 1);
+    tc::mbar_init(r_full, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -197,6 +202,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      tc::smem_u32(tmem_slot)),
                  "r"(512u));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  // Physical page of every 64-key half of the block's range (-1 past the
+  // last key or on a bad index), and those pages' K and V into L2, before the
+  // wait on the previous kernel: the page table was written before it started,
+  // cached prefix keys do not depend on it, and L2 is coherent with the
+  // canvas keys it writes.
+  const int n_halves = 2 * n_kt;
+  if (warp == 0) {
+    for (int i = lane; i < n_halves; i += 32) {
+      const int key = k_begin + 64 * i;
+      int pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
+      if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) {
+        if (p.err) atomicExch(p.err, 39);
+        pg_i = -1;
+      }
+      if (i < kAttnPages) pages[i] = pg_i;
+      if (pg_i < 0) continue;
+      const size_t off = ((size_t)pg_i * p.Hkv + g) * p.pg * HD + (size_t)(key % p.pg) * 64;
+      for (int b = 0; b < HB; ++b) {
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.k_pool + off + (size_t)b * p.pg * 64),
+                     "r"((uint32_t)kAttnSlotHalfBytes)
+                     : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.v_pool + off + (size_t)b * p.pg * 64),
+                     "r"((uint32_t)kAttnSlotHalfBytes)
+                     : "memory");
+      }
+    }
   }
   pdl_wait();
   pdl_trigger();
@@ -207,7 +239,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s = tmem, t_o = tmem + 256;  // S double buffer: columns [0,128) [128,256); O: [256, 256+HD)
 
-  if (warp == 0) {
+  // One 128-key K or V tile: per 64-key half, the page's hd sub-blocks; two
+  // halves of one page that follow each other move as one copy; a half past
+  // the block's last key (or on a bad page index) is a zero half (its P is
+  // zero; V must hold finite values).
+  auto load_tile = [&](const bf16 *pool, unsigned char *dst, int kt, uint64_t *bar) {
+    const int key0 = k_begin + 128 * kt;
+    int pgs[2];
+    for (int h = 0; h < 2; ++h) {
+      const int key = key0 + 64 * h, hi = 2 * kt + h;
+      int pg_i;
+      if (hi < kAttnPages) {
+        pg_i = pages[hi];
+      } else {
+        pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
+        if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) pg_i = -1;
+      }
+      pgs[h] = pg_i;
+    }
+    const bool whole = pgs[0] >= 0 && pgs[1] == pgs[0] && (key0 % p.pg) + 128 <= p.pg;
+    tc::mbar_expect_tx(bar, kTileBytes);
+    for (int h = 0; h < (whole ? 1 : 2); ++h) {
+      const uint32_t bytes = whole ? 2 * kAttnSlotHalfBytes : kAttnSlotHalfBytes;
+      const size_t off = pgs[h] < 0 ? 0 : ((size_t)pgs[h] * p.Hkv + g) * p.pg * HD + (size_t)((key0 + 64 * h) % p.pg) * 64;
+      for (int b = 0; b < HB; ++b)
+        attn_bulk(dst + (size_t)b * 16384 + h * kAttnSlotHalfBytes,
+                  pgs[h] < 0 ? (const void *)g_zero_half : (const void *)(pool + off + (size_t)b * p.pg * 64), bytes, bar);
+    }
+  };
+  // Bounded wait for the last copy into each of `depth` slots (after an abort).
+  auto drain = [&](uint64_t *full, int issued, int depth) {
+    for (int i = issued - 1; i >= 0 && i >= issued - depth; --i) {
+      const long long t0 = clock64();
+      while (!tc::mbar_try_wait(full + i % depth, (i / depth) & 1) && clock64() - t0 < tc::kWaitCycles) {
+      }
+    }
+  };
+
+  if (warp == 0) {  // Q, then the K ring (S of a tile needs only its K)
     if (lane == 0 && n_kt > 0) {
       tc::mbar_expect_tx(q_full, (uint32_t)(HB * 16384));
       for (int b = 0; b < HB; ++b) {
@@ -217,65 +286,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             "l"((uint64_t)&tq), "r"(64 * b), "r"(0), "r"(g), "r"(r_cta / p.G), "r"(tc::smem_u32(q_full))
             : "memory");
       }
-      // One 128-key K or V tile: per 64-key half, the page's hd sub-blocks;
-      // two halves of one page that follow each other move as one copy; a
-      // half past the block's last key (or on a bad page index) is a zero
-      // half (its P is zero; V must hold finite values).
-      auto load_tile = [&](const bf16 *pool, unsigned char *dst, int kt, uint64_t *bar) {
-        const int key0 = k_begin + 128 * kt;
-        int pgs[2];
-        for (int h = 0; h < 2; ++h) {
-          const int key = key0 + 64 * h;
-          int pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
-          if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) {
-            if (p.err) atomicExch(p.err, 39);
-            pg_i = -1;
-          }
-          pgs[h] = pg_i;
-        }
-        const bool whole = pgs[0] >= 0 && pgs[1] == pgs[0] && (key0 % p.pg) + 128 <= p.pg;
-        tc::mbar_expect_tx(bar, kTileBytes);
-        for (int h = 0; h < (whole ? 1 : 2); ++h) {
-          const uint32_t bytes = whole ? 2 * kAttnSlotHalfBytes : kAttnSlotHalfBytes;
-          const size_t off = pgs[h] < 0 ? 0
-                                        : ((size_t)pgs[h] * p.Hkv + g) * p.pg * HD + (size_t)((key0 + 64 * h) % p.pg) * 64;
-          for (int b = 0; b < HB; ++b)
-            attn_bulk(dst + (size_t)b * 16384 + h * kAttnSlotHalfBytes,
-                      pgs[h] < 0 ? (const void *)g_zero_half : (const void *)(pool + off + (size_t)b * p.pg * 64), bytes,
-                      bar);
-        }
-      };
-      auto issue_k = [&](int i) {
-        const int slot = i % KK;
-        if (i >= KK) tc::mbar_wait(k_empty + slot, ((i / KK) - 1) & 1, p.err, 31, abort);
-        if (!*abort) load_tile(p.k_pool, k_tile(slot), i, k_full + slot);
-      };
-      auto issue_v = [&](int i) {
-        const int slot = i % KV;
-        if (i >= KV) tc::mbar_wait(v_empty + slot, ((i / KV) - 1) & 1, p.err, 30, abort);
-        if (!*abort) load_tile(p.v_pool, v_tile(slot), i, v_full + slot);
-      };
-      // K runs one tile ahead of V: S of the next tile can start while P V of
-      // this one waits for its V
-      int nk = 0, nv = 0;
-      issue_k(0), ++nk;
-      for (int i = 0; i < n_kt && !*abort; ++i) {
-        if (i + 1 < n_kt) issue_k(i + 1), ++nk;
+      int nk = 0;
+      for (; nk < n_kt; ++nk) {
+        const int slot = nk % KK;
+        if (nk >= KK) tc::mbar_wait(k_empty + slot, ((nk / KK) - 1) & 1, p.err, 31, abort);
         if (*abort) break;
-        issue_v(i), ++nv;
+        load_tile(p.k_pool, k_tile(slot), nk, k_full + slot);
       }
-      if (*abort) {  // drain the copies still in flight: the last load of each slot (bounded)
-        for (int i = nk - 1; i >= 0 && i >= nk - KK; --i) {
-          const long long t0 = clock64();
-          while (!tc::mbar_try_wait(k_full + i % KK, (i / KK) & 1) && clock64() - t0 < tc::kWaitCycles) {
-          }
-        }
-        for (int i = nv - 1; i >= 0 && i >= nv - KV; --i) {
-          const long long t0 = clock64();
-          while (!tc::mbar_try_wait(v_full + i % KV, (i / KV) & 1) && clock64() - t0 < tc::kWaitCycles) {
-          }
-        }
+      if (*abort) drain(k_full, nk, KK);
+    }
+  } else if (warp == 6) {  // the V ring
+    if (lane == 0 && n_kt > 0) {
+      int nv = 0;
+      for (; nv < n_kt; ++nv) {
+        const int slot = nv % KV;
+        if (nv >= KV) tc::mbar_wait(v_empty + slot, ((nv / KV) - 1) & 1, p.err, 30, abort);
+        if (*abort) break;
+        load_tile(p.v_pool, v_tile(slot), nv, v_full + slot);
       }
+      if (*abort) drain(v_full, nv, KV);
     }
   } else if (warp == 1) {
     if (lane == 0 && n_kt > 0) {
@@ -303,14 +332,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc::mbar_wait(p_full, i & 1, p.err, 35, abort);
         tc::mbar_wait(v_full + slot, (i / KV) & 1, p.err, 29, abort);
         tc::fence_after();
-        const unsigned char *pb = base + S::pbuf;
+        const unsigned char *pb = base + S::pbuf + (size_t)(i & 1) * 32768;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA
           const uint64_t adesc = tc::sw128_desc(tc::smem_u32(pb + (size_t)(kk >> 2) * 16384)) + 2 * (kk & 3);
           const uint64_t bdesc = mn_desc(tc::smem_u32(v_tile(slot))) + (uint64_t)kk * (2048 >> 4);
           tc::mma_bf16(t_o, adesc, bdesc, idesc_o, (i | kk) ? 1u : 0u);
         }
-        tc::mma_commit(p_empty);
+        tc::mma_commit(p_empty + (i & 1));
         tc::mma_commit(v_empty + slot);
       }
       tc::mma_commit(o_full);
@@ -337,26 +366,66 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::fence_before();
       __syncwarp();
       if (lane == 0) attn_arrive(s_empty + buf);
-      // scaled scores; keys this row must not see are -inf
+      // keys this row must not see are -inf (only in a tile that holds some)
       const int nvalid = min(128, last - key_base + 1);  // <= 0: none
-      float tmax = NEG;
+      if (nvalid < 128) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (32 * c + j >= nvalid) x[c][j] = 0xff800000u;
+      }
+      // tile maximum of the raw scores (the scale is positive), four chains
+      float a0 = __int_as_float(0xff800000), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float v = __uint_as_float(x[c][j]) * p.scale_log2;
-          if (32 * c + j >= nvalid) v = NEG;
-          x[c][j] = __float_as_uint(v);
-          tmax = fmaxf(tmax, v);
+        for (int j = 0; j < 32; j += 4) {
+          a0 = fmaxf(a0, __uint_as_float(x[c][j]));
+          a1 = fmaxf(a1, __uint_as_float(x[c][j + 1]));
+          a2 = fmaxf(a2, __uint_as_float(x[c][j + 2]));
+          a3 = fmaxf(a3, __uint_as_float(x[c][j + 3]));
         }
+      const float tmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.scale_log2;
       const float m_new = fmaxf(m, tmax);
       const bool grow = m_new > m + kRescaleLog2;  // false while both are -inf
-      // P V of the previous tile must be done before P is rewritten and
-      // before O is rescaled
-      if (i > 0) tc::mbar_wait(p_empty, (i - 1) & 1, p.err, 37, abort);
+      // P tile i & 1 is free once P V of tile i - 2 is done
+      if (i >= 2) tc::mbar_wait(p_empty + (i & 1), ((i >> 1) - 1) & 1, p.err, 37, abort);
+      const float m_old = m;
+      if (grow) m = m_new;
+      // P = 2^(x scale - m): one FMA and one ex2 per key; -inf keys give 0.
+      // Each 32-key group goes to the P tile as soon as it is packed.
+      const float nmu = m == NEG ? 0.0f : -m;
+      float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+      unsigned char *prow = base + S::pbuf + (size_t)(i & 1) * 32768 + (size_t)row * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(x[c][j]), p.scale_log2, nmu));
+          const float p1 = ex2(fmaf(__uint_as_float(x[c][j + 1]), p.scale_log2, nmu));
+          if ((j & 6) == 0) s0 += p0 + p1;
+          else if ((j & 6) == 2) s1 += p0 + p1;
+          else if ((j & 6) == 4) s2 += p0 + p1;
+          else s3 += p0 + p1;
+          pk[j >> 1] = pack_bf16(p0, p1);
+        }
+        const int h = c >> 1;  // keys 0-63 in box 0, 64-127 in box 1
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {  // 16-byte chunks of this 32-key group
+          const int chunk = (c & 1) * 4 + u;
+          *(uint4 *)(prow + (size_t)h * 16384 + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      // rows whose maximum grew: O (and l) to the new reference, O <- O 2^(m_old - m)
+      float f = 1.0f;
       if (__any_sync(0xffffffffu, grow) && i > 0) {
+        // O must hold P V of every earlier tile: wait for tile i - 1's
+        tc::mbar_wait(p_empty + ((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, 40, abort);
         tc::fence_after();
-        const float f = grow ? ex2(m - m_new) : 1.0f;  // m = -inf: 0 (O holds zeros)
+        f = grow ? ex2(m_old - m) : 1.0f;  // m_old = -inf: 0 (O holds zeros)
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
@@ -367,32 +436,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_st32(t_o + lane_off + 32 * c, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-        l *= f;
       }
-      if (grow) m = m_new;
-      const float mu = m == NEG ? 0.0f : m;
-      uint32_t pk[4][16];
-      float ls = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = ex2(__uint_as_float(x[c][j]) - mu), p1 = ex2(__uint_as_float(x[c][j + 1]) - mu);
-          ls += p0 + p1;
-          pk[c][j >> 1] = pack_bf16(p0, p1);
-        }
-      l += ls;
-      unsigned char *prow = base + S::pbuf + (size_t)row * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int h = c >> 1;  // keys 0-63 in box 0, 64-127 in box 1
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 16-byte chunks of this 32-key group
-          const int chunk = (c & 1) * 4 + u;
-          uint4 v = make_uint4(pk[c][4 * u], pk[c][4 * u + 1], pk[c][4 * u + 2], pk[c][4 * u + 3]);
-          *(uint4 *)(prow + (size_t)h * 16384 + ((chunk ^ (row & 7)) << 4)) = v;
-        }
-      }
+      l = l * f + ((s0 + s1) + (s2 + s3));
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc::fence_before();
       __syncwarp();
@@ -404,7 +449,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::fence_after();
     }
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    float *orow = (float *)(base + S::kring) + (size_t)row * HD;  // the K ring is idle now
+    float *orow = (float *)(base + S::kring) + (size_t)row * HD;  // the K and V rings are idle now
 #pragma unroll 1
     for (int c = 0; c < HD / 32; ++c) {
       uint32_t v[32];
@@ -423,10 +468,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                 __uint_as_float(v[j + 2]) * sc, __uint_as_float(v[j + 3]) * sc);
       }
     }
-    if (!p.out && ok) {
-      const size_t prow_o = ((size_t)split * p.Hkv + g) * rows_total + r;
-      *(float2 *)(p.ml_part + prow_o * 2) = make_float2(m, l);
-    }
+    if (!p.out) ((float2 *)(base + S::vring))[row] = make_float2(m, l);  // split blocks: the row's softmax state
   }
   tc::fence_before();
   __syncthreads();
@@ -434,92 +476,95 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(512u));
   }
-  // Rows out of shared memory, one warp per row, lanes along hd.
-  {
+  if (p.out) {
+    // Rows out of shared memory, one warp per row, lanes along hd.
     const float *stage = (const float *)(base + S::kring);
     for (int rr = warp; rr < 128; rr += kAttnThreads / 32) {
       const int r = r_cta + rr;
       if (r >= rows_total) break;
+      const int t = r / p.G, h = g * p.G + r % p.G;
       for (int c4 = lane; c4 < HD / 4; c4 += 32) {
         const float4 v = *(const float4 *)(stage + (size_t)rr * HD + 4 * (c4 ^ (rr & 7)));
-        if (p.out) {
-          const int t = r / p.G, h = g * p.G + r % p.G;
-          uint2 w;
-          w.x = pack_bf16(v.x, v.y);
-          w.y = pack_bf16(v.z, v.w);
-          *(uint2 *)(p.out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = w;
-        } else {
-          *(float4 *)(p.o_part + (((size_t)split * p.Hkv + g) * rows_total + r) * HD + 4 * c4) = v;
-        }
+        uint2 w;
+        w.x = pack_bf16(v.x, v.y);
+        w.y = pack_bf16(v.z, v.w);
+        *(uint2 *)(p.out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = w;
       }
     }
+    return;
   }
-  if (!p.out) {
-    // Split-KV merge inside the cluster of this query tile's blocks: block z
-    // merges rows z, z + S, ... of the tile (every block's partial state is
-    // visible past the barrier); a warp takes up to 4 rows at once with all
-    // their loads in flight, lanes along hd.
-    const int S = gridDim.z;
-    tc::cluster_sync();
-    const float NEG = __int_as_float(0xff800000);
-    constexpr int R = 4;
-    for (int rr0 = split + S * R * warp; rr0 < 128; rr0 += S * R * (kAttnThreads / 32)) {
-      float2 ml[R][8];
-#pragma unroll
-      for (int u = 0; u < R; ++u) {
-        const int r = r_cta + rr0 + S * u;
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          ml[u][s] = (s < S && rr0 + S * u < 128 && r < rows_total)
-                         ? *(const float2 *)(p.ml_part + (((size_t)s * p.Hkv + g) * rows_total + r) * 2)
-                         : make_float2(NEG, 0.0f);
-      }
-      float w[R][8], invL[R];
-#pragma unroll
-      for (int u = 0; u < R; ++u) {
-        float mx = NEG;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) mx = fmaxf(mx, ml[u][s].x);
-        float L = 0.0f;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          w[u][s] = ml[u][s].x == NEG ? 0.0f : ex2(ml[u][s].x - mx);
-          L += w[u][s] * ml[u][s].y;
-        }
-        invL[u] = L > 0.0f ? 1.0f / L : 0.0f;
-      }
-      for (int c4 = lane; c4 < HD / 4; c4 += 32) {
-        float4 o[R][8];
-#pragma unroll
-        for (int u = 0; u < R; ++u)
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const int r = r_cta + rr0 + S * u;
-            o[u][s] = (s < S && w[u][s] != 0.0f)
-                          ? *(const float4 *)(p.o_part + (((size_t)s * p.Hkv + g) * rows_total + r) * HD + 4 * c4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-        for (int u = 0; u < R; ++u) {
-          const int r = r_cta + rr0 + S * u;
-          if (rr0 + S * u >= 128 || r >= rows_total) continue;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            acc.x += w[u][s] * o[u][s].x;
-            acc.y += w[u][s] * o[u][s].y;
-            acc.z += w[u][s] * o[u][s].z;
-            acc.w += w[u][s] * o[u][s].w;
-          }
-          const int t = r / p.G, h = g * p.G + r % p.G;
-          uint2 v;
-          v.x = pack_bf16(acc.x * invL[u], acc.y * invL[u]);
-          v.y = pack_bf16(acc.z * invL[u], acc.w * invL[u]);
-          *(uint2 *)(p.final_out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = v;
-        }
-      }
+  // Split-KV merge inside the cluster of this query tile's blocks.  Block z
+  // owns rows [z n, z n + n), n = ceil(128 / NS) rounded up to even (16-byte
+  // aligned softmax-state rows); every block sends its staged
+  // output rows and softmax states of those rows to their owner with bulk
+  // shared-to-shared copies (into the owner's idle P tiles), and the owner
+  // merges the NS partials (weights 2^(m_s - m*)) in shared memory.
+  const int NS = gridDim.z;
+  const int n_own = (((128 + NS - 1) / NS) + 1) & ~1;
+  const uint32_t o_slot = (uint32_t)n_own * HD * 4, ml_slot = (uint32_t)n_own * 8;
+  const uint32_t slot_bytes = o_slot + ml_slot;
+  const float *stage = (const float *)(base + S::kring);
+  const float2 *ml_stage = (const float2 *)(base + S::vring);
+  unsigned char *recv = base + S::pbuf;           // (NS - 1) slots: O rows, then (m, l) pairs
+  uint64_t *rbar = r_full;
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the copies read the staged rows
+  tc::cluster_sync();  // every block staged; every block's P tiles are idle
+  const int z = split, r0 = z * n_own, n_mine = max(0, min(128, r0 + n_own) - r0);
+  if (threadIdx.x == 0) {
+    tc::mbar_expect_tx(rbar, (uint32_t)(NS - 1) * ((uint32_t)n_mine * HD * 4 + (uint32_t)((n_mine + 1) & ~1) * 8));
+    for (int q = 1; q < NS; ++q) {
+      const int j = (z + q) % NS, jr0 = j * n_own, nj = max(0, min(128, jr0 + n_own) - jr0);
+      if (nj == 0) continue;
+      const int slot = z < j ? z : z - 1;
+      const uint32_t dst = tc::cluster_addr(tc::smem_u32(recv) + slot * slot_bytes, (uint32_t)j);
+      const uint32_t bar = tc::cluster_addr(tc::smem_u32(rbar), (uint32_t)j);
+      tc::bulk_copy_to_peer(dst, tc::smem_u32(stage + (size_t)jr0 * HD), (uint32_t)nj * HD * 4, bar);
+      tc::bulk_copy_to_peer(dst + o_slot, tc::smem_u32(ml_stage + jr0), (uint32_t)((nj + 1) & ~1) * 8, bar);
     }
   }
+  if (n_mine > 0) tc::mbar_wait(rbar, 0, p.err, 41, abort);
+  const float NEG = __int_as_float(0xff800000);
+  for (int idx = threadIdx.x; idx < n_mine * (HD / 4); idx += kAttnThreads) {
+    const int lr = idx / (HD / 4), c4 = idx - lr * (HD / 4), rr = r0 + lr, r = r_cta + rr;
+    if (r >= rows_total) continue;
+    float2 ml[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (q >= NS) {
+        ml[q] = make_float2(NEG, 0.0f);
+      } else if (q == z) {
+        ml[q] = ml_stage[rr];
+      } else {
+        const unsigned char *sl = recv + (size_t)(q < z ? q : q - 1) * slot_bytes;
+        ml[q] = ((const float2 *)(sl + o_slot))[lr];
+      }
+    }
+    float mx = NEG;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) mx = fmaxf(mx, ml[q].x);
+    float L = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (q >= NS || ml[q].x == NEG) continue;
+      const float w = ex2(ml[q].x - mx);
+      L += w * ml[q].y;
+      const float *rows = q == z ? stage + (size_t)rr * HD
+                                 : (const float *)(recv + (size_t)(q < z ? q : q - 1) * slot_bytes) + (size_t)lr * HD;
+      const float4 o = *(const float4 *)(rows + 4 * (c4 ^ (rr & 7)));  // the staging order travels with the rows
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+    const float invL = L > 0.0f ? 1.0f / L : 0.0f;
+    const int t = r / p.G, h = g * p.G + r % p.G;
+    uint2 v;
+    v.x = pack_bf16(acc.x * invL, acc.y * invL);
+    v.y = pack_bf16(acc.z * invL, acc.w * invL);
+    *(uint2 *)(p.final_out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = v;
+  }
+  tc::cluster_sync();  // every copy out of this block's shared memory has landed
 }
 
 struct SplitPlan {
@@ -545,41 +590,11 @@ SplitPlan plan_splits(const AttnShape &s) {
 
 }  // namespace
 
-// Fixed split-KV scratch for the entry point that must not allocate.  It is
-// a file-scope device array, so every GPU that loads the library holds it
-// for the life of the process.  Host code may not pass the symbol itself to
-// a kernel (on the host it only names a stand-in); its device address is
-// looked up once per device, with that device current.
-static __device__ __align__(256) unsigned char g_attention_scratch[kAttentionFixedScratchBytes];
-
-cudaError_t attention_fixed_scratch(void **ptr) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void *addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_attention_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
-  }
-  *ptr = addr[dev];
-  return cudaSuccess;
-}
-
 int attention_launch_count(const AttnShape &s) { return s.n_new <= 0 ? 0 : 1; }
 
-size_t attention_workspace_bytes(const AttnShape &s) {
-  if (s.n_new <= 0 || s.Hkv < 1) return 0;
-  const SplitPlan pl = plan_splits(s);
-  if (pl.splits <= 1) return 0;
-  const size_t rows = (size_t)(s.Hq / s.Hkv) * s.n_new;
-  return (size_t)pl.splits * s.Hkv * rows * (s.hd + 2) * sizeof(float);
-}
+// The split-KV partial states never leave the chip (the blocks of a query
+// tile merge them through distributed shared memory): no device scratch.
+size_t attention_workspace_bytes(const AttnShape &) { return 0; }
 
 namespace {
 
@@ -708,17 +723,10 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   p.err = err;
   p.n_pages = s.n_pages;
   const int rows_total = G * s.n_new;
-  if (pl.splits > 1) {
-    if (ws_bytes < attention_workspace_bytes(s) || ws == nullptr) return cudaErrorInvalidValue;
-    p.out = nullptr;
-    p.final_out = out;
-    p.o_part = (float *)ws;
-    p.ml_part = p.o_part + (size_t)pl.splits * s.Hkv * rows_total * s.hd;
-  } else {
-    p.out = out;
-    p.final_out = out;
-    p.o_part = p.ml_part = nullptr;
-  }
+  (void)ws;
+  (void)ws_bytes;
+  p.out = pl.splits > 1 ? nullptr : out;  // split blocks merge in the cluster, then write final_out
+  p.final_out = out;
   // Q [T][Hq][hd] as a 4-D tensor (hd, G, Hkv, T): a box of 64 x G x 1 x 128/G
   // lands as 128 rows (token, head of the group) of 128 bytes.
   CUtensorMap tq;

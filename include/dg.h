@@ -276,8 +276,10 @@ int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor
  *            finite values (e.g. a zero-initialised pool)
  *   page_table device int32, >= ceil((n_prefix + n_new) / page_size) entries
  *   out      device bf16 [n_new][Hq][hd]
- * workspace: device scratch of dg_op_attention_workspace_bytes() bytes (the
- * split-KV partial softmax states; 0 bytes when no split is needed). */
+ * workspace: device scratch of dg_op_attention_workspace_bytes() bytes.  The
+ * split-KV partial softmax states are merged on chip (the blocks of a query
+ * tile exchange them through distributed shared memory), so this is 0 for
+ * every shape; the argument stays for callers that size it. */
 size_t dg_op_attention_workspace_bytes(int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
                                        int32_t n_kv_heads, int32_t head_dim);
 int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
@@ -293,19 +295,10 @@ int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint
  * may synchronise the device) is not acceptable.  The paper has no
  * counterpart; this is a property of the library, not of the method.
  *
- * The split-KV scratch lives in a fixed 16 MiB device array inside the
- * library (held by every GPU that loads it until the process exits); no
- * device memory is allocated or freed by this call.  The split plan sizes
- * the key splits for about one wave of blocks, which keeps the scratch near
- * 10 MiB at most for any shape; a shape whose scratch
- * (dg_op_attention_workspace_bytes) exceeded 16 MiB would return DG_EINVAL
- * with the required size in dg_last_error().  The first call on a device looks up the
- * array's device address, with that device current; make that first call
- * before any stream capture.  All calls share the one array and it keeps the
- * previous call's contents (every value the kernels read is written earlier
- * in the same call, so nothing needs clearing); calls whose GPU work overlaps
- * in time, on any streams, race on it.  Inputs, outputs and errors otherwise
- * as dg_op_canvas_attention. */
+ * The kernel needs no device scratch (the split-KV partial states are merged
+ * in distributed shared memory), so no device memory is allocated, freed or
+ * held by this call, and calls on any streams may overlap.  Inputs, outputs
+ * and errors as dg_op_canvas_attention. */
 int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
                                    const uint16_t *v_pool, const int32_t *page_table,
                                    int32_t n_prefix, int32_t n_new, int32_t n_q_heads,

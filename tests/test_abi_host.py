@@ -63,7 +63,7 @@ def test_null_arguments_fail_cleanly_without_a_gpu(lib):
 def test_workspace_queries_are_host_only(lib):
     L = dgp.load()
     assert L.dg_op_attention_workspace_bytes(0, 0, 4, 2, 64) == 0
-    assert L.dg_op_attention_workspace_bytes(2048, 256, 16, 8, 128) > 0      # split-KV partials
+    assert L.dg_op_attention_workspace_bytes(2048, 256, 16, 8, 128) == 0     # split-KV merged on chip
     assert L.dg_op_moe_workspace_bytes(256, 2816, 128, 8, 704) > 256 * 8 * 2816 * 4
 
 
