@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0 && p.err && *(volatile int *)p.err) *abort = 1;
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -470,6 +471,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     if (!p.out) ((float2 *)(base + S::vring))[row] = make_float2(m, l);  // split blocks: the row's softmax state
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -508,6 +510,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   unsigned char *recv = base + S::pbuf;           // (NS - 1) slots: O rows, then (m, l) pairs
   uint64_t *rbar = r_full;
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the copies read the staged rows
+  __syncwarp();
   tc::cluster_sync();  // every block staged; every block's P tiles are idle
   const int z = split, r0 = z * n_own, n_mine = max(0, min(128, r0 + n_own) - r0);
   if (threadIdx.x == 0) {
@@ -564,6 +567,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     v.y = pack_bf16(acc.z * invL, acc.w * invL);
     *(uint2 *)(p.final_out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = v;
   }
+  __syncwarp();
   tc::cluster_sync();  // every copy out of this block's shared memory has landed
 }
 

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                  "r"((uint32_t)(2 * kLmAccCols)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       }
     }
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   if (warp == 1) {

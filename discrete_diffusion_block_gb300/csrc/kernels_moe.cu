@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
                  "r"((uint32_t)(2 * kFfnBN)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
       if (threadIdx.x == 0) mbar_arrive(q_empty + q);
     }
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   if (warp == 5) {

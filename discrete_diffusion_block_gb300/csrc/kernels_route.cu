@@ -65,7 +65,7 @@ struct RouteArgs {
 };
 
 struct RouteSmem {
-  uint32_t w_off, x_off, part_off, logit_off, ss_off, cnt_off, pid_off, bars_off, bytes;
+  uint32_t w_off, x_off, part_off, recv_off, logit_off, ss_off, cnt_off, pid_off, bars_off, bytes;
 };
 
 __host__ __device__ inline RouteSmem route_smem(int S, int nk_max, int stages, int m_tiles) {
@@ -74,12 +74,13 @@ __host__ __device__ inline RouteSmem route_smem(int S, int nk_max, int stages, i
   s.w_off = 0;
   s.x_off = s.w_off + (uint32_t)stages * m_tiles * kWBox;
   s.part_off = s.x_off + (uint32_t)nk_max * kXBox;
-  s.logit_off = s.part_off + (uint32_t)kRouteTok * ep * 4;
+  s.recv_off = s.part_off + (uint32_t)kRouteTok * ep * 4;           // [S][32/S tokens][ep] from the peers
+  s.logit_off = s.recv_off + (uint32_t)kRouteTok * ep * 4;
   s.ss_off = s.logit_off + (uint32_t)(kRouteTok / S) * ep * 4;
   s.cnt_off = s.ss_off + kRouteTok * 4;
   s.pid_off = s.cnt_off + ep * 4;
   s.bars_off = (s.pid_off + (uint32_t)(kRouteTok / S) * 16 * 4 + 15) & ~15u;
-  s.bytes = s.bars_off + (8 + 8 + 2) * 8 + 32 + 1024;  // full[8], empty[8], x, acc; words; alignment slack
+  s.bytes = s.bars_off + (8 + 8 + 3) * 8 + 32 + 1024;  // full[8], empty[8], x, acc, recv; words; alignment slack
   return s;
 }
 
@@ -158,7 +159,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   uint64_t *empty = full + 8;
   uint64_t *xbar = empty + 8;  // B operand loaded by TMA (no norm)
   uint64_t *accb = xbar + 1;
-  uint32_t *tmem_slot = (uint32_t *)(accb + 1);
+  uint64_t *rbar = accb + 1;  // peers' partial logits received
+  uint32_t *tmem_slot = (uint32_t *)(rbar + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
   int *flag = (int *)(tmem_slot + 2);  // [0] k-tiles multiplied, [2] k-tiles loaded
   unsigned char *wring = base + L.w_off, *xs = base + L.x_off;
@@ -174,7 +176,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   const int kb = KT * z / S, ke = KT * (z + 1) / S, nk = ke - kb;
   const int stages = a.stages;
   const uint32_t stage_bytes = (uint32_t)a.m_tiles * kWBox;
-  const uint32_t tcols = a.m_tiles * kRouteTok;  // 32 or 64 accumulator columns
+  // Four accumulators per 128-expert tile (the K16 steps of a k-tile go
+  // round-robin): dependent MMAs into one accumulator serialise, four short
+  // chains overlap.  128 or 256 columns.
+  constexpr int kAcc = 4;
+  const uint32_t tcols = a.m_tiles * kAcc * kRouteTok;
   for (int e = threadIdx.x; e < ep; e += kRouteThreads) cnt[e] = 0;
 
   if (threadIdx.x == 0) {
@@ -185,6 +191,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
     tc::mbar_init(accb, 1);
     tc::mbar_init(xbar, 1);
+    tc::mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -194,6 +201,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
                  "r"(tcols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -286,6 +294,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     tc::mbar_expect_tx(xbar, (uint32_t)nk * kXBox);
     for (int i = 0; i < nk; ++i) tc::tma_load_2d(xs + (size_t)i * kXBox, &tx, (kb + i) * 64, t0, xbar);
   }
+  __syncwarp();
   __syncthreads();
 
   if (threadIdx.x == 0) {  // producer: the rest of the K slice, if the ring is shorter
@@ -311,8 +320,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         const uint32_t wa = tc::smem_u32(wring + (size_t)s * stage_bytes + mt * kWBox);
 #pragma unroll
         for (int k16 = 0; k16 < 4; ++k16)
-          tc::mma_bf16(tmem + mt * kRouteTok, tc::sw128_desc(wa) + 2 * k16, tc::sw128_desc(xa) + 2 * k16, idesc,
-                       (i | k16) != 0);
+          tc::mma_bf16(tmem + (mt * kAcc + k16) * kRouteTok, tc::sw128_desc(wa) + 2 * k16,
+                       tc::sw128_desc(xa) + 2 * k16, idesc, i != 0);
       }
       tc::mma_commit(empty + s);
       ++issued;
@@ -320,6 +329,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (issued) tc::mma_commit(accb);
     flag[0] = issued;
   }
+  __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   __syncthreads();
   const int issued = flag[0];
 
@@ -335,8 +345,17 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       while (!tc::mbar_try_wait(accb, 0) && clock64() - c0 < tc::kWaitCycles) {
       }
       tc::fence_after();
-      tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + mt * kRouteTok, r);
-      tc::tmem_ld_wait();
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + mt * kAcc * kRouteTok;
+      tc::tmem_ld32(tl, r);
+      tc::tmem_ld_wait(r);
+#pragma unroll 1
+      for (int acc = 1; acc < kAcc; ++acc) {  // fixed order: deterministic
+        uint32_t r2[kRouteTok];
+        tc::tmem_ld32(tl + acc * kRouteTok, r2);
+        tc::tmem_ld_wait(r2);
+#pragma unroll
+        for (int t = 0; t < kRouteTok; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + __uint_as_float(r2[t]));
+      }
       have = !*abort;
     }
     if (mt < a.m_tiles) {
@@ -344,23 +363,43 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       for (int t = 0; t < kRouteTok; ++t) part[t * ep + e] = have ? __uint_as_float(r[t]) : 0.0f;
     }
   }
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the bulk copies read part
+  __syncwarp();
   tc::fence_before();
   __syncthreads();
   tc::cluster_sync();  // every CTA's partials are complete
 
+  // CTA q reduces tokens [q tpr, (q + 1) tpr): every CTA sends those rows of
+  // its partial to CTA q with one bulk shared-to-shared copy; the receiver
+  // adds the S rows in rank order (deterministic).
   const int tpr = kRouteTok / S;  // tokens reduced by this CTA
-  for (int idx = threadIdx.x; idx < tpr * ep; idx += kRouteThreads) {
-    const int j = idx / ep, e = idx - j * ep;
-    const uint32_t src = tc::smem_u32(part + (z * tpr + j) * ep + e);
-    float pv[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) pv[q] = q < S ? ld_cluster_f32(tc::cluster_addr(src, q)) : 0.0f;
-    float sum = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) sum += pv[q];  // rank order
-    logit[j * ep + e] = sum;
+  const uint32_t rows_bytes = (uint32_t)tpr * ep * 4;
+  float *recv = (float *)(base + L.recv_off);
+  if (threadIdx.x == 0) {
+    if (S > 1) tc::mbar_expect_tx(rbar, (uint32_t)(S - 1) * rows_bytes);
+    for (int q = 1; q < S; ++q) {
+      const int j = (z + q) % S;
+      tc::bulk_copy_to_peer(tc::cluster_addr(tc::smem_u32(recv) + (uint32_t)z * rows_bytes, (uint32_t)j),
+                            tc::smem_u32(part + (size_t)j * tpr * ep), rows_bytes,
+                            tc::cluster_addr(tc::smem_u32(rbar), (uint32_t)j));
+    }
   }
-  tc::cluster_sync();  // all reads of peers' partials done
+  if (S > 1) {  // bounded, and waited for even after an abort: no copy may still target this CTA at exit
+    const long long c0 = clock64();
+    while (!tc::mbar_try_wait(rbar, 0)) {
+      if (clock64() - c0 > tc::kWaitCycles) {
+        if (threadIdx.x == 0 && a.err) atomicExch(a.err, 54);
+        *abort = 1;
+        break;
+      }
+    }
+  }
+  for (int idx = threadIdx.x; idx < tpr * ep; idx += kRouteThreads) {
+    float sum = 0.0f;
+    for (int q = 0; q < S; ++q)  // rank order
+      sum += q == z ? part[(size_t)z * tpr * ep + idx] : recv[(size_t)q * tpr * ep + idx];
+    logit[idx] = sum;
+  }
   if (warp == 1) {
     tc::fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(tcols));
@@ -386,6 +425,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     else if (lane < k)
       pid[j * k + lane] = -1;
   }
+  __syncwarp();
   __syncthreads();
 
   // Stable ranks: pair p of this CTA ranks after the earlier pairs of the CTA
@@ -401,6 +441,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       atomicAdd(cnt + my_e[u], 1);
     }
   }
+  __syncwarp();
   tc::cluster_sync();  // every CTA's expert counts are complete
 #pragma unroll
   for (int u = 0; u < kPairIters; ++u) {
@@ -424,6 +465,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (int q = 0; q < 8; ++q) sum += pv[q];
     a.gcount[(size_t)grp * a.E + e] = sum;
   }
+  __syncwarp();
   tc::cluster_sync();  // peers' counts stay alive until every read is done
 }
 
@@ -528,6 +570,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
     if (lane >= off) x += y;
   }
   if (lane == 31) warp_tot[warp] = x;
+  __syncwarp();
   __syncthreads();
   int before = 0, all = 0;
 #pragma unroll
@@ -536,6 +579,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
     before += w < warp ? c : 0;
     all += c;
   }
+  __syncwarp();
   __syncthreads();  // warp_tot may be reused by the next scan
   *total = all;
   return before + x - v;
@@ -549,6 +593,7 @@ __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
   const int E = a.E, ng = a.ng, n = ng * E;
   int *soffs = tab + n, *stoff = soffs + E;
   for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
+  __syncwarp();
   __syncthreads();
   const int e = threadIdx.x;  // E <= kScatThreads
   int tot = 0;
@@ -586,6 +631,7 @@ __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
     }
     for (int i = threadIdx.x; i <= a.max_work; i += kScatThreads) a.sync[i] = 0;  // FFN counters
   }
+  __syncwarp();
   __syncthreads();
   // Pairs of this block: one warp per pair; the warp copies the token's row
   // into row r of its item's tiles (16-byte chunk c of k-tile kt at chunk
