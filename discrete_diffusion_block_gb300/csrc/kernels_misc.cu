@@ -67,6 +67,24 @@ __global__ void fill_gate_up_kernel(bf16 *dst, int E, int F, int d, uint32_t k0,
   }
 }
 
+// W_r (logical [E][d]) as tiles of 128-expert blocks, K = d; the last block
+// holds E % 128 rows (tiles of a block are rows x 64, contiguous per k-tile).
+__global__ void fill_router_kernel(bf16 *dst, int E, int d, uint32_t k0, uint32_t k1, uint32_t tid, float scale) {
+  const uint64_t n = (uint64_t)E * d;
+  const int KT = d / 64;
+  for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
+       j += (uint64_t)gridDim.x * blockDim.x) {
+    const int mt = (int)(j / ((uint64_t)128 * d));
+    const int rows = min(128, E - 128 * mt);
+    const uint64_t in_blk = j - (uint64_t)mt * 128 * d;  // within the block: [KT][rows][64]
+    const int kt = (int)(in_blk / ((uint64_t)rows * 64));
+    const int p = (int)(in_blk - (uint64_t)kt * rows * 64);
+    const int r = p >> 6;
+    const int c = kt * 64 + ((((p >> 3) & 7) ^ (r & 7)) << 3) + (p & 7);
+    dst[j] = weight_element((uint64_t)(128 * mt + r) * d + c, tid, k0, k1, scale);
+  }
+}
+
 // W_down (logical [E][d][F]) as tiles of 128-row blocks, K = F.
 __global__ void fill_down_kernel(bf16 *dst, int E, int F, int d, uint32_t k0, uint32_t k1, uint32_t tid,
                                  float scale) {
@@ -342,7 +360,10 @@ cudaError_t fill_weights(bf16 *dst, uint64_t n, uint64_t seed, uint32_t tid, uin
 cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F, int layer,
                              uint64_t seed, float std_dev, cudaStream_t st) {
   const uint32_t base = 100u + 16u * (uint32_t)layer;
-  cudaError_t e = fill_weights(wr, (uint64_t)E * d, seed, base + 4, 0, std_dev, st);
+  fill_router_kernel<<<grid_for((uint64_t)E * d, 256), 256, 0, st>>>(wr, E, d, (uint32_t)seed,
+                                                                       (uint32_t)(seed >> 32), base + 4,
+                                                                       weight_scale(std_dev));
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const uint64_t n = (uint64_t)E * 2 * F * d;
   fill_gate_up_kernel<<<grid_for(n, 256), 256, 0, st>>>(wgu, E, F, d, (uint32_t)seed,

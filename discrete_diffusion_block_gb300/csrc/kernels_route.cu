@@ -53,6 +53,7 @@ constexpr int kSmemBudget = 200 * 1024;  // dynamic; the expert sort adds 11 KB 
 struct RouteArgs {
   const float *h;      // norm: input rows fp32 [T][d]
   const float *gain;   // norm: RMSNorm gain [d]
+  const bf16 *wr;      // router weights as operand tiles (rows = experts, the last block partial)
   float eps;
   bf16 *xn;            // norm: normalised rows out [T][d]
   int T, d, E, k, tile_rows;
@@ -82,6 +83,24 @@ __host__ __device__ inline RouteSmem route_smem(int S, int nk_max, int stages, i
   s.bars_off = (s.pid_off + (uint32_t)(kRouteTok / S) * 16 * 4 + 15) & ~15u;
   s.bytes = s.bars_off + (8 + 8 + 3) * 8 + 32 + 1024;  // full[8], empty[8], x, acc, recv; words; alignment slack
   return s;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+// K-tile kt of every 128-expert block of W_r into one ring stage: block m
+// holds min(128, E - 128 m) rows, contiguous per k-tile.
+__device__ __forceinline__ void load_w_tile(const bf16 *wr, int E, int KT, int m_tiles, int kt, unsigned char *stage,
+                                            uint64_t *bar, bool expect = true) {
+  if (expect) tc::mbar_expect_tx(bar, (uint32_t)E * 128);
+  for (int mt = 0; mt < m_tiles; ++mt) {
+    const int rows = min(128, E - 128 * mt);
+    bulk_load(stage + mt * kWBox, wr + ((size_t)128 * KT * mt + (size_t)rows * kt) * 64, (uint32_t)rows * 128, bar);
+  }
 }
 
 __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
@@ -151,7 +170,7 @@ __device__ __forceinline__ void topk_warp(const float *lrow, int E, int k, int l
 
 template <bool NORM>
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, RouteArgs a) {
+    route_kernel(const __grid_constant__ CUtensorMap tx, RouteArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const RouteSmem L = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
@@ -162,7 +181,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   uint64_t *rbar = accb + 1;  // peers' partial logits received
   uint32_t *tmem_slot = (uint32_t *)(rbar + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
-  int *flag = (int *)(tmem_slot + 2);  // [0] k-tiles multiplied, [2] k-tiles loaded
+  int *flag = (int *)(tmem_slot + 2);  // [2] k-tiles loaded (the producer's own count)
   unsigned char *wring = base + L.w_off, *xs = base + L.x_off;
   float *part = (float *)(base + L.part_off), *logit = (float *)(base + L.logit_off);
   float *ss = (float *)(base + L.ss_off);
@@ -187,9 +206,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     *abort = 0;
     for (int s = 0; s < stages; ++s) {
       tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
+      tc::mbar_init(empty + s, kAcc);  // one commit per MMA issuer
     }
-    tc::mbar_init(accb, 1);
+    tc::mbar_init(accb, kAcc);
     tc::mbar_init(xbar, 1);
     tc::mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -209,13 +228,16 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
   // Weights never change: the first ring fill starts before the wait on the
   // kernel that produced this layer's activations.
+  // When the ring holds the whole K slice, all of it arrives on one barrier
+  // phase: copies in flight together, one wait (a barrier phase per stage
+  // paces the copies one after another).
   const int pre = min(stages, nk);
+  const bool one_phase = nk <= stages;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < pre; ++i) {
-      tc::mbar_expect_tx(full + i, stage_bytes);
-      for (int mt = 0; mt < a.m_tiles; ++mt)
-        tc::tma_load_2d(wring + (size_t)i * stage_bytes + mt * kWBox, &tw, (kb + i) * 64, mt * 128, full + i);
-    }
+    if (one_phase) tc::mbar_expect_tx(full, (uint32_t)nk * a.E * 128);
+    for (int i = 0; i < pre; ++i)
+      load_w_tile(a.wr, a.E, KT, a.m_tiles, kb + i, wring + (size_t)i * stage_bytes, one_phase ? full : full + i,
+                  !one_phase);
   }
   // Norm: kTokThreads threads per token; thread `sub` owns the float4
   // columns c4b + kTokThreads u of the CTA's slice.  The gain is a weight:
@@ -302,36 +324,32 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (; i < nk; ++i) {
       const int s = i % stages;
       if (!tc::mbar_wait(empty + s, ((i / stages) - 1) & 1, a.err, 51, abort)) break;
-      tc::mbar_expect_tx(full + s, stage_bytes);
-      for (int mt = 0; mt < a.m_tiles; ++mt)
-        tc::tma_load_2d(wring + (size_t)s * stage_bytes + mt * kWBox, &tw, (kb + i) * 64, mt * 128, full + s);
+      load_w_tile(a.wr, a.E, KT, a.m_tiles, kb + i, wring + (size_t)s * stage_bytes, full + s);
     }
     flag[2] = i;
-  } else if (threadIdx.x == 32) {  // MMA issuer
+  } else if (lane == 0 && warp >= 1 && warp <= kAcc) {
+    // MMA issuers: one thread per accumulator (K16 step k16 of every k-tile):
+    // a single thread issuing N = 32 MMAs back to back waits on each issue.
+    const int k16 = warp - 1;
     bool ok = NORM || tc::mbar_wait(xbar, 0, a.err, 52, abort);
     constexpr uint32_t idesc = tc::idesc_bf16(128, kRouteTok);
-    int issued = 0;
     for (int i = 0; i < nk && ok; ++i) {
       const int s = i % stages;
-      if (!tc::mbar_wait(full + s, (i / stages) & 1, a.err, 53, abort)) break;
+      if ((!one_phase || i == 0) && !tc::mbar_wait(one_phase ? full : full + s, one_phase ? 0 : (i / stages) & 1, a.err, 53, abort))
+        break;
       tc::fence_after();
       const uint32_t xa = tc::smem_u32(xs + (size_t)i * kXBox);
       for (int mt = 0; mt < a.m_tiles; ++mt) {
         const uint32_t wa = tc::smem_u32(wring + (size_t)s * stage_bytes + mt * kWBox);
-#pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16)
-          tc::mma_bf16(tmem + (mt * kAcc + k16) * kRouteTok, tc::sw128_desc(wa) + 2 * k16,
-                       tc::sw128_desc(xa) + 2 * k16, idesc, i != 0);
+        tc::mma_bf16(tmem + (mt * kAcc + k16) * kRouteTok, tc::sw128_desc(wa) + 2 * k16, tc::sw128_desc(xa) + 2 * k16,
+                     idesc, i != 0);
       }
-      tc::mma_commit(empty + s);
-      ++issued;
+      if (!one_phase) tc::mma_commit(empty + s);  // frees the stage for a refill
     }
-    if (issued) tc::mma_commit(accb);
-    flag[0] = issued;
+    tc::mma_commit(accb);  // always: with no MMA issued (an abort) it arrives at once
   }
   __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   __syncthreads();
-  const int issued = flag[0];
 
   // Partial logits: warp w drains TMEM lanes 32 (w % 4) .. of 128-expert tile w / 4.
   {
@@ -339,7 +357,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     const int e = mt * 128 + q * 32 + lane;
     uint32_t r[kRouteTok];
     bool have = false;
-    if (mt < a.m_tiles && issued) {
+    if (mt < a.m_tiles) {
       // bounded, and waited for even after an abort: TMEM is freed only after the MMAs finished
       const long long c0 = clock64();
       while (!tc::mbar_try_wait(accb, 0) && clock64() - c0 < tc::kWaitCycles) {
@@ -406,7 +424,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   // Bounded drain of weight boxes still in flight after an abort.
   if (threadIdx.x == 0 && *abort) {
-    for (int i = max(0, flag[2] - stages); i < flag[2]; ++i) {
+    for (int i = one_phase ? 0 : max(0, flag[2] - stages); i < (one_phase ? 1 : flag[2]); ++i) {
       const long long c0 = clock64();
       while (!tc::mbar_try_wait(full + i % stages, (i / stages) & 1) && clock64() - c0 < tc::kWaitCycles) {
       }
@@ -470,7 +488,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 }
 
 template <bool NORM>
-cudaError_t launch_route(const CUtensorMap &tw, const CUtensorMap &tx, RouteArgs a, cudaStream_t st) {
+cudaError_t launch_route(const CUtensorMap &tx, RouteArgs a, cudaStream_t st) {
   const RouteSmem L = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
   auto kern = route_kernel<NORM>;
   static unsigned long long attr_set = 0;
@@ -504,7 +522,7 @@ cudaError_t launch_route(const CUtensorMap &tw, const CUtensorMap &tx, RouteArgs
   ++na;
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a);
+  return cudaLaunchKernelEx(&cfg, kern, tx, a);
 }
 
 cudaError_t route_common(bool norm, const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr,
@@ -534,13 +552,13 @@ cudaError_t route_common(bool norm, const float *h, const float *gain, float eps
   a.rank = rank;
   a.gcount = gcount;
   a.err = err;
-  CUtensorMap tw, tx;
-  cudaError_t e = tmap_bf16_cached(&tw, wr, (uint64_t)E, (uint64_t)d, 128);
-  if (e != cudaSuccess) return e;
-  if (norm) return launch_route<true>(tw, tw, a, st);
+  a.wr = wr;
+  CUtensorMap tx{};  // the norm path writes the B operand itself
+  if (norm) return launch_route<true>(tx, a, st);
+  cudaError_t e;
   e = tmap_bf16_cached(&tx, xn, (uint64_t)T, (uint64_t)d, kRouteTok);
   if (e != cudaSuccess) return e;
-  return launch_route<false>(tw, tx, a, st);
+  return launch_route<false>(tx, a, st);
 }
 
 // ---------------------------------------------------------------------------

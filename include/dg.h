@@ -196,14 +196,17 @@ int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t
  *   EMBED, LM_HEAD   [V][d]
  *   WQKV             [(Hq + 2 Hkv) * hd][d]   rows: W_q, then W_k, then W_v
  *   WO               [d][Hq * hd]
- *   ROUTER           [E][d]
+ *   ROUTER           128-expert blocks of     block b: experts 128 b .. (rows =
+ *                    [d/64] tiles             min(128, E - 128 b)); tile (b, j):
+ *                                             those rows, columns 64 j .. 64 j + 63
  *   W_GATE_UP        [E][F/64][d/64] tiles    tile (e, b, j): rows 64 b .. 64 b + 63
  *                                             of W_gate,e then the same rows of
  *                                             W_up,e; columns 64 j .. 64 j + 63
  *   W_DOWN           [E][d/128][F/64] tiles   tile (e, b, j): rows 128 b ..
  *                                             128 b + 127 of W_down,e; columns
  *                                             64 j .. 64 j + 63
- *   A tile is 128 rows x 64 bf16 columns, 16 KB, row-major with 128-byte rows
+ *   A tile is 128 rows (fewer in the last ROUTER block) x 64 bf16 columns,
+ *   row-major with 128-byte rows
  *   in which the 16-byte chunk c of row r sits at chunk position c ^ (r % 8)
  *   (the tensor core's 128-byte-swizzled operand order, so that one bulk
  *   copy stages a tile).

@@ -43,6 +43,22 @@ def untile(phys, lead, blocks, kt):
     return np.moveaxis(t, -3, -2).reshape(*lead, blocks * 128, kt * 64)
 
 
+def untile_router(phys, E, d):
+    """Router tiles (128-expert blocks, the last one partial; per block the
+    k-tiles [rows][64], chunk c of row r at position c ^ (r % 8)) back to
+    [E][d]."""
+    out = np.zeros((E, d), np.float32)
+    off = 0
+    for b0 in range(0, E, 128):
+        rows = min(128, E - b0)
+        for j in range(d // 64):
+            t = phys[off: off + rows * 64].reshape(rows, 8, 8)
+            pos = np.arange(8)[None, :] ^ (np.arange(rows)[:, None] % 8)
+            out[b0:b0 + rows, 64 * j:64 * j + 64] = np.take_along_axis(t, pos[..., None], axis=1).reshape(rows, 64)
+            off += rows * 64
+    return out
+
+
 def test_moe_weight_layout_matches_logical_tensors():
     d, E, F, L = 256, 4, 192, 3
     wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
@@ -50,7 +66,7 @@ def test_moe_weight_layout_matches_logical_tensors():
     wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
     dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, L, 5, 0.02)
     base = 100 + 16 * L
-    assert np.array_equal(bf16_to_f32(wr).reshape(E, d), ow.tensor(5, base + 4, (E, d), 0.02))
+    assert np.array_equal(untile_router(bf16_to_f32(wr), E, d), ow.tensor(5, base + 4, (E, d), 0.02))
     # gate/up: 128-row blocks of 64 gate rows then the same 64 up rows
     gu = untile(bf16_to_f32(wgu), (E,), F // 64, d // 64).reshape(E, F // 64, 2, 64, d)
     g = ow.tensor(5, base + 5, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
@@ -58,6 +74,15 @@ def test_moe_weight_layout_matches_logical_tensors():
     assert np.array_equal(gu[:, :, 0], g) and np.array_equal(gu[:, :, 1], u)
     wdl = untile(bf16_to_f32(wd), (E,), d // 128, F // 64)
     assert np.array_equal(wdl, ow.tensor(5, base + 7, (E, d, F), 0.02))
+
+
+def test_router_layout_with_a_partial_expert_block():
+    d, E, F, L = 128, 200, 64, 1
+    wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
+    wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
+    wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
+    dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, L, 9, 0.02)
+    assert np.array_equal(untile_router(bf16_to_f32(wr), E, d), ow.tensor(9, 100 + 16 * L + 4, (E, d), 0.02))
 
 
 # ---- sampler: bit-exact given identical logits --------------------------------
