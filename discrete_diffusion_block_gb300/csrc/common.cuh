@@ -230,6 +230,19 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 bool pdl_enabled();  // host: on unless DG_PDL=0 is set in the environment
 
+// Operand tiles of a row-major [rows][cols] bf16 matrix (cols a multiple of
+// 64), the layout every tensor-core operand of the decoder is stored in: row
+// block b (128 rows; the last one rows % 128 when that is not 0) holds
+// cols / 64 tiles of rows_b x 64 elements, contiguous per k-tile; inside a
+// tile the 16-byte chunk c of row r sits at chunk position c ^ (r % 8) (the
+// tensor core's 128-byte-swizzled shared-memory order), so one contiguous
+// bulk copy stages a tile.  Element index of (r, c):
+__host__ __device__ inline size_t tiled_index(int rows, int cols, int r, int c) {
+  const int b = r >> 7, rr = r & 127, kt = c >> 6, cc = c & 63;
+  const int rows_b = rows - 128 * b < 128 ? rows - 128 * b : 128;
+  return (size_t)128 * cols * b + (size_t)rows_b * 64 * kt + (size_t)rr * 64 + (size_t)((((cc >> 3) ^ (rr & 7)) << 3) | (cc & 7));
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args &&...args) {

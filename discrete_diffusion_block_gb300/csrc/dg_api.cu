@@ -90,6 +90,7 @@ struct dg_model {
   int Tmax = 0;
   int *ids = nullptr;
   float *h = nullptr;
+  bf16 *xq = nullptr;  // the attention-norm output, as operand tiles (the QKV operand)
   bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr,
        *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
@@ -285,16 +286,16 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
   for (int L = 0; L < c.n_layers; ++L) {
     const Layer &W = m->layers[L];
     if (L == 0 || !fuse_norm)
-      KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xn, m->h, W.attn_norm, T, d, c.rms_eps, st));
+      KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xq, m->h, W.attn_norm, T, d, c.rms_eps, st, nullptr, true));
     dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), m->page_table, pos0, c.page_size,
                   c.n_q_heads, c.n_kv_heads, c.head_dim, m->cos_t, m->sin_t};
     int *err = m->done_dev + 1;
-    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xn, W.wqkv, T, d, qo, err, st));
+    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xq, W.wqkv, T, d, qo, err, st));
     if (kv_only_last && L == c.n_layers - 1) break;
     dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal, m->n_pages};
     KL(DG_K_ATTENTION, dg::attention_launch_count(as),
        dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
-                     m->attn_ws_bytes, st, err));
+                     m->attn_ws_bytes, st, err, true));
     KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
@@ -311,7 +312,7 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     if (fuse_norm && L + 1 < c.n_layers) {
       KL(DG_K_COMBINE, 1,
          dg::moe_combine_norm(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, m->layers[L + 1].attn_norm,
-                              c.rms_eps, m->xn, st));
+                              c.rms_eps, m->xq, st));
     } else {
       KL(DG_K_COMBINE, 1, dg::moe_combine(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, true, st));
     }
@@ -331,10 +332,8 @@ int fill_model_weights(dg_model *m) {
   for (int L = 0; L < c.n_layers; ++L) {
     const uint32_t b = 100u + 16u * (uint32_t)L;
     Layer &W = m->layers[L];
-    CK(dg::fill_weights(W.wqkv, (uint64_t)qd * d, s, b + 0, 0, sd, st));
-    CK(dg::fill_weights(W.wqkv + (size_t)qd * d, (uint64_t)kd * d, s, b + 1, 0, sd, st));
-    CK(dg::fill_weights(W.wqkv + (size_t)(qd + kd) * d, (uint64_t)kd * d, s, b + 2, 0, sd, st));
-    CK(dg::fill_weights(W.wo, (uint64_t)d * qd, s, b + 3, 0, sd, st));
+    CK(dg::fill_tiled_weights(W.wqkv, qd + 2 * kd, d, qd, qd + kd, b + 0, b + 1, b + 2, s, sd, st));
+    CK(dg::fill_tiled_weights(W.wo, d, qd, d, d, b + 3, b + 3, b + 3, s, sd, st));
     CK(dg::fill_moe_weights(W.wr, W.wgu, W.wd, d, c.n_experts, c.d_ff, L, s, sd, st));
     CK(dg::fill_const(W.attn_norm, d, 1.0f, st));
     CK(dg::fill_const(W.moe_norm, d, 1.0f, st));
@@ -377,6 +376,7 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->ids, T));
   CKR(m->alloc(&m->h, (size_t)T * d));
   CKR(m->alloc(&m->xn, (size_t)T * d));
+  CKR(m->alloc(&m->xq, (size_t)T * d));
   CKR(m->alloc(&m->xn_lo, (size_t)C * d));
   CKR(m->alloc(&m->moe_stats, 2));
   CKR(m->alloc(&m->q, (size_t)T * qd));

@@ -24,11 +24,8 @@
 namespace dg {
 
 struct TcArgs {
-  int M, N, K;             // N: valid B rows (non-grouped)
-  int a_group_rows;        // A row offset per group (expert)
-  const int *work;         // grouped: [n_work][2] = (group, n0)
-  const int *n_work;
-  const int *group_offs;   // grouped: B rows of group g = [offs[g], offs[g+1])
+  int M, N, K;             // D[M][N] = A[M][K] . B[N][K]^T
+  const bf16 *a, *b;       // A (weights) and B (activations) as operand tiles (tiled_index)
   int *err;                // device error word (timeouts)
 };
 
@@ -78,6 +75,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int *err
     }
   }
   return true;
+}
+
+// Contiguous bulk copy global -> this CTA's shared memory, completion on bar.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
@@ -246,8 +251,7 @@ struct SkSmem {
 
 template <int SPLIT, class Epi>
 __global__ void __launch_bounds__(128, 1)
-    tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                      TcArgs g, Epi epi) {
+    tc_gemm_sk_kernel(TcArgs g, Epi epi) {
   using S = tc::SkSmem<SPLIT, Epi>;
   constexpr int STAGES = tc::kSkStages, W = S::W;
   extern __shared__ unsigned char smem_raw[];
@@ -259,19 +263,11 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t *tmem_slot = (uint32_t *)(rbar + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
-  // Output units are (item, 128-row M tile) pairs; items are the n-tiles of a
-  // plain launch or the device work list of a grouped one.  Cluster c (the
-  // SPLIT CTAs blockIdx.x = c * SPLIT + z, one per K range) takes units c,
-  // c + n_clusters, ..., so the grid is sized to the machine and the units
-  // spread evenly over it.
-  int n_items;
-  if (g.work) {  // the work list is an earlier kernel's output
-    pdl_wait();
-    pdl_trigger();
-    n_items = *g.n_work;
-  } else {
-    n_items = ceil_div(g.N, tc::kSkBN);
-  }
+  // Output units are (256-column N tile, 128-row M tile) pairs.  Cluster c
+  // (the SPLIT CTAs blockIdx.x = c * SPLIT + z, one per K range) takes units
+  // c, c + n_clusters, ..., so the grid is sized to the machine and the
+  // units spread evenly over it.
+  const int n_items = ceil_div(g.N, tc::kSkBN);
   const int m_tiles = ceil_div(g.M, 128);
   const int n_units = n_items * m_tiles;
   const int cluster = blockIdx.x / SPLIT, n_clusters = gridDim.x / SPLIT;
@@ -306,23 +302,36 @@ __global__ void __launch_bounds__(128, 1)
   auto a_tile = [&](int s) { return base + (size_t)s * S::stage_bytes; };
   auto b_tile = [&](int s) { return base + (size_t)s * S::stage_bytes + tc::kATileBytes; };
 
-  // Weights never change: a plain launch starts streaming its first unit's A
-  // boxes before waiting for the kernel that produced B.
-  int pre = 0;
-  if (!g.work) {
-    pre = min(STAGES, ke - kb);
-    if (warp == 0 && lane == 0) {
-      const int y0 = cluster / m_tiles, mt0 = cluster - y0 * m_tiles;
-      const int nv = min(tc::kSkBN, g.N - y0 * tc::kSkBN);
-      const uint32_t tx0 = tc::kATileBytes + (uint32_t)((nv + 63) >> 6) * tc::kBChunkBytes;
-      for (int i = 0; i < pre; ++i) {
-        tc::mbar_expect_tx(full + i, tx0);
-        tc::tma_load_2d(a_tile(i), &ta, (kb + i) * tc::kBK, mt0 * 128, full + i);
-      }
+  // One k-tile of a unit: the A tile of M block mt and the B tiles of the
+  // (up to two) 128-row blocks of N tile y, each one contiguous bulk copy.
+  auto a_bytes = [&](int mt) { return (uint32_t)min(128, g.M - 128 * mt) * 128; };
+  auto b_rows = [&](int rb) { return max(0, min(128, g.N - 128 * rb)); };
+  auto tx_of = [&](int y, int mt) {
+    return a_bytes(mt) + (uint32_t)(b_rows(2 * y) + b_rows(2 * y + 1)) * 128;
+  };
+  auto load_a = [&](int s, int mt, int kt) {
+    tc::bulk_load(a_tile(s), g.a + tiled_index(g.M, g.K, 128 * mt, 64 * kt), a_bytes(mt), full + s);
+  };
+  auto load_b = [&](int s, int y, int kt) {
+    for (int h = 0; h < 2; ++h) {
+      const int rb = 2 * y + h, rows = b_rows(rb);
+      if (rows > 0)
+        tc::bulk_load(b_tile(s) + h * 16384, g.b + tiled_index(g.N, g.K, 128 * rb, 64 * kt), (uint32_t)rows * 128,
+                      full + s);
     }
-    pdl_wait();
-    pdl_trigger();
+  };
+  // Weights never change: the first unit's A tiles are requested before the
+  // wait on the kernel that produced B.
+  const int pre = min(STAGES, ke - kb);
+  if (warp == 0 && lane == 0) {
+    const int y0 = cluster / m_tiles, mt0 = cluster - y0 * m_tiles;
+    for (int i = 0; i < pre; ++i) {
+      tc::mbar_expect_tx(full + i, tx_of(y0, mt0));
+      load_a(i, mt0, kb + i);
+    }
   }
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;  // an earlier timeout: do not wait again
 
   int it = 0;     // ring position: k-tiles issued (producer) / consumed (MMA) so far
@@ -333,23 +342,12 @@ __global__ void __launch_bounds__(128, 1)
     ctx.m0 = mt * 128;
     ctx.group = 0;
     ctx.b_base = 0;
-    int n_total = g.N;
-    if (g.work) {
-      ctx.group = g.work[2 * y];
-      ctx.n0 = g.work[2 * y + 1];
-      ctx.b_base = g.group_offs[ctx.group];
-      n_total = g.group_offs[ctx.group + 1] - ctx.b_base;
-    } else {
-      ctx.n0 = y * tc::kSkBN;
-    }
+    ctx.n0 = y * tc::kSkBN;
     ctx.swz = 0;
     ctx.m_valid = min(128, g.M - ctx.m0);
-    ctx.n_valid = max(0, min(tc::kSkBN, n_total - ctx.n0));
-    const int nb = max(1, (ctx.n_valid + 63) >> 6);     // 64-row B boxes per stage
+    ctx.n_valid = max(0, min(tc::kSkBN, g.N - ctx.n0));
     const int n_mma = max(16, (ctx.n_valid + 15) & ~15);  // MMA N
-    const uint32_t tx_bytes = tc::kATileBytes + (uint32_t)nb * tc::kBChunkBytes;
-    const int a_row = ctx.group * g.a_group_rows + ctx.m0;
-    const int b_row = ctx.b_base + ctx.n0;
+    const uint32_t tx_bytes = tx_of(y, mt);
 
     if (warp == 0 && lane == 0) {
       int issued = it;
@@ -357,12 +355,11 @@ __global__ void __launch_bounds__(128, 1)
         const int s = issued % STAGES, r = issued / STAGES;
         if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 1, abort);
         if (*abort) break;
-        if (issued >= pre) {  // else this stage's A box is already on its way
+        if (issued >= pre) {  // else this stage's A tile is already on its way
           tc::mbar_expect_tx(full + s, tx_bytes);
-          tc::tma_load_2d(a_tile(s), &ta, kt * tc::kBK, a_row, full + s);
+          load_a(s, mt, kt);
         }
-        for (int c = 0; c < nb; ++c)
-          tc::tma_load_2d(b_tile(s) + c * tc::kBChunkBytes, &tb, kt * tc::kBK, b_row + 64 * c, full + s);
+        load_b(s, y, kt);
       }
       if (*abort) {
         // Drain: wait (bounded) for the last copy issued into each stage.
@@ -491,8 +488,7 @@ cudaError_t make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uin
 // Split-K launch: n_clusters clusters of SPLIT CTAs (grid.x = n_clusters *
 // SPLIT, cluster dims (SPLIT, 1, 1)); the clusters walk the output units.
 template <int SPLIT, class Epi>
-cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
-                         const Epi &epi, int n_clusters, cudaStream_t st) {
+cudaError_t launch_tc_sk(const TcArgs &g, const Epi &epi, int n_clusters, cudaStream_t st) {
   using S = tc::SkSmem<SPLIT, Epi>;
   static_assert(S::bytes <= 232448, "shared memory of the split-K GEMM");
   auto kern = tc_gemm_sk_kernel<SPLIT, Epi>;
@@ -528,7 +524,7 @@ cudaError_t launch_tc_sk(const CUtensorMap &ta, const CUtensorMap &tb, const TcA
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, g, epi);
+  return cudaLaunchKernelEx(&cfg, kern, g, epi);
 }
 
 }  // namespace dg

@@ -11,6 +11,10 @@ namespace dg {
 // ---- misc kernels (kernels_misc.cu) ---------------------------------------
 cudaError_t fill_weights(bf16 *dst, uint64_t n, uint64_t seed, uint32_t tid, uint64_t e0,
                          float std_dev, cudaStream_t st);
+// A [rows][cols] weight matrix as operand tiles (tiled_index) whose rows
+// [0, r1), [r1, r2), [r2, rows) are the generated tensors tid0, tid1, tid2.
+cudaError_t fill_tiled_weights(bf16 *dst, int rows, int cols, int r1, int r2, uint32_t tid0, uint32_t tid1,
+                               uint32_t tid2, uint64_t seed, float std_dev, cudaStream_t st);
 cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F, int layer,
                              uint64_t seed, float std_dev, cudaStream_t st);
 cudaError_t fill_const(float *dst, size_t n, float v, cudaStream_t st);
@@ -19,8 +23,10 @@ cudaError_t rope_table(float *cos_t, float *sin_t, int max_pos, int head_dim, fl
 cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
                         uint64_t seed, int canvas, cudaStream_t st);
 cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st);
+// out = RMSNorm(h) * gain (bf16), row-major, or as operand tiles (tiled_index)
+// when `tiled` (then out_lo must be null).
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
-                         cudaStream_t st, bf16 *out_lo = nullptr);
+                         cudaStream_t st, bf16 *out_lo = nullptr, bool tiled = false);
 // Routing of one MoE layer (kernels_route.cu), two launches.
 // moe_route: top-k of the router logits r = xn W_r^T (value desc, expert id
 // asc; softmax gates over the selected logits) into ids / gates [T][k]; for
@@ -65,10 +71,10 @@ cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
 // h[t] += sum_s gate * y (as moe_combine with accumulate), then the RMSNorm of
-// the updated row with `gain` into xn (bf16): the next layer's input norm.
-// d <= 4096.
+// the updated row with `gain` into x_tiles (bf16 operand tiles, tiled_index
+// over [T][d]): the next layer's QKV input.  d <= 4096, a multiple of 64.
 cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const int *slot_row,
-                             int T, int k, int d, const float *gain, float eps, bf16 *xn,
+                             int T, int k, int d, const float *gain, float eps, bf16 *x_tiles,
                              cudaStream_t st);
 cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,
                       const int *page_table, int L, int n_pages, int pos0, int n, int Hkv, int hd,
@@ -83,9 +89,11 @@ struct QkvOut {
   const float *cos_t, *sin_t;  // [max_pos][hd/2]
 };
 // `err`: device error word set by a tensor-core GEMM whose bounded wait gave up.
-cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o, int *err,
+// Operands are operand tiles (tiled_index): x_tiles / act_tiles [T][K],
+// wqkv [(Hq + 2 Hkv) hd][d] (rows W_q, W_k, W_v), w [N][K].
+cudaError_t gemm_qkv(const bf16 *x_tiles, const bf16 *wqkv, int T, int d, const QkvOut &o, int *err,
                      cudaStream_t st);
-cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
+cudaError_t gemm_residual(const bf16 *act_tiles, const bf16 *w, int T, int K, int N, float *h, int *err,
                           cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
   // out[T][N] = act . w^T
 constexpr int kExpertTileRows = 128;  // token rows per expert work item (MMA N <= 128)
@@ -119,8 +127,10 @@ struct AttnShape {
 size_t attention_workspace_bytes(const AttnShape &s);
 int attention_launch_count(const AttnShape &s);
 // err (optional, device): error word set when a bounded wait of the kernel gives up.
+// out_tiles: out as operand tiles (tiled_index over [n_new][Hq hd]), else
+// row-major [n_new][Hq][hd].
 cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const int *page_table,
                       const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st,
-                      int *err = nullptr);
+                      int *err = nullptr, bool out_tiles = false);
 
 }  // namespace dg

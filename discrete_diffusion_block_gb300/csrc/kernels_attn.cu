@@ -58,6 +58,7 @@ struct AttnParams {
   int *err;        // device error word (bounded waits, bad page indices), may be null
   int n_pages;     // physical pages of the pools, 0 when unknown
   bf16 *final_out; // split launches: where the cluster's merge writes the output
+  int out_tiles;   // outputs as operand tiles over [n_new][Hq hd] (the o-projection operand)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -490,7 +491,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint2 w;
         w.x = pack_bf16(v.x, v.y);
         w.y = pack_bf16(v.z, v.w);
-        *(uint2 *)(p.out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = w;
+        *(uint2 *)(p.out + (p.out_tiles ? tiled_index(p.n_new, p.Hq * HD, t, h * HD + 4 * c4)
+                                        : ((size_t)t * p.Hq + h) * HD + 4 * c4)) = w;
       }
     }
     return;
@@ -565,7 +567,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint2 v;
     v.x = pack_bf16(acc.x * invL, acc.y * invL);
     v.y = pack_bf16(acc.z * invL, acc.w * invL);
-    *(uint2 *)(p.final_out + ((size_t)t * p.Hq + h) * HD + 4 * c4) = v;
+    *(uint2 *)(p.final_out + (p.out_tiles ? tiled_index(p.n_new, p.Hq * HD, t, h * HD + 4 * c4)
+                                          : ((size_t)t * p.Hq + h) * HD + 4 * c4)) = v;
   }
   __syncwarp();
   tc::cluster_sync();  // every copy out of this block's shared memory has landed
@@ -704,7 +707,7 @@ cudaError_t launch_attn(const CUtensorMap &tq, const AttnParams &p, dim3 grid, c
 
 cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const int *page_table,
                       const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st,
-                      int *err) {
+                      int *err, bool out_tiles) {
   if (s.n_new <= 0) return cudaSuccess;
   if ((s.hd != 64 && s.hd != 128) || s.Hq % s.Hkv != 0 || s.pg % 64 != 0) return cudaErrorInvalidValue;
   const int G = s.Hq / s.Hkv;
@@ -731,6 +734,8 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   (void)ws_bytes;
   p.out = pl.splits > 1 ? nullptr : out;  // split blocks merge in the cluster, then write final_out
   p.final_out = out;
+  p.out_tiles = out_tiles ? 1 : 0;
+  if (out_tiles && (s.Hq * s.hd) % 64) return cudaErrorInvalidValue;
   // Q [T][Hq][hd] as a 4-D tensor (hd, G, Hkv, T): a box of 64 x G x 1 x 128/G
   // lands as 128 rows (token, head of the group) of 128 bytes.
   CUtensorMap tq;

@@ -157,11 +157,13 @@ struct EpiResidual {
   }
 };
 
-TcArgs targs(int M, int N, int K, int *err) {
+TcArgs targs(int M, int N, int K, const bf16 *a, const bf16 *b, int *err) {
   TcArgs g{};
   g.M = M;
   g.N = N;
   g.K = K;
+  g.a = a;
+  g.b = b;
   g.err = err;
   return g;
 }
@@ -279,38 +281,33 @@ static int pick_split(int units, int kt) {
 }
 
 template <class Epi>
-static cudaError_t launch_split(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &g,
+static cudaError_t launch_split(const TcArgs &g,
                                 const Epi &epi, int n_clusters, int split, cudaStream_t st) {
   switch (split) {
-    case 4: return launch_tc_sk<4>(ta, tb, g, epi, n_clusters, st);
-    case 2: return launch_tc_sk<2>(ta, tb, g, epi, n_clusters, st);
-    default: return launch_tc_sk<1>(ta, tb, g, epi, n_clusters, st);
+    case 4: return launch_tc_sk<4>(g, epi, n_clusters, st);
+    case 2: return launch_tc_sk<2>(g, epi, n_clusters, st);
+    default: return launch_tc_sk<1>(g, epi, n_clusters, st);
   }
 }
 
-cudaError_t gemm_qkv(const bf16 *xn, const bf16 *wqkv, int T, int d, const QkvOut &o,
+cudaError_t gemm_qkv(const bf16 *x_tiles, const bf16 *wqkv, int T, int d, const QkvOut &o,
                      int *err, cudaStream_t st) {
   const int M = (o.Hq + 2 * o.Hkv) * o.hd;
-  CUtensorMap ta, tb;
-  TMAP(ta, wqkv, M, d, 128);
-  TMAP(tb, xn, T, d, 64);
-  if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd) return cudaErrorInvalidValue;
+  if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd || d % 64) return cudaErrorInvalidValue;
   EpiQkv epi{o};
-  const TcArgs g = targs(M, T, d, err);
+  const TcArgs g = targs(M, T, d, wqkv, x_tiles, err);
   const int units = ceil_div(M, 128) * ceil_div(T, tc::kSkBN), kt = d / tc::kBK;
-  if (kt >= 4) return launch_tc_sk<4>(ta, tb, g, epi, plain_clusters(units, 4), st);
-  return launch_tc_sk<1>(ta, tb, g, epi, plain_clusters(units, 1), st);
+  if (kt >= 4) return launch_tc_sk<4>(g, epi, plain_clusters(units, 4), st);
+  return launch_tc_sk<1>(g, epi, plain_clusters(units, 1), st);
 }
 
-cudaError_t gemm_residual(const bf16 *act, const bf16 *w, int T, int K, int N, float *h, int *err,
+cudaError_t gemm_residual(const bf16 *act_tiles, const bf16 *w, int T, int K, int N, float *h, int *err,
                           cudaStream_t st) {
-  CUtensorMap ta, tb;
-  TMAP(ta, w, N, K, 128);
-  TMAP(tb, act, T, K, 64);
+  if (K % 64) return cudaErrorInvalidValue;
   EpiResidual epi{h, N};
   const int units = ceil_div(N, 128) * ceil_div(T, tc::kSkBN);
   const int split = pick_split(units, K / tc::kBK);
-  return launch_split(ta, tb, targs(N, T, K, err), epi, plain_clusters(units, split), split, st);
+  return launch_split(targs(N, T, K, w, act_tiles, err), epi, plain_clusters(units, split), split, st);
 }
 
 

@@ -67,21 +67,32 @@ __global__ void fill_gate_up_kernel(bf16 *dst, int E, int F, int d, uint32_t k0,
   }
 }
 
-// W_r (logical [E][d]) as tiles of 128-expert blocks, K = d; the last block
-// holds E % 128 rows (tiles of a block are rows x 64, contiguous per k-tile).
-__global__ void fill_router_kernel(bf16 *dst, int E, int d, uint32_t k0, uint32_t k1, uint32_t tid, float scale) {
-  const uint64_t n = (uint64_t)E * d;
-  const int KT = d / 64;
+// Inverse of tiled_index: the (row, column) of element j of the operand tiles
+// of a [rows][cols] matrix.
+__device__ __forceinline__ void tiled_coords(int rows, int cols, uint64_t j, int *r, int *c) {
+  const int b = (int)(j / ((uint64_t)128 * cols));
+  const int rows_b = min(128, rows - 128 * b);
+  const uint64_t within = j - (uint64_t)b * 128 * cols;
+  const int kt = (int)(within / ((uint64_t)rows_b * 64));
+  const int p = (int)(within - (uint64_t)kt * rows_b * 64);
+  const int rr = p >> 6;
+  *r = 128 * b + rr;
+  *c = kt * 64 + ((((p >> 3) & 7) ^ (rr & 7)) << 3) + (p & 7);
+}
+
+// A weight matrix [rows][cols] stored as operand tiles whose logical rows come
+// from up to three generated tensors: rows [0, r1) of tensor tid0, [r1, r2)
+// of tid1, [r2, rows) of tid2 (each row-major with `cols` columns).
+__global__ void fill_tiled_kernel(bf16 *dst, int rows, int cols, int r1, int r2, uint32_t tid0, uint32_t tid1,
+                                  uint32_t tid2, uint32_t k0, uint32_t k1, float scale) {
+  const uint64_t n = (uint64_t)rows * cols;
   for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
        j += (uint64_t)gridDim.x * blockDim.x) {
-    const int mt = (int)(j / ((uint64_t)128 * d));
-    const int rows = min(128, E - 128 * mt);
-    const uint64_t in_blk = j - (uint64_t)mt * 128 * d;  // within the block: [KT][rows][64]
-    const int kt = (int)(in_blk / ((uint64_t)rows * 64));
-    const int p = (int)(in_blk - (uint64_t)kt * rows * 64);
-    const int r = p >> 6;
-    const int c = kt * 64 + ((((p >> 3) & 7) ^ (r & 7)) << 3) + (p & 7);
-    dst[j] = weight_element((uint64_t)(128 * mt + r) * d + c, tid, k0, k1, scale);
+    int r, c;
+    tiled_coords(rows, cols, j, &r, &c);
+    const uint32_t tid = r < r1 ? tid0 : r < r2 ? tid1 : tid2;
+    const int r0 = r < r1 ? 0 : r < r2 ? r1 : r2;
+    dst[j] = weight_element((uint64_t)(r - r0) * cols + c, tid, k0, k1, scale);
   }
 }
 
@@ -150,7 +161,7 @@ __global__ void embed_kernel(float *h, const bf16 *table, const int *ids, int d)
 // registers (d <= 4096; longer rows are read twice).
 constexpr int kNormThreads = 128, kNormVec = 8;
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *out_lo, const float *h,
-                                                               const float *g, int d, float eps) {
+                                                               const float *g, int d, float eps, int tiled_rows) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x, d4 = d >> 2;
@@ -192,8 +203,13 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *
     const float4 gg = g4[c];
     const float y0 = a.x * inv * gg.x, y1 = a.y * inv * gg.y, y2 = a.z * inv * gg.z, y3 = a.w * inv * gg.w;
     const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
-    o2[2 * c] = h01;
-    o2[2 * c + 1] = h23;
+    if (tiled_rows > 0) {  // a tensor-core operand: operand tiles
+      *(uint2 *)(out + tiled_index(tiled_rows, d, t, 4 * c)) =
+          make_uint2(*(const uint32_t *)&h01, *(const uint32_t *)&h23);
+    } else {
+      o2[2 * c] = h01;
+      o2[2 * c + 1] = h23;
+    }
     if (l2) {
       l2[2 * c] = __floats2bfloat162_rn(y0 - __low2float(h01), y1 - __high2float(h01));
       l2[2 * c + 1] = __floats2bfloat162_rn(y2 - __low2float(h23), y3 - __high2float(h23));
@@ -247,7 +263,7 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
 constexpr int kCombNormVec = 4;
 __global__ void __launch_bounds__(256) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
                                                            const int *slot_row, int k, int d4,
-                                                           const float *gain, float eps, bf16 *xn) {
+                                                           const float *gain, float eps, bf16 *x_tiles, int T) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -294,14 +310,14 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(float4 *h, const floa
   for (int w = 0; w < 8; ++w) tot += red[w];
   const float inv = rsqrtf(tot / (4 * d4) + eps);
   const float4 *g4 = (const float4 *)gain;
-  __nv_bfloat162 *o2 = (__nv_bfloat162 *)(xn + (size_t)t * 4 * d4);
 #pragma unroll
   for (int u = 0; u < kCombNormVec; ++u) {
     const int c = threadIdx.x + 256 * u;
-    if (c < d4) {
+    if (c < d4) {  // the next layer's QKV operand, in operand tiles
       const float4 gg = g4[c];
-      o2[2 * c] = __floats2bfloat162_rn(hv[u].x * inv * gg.x, hv[u].y * inv * gg.y);
-      o2[2 * c + 1] = __floats2bfloat162_rn(hv[u].z * inv * gg.z, hv[u].w * inv * gg.w);
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(hv[u].x * inv * gg.x, hv[u].y * inv * gg.y);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(hv[u].z * inv * gg.z, hv[u].w * inv * gg.w);
+      *(uint2 *)(x_tiles + tiled_index(T, 4 * d4, t, 4 * c)) = make_uint2(*(uint32_t *)&p0, *(uint32_t *)&p1);
     }
   }
 }
@@ -357,13 +373,20 @@ cudaError_t fill_weights(bf16 *dst, uint64_t n, uint64_t seed, uint32_t tid, uin
   return cudaGetLastError();
 }
 
+cudaError_t fill_tiled_weights(bf16 *dst, int rows, int cols, int r1, int r2, uint32_t tid0, uint32_t tid1,
+                               uint32_t tid2, uint64_t seed, float std_dev, cudaStream_t st) {
+  const uint64_t n = (uint64_t)rows * cols;
+  if (n == 0) return cudaSuccess;
+  if (cols % 64) return cudaErrorInvalidValue;
+  fill_tiled_kernel<<<grid_for(n, 256), 256, 0, st>>>(dst, rows, cols, r1, r2, tid0, tid1, tid2, (uint32_t)seed,
+                                                      (uint32_t)(seed >> 32), weight_scale(std_dev));
+  return cudaGetLastError();
+}
+
 cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F, int layer,
                              uint64_t seed, float std_dev, cudaStream_t st) {
   const uint32_t base = 100u + 16u * (uint32_t)layer;
-  fill_router_kernel<<<grid_for((uint64_t)E * d, 256), 256, 0, st>>>(wr, E, d, (uint32_t)seed,
-                                                                       (uint32_t)(seed >> 32), base + 4,
-                                                                       weight_scale(std_dev));
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = fill_tiled_weights(wr, E, d, E, E, base + 4, base + 4, base + 4, seed, std_dev, st);
   if (e != cudaSuccess) return e;
   const uint64_t n = (uint64_t)E * 2 * F * d;
   fill_gate_up_kernel<<<grid_for(n, 256), 256, 0, st>>>(wgu, E, F, d, (uint32_t)seed,
@@ -398,10 +421,11 @@ cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d
 }
 
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
-                         cudaStream_t st, bf16 *out_lo) {
+                         cudaStream_t st, bf16 *out_lo, bool tiled) {
   if (T == 0) return cudaSuccess;
-  if (d % 4) return cudaErrorInvalidValue;
-  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, out, out_lo, h, gain, d, eps);
+  if (d % 4 || (tiled && (d % 64 || out_lo))) return cudaErrorInvalidValue;
+  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, out, out_lo, h, gain, d, eps,
+                    tiled ? T : 0);
 }
 
 
@@ -421,12 +445,12 @@ cudaError_t moe_combine(float *h, const float *y, const float *gates, const int 
 }
 
 cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const int *slot_row,
-                             int T, int k, int d, const float *gain, float eps, bf16 *xn,
+                             int T, int k, int d, const float *gain, float eps, bf16 *x_tiles,
                              cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  if (k > 16 || d % 4 || d > 4 * 256 * kCombNormVec) return cudaErrorInvalidValue;
+  if (k > 16 || d % 64 || d > 4 * 256 * kCombNormVec) return cudaErrorInvalidValue;
   return launch_pdl(combine_norm_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const float4 *)y, gates,
-                    slot_row, k, d / 4, gain, eps, xn);
+                    slot_row, k, d / 4, gain, eps, x_tiles, T);
 }
 
 

@@ -194,8 +194,9 @@ int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t
 /* Device pointer and size of a weight tensor.  which: DG_W_* below; layer is
  * ignored for the embedding, LM head and final norm.  Physical layouts:
  *   EMBED, LM_HEAD   [V][d]
- *   WQKV             [(Hq + 2 Hkv) * hd][d]   rows: W_q, then W_k, then W_v
- *   WO               [d][Hq * hd]
+ *   WQKV             operand tiles of         rows: W_q, then W_k, then W_v
+ *                    [(Hq + 2 Hkv) * hd][d]
+ *   WO               operand tiles of [d][Hq * hd]
  *   ROUTER           128-expert blocks of     block b: experts 128 b .. (rows =
  *                    [d/64] tiles             min(128, E - 128 b)); tile (b, j):
  *                                             those rows, columns 64 j .. 64 j + 63
@@ -205,8 +206,9 @@ int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t
  *   W_DOWN           [E][d/128][F/64] tiles   tile (e, b, j): rows 128 b ..
  *                                             128 b + 127 of W_down,e; columns
  *                                             64 j .. 64 j + 63
- *   A tile is 128 rows (fewer in the last ROUTER block) x 64 bf16 columns,
- *   row-major with 128-byte rows
+ *   Operand tiles of a [rows][cols] matrix: 128-row blocks (the last one
+ *   rows % 128 when that is not 0), each cols / 64 tiles of (block rows) x 64
+ *   bf16 columns, contiguous per tile and row-major with 128-byte rows
  *   in which the 16-byte chunk c of row r sits at chunk position c ^ (r % 8)
  *   (the tensor core's 128-byte-swizzled operand order, so that one bulk
  *   copy stages a tile).

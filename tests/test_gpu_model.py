@@ -7,6 +7,8 @@ early divergence cannot cascade.  Argmax / Gumbel winners may differ only
 where the oracle's top-2 gap is below 1e-2; the commit rule applied to the
 GPU's per-position outputs must reproduce the GPU's new state bit for bit.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -198,4 +200,38 @@ def test_profile_counts_launches():
     prof = dgp.dg_profile_read(m)
     assert prof["expert_ffn"][1] == 2 and prof["lm_head"][1] == 1
     assert all(ms >= 0 for ms, _ in prof.values()) and prof["expert_ffn"][0] > 0
+    m.close()
+
+
+def untile_matrix(phys, rows, cols):
+    """Operand tiles of a [rows][cols] matrix (128-row blocks, the last one
+    partial; per block the cols/64 tiles of (block rows) x 64, chunk c of row r
+    at position c ^ (r % 8)) back to row-major [rows][cols]."""
+    out = np.zeros((rows, cols), np.float32)
+    off = 0
+    for b0 in range(0, rows, 128):
+        n = min(128, rows - b0)
+        for j in range(cols // 64):
+            t = phys[off: off + n * 64].reshape(n, 8, 8)
+            pos = np.arange(8)[None, :] ^ (np.arange(n)[:, None] % 8)
+            out[b0:b0 + n, 64 * j:64 * j + 64] = np.take_along_axis(t, pos[..., None], axis=1).reshape(n, 64)
+            off += n * 64
+    return out
+
+
+def test_projection_weights_are_operand_tiles_of_the_logical_matrices(oracle_weights):
+    m = new_model()
+    cfg = om.TINY
+    d, qd, kd = cfg.d_model, cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    for which, rows, cols, ref in [
+            (dgp.DG_W_WQKV, qd + 2 * kd, d, lambda W: np.vstack([W["wq"], W["wk"], W["wv"]])),
+            (dgp.DG_W_WO, d, qd, lambda W: W["wo"])]:
+        ptr, nbytes = dgp.dg_get_weight(m, which, 1)
+        assert nbytes == rows * cols * 2
+        host = np.zeros(rows * cols, np.uint16)
+        torch.cuda.synchronize()  # the primary context is current on this thread
+        drv = ctypes.CDLL("libcuda.so.1")
+        assert drv.cuMemcpyDtoH_v2(ctypes.c_void_p(host.ctypes.data), ctypes.c_uint64(ptr), ctypes.c_size_t(nbytes)) == 0
+        phys = bits_to_f32(host)
+        assert np.array_equal(untile_matrix(phys, rows, cols), ref(oracle_weights.layers[1]))
     m.close()
