@@ -5,15 +5,25 @@
 // of the decoder.  The LM head has its own persistent kernel built from the
 // same pieces (kernels_lmhead.cu).
 //
+// Both operands are stored as operand tiles (tiled_index in common.cuh): 128
+// rows x 64 columns per tile, already in the 128-byte swizzled order of a
+// K-major shared-memory operand, so one contiguous bulk copy stages a tile.
 // Roles inside a GEMM CTA (128 threads):
-//   warp 0, one thread  -- TMA producer: 128-row A boxes and 64-row B boxes,
-//                          64 K-elements each, 128-byte swizzled, into a
-//                          4-stage shared-memory ring;
+//   warp 0, one thread  -- producer: per 64-wide K step the weight tile (A,
+//                          <= 16 KB) and the activation tiles of up to 256
+//                          token rows (B) into a 4-stage shared-memory ring;
+//                          the first weight tile is requested before the
+//                          wait on the previous kernel;
 //   warp 1, one thread  -- allocates the TMEM accumulator and issues
 //                          tcgen05.mma (M = 128, N <= 256, K = 16) per stage,
 //                          releasing each stage with tcgen05.commit;
 //   warps 0-3           -- read the accumulator out of TMEM (each warp its
 //                          32-lane quarter) and run the fused epilogue.
+// Split-K: the SPLIT CTAs of a cluster own 1/SPLIT of K each; after the main
+// loop every CTA stages its fp32 partial tile slice by slice, pushes slice j
+// to CTA j with a bulk shared-to-shared copy, and CTA j adds the SPLIT
+// partials of its slice in rank order (deterministic) and runs the epilogue
+// on that slice.
 // Every mbarrier wait is bounded; a wait that gives up records an error word
 // and lets the CTA finish, so a fault can never hang the GPU.
 #pragma once

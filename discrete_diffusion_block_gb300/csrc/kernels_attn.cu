@@ -14,22 +14,27 @@
 // operand order (16-byte chunk c of slot s at chunk position c ^ (s % 8)), so
 // a 64- or 128-key K or V operand tile is one contiguous bulk copy.
 //
-// The kernel is a tcgen05 tensor-core kernel with two passes over the
-// block's key range:
-//   pass 1  S = Q K^T per 128-key tile (TMEM), running row max m;
-//   pass 2  S again, P = 2^(S*scale - m) as bf16 into shared memory, row sum
-//           l in fp32, O += P V (TMEM) -- with m final, O is never rescaled.
-// The second QK^T costs a third more tensor work and saves the read-modify-
-// write of the accumulator that a one-pass online softmax needs.  Roles:
-// warp 0 streams Q once and the K (and V) tiles of each pass through a
-// two-slot ring (Q with TMA through a 4-D map that packs the G heads of a
-// token as consecutive rows; K and V with bulk copies of their pages); warp 1
-// issues the MMAs (V is the N-contiguous "MN-major" B operand of P V); warps
-// 2-5 hold one row each and do the softmax on the accumulator rows they read
-// from TMEM.  With the key range split over several blocks, the blocks of
-// one query tile form a cluster: each writes its unnormalised output and
-// softmax state, and after a cluster barrier each block merges a slice of
-// the tile's rows (weights 2^(m_s - m*)).
+// The kernel is a tcgen05 tensor-core kernel with one pass over the block's
+// key range and an online softmax: per 128-key tile, S = Q K^T (TMEM), the
+// tile's raw-score maximum, P = 2^(S*scale - m) as bf16 into shared memory,
+// row sum l in fp32, O += P V (TMEM).  The running maximum m is raised lazily:
+// only a row whose maximum grows by more than 2^8 moves to the new reference
+// and rescales its accumulator row in TMEM (read, scale, write back) after the
+// previous tile's P V has landed; below that P stays <= 2^8 and the final
+// O / l does not depend on which reference was used.  Roles (224 threads):
+// warp 0 streams Q once (TMA through a 4-D map that packs the G heads of a
+// token as consecutive rows) and the K tiles through a two-slot ring; warp 6
+// streams the V tiles through their own two-slot ring (both as bulk copies
+// of the pool's pre-swizzled pages, from a page list resolved before the
+// dependency wait); warp 1 issues the MMAs, S of tile i + 1 before P V of
+// tile i, with two S accumulators and two P tiles so the softmax of one tile
+// overlaps the tensor work of the next (V is the N-contiguous "MN-major" B
+// operand of P V); warps 2-5 hold one query row per thread.  With the key
+// range split over several blocks, the blocks of one query tile form a
+// cluster: each stages its unnormalised output rows and softmax state (m, l)
+// in shared memory, pushes to every peer the slice of rows that peer owns
+// (bulk shared-to-shared copies), and each block merges its slice (weights
+// 2^(m_s - m*)) and writes it; no device scratch is used.
 #include <cuda.h>
 
 #include <cudaTypedefs.h>

@@ -49,24 +49,6 @@ __device__ __forceinline__ void tile_coords(uint64_t j, int KT, uint64_t *blk, i
   *c = *kt * 64 + ((((p >> 3) & 7) ^ (*r & 7)) << 3) + (p & 7);
 }
 
-// W_gate / W_up (logical [E][F][d]) as tiles of 128-row blocks that hold 64
-// gate rows then the matching 64 up rows (block fb of expert e: features
-// 64 fb .. 64 fb + 63), K = d.
-__global__ void fill_gate_up_kernel(bf16 *dst, int E, int F, int d, uint32_t k0, uint32_t k1,
-                                    uint32_t tid_gate, uint32_t tid_up, float scale) {
-  const uint64_t n = (uint64_t)E * 2 * F * d;
-  const int KT = d / 64, mA = F / 64;
-  for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
-       j += (uint64_t)gridDim.x * blockDim.x) {
-    uint64_t blk;
-    int kt, r, c;
-    tile_coords(j, KT, &blk, &kt, &r, &c);
-    const int fb = (int)(blk % mA), e = (int)(blk / mA);
-    const uint64_t logical = ((uint64_t)e * F + fb * 64 + (r & 63)) * d + c;
-    dst[j] = weight_element(logical, r >= 64 ? tid_up : tid_gate, k0, k1, scale);
-  }
-}
-
 // Inverse of tiled_index: the (row, column) of element j of the operand tiles
 // of a [rows][cols] matrix.
 __device__ __forceinline__ void tiled_coords(int rows, int cols, uint64_t j, int *r, int *c) {
@@ -78,6 +60,21 @@ __device__ __forceinline__ void tiled_coords(int rows, int cols, uint64_t j, int
   const int rr = p >> 6;
   *r = 128 * b + rr;
   *c = kt * 64 + ((((p >> 3) & 7) ^ (rr & 7)) << 3) + (p & 7);
+}
+
+// W_gate and W_up (logical [E][F][d] each): per expert, the operand tiles of
+// W_gate,e ([F][d], tiled_index) followed by the operand tiles of W_up,e.
+__global__ void fill_gate_up_kernel(bf16 *dst, int E, int F, int d, uint32_t k0, uint32_t k1,
+                                    uint32_t tid_gate, uint32_t tid_up, float scale) {
+  const uint64_t n = (uint64_t)E * 2 * F * d, per = (uint64_t)F * d;
+  for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n;
+       j += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t mat = j / per;  // 2 e (gate) or 2 e + 1 (up)
+    int r, c;
+    tiled_coords(F, d, j - mat * per, &r, &c);
+    const uint64_t logical = ((mat >> 1) * F + r) * d + c;
+    dst[j] = weight_element(logical, (mat & 1) ? tid_up : tid_gate, k0, k1, scale);
+  }
 }
 
 // A weight matrix [rows][cols] stored as operand tiles whose logical rows come

@@ -4,35 +4,42 @@
 //   act_e = SiLU(X_e Wg_e^T) * (X_e Wu_e^T)        (phase A, "gate/up")
 //   y_e   = act_e Wd_e^T                           (phase B, "down")
 //
-// Units.  A work item is (expert, up to 128 of its rows).  Phase A units are
-// (item, 128-row block of the interleaved gate/up weights) -- 64 gate rows
-// and the matching 64 up rows, so SwiGLU is local to the tile; phase B units
-// are (item, 128-row block of W_down).  All units sit in one list, phase A
-// first; CTAs (one per SM) take the next unit from a global counter, so the
-// small phase B units fill the tail of phase A and no SM idles while another
-// still has a long queue.  A phase B unit needs the whole act row block of its
-// item: its producer waits (bounded) until the item's phase A units have all
-// published their outputs (per-item counter, release/acquire, then a proxy
-// fence before the TMA reads them).
+// Units.  A work item is (expert, up to 128 of its rows).  A phase A unit is
+// (item, 128 features): two MMAs per k-step, the gate rows into one TMEM
+// accumulator and the up rows of the same features into a second one, both
+// against the one copy of the item's rows staged for that k-step -- so a
+// thread that owns a feature's TMEM lane holds its gate and up projections
+// and SwiGLU needs no exchange.  A phase B unit is (item, 256 rows of
+// W_down), again two accumulators sharing one staged act tile.  Sharing the
+// B operand between two weight blocks halves the re-reads of the item's rows,
+// which are as many bytes as the weights themselves.  All units sit in one
+// list, phase A first; CTAs (one per SM) take the next unit from a global
+// counter.  A phase B unit needs the whole act row block of its item: its
+// producer first requests the unit's leading weight tiles, then waits
+// (bounded) until the item's phase A units have all published their outputs
+// (per-item counter, release/acquire, then a proxy fence before the copies
+// read them).
 //
 // Operands.  Expert weights and the item rows (gathered by moe_scatter, and
 // the SwiGLU output written here by phase A) are stored as 16 KB tiles of 128
 // rows x 64 columns already in the tensor core's swizzled shared-memory order,
-// so each k-step of a unit stages its operands with two contiguous bulk
-// copies (the weight tile, the item's valid rows) instead of row-by-row
-// tensor copies.
+// so each k-step of a unit stages its operands with three contiguous bulk
+// copies (two weight tiles, the item's valid rows).
 //
-// Roles (192 threads):
-//   warp 4, one thread  -- takes units, hands them to the other roles through
-//                          a 4-deep shared-memory queue, and streams A (one
-//                          weight tile) and B (the item's rows) per k-step
-//                          into a 6-stage ring;
-//   warp 5, one thread  -- owns 2 x 128 TMEM columns and issues tcgen05.mma
+// Roles (320 threads):
+//   warp 8, one thread  -- takes units, hands them to the other roles through
+//                          a 4-deep shared-memory queue, and streams the
+//                          operands per k-step into a 4-stage ring (48 KB a
+//                          stage);
+//   warp 9, one thread  -- owns all 512 TMEM columns and issues tcgen05.mma
 //                          (M = 128, N = rows rounded up to 16), unit n into
-//                          accumulator n & 1;
-//   warps 0-3           -- drain accumulator n & 1 into an fp32 tile and run
-//                          the SwiGLU (A) or store (B) epilogue while the
-//                          tensor core already works on the next unit.
+//                          accumulator pair n & 1;
+//   warps 0-7           -- epilogue straight from TMEM: warp w reads lane
+//                          quarter w % 4 and token columns 64 (w / 4) ..
+//                          64 (w / 4) + 63 of the pair, computes SwiGLU and
+//                          writes the act tile (A) or writes y rows (B) with
+//                          coalesced stores, while the tensor core already
+//                          works on the next unit.
 // Every wait is bounded; a wait that gives up records an error word and makes
 // the CTA's later waits return at once.
 #include <cuda.h>
@@ -44,39 +51,43 @@ namespace dg {
 
 namespace {
 
-constexpr int kFfnStages = 6;
-constexpr int kFfnThreads = 192;
+constexpr int kFfnStages = 4;
+constexpr int kFfnEpiWarps = 8;
+constexpr int kFfnEpiThreads = 32 * kFfnEpiWarps;
+constexpr int kFfnThreads = kFfnEpiThreads + 64;
+constexpr int kFfnProducerWarp = kFfnEpiWarps, kFfnMmaWarp = kFfnEpiWarps + 1;
 constexpr int kFfnBN = kExpertTileRows;  // rows per item = MMA N upper bound
 constexpr int kFfnQueue = 4;
-constexpr uint32_t kFfnABytes = 128 * 128;
+constexpr uint32_t kFfnATileBytes = 128 * 128;  // one weight tile, up to 128 rows x 64
 constexpr uint32_t kFfnBBytes = kFfnBN * 128;
-constexpr uint32_t kFfnStageBytes = kFfnABytes + kFfnBBytes;
-constexpr int kFfnEpiCols = 64;            // accumulator columns (rows of the item) per epilogue pass
-constexpr int kFfnLdc = kFfnEpiCols + 1;
-
-struct FfnSmem {
-  static constexpr size_t ring = (size_t)kFfnStages * kFfnStageBytes;
-  static constexpr size_t tile = ring;                                   // fp32 [128][kFfnLdc]: 64 columns at a time
-  static constexpr size_t queue = tile + (size_t)128 * kFfnLdc * 4;      // UnitInfo [kFfnQueue]
-  static constexpr size_t bars = (queue + kFfnQueue * 32 + 15) & ~(size_t)15;
-  // full[S], empty[S], acc_full[2], acc_empty[2], q_full[Q], q_empty[Q]; TMEM address; abort flag
-  static constexpr size_t bytes = bars + (2 * kFfnStages + 4 + 2 * kFfnQueue) * 8 + 16 + 1024;
-};
+constexpr uint32_t kFfnStageBytes = 2 * kFfnATileBytes + kFfnBBytes;
+constexpr uint32_t kFfnPairCols = 2 * kFfnBN;  // TMEM columns of one accumulator pair
 
 struct UnitInfo {
   int u;        // unit index, -1 = no more units
   int phase;    // 0: gate/up, 1: down
-  int item, mt, b_row, n_valid, e, pad;
+  int item, mt, b_row, n_valid, e;
+  int a_rows;   // valid rows of each weight tile (phase A: features in the block)
+  int n_acc;    // weight blocks (accumulators) of the unit: 2, or 1 for an odd last block of W_down
+  int pad[3];
+};
+
+struct FfnSmem {
+  static constexpr size_t ring = (size_t)kFfnStages * kFfnStageBytes;
+  static constexpr size_t queue = ring;  // UnitInfo [kFfnQueue]
+  static constexpr size_t bars = (queue + kFfnQueue * sizeof(UnitInfo) + 15) & ~(size_t)15;
+  // full[S], empty[S], acc_full[2], acc_empty[2], q_full[Q], q_empty[Q]; TMEM address; abort flag
+  static constexpr size_t bytes = bars + (2 * kFfnStages + 4 + 2 * kFfnQueue) * 8 + 16 + 1024;
 };
 
 // Operands are stored as 16 KB tiles (128 rows x 64 columns, in the
-// tensor core's 128-byte swizzled shared-memory order), [row block][k-tile];
-// one contiguous bulk copy moves a weight tile, one moves the valid rows of
-// an item's tile.
+// tensor core's 128-byte swizzled shared-memory order); one contiguous bulk
+// copy moves a weight tile, one moves the valid rows of an item's tile.
 struct FfnArgs {
   const int *work, *n_work, *offs;
-  const bf16 *wgu, *wd;  // [E][2F/128][d/64] and [E][d/128][F/64] tiles
-  const bf16 *x;         // [item][d/64] tiles: the item's token rows
+  const bf16 *wgu;  // per expert: operand tiles of W_gate [F][d], then of W_up [F][d]
+  const bf16 *wd;   // per expert: operand tiles of W_down [d][F]
+  const bf16 *x;    // [item][d/64] tiles: the item's token rows
   int *done;   // [max_work] phase A units finished per item
   int *next;   // unit counter
   int E, d, F;
@@ -100,7 +111,17 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
   return v;
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// Named barrier 1 over the epilogue warps; epi_any also ORs a predicate over them.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kFfnEpiThreads) : "memory"); }
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kFfnEpiThreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(b)) : "memory");
@@ -108,11 +129,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
 
 __device__ __forceinline__ float swiglu_f(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *(uint32_t *)&v;
+}
+
 __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   using S = FfnSmem;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  float *tile = (float *)(base + S::tile);
   UnitInfo *queue = (UnitInfo *)(base + S::queue);
   uint64_t *full = (uint64_t *)(base + S::bars);
   uint64_t *empty = full + kFfnStages;
@@ -132,19 +157,19 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(acc_full + b, 1);
-      tc::mbar_init(acc_empty + b, 4);  // one arrival per epilogue warp
+      tc::mbar_init(acc_empty + b, kFfnEpiWarps);  // one arrival per epilogue warp
     }
     for (int q = 0; q < kFfnQueue; ++q) {
       tc::mbar_init(q_full + q, 1);
-      tc::mbar_init(q_empty + q, 2);  // the MMA thread and the epilogue
+      tc::mbar_init(q_empty + q, 1 + kFfnEpiWarps);  // the MMA thread and every epilogue warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == kFfnMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      tc::smem_u32(tmem_slot)),
-                 "r"((uint32_t)(2 * kFfnBN)));
+                 "r"(2u * kFfnPairCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
   __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
@@ -157,13 +182,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;
 
   const int n_items = *g.n_work;
-  const int mA = (2 * g.F) / 128, mB = g.d / 128;
+  const int mA = (g.F + 127) / 128, mB = (g.d + 255) / 256;
   const int nA = n_items * mA, n_units = nA + n_items * mB;
   const int KTA = g.d / tc::kBK, KTB = g.F / tc::kBK;
-  auto a_tile = [&](int s) { return base + (size_t)s * kFfnStageBytes; };
-  auto b_tile = [&](int s) { return base + (size_t)s * kFfnStageBytes + kFfnABytes; };
+  auto a_tile = [&](int s, int j) { return base + (size_t)s * kFfnStageBytes + (size_t)j * kFfnATileBytes; };
+  auto b_tile = [&](int s) { return base + (size_t)s * kFfnStageBytes + 2 * kFfnATileBytes; };
 
-  if (warp == 4) {
+  if (warp == kFfnProducerWarp) {
     if (lane == 0) {
       int it = 0;
       for (int n = 0;; ++n) {
@@ -182,16 +207,41 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           inf.b_row = e0 + n0;
           inf.n_valid = min(kFfnBN, g.offs[e + 1] - e0 - n0);
           inf.e = e;
+          inf.a_rows = inf.phase ? 128 : min(128, g.F - 128 * inf.mt);
+          inf.n_acc = inf.phase ? min(2, g.d / 128 - 2 * inf.mt) : 2;
         }
         queue[q] = inf;
         mbar_arrive(q_full + q);  // release: the entry is visible to the waiting roles
         if (inf.u < 0) break;
         const int KT = inf.phase ? KTB : KTA;
-        const bf16 *asrc = inf.phase ? g.wd + (size_t)(inf.e * mB + inf.mt) * KTB * kTileElems
-                                     : g.wgu + (size_t)(inf.e * mA + inf.mt) * KTA * kTileElems;
+        // weight tile kt of block j: a0 + j * a_blk + kt * a_kt
+        const bf16 *a0;
+        size_t a_blk;
+        if (inf.phase) {
+          a0 = g.wd + (size_t)inf.e * g.d * g.F + (size_t)(2 * inf.mt) * 128 * g.F;
+          a_blk = (size_t)128 * g.F;
+        } else {
+          a0 = g.wgu + (size_t)inf.e * 2 * g.F * g.d + (size_t)128 * g.d * inf.mt;
+          a_blk = (size_t)g.F * g.d;
+        }
+        const size_t a_kt = (size_t)inf.a_rows * 64;
+        const uint32_t a_bytes = (uint32_t)inf.a_rows * 128;
         const bf16 *bsrc = (inf.phase ? g.act : g.x) + (size_t)inf.item * KT * kTileElems;
         const uint32_t b_bytes = (uint32_t)((inf.n_valid + 7) & ~7) * 128;  // the item's valid rows
-        const uint32_t tx = kFfnABytes + b_bytes;
+        const uint32_t tx = (uint32_t)inf.n_acc * a_bytes + b_bytes;
+        auto load_a = [&](int s, int kt) {
+          for (int j = 0; j < inf.n_acc; ++j)
+            bulk_load(a_tile(s, j), a0 + j * a_blk + kt * a_kt, a_bytes, full + s);
+        };
+        // Phase B: the first stages' weight tiles go out before the wait on act.
+        const int pre = inf.phase ? min(KT, kFfnStages) : 0;
+        for (int kt = 0; kt < pre; ++kt) {
+          const int i = it + kt, s = i % kFfnStages, r = i / kFfnStages;
+          if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 23, abort);
+          if (*abort) break;
+          tc::mbar_expect_tx(full + s, tx);
+          load_a(s, kt);
+        }
         if (inf.phase) {
           // the item's act rows: every phase A unit of it must have published
           const long long t0 = clock64();
@@ -205,25 +255,35 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           }
           asm volatile("fence.proxy.async.global;\n" ::: "memory");
         }
-        for (int kt = 0; kt < KT; ++kt, ++it) {
-          const int s = it % kFfnStages, r = it / kFfnStages;
-          if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 23, abort);
-          if (*abort) break;
-          tc::mbar_expect_tx(full + s, tx);
-          bulk_load(a_tile(s), asrc + (size_t)kt * kTileElems, kFfnABytes, full + s);
+        int issued = it;  // stages whose copies went out (for the drain below)
+        for (int kt = 0; kt < KT; ++kt) {
+          const int i = it + kt, s = i % kFfnStages, r = i / kFfnStages;
+          if (kt >= pre) {
+            if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 23, abort);
+            if (*abort) break;
+            tc::mbar_expect_tx(full + s, tx);
+            load_a(s, kt);
+          } else if (*abort) {
+            break;
+          }
           bulk_load(b_tile(s), bsrc + (size_t)kt * kTileElems, b_bytes, full + s);
+          issued = i + 1;
         }
-        if (*abort) {  // drain the copies in flight (bounded), then hand over the end marker
-          for (int i = it - 1; i >= 0 && i >= it - kFfnStages; --i) {
+        if (*abort) {
+          // Drain: wait (bounded) for the copies in flight, including weight
+          // tiles requested ahead of the act wait, then hand over the end marker.
+          const int last = max(issued, it + pre);
+          for (int i = last - 1; i >= 0 && i >= last - kFfnStages; --i) {
             const long long t0 = clock64();
             while (!tc::mbar_try_wait(full + i % kFfnStages, (i / kFfnStages) & 1) &&
                    clock64() - t0 < tc::kWaitCycles) {
             }
           }
         }
+        it += KT;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kFfnMmaWarp) {
     if (lane == 0) {
       int it = 0;
       for (int n = 0;; ++n) {
@@ -234,18 +294,21 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         const int buf = n & 1;
         if (n >= 2) tc::mbar_wait(acc_empty + buf, ((n >> 1) - 1) & 1, g.err, 25, abort);
         tc::fence_after();
-        const uint32_t d_tmem = tmem + buf * kFfnBN;
+        const uint32_t d0 = tmem + buf * kFfnPairCols, d1 = d0 + kFfnBN;
         const uint32_t idesc = tc::idesc_bf16(128, max(16, (inf.n_valid + 15) & ~15));
         const int KT = inf.phase ? KTB : KTA;
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int s = it % kFfnStages, r = it / kFfnStages;
           tc::mbar_wait(full + s, r & 1, g.err, 26, abort);
           tc::fence_after();
-          const uint64_t adesc = tc::sw128_desc(tc::smem_u32(a_tile(s)));
+          const uint64_t adesc0 = tc::sw128_desc(tc::smem_u32(a_tile(s, 0)));
+          const uint64_t adesc1 = tc::sw128_desc(tc::smem_u32(a_tile(s, 1)));
           const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(b_tile(s)));
 #pragma unroll
-          for (int kk = 0; kk < tc::kBK / 16; ++kk)
-            tc::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+          for (int kk = 0; kk < tc::kBK / 16; ++kk) {
+            tc::mma_bf16(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+            if (inf.n_acc > 1) tc::mma_bf16(d1, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+          }
           tc::mma_commit(empty + s);
         }
         tc::mma_commit(acc_full + buf);
@@ -253,95 +316,85 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
       }
     }
   } else {
-    // ---- epilogue: warps 0-3, thread = accumulator row ------------------------
-    const int row = threadIdx.x;
+    // ---- epilogue: warps 0-7; lane = accumulator row, 64 token columns per warp
+    const int q4 = warp & 3, half = warp >> 2;
+    const int lrow = 32 * q4 + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     for (int n = 0;; ++n) {
       const int q = n % kFfnQueue;
       tc::mbar_wait(q_full + q, (n / kFfnQueue) & 1, g.err, 27, abort);
       const UnitInfo inf = queue[q];
-      if (inf.u < 0 || *abort) break;
+      // every epilogue warp takes the same decision (the named barriers below)
+      if (epi_any(inf.u < 0 || *abort)) break;
       const int buf = n & 1;
       tc::mbar_wait(acc_full + buf, (n >> 1) & 1, g.err, 28, abort);
       tc::fence_after();
-      const uint32_t trow = tmem + buf * kFfnBN + ((uint32_t)(warp * 32) << 16);
-      // 64 accumulator columns (item rows) per pass through the fp32 tile
-      for (int h0 = 0; h0 < inf.n_valid; h0 += kFfnEpiCols) {
-        const int nh = min(kFfnEpiCols, inf.n_valid - h0);
-        const int nchunks = (nh + 31) >> 5;
+      const uint32_t tp = tmem + buf * kFfnPairCols + lane_off;
+      if (inf.phase == 0) {
+        // SwiGLU of feature f = 128 mt + lrow for the warp's token columns;
+        // lanes 2i and 2i + 1 trade values so that each stores a bf16 pair
+        // (features f, f + 1) of one token row into the act tile.
+        const bool fok = lrow < inf.a_rows;
+        const int fb = 128 * inf.mt + (lrow & ~1), cc = fb & 63;
+        unsigned char *blk =
+            (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + (fb >> 6)) * kTileElems);
 #pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
-          uint32_t v[32];
-          tc::tmem_ld32(trow + h0 + 32 * c, v);
-          tc::tmem_ld_wait(v);
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * half + 32 * c;
+          if (col0 >= inf.n_valid) break;
+          uint32_t gv[32], uv[32];
+          tc::tmem_ld32(tp + col0, gv);
+          tc::tmem_ld32(tp + kFfnBN + col0, uv);
+          tc::tmem_ld_wait(gv);
+          tc::tmem_ld_wait(uv);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tile[row * kFfnLdc + 32 * c + j] = __uint_as_float(v[j]);
-        }
-        if (h0 + kFfnEpiCols >= inf.n_valid) {  // last pass: the accumulator is free for unit n + 2
-          tc::fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty + buf);
-        }
-        epi_sync();
-        if (inf.phase == 0) {
-          // SwiGLU: rows j and 64 + j hold the gate and up projections of
-          // feature 64 * mt + j; each lane writes two adjacent features of an
-          // item row into the act tile (item, k-tile mt) of the down GEMM.
-          const int j = 2 * lane;
-          unsigned char *blk = (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + inf.mt) * kTileElems);
-          for (int tb = warp; tb < nh; tb += 16) {
-            float g0[4], g1[4], u0[4], u1[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int t = min(tb + 4 * k, nh - 1);
-              g0[k] = tile[j * kFfnLdc + t];
-              g1[k] = tile[(j + 1) * kFfnLdc + t];
-              u0[k] = tile[(64 + j) * kFfnLdc + t];
-              u1[k] = tile[(65 + j) * kFfnLdc + t];
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int t = tb + 4 * k, r = h0 + t;
-              if (t < nh)
-                *(__nv_bfloat162 *)(blk + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2))) =
-                    __floats2bfloat162_rn(swiglu_f(g0[k], u0[k]), swiglu_f(g1[k], u1[k]));
-            }
-          }
-        } else {
-          // y[row][feature] = tile: lanes walk features, four tokens per step
-          float *dst = g.y + (size_t)(inf.b_row + h0) * g.d + inf.mt * 128;
-          for (int tb = warp; tb < nh; tb += 16) {
-            float v[4][4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-              for (int f4 = 0; f4 < 4; ++f4) v[k][f4] = tile[(32 * f4 + lane) * kFfnLdc + min(tb + 4 * k, nh - 1)];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int t = tb + 4 * k;
-              if (t < nh)
-#pragma unroll
-                for (int f4 = 0; f4 < 4; ++f4) dst[(size_t)t * g.d + 32 * f4 + lane] = v[k][f4];
-            }
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = swiglu_f(__uint_as_float(gv[2 * j]), __uint_as_float(uv[2 * j]));
+            const float a1 = swiglu_f(__uint_as_float(gv[2 * j + 1]), __uint_as_float(uv[2 * j + 1]));
+            const float recv = __shfl_xor_sync(0xffffffffu, (lane & 1) ? a0 : a1, 1);
+            const int t = col0 + 2 * j + (lane & 1);
+            const uint32_t w = (lane & 1) ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
+            if (fok && t < inf.n_valid)
+              *(uint32_t *)(blk + t * 128 + ((((cc >> 3) ^ (t & 7)) << 4) | ((cc & 7) << 1))) = w;
           }
         }
-        epi_sync();  // the tile is free for the next pass
+      } else {
+        // y[row][256 mt + 128 a + lrow] for the warp's token columns: for each
+        // token the warp stores 32 consecutive features (128 bytes).
+#pragma unroll 1
+        for (int a = 0; a < inf.n_acc; ++a) {
+          float *dst = g.y + (size_t)inf.b_row * g.d + 256 * inf.mt + 128 * a + lrow;
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            const int col0 = 64 * half + 32 * c;
+            if (col0 >= inf.n_valid) break;
+            uint32_t v[32];
+            tc::tmem_ld32(tp + a * kFfnBN + col0, v);
+            tc::tmem_ld_wait(v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < inf.n_valid) dst[(size_t)(col0 + j) * g.d] = __uint_as_float(v[j]);
+          }
+        }
       }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + buf);  // this warp's reads of the pair are done
       if (inf.phase == 0) {
         __threadfence();
         asm volatile("fence.proxy.async.global;\n" ::: "memory");
         epi_sync();
         if (threadIdx.x == 0) atomicAdd(g.done + inf.item, 1);  // publish after every thread's stores
       }
-      if (threadIdx.x == 0) mbar_arrive(q_empty + q);
+      if (lane == 0) mbar_arrive(q_empty + q);  // this warp is done with the queue entry
     }
   }
   __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kFfnMmaWarp) {
     tc::fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
-                 "r"((uint32_t)(2 * kFfnBN)));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(2u * kFfnPairCols));
   }
 }
 

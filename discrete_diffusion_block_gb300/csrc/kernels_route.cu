@@ -12,13 +12,16 @@
 //      slice of xn (bf16) to global memory and, 128-byte swizzled, to shared
 //      memory as the MMA B operand.  Without the norm, the B slice is loaded
 //      from xn with TMA.
-//   2. one thread streams the CTA's K-slice of W_r (128-expert x 64 boxes,
-//      issued before the wait on the previous kernel: weights never change)
-//      and one thread issues tcgen05.mma (M = 128 experts, N = 32 tokens) into
-//      a 32-column TMEM accumulator per 128 experts.
-//   3. the partial logits go to shared memory; after a cluster barrier CTA z
-//      adds the S partials of 32/S tokens in rank order (deterministic) and
-//      one warp per token selects the top k.
+//   2. one thread streams the CTA's K-slice of W_r (stored as operand tiles,
+//      one bulk copy per 128-expert x 64 tile; weights never change, so they
+//      are requested before the wait on the previous kernel) and four
+//      threads in four warps issue tcgen05.mma (M = 128 experts, N = 32
+//      tokens), each into its own 32-column TMEM accumulator per 128 experts
+//      over every fourth K step, so that short MMAs are issued in parallel.
+//   3. the four accumulators are summed into the CTA's partial logits; CTA
+//      z receives the partials of its 32/S tokens from every peer (bulk
+//      shared-to-shared copies), adds the S partials in rank order
+//      (deterministic), and one warp per token selects the top k.
 //   4. per-CTA expert counts are exchanged in the cluster: each pair gets its
 //      rank within the group, and the group's per-expert counts go to global
 //      memory.

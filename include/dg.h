@@ -200,9 +200,8 @@ int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t
  *   ROUTER           128-expert blocks of     block b: experts 128 b .. (rows =
  *                    [d/64] tiles             min(128, E - 128 b)); tile (b, j):
  *                                             those rows, columns 64 j .. 64 j + 63
- *   W_GATE_UP        [E][F/64][d/64] tiles    tile (e, b, j): rows 64 b .. 64 b + 63
- *                                             of W_gate,e then the same rows of
- *                                             W_up,e; columns 64 j .. 64 j + 63
+ *   W_GATE_UP        per expert e: operand    W_gate,e first, then W_up,e
+ *                    tiles of [F][d], twice
  *   W_DOWN           [E][d/128][F/64] tiles   tile (e, b, j): rows 128 b ..
  *                                             128 b + 127 of W_down,e; columns
  *                                             64 j .. 64 j + 63
@@ -314,7 +313,7 @@ int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
  * (device bf16 [T][d], already RMS-normalised),
  *   r = xn W_r^T; S = the top_k largest r (ties -> lower expert id);
  *   gates = softmax(r_S); y = sum_{e in S} gate_e W_down,e (silu(W_gate,e xn) * W_up,e xn)
- * Weights in the layouts of dg_get_weight (W_GATE_UP interleaved, W_DOWN).
+ * Weights in the layouts of dg_get_weight (W_GATE_UP, W_DOWN).
  * Outputs (device): y fp32 [T][d]; expert_ids int32 [T][top_k] (descending
  * router logit); gates fp32 [T][top_k].  workspace: dg_op_moe_workspace_bytes(). */
 size_t dg_op_moe_workspace_bytes(int32_t T, int32_t d, int32_t n_experts, int32_t top_k,

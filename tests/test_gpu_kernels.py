@@ -43,10 +43,10 @@ def untile(phys, lead, blocks, kt):
     return np.moveaxis(t, -3, -2).reshape(*lead, blocks * 128, kt * 64)
 
 
-def untile_router(phys, E, d):
-    """Router tiles (128-expert blocks, the last one partial; per block the
-    k-tiles [rows][64], chunk c of row r at position c ^ (r % 8)) back to
-    [E][d]."""
+def untile_blocks(phys, E, d):
+    """Operand tiles of an [E][d] matrix (128-row blocks, the last one
+    partial; per block the k-tiles [rows][64], chunk c of row r at position
+    c ^ (r % 8)) back to row-major [E][d]."""
     out = np.zeros((E, d), np.float32)
     off = 0
     for b0 in range(0, E, 128):
@@ -66,12 +66,15 @@ def test_moe_weight_layout_matches_logical_tensors():
     wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
     dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, L, 5, 0.02)
     base = 100 + 16 * L
-    assert np.array_equal(untile_router(bf16_to_f32(wr), E, d), ow.tensor(5, base + 4, (E, d), 0.02))
-    # gate/up: 128-row blocks of 64 gate rows then the same 64 up rows
-    gu = untile(bf16_to_f32(wgu), (E,), F // 64, d // 64).reshape(E, F // 64, 2, 64, d)
-    g = ow.tensor(5, base + 5, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
-    u = ow.tensor(5, base + 6, (E, F, d), 0.02).reshape(E, F // 64, 64, d)
-    assert np.array_equal(gu[:, :, 0], g) and np.array_equal(gu[:, :, 1], u)
+    assert np.array_equal(untile_blocks(bf16_to_f32(wr), E, d), ow.tensor(5, base + 4, (E, d), 0.02))
+    # gate/up: per expert the operand tiles of W_gate [F][d], then those of
+    # W_up (F = 192: a full 128-row block and a 64-row one)
+    phys = bf16_to_f32(wgu).reshape(E, 2, F * d)
+    g = ow.tensor(5, base + 5, (E, F, d), 0.02)
+    u = ow.tensor(5, base + 6, (E, F, d), 0.02)
+    for e in range(E):
+        assert np.array_equal(untile_blocks(phys[e, 0], F, d), g[e])
+        assert np.array_equal(untile_blocks(phys[e, 1], F, d), u[e])
     wdl = untile(bf16_to_f32(wd), (E,), d // 128, F // 64)
     assert np.array_equal(wdl, ow.tensor(5, base + 7, (E, d, F), 0.02))
 
@@ -82,7 +85,7 @@ def test_router_layout_with_a_partial_expert_block():
     wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
     wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
     dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, L, 9, 0.02)
-    assert np.array_equal(untile_router(bf16_to_f32(wr), E, d), ow.tensor(9, 100 + 16 * L + 4, (E, d), 0.02))
+    assert np.array_equal(untile_blocks(bf16_to_f32(wr), E, d), ow.tensor(9, 100 + 16 * L + 4, (E, d), 0.02))
 
 
 # ---- sampler: bit-exact given identical logits --------------------------------
