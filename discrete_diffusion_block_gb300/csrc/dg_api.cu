@@ -95,6 +95,7 @@ struct dg_model {
        *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   float *gates = nullptr, *y = nullptr;
+  float *xchg = nullptr;  // split-K partial exchange of the projection GEMMs
   int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
       *n_work = nullptr;
   int max_work = 0;
@@ -290,13 +291,13 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), m->page_table, pos0, c.page_size,
                   c.n_q_heads, c.n_kv_heads, c.head_dim, m->cos_t, m->sin_t};
     int *err = m->done_dev + 1;
-    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xq, W.wqkv, T, d, qo, err, st));
+    KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xq, W.wqkv, T, d, qo, err, m->xchg, st));
     if (kv_only_last && L == c.n_layers - 1) break;
     dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal, m->n_pages};
     KL(DG_K_ATTENTION, dg::attention_launch_count(as),
        dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
                      m->attn_ws_bytes, st, err, true));
-    KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, st));
+    KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, m->xchg, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
     KL(DG_K_ROUTE, 1,
@@ -381,6 +382,7 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->moe_stats, 2));
   CKR(m->alloc(&m->q, (size_t)T * qd));
   CKR(m->alloc(&m->o, (size_t)T * qd));
+  CKR(m->alloc(&m->xchg, dg::gemm_xchg_bytes() / sizeof(float)));
   CKR(m->alloc(&m->topk, (size_t)c.n_layers * T * k));  // per-layer routing record
   m->routing_rows.assign(c.n_layers, 0);
   CKR(m->alloc(&m->gates, (size_t)T * k));

@@ -20,10 +20,10 @@
 //   warps 0-3           -- read the accumulator out of TMEM (each warp its
 //                          32-lane quarter) and run the fused epilogue.
 // Split-K: the SPLIT CTAs of a cluster own 1/SPLIT of K each; after the main
-// loop every CTA stages its fp32 partial tile slice by slice, pushes slice j
-// to CTA j with a bulk shared-to-shared copy, and CTA j adds the SPLIT
-// partials of its slice in rank order (deterministic) and runs the epilogue
-// on that slice.
+// loop every CTA stores the slices of its fp32 partial tile that its peers
+// own to a global exchange buffer (it stays in L2), and CTA j adds the SPLIT
+// partials of slice j in rank order (deterministic) and runs the epilogue on
+// that slice.
 // Every mbarrier wait is bounded; a wait that gives up records an error word
 // and lets the CTA finish, so a fault can never hang the GPU.
 #pragma once
@@ -37,6 +37,7 @@ struct TcArgs {
   int M, N, K;             // D[M][N] = A[M][K] . B[N][K]^T
   const bf16 *a, *b;       // A (weights) and B (activations) as operand tiles (tiled_index)
   int *err;                // device error word (timeouts)
+  float *xchg;             // split-K: partial-slice exchange scratch (split_k_xchg_bytes)
 };
 
 namespace tc {
@@ -235,10 +236,9 @@ constexpr int kSkStages = 4;
 constexpr uint32_t kBChunkBytes = 64 * 128;  // one 64-row B box
 
 // Shared memory of a split-K CTA.  The epilogue area overlays the ring.
-// SPLIT > 1: part = the CTA's fp32 partial tile, slice-major ([SPLIT][128][W],
-// element (f, t) of a slice at f * W + (t ^ (f & 31)), so that row-wise
-// writes and column-wise reads are both conflict-free); recv = the SPLIT - 1
-// peer partials of this CTA's own slice, later the epilogue's scratch.
+// SPLIT > 1: mine = the CTA's reduced output slice [128][W] (element (f, t)
+// at f * W + (t ^ (f & 31)), so that the per-row writes and the epilogue's
+// column walks are both conflict-free), then the epilogue's scratch.
 // SPLIT == 1: red = the tile, [128][kSkBN + 1], then the epilogue scratch.
 template <int SPLIT, class Epi>
 struct SkSmem {
@@ -246,16 +246,18 @@ struct SkSmem {
   static constexpr uint32_t stage_bytes = kATileBytes + kSkBN * 128;
   static constexpr size_t ring = (size_t)kSkStages * stage_bytes;
   static constexpr uint32_t slice_bytes = 128u * W * 4u;
-  static constexpr size_t part = SPLIT > 1 ? (size_t)SPLIT * slice_bytes : 0;
-  static constexpr size_t recv = SPLIT > 1 ? (size_t)(SPLIT - 1) * slice_bytes : 0;
+  static constexpr size_t mine = SPLIT > 1 ? slice_bytes : 0;
   static constexpr int red_ld = kSkBN + 1;  // odd: column walks are conflict-free
   static constexpr size_t red = SPLIT > 1 ? 0 : (size_t)128 * red_ld * 4;
-  static constexpr size_t scratch = SPLIT > 1 ? (recv > Epi::extra_smem ? recv : Epi::extra_smem)
-                                              : Epi::extra_smem;
-  static constexpr size_t epi = part + red + scratch;
+  static constexpr size_t epi = mine + red + Epi::extra_smem;
   static constexpr size_t bars_off = ((ring > epi ? ring : epi) + 15) & ~(size_t)15;
-  static constexpr size_t bytes = bars_off + (2 * kSkStages + 2) * 8 + 16 + 1024;
+  static constexpr size_t bytes = bars_off + (2 * kSkStages + 1) * 8 + 16 + 1024;
 };
+
+// Global scratch of the split-K exchange for a launch of n_ctas CTAs: each
+// CTA's partial slices for the SPLIT CTAs of its cluster (the owner's own
+// slot unused), 128 x 256 fp32 per CTA whatever SPLIT is.
+inline size_t split_k_xchg_bytes(int n_ctas) { return (size_t)n_ctas * 128 * kSkBN * 4; }
 
 }  // namespace tc
 
@@ -269,8 +271,7 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t *full = (uint64_t *)(base + S::bars_off);
   uint64_t *empty = full + STAGES;
   uint64_t *accb = empty + STAGES;
-  uint64_t *rbar = accb + 1;  // peer partials received
-  uint32_t *tmem_slot = (uint32_t *)(rbar + 1);
+  uint32_t *tmem_slot = (uint32_t *)(accb + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
   // Output units are (256-column N tile, 128-row M tile) pairs.  Cluster c
@@ -295,7 +296,6 @@ __global__ void __launch_bounds__(128, 1)
       tc::mbar_init(empty + s, 1);
     }
     tc::mbar_init(accb, 1);
-    tc::mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(128, 1)
     const int row = warp * 32 + lane;
     const int nchunks = (ctx.n_valid + 31) >> 5;  // 32-column TMEM chunks holding valid outputs
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    unsigned char *extra = base + S::part + S::red;
+    unsigned char *extra = base + S::mine + S::red;
     if (SPLIT == 1) {
       float *red = (float *)base;
 #pragma unroll 1
@@ -417,65 +417,65 @@ __global__ void __launch_bounds__(128, 1)
       __syncthreads();
       if (ctx.n_valid > 0) epi(red, S::red_ld, ctx, extra);
     } else {
-      // Each CTA writes its fp32 partial into its own shared memory (part);
-      // after a cluster barrier it pushes slice j to CTA j with one bulk copy
-      // per peer.  CTA z adds the SPLIT partials of slice z in rank order (a
-      // fixed order: deterministic) and runs the epilogue on that 128 x W
-      // slice.  A second cluster barrier ends the unit: every copy into and
-      // out of this CTA's shared memory is complete past it.
-      float *part = (float *)base;
-      float *recv = (float *)(base + S::part);
-      const int sw = row & 31;
+      // Each CTA stores the partial slices that its peers own to global
+      // scratch straight from TMEM (slice j of CTA z at xchg[z][j], stored
+      // [W tokens][128 rows]: one coalesced 128-byte store per token and
+      // warp).  After a cluster barrier (release / acquire at cluster scope)
+      // CTA z reads slice z of every peer from L2 and adds the SPLIT partials
+      // in rank order (a fixed order: deterministic), its own straight from
+      // TMEM, into shared memory, then runs the epilogue on that 128 x W
+      // slice.  A second cluster barrier ends the unit: no peer still reads
+      // this CTA's scratch past it.  (Shared-memory pushes between the CTAs
+      // of a cluster measured about three times slower than L2.)
+      constexpr size_t slice_elems = (size_t)128 * W;
+      float *xc = g.xchg + (size_t)(blockIdx.x - z) * SPLIT * slice_elems;  // this cluster's [z][j] slices
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
+        const int sl = (32 * c) / W, o = 32 * c - sl * W;
+        if (sl == z) continue;
         uint32_t v[32];
         tc::tmem_ld32(trow + 32 * c, v);
         tc::tmem_ld_wait(v);
-        const int sl = (32 * c) / W, o = 32 * c - sl * W;
-        float *dst = part + (size_t)sl * 128 * W + (size_t)row * W + o;
+        float *dst = xc + ((size_t)z * SPLIT + sl) * slice_elems + (size_t)o * 128 + row;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[j ^ sw] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) dst[(size_t)j * 128] = __uint_as_float(v[j]);
       }
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the bulk copies read part
-      tc::cluster_sync();  // every CTA staged; every ring is idle
-      if (threadIdx.x == 0) {
-        tc::mbar_expect_tx(rbar, (SPLIT - 1) * S::slice_bytes);
-        for (int q = 1; q < SPLIT; ++q) {
-          const int j = (z + q) % SPLIT, slot = z < j ? z : z - 1;
-          tc::bulk_copy_to_peer(tc::cluster_addr(tc::smem_u32(recv) + slot * S::slice_bytes, (uint32_t)j),
-                                tc::smem_u32(part) + j * S::slice_bytes, S::slice_bytes,
-                                tc::cluster_addr(tc::smem_u32(rbar), (uint32_t)j));
-        }
-      }
-      tc::mbar_wait(rbar, tiles & 1, g.err, 4, abort);
+      tc::cluster_sync();  // every CTA's partials are in L2
       TileCtx sub = ctx;
       sub.n0 = ctx.n0 + z * W;
       sub.n_valid = min(W, ctx.n_valid - z * W);
       sub.swz = 31;
-      float *mine = part + (size_t)z * 128 * W;
+      float *mine = (float *)base;
       if (sub.n_valid > 0 && !*abort) {
-        constexpr int n4 = 128 * W / 4;
-        float4 *m4 = (float4 *)mine;
-        for (int i = threadIdx.x; i < n4; i += 128) {
-          float4 v[SPLIT];
+#pragma unroll 1
+        for (int c = 0; c < W / 32; ++c) {
+          if (32 * c >= sub.n_valid) break;
+          uint32_t own[32];
+          tc::tmem_ld32(trow + z * W + 32 * c, own);
+          float pv[SPLIT][32];  // pv[q]: CTA q's partial (q != z), indexed at compile time
 #pragma unroll
-          for (int q = 0; q < SPLIT; ++q)
-            v[q] = q == z ? m4[i] : ((const float4 *)(recv + (size_t)(q < z ? q : q - 1) * 128 * W))[i];
-          float4 acc = v[0];
+          for (int q = 0; q < SPLIT; ++q) {
+            const float *src = xc + ((size_t)q * SPLIT + z) * slice_elems + (size_t)(32 * c) * 128 + row;
 #pragma unroll
-          for (int q = 1; q < SPLIT; ++q) {  // rank order
-            acc.x += v[q].x;
-            acc.y += v[q].y;
-            acc.z += v[q].z;
-            acc.w += v[q].w;
+            for (int j = 0; j < 32; ++j) pv[q][j] = q == z ? 0.0f : src[(size_t)j * 128];
           }
-          m4[i] = acc;
+          tc::tmem_ld_wait(own);
+          float *mrow = mine + (size_t)row * W;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float acc = z == 0 ? __uint_as_float(own[j]) : pv[0][j];
+#pragma unroll
+            for (int q = 1; q < SPLIT; ++q)  // rank order
+              acc += q == z ? __uint_as_float(own[j]) : pv[q][j];
+            mrow[(32 * c + j) ^ (row & 31)] = acc;
+          }
         }
         __syncthreads();
-        epi(mine, W, sub, (unsigned char *)recv);
+        epi(mine, W, sub, base + S::mine);
       }
       tc::cluster_sync();
     }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the next unit's copies reuse this memory
     // The next unit's MMAs overwrite the accumulator and its copies the
     // shared memory the epilogue used.
     tc::fence_before();
@@ -512,6 +512,7 @@ cudaError_t launch_tc_sk(const TcArgs &g, const Epi &epi, int n_clusters, cudaSt
     if (dev < 64) attr_set |= 1ull << dev;
   }
   if (g.K % tc::kBK || g.K / tc::kBK < SPLIT) return cudaErrorInvalidValue;
+  if (SPLIT > 1 && !g.xchg) return cudaErrorInvalidValue;
   if (n_clusters <= 0 || g.M <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_clusters * SPLIT, 1, 1);

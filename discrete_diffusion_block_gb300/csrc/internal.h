@@ -91,11 +91,13 @@ struct QkvOut {
 // `err`: device error word set by a tensor-core GEMM whose bounded wait gave up.
 // Operands are operand tiles (tiled_index): x_tiles / act_tiles [T][K],
 // wqkv [(Hq + 2 Hkv) hd][d] (rows W_q, W_k, W_v), w [N][K].
+// xchg: device scratch of gemm_xchg_bytes() for the split-K partial exchange
+// (one buffer serves every call on a stream; calls must not overlap).
+size_t gemm_xchg_bytes();
 cudaError_t gemm_qkv(const bf16 *x_tiles, const bf16 *wqkv, int T, int d, const QkvOut &o, int *err,
-                     cudaStream_t st);
+                     float *xchg, cudaStream_t st);
 cudaError_t gemm_residual(const bf16 *act_tiles, const bf16 *w, int T, int K, int N, float *h, int *err,
-                          cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
-  // out[T][N] = act . w^T
+                          float *xchg, cudaStream_t st);  // h[T][N] += act[T][K] . w[N][K]^T
 constexpr int kExpertTileRows = 128;  // token rows per expert work item (MMA N <= 128)
 // xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
 // the logits are then w_out . (xn + xn_lo).

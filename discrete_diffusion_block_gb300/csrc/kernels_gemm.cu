@@ -157,8 +157,9 @@ struct EpiResidual {
   }
 };
 
-TcArgs targs(int M, int N, int K, const bf16 *a, const bf16 *b, int *err) {
+TcArgs targs(int M, int N, int K, const bf16 *a, const bf16 *b, int *err, float *xchg = nullptr) {
   TcArgs g{};
+  g.xchg = xchg;
   g.M = M;
   g.N = N;
   g.K = K;
@@ -290,24 +291,26 @@ static cudaError_t launch_split(const TcArgs &g,
   }
 }
 
+size_t gemm_xchg_bytes() { return tc::split_k_xchg_bytes(num_sms()); }
+
 cudaError_t gemm_qkv(const bf16 *x_tiles, const bf16 *wqkv, int T, int d, const QkvOut &o,
-                     int *err, cudaStream_t st) {
+                     int *err, float *xchg, cudaStream_t st) {
   const int M = (o.Hq + 2 * o.Hkv) * o.hd;
   if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd || d % 64) return cudaErrorInvalidValue;
   EpiQkv epi{o};
-  const TcArgs g = targs(M, T, d, wqkv, x_tiles, err);
+  const TcArgs g = targs(M, T, d, wqkv, x_tiles, err, xchg);
   const int units = ceil_div(M, 128) * ceil_div(T, tc::kSkBN), kt = d / tc::kBK;
   if (kt >= 4) return launch_tc_sk<4>(g, epi, plain_clusters(units, 4), st);
   return launch_tc_sk<1>(g, epi, plain_clusters(units, 1), st);
 }
 
 cudaError_t gemm_residual(const bf16 *act_tiles, const bf16 *w, int T, int K, int N, float *h, int *err,
-                          cudaStream_t st) {
+                          float *xchg, cudaStream_t st) {
   if (K % 64) return cudaErrorInvalidValue;
   EpiResidual epi{h, N};
   const int units = ceil_div(N, 128) * ceil_div(T, tc::kSkBN);
   const int split = pick_split(units, K / tc::kBK);
-  return launch_split(targs(N, T, K, w, act_tiles, err), epi, plain_clusters(units, split), split, st);
+  return launch_split(targs(N, T, K, w, act_tiles, err, xchg), epi, plain_clusters(units, split), split, st);
 }
 
 
