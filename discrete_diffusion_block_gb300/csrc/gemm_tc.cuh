@@ -250,7 +250,12 @@ struct SkSmem {
   static constexpr int red_ld = kSkBN + 1;  // odd: column walks are conflict-free
   static constexpr size_t red = SPLIT > 1 ? 0 : (size_t)128 * red_ld * 4;
   static constexpr size_t epi = mine + red + Epi::extra_smem;
-  static constexpr size_t bars_off = ((ring > epi ? ring : epi) + 15) & ~(size_t)15;
+  // pre: the epilogue inputs its prepare() loads early (split > 1), beside
+  // the ring so that they can arrive while the main loop runs.
+  static constexpr bool prep = SPLIT > 1 && Epi::prep_bytes(W) > 0;
+  static constexpr size_t pre_off = ((ring > epi ? ring : epi) + 127) & ~(size_t)127;
+  static constexpr size_t pre_bytes = prep ? Epi::prep_bytes(W) : 0;
+  static constexpr size_t bars_off = (pre_off + pre_bytes + 15) & ~(size_t)15;
   static constexpr size_t bytes = bars_off + (2 * kSkStages + 1) * 8 + 16 + 1024;
 };
 
@@ -340,22 +345,48 @@ __global__ void __launch_bounds__(128, 1)
       load_a(i, mt0, kb + i);
     }
   }
+  // The tile of a unit, and (split > 1) this CTA's slice of it.
+  auto unit_ctx = [&](int unit) {
+    const int y = unit / m_tiles, mt = unit - y * m_tiles;
+    TileCtx c;
+    c.m0 = mt * 128;
+    c.group = 0;
+    c.b_base = 0;
+    c.n0 = y * tc::kSkBN;
+    c.swz = 0;
+    c.prepared = 0;
+    c.m_valid = min(128, g.M - c.m0);
+    c.n_valid = max(0, min(tc::kSkBN, g.N - c.n0));
+    return c;
+  };
+  auto slice_ctx = [&](const TileCtx &c) {
+    TileCtx sub = c;
+    sub.n0 = c.n0 + z * W;
+    sub.n_valid = min(W, c.n_valid - z * W);
+    sub.swz = 31;
+    sub.prepared = S::prep ? 1 : 0;
+    return sub;
+  };
+  // The first unit's epilogue inputs: before the dependency wait when they
+  // do not come from earlier kernels, else right after it.
+  // (Warps 2-3 only: the producer and MMA threads go straight on.)
+  if (S::prep && Epi::kPrepEarly && warp >= 2) {
+    const TileCtx sub = slice_ctx(unit_ctx(cluster));
+    if (sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x - 64, 64);
+  }
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;  // an earlier timeout: do not wait again
+  if (S::prep && !Epi::kPrepEarly && warp >= 2) {
+    const TileCtx sub = slice_ctx(unit_ctx(cluster));
+    if (sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x - 64, 64);
+  }
 
   int it = 0;     // ring position: k-tiles issued (producer) / consumed (MMA) so far
   int tiles = 0;  // accumulator phase
   for (int unit = cluster; unit < n_units; unit += n_clusters, ++tiles) {
     const int y = unit / m_tiles, mt = unit - y * m_tiles;
-    TileCtx ctx;
-    ctx.m0 = mt * 128;
-    ctx.group = 0;
-    ctx.b_base = 0;
-    ctx.n0 = y * tc::kSkBN;
-    ctx.swz = 0;
-    ctx.m_valid = min(128, g.M - ctx.m0);
-    ctx.n_valid = max(0, min(tc::kSkBN, g.N - ctx.n0));
+    const TileCtx ctx = unit_ctx(unit);
     const int n_mma = max(16, (ctx.n_valid + 15) & ~15);  // MMA N
     const uint32_t tx_bytes = tx_of(y, mt);
 
@@ -429,6 +460,7 @@ __global__ void __launch_bounds__(128, 1)
       // of a cluster measured about three times slower than L2.)
       constexpr size_t slice_elems = (size_t)128 * W;
       float *xc = g.xchg + (size_t)(blockIdx.x - z) * SPLIT * slice_elems;  // this cluster's [z][j] slices
+      const TileCtx sub = slice_ctx(ctx);
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
         const int sl = (32 * c) / W, o = 32 * c - sl * W;
@@ -440,11 +472,9 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) dst[(size_t)j * 128] = __uint_as_float(v[j]);
       }
+      // a later unit's epilogue inputs load while the stores drain
+      if (S::prep && unit != cluster && sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x, 128);
       tc::cluster_sync();  // every CTA's partials are in L2
-      TileCtx sub = ctx;
-      sub.n0 = ctx.n0 + z * W;
-      sub.n_valid = min(W, ctx.n_valid - z * W);
-      sub.swz = 31;
       float *mine = (float *)base;
       if (sub.n_valid > 0 && !*abort) {
 #pragma unroll 1
@@ -471,7 +501,7 @@ __global__ void __launch_bounds__(128, 1)
           }
         }
         __syncthreads();
-        epi(mine, W, sub, base + S::mine);
+        epi(mine, W, sub, S::prep ? base + S::pre_off : base + S::mine);
       }
       tc::cluster_sync();
     }

@@ -26,6 +26,49 @@ struct EpiQkv {
   static constexpr int kTok = 64, kMaxHalf = 64;
   static constexpr size_t extra_smem = (size_t)kTok * kMaxHalf * 2 * sizeof(float) + kTok * sizeof(long long);
   QkvOut o;
+  // Stage the cos/sin rows and page slots of tokens t0 .. t0 + nt - 1 of the
+  // tile with threads tid of nthr (64 or 128; nt <= kTok <= nthr), all loads
+  // in flight at once.
+  __device__ void stage(const TileCtx &c, unsigned char *extra, int t0, int nt, int tid, int nthr) const {
+    const int half = o.hd >> 1, q4 = half >> 2, n4 = nt * q4;
+    float *cs = (float *)extra;
+    float *sn = cs + kTok * kMaxHalf;
+    long long *slot = (long long *)(sn + kTok * kMaxHalf);
+    const int ps = o.pos0 + c.n0 + t0 + tid;
+    const long long page = tid < nt ? (long long)o.page_table[ps / o.pg] : 0;
+    for (int i0 = 0; i0 < n4; i0 += 8 * nthr) {
+      float4 rc[8], rs[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + tid + nthr * u;
+        if (i < n4) {
+          const int t = i / q4, j4 = i - t * q4;
+          const size_t p = (size_t)(o.pos0 + c.n0 + t0 + t);
+          rc[u] = ((const float4 *)(o.cos_t + p * half))[j4];
+          rs[u] = ((const float4 *)(o.sin_t + p * half))[j4];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + tid + nthr * u;
+        if (i < n4) {
+          const int t = i / q4, j4 = i - t * q4;
+          ((float4 *)(cs + t * half))[j4] = rc[u];
+          ((float4 *)(sn + t * half))[j4] = rs[u];
+        }
+      }
+    }
+    if (tid < nt) slot[tid] = page * o.Hkv * o.pg * o.hd + (long long)(ps % o.pg) * 64;
+  }
+  // Split-K with slices of up to kTok tokens: the slice's cos/sin rows and
+  // page slots are staged by prepare() into memory of their own, before the
+  // wait on the previous kernel (tables and page table are inputs of the
+  // step, not outputs of earlier kernels).
+  static constexpr bool kPrepEarly = true;
+  static constexpr size_t prep_bytes(int w) { return w <= kTok ? extra_smem : 0; }
+  __device__ void prepare(const TileCtx &c, unsigned char *extra, int tid, int nthr) const {
+    stage(c, extra, 0, min(kTok, c.n_valid), tid, nthr);
+  }
   __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *extra) const {
     const int hd = o.hd, half = hd >> 1, qdim = o.Hq * hd, kdim = o.Hkv * hd;
     const int pairs_log = hd == 128 ? 5 : 4;  // half/2 = 32 or 16 pairs of pairs per head
@@ -36,33 +79,9 @@ struct EpiQkv {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t0 = 0; t0 < c.n_valid; t0 += kTok) {
       const int nt = min(kTok, c.n_valid - t0);
-      __syncthreads();
-      {  // all of this chunk's cos/sin loads in flight at once (blockDim.x == 128)
-        const int q4 = half >> 2, n4 = nt * q4;
-        float4 rc[8], rs[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = threadIdx.x + 128 * u;
-          if (i < n4) {
-            const int t = i / q4, j4 = i - t * q4;
-            const size_t p = (size_t)(o.pos0 + c.n0 + t0 + t);
-            rc[u] = ((const float4 *)(o.cos_t + p * half))[j4];
-            rs[u] = ((const float4 *)(o.sin_t + p * half))[j4];
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = threadIdx.x + 128 * u;
-          if (i < n4) {
-            const int t = i / q4, j4 = i - t * q4;
-            ((float4 *)(cs + t * half))[j4] = rc[u];
-            ((float4 *)(sn + t * half))[j4] = rs[u];
-          }
-        }
-      }
-      for (int t = threadIdx.x; t < nt; t += blockDim.x) {
-        const int p = o.pos0 + c.n0 + t0 + t;
-        slot[t] = (long long)o.page_table[p / o.pg] * o.Hkv * o.pg * hd + (long long)(p % o.pg) * 64;
+      if (!(c.prepared && t0 == 0)) {
+        __syncthreads();
+        stage(c, extra, t0, nt, threadIdx.x, blockDim.x);
       }
       __syncthreads();
       const int nw = blockDim.x >> 5;
@@ -127,12 +146,36 @@ struct EpiQkv {
 
 // h[token][feature] += tile; lanes walk features (coalesced).  A warp takes
 // 16 of its tokens x 4 feature groups of 32 at a time and issues all 64
-// loads before any store.
+// loads before any store.  Split-K with slices of up to kMaxW tokens:
+// prepare() copies the slice's h rows into shared memory of their own right
+// after the wait on the previous kernel, so their latency hides under the
+// main loop.
 struct EpiResidual {
+  static constexpr int kMaxW = 64;
   static constexpr size_t extra_smem = 0;
+  static constexpr bool kPrepEarly = false;  // h was written by earlier kernels
+  static constexpr size_t prep_bytes(int w) { return w <= kMaxW ? (size_t)w * 128 * sizeof(float) : 0; }
   float *h;
   int ldh;
-  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *) const {
+  __device__ void prepare(const TileCtx &c, unsigned char *extra, int tid, int nthr) const {
+    float4 *hb = (float4 *)extra;  // [token][128 features]
+    const int n4 = min(c.n_valid, kMaxW) * 32;
+    for (int i0 = 0; i0 < n4; i0 += nthr * 16) {
+      float4 r[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = i0 + tid + nthr * u, t = i >> 5, f4 = i & 31;
+        if (i < n4 && 4 * f4 < c.m_valid) r[u] = ((const float4 *)(h + (size_t)(c.n0 + t) * ldh + c.m0))[f4];
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = i0 + tid + nthr * u;
+        if (i < n4 && 4 * (i & 31) < c.m_valid) hb[i] = r[u];
+      }
+    }
+  }
+  __device__ void operator()(float *tile, int ldc, const TileCtx &c, unsigned char *extra) const {
+    const float *hb = c.prepared ? (const float *)extra : nullptr;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     for (int f0 = 0; f0 < c.m_valid; f0 += 128) {
       for (int tb = warp; tb < c.n_valid; tb += 16 * nw) {
@@ -142,7 +185,9 @@ struct EpiResidual {
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             const int t = tb + u * nw, f = f0 + 32 * g + lane;
-            v[g][u] = (f < c.m_valid && t < c.n_valid) ? h[(size_t)(c.n0 + t) * ldh + c.m0 + f] : 0.0f;
+            v[g][u] = (f < c.m_valid && t < c.n_valid)
+                          ? (hb ? hb[t * 128 + f] : h[(size_t)(c.n0 + t) * ldh + c.m0 + f])
+                          : 0.0f;
           }
 #pragma unroll
         for (int g = 0; g < 4; ++g)
