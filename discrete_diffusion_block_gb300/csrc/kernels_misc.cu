@@ -255,67 +255,63 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
 }
 
 // combine_kernel followed by the RMSNorm of the updated row (the next
-// layer's input norm, same formula as rmsnorm_kernel): the row stays in
-// registers between the two.  d4 <= 4 * 256.
-constexpr int kCombNormVec = 4;
-__global__ void __launch_bounds__(256) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
-                                                           const int *slot_row, int k, int d4,
-                                                           const float *gain, float eps, bf16 *x_tiles, int T) {
+// layer's input norm, same formula as rmsnorm_kernel): one block per token,
+// one float4 column per thread (d4 <= 1024), so that the h row, the gain and
+// all k expert rows of a column are in flight at once; the row stays in
+// registers between the two steps.
+__global__ void __launch_bounds__(1024) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
+                                                            const int *slot_row, int k, int d4,
+                                                            const float *gain, float eps, bf16 *x_tiles, int T) {
   pdl_wait();
   pdl_trigger();
-  const int t = blockIdx.x;
+  const int t = blockIdx.x, c = threadIdx.x;
+  const bool ok = c < d4;
   __shared__ float g_s[16];
   __shared__ int r_s[16];
-  __shared__ float red[8];
+  __shared__ float red[32];
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 acc = ok ? h[(size_t)t * d4 + c] : zero;
+  const float4 gg = ok ? ((const float4 *)gain)[c] : zero;
   if (threadIdx.x < k) {
     g_s[threadIdx.x] = gates[(size_t)t * k + threadIdx.x];
     r_s[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
-  float4 hv[kCombNormVec];
+  float4 hv = zero;
   float ss = 0.0f;
+  if (ok) {
+    float4 mo = zero;
+    for (int s0 = 0; s0 < k; s0 += 8) {  // eight expert rows in flight at a time, summed in slot order
+      float4 v[8];
 #pragma unroll
-  for (int u = 0; u < kCombNormVec; ++u) {
-    const int c = threadIdx.x + 256 * u;
-    hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < d4) {
-      float4 v[16];
+      for (int s = 0; s < 8; ++s)
+        if (s0 + s < k) v[s] = y[(size_t)r_s[s0 + s] * d4 + c];
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
-        if (s < k) v[s] = y[(size_t)r_s[s] * d4 + c];
-      const float4 acc = h[(size_t)t * d4 + c];
-      float4 mo = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int s = 0; s < 16; ++s)
-        if (s < k) {
-          mo.x += g_s[s] * v[s].x;
-          mo.y += g_s[s] * v[s].y;
-          mo.z += g_s[s] * v[s].z;
-          mo.w += g_s[s] * v[s].w;
+      for (int s = 0; s < 8; ++s)
+        if (s0 + s < k) {
+          const float gs = g_s[s0 + s];
+          mo.x += gs * v[s].x;
+          mo.y += gs * v[s].y;
+          mo.z += gs * v[s].z;
+          mo.w += gs * v[s].w;
         }
-      hv[u] = make_float4(acc.x + mo.x, acc.y + mo.y, acc.z + mo.z, acc.w + mo.w);
-      h[(size_t)t * d4 + c] = hv[u];
-      ss += hv[u].x * hv[u].x + hv[u].y * hv[u].y + hv[u].z * hv[u].z + hv[u].w * hv[u].w;
     }
+    hv = make_float4(acc.x + mo.x, acc.y + mo.y, acc.z + mo.z, acc.w + mo.w);
+    h[(size_t)t * d4 + c] = hv;
+    ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const int nw = (blockDim.x + 31) >> 5;
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   float tot = 0.0f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) tot += red[w];
+  for (int w = 0; w < nw; ++w) tot += red[w];
   const float inv = rsqrtf(tot / (4 * d4) + eps);
-  const float4 *g4 = (const float4 *)gain;
-#pragma unroll
-  for (int u = 0; u < kCombNormVec; ++u) {
-    const int c = threadIdx.x + 256 * u;
-    if (c < d4) {  // the next layer's QKV operand, in operand tiles
-      const float4 gg = g4[c];
-      __nv_bfloat162 p0 = __floats2bfloat162_rn(hv[u].x * inv * gg.x, hv[u].y * inv * gg.y);
-      __nv_bfloat162 p1 = __floats2bfloat162_rn(hv[u].z * inv * gg.z, hv[u].w * inv * gg.w);
-      *(uint2 *)(x_tiles + tiled_index(T, 4 * d4, t, 4 * c)) = make_uint2(*(uint32_t *)&p0, *(uint32_t *)&p1);
-    }
+  if (ok) {  // the next layer's QKV operand, in operand tiles
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(hv.x * inv * gg.x, hv.y * inv * gg.y);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(hv.z * inv * gg.z, hv.w * inv * gg.w);
+    *(uint2 *)(x_tiles + tiled_index(T, 4 * d4, t, 4 * c)) = make_uint2(*(uint32_t *)&p0, *(uint32_t *)&p1);
   }
 }
 
@@ -445,9 +441,9 @@ cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const
                              int T, int k, int d, const float *gain, float eps, bf16 *x_tiles,
                              cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  if (k > 16 || d % 64 || d > 4 * 256 * kCombNormVec) return cudaErrorInvalidValue;
-  return launch_pdl(combine_norm_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const float4 *)y, gates,
-                    slot_row, k, d / 4, gain, eps, x_tiles, T);
+  if (k > 16 || d % 64 || d > 4 * 1024) return cudaErrorInvalidValue;
+  return launch_pdl(combine_norm_kernel, dim3(T), dim3((d / 4 + 31) & ~31), 0, st, (float4 *)h, (const float4 *)y,
+                    gates, slot_row, k, d / 4, gain, eps, x_tiles, T);
 }
 
 
