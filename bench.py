@@ -224,7 +224,7 @@ def decode_all(dgp, m, seed, scfg):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 128-expert MoE
 # layer shape of `--micro moe`; the decoder's launches touch fewer experts and
 # their traffic is this ratio times their algorithmic bytes.
-FFN_TRAFFIC_RATIO = 1.5652e9 / 1.5634e9
+FFN_TRAFFIC_RATIO = 1.5642e9 / 1.5634e9
 
 
 def expert_bytes(cfg, experts_per_launch, rows_per_launch):
