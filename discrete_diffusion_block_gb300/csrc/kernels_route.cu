@@ -575,6 +575,7 @@ struct ScatArgs {
   int *slot_row;  // in: rank within the token group; out: sorted row
   bf16 *x_tiles;  // [item][d/64] tiles of 128 rows x 64 columns, swizzled
   int T, d, E, k, tile_rows, ng;
+  int per;        // pairs per block
   int *offs, *work, *n_work, *sync;
   int max_work;
   unsigned long long *stats;
@@ -607,12 +608,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
 }
 
 __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
-  extern __shared__ int tab[];  // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]
+  // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]; then
+  // the expert and group rank of each of this block's pairs
+  extern __shared__ int tab[];
   __shared__ int warp_tot[kScatThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int E = a.E, ng = a.ng, n = ng * E;
-  int *soffs = tab + n, *stoff = soffs + E;
+  int *soffs = tab + n, *stoff = soffs + E, *s_ex = stoff + E, *s_rk = s_ex + a.per;
+  const int TK = a.T * a.k;
+  const int p0 = blockIdx.x * a.per, p1 = min(TK, p0 + a.per);
+  // the block's pairs and the group counts: all loads in flight together
+  for (int i = threadIdx.x; i < p1 - p0; i += kScatThreads) {
+    s_ex[i] = a.ids[p0 + i];
+    s_rk[i] = a.slot_row[p0 + i];
+  }
   for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
   __syncwarp();
   __syncthreads();
@@ -654,31 +664,50 @@ __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
   }
   __syncwarp();
   __syncthreads();
-  // Pairs of this block: one warp per pair; the warp copies the token's row
-  // into row r of its item's tiles (16-byte chunk c of k-tile kt at chunk
-  // position c ^ (r % 8): the tensor core's swizzled operand order).
-  const int TK = a.T * a.k, per = (TK + gridDim.x - 1) / gridDim.x;
-  const int p0 = blockIdx.x * per, p1 = min(TK, p0 + per);
+  // Pairs of this block: one warp per pair, two pairs at a time; the warp
+  // copies the token's row into row r of its item's tiles (16-byte chunk c of
+  // k-tile kt at chunk position c ^ (r % 8): the tensor core's swizzled
+  // operand order), both rows' loads in flight before any store.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
-  for (int p = p0 + warp; p < p1; p += kScatThreads / 32) {
-    const int ex = a.ids[p], t = p / a.k, g = t / kRouteTok;
-    const int within = tab[g * E + ex] + a.slot_row[p];  // rank among the expert's rows
-    const int row = soffs[ex] + within;
-    __syncwarp();
-    if (lane == 0) a.slot_row[p] = row;
-    const int item = stoff[ex] + within / a.tile_rows, r = within % a.tile_rows;
-    const uint4 *src = (const uint4 *)(a.xn + (size_t)t * a.d);
-    uint4 *dst = (uint4 *)(a.x_tiles + (size_t)item * KT * (128 * 64)) + r * 8;
-    constexpr int U = 4;
-    for (int c = lane; c < vec; c += 32 * U) {
-      uint4 v[U];
+  constexpr int NW = kScatThreads / 32, U = 12;
+  for (int pb = p0 + warp; pb < p1; pb += 2 * NW) {
+    const uint4 *src[2];
+    uint4 *dst[2];
+    int rr[2];
+    bool ok[2];
 #pragma unroll
-      for (int u = 0; u < U; ++u) v[u] = c + 32 * u < vec ? src[c + 32 * u] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int cc = c + 32 * u;
-        if (cc < vec) dst[(cc >> 3) * 1024 + ((cc & 7) ^ (r & 7))] = v[u];
+    for (int q = 0; q < 2; ++q) {
+      const int p = pb + q * NW;
+      ok[q] = p < p1;
+      src[q] = nullptr;
+      dst[q] = nullptr;
+      rr[q] = 0;
+      if (ok[q]) {
+        const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
+        const int within = tab[g * E + ex] + s_rk[p - p0];  // rank among the expert's rows
+        if (lane == 0) a.slot_row[p] = soffs[ex] + within;
+        const int item = stoff[ex] + within / a.tile_rows;
+        rr[q] = within % a.tile_rows;
+        src[q] = (const uint4 *)(a.xn + (size_t)t * a.d);
+        dst[q] = (uint4 *)(a.x_tiles + (size_t)item * KT * (128 * 64)) + rr[q] * 8;
       }
+    }
+    for (int c0 = 0; c0 < vec; c0 += 32 * U) {
+      uint4 v[2][U];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (ok[q] && c < vec) v[q][u] = src[q][c];
+        }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (ok[q] && c < vec) dst[q][(c >> 3) * 1024 + ((c & 7) ^ (rr[q] & 7))] = v[q][u];
+        }
     }
   }
 }
@@ -734,7 +763,10 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
   a.sync = work + 2 * max_work;
   a.max_work = max_work;
   a.stats = stats;
-  const size_t smem = ((size_t)a.ng * E + 2 * E) * sizeof(int);
+  const int TK = T * k;
+  const int grid = max(1, min(ceil_div(TK, 2 * (kScatThreads / 32)), 2 * num_sms_route()));
+  a.per = ceil_div(TK, grid);
+  const size_t smem = ((size_t)a.ng * E + 2 * E + 2 * (size_t)a.per) * sizeof(int);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static unsigned long long attr_set = 0;
   int dev = 0;
@@ -745,8 +777,6 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set |= 1ull << dev;
   }
-  const int TK = T * k;
-  const int grid = max(1, min(ceil_div(TK, 2 * (kScatThreads / 32)), 2 * num_sms_route()));
   return launch_pdl(scatter_kernel, dim3(grid), dim3(kScatThreads), smem, st, a);
 }
 
