@@ -253,7 +253,12 @@ def test_canvas_attention_against_fp64(P, causal, Hq, Hkv, hd):
 # ---- mixture of experts -----------------------------------------------------------
 
 @pytest.mark.parametrize("T,d,E,k,F", [(256, 256, 8, 2, 512), (77, 256, 8, 2, 512), (256, 2816, 128, 8, 704),
-                                       (64, 256, 200, 4, 128)])
+                                       (64, 256, 200, 4, 128),
+                                       # d = 384: a down unit with a single 128-row block of W_down;
+                                       # F = 192: a gate/up unit of 64 features; a ragged token group
+                                       (130, 384, 16, 3, 192),
+                                       # ~150 rows per expert: experts split into several work items
+                                       (300, 384, 4, 2, 128)])
 def test_moe_against_fp64(T, d, E, k, F):
     wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
     wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
