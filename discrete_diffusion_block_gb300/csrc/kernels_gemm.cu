@@ -289,14 +289,9 @@ cudaError_t tmap_bf16_cached(CUtensorMap *map, const void *ptr, uint64_t rows, u
   return tmap_cached(map, ptr, rows, cols, box);
 }
 
-#define TMAP(map, ptr, rows, cols, box)                                            \
-  do {                                                                             \
-    cudaError_t e_ = tmap_cached(&(map), (ptr), (rows), (cols), (box));            \
-    if (e_ != cudaSuccess) return e_;                                              \
-  } while (0)
-
 // Projections: A = weights [M][K] (rows = output features), B = activations
-// [T][K]; the tile is [feature][token].
+// [T][K], both as operand tiles; the tile is [feature][token].
+
 // Streaming multiprocessors of the current device (cached per device).
 static int num_sms() {
   static int cached[64] = {0};
