@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
 // one float4 column per thread (d4 <= 1024), so that the h row, the gain and
 // all k expert rows of a column are in flight at once; the row stays in
 // registers between the two steps.
-__global__ void __launch_bounds__(1024) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
+__global__ void __launch_bounds__(1024, 2) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
                                                             const int *slot_row, int k, int d4,
                                                             const float *gain, float eps, bf16 *x_tiles, int T) {
   pdl_wait();
@@ -281,13 +281,13 @@ __global__ void __launch_bounds__(1024) combine_norm_kernel(float4 *h, const flo
   float ss = 0.0f;
   if (ok) {
     float4 mo = zero;
-    for (int s0 = 0; s0 < k; s0 += 8) {  // eight expert rows in flight at a time, summed in slot order
-      float4 v[8];
+    for (int s0 = 0; s0 < k; s0 += 4) {  // four expert rows in flight at a time, summed in slot order
+      float4 v[4];
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
+      for (int s = 0; s < 4; ++s)
         if (s0 + s < k) v[s] = y[(size_t)r_s[s0 + s] * d4 + c];
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
+      for (int s = 0; s < 4; ++s)
         if (s0 + s < k) {
           const float gs = g_s[s0 + s];
           mo.x += gs * v[s].x;
