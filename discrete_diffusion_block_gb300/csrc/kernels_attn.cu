@@ -533,10 +533,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
   if (n_mine > 0) tc::mbar_wait(rbar, 0, p.err, 41, abort);
+  // Once per owned row: the partials' weights 2^(m_s - m*) (0 for a split
+  // that saw no key), 1 / L and the output row (token, head), into the idle
+  // V ring past the staged softmax states; then every thread merges float4
+  // columns with them.
   const float NEG = __int_as_float(0xff800000);
-  for (int idx = threadIdx.x; idx < n_mine * (HD / 4); idx += kAttnThreads) {
-    const int lr = idx / (HD / 4), c4 = idx - lr * (HD / 4), rr = r0 + lr, r = r_cta + rr;
-    if (r >= rows_total) continue;
+  float *wtab = (float *)(base + S::vring + 2048);  // [n_own][8] weights, then [n_own] 1 / L
+  int *otab = (int *)(wtab + 9 * n_own);            // [n_own] (token << 12) | head, -1 past the rows
+  for (int lr = threadIdx.x; lr < n_mine; lr += kAttnThreads) {
+    const int rr = r0 + lr, r = r_cta + rr;
     float2 ml[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -553,12 +558,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
     for (int q = 0; q < 8; ++q) mx = fmaxf(mx, ml[q].x);
     float L = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float w = 0.0f;
+      if (q < NS && ml[q].x != NEG) {
+        w = ex2(ml[q].x - mx);
+        L += w * ml[q].y;
+      }
+      wtab[lr * 8 + q] = w;
+    }
+    wtab[8 * n_own + lr] = L > 0.0f ? 1.0f / L : 0.0f;
+    otab[lr] = r < rows_total ? ((r / p.G) << 12) | (g * p.G + r % p.G) : -1;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < n_mine * (HD / 4); idx += kAttnThreads) {
+    const int lr = idx / (HD / 4), c4 = idx - lr * (HD / 4), rr = r0 + lr;
+    const int th = otab[lr];
+    if (th < 0) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      if (q >= NS || ml[q].x == NEG) continue;
-      const float w = ex2(ml[q].x - mx);
-      L += w * ml[q].y;
+      const float w = q < NS ? wtab[lr * 8 + q] : 0.0f;
+      if (w == 0.0f) continue;
       const float *rows = q == z ? stage + (size_t)rr * HD
                                  : (const float *)(recv + (size_t)(q < z ? q : q - 1) * slot_bytes) + (size_t)lr * HD;
       const float4 o = *(const float4 *)(rows + 4 * (c4 ^ (rr & 7)));  // the staging order travels with the rows
@@ -567,8 +588,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       acc.z += w * o.z;
       acc.w += w * o.w;
     }
-    const float invL = L > 0.0f ? 1.0f / L : 0.0f;
-    const int t = r / p.G, h = g * p.G + r % p.G;
+    const float invL = wtab[8 * n_own + lr];
+    const int t = th >> 12, h = th & 4095;
     uint2 v;
     v.x = pack_bf16(acc.x * invL, acc.y * invL);
     v.y = pack_bf16(acc.z * invL, acc.w * invL);
@@ -714,7 +735,8 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
                       const AttnShape &s, bf16 *out, void *ws, size_t ws_bytes, cudaStream_t st,
                       int *err, bool out_tiles) {
   if (s.n_new <= 0) return cudaSuccess;
-  if ((s.hd != 64 && s.hd != 128) || s.Hq % s.Hkv != 0 || s.pg % 64 != 0) return cudaErrorInvalidValue;
+  if ((s.hd != 64 && s.hd != 128) || s.Hq % s.Hkv != 0 || s.Hq > 4096 || s.n_new >= (1 << 19) || s.pg % 64 != 0)
+    return cudaErrorInvalidValue;
   const int G = s.Hq / s.Hkv;
   if (128 % G) return cudaErrorInvalidValue;
   const SplitPlan pl = plan_splits(s);
