@@ -491,17 +491,26 @@ __global__ void __launch_bounds__(128, 1)
           }
           tc::tmem_ld_wait(own);
           float *mrow = mine + (size_t)row * W;
+          float red[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             float acc = z == 0 ? __uint_as_float(own[j]) : pv[0][j];
 #pragma unroll
             for (int q = 1; q < SPLIT; ++q)  // rank order
               acc += q == z ? __uint_as_float(own[j]) : pv[q][j];
-            mrow[(32 * c + j) ^ (row & 31)] = acc;
+            red[j] = acc;
+          }
+          if (Epi::kDirect) {  // the epilogue takes this row's sums as they are
+            epi.direct(sub, row, 32 * c, red, S::prep ? base + S::pre_off : nullptr);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mrow[(32 * c + j) ^ (row & 31)] = red[j];
           }
         }
-        __syncthreads();
-        epi(mine, W, sub, S::prep ? base + S::pre_off : base + S::mine);
+        if (!Epi::kDirect) {
+          __syncthreads();
+          epi(mine, W, sub, S::prep ? base + S::pre_off : base + S::mine);
+        }
       }
       tc::cluster_sync();
     }

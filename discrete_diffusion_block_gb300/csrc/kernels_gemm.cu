@@ -65,7 +65,9 @@ struct EpiQkv {
   // wait on the previous kernel (tables and page table are inputs of the
   // step, not outputs of earlier kernels).
   static constexpr bool kPrepEarly = true;
+  static constexpr bool kDirect = false;  // RoPE pairs rows f and f + hd/2: through the shared tile
   static constexpr size_t prep_bytes(int w) { return w <= kTok ? extra_smem : 0; }
+  __device__ void direct(const TileCtx &, int, int, const float (&)[32], unsigned char *) const {}
   __device__ void prepare(const TileCtx &c, unsigned char *extra, int tid, int nthr) const {
     stage(c, extra, 0, min(kTok, c.n_valid), tid, nthr);
   }
@@ -157,6 +159,24 @@ struct EpiResidual {
   static constexpr size_t prep_bytes(int w) { return w <= kMaxW ? (size_t)w * 128 * sizeof(float) : 0; }
   float *h;
   int ldh;
+  // Split-K: feature row f of the slice gets its reduced sums v[j] for the
+  // slice's tokens t0 + j straight from the reduction (lanes walk features:
+  // one coalesced 128-byte store per token and warp); hb: the rows staged
+  // by prepare(), or null.
+  static constexpr bool kDirect = true;
+  __device__ void direct(const TileCtx &c, int f, int t0, const float (&v)[32], unsigned char *pre) const {
+    if (f >= c.m_valid) return;
+    const float *hb = (const float *)pre;
+    float *dst = h + (size_t)(c.n0 + t0) * ldh + c.m0 + f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int t = t0 + j;
+      if (t < c.n_valid) {
+        const float hv = hb ? hb[t * 128 + f] : dst[(size_t)j * ldh];
+        dst[(size_t)j * ldh] = hv + v[j];
+      }
+    }
+  }
   __device__ void prepare(const TileCtx &c, unsigned char *extra, int tid, int nthr) const {
     float4 *hb = (float4 *)extra;  // [token][128 features]
     const int n4 = min(c.n_valid, kMaxW) * 32;
