@@ -350,8 +350,6 @@ __global__ void __launch_bounds__(128, 1)
     const int y = unit / m_tiles, mt = unit - y * m_tiles;
     TileCtx c;
     c.m0 = mt * 128;
-    c.group = 0;
-    c.b_base = 0;
     c.n0 = y * tc::kSkBN;
     c.swz = 0;
     c.prepared = 0;
