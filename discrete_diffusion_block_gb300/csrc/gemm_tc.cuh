@@ -186,12 +186,13 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t *r) {
 // busy per instruction: with N = 64 the single-thread MMA issue and the
 // shared-memory operand traffic, not HBM, bounded the mainloop.
 //
-// The SPLIT CTAs of one output tile form a thread-block cluster.  Each writes
-// its fp32 partial tile into its own shared memory, slice-major (W = 256 /
-// SPLIT columns per slice); after a cluster barrier it sends slice j to CTA j
-// with one bulk shared-to-shared copy (the TMA engine moves the bytes, no
-// register round trip), CTA z sums the SPLIT partials of slice z in rank order
-// (a fixed order, so results are deterministic) and runs the epilogue on that
+// The SPLIT CTAs of one output tile form a thread-block cluster.  Each
+// stores the slices of its fp32 partial tile that its peers own (W = 256 /
+// SPLIT columns per slice) to an exchange buffer in global memory, which
+// stays in L2 (measured about three times faster than pushing them through
+// distributed shared memory); after a cluster barrier CTA z sums the SPLIT
+// partials of slice z in rank order (a fixed order, so results are
+// deterministic), its own straight from TMEM, and runs the epilogue on that
 // 128 x W slice.  A second cluster barrier ends the unit.
 // ---------------------------------------------------------------------------
 namespace tc {

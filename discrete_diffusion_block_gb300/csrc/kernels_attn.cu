@@ -74,14 +74,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 constexpr int kAttnThreads = 224;
 constexpr int kAttnPages = 256;  // 64-key halves whose physical page is looked up before the key loop
-constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one TMA box)
+constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one 8 KB copy)
 
 // Shared memory (bytes from a 1024-aligned base): Q [HB][128 rows][64]; a
 // 2-slot K ring and a 2-slot V ring of 128-key tiles [HB][128 keys][64]; two
-// P tiles [2][128 rows][64 keys] (bf16, the A operand of P V), so that the
-// softmax of tile i does not wait for P V of tile i - 1; barriers.  After the
-// key loop the K and V rings hold the fp32 output rows [128][HD] on their way
-// out.
+// P tiles of 128 rows x 128 keys ([2 key halves][128][64] bf16 each, the A
+// operand of P V), so that the softmax of tile i does not wait for P V of
+// tile i - 1; the page list; barriers.  After the key loop the K ring holds
+// the fp32 output rows [128][HD] on their way out; with split keys the V ring
+// holds the rows' softmax states and merge weights, and the P tiles receive
+// the peers' partial rows.
 template <int HD>
 struct AttnSmem {
   static constexpr int HB = HD / 64;                       // 64-wide hd blocks
