@@ -222,8 +222,10 @@ int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, siz
 
 /* Kernel classes of the decoder, for per-class timing and launch counts.
  * DG_K_ROUTE counts two launches per MoE layer: the routing kernel (the MoE
- * RMSNorm, router logits, top-k and gates, and the sort of the routed rows
- * by expert) and the row gather. */
+ * RMSNorm, router logits, top-k and gates, and each routed pair's rank among
+ * its token group's pairs of the same expert) and the scatter kernel (the
+ * stable sort of the routed pairs by expert, the gather of their rows into
+ * the expert FFN's operand tiles, and its work list). */
 enum {
     DG_K_EMBED = 0, DG_K_RMSNORM, DG_K_QKV_ROPE, DG_K_ATTENTION, DG_K_O_PROJ,
     DG_K_ROUTE, DG_K_EXPERT_FFN, DG_K_COMBINE, DG_K_LM_HEAD,
