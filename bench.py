@@ -511,7 +511,7 @@ def main():
                     choices=["moe", "lmhead", "sampler", "attention", "kv_append", "all"],
                     help="kernel micro-benchmarks at the micro-op shapes instead of the decoder")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the dominant kernel, if measured for this build")
+                    help="ncu dram bytes per launch of the dominant kernel, if measured for the current binaries")
     args = ap.parse_args()
     if args.micro:
         return micro(args)
