@@ -105,13 +105,6 @@ struct AttnSmem {
 // One 64-key half of a K or V operand tile, all zero (keys past the end).
 __device__ __align__(128) unsigned char g_zero_half[kAttnSlotHalfBytes];
 
-__device__ __forceinline__ void attn_bulk(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                   tc::smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-               : "memory");
-}
-
 __device__ __forceinline__ void attn_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(b)) : "memory");
 }
@@ -272,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t bytes = whole ? 2 * kAttnSlotHalfBytes : kAttnSlotHalfBytes;
       const size_t off = pgs[h] < 0 ? 0 : ((size_t)pgs[h] * p.Hkv + g) * p.pg * HD + (size_t)((key0 + 64 * h) % p.pg) * 64;
       for (int b = 0; b < HB; ++b)
-        attn_bulk(dst + (size_t)b * 16384 + h * kAttnSlotHalfBytes,
+        tc::bulk_load(dst + (size_t)b * 16384 + h * kAttnSlotHalfBytes,
                   pgs[h] < 0 ? (const void *)g_zero_half : (const void *)(pool + off + (size_t)b * p.pg * 64), bytes, bar);
     }
   };

@@ -98,13 +98,6 @@ struct FfnArgs {
 
 constexpr int kTileElems = 128 * 64;
 
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                   tc::smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-               : "memory");
-}
-
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
@@ -231,7 +224,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         const uint32_t tx = (uint32_t)inf.n_acc * a_bytes + b_bytes;
         auto load_a = [&](int s, int kt) {
           for (int j = 0; j < inf.n_acc; ++j)
-            bulk_load(a_tile(s, j), a0 + j * a_blk + kt * a_kt, a_bytes, full + s);
+            tc::bulk_load(a_tile(s, j), a0 + j * a_blk + kt * a_kt, a_bytes, full + s);
         };
         // Phase B: the first stages' weight tiles go out before the wait on act.
         const int pre = inf.phase ? min(KT, kFfnStages) : 0;
@@ -266,7 +259,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           } else if (*abort) {
             break;
           }
-          bulk_load(b_tile(s), bsrc + (size_t)kt * kTileElems, b_bytes, full + s);
+          tc::bulk_load(b_tile(s), bsrc + (size_t)kt * kTileElems, b_bytes, full + s);
           issued = i + 1;
         }
         if (*abort) {
