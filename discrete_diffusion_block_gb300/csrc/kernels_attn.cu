@@ -23,13 +23,14 @@
 // previous tile's P V has landed; below that P stays <= 2^8 and the final
 // O / l does not depend on which reference was used.  Roles (224 threads):
 // warp 0 streams Q once (TMA through a 4-D map that packs the G heads of a
-// token as consecutive rows) and the K tiles through a two-slot ring; warp 6
-// streams the V tiles through their own two-slot ring (both as bulk copies
-// of the pool's pre-swizzled pages, from a page list resolved before the
-// dependency wait); warp 1 issues the MMAs, S of tile i + 1 before P V of
+// token as consecutive rows) and the K tiles through a three-slot ring; warp
+// 6 streams the V tiles through their own three-slot ring (both as bulk
+// copies of the pool's pre-swizzled pages, from a page list resolved before
+// the dependency wait); warp 1 issues the MMAs, S of tile i + 1 before P V of
 // tile i, with two S accumulators and two P tiles so the softmax of one tile
-// overlaps the tensor work of the next (V is the N-contiguous "MN-major" B
-// operand of P V); warps 2-5 hold one query row per thread.  With the key
+// overlaps the tensor work of the next (P is written to tensor memory by the
+// softmax threads and read from there as the A operand of P V; V is the
+// N-contiguous "MN-major" B operand); warps 2-5 hold one query row per thread.  With the key
 // range split over several blocks, the blocks of one query tile form a
 // cluster: each stages its unnormalised output rows and softmax state (m, l)
 // in shared memory, pushes to every peer the slice of rows that peer owns
@@ -77,23 +78,23 @@ constexpr int kAttnPages = 256;  // 64-key halves whose physical page is looked 
 constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one 8 KB copy)
 
 // Shared memory (bytes from a 1024-aligned base): Q [HB][128 rows][64]; a
-// 2-slot K ring and a 2-slot V ring of 128-key tiles [HB][128 keys][64]; two
-// P tiles of 128 rows x 128 keys ([2 key halves][128][64] bf16 each, the A
-// operand of P V), so that the softmax of tile i does not wait for P V of
-// tile i - 1; the page list; barriers.  After the key loop the K ring holds
-// the fp32 output rows [128][HD] on their way out; with split keys the V ring
-// holds the rows' softmax states and merge weights, and the P tiles receive
-// the peers' partial rows.
+// 3-slot K ring and a 3-slot V ring of 128-key tiles [HB][128 keys][64] (the
+// P tiles live in tensor memory, which leaves room for the third slots: the
+// key loop is bound by copy latency times ring depth); the page list;
+// barriers.  After the key loop the K ring holds the fp32 output rows
+// [128][HD] on their way out; with split keys the V ring holds the rows'
+// softmax states and merge weights (first 8 KB) and receives the peers'
+// partial rows (from 8 KB on).
 template <int HD>
 struct AttnSmem {
   static constexpr int HB = HD / 64;                       // 64-wide hd blocks
-  static constexpr int kK = 2, kV = 2;                     // ring depths
+  static constexpr int kK = 3, kV = 3;                     // ring depths
   static constexpr size_t tile = (size_t)HB * 16384;       // one 128-key K or V tile, or Q
   static constexpr size_t q = 0;
   static constexpr size_t kring = q + tile;
   static constexpr size_t vring = kring + kK * tile;
-  static constexpr size_t pbuf = vring + kV * tile;        // 2 x 2 x [128 rows][64 keys] bf16
-  static constexpr size_t pages = pbuf + 2 * 32768;          // physical page per 64-key half (ints)
+  static constexpr size_t recv = vring + 8192;             // split merge: the peers' partial rows
+  static constexpr size_t pages = vring + kV * tile;       // physical page per 64-key half (ints)
   static constexpr size_t bars = pages + kAttnPages * 4;
   // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty[2], o_full,
   // r_full (peer partials received)
@@ -130,6 +131,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// O += P V with P (bf16, two keys per 32-bit column, row = lane) read from
+// tensor memory as the A operand.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum));
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -239,7 +259,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_o = tmem + 256;  // S double buffer: columns [0,128) [128,256); O: [256, 256+HD)
+  // S double buffer: columns [0,128) [128,256); O: [256, 256+HD); P double
+  // buffer (bf16 pairs): [384, 448) [448, 512)
+  const uint32_t t_s = tmem, t_o = tmem + 256, t_p = tmem + 384;
 
   // One 128-key K or V tile: per 64-key half, the page's hd sub-blocks; two
   // halves of one page that follow each other move as one copy; a half past
@@ -334,12 +356,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc::mbar_wait(p_full, i & 1, p.err, 35, abort);
         tc::mbar_wait(v_full + slot, (i / KV) & 1, p.err, 29, abort);
         tc::fence_after();
-        const unsigned char *pb = base + S::pbuf + (size_t)(i & 1) * 32768;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA
-          const uint64_t adesc = tc::sw128_desc(tc::smem_u32(pb + (size_t)(kk >> 2) * 16384)) + 2 * (kk & 3);
+        for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 (8 columns of P) per MMA
           const uint64_t bdesc = mn_desc(tc::smem_u32(v_tile(slot))) + (uint64_t)kk * (2048 >> 4);
-          tc::mma_bf16(t_o, adesc, bdesc, idesc_o, (i | kk) ? 1u : 0u);
+          mma_bf16_tmem_a(t_o, t_p + 64 * (i & 1) + 8 * kk, bdesc, idesc_o, (i | kk) ? 1u : 0u);
         }
         tc::mma_commit(p_empty + (i & 1));
         tc::mma_commit(v_empty + slot);
@@ -396,10 +416,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float m_old = m;
       if (grow) m = m_new;
       // P = 2^(x scale - m): one FMA and one ex2 per key; -inf keys give 0.
-      // Each 32-key group goes to the P tile as soon as it is packed.
+      // Each 32-key group goes to the row's P columns in tensor memory as
+      // soon as it is packed.
       const float nmu = m == NEG ? 0.0f : -m;
       float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-      unsigned char *prow = base + S::pbuf + (size_t)(i & 1) * 32768 + (size_t)row * 128;
+      const uint32_t prow = t_p + 64 * (i & 1) + lane_off;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -413,13 +434,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           else s3 += p0 + p1;
           pk[j >> 1] = pack_bf16(p0, p1);
         }
-        const int h = c >> 1;  // keys 0-63 in box 0, 64-127 in box 1
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 16-byte chunks of this 32-key group
-          const int chunk = (c & 1) * 4 + u;
-          *(uint4 *)(prow + (size_t)h * 16384 + ((chunk ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        tmem_st16(prow + 16 * c, pk);
       }
       // rows whose maximum grew: O (and l) to the new reference, O <- O 2^(m_old - m)
       float f = 1.0f;
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
       }
       l = l * f + ((s0 + s1) + (s2 + s3));
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");  // P (and O) written before the release
       tc::fence_before();
       __syncwarp();
       if (lane == 0) attn_arrive(p_full);
@@ -501,19 +516,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // owns rows [z n, z n + n), n = ceil(128 / NS) rounded up to even (16-byte
   // aligned softmax-state rows); every block sends its staged
   // output rows and softmax states of those rows to their owner with bulk
-  // shared-to-shared copies (into the owner's idle P tiles), and the owner
-  // merges the NS partials (weights 2^(m_s - m*)) in shared memory.
+  // shared-to-shared copies (into the owner's idle V ring past its first
+  // 8 KB), and the owner merges the NS partials (weights 2^(m_s - m*)) in
+  // shared memory.
   const int NS = gridDim.z;
   const int n_own = (((128 + NS - 1) / NS) + 1) & ~1;
   const uint32_t o_slot = (uint32_t)n_own * HD * 4, ml_slot = (uint32_t)n_own * 8;
   const uint32_t slot_bytes = o_slot + ml_slot;
   const float *stage = (const float *)(base + S::kring);
   const float2 *ml_stage = (const float2 *)(base + S::vring);
-  unsigned char *recv = base + S::pbuf;           // (NS - 1) slots: O rows, then (m, l) pairs
+  unsigned char *recv = base + S::recv;           // (NS - 1) slots: O rows, then (m, l) pairs
   uint64_t *rbar = r_full;
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the copies read the staged rows
   __syncwarp();
-  tc::cluster_sync();  // every block staged; every block's P tiles are idle
+  tc::cluster_sync();  // every block staged; every block's V ring is idle
   const int z = split, r0 = z * n_own, n_mine = max(0, min(128, r0 + n_own) - r0);
   if (threadIdx.x == 0) {
     tc::mbar_expect_tx(rbar, (uint32_t)(NS - 1) * ((uint32_t)n_mine * HD * 4 + (uint32_t)((n_mine + 1) & ~1) * 8));
@@ -767,6 +783,13 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
     const uint32_t box[4] = {64, (uint32_t)G, 1, (uint32_t)(128 / G)};
     cudaError_t e = attn_map(&tq, q, 4, dims, strides, box);
     if (e != cudaSuccess) return e;
+  }
+  if (pl.splits > 1) {  // the peers' partial rows fit the V ring past its first 8 KB
+    const size_t n_own = (size_t)(((128 + pl.splits - 1) / pl.splits) + 1) & ~(size_t)1;
+    const size_t need = (size_t)(pl.splits - 1) * (n_own * s.hd * 4 + n_own * 8);
+    const size_t room = (s.hd == 128 ? AttnSmem<128>::pages - AttnSmem<128>::recv
+                                     : AttnSmem<64>::pages - AttnSmem<64>::recv);
+    if (need > room) return cudaErrorInvalidValue;
   }
   const dim3 grid(ceil_div(rows_total, kRowsPerBlock), s.Hkv, pl.splits);
   return s.hd == 128 ? launch_attn<128>(tq, p, grid, st) : launch_attn<64>(tq, p, grid, st);
