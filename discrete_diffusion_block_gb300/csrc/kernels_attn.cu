@@ -21,7 +21,7 @@
 // only a row whose maximum grows by more than 2^8 moves to the new reference
 // and rescales its accumulator row in TMEM (read, scale, write back) after the
 // previous tile's P V has landed; below that P stays <= 2^8 and the final
-// O / l does not depend on which reference was used.  Roles (224 threads):
+// O / l does not depend on which reference was used.  Roles (352 threads):
 // warp 0 streams Q once (TMA through a 4-D map that packs the G heads of a
 // token as consecutive rows) and the K tiles through a three-slot ring; warp
 // 6 streams the V tiles through their own three-slot ring (both as bulk
@@ -30,8 +30,10 @@
 // tile i, with two S accumulators and two P tiles so the softmax of one tile
 // overlaps the tensor work of the next (P is written to tensor memory by the
 // softmax threads and read from there as the A operand of P V; V is the
-// N-contiguous "MN-major" B operand); warps 2-5 hold one query row per thread.  With the key
-// range split over several blocks, the blocks of one query tile form a
+// N-contiguous "MN-major" B operand); warps 2-5 and 7-10 do the softmax, two
+// warps per TMEM lane quarter (thread = query row), each on half of a tile's
+// keys, exchanging their halves' maxima per tile.  With the key range split
+// over several blocks, the blocks of one query tile form a
 // cluster: each stages its unnormalised output rows and softmax state (m, l)
 // in shared memory, pushes to every peer the slice of rows that peer owns
 // (bulk shared-to-shared copies), and each block merges its slice (weights
@@ -73,8 +75,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 
-constexpr int kAttnThreads = 224;
-constexpr int kAttnPages = 256;  // 64-key halves whose physical page is looked up before the key loop
+constexpr int kAttnThreads = 352;  // warps 0, 1, 6: copies and MMAs; 2-5 and 7-10: softmax
+constexpr int kAttnPages = 64;  // 64-key halves whose physical page is looked up before the key loop
 constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one 8 KB copy)
 
 // Shared memory (bytes from a 1024-aligned base): Q [HB][128 rows][64]; a
@@ -95,7 +97,8 @@ struct AttnSmem {
   static constexpr size_t vring = kring + kK * tile;
   static constexpr size_t recv = vring + 8192;             // split merge: the peers' partial rows
   static constexpr size_t pages = vring + kV * tile;       // physical page per 64-key half (ints)
-  static constexpr size_t bars = pages + kAttnPages * 4;
+  static constexpr size_t xch = pages + kAttnPages * 4;    // [2 halves][128 rows] fp32: the softmax pairs' exchange
+  static constexpr size_t bars = xch + 2 * 128 * 4;
   // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty[2], o_full,
   // r_full (peer partials received)
   static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 4 + 1;
@@ -208,9 +211,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(s_full + i, 1);
-      tc::mbar_init(s_empty + i, 4);
+      tc::mbar_init(s_empty + i, 8);  // one arrival per softmax warp
     }
-    tc::mbar_init(p_full, 4);
+    tc::mbar_init(p_full, 8);
     tc::mbar_init(p_empty, 1);
     tc::mbar_init(p_empty + 1, 1);
     tc::mbar_init(o_full, 1);
@@ -367,40 +370,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::mma_commit(o_full);
     }
   } else {
-    // ---- softmax warps: thread = query row, one pass ------------------------
+    // ---- softmax warps: two per TMEM lane quarter (warps 2-5: keys 0-63 of a
+    // tile, warps 7-10: keys 64-127); thread = query row; the pair exchanges
+    // its halves' maxima through shared memory (named barrier 1 + quarter)
+    const int half = warp >= 7 ? 1 : 0;
     const int q4 = warp & 3, row = 32 * q4 + lane, r = r_cta + row;
     const bool ok = r < rows_total;
     const int lim = p.causal ? p.n_prefix + (ok ? r / p.G : 0) : n_keys - 1;
     const int last = min(k_end - 1, lim);  // last key this row sees in the block's range
     const float NEG = __int_as_float(0xff800000);
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    float m = NEG, l = 0.0f;
+    float *xch = (float *)(base + S::xch);  // [2 halves][128 rows]
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;\n" ::"r"(1 + q4) : "memory"); };
+    float m = NEG, l = 0.0f;  // l: this half's share of the row sum
     for (int i = 0; i < n_kt; ++i) {
       const int buf = i & 1;
       tc::mbar_wait(s_full + buf, (i >> 1) & 1, p.err, 36, abort);
       tc::fence_after();
-      const int key_base = k_begin + 128 * i;
-      uint32_t x[4][32];
+      const int key_base = k_begin + 128 * i + 64 * half;
+      uint32_t x[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(t_s + buf * 128 + lane_off + 32 * c, x[c]);
+      for (int c = 0; c < 2; ++c) tc::tmem_ld32(t_s + buf * 128 + lane_off + 64 * half + 32 * c, x[c]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld_wait(x[c]);  // ties every loaded register to the wait
+      for (int c = 0; c < 2; ++c) tc::tmem_ld_wait(x[c]);  // ties every loaded register to the wait
       tc::fence_before();
       __syncwarp();
       if (lane == 0) attn_arrive(s_empty + buf);
-      // keys this row must not see are -inf (only in a tile that holds some)
-      const int nvalid = min(128, last - key_base + 1);  // <= 0: none
-      if (nvalid < 128) {
+      // keys this row must not see are -inf (only in a half that holds some)
+      const int nvalid = min(64, last - key_base + 1);  // <= 0: none
+      if (nvalid < 64) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (32 * c + j >= nvalid) x[c][j] = 0xff800000u;
       }
-      // tile maximum of the raw scores (the scale is positive), four chains
+      // maximum of the raw scores of this half (the scale is positive), four
+      // chains, then the pair's maximum
       float a0 = __int_as_float(0xff800000), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           a0 = fmaxf(a0, __uint_as_float(x[c][j]));
@@ -408,21 +417,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           a2 = fmaxf(a2, __uint_as_float(x[c][j + 2]));
           a3 = fmaxf(a3, __uint_as_float(x[c][j + 3]));
         }
-      const float tmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.scale_log2;
+      const float hmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      xch[half * 128 + row] = hmax;
+      pair_sync();
+      const float tmax = fmaxf(hmax, xch[(half ^ 1) * 128 + row]) * p.scale_log2;
+      pair_sync();  // both read before the next tile's maxima overwrite the slots
       const float m_new = fmaxf(m, tmax);
-      const bool grow = m_new > m + kRescaleLog2;  // false while both are -inf
+      const bool grow = m_new > m + kRescaleLog2;  // false while both are -inf; the same in both halves
       // P tile i & 1 is free once P V of tile i - 2 is done
       if (i >= 2) tc::mbar_wait(p_empty + (i & 1), ((i >> 1) - 1) & 1, p.err, 37, abort);
       const float m_old = m;
       if (grow) m = m_new;
       // P = 2^(x scale - m): one FMA and one ex2 per key; -inf keys give 0.
       // Each 32-key group goes to the row's P columns in tensor memory as
-      // soon as it is packed.
+      // soon as it is packed (this half: columns 32 half .. 32 half + 31).
       const float nmu = m == NEG ? 0.0f : -m;
       float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-      const uint32_t prow = t_p + 64 * (i & 1) + lane_off;
+      const uint32_t prow = t_p + 64 * (i & 1) + 32 * half + lane_off;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
@@ -436,7 +449,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         tmem_st16(prow + 16 * c, pk);
       }
-      // rows whose maximum grew: O (and l) to the new reference, O <- O 2^(m_old - m)
+      // rows whose maximum grew: O (and l) to the new reference, O <- O 2^(m_old - m);
+      // each half rescales its half of the O columns
       float f = 1.0f;
       if (__any_sync(0xffffffffu, grow) && i > 0) {
         // O must hold P V of every earlier tile: wait for tile i - 1's
@@ -444,7 +458,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc::fence_after();
         f = grow ? ex2(m_old - m) : 1.0f;  // m_old = -inf: 0 (O holds zeros)
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
           uint32_t o[32];
           tc::tmem_ld32(t_o + lane_off + 32 * c, o);
           tc::tmem_ld_wait(o);
@@ -452,7 +466,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
           tmem_st32(t_o + lane_off + 32 * c, o);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
       }
       l = l * f + ((s0 + s1) + (s2 + s3));
       asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");  // P (and O) written before the release
@@ -460,15 +473,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       __syncwarp();
       if (lane == 0) attn_arrive(p_full);
     }
+    // the row sum of both halves
+    xch[half * 128 + row] = l;
+    pair_sync();
+    const float lt = half ? xch[row] + l : l + xch[128 + row];  // keys 0-63 first
     // ---- output: TMEM -> shared rows -> coalesced stores --------------------
     if (n_kt > 0) {
       tc::mbar_wait(o_full, 0, p.err, 38, abort);
       tc::fence_after();
     }
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
     float *orow = (float *)(base + S::kring) + (size_t)row * HD;  // the K and V rings are idle now
 #pragma unroll 1
-    for (int c = 0; c < HD / 32; ++c) {
+    for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
       uint32_t v[32];
       if (n_kt > 0) {
         tc::tmem_ld32(t_o + lane_off + 32 * c, v);
@@ -485,7 +502,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                 __uint_as_float(v[j + 2]) * sc, __uint_as_float(v[j + 3]) * sc);
       }
     }
-    if (!p.out) ((float2 *)(base + S::vring))[row] = make_float2(m, l);  // split blocks: the row's softmax state
+    if (!p.out && half == 0) ((float2 *)(base + S::vring))[row] = make_float2(m, lt);  // split blocks: the row's softmax state
   }
   __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
