@@ -32,6 +32,8 @@ class SamplerConfig:
     commit_mode: str = "causal"
     conf_threshold: float = 0.9
     sample_seed: int = 0
+    temp_start: float = 1.0     # re-noise temperature at step 1 ...
+    temp_end: float = 1.0       # ... and at step N (linear in between)
 
 
 def run_canvas(logits_fn, scfg, k, on_step=None):
@@ -42,7 +44,8 @@ def run_canvas(logits_fn, scfg, k, on_step=None):
         x_in = st.x.copy()
         l = np.asarray(logits_fn(x_in), np.float32)
         done, a, conf, g = sampler.step(st, l, scfg.sample_seed, k, n, scfg.budget_N,
-                                        scfg.stable_steps, scfg.conf_threshold, scfg.adaptive)
+                                        scfg.stable_steps, scfg.conf_threshold, scfg.adaptive,
+                                        scfg.temp_start, scfg.temp_end)
         if on_step is not None:
             on_step(k=k, n=n, x_in=x_in, logits=l, a=a, conf=conf, g=g, state=st.copy(), done=done)
         if done:

@@ -120,14 +120,16 @@ def silu(x):
 ROUTING_TOL = 1e-2
 
 
-def route(y, wr, k, forced=None, tol=ROUTING_TOL):
+def route(y, wr, k, forced=None, tol=ROUTING_TOL, rel_tol=None):
     """Top-k experts (ties -> lower id) and softmax gates over their logits.
 
     `forced` [T, k] replays another implementation's expert choice: top-k is
     an integer decided by floating point, so where router logits are tied
     within rounding either side of the tie is a correct result.  A forced set
     is accepted only if it holds k distinct experts whose logits all reach
-    the k-th largest logit minus `tol`; otherwise ValueError.
+    the k-th largest logit minus the allowance; otherwise ValueError.  The
+    allowance is `tol`, or with `rel_tol` that fraction of the row's largest
+    |logit| (the normwise relative error of bf16 logits against fp32).
     """
     r = y @ np.asarray(wr, np.float64).T                       # [T, E]
     order = np.argsort(-r, axis=1, kind="stable")
@@ -135,15 +137,26 @@ def route(y, wr, k, forced=None, tol=ROUTING_TOL):
     if forced is not None:
         forced = np.asarray(forced).astype(np.int64)
         kth = np.take_along_axis(r, ids[:, -1:], axis=1)[:, 0]
-        ok = np.take_along_axis(r, forced, axis=1).min(axis=1) >= kth - tol
+        allow = tol if rel_tol is None else rel_tol * np.abs(r).max(axis=1)
+        ok = np.take_along_axis(r, forced, axis=1).min(axis=1) >= kth - allow
         ok &= np.array([len(set(row)) == k for row in forced])
         if not ok.all():
-            raise ValueError(f"forced routing is not a top-{k} choice within {tol} "
+            raise ValueError(f"forced routing is not a top-{k} choice within the allowance "
                              f"(tokens {np.nonzero(~ok)[0][:8].tolist()})")
         ids = forced
     sel = np.take_along_axis(r, ids, axis=1)
     g = np.exp(sel - sel.max(axis=1, keepdims=True))
     return ids.astype(np.int32), g / g.sum(axis=1, keepdims=True), r
+
+
+def routing_margin(y, wr, forced):
+    """Per token: the lowest logit of the forced experts minus the k-th largest
+    logit (>= 0 when the forced set is the exact top-k), and the row's largest
+    |logit|; for reporting how close a replayed expert choice is to the top-k."""
+    r = y @ np.asarray(wr, np.float64).T
+    k = forced.shape[1]
+    kth = -np.sort(-r, axis=1)[:, k - 1]
+    return np.take_along_axis(r, np.asarray(forced, np.int64), axis=1).min(axis=1) - kth, np.abs(r).max(axis=1)
 
 
 def expert_ffn(x, wg, wu, wd):
@@ -160,16 +173,17 @@ def moe_given_routing(y, ids, gates, W):
     return out
 
 
-def moe(y, W, k, forced=None):
-    ids, gates, r = route(y, W["wr"], k, forced)
+def moe(y, W, k, forced=None, rel_tol=None):
+    ids, gates, r = route(y, W["wr"], k, forced, rel_tol=rel_tol)
     return moe_given_routing(y, ids, gates, W), ids, gates, r
 
 
-def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=None):
+def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=None, routing_rel_tol=None):
     """One decoder layer over new tokens h [T, d] at positions pos.
 
     prefix_k/v [S, Hkv, hd] are the cached (rotated) keys/values visible to
-    every new token; forced_routing (optional [T, k]) as in route().
+    every new token; forced_routing (optional [T, k]) and routing_rel_tol as
+    in route().
     Returns (h_out, k_new, v_new).
     """
     T = h.shape[0]
@@ -185,7 +199,7 @@ def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=N
     o = attention(q, K, V, visibility(prefix_k.shape[0], T, mode))
     h = h + o.reshape(T, Hq * hd) @ np.asarray(W["wo"], np.float64).T
     n2 = rmsnorm(h, W["moe_norm"], cfg.rms_eps)
-    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing)
+    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing, routing_rel_tol)
     if trace is not None:
         trace.append(dict(n=n, q=q, k=k, v=v, o=o, n2=n2, ids=ids, gates=gates, router=r, y=y))
     return h + y, k, v
@@ -207,6 +221,14 @@ class KVCache:
         self.v[layer] = np.concatenate([self.v[layer], v], axis=0)
 
 
+def embed_rows(W, ids):
+    """Embedding rows of token ids (fp64); W.embed is an array or a table that
+    generates rows on demand (oracle.weights.RowTensor)."""
+    if isinstance(W.embed, np.ndarray):
+        return np.asarray(W.embed, np.float64)[ids]
+    return W.embed.take(ids).astype(np.float64)
+
+
 def forward(W, cfg, ids, pos, cache, mode, append=False, trace=None, routing=None):
     """Run all layers over tokens `ids` at positions `pos` with `cache` as prefix.
 
@@ -218,7 +240,7 @@ def forward(W, cfg, ids, pos, cache, mode, append=False, trace=None, routing=Non
     """
     ids = np.asarray(ids)
     pos = pos + np.arange(len(ids)) if np.ndim(pos) == 0 else np.asarray(pos)
-    h = np.asarray(W.embed, np.float64)[ids]
+    h = embed_rows(W, ids)
     new_kv = []
     for L, WL in enumerate(W.layers):
         forced = None if routing is None else routing[L]

@@ -21,6 +21,16 @@ pages; this is the commit rule of the synthetic workload):
     or the step count reaches N; on reaching N the still-uncommitted
     positions take a_i.
 
+Temperature annealing (report §5: the online teacher samples "with mild
+temperature annealing"; no schedule is given).  Reading: the re-noise sample
+of step n is drawn from softmax(l / tau_n), with tau_n moving linearly from
+temp_start at step 1 to temp_end at step N:
+    tau_n = temp_start + (temp_end - temp_start) * (n - 1) / (N - 1)   (N > 1)
+in double, and inv_tau_n = fp32(1 / tau_n); the Gumbel keys become
+k_v = fp32(l_v * inv_tau_n) + G_v (two roundings, no fused multiply-add),
+which at tau = 1 are the keys above exactly.  The argmax and the confidence
+are those of the model's own distribution (tau = 1).
+
 Canonical reduction order (the pages give none; this one makes the sampler
 reproducible bit for bit on any hardware given the same fp32 logits):
   1. vocab tiles of 256 entries, t = 0 .. V/256-1; inside tile t, ascending v:
@@ -52,8 +62,18 @@ TILE = 256
 f32 = np.float32
 
 
-def tile_partials(l, G):
-    """Per-(position, tile) partials of fp32 logits l [R, V] and Gumbel noise G [R, V]."""
+def annealed_inv_tau(n, budget_N, temp_start=1.0, temp_end=1.0):
+    """fp32(1 / tau_n) of step n (1-based) under the linear schedule above."""
+    if budget_N > 1:
+        tau = float(temp_start) + (float(temp_end) - float(temp_start)) * (n - 1) / (budget_N - 1)
+    else:
+        tau = float(temp_start)
+    return f32(1.0 / tau)
+
+
+def tile_partials(l, G, inv_tau=f32(1.0)):
+    """Per-(position, tile) partials of fp32 logits l [R, V] and Gumbel noise G [R, V];
+    the Gumbel keys are fp32(l * inv_tau) + G."""
     R, V = l.shape
     assert V % TILE == 0
     T = V // TILE
@@ -63,7 +83,8 @@ def tile_partials(l, G):
     s = np.zeros((R, T), f32)
     for v in range(TILE):                      # ascending, one rounding per add
         s = s + dg_exp(lt[:, :, v] - m)
-    kap = (lt + G.reshape(R, T, TILE).astype(f32)).astype(f32)
+    lk = (lt * f32(inv_tau)).astype(f32)       # exact when inv_tau == 1
+    kap = (lk + G.reshape(R, T, TILE).astype(f32)).astype(f32)
     gk = kap.max(axis=2)
     gi = kap.argmax(axis=2).astype(np.int64) + np.arange(T)[None, :] * TILE
     return dict(m=m, a=a, s=s, gk=gk, gi=gi)
@@ -104,17 +125,18 @@ def reduce_tiles(p):
     return {k: v[:, 0] for k, v in p.items()}
 
 
-def position_outputs(l, seed, k, n, positions=None):
+def position_outputs(l, seed, k, n, positions=None, inv_tau=f32(1.0)):
     """(argmax a, confidence conf, Gumbel sample g) for fp32 logits l [R, V].
 
     `positions` gives the canvas index of each row of l (default 0..R-1); the
     Gumbel stream of step n (1-based) of canvas k (0-based) is keyed by it.
+    g is a sample of softmax(l * inv_tau).
     """
     l = np.asarray(l, dtype=f32)
     R, V = l.shape
     positions = np.arange(R) if positions is None else np.asarray(positions)
     G = gumbel_from_uniform(philox.gumbel_uniforms(seed, k, n, positions, V))
-    r = reduce_tiles(tile_partials(l, G))
+    r = reduce_tiles(tile_partials(l, G, inv_tau))
     conf = (f32(1.0) / r["s"]).astype(f32)
     return r["a"].astype(np.int32), conf, r["gi"].astype(np.int32), r
 
@@ -154,8 +176,9 @@ def apply_rule(state, a, conf, g, n, budget_N, stable_steps=2, conf_threshold=0.
     return all_done and adaptive
 
 
-def step(state, l, seed, k, n, budget_N, stable_steps=2, conf_threshold=0.9, adaptive=True):
+def step(state, l, seed, k, n, budget_N, stable_steps=2, conf_threshold=0.9, adaptive=True,
+         temp_start=1.0, temp_end=1.0):
     """Full sampler step on fp32 logits [C, V]: returns (done, a, conf, g)."""
-    a, conf, g, _ = position_outputs(l, seed, k, n)
+    a, conf, g, _ = position_outputs(l, seed, k, n, inv_tau=annealed_inv_tau(n, budget_N, temp_start, temp_end))
     done = apply_rule(state, a, conf, g, n, budget_N, stable_steps, conf_threshold, adaptive)
     return done, a, conf, g

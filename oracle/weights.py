@@ -125,3 +125,75 @@ class Weights:
                 moe_norm=np.ones(d, np.float32),
             ))
         self.final_norm = np.ones(d, np.float32)
+
+
+class ExpertTensor:
+    """Expert tensor [E, a, b] whose experts are generated when indexed (never
+    stored: a full-width layer holds ~3 GB of expert weights in fp32)."""
+
+    def __init__(self, seed, tid, shape, std):
+        self.seed, self.tid, self.shape, self.std = seed, tid, tuple(shape), std
+
+    def __getitem__(self, e):
+        inner = self.shape[1] * self.shape[2]
+        return elements(self.seed, self.tid, int(e) * inner, inner, self.std).reshape(self.shape[1:])
+
+    def __len__(self):
+        return self.shape[0]
+
+
+class RowTensor:
+    """[V, d] table (embedding, LM head) generated row range by row range."""
+
+    def __init__(self, seed, tid, shape, std):
+        self.seed, self.tid, self.shape, self.std = seed, tid, tuple(shape), std
+
+    def take(self, row_ids):
+        return rows(self.seed, self.tid, self.shape, row_ids, self.std)
+
+    def block(self, r0, n):
+        d = self.shape[1]
+        return elements(self.seed, self.tid, int(r0) * d, int(n) * d, self.std).reshape(n, d)
+
+
+class LazyWeights:
+    """The decoder's tensors for full-width shapes: the same generator and
+    values as Weights, but expert tensors are generated per expert when used
+    and the embedding / LM head per row range, so that a 30-layer model of
+    the full configuration fits in host memory.  Per-layer projection and
+    router matrices are generated once, on the layer's first use."""
+
+    def __init__(self, cfg):
+        self.cfg = cfg
+        s, std = cfg.weight_seed, cfg.init_std
+        self.embed = RowTensor(s, EMBED, (cfg.vocab, cfg.d_model), std)
+        self.lm_head = RowTensor(s, LM_HEAD, (cfg.vocab, cfg.d_model), std)
+        self.final_norm = np.ones(cfg.d_model, np.float32)
+        self.layers = _LazyLayers(cfg)
+
+
+class _LazyLayers:
+    def __init__(self, cfg):
+        self.cfg, self._done = cfg, {}
+
+    def __len__(self):
+        return self.cfg.n_layers
+
+    def __iter__(self):
+        return (self[L] for L in range(len(self)))
+
+    def __getitem__(self, L):
+        if L not in self._done:
+            cfg = self.cfg
+            s, std = cfg.weight_seed, cfg.init_std
+            d, E, F = cfg.d_model, cfg.n_experts, cfg.d_ff
+            qd, kd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+            t = lambda w: layer_tid(L, w)
+            self._done[L] = dict(
+                wq=tensor(s, t(WQ), (qd, d), std), wk=tensor(s, t(WK), (kd, d), std),
+                wv=tensor(s, t(WV), (kd, d), std), wo=tensor(s, t(WO), (d, qd), std),
+                wr=tensor(s, t(WR), (E, d), std),
+                wg=ExpertTensor(s, t(WG), (E, F, d), std), wu=ExpertTensor(s, t(WU), (E, F, d), std),
+                wd=ExpertTensor(s, t(WD), (E, d, F), std),
+                attn_norm=np.ones(d, np.float32), moe_norm=np.ones(d, np.float32))
+        return self._done[L]

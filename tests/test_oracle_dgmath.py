@@ -50,3 +50,19 @@ def test_gumbel_moments():
     g = gumbel_from_uniform(u).astype(np.float64)
     assert abs(g.mean() - 0.5772156649) < 2e-3
     assert abs(g.var() - math.pi ** 2 / 6) < 1e-2
+
+
+def test_gumbel_noise_strictly_increasing_over_every_input():
+    # The sampler's noise takes 2^23 distinct inputs u = (2 i + 1) 2^-24.  A
+    # strictly increasing transform is what lets a kernel bound the noise of a
+    # whole bucket of Philox words (those sharing their top byte) by its value
+    # at the bucket's largest word; check it exhaustively, together with the
+    # limits of the standard Gumbel at the two ends of the open interval.
+    i = np.arange(1 << 23, dtype=np.int64)
+    u = ((2 * i + 1).astype(np.float32) * np.float32(2.0 ** -24)).astype(np.float32)
+    g = gumbel_from_uniform(u).astype(np.float64)
+    assert np.all(np.diff(g) > 0)
+    # -log(-log u) near u = 2^-24 and u = 1 - 2^-24, evaluated in double
+    lo, hi = float(u[0]), float(u[-1])
+    assert abs(g[0] - (-math.log(-math.log(lo)))) < 1e-5
+    assert abs(g[-1] - (-math.log(-math.log(hi)))) < 1e-4

@@ -215,3 +215,19 @@ def test_forced_routing_accepts_valid_ties_and_rejects_others(small_weights):
     assert np.array_equal(ok_ids, alt) and np.allclose(ok_g.sum(axis=1), 1.0)
     with pytest.raises(ValueError):                                   # repeated expert
         model.route(y, W["wr"], SMALL.top_k, forced=np.repeat(ids[:, :1], SMALL.top_k, 1), tol=10.0)
+
+
+def test_forced_routing_relative_allowance():
+    # rel_tol scales the near-tie allowance by the row's largest |logit|:
+    # with logits up to 2.0 and rel_tol 2e-2 a swap across a 0.03 gap is a
+    # valid top-k, across a 0.05 gap it is not.
+    wr = np.eye(4)
+    y = np.array([[2.0, 1.0, 0.97, 0.0], [2.0, 1.0, 0.95, 0.0]])
+    ids, _, _ = model.route(y[:1], wr, 2, forced=[[0, 2]], rel_tol=2e-2)
+    assert ids.tolist() == [[0, 2]]
+    with pytest.raises(ValueError):
+        model.route(y[1:], wr, 2, forced=[[0, 2]], rel_tol=2e-2)
+    with pytest.raises(ValueError):
+        model.route(y[:1], wr, 2, forced=[[0, 2]])          # the absolute 1e-2 allowance
+    m, mx = model.routing_margin(y, wr, np.array([[0, 2], [0, 2]]))
+    assert np.allclose(m, [-0.03, -0.05]) and np.allclose(mx, [2.0, 2.0])

@@ -129,3 +129,41 @@ def test_tile_partial_definition_matches_brute_force_in_small_case():
     for v in range(256):
         acc = f32(acc + dg_exp(f32(l[0, v] - l.max())))
     assert p["s"][0, 0] == acc
+
+
+def test_tempered_gumbel_max_samples_the_tempered_softmax():
+    # Re-noise at temperature tau samples softmax(l / tau): chi-square of the
+    # draws against it for a sharpening (0.5) and a flattening (2.0) tau; the
+    # argmax and confidence stay those of tau = 1.
+    l = np.log(np.array([0.3, 0.2, 0.15, 0.1, 0.1, 0.05, 0.05, 0.05] + [1e-30] * 248)).astype(f32)
+    for tau in (0.5, 2.0):
+        inv = f32(1.0 / tau)
+        draws = []
+        for n in range(1, 401):
+            a, conf, g, _ = position_outputs(np.broadcast_to(l, (250, 256)), 13, 0, n, inv_tau=inv)
+            draws.append(g)
+        draws = np.concatenate(draws)
+        counts = np.bincount(draws, minlength=256)[:8]
+        assert counts.sum() == len(draws)
+        expect = special.softmax(l.astype(np.float64) / tau)[:8] * len(draws)
+        assert stats.chisquare(counts, expect).pvalue > 1e-3
+        assert np.all(a == 0) and np.allclose(conf, 0.3, rtol=1e-5)
+
+
+def test_temperature_one_keys_are_the_untempered_keys_and_schedule_endpoints():
+    rng = np.random.default_rng(5)
+    l = (rng.standard_normal((4, 1024)) * 2).astype(f32)
+    a1 = position_outputs(l, 3, 1, 2)
+    a2 = position_outputs(l, 3, 1, 2, inv_tau=sampler.annealed_inv_tau(5, 48))   # default schedule: tau = 1
+    assert all(np.array_equal(x, y) for x, y in zip(a1[:3], a2[:3]))
+    assert sampler.annealed_inv_tau(1, 48, 1.5, 0.5) == f32(1 / 1.5)
+    assert sampler.annealed_inv_tau(48, 48, 1.5, 0.5) == f32(2.0)
+    taus = [1 / float(sampler.annealed_inv_tau(n, 48, 1.5, 0.5)) for n in range(1, 49)]
+    assert all(x > y for x, y in zip(taus, taus[1:]))
+    assert sampler.annealed_inv_tau(1, 1, 0.8, 0.2) == f32(1 / 0.8)
+    # a cold temperature turns the re-noise sample into the argmax where the
+    # top-2 gap times 1/tau dwarfs the Gumbel range (< 20)
+    l2 = l.copy()
+    l2[:, 17] = l.max(axis=1) + f32(1.0)
+    a, _, g, _ = position_outputs(l2, 3, 1, 2, inv_tau=f32(1000.0))
+    assert np.array_equal(g, a) and np.all(a == 17)

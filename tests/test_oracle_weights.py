@@ -41,3 +41,22 @@ def test_offsets_and_tensor_ids_are_independent_streams():
 def test_values_are_bf16():
     x = weights.elements(0, 1, 0, 10000, 0.02)
     assert np.all((x.view(np.uint32) & 0xFFFF) == 0)
+
+
+def test_lazy_weights_equal_the_eager_tensors():
+    # The full-width tests generate weights lazily (per expert, per row range);
+    # on the tiny model both forms must give the same values and the same prefill.
+    from oracle import model as om
+    cfg = om.TINY
+    W, L = weights.Weights(cfg), weights.LazyWeights(cfg)
+    ids = np.arange(0, cfg.vocab, 37)
+    assert np.array_equal(om.embed_rows(W, ids), om.embed_rows(L, ids))
+    for k in ("wq", "wk", "wv", "wo", "wr"):
+        assert np.array_equal(W.layers[1][k], L.layers[1][k])
+    for k in ("wg", "wu", "wd"):
+        for e in (0, 5, cfg.n_experts - 1):
+            assert np.array_equal(W.layers[1][k][e], L.layers[1][k][e])
+    assert np.array_equal(W.lm_head[100:164], L.lm_head.block(100, 64))
+    prompt = np.arange(64) * 13 % cfg.vocab
+    a, b = om.prefill(W, cfg, prompt), om.prefill(L, cfg, prompt)
+    assert all(np.array_equal(x, y) for x, y in zip(a.k + a.v, b.k + b.v))
