@@ -14,6 +14,13 @@ forwards between canvases.  The prompt is encoded once before timing
 (decode-only, as the pages measure); each step rewinds to it and uses a new
 sample seed.  value = denoise steps/s (Eq. 8 total steps / time); output
 tokens/s and TPF (Eq. 7, 10) are reported beside it.
+
+The same JSON line also carries, each timed on the device with CUDA events:
+the prompt encoding (prefill) of that workload; the kernel micro-ops at the
+attention shapes (256 canvas queries, 16/4 heads of 128, prefix 0 / 1k / 8k /
+32k keys), the MoE layer and LM head + sampler shapes (256 tokens, 128
+experts top-8, vocab 262144) and the all-layer KV append; and the long
+context workload (32768-token prompt, 16 canvases of 256, N = 48, paged KV).
 """
 import argparse
 import json
@@ -171,9 +178,10 @@ class OracleSample:
 
     def describe(self):
         return (f"oracle (numpy fp64 forward + fp32 sampler) on layer 0 of a denoising step "
-                f"(256-token canvas, {PROMPT}-token prefix, MoE over 128 experts) and the LM head + "
-                f"sampler for {self.head_rows} positions; step time = 30 x layer + "
-                f"{C // self.head_rows} x head")
+                f"(256-token canvas, {PROMPT}-token prefix, MoE over the experts its routing picks, "
+                f"~120 of 128 in layer 0 vs ~15 in deep layers, so 30 x layer overstates the oracle's "
+                f"step time) and the LM head + sampler for {self.head_rows} positions; "
+                f"step time = 30 x layer + {C // self.head_rows} x head")
 
 
 def reference_arm(args):
@@ -183,14 +191,22 @@ def reference_arm(args):
     smp = OracleSample()
     for _ in range(args.warmup):
         smp.run()
-    est = [smp.run() for _ in range(args.steps)]
+    walls, est = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        est.append(smp.run())
+        walls.append(time.perf_counter() - t0)
     step_s = sum(est) / len(est)
     v = 1.0 / step_s
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "denoise steps/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": sum(walls) / len(walls) * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "step": "one denoising step, estimated from a bounded sample"},
+            "config": {"workload": WORKLOAD,
+                       "step": ("a bounded sample of one denoising step (one layer + 8 LM-head rows); "
+                                "ms_per_step is the sample's measured wall time, value the denoising "
+                                "steps/s of the full step it extrapolates to")},
+            "estimated_ms_per_full_step": step_s * 1e3,
             "cpu_baseline": {"value": v, "unit": "denoise steps/s", "cores": smp.threads,
                              "kind": "oracle", "sample": smp.describe()},
             "e2e": {"value": v, "unit": "denoise steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -259,7 +275,8 @@ def gpu_arm(args):
     scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1)
     m = dgp.dg_init_model(cfg, scfg, stream=stream)
     prompt = synth.prompt_ids(PROMPT, cfg.vocab, seed=1000 + rank)
-    dgp.dg_prefill(m, prompt)
+    dgp.dg_prefill(m, prompt)                       # first call: kernel attributes, tensor maps
+    prefill = time_prefill(dgp, m, prompt, stream, cfg, tf_burst)
 
     for w in range(args.warmup):
         decode_all(dgp, m, 10_000 + w, scfg)
@@ -313,16 +330,20 @@ def gpu_arm(args):
             a = b / (prof[name][0] / 1e3 / prof[name][1]) / 1e9
             kernels[name].update(GBps=round(a, 1), frac_hbm=round(a / hbm, 4))
     if prof["lm_head"][1] and prof["lm_head"][0] > 0:
-        fl = 2 * 2.0 * C * cfg.d_model * cfg.vocab     # hi + lo halves of the split activation
+        # the method's work, 2 C d V flops; the kernel issues two MMAs per weight
+        # tile (hi and lo bf16 halves of the fp32 final-norm rows), twice that
+        fl = 2.0 * C * cfg.d_model * cfg.vocab
         a = fl / (prof["lm_head"][0] / 1e3 / prof["lm_head"][1]) / 1e12
-        kernels["lm_head"].update(TFLOPs=round(a, 1), frac_bf16_sustained=round(a / tf_sust, 4))
+        kernels["lm_head"].update(TFLOPs=round(a, 1), frac_bf16_sustained=round(a / tf_sust, 4),
+                                  flops_per_launch=fl, mma_flops_per_launch=2 * fl,
+                                  note="TFLOPs on the method's 2*C*d*V; the hi/lo split issues 2x that in MMAs")
     # the dominant kernel class of the step with a roofline: the expert FFN
     # (HBM-bound weight streaming) or the LM head (tensor-bound contraction)
     measured_in = (f"profiled step after the timed region ({pe0.elapsed_time(pe1):.0f} ms, "
                    f"{sum(pN)} denoising steps)")
     if prof["lm_head"][0] > prof["expert_ffn"][0] and "TFLOPs" in kernels.get("lm_head", {}):
         kms, n = prof["lm_head"]
-        fl = 2 * 2.0 * C * cfg.d_model * cfg.vocab
+        fl = 2.0 * C * cfg.d_model * cfg.vocab
         achieved = fl / (kms / 1e3 / n) / 1e12
         roofline = {"kernel": "lm_head", "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": tf_sust, "unit": "TFLOP/s", "frac": round(achieved / tf_sust, 4),
@@ -354,8 +375,16 @@ def gpu_arm(args):
         el = time.perf_counter() - t0
         e2e = {"value": e_steps / el, "unit": "denoise steps/s",
                "h2d_bytes_per_step": h2d // args.e2e_steps, "d2h_bytes_per_step": d2h // args.e2e_steps,
+               "calls": args.e2e_steps,
                "includes": "prefill of the 2048-token prompt + decode of 4 canvases per dg_generate call"}
     m.close()
+    del m
+
+    micro_lines, long_ctx = None, None
+    if rank == 0 and not args.no_extra:
+        micro_lines = micro_results(dgp, "all", args.micro_reps)
+        long_ctx = long_context(dgp, stream, tf_burst)
+    expert_gb = touched / n_moe * 3 * cfg.d_ff * cfg.d_model * 2 * cfg.n_layers / 1e9
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -370,12 +399,15 @@ def gpu_arm(args):
                 "data": "synthetic: seeded random-init weights, uniform random prompt ids",
                 "config": {"workload": WORKLOAD,
                            "step": "decode of 4 canvases (all denoising steps + 3 KV-append forwards), prompt cached",
-                           "l2": "inputs larger than L2: ~45.7 GB of expert weights streamed per denoising step",
+                           "l2": (f"inputs larger than L2 (129 MB): {expert_gb:.1f} GB of expert weights "
+                                  f"({touched / n_moe:.1f} experts touched per MoE launch, measured) and "
+                                  f"the 1.48 GB LM head streamed per denoising step"),
                            "parallelism": f"replicas x{world}"},
                 "output_tokens_per_s": tok_s, "tpf": tpf, "effective_steps": eff,
                 "N_k_mean": sum(allN) / len(allN),
                 "experts_touched_per_moe_launch": round(touched / n_moe, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "prefill": prefill, "micro": micro_lines, "long_context": long_ctx,
                 "clocks": clk.summary(), "gpu_launches": launches}
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -383,22 +415,58 @@ def gpu_arm(args):
     return 0
 
 
-# ---- kernel micro-benchmarks (attention and MoE + sampler micro-op shapes) ---
+# ---- prefill, kernel micro-ops and the long-context workload ---------------------
 
-def micro(args):
-    """Per-kernel timings at the micro-op shapes; one JSON line per case."""
+def causal_attention_flops(n, prefix, Hq, hd):
+    """Algorithmic flops of one layer's attention for n new tokens after
+    `prefix` cached ones, causal inside the new block: 4 Hq hd per visible pair."""
+    return 4.0 * Hq * hd * (n * prefix + n * (n + 1) / 2)
+
+
+def time_prefill(dgp, m, prompt, stream, cfg, tf_burst, chunk=2048):
+    """Device time of dg_prefill (events on the model's stream; the call also
+    syncs after each chunk), then a second prefill with per-kernel events for
+    the causal attention's rate."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dgp.dg_profile(m, 2)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    dgp.dg_prefill(m, prompt)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    dgp.dg_profile(m, 1)
+    dgp.dg_prefill(m, prompt)
+    prof = dgp.dg_profile_read(m)
+    dgp.dg_profile(m, 0)
+    n = len(prompt)
+    fl = 0.0
+    for p0 in range(0, n, chunk):      # the prompt is encoded in chunks; the last layer needs K/V only
+        fl += (cfg.n_layers - 1) * causal_attention_flops(min(chunk, n - p0), p0, cfg.n_q_heads, cfg.head_dim)
+    ams, al = prof["attention"]
+    out = {"tokens": n, "ms": round(e0.elapsed_time(e1), 3), "wall_ms": round(wall * 1e3, 3),
+           "tokens_per_s": round(n / (e0.elapsed_time(e1) / 1e3), 1)}
+    if ams > 0:
+        a = fl / (ams / 1e3) / 1e12
+        out["attention"] = {"launches": al, "ms": round(ams, 3), "TFLOPs": round(a, 1),
+                            "frac_bf16": round(a / tf_burst, 4), "flops": fl,
+                            "note": "causal; flops count visible (query, key) pairs only"}
+    out["kernels_ms"] = {k: round(v[0], 3) for k, v in prof.items() if v[1]}
+    return out
+
+
+def micro_results(dgp, which, reps):
+    """Per-kernel timings at the micro-op shapes (median of `reps` L2-flushed runs)."""
     import numpy as np
     import torch
-    import discrete_diffusion_block_gb300 as dgp
-    from discrete_diffusion_block_gb300 import build, synth
-    torch.cuda.set_device(0)
-    build.build()
-    dgp.load()
+    from discrete_diffusion_block_gb300 import synth
     hbm, tf_burst, tf_sust, src = peaks()
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > L2
 
-    def timed(fn, reps):
+    def timed(fn):
         for _ in range(3):
             fn()
         ts = []
@@ -413,7 +481,24 @@ def micro(args):
         return statistics.median(ts) / 1e3
 
     out = []
-    which = args.micro
+    if which in ("attention", "all"):
+        Hq, Hkv, hd, C_, pg = 16, 4, 128, 256, 128
+        for P in (0, 1024, 8192, 32768):
+            S = P + C_
+            n_pages = (S + pg - 1) // pg
+            kp = torch.randn(n_pages, Hkv, pg, hd, device=dev).to(torch.bfloat16)
+            vp = torch.randn(n_pages, Hkv, pg, hd, device=dev).to(torch.bfloat16)
+            q = torch.randn(C_, Hq, hd, device=dev).to(torch.bfloat16)
+            table = torch.arange(n_pages, dtype=torch.int32, device=dev)
+            o = torch.empty_like(q)
+            ws = torch.empty(max(dgp.dg_op_attention_workspace_bytes(P, C_, Hq, Hkv, hd), 1),
+                             dtype=torch.uint8, device=dev)
+            sec = timed(lambda: dgp.dg_op_canvas_attention(q, kp, vp, table, P, C_, Hq, Hkv, hd, pg,
+                                                           False, o, ws))
+            fl = 4.0 * C_ * Hq * S * hd
+            out.append({"micro": "canvas_attention", "shape": f"P={P} C={C_} Hq={Hq} Hkv={Hkv} hd={hd}",
+                        "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst})
+            del kp, vp
     if which in ("moe", "all"):
         T, d, E, k, F = 256, 2816, 128, 8, 704
         wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev)
@@ -426,13 +511,15 @@ def micro(args):
         ids = torch.empty(T, k, dtype=torch.int32, device=dev)
         gates = torch.empty(T, k, dtype=torch.float32, device=dev)
         ws = torch.empty(dgp.dg_op_moe_workspace_bytes(T, d, E, k, F), dtype=torch.uint8, device=dev)
-        sec = timed(lambda: dgp.dg_op_moe(x, wr, wgu, wd, T, d, E, k, F, y, ids, gates, ws), args.steps)
+        sec = timed(lambda: dgp.dg_op_moe(x, wr, wgu, wd, T, d, E, k, F, y, ids, gates, ws))
         touched = len(np.unique(ids.cpu().numpy()))
         byt = touched * 3 * F * d * 2 + E * d * 2
         fl = 2.0 * T * k * 3 * F * d
         out.append({"micro": "moe_layer", "shape": f"T={T} d={d} E={E} top{k} F={F}",
                     "experts_touched": touched, "ms": sec * 1e3, "GBps": byt / sec / 1e9,
-                    "frac_hbm": byt / sec / 1e9 / hbm, "TFLOPs": fl / sec / 1e12})
+                    "frac_hbm": byt / sec / 1e9 / hbm, "TFLOPs": fl / sec / 1e12,
+                    "includes": "route + scatter + expert FFN + combine"})
+        del wr, wgu, wd
     if which in ("lmhead", "all"):
         T, d, V = 256, 2816, 262144
         w = torch.empty(V * d, dtype=torch.bfloat16, device=dev)
@@ -440,46 +527,30 @@ def micro(args):
         _, xt = synth.normal_bf16((T, d), seed=2)
         x = xt.to(dev)
         part = torch.empty(dgp.partials_bytes(T, V) // 4, dtype=torch.int32, device=dev)
-        sec = timed(lambda: dgp.dg_op_lm_head_partials(x, w, T, d, V, 1, 0, 1, part), args.steps)
+        sec = timed(lambda: dgp.dg_op_lm_head_partials(x, w, T, d, V, 1, 0, 1, part))
         fl = 2.0 * T * d * V
-        out.append({"micro": "lm_head_partials", "shape": f"T={T} d={d} V={V}", "ms": sec * 1e3,
-                    "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst,
+        out.append({"micro": "lm_head_partials", "shape": f"T={T} d={d} V={V} (single bf16 activation)",
+                    "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst,
                     "GBps_weights": V * d * 2 / sec / 1e9})
+        del w
     if which in ("sampler", "all"):
-        C, V = 256, 262144
-        logits = torch.from_numpy(synth.logits(C, V, seed=1)).to(dev)
-        part = torch.empty(dgp.partials_bytes(C, V) // 4, dtype=torch.int32, device=dev)
+        C_, V = 256, 262144
+        logits = torch.from_numpy(synth.logits(C_, V, seed=1)).to(dev)
+        part = torch.empty(dgp.partials_bytes(C_, V) // 4, dtype=torch.int32, device=dev)
         sc = dgp.SamplerConfig()
-        st = [torch.zeros(C, dtype=torch.int32, device=dev) for _ in range(6)]
-        com = torch.zeros(C, dtype=torch.uint8, device=dev)
-        conf = torch.zeros(C, dtype=torch.float32, device=dev)
+        st = [torch.zeros(C_, dtype=torch.int32, device=dev) for _ in range(6)]
+        com = torch.zeros(C_, dtype=torch.uint8, device=dev)
+        conf = torch.zeros(C_, dtype=torch.float32, device=dev)
         done = torch.zeros(1, dtype=torch.int32, device=dev)
 
         def run():
-            dgp.dg_op_logits_partials(logits, C, V, 1, 0, 1, part)
-            dgp.dg_op_sampler_update(part, C, V, 1, sc, st[0], com, st[1], st[2], st[3], conf, st[4], done)
-        sec = timed(run, args.steps)
-        byt = C * V * 4
-        out.append({"micro": "sampler_materialized_logits", "shape": f"C={C} V={V}", "ms": sec * 1e3,
+            dgp.dg_op_logits_partials(logits, C_, V, 1, 0, 1, part)
+            dgp.dg_op_sampler_update(part, C_, V, 1, sc, st[0], com, st[1], st[2], st[3], conf, st[4], done)
+        sec = timed(run)
+        byt = C_ * V * 4
+        out.append({"micro": "sampler_materialized_logits", "shape": f"C={C_} V={V}", "ms": sec * 1e3,
                     "GBps": byt / sec / 1e9, "frac_hbm": byt / sec / 1e9 / hbm})
-    if which in ("attention", "all"):
-        Hq, Hkv, hd, C, pg = 16, 4, 128, 256, 128
-        for P in (0, 1024, 8192, 32768):
-            S = P + C
-            n_pages = (S + pg - 1) // pg
-            kp = torch.randn(n_pages, Hkv, pg, hd, device=dev).to(torch.bfloat16)
-            vp = torch.randn(n_pages, Hkv, pg, hd, device=dev).to(torch.bfloat16)
-            q = torch.randn(C, Hq, hd, device=dev).to(torch.bfloat16)
-            table = torch.arange(n_pages, dtype=torch.int32, device=dev)
-            o = torch.empty_like(q)
-            ws = torch.empty(max(dgp.dg_op_attention_workspace_bytes(P, C, Hq, Hkv, hd), 1),
-                             dtype=torch.uint8, device=dev)
-            sec = timed(lambda: dgp.dg_op_canvas_attention(q, kp, vp, table, P, C, Hq, Hkv, hd, pg,
-                                                           False, o, ws), args.steps)
-            fl = 4.0 * C * Hq * S * hd
-            out.append({"micro": "canvas_attention", "shape": f"P={P} C={C} Hq={Hq} Hkv={Hkv} hd={hd}",
-                        "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12,
-                        "frac_bf16": fl / sec / 1e12 / tf_burst})
+        del logits
     if which in ("kv_append", "all"):
         L, n, Hkv, hd, pg = 30, 256, 8, 128, 128
         n_pages = 32
@@ -488,13 +559,83 @@ def micro(args):
         kp = torch.zeros(L, n_pages, Hkv, pg, hd, dtype=torch.bfloat16, device=dev)
         vp = torch.zeros_like(kp)
         table = torch.arange(n_pages, dtype=torch.int32, device=dev)
-        sec = timed(lambda: dgp.dg_op_kv_append(kn, vn, kp, vp, table, L, n_pages, 2048, n, Hkv, hd, pg),
-                    args.steps)
+        sec = timed(lambda: dgp.dg_op_kv_append(kn, vn, kp, vp, table, L, n_pages, 2048, n, Hkv, hd, pg))
         byt = 2 * 2 * L * n * Hkv * hd * 2
         out.append({"micro": "kv_append", "shape": f"layers={L} tokens={n} Hkv={Hkv} hd={hd}",
                     "ms": sec * 1e3, "GBps": byt / sec / 1e9, "frac_hbm": byt / sec / 1e9 / hbm})
     for o in out:
         o["peak_source"] = src
+        for k in ("ms", "TFLOPs", "GBps", "GBps_weights"):
+            if k in o:
+                o[k] = round(o[k], 4 if k == "ms" else 1)
+        for k in ("frac_bf16", "frac_hbm"):
+            if k in o:
+                o[k] = round(o[k], 4)
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+LONG_PROMPT, LONG_CANVASES = 32768, 16
+
+
+def long_context(dgp, stream, tf_burst):
+    """The long-context workload: 32768-token random prompt, 16 canvases of
+    256, N = 48, adaptive stopping, paged KV cache (pages of 128 tokens).
+    One decode of all canvases, timed with CUDA events on the model's
+    stream, after one untimed decode of the first canvas (graph capture)."""
+    import torch
+    from discrete_diffusion_block_gb300 import synth
+    cfg = dgp.full_config(max_context=LONG_PROMPT + LONG_CANVASES * C)
+    scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1, sample_seed=50_000)
+    m = dgp.dg_init_model(cfg, scfg, stream=stream)
+    prompt = synth.prompt_ids(LONG_PROMPT, cfg.vocab, seed=77)
+    dgp.dg_prefill(m, prompt)
+    prefill = time_prefill(dgp, m, prompt, stream, cfg, tf_burst)
+    Ns, Cs = [], []
+    dgp.dg_profile(m, 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(LONG_CANVASES):
+        n, done = 0, False
+        while not done:
+            done = dgp.dg_denoise_step(m)
+            n += 1
+        Ns.append(n)
+        if k < LONG_CANVASES - 1:
+            _, valid = dgp.dg_commit_canvas(m)
+        else:
+            valid = C
+        Cs.append(valid)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    launches = int(sum(n for _, n in dgp.dg_profile_read(m).values()))
+    m.close()
+    del m
+    torch.cuda.empty_cache()
+    steps, tok = sum(Ns), sum(Cs)
+    return {"workload": (f"{LONG_PROMPT}-token random prompt, {LONG_CANVASES} canvases of {C}, N={BUDGET}, "
+                         "adaptive, paged KV (128-token pages), same decoder"),
+            "denoise_steps_per_s": round(steps / (ms / 1e3), 2),
+            "output_tokens_per_s": round(tok / (ms / 1e3), 1),
+            "decode_ms": round(ms, 1), "total_steps": steps, "total_tokens": tok,
+            "effective_steps_eq9": round(sum(n * c for n, c in zip(Ns, Cs)) / tok, 3),
+            "tpf_eq10": round(tok / (steps + LONG_CANVASES - 1), 3), "N_k": Ns,
+            "prefill": prefill, "gpu_launches": launches,
+            "note": "decode from the cached prompt, first canvas included (its CUDA graphs are captured on the fly)"}
+
+
+def micro(args):
+    """--micro: the kernel micro-ops only, one JSON line per case."""
+    import torch
+    import discrete_diffusion_block_gb300 as dgp
+    from discrete_diffusion_block_gb300 import build
+    torch.cuda.set_device(0)
+    build.build()
+    dgp.load()
+    for o in micro_results(dgp, args.micro, args.steps):
         print(json.dumps(o), flush=True)
     return 0
 
@@ -505,8 +646,11 @@ def main():
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the micro-op and long-context sections of the JSON line")
+    ap.add_argument("--micro-reps", type=int, default=10)
     ap.add_argument("--micro", default=None,
                     choices=["moe", "lmhead", "sampler", "attention", "kv_append", "all"],
                     help="kernel micro-benchmarks at the micro-op shapes instead of the decoder")

@@ -39,7 +39,8 @@ class dg_config(ctypes.Structure):
 class dg_sampler_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "canvas_len", "budget_N", "stable_steps", "adaptive", "eos_id", "commit_causal")] + [
-        ("conf_threshold", ctypes.c_float), ("sample_seed", ctypes.c_uint64)]
+        ("conf_threshold", ctypes.c_float), ("temp_start", ctypes.c_float), ("temp_end", ctypes.c_float),
+        ("sample_seed", ctypes.c_uint64)]
 
 
 class dg_stats(ctypes.Structure):
@@ -47,6 +48,7 @@ class dg_stats(ctypes.Structure):
                 ("total_steps", ctypes.c_int32), ("n_forwards", ctypes.c_int32),
                 ("effective_steps", ctypes.c_double), ("tpf", ctypes.c_double),
                 ("prefill_seconds", ctypes.c_double), ("decode_seconds", ctypes.c_double),
+                ("steps_per_s", ctypes.c_double), ("tokens_per_s", ctypes.c_double),
                 ("N_k", ctypes.POINTER(ctypes.c_int32)), ("C_k", ctypes.POINTER(ctypes.c_int32))]
 
 
@@ -83,6 +85,8 @@ class SamplerConfig:
     eos_id: int = -1
     commit_causal: int = 1
     conf_threshold: float = 0.9
+    temp_start: float = 1.0
+    temp_end: float = 1.0
     sample_seed: int = 0
 
     def to_c(self):
@@ -114,7 +118,7 @@ _SZ = ctypes.c_size_t
 _F = ctypes.c_float
 _SIGS = {
     "dg_last_error": (ctypes.c_char_p, []),
-    "dg_init_model": (_I, [ctypes.POINTER(dg_config), ctypes.POINTER(dg_sampler_config), _P,
+    "dg_init_model": (_I, [ctypes.POINTER(dg_config), ctypes.POINTER(dg_sampler_config), _P, _P,
                            ctypes.POINTER(_P)]),
     "dg_free_model": (None, [_P]),
     "dg_prefill": (_I, [_P, _P, _I]),
@@ -137,13 +141,15 @@ _SIGS = {
     "dg_profile_experts": (_I, [_P, _P, _P]),
     "dg_op_fill_weights": (_I, [_P, _U64, _U64, ctypes.c_uint32, _U64, _F, _P]),
     "dg_op_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
-    "dg_op_canvas_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
-    "dg_op_canvas_attention_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "dg_op_status": (_I, [_P]),
+    "dg_op_canvas_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "dg_op_canvas_attention_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "dg_op_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "dg_op_moe": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "dg_op_fill_moe_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _U64, _F, _P]),
-    "dg_op_lm_head_partials": (_I, [_P, _P, _I, _I, _I, _U64, _I, _I, _P, _P]),
-    "dg_op_logits_partials": (_I, [_P, _I, _I, _U64, _I, _I, _P, _P]),
+    "dg_op_lm_head_partials": (_I, [_P, _P, _P, _I, _I, _I, _U64, _I, _I, _F, _P, _P, _P]),
+    "dg_op_logits_partials": (_I, [_P, _I, _I, _U64, _I, _I, _F, _P, _P]),
+    "dg_op_gumbel_noise": (_I, [_P, _P, _U64, _P]),
     "dg_op_sampler_update": (_I, [_P, _I, _I, _I, ctypes.POINTER(dg_sampler_config), _P, _P, _P,
                                   _P, _P, _P, _P, _P, _P]),
     "dg_op_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -223,12 +229,26 @@ class Model:
             pass
 
 
-def dg_init_model(cfg, scfg=None, stream=None):
+def n_weight_tensors(cfg):
+    """Entries of dg_init_model's borrowed-weights array."""
+    return 3 + 7 * cfg.n_layers
+
+
+def dg_init_model(cfg, scfg=None, stream=None, weights=None):
+    """weights: None (seeded weights owned by the model) or a sequence of
+    n_weight_tensors(cfg) device tensors / addresses in the DG_W_* order
+    (borrowed: they must outlive the model)."""
     scfg = scfg or SamplerConfig()
     c, s = cfg.to_c(), scfg.to_c()
     h = ctypes.c_void_p()
-    _check(load().dg_init_model(ctypes.byref(c), ctypes.byref(s), _stream(stream), ctypes.byref(h)))
-    return Model(h.value, cfg, scfg)
+    arr = None
+    if weights is not None:
+        assert len(weights) == n_weight_tensors(cfg)
+        arr = (ctypes.c_void_p * len(weights))(*[_ptr(w) for w in weights])
+    _check(load().dg_init_model(ctypes.byref(c), ctypes.byref(s), arr, _stream(stream), ctypes.byref(h)))
+    model = Model(h.value, cfg, scfg)
+    model.borrowed = weights          # keeps borrowed tensors alive as long as the model
+    return model
 
 
 def dg_free_model(m):
@@ -266,6 +286,7 @@ def dg_generate(m, prompt, K_max):
     stats = dict(K=K, total_tokens=st.total_tokens, total_steps=st.total_steps,
                  n_forwards=st.n_forwards, effective_steps=st.effective_steps, tpf=st.tpf,
                  prefill_seconds=st.prefill_seconds, decode_seconds=st.decode_seconds,
+                 steps_per_s=st.steps_per_s, tokens_per_s=st.tokens_per_s,
                  N_k=Nk[:K].tolist(), C_k=Ck[:K].tolist())
     return out[:K], stats
 
@@ -368,21 +389,29 @@ def dg_op_attention_workspace_bytes(n_prefix, n_new, Hq, Hkv, hd):
     return load().dg_op_attention_workspace_bytes(n_prefix, n_new, Hq, Hkv, hd)
 
 
+def dg_op_status(stream=None):
+    """Raises DgError if a kernel-level call since the last check recorded a
+    device-side failure (bounded wait timeout, bad page index)."""
+    _check(load().dg_op_status(_stream(stream)))
+
+
 def dg_op_canvas_attention(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, Hkv, hd, page_size,
-                           causal, out, workspace, stream=None):
+                           causal, out, workspace, stream=None, n_pages=None):
+    n_pages = k_pool.shape[0] if n_pages is None else n_pages     # pools [n_pages][Hkv][pg][hd]
     _check(load().dg_op_canvas_attention(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
-                                         n_prefix, n_new, Hq, Hkv, hd, page_size, int(causal),
+                                         n_prefix, n_new, Hq, Hkv, hd, page_size, n_pages, int(causal),
                                          _ptr(out), _ptr(workspace), _nbytes(workspace),
                                          _stream(stream)))
 
 
 def dg_op_canvas_attention_noalloc(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, Hkv, hd,
-                                   page_size, causal, out, stream=None):
-    """dg_op_canvas_attention without a workspace argument (no device scratch
-    is needed: split-KV states are merged on chip)."""
+                                   page_size, causal, out, stream=None, n_pages=None):
+    """dg_op_canvas_attention without a workspace argument; allocates nothing."""
+    n_pages = k_pool.shape[0] if n_pages is None else n_pages
     _check(load().dg_op_canvas_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool),
                                                  _ptr(page_table), n_prefix, n_new, Hq, Hkv, hd,
-                                                 page_size, int(causal), _ptr(out), _stream(stream)))
+                                                 page_size, n_pages, int(causal), _ptr(out),
+                                                 _stream(stream)))
 
 
 def dg_op_moe_workspace_bytes(T, d, E, k, F):
@@ -404,14 +433,19 @@ def partials_bytes(rows, V):
     return rows * (V // 256) * 20
 
 
-def dg_op_lm_head_partials(xn, w_out, rows, d, V, seed, canvas, step, partials, stream=None):
-    _check(load().dg_op_lm_head_partials(_ptr(xn), _ptr(w_out), rows, d, V, seed, canvas, step,
-                                         _ptr(partials), _stream(stream)))
+def dg_op_lm_head_partials(xn, w_out, rows, d, V, seed, canvas, step, partials, stream=None,
+                           xn_lo=None, logits=None, inv_tau=1.0):
+    _check(load().dg_op_lm_head_partials(_ptr(xn), _ptr(xn_lo), _ptr(w_out), rows, d, V, seed, canvas,
+                                         step, inv_tau, _ptr(partials), _ptr(logits), _stream(stream)))
 
 
-def dg_op_logits_partials(logits, rows, V, seed, canvas, step, partials, stream=None):
-    _check(load().dg_op_logits_partials(_ptr(logits), rows, V, seed, canvas, step, _ptr(partials),
+def dg_op_logits_partials(logits, rows, V, seed, canvas, step, partials, stream=None, inv_tau=1.0):
+    _check(load().dg_op_logits_partials(_ptr(logits), rows, V, seed, canvas, step, inv_tau, _ptr(partials),
                                         _stream(stream)))
+
+
+def dg_op_gumbel_noise(words, out, stream=None):
+    _check(load().dg_op_gumbel_noise(_ptr(words), _ptr(out), words.numel(), _stream(stream)))
 
 
 def dg_op_sampler_update(partials, C, V, step, scfg, x, committed, last, stable, argmax, conf,

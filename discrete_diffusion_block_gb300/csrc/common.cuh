@@ -159,10 +159,12 @@ __host__ __device__ __forceinline__ uint32_t gumbel_ctr2(int canvas, int step) {
 
 // Per-step sampler parameters kept in device memory, so that a captured
 // denoising step can be replayed for every step of a canvas: Gumbel counter
-// word 2, Philox key of the sample seed, 1-based step number.
+// word 2, Philox key of the sample seed, 1-based step number, and 1 / the
+// re-noise temperature of that step.
 struct StepParams {
   uint32_t ctr2, key0, key1;
   int step;
+  float inv_tau;
 };
 
 // Merge of two adjacent ranges, L the lower vocab range.  An empty right

@@ -20,7 +20,9 @@
 #include <chrono>
 #include <cstdarg>
 #include <map>
+#include <mutex>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -72,6 +74,7 @@ double now_s() {
 struct dg_model {
   dg_config cfg;
   dg_sampler_config sc;
+  bool borrowed_weights = false;  // weights are the caller's (dg_init_model's weights[])
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   std::vector<void *> allocs;
@@ -132,10 +135,14 @@ struct dg_model {
   bool eager_step_done = false;  // the first step runs eagerly (sets kernel attributes)
   dg::StepParams *dyn_dev = nullptr, *dyn_host = nullptr;  // per-step sampler words
 
+  int alloc_count = 0;    // device allocations made by this model
+  int fail_alloc_at = 0;  // host-side fault injection: make allocation n (1-based) fail
   template <class T>
   int alloc(T **p, size_t n) {
     void *v = nullptr;
     if (n == 0) n = 1;
+    if (++alloc_count == fail_alloc_at)
+      return fail(DG_ENOMEM, "device allocation %d failed (injected by DG_FAULT_ALLOC)", alloc_count);
     if (cudaMalloc(&v, n * sizeof(T)) != cudaSuccess) {
       cudaGetLastError();
       return fail(DG_ENOMEM, "cudaMalloc of %zu bytes failed", n * sizeof(T));
@@ -273,6 +280,8 @@ int validate(const dg_config *c, const dg_sampler_config *s) {
   if (c->max_context < s->canvas_len) return fail(DG_EINVAL, "max_context smaller than one canvas");
   if (s->budget_N < 1 || s->budget_N > 65535) return fail(DG_EINVAL, "budget_N must be in [1, 65535]");
   if (s->stable_steps < 1) return fail(DG_EINVAL, "stable_steps must be >= 1");
+  if (!(s->temp_start > 0.0f) || !(s->temp_end > 0.0f))
+    return fail(DG_EINVAL, "temp_start and temp_end must be > 0");
   return DG_OK;
 }
 
@@ -342,22 +351,44 @@ int fill_model_weights(dg_model *m) {
   return DG_OK;
 }
 
-int alloc_model(dg_model *m) {
+int alloc_model(dg_model *m, const void *const *weights) {
   const dg_config &c = m->cfg;
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
   const int E = c.n_experts, F = c.d_ff, k = c.top_k, C = m->sc.canvas_len;
-  CKR(m->alloc(&m->embed, (size_t)c.vocab * d));
-  CKR(m->alloc(&m->lm_head, (size_t)c.vocab * d));
-  CKR(m->alloc(&m->final_norm, d));
   m->layers.resize(c.n_layers);
-  for (auto &W : m->layers) {
-    CKR(m->alloc(&W.wqkv, (size_t)(qd + 2 * kd) * d));
-    CKR(m->alloc(&W.wo, (size_t)d * qd));
-    CKR(m->alloc(&W.wr, (size_t)E * d));
-    CKR(m->alloc(&W.wgu, (size_t)E * 2 * F * d));
-    CKR(m->alloc(&W.wd, (size_t)E * d * F));
-    CKR(m->alloc(&W.attn_norm, d));
-    CKR(m->alloc(&W.moe_norm, d));
+  if (weights) {
+    const int n = 3 + 7 * c.n_layers;
+    for (int i = 0; i < n; ++i)
+      if (!weights[i] || ((uintptr_t)weights[i] & 15))
+        return fail(DG_EINVAL, "borrowed weight %d is null or not 16-byte aligned", i);
+    m->embed = (bf16 *)weights[DG_W_EMBED];
+    m->lm_head = (bf16 *)weights[DG_W_LM_HEAD];
+    m->final_norm = (float *)weights[DG_W_FINAL_NORM];
+    for (int L = 0; L < c.n_layers; ++L) {
+      const void *const *w = weights + 3 + 7 * L;
+      Layer &W = m->layers[L];
+      W.wqkv = (bf16 *)w[DG_W_WQKV - 3];
+      W.wo = (bf16 *)w[DG_W_WO - 3];
+      W.wr = (bf16 *)w[DG_W_ROUTER - 3];
+      W.wgu = (bf16 *)w[DG_W_GATE_UP - 3];
+      W.wd = (bf16 *)w[DG_W_DOWN - 3];
+      W.attn_norm = (float *)w[DG_W_ATTN_NORM - 3];
+      W.moe_norm = (float *)w[DG_W_MOE_NORM - 3];
+    }
+    m->borrowed_weights = true;
+  } else {
+    CKR(m->alloc(&m->embed, (size_t)c.vocab * d));
+    CKR(m->alloc(&m->lm_head, (size_t)c.vocab * d));
+    CKR(m->alloc(&m->final_norm, d));
+    for (auto &W : m->layers) {
+      CKR(m->alloc(&W.wqkv, (size_t)(qd + 2 * kd) * d));
+      CKR(m->alloc(&W.wo, (size_t)d * qd));
+      CKR(m->alloc(&W.wr, (size_t)E * d));
+      CKR(m->alloc(&W.wgu, (size_t)E * 2 * F * d));
+      CKR(m->alloc(&W.wd, (size_t)E * d * F));
+      CKR(m->alloc(&W.attn_norm, d));
+      CKR(m->alloc(&W.moe_norm, d));
+    }
   }
   m->n_pages = dg::ceil_div(c.max_context, c.page_size);
   m->layer_pool_elems = (size_t)m->n_pages * kd * c.page_size;
@@ -411,8 +442,9 @@ int alloc_model(dg_model *m) {
   CKR(m->alloc(&m->stable, C));
   CKR(m->alloc(&m->argmax, C));
   CKR(m->alloc(&m->gumbel, C));
-  CKR(m->alloc(&m->done_dev, 2));  // [0] canvas done, [1] error word of bounded device waits
-  CK(cudaMemset(m->done_dev, 0, 2 * sizeof(int)));
+  // [0] canvas done, [1] error word of bounded device waits, [2] bad page index
+  CKR(m->alloc(&m->done_dev, 3));
+  CK(cudaMemset(m->done_dev, 0, 3 * sizeof(int)));
   CKR(m->alloc(&m->committed, C));
   CKR(m->alloc(&m->conf, C));
   if (cudaMallocHost(&m->done_host, 2 * sizeof(int)) != cudaSuccess ||
@@ -463,6 +495,13 @@ int canvas_forward(dg_model *m) {
   return DG_OK;
 }
 
+// fp32(1 / tau_n) of step n under the linear annealing schedule (in double).
+float annealed_inv_tau(const dg_sampler_config &s, int n) {
+  double tau = s.temp_start;
+  if (s.budget_N > 1) tau += ((double)s.temp_end - (double)s.temp_start) * (n - 1) / (s.budget_N - 1);
+  return (float)(1.0 / tau);
+}
+
 int begin_canvas(dg_model *m) {
   if (!m->prefilled) return fail(DG_ESTATE, "dg_prefill must come first");
   if (m->canvas_done) return fail(DG_ESTATE, "canvas finished: call dg_commit_canvas");
@@ -489,7 +528,7 @@ int step_launches(dg_model *m) {
   CKR(canvas_forward(m));
   KL(DG_K_LM_HEAD, 1,
      dg::gemm_lm_head_partials(m->xn, m->xn_lo, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
-                               m->canvas_index, m->step, m->partials, m->done_dev + 1, m->stream,
+                               m->canvas_index, m->step, 1.0f, m->partials, m->done_dev + 1, m->stream,
                                m->dyn_dev));
   KL(DG_K_SAMPLER_MERGE, 1,
      dg::sampler_merge(m->partials, C, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
@@ -527,6 +566,7 @@ int denoise_impl(dg_model *m, int32_t *done) {
   m->dyn_host->key0 = (uint32_t)s.sample_seed;
   m->dyn_host->key1 = (uint32_t)(s.sample_seed >> 32);
   m->dyn_host->step = m->step;
+  m->dyn_host->inv_tau = annealed_inv_tau(s, m->step);
   CK(cudaMemcpyAsync(m->dyn_dev, m->dyn_host, sizeof(dg::StepParams), cudaMemcpyHostToDevice,
                      m->stream));
   const dg_model::StepGraph *used = nullptr;
@@ -593,14 +633,15 @@ extern "C" {
 
 const char *dg_last_error(void) { return g_err.c_str(); }
 
-int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, void *cuda_stream,
-                  dg_model **out) {
+int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, const void *const *weights,
+                  void *cuda_stream, dg_model **out) {
   if (!out) return fail(DG_EINVAL, "null out");
   *out = nullptr;
   CKR(validate(cfg, scfg));
   dg_model *m = new dg_model();
   m->cfg = *cfg;
   m->sc = *scfg;
+  if (const char *f = getenv("DG_FAULT_ALLOC")) m->fail_alloc_at = atoi(f);
   if (cuda_stream) {
     m->stream = (cudaStream_t)cuda_stream;
   } else {
@@ -611,8 +652,8 @@ int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, void *cud
     }
     m->own_stream = true;
   }
-  int r = alloc_model(m);
-  if (r == DG_OK) r = fill_model_weights(m);
+  int r = alloc_model(m, weights);
+  if (r == DG_OK && !weights) r = fill_model_weights(m);
   if (r == DG_OK) {
     cudaError_t e = dg::rope_table(m->cos_t, m->sin_t, cfg->max_context, cfg->head_dim,
                                    cfg->rope_base, m->stream);
@@ -702,6 +743,8 @@ int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_
     stats->tpf = (double)tok / (double)(steps + K - 1);
     stats->prefill_seconds = t1 - t0;
     stats->decode_seconds = t2 - t1;
+    stats->steps_per_s = t2 > t1 ? (double)steps / (t2 - t1) : 0.0;
+    stats->tokens_per_s = t2 > t1 ? (double)tok / (t2 - t1) : 0.0;
   }
   return DG_OK;
 }
@@ -928,6 +971,69 @@ int dg_profile_read(dg_model *m, double *ms, int64_t *launches) {
 
 // ---- kernel-level entry points ----------------------------------------------
 
+}  // extern "C"
+
+namespace {
+
+// Status words of the kernel-level entry points, one set per device that loads
+// the library: a bounded device-side wait that gives up writes its code to
+// [0], and the attention writes 39 to [1] for a page index outside the pools.  It is a
+// file-scope device array rather than an allocation, so that the entry points
+// that must not allocate can use it too; it is zero when the library is
+// loaded, sticky (a later kernel that sees it set skips its waits), and read
+// and cleared by dg_op_status.  Calls that overlap on the GPU share it.
+static __device__ __align__(256) int g_op_status[64];
+
+std::mutex g_status_mu;
+int *g_status_ptr[64];
+
+// Address of g_op_status on the current device.  In host code the array's
+// name is only a stand-in, so the address is looked up once per device, with
+// that device current, by the first kernel-level call made on it.
+int op_status_ptr(int **out) {
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(DG_EINVAL, "device %d: only devices 0-63 are supported", dev);
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void *p = nullptr;
+    CK(cudaGetSymbolAddress(&p, g_op_status));
+    g_status_ptr[dev] = (int *)p;
+  }
+  *out = g_status_ptr[dev];
+  return DG_OK;
+}
+
+int check_attention_args(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                         const int32_t *page_table, const uint16_t *out, int32_t n_prefix,
+                         int32_t n_new, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                         int32_t page_size, int32_t n_pages) {
+  if (!q || !k_pool || !v_pool || !page_table || !out) return fail(DG_EINVAL, "null pointer");
+  if (n_prefix < 0 || n_new < 0 || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
+      (head_dim != 64 && head_dim != 128) || page_size < 64 || page_size % 64 || n_pages < 1)
+    return fail(DG_EINVAL, "unsupported attention shape");
+  if ((int64_t)n_pages * page_size < (int64_t)n_prefix + n_new)
+    return fail(DG_EINVAL, "%d pages of %d tokens cannot hold %d keys", n_pages, page_size, n_prefix + n_new);
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dg_op_status(void *stream) {
+  int *st = nullptr;
+  CKR(op_status_ptr(&st));
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  int v[2] = {0, 0};
+  CK(cudaMemcpy(v, st, sizeof(v), cudaMemcpyDeviceToHost));
+  if (v[0] == 0 && v[1] == 0) return DG_OK;
+  CK(cudaMemset(st, 0, sizeof(v)));
+  if (v[0]) return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", v[0]);
+  return fail(DG_EINVAL, "a page table entry was outside the pools (its keys were skipped)");
+}
+
+
 int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor_id, uint64_t e0,
                        float std_dev, void *stream) {
   if (!dst && n) return fail(DG_EINVAL, "null dst");
@@ -945,16 +1051,16 @@ size_t dg_op_attention_workspace_bytes(int32_t n_prefix, int32_t n_new, int32_t 
 int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
                            const int32_t *page_table, int32_t n_prefix, int32_t n_new,
                            int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                           int32_t page_size, int32_t causal, uint16_t *out, void *workspace,
-                           size_t workspace_bytes, void *stream) {
-  if (!q || !k_pool || !v_pool || !page_table || !out) return fail(DG_EINVAL, "null pointer");
-  if (n_prefix < 0 || n_new < 0 || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
-      (head_dim != 64 && head_dim != 128) || page_size < 64 || page_size % 64)
-    return fail(DG_EINVAL, "unsupported attention shape");
-  dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, page_size, causal ? 1 : 0};
+                           int32_t page_size, int32_t n_pages, int32_t causal, uint16_t *out,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  CKR(check_attention_args(q, k_pool, v_pool, page_table, out, n_prefix, n_new, n_q_heads, n_kv_heads,
+                           head_dim, page_size, n_pages));
+  dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, page_size, causal ? 1 : 0, n_pages};
   if (workspace_bytes < dg::attention_workspace_bytes(as)) return fail(DG_EINVAL, "workspace too small");
+  int *status = nullptr;
+  CKR(op_status_ptr(&status));
   CK(dg::attention((const bf16 *)q, (const bf16 *)k_pool, (const bf16 *)v_pool, page_table, as,
-                   (bf16 *)out, workspace, workspace_bytes, (cudaStream_t)stream));
+                   (bf16 *)out, workspace, workspace_bytes, (cudaStream_t)stream, status));
   return DG_OK;
 }
 
@@ -962,14 +1068,14 @@ int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
                                    const uint16_t *v_pool, const int32_t *page_table,
                                    int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
                                    int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
-                                   int32_t causal, uint16_t *out, void *stream) {
-  if (!q || !k_pool || !v_pool || !page_table || !out) return fail(DG_EINVAL, "null pointer");
-  if (n_prefix < 0 || n_new < 0 || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
-      (head_dim != 64 && head_dim != 128) || page_size < 64 || page_size % 64)
-    return fail(DG_EINVAL, "unsupported attention shape");
-  dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, page_size, causal ? 1 : 0};
+                                   int32_t n_pages, int32_t causal, uint16_t *out, void *stream) {
+  CKR(check_attention_args(q, k_pool, v_pool, page_table, out, n_prefix, n_new, n_q_heads, n_kv_heads,
+                           head_dim, page_size, n_pages));
+  dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, page_size, causal ? 1 : 0, n_pages};
+  int *status = nullptr;  // the library's status array: no device memory of the caller's or ours
+  CKR(op_status_ptr(&status));
   CK(dg::attention((const bf16 *)q, (const bf16 *)k_pool, (const bf16 *)v_pool, page_table, as,
-                   (bf16 *)out, nullptr, 0, (cudaStream_t)stream));
+                   (bf16 *)out, nullptr, 0, (cudaStream_t)stream, status));
   return DG_OK;
 }
 
@@ -1026,13 +1132,15 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   MoeWs w = moe_layout(workspace, T, d, n_experts, top_k, d_ff);
   if (workspace_bytes < w.bytes) return fail(DG_EINVAL, "workspace too small");
   cudaStream_t st = (cudaStream_t)stream;
+  int *status = nullptr;
+  CKR(op_status_ptr(&status));
   CK(dg::moe_route((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, top_k, expert_ids, gates,
-                   w.slot_row, w.gcount, nullptr, st));
+                   w.slot_row, w.gcount, status, st));
   CK(dg::moe_scatter((const bf16 *)xn, expert_ids, w.gcount, w.slot_row, T, d, n_experts, top_k,
                      dg::kExpertTileRows, w.x_tiles, w.offs, w.work, w.n_work, w.max_work, st));
   const int rows = T * top_k;
   CK(dg::moe_ffn(w.x_tiles, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
-                 w.max_work, n_experts, d, d_ff, w.act, w.y_rows, nullptr, st));
+                 w.max_work, n_experts, d, d_ff, w.act, w.y_rows, status, st));
   CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));
   return DG_OK;
 }
@@ -1046,20 +1154,33 @@ int dg_op_fill_moe_weights(uint16_t *w_router, uint16_t *w_gate_up, uint16_t *w_
   return DG_OK;
 }
 
-int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *w_out, int32_t rows, int32_t d,
-                           int32_t V, uint64_t sample_seed, int32_t canvas, int32_t step,
-                           void *partials, void *stream) {
-  if (!xn || !w_out || !partials || rows < 1 || d % 64 || V % 256 || V < 256)
+int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *xn_lo, const uint16_t *w_out,
+                           int32_t rows, int32_t d, int32_t V, uint64_t sample_seed,
+                           int32_t canvas, int32_t step, float inv_tau, void *partials,
+                           float *logits, void *stream) {
+  if (!xn || !w_out || !partials || rows < 1 || d % 64 || V % 256 || V < 256 || !(inv_tau > 0.0f))
     return fail(DG_EINVAL, "bad arguments");
-  CK(dg::gemm_lm_head_partials((const bf16 *)xn, nullptr, (const bf16 *)w_out, rows, d, V,
-                               sample_seed, canvas, step, partials, nullptr, (cudaStream_t)stream));
+  int *status = nullptr;
+  CKR(op_status_ptr(&status));
+  CK(dg::gemm_lm_head_partials((const bf16 *)xn, (const bf16 *)xn_lo, (const bf16 *)w_out, rows, d, V,
+                               sample_seed, canvas, step, inv_tau, partials, status,
+                               (cudaStream_t)stream, nullptr, logits));
   return DG_OK;
 }
 
 int dg_op_logits_partials(const float *logits, int32_t rows, int32_t V, uint64_t sample_seed,
-                          int32_t canvas, int32_t step, void *partials, void *stream) {
-  if (!logits || !partials || rows < 1 || V % 256 || V < 256) return fail(DG_EINVAL, "bad arguments");
-  CK(dg::logits_partials(logits, rows, V, sample_seed, canvas, step, partials, (cudaStream_t)stream));
+                          int32_t canvas, int32_t step, float inv_tau, void *partials,
+                          void *stream) {
+  if (!logits || !partials || rows < 1 || V % 256 || V < 256 || !(inv_tau > 0.0f))
+    return fail(DG_EINVAL, "bad arguments");
+  CK(dg::logits_partials(logits, rows, V, sample_seed, canvas, step, inv_tau, partials,
+                         (cudaStream_t)stream));
+  return DG_OK;
+}
+
+int dg_op_gumbel_noise(const uint32_t *words, float *out, uint64_t n, void *stream) {
+  if ((!words || !out) && n) return fail(DG_EINVAL, "null pointer");
+  CK(dg::gumbel_noise(words, out, (size_t)n, (cudaStream_t)stream));
   return DG_OK;
 }
 

@@ -102,15 +102,20 @@ constexpr int kExpertTileRows = 128;  // token rows per expert work item (MMA N 
 // xn_lo (optional): low part of a hi/lo split of the fp32 normalised rows;
 // the logits are then w_out . (xn + xn_lo).
 // dyn (optional, device): stream words taken from memory instead of seed/canvas/step.
+// logits (optional, device [T][V] fp32): also written, from the same accumulators
+// the partials are reduced from.
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
-                                  int V, uint64_t seed, int canvas, int step, void *partials,
-                                  int *err, cudaStream_t st, const StepParams *dyn = nullptr);
+                                  int V, uint64_t seed, int canvas, int step, float inv_tau,
+                                  void *partials, int *err, cudaStream_t st,
+                                  const StepParams *dyn = nullptr, float *logits = nullptr);
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                 int V, float *logits, int *err, cudaStream_t st);
 
 // ---- sampler (kernels_sampler.cu) -------------------------------------------
+// out[i] = the sampler's Gumbel noise of Philox word words[i].
+cudaError_t gumbel_noise(const uint32_t *words, float *out, size_t n, cudaStream_t st);
 cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,
-                            int step, void *partials, cudaStream_t st);
+                            int step, float inv_tau, void *partials, cudaStream_t st);
 cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,
                           int *gumbel, cudaStream_t st);
 // dyn (optional, device): the step number is taken from dyn->step.
@@ -128,7 +133,8 @@ struct AttnShape {
 // ws_bytes of attention() are accepted and unused.
 size_t attention_workspace_bytes(const AttnShape &s);
 int attention_launch_count(const AttnShape &s);
-// err (optional, device): error word set when a bounded wait of the kernel gives up.
+// err (optional, device, 2 ints): err[0] is set when a bounded wait of the kernel
+// gives up, err[1] to 39 when a page index is outside the pools (its keys are skipped).
 // out_tiles: out as operand tiles (tiled_index over [n_new][Hq hd]), else
 // row-major [n_new][Hq][hd].
 cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const int *page_table,

@@ -63,7 +63,7 @@ struct AttnParams {
   float scale_log2;
   int keys_per_split;
   bf16 *out;       // unsplit launches: the output
-  int *err;        // device error word (bounded waits, bad page indices), may be null
+  int *err;        // device error words, may be null: [0] a bounded wait gave up, [1] a bad page index
   int n_pages;     // physical pages of the pools, 0 when unknown
   bf16 *final_out; // split launches: where the cluster's merge writes the output
   int out_tiles;   // outputs as operand tiles over [n_new][Hq hd] (the o-projection operand)
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int key = k_begin + 64 * i;
       int pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
       if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) {
-        if (p.err) atomicExch(p.err, 39);
+        if (p.err) atomicExch(p.err + 1, 39);  // reported, not an abort: later blocks still run
         pg_i = -1;
       }
       if (i < kAttnPages) pages[i] = pg_i;

@@ -17,11 +17,11 @@
 //                        (units n = e, e + 2, ...) while the tensor core
 //                        fills the other.  Thread = one token row, read
 //                        straight from TMEM 32 columns at a time:
-//                        pass 1 -- max / first argmax and the Gumbel-max key
-//                        (Philox words, dg_log) in ascending vocab order;
-//                        pass 2 -- the ascending fp32 sum of dg_exp(l - m).
-//                        These are exactly the canonical tile partials of the
-//                        sampler (sampler.cuh); the logits never reach HBM.
+//                        row_tile_partial (sampler.cuh), the same code the
+//                        standalone reduction of given logits runs: the
+//                        canonical tile partials of the sampler; the logits
+//                        never reach HBM (MODE 0).  MODE 1 writes the fp32
+//                        logits instead, MODE 2 both, from one accumulator.
 //
 // Every wait is bounded (about a second); a wait that gives up records an
 // error word and makes the CTA's later waits return at once.
@@ -29,6 +29,7 @@
 
 #include "gemm_tc.cuh"
 #include "internal.h"
+#include "sampler.cuh"
 
 namespace dg {
 
@@ -51,28 +52,25 @@ struct LmSmem {
   static constexpr size_t bytes = bars + (2 * kLmStages + 4) * 8 + 16 + 1024;
 };
 
-// Upper bound of the Gumbel noise of every Philox word whose top byte is b:
-// the noise -log(-log u) increases with u, so its value at the largest u of
-// the bucket, plus a margin far above the few-ulp error of dg_log, bounds
-// the whole bucket.  The Gumbel-max scan then computes the exact key only for
-// entries whose bound can beat the running maximum; the winner and its key
-// are the same as with every key computed.
-constexpr float kGumbelBoundMargin = 1e-3f;
-__device__ __forceinline__ float gumbel_bucket_bound(int b) {
-  const uint32_t w = ((uint32_t)b << 24) | 0x00FFFFFFu;
-  return fadd(gumbel(open_uniform(w)), kGumbelBoundMargin);
-}
+// One token row of an accumulator in tensor memory, 32 columns per load.
+struct TmemRowSrc {
+  uint32_t taddr;  // lane (row) and first column of the row's 256 logits
+  __device__ __forceinline__ void issue(int c, uint32_t *x) { tc::tmem_ld32(taddr + 32 * c, x); }
+  __device__ __forceinline__ void wait(uint32_t *x) { tc::tmem_ld_wait(x); }
+};
 
 struct LmArgs {
   int T, V, K;              // token rows, vocabulary, model width
-  PartialPlanes P;          // partials planes [T][V/256] (mode 0)
-  float *logits;            // [T][V] fp32 (mode 1)
+  PartialPlanes P;          // partials planes [T][V/256] (modes 0, 2)
+  float *logits;            // [T][V] fp32 (modes 1, 2)
   uint32_t ctr2, key0, key1;
-  const StepParams *dyn;    // when set, the stream words come from device memory
+  float inv_tau;            // 1 / temperature of the re-noise keys
+  const StepParams *dyn;    // when set, the stream words and inv_tau come from device memory
   int *err;
 };
 
-// MODE 0: sampler partials; MODE 1: fp32 logits.
+// MODE 0: sampler partials; MODE 1: fp32 logits; MODE 2: both, from the same
+// accumulator (so that the partials can be checked on the logits they came from).
 template <int NA, int MODE>
 __global__ void __launch_bounds__(kLmThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap ta2,
@@ -106,7 +104,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
-  if (MODE == 0 && threadIdx.x >= 64)
+  if (MODE != 1 && threadIdx.x >= 64)
     for (int b = threadIdx.x - 64; b < 256; b += kLmThreads - 64) gbound[b] = gumbel_bucket_bound(b);
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
@@ -195,10 +193,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may read
     const int row = 32 * q + lane;   // token row inside the unit
     uint32_t c2 = g.ctr2, k0 = g.key0, k1 = g.key1;
+    float inv_tau = g.inv_tau;
     if (g.dyn) {
       c2 = g.dyn->ctr2;
       k0 = g.dyn->key0;
       k1 = g.dyn->key1;
+      inv_tau = g.dyn->inv_tau;
     }
     int n = e;
     for (int u = blockIdx.x + e * gridDim.x; u < n_units; u += 2 * gridDim.x, n += 2) {
@@ -207,13 +207,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       tc::mbar_wait(acc_full + e, (n >> 1) & 1, g.err, 14, abort);
       tc::fence_after();
       const uint32_t taddr = tmem + e * kLmAccCols + ((uint32_t)(32 * q) << 16);
-      if (MODE == 1) {
+      if (MODE != 0) {
         float *dst = g.logits + (size_t)pos * g.V + (size_t)v * kVocabTile;
 #pragma unroll 1
         for (int c = 0; c < kLmAccCols / 32; ++c) {
           uint32_t x[32];
           tc::tmem_ld32(taddr + 32 * c, x);
-          tc::tmem_ld_wait();
+          tc::tmem_ld_wait(x);
           if (pos < g.T) {
             float4 *d4 = (float4 *)(dst + 32 * c);
 #pragma unroll
@@ -222,88 +222,23 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                                   __uint_as_float(x[4 * j + 2]), __uint_as_float(x[4 * j + 3]));
           }
         }
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(acc_empty + e)) : "memory");
-        continue;
       }
-      // pass 1: max / first argmax and the Gumbel-max key, ascending vocab
-      // order.  Per 32 columns: all eight Philox calls first (independent
-      // chains the scheduler can interleave), then a branch-free max scan,
-      // then exact keys only for the columns whose bound beats the running
-      // maximum -- gk only grows along the scan, so the bound against its
-      // value at the chunk start selects a superset of the columns needed.
-      float m = 0.0f, gk = 0.0f;
-      int a = 0, gi = 0;
-      const uint32_t w0 = (uint32_t)(v * (kVocabTile / 4));
-#pragma unroll 1
-      for (int c = 0; c < kLmAccCols / 32; ++c) {
-        uint32_t x[32], wd[32];
-        tc::tmem_ld32(taddr + 32 * c, x);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const U4 w = philox10(w0 + (uint32_t)(8 * c + j4), (uint32_t)pos, c2, kTagGumbel, k0, k1);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) wd[4 * j4 + jj] = w.w[jj];
-        }
-        tc::tmem_ld_wait(x);
-        int j0 = 0;
-        if (c == 0) {
-          m = __uint_as_float(x[0]);
-          gk = fadd(m, gumbel(open_uniform(wd[0])));
-          j0 = 1;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float l = __uint_as_float(x[j]);
-          const bool up = j >= j0 && l > m;
-          m = up ? l : m;
-          a = up ? 32 * c + j : a;
-        }
-        uint32_t cand = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          cand |= (j >= j0 && fadd(__uint_as_float(x[j]), gbound[wd[j] >> 24]) > gk) ? (1u << j) : 0u;
-        while (cand) {
-          const int j = __ffs(cand) - 1;
-          cand &= cand - 1;
-          uint32_t xj = 0, wj = 0;
-#pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            xj = t == j ? x[t] : xj;
-            wj = t == j ? wd[t] : wj;
-          }
-          const float key = fadd(__uint_as_float(xj), gumbel(open_uniform(wj)));
-          if (key > gk) {
-            gk = key;
-            gi = 32 * c + j;
-          }
-        }
-      }
-      // pass 2: the ascending fp32 sum of dg_exp(l - m)
-      float s = 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < kLmAccCols / 32; ++c) {
-        uint32_t x[32];
-        tc::tmem_ld32(taddr + 32 * c, x);
-        tc::tmem_ld_wait();
-        float ex[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ex[j] = dg_exp(fsub(__uint_as_float(x[j]), m));
-#pragma unroll
-        for (int j = 0; j < 32; ++j) s = fadd(s, ex[j]);
+      Partial p{};
+      if (MODE != 1) {
+        TmemRowSrc src{taddr};
+        p = row_tile_partial(src, v, (uint32_t)pos, c2, k0, k1, gbound, inv_tau);
       }
       // the accumulator is free for unit n + 2
       tc::fence_before();
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(acc_empty + e)) : "memory");
-      if (pos < g.T) {
+      if (MODE != 1 && pos < g.T) {
         const size_t o = (size_t)pos * tiles + v;
-        g.P.m[o] = m;
-        g.P.a[o] = v * kVocabTile + a;
-        g.P.s[o] = s;
-        g.P.gk[o] = gk;
-        g.P.gi[o] = v * kVocabTile + gi;
+        g.P.m[o] = p.m;
+        g.P.a[o] = p.a;
+        g.P.s[o] = p.s;
+        g.P.gk[o] = p.gk;
+        g.P.gi[o] = p.gi;
       }
     }
   }
@@ -372,20 +307,25 @@ static cudaError_t lm_head_launch(const bf16 *xn, const bf16 *xn_lo, const bf16 
   g.K = d;
   if (mode == 0)
     return xn_lo ? launch_lm_head<2, 0>(ta, ta2, tb, g, st) : launch_lm_head<1, 0>(ta, ta2, tb, g, st);
+  if (mode == 2)
+    return xn_lo ? launch_lm_head<2, 2>(ta, ta2, tb, g, st) : launch_lm_head<1, 2>(ta, ta2, tb, g, st);
   return xn_lo ? launch_lm_head<2, 1>(ta, ta2, tb, g, st) : launch_lm_head<1, 1>(ta, ta2, tb, g, st);
 }
 
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
-                                  int V, uint64_t seed, int canvas, int step, void *partials,
-                                  int *err, cudaStream_t st, const StepParams *dyn) {
+                                  int V, uint64_t seed, int canvas, int step, float inv_tau,
+                                  void *partials, int *err, cudaStream_t st, const StepParams *dyn,
+                                  float *logits) {
   LmArgs g{};
+  g.inv_tau = inv_tau;
   g.P = PartialPlanes::at(partials, T, V / kVocabTile);
+  g.logits = logits;
   g.ctr2 = gumbel_ctr2(canvas, step);
   g.key0 = (uint32_t)seed;
   g.key1 = (uint32_t)(seed >> 32);
   g.dyn = dyn;
   g.err = err;
-  return lm_head_launch(xn, xn_lo, w_out, T, d, V, g, 0, st);
+  return lm_head_launch(xn, xn_lo, w_out, T, d, V, g, logits ? 2 : 0, st);
 }
 
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,

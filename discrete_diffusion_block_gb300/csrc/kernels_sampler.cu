@@ -11,8 +11,9 @@
 // is committed (adaptive) or at the budget N, where the rest take a.
 //
 // The reduction order is fixed so that results are reproducible bit for bit:
-// 256-wide vocab tiles (sampler.cuh), merged by a balanced binary tree in
-// tile order (left = lower vocab range).
+// 256-wide vocab tiles (row_tile_partial in sampler.cuh, the same code as the
+// LM-head epilogue), merged by a balanced binary tree in tile order (left =
+// lower vocab range).
 #include "internal.h"
 #include "sampler.cuh"
 
@@ -20,29 +21,54 @@ namespace dg {
 
 namespace {
 
-constexpr int kLogitRowsPerBlock = 32;
-constexpr int kLdl = kVocabTile + 1;
+// One row of a vocabulary tile of fp32 logits in global memory.  A thread's
+// chunk of 32 logits is one 128-byte line, read as eight 16-byte loads.
+struct GlobalRowSrc {
+  const float *row;  // the tile's 256 logits
+  __device__ __forceinline__ void issue(int c, uint32_t *x) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(row + 32 * c);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 q = __ldg(p + j);
+      x[4 * j] = q.x;
+      x[4 * j + 1] = q.y;
+      x[4 * j + 2] = q.z;
+      x[4 * j + 3] = q.w;
+    }
+  }
+  __device__ __forceinline__ void wait(uint32_t *) {}
+};
 
-__global__ void __launch_bounds__(256) logits_partials_kernel(const float *logits, int rows, int V,
-                                                              uint32_t key0, uint32_t key1,
-                                                              uint32_t ctr2, PartialPlanes P) {
+constexpr int kPartialThreads = 256;
+
+// One thread per (row, vocabulary tile), tiles of a row on consecutive
+// threads; the reduction is row_tile_partial, the LM-head epilogue's code.
+__global__ void __launch_bounds__(kPartialThreads) logits_partials_kernel(const float *logits, int rows,
+                                                                          int V, uint32_t key0,
+                                                                          uint32_t key1, uint32_t ctr2,
+                                                                          float inv_tau, PartialPlanes P) {
+  __shared__ float gbound[256];
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) gbound[b] = gumbel_bucket_bound(b);
   pdl_wait();
   pdl_trigger();
-  extern __shared__ float sm[];
-  float *L = sm;
-  float *K = L + kLogitRowsPerBlock * kLdl;
-  float *rm = K + kLogitRowsPerBlock * kLdl;
-  int *ra = (int *)(rm + kLogitRowsPerBlock);
-  const int tile = blockIdx.x, r0 = blockIdx.y * kLogitRowsPerBlock;
-  const int R = min(kLogitRowsPerBlock, rows - r0);
-  const int v0 = tile * kVocabTile;
-  for (int idx = threadIdx.x; idx < R * kVocabTile; idx += blockDim.x) {
-    const int r = idx / kVocabTile, v = idx % kVocabTile;
-    L[r * kLdl + v] = logits[(size_t)(r0 + r) * V + v0 + v];
-  }
   __syncthreads();
-  PartialScratch sc{K, rm, ra};
-  block_tile_partials(L, kLdl, sc, R, v0, tile, V / kVocabTile, r0, ctr2, key0, key1, P, r0);
+  const int tiles = V / kVocabTile;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)rows * tiles) return;
+  const int r = (int)(idx / tiles), v = (int)(idx - (long long)r * tiles);
+  GlobalRowSrc src{logits + (size_t)r * V + (size_t)v * kVocabTile};
+  const Partial p = row_tile_partial(src, v, (uint32_t)r, ctr2, key0, key1, gbound, inv_tau);
+  const size_t o = (size_t)r * tiles + v;
+  P.m[o] = p.m;
+  P.a[o] = p.a;
+  P.s[o] = p.s;
+  P.gk[o] = p.gk;
+  P.gi[o] = p.gi;
+}
+
+__global__ void gumbel_noise_kernel(const uint32_t *words, float *out, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    out[i] = gumbel(open_uniform(words[i]));
 }
 
 // Balanced binary tree over the tiles of one position; one block per position.
@@ -127,17 +153,22 @@ __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum
 }  // namespace
 
 cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed, int canvas,
-                            int step, void *partials, cudaStream_t st) {
+                            int step, float inv_tau, void *partials, cudaStream_t st) {
   const int tiles = V / kVocabTile;
   const PartialPlanes P = PartialPlanes::at(partials, rows, tiles);
-  const size_t smem = (size_t)2 * kLogitRowsPerBlock * kLdl * sizeof(float) +
-                      kLogitRowsPerBlock * (sizeof(float) + sizeof(int));
-  cudaError_t e = cudaFuncSetAttribute(logits_partials_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(tiles, ceil_div(rows, kLogitRowsPerBlock));
-  return launch_pdl(logits_partials_kernel, grid, dim3(256), smem, st, logits, rows, V, (uint32_t)seed,
-                    (uint32_t)(seed >> 32), gumbel_ctr2(canvas, step), P);
+  const long long n = (long long)rows * tiles;
+  if (n <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((n + kPartialThreads - 1) / kPartialThreads);
+  return launch_pdl(logits_partials_kernel, dim3(blocks), dim3(kPartialThreads), 0, st, logits, rows, V,
+                    (uint32_t)seed, (uint32_t)(seed >> 32), gumbel_ctr2(canvas, step), inv_tau, P);
+}
+
+cudaError_t gumbel_noise(const uint32_t *words, float *out, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  size_t blocks = (n + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  gumbel_noise_kernel<<<(unsigned)blocks, 256, 0, st>>>(words, out, n);
+  return cudaGetLastError();
 }
 
 cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,

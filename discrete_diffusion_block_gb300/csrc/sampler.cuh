@@ -1,92 +1,113 @@
-// Block-level vocabulary-tile partials used both by the LM-head GEMM epilogue
-// (logits straight from the accumulators, never written to HBM) and by the
-// standalone kernel that reduces given fp32 logits.
+// The per-(row, vocabulary tile) reduction of the sampler, written once and
+// used both by the LM-head epilogue (logits read straight from the tensor
+// memory accumulator, never written to HBM) and by the standalone kernel that
+// reduces given fp32 logits, so that injected-logit tests run the decoder's
+// own reduction code.
 #pragma once
 #include "common.cuh"
 
 namespace dg {
 
-// Per-row scratch needed next to the logits tile.
-struct PartialScratch {
-  float *kap;   // [R][ldl] Gumbel keys
-  float *rm;    // [R] tile max
-  int *ra;      // [R] first argmax
-};
+// Upper bound of the Gumbel noise of every Philox word whose top byte is b:
+// the noise of word w is G(w) = -dg_log(-dg_log(open_uniform(w))), and G is
+// strictly increasing in w >> 9 over all 2^23 values (checked exhaustively on
+// the host against the oracle's fp32 transform, and the device transform
+// against the oracle's bit for bit), so its value at the largest word of the
+// bucket bounds the whole bucket.  The Gumbel-max scan computes the exact key
+// only where l + bound can beat the running maximum; as fp32 addition is
+// monotone, l + G(w) <= l + bound, and the winner and its key are the same as
+// with every key computed.
+__device__ __forceinline__ float gumbel_bucket_bound(int b) {
+  return gumbel(open_uniform(((uint32_t)b << 24) | 0x00FFFFFFu));
+}
 
-// L: shared fp32 [R][ldl] logits of one 256-wide vocab tile starting at v0;
-// row r is canvas position pos0 + r and is stored at planes row (out_row0 + r).
-// Overwrites L with dg_exp(l - m).  All threads of the block must call it.
-__device__ __forceinline__ void block_tile_partials(float *L, int ldl, PartialScratch sc, int R,
-                                                    int v0, int tile, int tiles, int pos0,
-                                                    uint32_t ctr2, uint32_t key0, uint32_t key1,
-                                                    const PartialPlanes &P, int out_row0) {
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  // 1. max and first argmax per row (order-free: value desc, index asc)
-  for (int r = warp; r < R; r += nw) {
-    float m = L[r * ldl + lane];
-    int a = lane;
+// Partials of one row of one 256-wide vocabulary tile (tile index v, vocab
+// entries 256 v .. 256 v + 255, canvas position pos):
+//   m = max logit, a = first index reaching it (ascending v),
+//   s = left-to-right fp32 sum of dg_exp(l - m),
+//   (gk, gi) = max and first argmax of fp32(l * inv_tau) + G with the Gumbel
+//              noise of the Philox words at counter (v * 64 + j / 4, pos, c2,
+//              tag) word j % 4 (inv_tau = 1: exactly l + G).
+// The 256 logits are read through `src` in eight chunks of 32:
+//   src.issue(c, x) starts loading logits 32 c .. 32 c + 31 into x (bit patterns),
+//   src.wait(x)     completes that load.
+// gbound: the 256 bucket bounds of gumbel_bucket_bound (shared memory).
+// Pass 1 per chunk: the eight Philox calls first (independent chains the
+// scheduler can interleave with the load), then a branch-free max scan, then
+// exact keys only for the columns whose bound beats the running maximum --
+// gk only grows along the scan, so the bound against its value at the chunk
+// start selects a superset of the columns needed.  Pass 2 re-reads the
+// logits for the ascending sum of dg_exp(l - m).
+template <class Src>
+__device__ __forceinline__ Partial row_tile_partial(Src &src, int v, uint32_t pos, uint32_t c2,
+                                                    uint32_t k0, uint32_t k1, const float *gbound,
+                                                    float inv_tau) {
+  float m = 0.0f, gk = 0.0f;
+  int a = 0, gi = 0;
+  const uint32_t w0 = (uint32_t)v * (kVocabTile / 4);
+#pragma unroll 1
+  for (int c = 0; c < kVocabTile / 32; ++c) {
+    uint32_t x[32], wd[32];
+    src.issue(c, x);
 #pragma unroll
-    for (int j = 1; j < kVocabTile / 32; ++j) {
-      const float l = L[r * ldl + lane + 32 * j];
-      if (l > m) {
-        m = l;
-        a = lane + 32 * j;
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const U4 w = philox10(w0 + (uint32_t)(8 * c + j4), pos, c2, kTagGumbel, k0, k1);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) wd[4 * j4 + jj] = w.w[jj];
+    }
+    src.wait(x);
+    int j0 = 0;
+    if (c == 0) {
+      m = __uint_as_float(x[0]);
+      gk = fadd(fmul(m, inv_tau), gumbel(open_uniform(wd[0])));
+      j0 = 1;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float l = __uint_as_float(x[j]);
+      const bool up = j >= j0 && l > m;
+      m = up ? l : m;
+      a = up ? 32 * c + j : a;
+    }
+    uint32_t cand = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      cand |= (j >= j0 && fadd(fmul(__uint_as_float(x[j]), inv_tau), gbound[wd[j] >> 24]) > gk) ? (1u << j) : 0u;
+    while (cand) {
+      const int j = __ffs(cand) - 1;
+      cand &= cand - 1;
+      uint32_t xj = 0, wj = 0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        xj = t == j ? x[t] : xj;
+        wj = t == j ? wd[t] : wj;
+      }
+      const float key = fadd(fmul(__uint_as_float(xj), inv_tau), gumbel(open_uniform(wj)));
+      if (key > gk) {
+        gk = key;
+        gi = 32 * c + j;
       }
     }
+  }
+  float s = 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < kVocabTile / 32; ++c) {
+    uint32_t x[32];
+    src.issue(c, x);
+    src.wait(x);
+    float ex[32];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-      const int ao = __shfl_xor_sync(0xffffffffu, a, off);
-      if (mo > m || (mo == m && ao < a)) {
-        m = mo;
-        a = ao;
-      }
-    }
-    if (lane == 0) {
-      sc.rm[r] = m;
-      sc.ra[r] = a;
-    }
-  }
-  __syncthreads();
-  // 2. elementwise: exponentials and Gumbel keys (one Philox call per 4 entries)
-  for (int idx = tid; idx < R * (kVocabTile / 4); idx += nt) {
-    const int r = idx / (kVocabTile / 4), q = idx % (kVocabTile / 4);
-    const U4 w = philox10((uint32_t)(v0 / 4 + q), (uint32_t)(pos0 + r), ctr2, kTagGumbel, key0, key1);
-    const float m = sc.rm[r];
+    for (int j = 0; j < 32; ++j) ex[j] = dg_exp(fsub(__uint_as_float(x[j]), m));
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int v = 4 * q + j;
-      const float l = L[r * ldl + v];
-      sc.kap[r * ldl + v] = fadd(l, gumbel(open_uniform(w.w[j])));
-      L[r * ldl + v] = dg_exp(fsub(l, m));
-    }
+    for (int j = 0; j < 32; ++j) s = fadd(s, ex[j]);
   }
-  __syncthreads();
-  // 3. sequential ascending sums (one thread per row) and Gumbel argmax
-  for (int r = tid; r < 2 * R; r += nt) {
-    if (r < R) {
-      float s = 0.0f;
-      for (int v = 0; v < kVocabTile; ++v) s = fadd(s, L[r * ldl + v]);
-      const size_t o = (size_t)(out_row0 + r) * tiles + tile;
-      P.m[o] = sc.rm[r];
-      P.a[o] = v0 + sc.ra[r];
-      P.s[o] = s;
-    } else {
-      const int rr = r - R;
-      float gk = sc.kap[rr * ldl];
-      int gi = 0;
-      for (int v = 1; v < kVocabTile; ++v) {
-        const float k = sc.kap[rr * ldl + v];
-        if (k > gk) {
-          gk = k;
-          gi = v;
-        }
-      }
-      const size_t o = (size_t)(out_row0 + rr) * tiles + tile;
-      P.gk[o] = gk;
-      P.gi[o] = v0 + gi;
-    }
-  }
+  Partial p;
+  p.m = m;
+  p.a = v * kVocabTile + a;
+  p.s = s;
+  p.gk = gk;
+  p.gi = v * kVocabTile + gi;
+  return p;
 }
 
 }  // namespace dg

@@ -77,8 +77,13 @@ typedef struct dg_config {
 /* Sampler of one canvas.  Commit rule: an uncommitted position commits to its
  * argmax when conf >= conf_threshold or when its argmax was unchanged for
  * stable_steps consecutive steps; every other position is re-noised with a
- * Gumbel-max sample of its softmax; the canvas stops when all positions are
- * committed (adaptive != 0) or after budget_N steps. */
+ * Gumbel-max sample of its softmax at temperature tau_n; the canvas stops
+ * when all positions are committed (adaptive != 0) or after budget_N steps.
+ * Temperature annealing (report §5, the online teacher's sampler): tau_n
+ * moves linearly from temp_start at step 1 to temp_end at step budget_N,
+ * tau_n = temp_start + (temp_end - temp_start) (n - 1) / (budget_N - 1) in
+ * double, and the Gumbel keys are fp32(l * fp32(1 / tau_n)) + G; 1.0 and 1.0
+ * sample the model's own softmax.  argmax and conf always use tau = 1. */
 typedef struct dg_sampler_config {
     int32_t canvas_len;      /* C (256 in the method; 1..1024 supported)       */
     int32_t budget_N;        /* denoising budget N (48)                        */
@@ -87,6 +92,8 @@ typedef struct dg_sampler_config {
     int32_t eos_id;          /* -1: no end-of-sequence token                   */
     int32_t commit_causal;   /* 1: causal mask inside the canvas in the KV-append forward */
     float conf_threshold;    /* 0.9                                             */
+    float temp_start;        /* re-noise temperature at step 1 (1.0; > 0)      */
+    float temp_end;          /* ... and at step budget_N (1.0; > 0)            */
     uint64_t sample_seed;    /* seed of the canvas-init and Gumbel streams     */
 } dg_sampler_config;
 
@@ -100,6 +107,8 @@ typedef struct dg_stats {
     double tpf;              /* Eq. 10                                         */
     double prefill_seconds;  /* wall time of the prompt encoding               */
     double decode_seconds;   /* wall time of the canvases (prefill excluded)   */
+    double steps_per_s;      /* total_steps / decode_seconds                   */
+    double tokens_per_s;     /* total_tokens / decode_seconds                  */
     int32_t *N_k;            /* host, caller-owned, >= K_max entries, or NULL  */
     int32_t *C_k;            /* host, caller-owned, >= K_max entries, or NULL  */
 } dg_stats;
@@ -109,13 +118,22 @@ typedef struct dg_model dg_model;
 /* Message of the last failed call on this thread ("" if none). */
 const char *dg_last_error(void);
 
-/* Create a model on the current CUDA device: allocate seeded random-init
- * bf16 weights (Philox4x32-10, see dg_op_fill_weights), the paged KV pool for
- * cfg->max_context tokens and all scratch.  `cuda_stream` (a cudaStream_t)
- * orders all of the model's work; NULL creates a private non-blocking stream.
- * On success *out owns everything until dg_free_model. */
-int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, void *cuda_stream,
-                  dg_model **out);
+/* Create a model on the current CUDA device: the paged KV pool for
+ * cfg->max_context tokens, all scratch, and the weights.  `weights` NULL:
+ * the model allocates and owns seeded random-init bf16 weights
+ * (Philox4x32-10, see dg_op_fill_weights).  Otherwise weights[] holds
+ * 3 + 7 * n_layers device pointers the model borrows (never writes or frees;
+ * they must stay valid until dg_free_model), in the order of the DG_W_*
+ * enum below: weights[0..2] = EMBED, LM_HEAD, FINAL_NORM; then for layer L,
+ * weights[3 + 7 L + j], j = 0..6 = WQKV, WO, ROUTER, W_GATE_UP, W_DOWN,
+ * ATTN_NORM, MOE_NORM, each in the physical layout dg_get_weight documents
+ * (bf16 except the fp32 norm gains; device addresses 16-byte aligned).
+ * `cuda_stream` (a cudaStream_t) orders all of the model's work; NULL
+ * creates a private non-blocking stream.  On success *out owns everything
+ * but borrowed weights until dg_free_model.  DG_ENOMEM if a device
+ * allocation fails (everything allocated so far is released). */
+int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg,
+                  const void *const *weights, void *cuda_stream, dg_model **out);
 void dg_free_model(dg_model *m);
 
 /* Encode prompt_ids[0..n) (host) with causal attention at positions 0..n-1
@@ -138,10 +156,15 @@ int dg_denoise_step(dg_model *m, int32_t *done);
  * and appends its K/V to the prefix.  DG_ESTATE if the canvas is not done. */
 int dg_commit_canvas(dg_model *m, int32_t *out_ids, int32_t *out_valid);
 
-/* Prefill + up to K_max canvases (stopping after the canvas holding the first
- * EOS); no KV-append forward follows the last canvas.  out_ids (host,
- * K_max * canvas_len entries) receives the canvases; stats (may be NULL)
- * receives Eq. 7-10.  The per-step done flag is the only device->host
+/* The whole block-diffusion generation of the report (§3.3 adaptive
+ * stopping under a budget N; §3.4 Eq. 7-10 and the single extra forward
+ * between canvases; §1 causal context encoding; blog "Once Written, a Prefix
+ * Becomes History": finished canvases become read-only prefix): prefill of
+ * the prompt, then up to K_max canvases, each denoised until done and, but
+ * for the last, committed with its KV-append forward; generation stops after
+ * the canvas holding the first EOS.  out_ids (host, K_max * canvas_len
+ * entries) receives the canvases; stats (may be NULL) receives Eq. 7-10 and
+ * the timings.  The per-step done flag is the only device->host
  * synchronisation inside the canvas loop. */
 int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_max,
                 int32_t *out_ids, dg_stats *stats);
@@ -263,6 +286,19 @@ int dg_profile_experts(dg_model *m, int64_t *experts_touched, int64_t *rows_rout
 int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor_id,
                        uint64_t e0, float std_dev, void *stream);
 
+/* Status of the kernel-level entry points (dg_op_*) on the current device.
+ * They are asynchronous on the caller's stream, so a failure inside a kernel
+ * cannot be returned by the call that launched it: a bounded device-side wait
+ * that gives up (about a second; the kernel then skips its remaining work and
+ * its outputs are not valid), or an attention page-table entry outside the
+ * pools, is recorded in a per-device status word that this call reads.  It
+ * synchronises `stream`, returns DG_ETIMEOUT (a wait gave up) or DG_EINVAL (a
+ * bad page index) when a kernel-level call since the last dg_op_status
+ * recorded one, and clears the record; DG_OK otherwise.  The record is
+ * shared by every kernel-level call on the device, and while it is set later
+ * kernel-level kernels skip their waits (their outputs are not valid). */
+int dg_op_status(void *stream);
+
 /* Canvas attention (report §1, §4; blog "Once Written..."): for every query
  * position t < n_new (absolute position n_prefix + t) and query head h,
  *   out[t][h] = softmax_j(q[t][h] . k_j / sqrt(hd)) v_j
@@ -280,36 +316,48 @@ int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor
  *            read in 64-key groups: the slots after the last key in its
  *            group (same page) are read too, weighted by zero, and must hold
  *            finite values (e.g. a zero-initialised pool)
- *   page_table device int32, >= ceil((n_prefix + n_new) / page_size) entries
+ *   page_table device int32, >= ceil((n_prefix + n_new) / page_size) entries,
+ *            each in [0, n_pages); an entry outside that range is not read
+ *            (its keys are skipped) and is reported by dg_op_status
+ *   n_pages  physical pages in each pool (>= 1, and n_pages * page_size >=
+ *            n_prefix + n_new)
  *   out      device bf16 [n_new][Hq][hd]
  * workspace: device scratch of dg_op_attention_workspace_bytes() bytes.  The
  * split-KV partial softmax states are merged on chip (the blocks of a query
  * tile exchange them through distributed shared memory), so this is 0 for
- * every shape; the argument stays for callers that size it. */
+ * every shape; the argument stays for callers that size it.  Timeouts and bad
+ * page indices are reported by dg_op_status. */
 size_t dg_op_attention_workspace_bytes(int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
                                        int32_t n_kv_heads, int32_t head_dim);
 int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
                            const int32_t *page_table, int32_t n_prefix, int32_t n_new,
                            int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                           int32_t page_size, int32_t causal, uint16_t *out, void *workspace,
-                           size_t workspace_bytes, void *stream);
+                           int32_t page_size, int32_t n_pages, int32_t causal, uint16_t *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
-/* Same computation as dg_op_canvas_attention, for callers that cannot hand
- * the library a workspace or let it allocate one: code whose device memory
- * is owned and budgeted entirely by a host framework, plugin interfaces with
- * a fixed argument list, or latency-critical loops where an allocation (which
- * may synchronise the device) is not acceptable.  The paper has no
- * counterpart; this is a property of the library, not of the method.
+/* The canvas attention for callers that cannot allocate device memory or
+ * hand the library a workspace: code whose device memory is owned and
+ * budgeted entirely by a host framework (a serving engine's memory pool), a
+ * plugin interface whose signature has no workspace argument, or a
+ * latency-critical loop in which an allocation (which may synchronise the
+ * device) is not acceptable.  The paper has no counterpart; this is a
+ * property of the library, not of the method.
  *
- * The kernel needs no device scratch (the split-KV partial states are merged
- * in distributed shared memory), so no device memory is allocated, freed or
- * held by this call, and calls on any streams may overlap.  Inputs, outputs
- * and errors as dg_op_canvas_attention. */
+ * Inputs, outputs and results as dg_op_canvas_attention.  The kernel needs no
+ * device scratch (the split-KV partial states are merged in distributed
+ * shared memory); the only device memory it touches besides its inputs and
+ * outputs is the library's status word (see dg_op_status), a file-scope
+ * device array of 256 bytes that every device loading the library holds
+ * until exit.  Nothing is allocated or freed by this call.  The first
+ * kernel-level call on a device looks up that array's device address (a
+ * host-side query, once per device), so make it before any stream capture.
+ * Calls that overlap on the GPU share the status word: a timeout recorded by
+ * one is reported to whichever reads it first. */
 int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
                                    const uint16_t *v_pool, const int32_t *page_table,
                                    int32_t n_prefix, int32_t n_new, int32_t n_q_heads,
                                    int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
-                                   int32_t causal, uint16_t *out, void *stream);
+                                   int32_t n_pages, int32_t causal, uint16_t *out, void *stream);
 
 /* Mixture-of-experts FFN (report §6 "MoE"): for each of T rows of xn
  * (device bf16 [T][d], already RMS-normalised),
@@ -331,22 +379,40 @@ int dg_op_fill_moe_weights(uint16_t *w_router, uint16_t *w_gate_up, uint16_t *w_
                            int32_t n_experts, int32_t d_ff, int32_t layer, uint64_t seed,
                            float std_dev, void *stream);
 
-/* Per-(position, vocab tile) sampler partials.  Tiles are 256 vocab entries;
- * inside tile t, in ascending v: m = max logit, a = first index reaching it,
- * s = left-to-right fp32 sum of dg_exp(l_v - m), (gk, gi) = max and first
- * argmax of l_v + G_v with Gumbel noise G_v = -dg_log(-dg_log(u)) and
- * u = (2 (w >> 9) + 1) 2^-24, w = word (v mod 4) of Philox4x32-10 at counter
- * (v div 4, position, (canvas << 16) | step, 3), key = sample seed.
+/* Per-(position, vocab tile) sampler partials (report §6 "GPU time
+ * breakdown": sampling is one of the three dominant operations; the blog's
+ * commit rule needs a full-vocabulary softmax per position).  Tiles are 256
+ * vocab entries; inside tile t, in ascending v: m = max logit, a = first
+ * index reaching it, s = left-to-right fp32 sum of dg_exp(l_v - m), (gk, gi)
+ * = max and first argmax of fp32(l_v * inv_tau) + G_v (inv_tau = 1 / temperature
+ * of the re-noise sample, 1.0 for the model's own softmax; see
+ * dg_sampler_config) with Gumbel noise G_v = -dg_log(-dg_log(u))
+ * and u = (2 (w >> 9) + 1) 2^-24, w = word (v mod 4) of Philox4x32-10 at
+ * counter (v div 4, position, (canvas << 16) | step, 3), key = sample seed.
  * Layout of `partials` (device, rows * V/256 * 20 bytes): 5 planes of
  * [rows][V/256]: m (f32), a (i32), s (f32), gk (f32), gi (i32).
- * dg_op_lm_head_partials computes logits = xn W_out^T (fp32 accumulation, the
- * logits never leave the chip) and their partials; dg_op_logits_partials
- * does the same for given fp32 logits [rows][V] (device). */
-int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *w_out, int32_t rows, int32_t d,
-                           int32_t V, uint64_t sample_seed, int32_t canvas, int32_t step,
-                           void *partials, void *stream);
+ * dg_op_lm_head_partials computes logits = (xn + xn_lo) W_out^T with fp32
+ * accumulation in tensor memory (xn_lo, device bf16 [rows][d], may be NULL:
+ * the low half of a hi/lo split of fp32 rows, as the decoder's final norm
+ * writes it) and reduces them with the decoder's own LM-head epilogue, the
+ * logits never leaving the chip; when `logits` (device fp32 [rows][V]) is not
+ * NULL the same launch also writes the logits the partials were reduced from.
+ * dg_op_logits_partials runs the same per-(row, tile) reduction code on
+ * given fp32 logits [rows][V] (device): the injected-logit entry of the
+ * sampler, bit-identical to the epilogue on the same logits. */
+int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *xn_lo, const uint16_t *w_out,
+                           int32_t rows, int32_t d, int32_t V, uint64_t sample_seed,
+                           int32_t canvas, int32_t step, float inv_tau, void *partials,
+                           float *logits, void *stream);
 int dg_op_logits_partials(const float *logits, int32_t rows, int32_t V, uint64_t sample_seed,
-                          int32_t canvas, int32_t step, void *partials, void *stream);
+                          int32_t canvas, int32_t step, float inv_tau, void *partials,
+                          void *stream);
+
+/* The sampler's Gumbel noise transform: out[i] = -dg_log(-dg_log(u)),
+ * u = (2 (words[i] >> 9) + 1) 2^-24 (device uint32 in, device fp32 out, n
+ * entries).  Test hook: lets the transform be compared with a reference over
+ * every distinct input. */
+int dg_op_gumbel_noise(const uint32_t *words, float *out, uint64_t n, void *stream);
 
 /* Merge the partials of each row by a balanced binary tree over the tiles
  * (left = lower vocab range; M = max; S = sL*exp(mL-M) + sR*exp(mR-M);

@@ -55,7 +55,7 @@ def test_null_arguments_fail_cleanly_without_a_gpu(lib):
     L = dgp.load()
     assert L.dg_prefill(None, None, 0) == dgp.DG_EINVAL
     assert L.dg_denoise_step(None, None) == dgp.DG_EINVAL
-    assert L.dg_op_canvas_attention(*([None] * 4), 0, 1, 4, 2, 64, 128, 0, None, None, 0, None) == dgp.DG_EINVAL
+    assert L.dg_op_canvas_attention(*([None] * 4), 0, 1, 4, 2, 64, 128, 2, 0, None, None, 0, None) == dgp.DG_EINVAL
     assert L.dg_op_moe(*([None] * 4), 1, 64, 4, 2, 64, None, None, None, None, 0, None) == dgp.DG_EINVAL
     assert "null" in L.dg_last_error().decode()
 

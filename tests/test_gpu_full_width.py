@@ -1,0 +1,145 @@
+"""Full-width parity of the decoder (d_model 2816, 16/8 heads of 128, 128
+experts top-8, FFN 704, vocab 262144) against the fp64 oracle.
+
+The tiny model's projections run one k-step per CTA; at full width the QKV /
+o-proj split-K GEMMs wrap their shared-memory rings (11 k-steps per CTA),
+RoPE runs at hd = 128 at positions past 2048, and the expert FFN sees the
+full expert count.  The oracle generates the same seeded weights lazily
+(oracle.weights.LazyWeights) and runs layer by layer; where the GPU's expert
+choice is a valid top-k the oracle follows it (route(forced=)).  At this
+width the router input is a 2816-element bf16 row, and the float tolerance
+(normwise 2e-2 of bf16 logits against fp32) applied to the router logits is
+the near-tie allowance: a chosen expert's logit may sit below the k-th
+largest by up to 2e-2 of the row's largest |logit|.
+
+The second test checks that the decoder's small number of experts per MoE
+launch in deep layers (random-init weights) is the model's own behaviour:
+the oracle, run free (no forced routing) on the same 30-layer model, shows
+the same collapse layer by layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import discrete_diffusion_block_gb300 as dgp
+from discrete_diffusion_block_gb300 import synth
+from gpu_util import bits_to_f32, dev, rel_err, top2_gap
+from oracle import model as om, philox, weights as ow
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+C = 256
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from discrete_diffusion_block_gb300 import build
+    build.build()
+    dgp.load()
+    torch.cuda.set_device(0)
+
+
+class _Reuse:
+    """Expert tensor whose experts are generated once per layer (the prompt
+    and the canvas pass of a layer share them)."""
+
+    def __init__(self, t):
+        self.t, self.c = t, {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.c:
+            self.c[e] = self.t[e]
+        return self.c[e]
+
+
+def _layer(W, L):
+    WL = dict(W.layers[L])
+    for k in ("wg", "wu", "wd"):
+        WL[k] = _Reuse(WL[k])
+    return WL
+
+
+def test_full_width_layers_against_oracle():
+    P, nl = 2048, 2
+    cfg = dgp.full_config(n_layers=nl, max_context=P + C)
+    m = dgp.dg_init_model(cfg, dgp.SamplerConfig(budget_N=4))
+    prompt = synth.prompt_ids(P, cfg.vocab, seed=7)
+    dgp.dg_prefill(m, prompt)
+    route_prompt0 = dgp.dg_read_routing(m, 0)          # the last layer's MoE is skipped in prefill
+    logits = torch.empty(C, cfg.vocab, dtype=torch.float32, device=dev())
+    dgp.dg_canvas_logits(m, logits)
+    st = dgp.dg_read_canvas(m)
+    route_canvas = [dgp.dg_read_routing(m, L) for L in range(nl)]
+    kv_prompt = [dgp.dg_read_kv(m, L, 0, P) for L in range(nl)]
+    kv_canvas = [dgp.dg_read_kv(m, L, P, C) for L in range(nl)]
+    rows = np.array([0, 1, 100, 128, 200, 255])
+    lg = logits.cpu().numpy()[rows]
+    m.close()
+    assert np.array_equal(st["ids"], philox.canvas_init_ids(0, 0, C, cfg.vocab))
+
+    ocfg = om.FULL.with_(n_layers=nl)
+    W = ow.LazyWeights(ocfg)
+    hp, hc = om.embed_rows(W, prompt), om.embed_rows(W, st["ids"])
+    pp, pc = np.arange(P), P + np.arange(C)
+    none = np.zeros((0, ocfg.n_kv_heads, ocfg.head_dim))
+    for L in range(nl):
+        WL = _layer(W, L)
+        tr = []
+        hp_next, k, v = om.block(hp, pp, WL, ocfg, none, none, "causal", trace=tr,
+                                 forced_routing=route_prompt0 if L == 0 else None, routing_rel_tol=TOL)
+        if L == 0:
+            mg, mx = om.routing_margin(tr[0]["n2"], WL["wr"], route_prompt0)
+            print(f"prompt routing, layer 0: {np.mean(mg >= 0):.4f} exact top-8, "
+                  f"worst margin {mg.min():.4f} (row max |logit| {mx[mg.argmin()]:.3f})")
+        # prompt K/V (layer 1's depend on all of layer 0: QKV + RoPE, attention,
+        # o-proj + residual, router, expert FFN, combine, the next norm)
+        assert rel_err(bits_to_f32(kv_prompt[L][0]), k) <= TOL, L
+        assert rel_err(bits_to_f32(kv_prompt[L][1]), v) <= TOL, L
+        hc, kc, vc = om.block(hc, pc, WL, ocfg, k, v, "bidir", forced_routing=route_canvas[L],
+                              routing_rel_tol=TOL)
+        assert rel_err(bits_to_f32(kv_canvas[L][0]), kc) <= TOL, L     # RoPE at positions 2048..2303
+        assert rel_err(bits_to_f32(kv_canvas[L][1]), vc) <= TOL, L
+        hp = hp_next
+    n = om.rmsnorm(hc[rows], W.final_norm, ocfg.rms_eps)
+    lo = np.empty((len(rows), ocfg.vocab))
+    for v0 in range(0, ocfg.vocab, 16384):
+        lo[:, v0:v0 + 16384] = n @ W.lm_head.block(v0, 16384).astype(np.float64).T
+    assert rel_err(lg, lo) <= TOL
+    clear = top2_gap(lo) > 1e-2
+    assert np.array_equal(lg.argmax(1)[clear], lo.argmax(1)[clear])
+
+
+def test_deep_layer_routing_collapse_is_the_models():
+    P, nl = 128, 30
+    cfg = dgp.full_config(max_context=P + C)
+    m = dgp.dg_init_model(cfg, dgp.SamplerConfig(budget_N=4))
+    prompt = synth.prompt_ids(P, cfg.vocab, seed=1000)
+    dgp.dg_prefill(m, prompt)
+    logits = torch.empty(C, cfg.vocab, dtype=torch.float32, device=dev())
+    dgp.dg_canvas_logits(m, logits)
+    ids = dgp.dg_read_canvas(m)["ids"]
+    gpu = [len(np.unique(dgp.dg_read_routing(m, L))) for L in range(nl)]
+    m.close()
+    del logits
+
+    ocfg = om.FULL
+    W = ow.LazyWeights(ocfg)
+    hp, hc = om.embed_rows(W, prompt), om.embed_rows(W, ids)
+    pp, pc = np.arange(P), P + np.arange(C)
+    none = np.zeros((0, ocfg.n_kv_heads, ocfg.head_dim))
+    ref = []
+    for L in range(nl):
+        WL = _layer(W, L)
+        tr = []
+        hp, k, v = om.block(hp, pp, WL, ocfg, none, none, "causal")
+        hc, _, _ = om.block(hc, pc, WL, ocfg, k, v, "bidir", trace=tr)
+        ref.append(len(np.unique(tr[0]["ids"])))
+    print("experts touched per layer, GPU:   ", gpu)
+    print("experts touched per layer, oracle:", ref)
+    gpu, ref = np.array(gpu), np.array(ref)
+    # the first layer spreads over most experts, deep layers over few, on both sides
+    assert gpu[0] >= 96 and ref[0] >= 96
+    assert ref[10:].mean() < 40 and gpu[10:].mean() < 40
+    # layer by layer the counts agree within 30% (or 5 experts)
+    assert np.all(np.abs(gpu - ref) <= np.maximum(5, 0.3 * ref)), (gpu.tolist(), ref.tolist())

@@ -110,11 +110,11 @@ def gpu_sampler(l, scfg, step, canvas, state):
                 last=last.cpu().numpy(), stable=stab.cpu().numpy(), done=bool(done.item()))
 
 
-def oracle_partials(l, seed, canvas, step, positions=None):
+def oracle_partials(l, seed, canvas, step, positions=None, inv_tau=np.float32(1.0)):
     """Partials of the rows of l, row r being canvas position positions[r]."""
     positions = np.arange(l.shape[0]) if positions is None else np.asarray(positions)
     G = dgmath.gumbel_from_uniform(philox.gumbel_uniforms(seed, canvas, step, positions, l.shape[1]))
-    return osamp.tile_partials(l, G)
+    return osamp.tile_partials(l, G, inv_tau)
 
 
 @pytest.mark.parametrize("C,V,seed", [(256, 1024, 0), (40, 768, 3), (32, 262144, 9)])
@@ -134,6 +134,19 @@ def test_sampler_partials_and_outputs_bit_exact(C, V, seed):
     for k in ("x", "committed", "last", "stable"):
         assert np.array_equal(got[k], getattr(st, k)), k
     assert got["done"] == done
+
+
+@pytest.mark.parametrize("tau", [0.5, 2.0])
+def test_tempered_sampler_partials_bit_exact(tau):
+    C, V = 64, 65536
+    l = synth.logits(C, V, seed=21)
+    inv = np.float32(1.0 / tau)
+    part = new_partials(C, V)
+    dgp.dg_op_logits_partials(torch.from_numpy(l).to(dev()), C, V, 77, 1, 9, part, inv_tau=float(inv))
+    got = partial_planes(part, C, V)
+    ref = oracle_partials(l, 77, 1, 9, inv_tau=inv)
+    for k in ("m", "a", "s", "gk", "gi"):
+        assert np.array_equal(got[k].view(np.uint32), ref[k].astype(got[k].dtype).view(np.uint32)), k
 
 
 def test_sampler_full_vocab_full_canvas_sampled_rows():
@@ -202,6 +215,95 @@ def test_lm_head_partials_against_fp64_logits(rows, d, V, sample):
     clear = top2_gap(tiles) > 1e-2
     assert np.array_equal(got["a"][sample][clear], ref["a"][clear])
     assert np.allclose(got["s"][sample], ref["s"], rtol=TOL)
+
+
+def test_gumbel_noise_matches_oracle_on_every_input():
+    # All 2^23 distinct uniforms (the low 9 bits of a word are dropped; they
+    # are random here).  With the transform strictly increasing (a CPU pin of
+    # the oracle), this makes the LM-head epilogue's per-bucket noise bound exact.
+    i = np.arange(1 << 23, dtype=np.uint32)
+    low = np.random.default_rng(0).integers(0, 512, 1 << 23, dtype=np.uint32)
+    words = torch.from_numpy(((i << np.uint32(9)) | low).view(np.int32)).to(dev())
+    out = torch.empty(1 << 23, dtype=torch.float32, device=dev())
+    dgp.dg_op_gumbel_noise(words, out)
+    u = (2 * i.astype(np.int64) + 1).astype(np.float32) * np.float32(2.0 ** -24)
+    ref = dgmath.gumbel_from_uniform(u)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def _lm_head_rows(C, d, seed, split):
+    """Final-norm-like rows: fp32 N(0, 1), as bf16 (hi) and, with `split`, the
+    bf16 rounding of the remainder (lo).  Rows 0-7 are zero (every logit is
+    exactly 0: all ties, the Gumbel winner decided by the noise alone and
+    every noise bucket a candidate); rows 8-15 are scaled by 1e-3 (near-flat
+    logits: many keys within a few ulp of the running maximum)."""
+    x = np.random.default_rng(seed).standard_normal((C, d)).astype(np.float32)
+    x[:8] = 0.0
+    x[8:16] *= np.float32(1e-3)
+    xt = torch.from_numpy(x)
+    hi = xt.to(torch.bfloat16)
+    lo = (xt - hi.float()).to(torch.bfloat16) if split else None
+    return hi.to(dev()), (lo.to(dev()) if split else None)
+
+
+@pytest.mark.parametrize("split,canvas,step,seed,rows,inv_tau", [
+    (True, 0, 1, 5, None, 1.0),                              # the decoder's hi/lo instantiation, every row
+    (False, 3, 17, (1 << 40) + 9, [0, 5, 8, 13, 16, 100, 129, 255], 1.0 / 0.7)])   # tempered re-noise keys
+def test_lm_head_epilogue_partials_bit_exact_on_its_own_logits(split, canvas, step, seed, rows, inv_tau):
+    """The decoder's fused LM-head epilogue, bit for bit: one launch writes the
+    fp32 logits and the partials reduced from the same accumulators; the
+    oracle's canonical tile partials of those logits (with the oracle's own
+    Gumbel stream) must equal them in every plane, and the partials-only
+    launch the decoder runs must equal them too."""
+    C, d, V = 256, 2816, 262144
+    w = torch.empty(V * d, dtype=torch.bfloat16, device=dev())
+    dgp.dg_op_fill_weights(w, 0, 2, 0, 0.02)
+    hi, lo = _lm_head_rows(C, d, 31 + step, split)
+    logits = torch.empty(C, V, dtype=torch.float32, device=dev())
+    inv_tau = np.float32(inv_tau)
+    both = new_partials(C, V)
+    dgp.dg_op_lm_head_partials(hi, w, C, d, V, seed, canvas, step, both, xn_lo=lo, logits=logits,
+                               inv_tau=float(inv_tau))
+    only = new_partials(C, V)
+    dgp.dg_op_lm_head_partials(hi, w, C, d, V, seed, canvas, step, only, xn_lo=lo, inv_tau=float(inv_tau))
+    injected = new_partials(C, V)
+    dgp.dg_op_logits_partials(logits, C, V, seed, canvas, step, injected, inv_tau=float(inv_tau))
+    torch.cuda.synchronize()
+    assert torch.equal(both, only)          # the decoder's partials-only launch: same bits
+    assert torch.equal(both, injected)      # the injected-logit entry: same code, same bits
+    l = logits.cpu().numpy()
+    assert np.all(l[:8] == 0.0)
+    got = partial_planes(both, C, V)
+    sample = np.arange(C) if rows is None else np.asarray(rows)
+    ref = oracle_partials(l[sample], seed, canvas, step, sample, inv_tau)
+    for k in ("m", "a", "s", "gk", "gi"):
+        assert np.array_equal(got[k][sample].view(np.uint32), ref[k].astype(got[k].dtype).view(np.uint32)), k
+    # merge + rule on the GPU against the oracle on the same logits
+    scfg = dgp.SamplerConfig(sample_seed=seed)
+    st = osamp.CanvasState(philox.canvas_init_ids(seed, canvas, C, V))
+    st.last[::3] = 7                                         # some positions one step from stable
+    st.stable[::3] = 1
+    st.committed[::11] = 1
+    x, com = torch.from_numpy(st.x.copy()).to(dev()), torch.from_numpy(st.committed.copy()).to(dev())
+    last, stab = torch.from_numpy(st.last.copy()).to(dev()), torch.from_numpy(st.stable.copy()).to(dev())
+    a = torch.zeros(C, dtype=torch.int32, device=dev())
+    conf = torch.zeros(C, dtype=torch.float32, device=dev())
+    g = torch.zeros(C, dtype=torch.int32, device=dev())
+    done = torch.zeros(1, dtype=torch.int32, device=dev())
+    dgp.dg_op_sampler_update(only, C, V, step, scfg, x, com, last, stab, a, conf, g, done)
+    torch.cuda.synchronize()
+    r = osamp.reduce_tiles(ref)
+    assert np.array_equal(a.cpu().numpy()[sample], r["a"])
+    assert np.array_equal(g.cpu().numpy()[sample], r["gi"])
+    assert np.array_equal(conf.cpu().numpy()[sample].view(np.uint32),
+                          (np.float32(1) / r["s"]).astype(np.float32).view(np.uint32))
+    assert np.all(a.cpu().numpy()[:8] == 0)                  # all-equal logits: the first index
+    if rows is None:
+        co = (np.float32(1) / r["s"]).astype(np.float32)
+        d_ref = osamp.apply_rule(st, r["a"].astype(np.int32), co, r["gi"].astype(np.int32), step, scfg.budget_N)
+        for k, t in (("x", x), ("committed", com), ("last", last), ("stable", stab)):
+            assert np.array_equal(t.cpu().numpy(), getattr(st, k)), k
+        assert bool(done.item()) == d_ref
 
 
 # ---- canvas attention -----------------------------------------------------------

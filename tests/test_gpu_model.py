@@ -122,6 +122,8 @@ def test_generate_metrics_and_free_running_report(oracle_weights):
     assert stats["total_tokens"] == ref["total_tokens"] and stats["total_steps"] == ref["total_steps"]
     assert stats["effective_steps"] == ref["effective_steps"] and stats["tpf"] == ref["tpf"]
     assert stats["n_forwards"] == 17
+    assert stats["steps_per_s"] == pytest.approx(stats["total_steps"] / stats["decode_seconds"])
+    assert stats["tokens_per_s"] == pytest.approx(stats["total_tokens"] / stats["decode_seconds"])
     ids_o, Ns, Cs, _ = ogen.generate(oracle_weights, om.TINY, ogen.SamplerConfig(budget_N=8), prompt, 2)
     assert Ns == stats["N_k"] and Cs == stats["C_k"]
     # Free-running tokens are reported, not asserted: every near-tie (router
@@ -234,4 +236,87 @@ def test_projection_weights_are_operand_tiles_of_the_logical_matrices(oracle_wei
         assert drv.cuMemcpyDtoH_v2(ctypes.c_void_p(host.ctypes.data), ctypes.c_uint64(ptr), ctypes.c_size_t(nbytes)) == 0
         phys = bits_to_f32(host)
         assert np.array_equal(untile_matrix(phys, rows, cols), ref(oracle_weights.layers[1]))
+    m.close()
+
+
+def _copy_device(dst_ptr, src_ptr, nbytes):
+    torch.cuda.synchronize()
+    drv = ctypes.CDLL("libcuda.so.1")
+    assert drv.cuMemcpyDtoD_v2(ctypes.c_uint64(dst_ptr), ctypes.c_uint64(src_ptr), ctypes.c_size_t(nbytes)) == 0
+
+
+def test_borrowed_weights_match_the_seeded_model():
+    # A caller that owns its weights hands their device pointers to
+    # dg_init_model; the model must compute exactly what the seeded one does.
+    cfg = dgp.tiny_config()
+    a = new_model()
+    borrowed = []
+    for i in range(dgp.n_weight_tensors(cfg)):
+        which, layer = (i, 0) if i < 3 else (3 + (i - 3) % 7, (i - 3) // 7)
+        ptr, nbytes = dgp.dg_get_weight(a, which, layer)
+        t = torch.empty(nbytes, dtype=torch.uint8, device=dev())
+        _copy_device(t.data_ptr(), ptr, nbytes)
+        borrowed.append(t)
+    b = dgp.dg_init_model(cfg, dgp.SamplerConfig(budget_N=8), weights=borrowed)
+    assert dgp.dg_get_weight(b, dgp.DG_W_DOWN, 1)[0] == borrowed[3 + 7 + 4].data_ptr()
+    prompt = synth.prompt_ids(P, 1024, seed=3)
+    la, lb = (torch.empty(256, 1024, dtype=torch.float32, device=dev()) for _ in range(2))
+    for m, l in ((a, la), (b, lb)):
+        dgp.dg_prefill(m, prompt)
+        dgp.dg_canvas_logits(m, l)
+    assert torch.equal(la, lb)
+    for m in (a, b):
+        dgp.dg_denoise_step(m)
+    assert all(np.array_equal(x, y) for x, y in zip(dgp.dg_read_step_outputs(a), dgp.dg_read_step_outputs(b)))
+    b.close()
+    a.close()
+    with pytest.raises(dgp.DgError) as e:
+        dgp.dg_init_model(cfg, dgp.SamplerConfig(), weights=[0] * dgp.n_weight_tensors(cfg))
+    assert e.value.code == dgp.DG_EINVAL
+
+
+def test_injected_allocation_failure_returns_enomem_and_releases(monkeypatch):
+    # Host-side fault injection: the n-th device allocation of dg_init_model
+    # fails; the call must return DG_ENOMEM and release what it had allocated.
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for n in (1, 9, 30):
+        monkeypatch.setenv("DG_FAULT_ALLOC", str(n))
+        with pytest.raises(dgp.DgError) as e:
+            new_model()
+        assert e.value.code == dgp.DG_ENOMEM and "injected" in str(e.value)
+    monkeypatch.delenv("DG_FAULT_ALLOC")
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free0 - free1 < (64 << 20)          # nothing of the failed inits is held
+    m = new_model()
+    dgp.dg_prefill(m, synth.prompt_ids(P, 1024))
+    dgp.dg_denoise_step(m)
+    m.close()
+
+
+def test_annealed_re_noise_follows_the_oracle_schedule(oracle_weights):
+    # Temperature annealing: step n's re-noise samples are drawn at tau_n
+    # (linear from 1.5 to 0.5 over the budget); teacher-forced against the
+    # oracle, the Gumbel winners must agree wherever the oracle's tempered
+    # top-2 key gap is not a near-tie.
+    m = new_model(temp_start=1.5, temp_end=0.5, budget_N=4)
+    prompt = synth.prompt_ids(P, 1024, seed=1)
+    dgp.dg_prefill(m, prompt)
+    cache = om.prefill(oracle_weights, om.TINY, prompt, routing=gpu_routing(m, skip_last=True))
+    n, done = 0, False
+    while not done:
+        pre = dgp.dg_read_canvas(m)
+        done = dgp.dg_denoise_step(m)
+        n += 1
+        a, conf, g = dgp.dg_read_step_outputs(m)
+        lo = om.canvas_logits(oracle_weights, om.TINY, cache, pre["ids"], P,
+                              routing=gpu_routing(m)).astype(np.float32)
+        inv = osamp.annealed_inv_tau(n, 4, 1.5, 0.5)
+        ao, co, go, _ = osamp.position_outputs(lo, 0, 0, n, inv_tau=inv)
+        G = dgmath.gumbel_from_uniform(philox.gumbel_uniforms(0, 0, n, np.arange(256), 1024))
+        kap = ((lo * inv).astype(np.float32) + G).astype(np.float32)
+        assert np.all((g == go) | (top2_gap(kap) < 1e-2)), n
+        assert np.all((a == ao) | (top2_gap(lo) < 1e-2)), n
+    assert n == 4
     m.close()
