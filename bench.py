@@ -5,8 +5,8 @@ Workload: the full synthetic decoder (30 layers, d_model 2816, 16/8 heads of
 weights), a 2048-token uniform-random prompt, 4 canvases of 256 tokens,
 denoising budget N = 48, adaptive stopping on, no EOS.
 
-One step = the decode of all 4 canvases from the cached prompt: every
-denoising forward (embed, 30 x {RMSNorm, QKV+RoPE, canvas attention, o-proj,
+One step = the decode of all 4 canvases from the cached prompt, each canvas
+denoised by the device-side loop (dg_denoise_canvas): every denoising forward (embed, 30 x {RMSNorm, QKV+RoPE, canvas attention, o-proj,
 RMSNorm, router, routing (top-k + sort by expert), row gather, fused expert
 FFN, combine}, final norm,
 LM head fused with the vocab reduction, sampler) plus the 3 KV-append
@@ -223,11 +223,7 @@ def decode_all(dgp, m, seed, scfg):
     dgp.dg_set_sampler(m, scfg)
     Ns, Cs = [], []
     for k in range(CANVASES):
-        n, done = 0, False
-        while not done:
-            done = dgp.dg_denoise_step(m)
-            n += 1
-        Ns.append(n)
+        Ns.append(dgp.dg_denoise_canvas(m))          # device-side loop: one sync per canvas
         if k < CANVASES - 1:
             _, valid = dgp.dg_commit_canvas(m)
         else:
@@ -598,11 +594,7 @@ def long_context(dgp, stream, tf_burst):
     torch.cuda.synchronize()
     e0.record(stream)
     for k in range(LONG_CANVASES):
-        n, done = 0, False
-        while not done:
-            done = dgp.dg_denoise_step(m)
-            n += 1
-        Ns.append(n)
+        Ns.append(dgp.dg_denoise_canvas(m))
         if k < LONG_CANVASES - 1:
             _, valid = dgp.dg_commit_canvas(m)
         else:

@@ -49,6 +49,7 @@ class dg_stats(ctypes.Structure):
                 ("effective_steps", ctypes.c_double), ("tpf", ctypes.c_double),
                 ("prefill_seconds", ctypes.c_double), ("decode_seconds", ctypes.c_double),
                 ("steps_per_s", ctypes.c_double), ("tokens_per_s", ctypes.c_double),
+                ("canvas_loop_syncs", ctypes.c_int32),
                 ("N_k", ctypes.POINTER(ctypes.c_int32)), ("C_k", ctypes.POINTER(ctypes.c_int32))]
 
 
@@ -123,6 +124,7 @@ _SIGS = {
     "dg_free_model": (None, [_P]),
     "dg_prefill": (_I, [_P, _P, _I]),
     "dg_denoise_step": (_I, [_P, _P]),
+    "dg_denoise_canvas": (_I, [_P, _P]),
     "dg_commit_canvas": (_I, [_P, _P, _P]),
     "dg_generate": (_I, [_P, _P, _I, _I, _P, ctypes.POINTER(dg_stats)]),
     "dg_set_sampler": (_I, [_P, ctypes.POINTER(dg_sampler_config)]),
@@ -142,6 +144,7 @@ _SIGS = {
     "dg_op_fill_weights": (_I, [_P, _U64, _U64, ctypes.c_uint32, _U64, _F, _P]),
     "dg_op_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "dg_op_status": (_I, [_P]),
+    "dg_op_wait_selftest": (_I, [ctypes.c_int64, _P]),
     "dg_op_canvas_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "dg_op_canvas_attention_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "dg_op_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
@@ -266,6 +269,13 @@ def dg_denoise_step(m):
     return bool(done.value)
 
 
+def dg_denoise_canvas(m):
+    """Denoise the current canvas to the end on the device; returns the steps taken."""
+    n = ctypes.c_int32()
+    _check(load().dg_denoise_canvas(m.handle, ctypes.byref(n)))
+    return n.value
+
+
 def dg_commit_canvas(m):
     ids = np.zeros(m.scfg.canvas_len, np.int32)
     valid = ctypes.c_int32()
@@ -287,6 +297,7 @@ def dg_generate(m, prompt, K_max):
                  n_forwards=st.n_forwards, effective_steps=st.effective_steps, tpf=st.tpf,
                  prefill_seconds=st.prefill_seconds, decode_seconds=st.decode_seconds,
                  steps_per_s=st.steps_per_s, tokens_per_s=st.tokens_per_s,
+                 canvas_loop_syncs=st.canvas_loop_syncs,
                  N_k=Nk[:K].tolist(), C_k=Ck[:K].tolist())
     return out[:K], stats
 
@@ -393,6 +404,10 @@ def dg_op_status(stream=None):
     """Raises DgError if a kernel-level call since the last check recorded a
     device-side failure (bounded wait timeout, bad page index)."""
     _check(load().dg_op_status(_stream(stream)))
+
+
+def dg_op_wait_selftest(limit_cycles, stream=None):
+    _check(load().dg_op_wait_selftest(limit_cycles, _stream(stream)))
 
 
 def dg_op_canvas_attention(q, k_pool, v_pool, page_table, n_prefix, n_new, Hq, Hkv, hd, page_size,

@@ -132,6 +132,15 @@ struct dg_model {
   };
   std::map<std::pair<int, int>, StepGraph> graphs;
   StepGraph *capturing = nullptr;
+  // Device-side canvas loops, one per prefix length: a graph whose WHILE
+  // node repeats the captured step until the sampler reports the canvas done.
+  struct LoopGraph {
+    cudaGraphExec_t exec = nullptr;
+    int64_t launches[DG_K_CLASSES] = {};  // kernels of one iteration
+  };
+  std::map<int, LoopGraph> loop_graphs;
+  dg::LoopCtl loop_ctl{};  // set while a loop body is being captured
+  int64_t host_syncs = 0;  // device -> host synchronisations of the canvas loops
   bool eager_step_done = false;  // the first step runs eagerly (sets kernel attributes)
   dg::StepParams *dyn_dev = nullptr, *dyn_host = nullptr;  // per-step sampler words
 
@@ -222,6 +231,9 @@ void prof_collect_graph(dg_model *m, const dg_model::StepGraph &g) {
 }
 
 void destroy_graphs(dg_model *m) {
+  for (auto &kv : m->loop_graphs)
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+  m->loop_graphs.clear();
   for (auto &kv : m->graphs) {
     if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
     for (auto &r : kv.second.recs) {
@@ -535,7 +547,7 @@ int step_launches(dg_model *m) {
   KL(DG_K_SAMPLER_RULE, 1,
      dg::sampler_rule(m->argmax, m->conf, m->gumbel, C, m->step, s.budget_N, s.stable_steps,
                       s.adaptive, s.conf_threshold, m->x, m->committed, m->last, m->stable,
-                      m->done_dev, m->stream, m->dyn_dev));
+                      m->done_dev, m->stream, m->dyn_dev, m->loop_ctl));
   return DG_OK;
 }
 
@@ -558,17 +570,23 @@ int capture_step(dg_model *m, dg_model::StepGraph *g) {
   return DG_OK;
 }
 
-int denoise_impl(dg_model *m, int32_t *done) {
-  CKR(begin_canvas(m));
+// The step words of step n of the current canvas to the device.
+int put_step_params(dg_model *m, int n) {
   const dg_sampler_config &s = m->sc;
-  m->step += 1;
-  m->dyn_host->ctr2 = dg::gumbel_ctr2(m->canvas_index, m->step);
+  m->dyn_host->ctr2 = dg::gumbel_ctr2(m->canvas_index, n);
   m->dyn_host->key0 = (uint32_t)s.sample_seed;
   m->dyn_host->key1 = (uint32_t)(s.sample_seed >> 32);
-  m->dyn_host->step = m->step;
-  m->dyn_host->inv_tau = annealed_inv_tau(s, m->step);
+  m->dyn_host->step = n;
+  m->dyn_host->inv_tau = annealed_inv_tau(s, n);
   CK(cudaMemcpyAsync(m->dyn_dev, m->dyn_host, sizeof(dg::StepParams), cudaMemcpyHostToDevice,
                      m->stream));
+  return DG_OK;
+}
+
+int denoise_impl(dg_model *m, int32_t *done) {
+  CKR(begin_canvas(m));
+  m->step += 1;
+  CKR(put_step_params(m, m->step));
   const dg_model::StepGraph *used = nullptr;
   if (!m->eager_step_done) {
     CKR(step_launches(m));
@@ -593,11 +611,95 @@ int denoise_impl(dg_model *m, int32_t *done) {
   }
   CK(cudaMemcpyAsync(m->done_host, m->done_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, m->stream));
   SYNC(m);
+  m->host_syncs += 1;
   if (used) prof_collect_graph(m, *used);
   if (m->done_host[1])
     return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", m->done_host[1]);
   m->canvas_done = m->done_host[0] != 0;
   if (done) *done = m->canvas_done ? 1 : 0;
+  return DG_OK;
+}
+
+// Capture the canvas loop for the current prefix length: a graph holding one
+// WHILE conditional node (condition 1 at launch) whose body is the step;
+// the step's rule kernel clears the condition once the canvas is done.
+int capture_loop(dg_model *m, dg_model::LoopGraph *lg) {
+  cudaGraph_t graph = nullptr;
+  CK(cudaGraphCreate(&graph, 0));
+  cudaGraphConditionalHandle h;
+  cudaError_t e = cudaGraphConditionalHandleCreate(&h, graph, 1, cudaGraphCondAssignDefault);
+  cudaGraphNodeParams cp = {};
+  cudaGraphNode_t node;
+  if (e == cudaSuccess) {
+    cp.type = cudaGraphNodeTypeConditional;
+    cp.conditional.handle = h;
+    cp.conditional.type = cudaGraphCondTypeWhile;
+    cp.conditional.size = 1;
+    e = cudaGraphAddNode(&node, graph, nullptr, nullptr, 0, &cp);
+  }
+  if (e == cudaSuccess)
+    e = cudaStreamBeginCaptureToGraph(m->stream, cp.conditional.phGraph_out[0], nullptr, nullptr, 0,
+                                      cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return fail(DG_ECUDA, "canvas loop graph: %s", cudaGetErrorString(e));
+  }
+  dg_model::StepGraph counts;  // launch counts of one iteration (no event nodes: profiling is off)
+  m->capturing = &counts;
+  m->loop_ctl = dg::LoopCtl{1, h, m->sc.temp_start, m->sc.temp_end, m->done_dev + 1};
+  const int r = step_launches(m);
+  m->loop_ctl = dg::LoopCtl{};
+  m->capturing = nullptr;
+  cudaGraph_t body = nullptr;
+  e = cudaStreamEndCapture(m->stream, &body);
+  if (r != DG_OK || e != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return r != DG_OK ? r : fail(DG_ECUDA, "canvas loop capture: %s", cudaGetErrorString(e));
+  }
+  e = cudaGraphInstantiate(&lg->exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(DG_ECUDA, "canvas loop instantiation: %s", cudaGetErrorString(e));
+  for (int i = 0; i < DG_K_CLASSES; ++i) lg->launches[i] = counts.launches[i];
+  return DG_OK;
+}
+
+// Denoise the current canvas to the end.  With profiling off and the
+// kernels' attributes set (one eager step done), every remaining step runs
+// in one launch of the device-side loop, with a single synchronisation;
+// otherwise step by step.
+int denoise_canvas_impl(dg_model *m, int32_t *n_steps) {
+  CKR(begin_canvas(m));
+  const int start = m->step;
+  if (m->prof_on || !m->eager_step_done) {
+    int32_t done = 0;
+    CKR(denoise_impl(m, &done));
+    while (!done && m->prof_on) CKR(denoise_impl(m, &done));
+    if (done) {
+      if (n_steps) *n_steps = m->step - start;
+      return DG_OK;
+    }
+  }
+  auto it = m->loop_graphs.find(m->prefix_len);
+  if (it == m->loop_graphs.end()) {
+    dg_model::LoopGraph lg;
+    CKR(capture_loop(m, &lg));
+    it = m->loop_graphs.emplace(m->prefix_len, lg).first;
+  }
+  CKR(put_step_params(m, m->step + 1));
+  CK(cudaGraphLaunch(it->second.exec, m->stream));
+  CK(cudaMemcpyAsync(m->done_host, m->done_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaMemcpyAsync(&m->dyn_host->step, &m->dyn_dev->step, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  m->host_syncs += 1;
+  if (m->done_host[1])
+    return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", m->done_host[1]);
+  const int steps = m->dyn_host->step - start;  // the loop leaves dyn at its last step
+  const int loop_steps = m->dyn_host->step - m->step;
+  for (int i = 0; i < DG_K_CLASSES; ++i) m->prof_launches[i] += it->second.launches[i] * loop_steps;
+  m->step = m->dyn_host->step;
+  m->canvas_done = m->done_host[0] != 0;
+  if (!m->canvas_done) return fail(DG_ECUDA, "the canvas loop ended before the canvas was done");
+  if (n_steps) *n_steps = steps;
   return DG_OK;
 }
 
@@ -696,6 +798,11 @@ int dg_denoise_step(dg_model *m, int32_t *done) {
   return denoise_impl(m, done);
 }
 
+int dg_denoise_canvas(dg_model *m, int32_t *n_steps) {
+  CKR(check_model(m));
+  return denoise_canvas_impl(m, n_steps);
+}
+
 int dg_commit_canvas(dg_model *m, int32_t *out_ids, int32_t *out_valid) {
   CKR(check_model(m));
   return commit_impl(m, out_ids, out_valid, true);
@@ -710,12 +817,10 @@ int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_
   CKR(prefill_impl(m, prompt, n_prompt));
   const double t1 = now_s();
   std::vector<int> Ns, Cs;
+  const int64_t syncs0 = m->host_syncs;
   for (int k = 0; k < K_max; ++k) {
-    int done = 0, n = 0;
-    while (!done) {
-      CKR(denoise_impl(m, &done));
-      ++n;
-    }
+    int n = 0;
+    CKR(denoise_canvas_impl(m, &n));
     int valid = 0;
     const bool last = (k == K_max - 1);
     CKR(commit_impl(m, out_ids + (size_t)k * C, &valid, false));
@@ -744,6 +849,7 @@ int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_
     stats->prefill_seconds = t1 - t0;
     stats->decode_seconds = t2 - t1;
     stats->steps_per_s = t2 > t1 ? (double)steps / (t2 - t1) : 0.0;
+    stats->canvas_loop_syncs = (int32_t)(m->host_syncs - syncs0);
     stats->tokens_per_s = t2 > t1 ? (double)tok / (t2 - t1) : 0.0;
   }
   return DG_OK;
@@ -755,7 +861,8 @@ int dg_set_sampler(dg_model *m, const dg_sampler_config *scfg) {
   if (scfg->canvas_len != m->sc.canvas_len) return fail(DG_EINVAL, "canvas_len is fixed at init");
   const dg_sampler_config &o = m->sc;
   if (scfg->budget_N != o.budget_N || scfg->stable_steps != o.stable_steps ||
-      scfg->adaptive != o.adaptive || scfg->conf_threshold != o.conf_threshold) {
+      scfg->adaptive != o.adaptive || scfg->conf_threshold != o.conf_threshold ||
+      scfg->temp_start != o.temp_start || scfg->temp_end != o.temp_end) {
     CK(cudaStreamSynchronize(m->stream));
     destroy_graphs(m);  // captured steps hold the old rule constants
   }
@@ -1046,6 +1153,14 @@ size_t dg_op_attention_workspace_bytes(int32_t n_prefix, int32_t n_new, int32_t 
   if (n_kv_heads < 1 || n_new < 0 || n_prefix < 0) return 0;
   dg::AttnShape as{n_prefix, n_new, n_q_heads, n_kv_heads, head_dim, 64, 0};
   return dg::attention_workspace_bytes(as);
+}
+
+int dg_op_wait_selftest(int64_t limit_cycles, void *stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t)1 << 31) return fail(DG_EINVAL, "limit_cycles out of range");
+  int *status = nullptr;
+  CKR(op_status_ptr(&status));
+  CK(dg::bounded_wait_selftest(status, (long long)limit_cycles, (cudaStream_t)stream));
+  return DG_OK;
 }
 
 int dg_op_canvas_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,

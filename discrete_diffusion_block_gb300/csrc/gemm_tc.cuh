@@ -71,15 +71,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after ~1 s, records `code` in *err and raises the
-// CTA's abort flag, after which every later wait of the CTA returns at once.
+// Bounded wait: gives up after ~1 s (or `limit` cycles), records `code` in
+// *err and raises the CTA's abort flag, after which every later wait of the
+// CTA returns at once.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int *err, int code,
-                                         volatile int *abort) {
+                                         volatile int *abort, long long limit = kWaitCycles) {
   if (*abort) return false;
   const long long t0 = clock64();
   while (!mbar_try_wait(b, parity)) {
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       if (err) atomicExch(err, code);
       *abort = 1;
       return false;

@@ -111,6 +111,10 @@ cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                 int V, float *logits, int *err, cudaStream_t st);
 
+// A bounded wait that nothing completes (kernels_gemm.cu): gives up after
+// limit_cycles and records code 99 in *err, as a kernel's timed-out wait does.
+cudaError_t bounded_wait_selftest(int *err, long long limit_cycles, cudaStream_t st);
+
 // ---- sampler (kernels_sampler.cu) -------------------------------------------
 // out[i] = the sampler's Gumbel noise of Philox word words[i].
 cudaError_t gumbel_noise(const uint32_t *words, float *out, size_t n, cudaStream_t st);
@@ -118,11 +122,23 @@ cudaError_t logits_partials(const float *logits, int rows, int V, uint64_t seed,
                             int step, float inv_tau, void *partials, cudaStream_t st);
 cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float *conf,
                           int *gumbel, cudaStream_t st);
-// dyn (optional, device): the step number is taken from dyn->step.
+// Continuation of a device-side canvas loop: the rule kernel of a step inside
+// a CUDA graph WHILE node sets the node's condition to "not done" (and to 0
+// once `err` records a bounded wait that gave up) and, when the loop goes on,
+// advances the step words in dyn to the next step (step + 1, its Gumbel
+// counter word and its annealed 1 / temperature).
+struct LoopCtl {
+  int active;                         // 0: an ordinary step
+  cudaGraphConditionalHandle handle;  // condition of the WHILE node
+  float temp_start, temp_end;         // re-noise temperature schedule
+  const int *err;                     // error word of the step's bounded waits
+};
+// dyn (optional, device): the step number is taken from dyn->step (and, in a
+// loop, the next step's words are written back to it).
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
                          int budget_N, int stable_steps, int adaptive, float conf_threshold,
                          int *x, uint8_t *committed, int *last, int *stable, int *done,
-                         cudaStream_t st, const StepParams *dyn = nullptr);
+                         cudaStream_t st, StepParams *dyn = nullptr, LoopCtl loop = LoopCtl{});
 
 // ---- attention (kernels_attn.cu) -------------------------------------------
 struct AttnShape {

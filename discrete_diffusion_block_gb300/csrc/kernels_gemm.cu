@@ -374,4 +374,29 @@ cudaError_t gemm_residual(const bf16 *act_tiles, const bf16 *w, int T, int K, in
 }
 
 
+// ---- failure detection -------------------------------------------------------
+namespace {
+
+// A wait that nothing completes: one thread initialises an mbarrier expecting
+// one arrival that never comes and waits on it with the bounded wait every
+// tensor-core kernel uses, which gives up after `limit` cycles, records code
+// 99 in the error word and raises the CTA's abort flag.  Nothing is in flight.
+__global__ void bounded_wait_selftest_kernel(int *err, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tc::mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    tc::mbar_wait(&bar, 0, err, 99, (volatile int *)&abort_flag, limit);
+  }
+}
+
+}  // namespace
+
+cudaError_t bounded_wait_selftest(int *err, long long limit_cycles, cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_cycles);
+  return cudaGetLastError();
+}
+
 }  // namespace dg

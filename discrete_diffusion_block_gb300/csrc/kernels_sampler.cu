@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(PartialPlanes P, i
 __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum, int C, int step,
                             int budget_N, int stable_steps, int adaptive, float thr, int *x,
                             uint8_t *committed, int *last, int *stable, int *done,
-                            const StepParams *dyn) {
+                            StepParams *dyn, LoopCtl loop) {
   pdl_wait();
   pdl_trigger();
   const int i = threadIdx.x;
@@ -147,7 +147,22 @@ __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum
     }
   }
   const int n_free = __syncthreads_count(!com);
-  if (i == 0) *done = (step >= budget_N || (adaptive && n_free == 0)) ? 1 : 0;
+  if (i == 0) {
+    const int d = (step >= budget_N || (adaptive && n_free == 0)) ? 1 : 0;
+    *done = d;
+    if (loop.active) {
+      const bool stop = d || (loop.err && *(volatile const int *)loop.err);
+      if (!stop && dyn) {  // the next step's words (the same schedule as the host's, in double)
+        const int nx = step + 1;
+        double tau = loop.temp_start;
+        if (budget_N > 1) tau += ((double)loop.temp_end - (double)loop.temp_start) * (nx - 1) / (budget_N - 1);
+        dyn->step = nx;
+        dyn->ctr2 = (dyn->ctr2 & 0xFFFF0000u) | (uint32_t)nx;
+        dyn->inv_tau = (float)(1.0 / tau);
+      }
+      cudaGraphSetConditional(loop.handle, stop ? 0u : 1u);
+    }
+  }
 }
 
 }  // namespace
@@ -185,11 +200,11 @@ cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
                          int budget_N, int stable_steps, int adaptive, float conf_threshold,
                          int *x, uint8_t *committed, int *last, int *stable, int *done,
-                         cudaStream_t st, const StepParams *dyn) {
+                         cudaStream_t st, StepParams *dyn, LoopCtl loop) {
   if (C > 1024) return cudaErrorInvalidValue;
   const int threads = ((C + 31) / 32) * 32;
   return launch_pdl(rule_kernel, dim3(1), dim3(threads), 0, st, argmax, conf, gumbel, C, step, budget_N,
-                    stable_steps, adaptive, conf_threshold, x, committed, last, stable, done, dyn);
+                    stable_steps, adaptive, conf_threshold, x, committed, last, stable, done, dyn, loop);
 }
 
 }  // namespace dg

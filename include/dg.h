@@ -109,6 +109,7 @@ typedef struct dg_stats {
     double decode_seconds;   /* wall time of the canvases (prefill excluded)   */
     double steps_per_s;      /* total_steps / decode_seconds                   */
     double tokens_per_s;     /* total_tokens / decode_seconds                  */
+    int32_t canvas_loop_syncs; /* device->host synchronisations of the denoising loops */
     int32_t *N_k;            /* host, caller-owned, >= K_max entries, or NULL  */
     int32_t *C_k;            /* host, caller-owned, >= K_max entries, or NULL  */
 } dg_stats;
@@ -149,6 +150,17 @@ int dg_prefill(dg_model *m, const int32_t *prompt_ids, int32_t n);
  * *done (host) receives 1 when the canvas is finished, else 0. */
 int dg_denoise_step(dg_model *m, int32_t *done);
 
+/* Denoise the current canvas until it is done (report §3.3: adaptive
+ * stopping under the budget N), as a device-side loop: a CUDA graph whose
+ * conditional WHILE node repeats the denoising step while the sampler's done
+ * flag is 0, the step's sampler advancing the step number, Gumbel counter and
+ * annealed temperature on the device; the host synchronises once, at the
+ * end.  The first step of a model (which sets kernel attributes) and steps
+ * with per-kernel profiling on (dg_profile(m, 1)) run one by one instead.
+ * The results are those of calling dg_denoise_step until it reports done.
+ * *n_steps (host, may be NULL) receives the steps taken by this call. */
+int dg_denoise_canvas(dg_model *m, int32_t *n_steps);
+
 /* Finish the current canvas: copy its ids to out_ids (host, canvas_len
  * entries, may be NULL), set *out_valid (host, may be NULL) to C_k (tokens
  * before the first EOS, report §3.4), then run the single extra forward that
@@ -164,8 +176,8 @@ int dg_commit_canvas(dg_model *m, int32_t *out_ids, int32_t *out_valid);
  * for the last, committed with its KV-append forward; generation stops after
  * the canvas holding the first EOS.  out_ids (host, K_max * canvas_len
  * entries) receives the canvases; stats (may be NULL) receives Eq. 7-10 and
- * the timings.  The per-step done flag is the only device->host
- * synchronisation inside the canvas loop. */
+ * the timings.  Each canvas is denoised as in dg_denoise_canvas: one
+ * device->host synchronisation per canvas (stats->canvas_loop_syncs). */
 int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_max,
                 int32_t *out_ids, dg_stats *stats);
 
@@ -298,6 +310,14 @@ int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor
  * shared by every kernel-level call on the device, and while it is set later
  * kernel-level kernels skip their waits (their outputs are not valid). */
 int dg_op_status(void *stream);
+
+/* Failure-detection self-test: launches one kernel that waits, with the
+ * bounded wait every tensor-core kernel of the library uses, on an mbarrier
+ * that nothing completes; after limit_cycles (1 .. 2^31 SM clock cycles) the
+ * wait gives up and records code 99 in the status word, so that the next
+ * dg_op_status on the stream returns DG_ETIMEOUT.  Nothing else is in flight
+ * and the CUDA context stays usable.  No counterpart in the paper. */
+int dg_op_wait_selftest(int64_t limit_cycles, void *stream);
 
 /* Canvas attention (report §1, §4; blog "Once Written..."): for every query
  * position t < n_new (absolute position n_prefix + t) and query head h,

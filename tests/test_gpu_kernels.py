@@ -409,3 +409,20 @@ def test_kv_append_bit_exact_with_shuffled_pages():
         vref[:, perm[p // pg], :, p % pg, :] = vn[:, t]
     assert np.array_equal(kp.cpu().numpy().view(np.uint16), pool_layout(kref))
     assert np.array_equal(vp.cpu().numpy().view(np.uint16), pool_layout(vref))
+
+
+# ---- failure detection (no GPU fault: a wait that nothing completes) -------------
+
+def test_bounded_wait_gives_up_and_reports_etimeout():
+    # The bounded wait of the tensor-core kernels, on a barrier nothing
+    # arrives at, must give up after its limit, record its code in the status
+    # word (dg_op_status -> DG_ETIMEOUT, then cleared) and leave the context
+    # usable: an attention call afterwards is still correct.
+    dgp.dg_op_status()
+    dgp.dg_op_wait_selftest(200_000)
+    with pytest.raises(dgp.DgError) as e:
+        dgp.dg_op_status()
+    assert e.value.code == dgp.DG_ETIMEOUT and "code 99" in str(e.value)
+    dgp.dg_op_status()
+    test_canvas_attention_against_fp64(1000, False, 16, 4, 128)
+    dgp.dg_op_status()

@@ -306,11 +306,12 @@ def test_annealed_re_noise_follows_the_oracle_schedule(oracle_weights):
     cache = om.prefill(oracle_weights, om.TINY, prompt, routing=gpu_routing(m, skip_last=True))
     n, done = 0, False
     while not done:
-        pre = dgp.dg_read_canvas(m)
+        # the first step initialises the canvas (x_1 from the Philox stream)
+        ids = philox.canvas_init_ids(0, 0, 256, 1024) if n == 0 else dgp.dg_read_canvas(m)["ids"]
         done = dgp.dg_denoise_step(m)
         n += 1
         a, conf, g = dgp.dg_read_step_outputs(m)
-        lo = om.canvas_logits(oracle_weights, om.TINY, cache, pre["ids"], P,
+        lo = om.canvas_logits(oracle_weights, om.TINY, cache, ids, P,
                               routing=gpu_routing(m)).astype(np.float32)
         inv = osamp.annealed_inv_tau(n, 4, 1.5, 0.5)
         ao, co, go, _ = osamp.position_outputs(lo, 0, 0, n, inv_tau=inv)
@@ -319,4 +320,46 @@ def test_annealed_re_noise_follows_the_oracle_schedule(oracle_weights):
         assert np.all((g == go) | (top2_gap(kap) < 1e-2)), n
         assert np.all((a == ao) | (top2_gap(lo) < 1e-2)), n
     assert n == 4
+    m.close()
+
+
+@pytest.mark.parametrize("skw", [dict(budget_N=8), dict(budget_N=6, temp_start=1.3, temp_end=0.6),
+                                 dict(conf_threshold=0.0)])
+def test_device_canvas_loop_matches_step_by_step(skw):
+    # The device-side loop (one graph launch per canvas, the sampler advancing
+    # the step words on the device) must reproduce the host-driven steps bit
+    # for bit: ids, commit state, step count, the last step's outputs; on the
+    # first canvas (an eager first step, then the loop) and on the next one.
+    a, b = new_model(**skw), new_model(**skw)
+    prompt = synth.prompt_ids(P, 1024, seed=4)
+    for m in (a, b):
+        dgp.dg_prefill(m, prompt)
+    for canvas in range(2):
+        n_a, done = 0, False
+        while not done:
+            done = dgp.dg_denoise_step(a)
+            n_a += 1
+        dgp.dg_profile(b, 2)
+        n_b = dgp.dg_denoise_canvas(b)
+        launches = dgp.dg_profile_read(b)
+        assert n_a == n_b
+        sa, sb = dgp.dg_read_canvas(a), dgp.dg_read_canvas(b)
+        for k in ("ids", "committed", "last", "stable"):
+            assert np.array_equal(sa[k], sb[k]), (canvas, k)
+        assert sa["step"] == sb["step"] == n_a
+        assert all(np.array_equal(x, y) for x, y in zip(dgp.dg_read_step_outputs(a), dgp.dg_read_step_outputs(b)))
+        assert launches["lm_head"][1] == n_b and launches["sampler_rule"][1] == n_b
+        if canvas == 0:
+            dgp.dg_commit_canvas(a)
+            dgp.dg_commit_canvas(b)
+    a.close()
+    b.close()
+
+
+def test_generate_synchronises_once_per_canvas():
+    m = new_model(budget_N=5)
+    out, stats = dgp.dg_generate(m, synth.prompt_ids(P, 1024, seed=1), 3)
+    assert stats["K"] == 3 and stats["N_k"] == [5, 5, 5]
+    # the first canvas's eager first step synchronises on its own
+    assert stats["canvas_loop_syncs"] == 3 + 1
     m.close()
