@@ -20,7 +20,8 @@ the prompt encoding (prefill) of that workload; the kernel micro-ops at the
 attention shapes (256 canvas queries, 16/4 heads of 128, prefix 0 / 1k / 8k /
 32k keys), the MoE layer and LM head + sampler shapes (256 tokens, 128
 experts top-8, vocab 262144) and the all-layer KV append; and the long
-context workload (32768-token prompt, 16 canvases of 256, N = 48, paged KV).
+context workload (32768-token prompt, 16 canvases of 256, N = 48, paged KV);
+and 4 such requests decoded in lockstep batches.
 """
 import argparse
 import json
@@ -38,6 +39,15 @@ METRIC = "denoise steps/s and output tokens/s per 256-token canvas on 1 GB300; %
 PROMPT, CANVASES, BUDGET, C = 2048, 4, 48, 256
 WORKLOAD = ("full synthetic decoder (30 layers, d_model 2816, 16/8 heads x 128, 128 experts top-8, "
             "FFN 704, vocab 262144), 2048-token random prompt, 4 canvases of 256, N=48, adaptive")
+
+
+T_START = time.perf_counter()
+VERBOSE = os.environ.get("DG_BENCH_VERBOSE") == "1"
+
+
+def log(msg):
+    """Progress of the run on stderr (the JSON line alone goes to stdout)."""
+    print(f"[bench {time.perf_counter() - T_START:7.1f}s] {msg}", file=sys.stderr, flush=True)
 
 
 def peaks():
@@ -224,6 +234,8 @@ def decode_all(dgp, m, seed, scfg):
     Ns, Cs = [], []
     for k in range(CANVASES):
         Ns.append(dgp.dg_denoise_canvas(m))          # device-side loop: one sync per canvas
+        if VERBOSE:
+            log(f"canvas {k}: {Ns[-1]} steps")
         if k < CANVASES - 1:
             _, valid = dgp.dg_commit_canvas(m)
         else:
@@ -270,12 +282,15 @@ def gpu_arm(args):
     cfg = dgp.full_config(max_context=PROMPT + CANVASES * C)
     scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1)
     m = dgp.dg_init_model(cfg, scfg, stream=stream)
+    log("model initialised")
     prompt = synth.prompt_ids(PROMPT, cfg.vocab, seed=1000 + rank)
     dgp.dg_prefill(m, prompt)                       # first call: kernel attributes, tensor maps
     prefill = time_prefill(dgp, m, prompt, stream, cfg, tf_burst)
+    log("prefill timed")
 
     for w in range(args.warmup):
         decode_all(dgp, m, 10_000 + w, scfg)
+        log(f"warm-up decode {w + 1} of {args.warmup}")
 
     # ---- timed region: the value (launch counting only, no per-kernel events)
     dgp.dg_profile(m, 2)
@@ -295,6 +310,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
     launches = int(sum(n for _, n in dgp.dg_profile_read(m).values()))
     ms = ev0.elapsed_time(ev1)
+    log(f"timed region: {args.steps} decodes in {ms:.0f} ms")
     ms_max = reduce_over_ranks(pg, ms, "max", rdev)
     steps_total = reduce_over_ranks(pg, sum(allN), "sum", rdev)
     tokens_total = reduce_over_ranks(pg, sum(allC), "sum", rdev)
@@ -313,7 +329,8 @@ def gpu_arm(args):
     prof = dgp.dg_profile_read(m)
     touched, routed = dgp.dg_profile_experts(m)
     dgp.dg_profile(m, 0)
-    n_moe = max(prof["route"][1] // 2, 1)                    # routing + row gather per MoE
+    log("profiled decode done")
+    n_moe = max(prof["expert_ffn"][1], 1)                    # one expert-FFN launch per MoE layer
     per_launch = expert_bytes(cfg, touched / n_moe, routed / n_moe)
     hbm, tf_burst, tf_sust, peak_src = peaks()
     kernels = {}
@@ -373,19 +390,25 @@ def gpu_arm(args):
                "h2d_bytes_per_step": h2d // args.e2e_steps, "d2h_bytes_per_step": d2h // args.e2e_steps,
                "calls": args.e2e_steps,
                "includes": "prefill of the 2048-token prompt + decode of 4 canvases per dg_generate call"}
+    log("end-to-end calls done")
     m.close()
     del m
 
-    micro_lines, long_ctx = None, None
+    micro_lines, long_ctx, batch = None, None, None
     if rank == 0 and not args.no_extra:
         micro_lines = micro_results(dgp, "all", args.micro_reps)
+        log("micro-ops done")
         long_ctx = long_context(dgp, stream, tf_burst)
+        log("long context done")
+        batch = batched(dgp, stream)
+        log("batched done")
     expert_gb = touched / n_moe * 3 * cfg.d_ff * cfg.d_model * 2 * cfg.n_layers / 1e9
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample()
         est = smp.run()
+        log("CPU baseline sample done")
         cpu = {"value": 1.0 / est, "unit": "denoise steps/s", "cores": smp.threads, "kind": "oracle",
                "sample": smp.describe()}
     if rank == 0:
@@ -403,7 +426,7 @@ def gpu_arm(args):
                 "N_k_mean": sum(allN) / len(allN),
                 "experts_touched_per_moe_launch": round(touched / n_moe, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "prefill": prefill, "micro": micro_lines, "long_context": long_ctx,
+                "prefill": prefill, "micro": micro_lines, "long_context": long_ctx, "batched": batch,
                 "clocks": clk.summary(), "gpu_launches": launches}
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -492,6 +515,7 @@ def micro_results(dgp, which, reps):
             sec = timed(lambda: dgp.dg_op_canvas_attention(q, kp, vp, table, P, C_, Hq, Hkv, hd, pg,
                                                            False, o, ws))
             fl = 4.0 * C_ * Hq * S * hd
+            log(f"micro attention P={P}")
             out.append({"micro": "canvas_attention", "shape": f"P={P} C={C_} Hq={Hq} Hkv={Hkv} hd={hd}",
                         "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst})
             del kp, vp
@@ -511,6 +535,7 @@ def micro_results(dgp, which, reps):
         touched = len(np.unique(ids.cpu().numpy()))
         byt = touched * 3 * F * d * 2 + E * d * 2
         fl = 2.0 * T * k * 3 * F * d
+        log("micro moe")
         out.append({"micro": "moe_layer", "shape": f"T={T} d={d} E={E} top{k} F={F}",
                     "experts_touched": touched, "ms": sec * 1e3, "GBps": byt / sec / 1e9,
                     "frac_hbm": byt / sec / 1e9 / hbm, "TFLOPs": fl / sec / 1e12,
@@ -519,12 +544,13 @@ def micro_results(dgp, which, reps):
     if which in ("lmhead", "all"):
         T, d, V = 256, 2816, 262144
         w = torch.empty(V * d, dtype=torch.bfloat16, device=dev)
-        dgp.dg_op_fill_weights(w, 0, 2)
+        dgp.dg_op_fill_tiled_weights(w, V, d, 0, 2)
         _, xt = synth.normal_bf16((T, d), seed=2)
-        x = xt.to(dev)
+        x = torch.from_numpy(dgp.to_operand_tiles(xt.view(torch.int16).numpy())).view(torch.bfloat16).to(dev)
         part = torch.empty(dgp.partials_bytes(T, V) // 4, dtype=torch.int32, device=dev)
         sec = timed(lambda: dgp.dg_op_lm_head_partials(x, w, T, d, V, 1, 0, 1, part))
         fl = 2.0 * T * d * V
+        log("micro lm head")
         out.append({"micro": "lm_head_partials", "shape": f"T={T} d={d} V={V} (single bf16 activation)",
                     "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst,
                     "GBps_weights": V * d * 2 / sec / 1e9})
@@ -544,6 +570,7 @@ def micro_results(dgp, which, reps):
             dgp.dg_op_sampler_update(part, C_, V, 1, sc, st[0], com, st[1], st[2], st[3], conf, st[4], done)
         sec = timed(run)
         byt = C_ * V * 4
+        log("micro sampler")
         out.append({"micro": "sampler_materialized_logits", "shape": f"C={C_} V={V}", "ms": sec * 1e3,
                     "GBps": byt / sec / 1e9, "frac_hbm": byt / sec / 1e9 / hbm})
         del logits
@@ -587,7 +614,9 @@ def long_context(dgp, stream, tf_burst):
     m = dgp.dg_init_model(cfg, scfg, stream=stream)
     prompt = synth.prompt_ids(LONG_PROMPT, cfg.vocab, seed=77)
     dgp.dg_prefill(m, prompt)
+    log("long context: prefill done")
     prefill = time_prefill(dgp, m, prompt, stream, cfg, tf_burst)
+    log("long context: prefill timed")
     Ns, Cs = [], []
     dgp.dg_profile(m, 2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -595,6 +624,7 @@ def long_context(dgp, stream, tf_burst):
     e0.record(stream)
     for k in range(LONG_CANVASES):
         Ns.append(dgp.dg_denoise_canvas(m))
+        log(f"long context: canvas {k} ({Ns[-1]} steps)")
         if k < LONG_CANVASES - 1:
             _, valid = dgp.dg_commit_canvas(m)
         else:
@@ -617,6 +647,59 @@ def long_context(dgp, stream, tf_burst):
             "tpf_eq10": round(tok / (steps + LONG_CANVASES - 1), 3), "N_k": Ns,
             "prefill": prefill, "gpu_launches": launches,
             "note": "decode from the cached prompt, first canvas included (its CUDA graphs are captured on the fly)"}
+
+
+BATCH = 4
+
+
+def batched(dgp, stream):
+    """Lockstep multi-request batching on the same decoder: 4 requests, each a
+    2048-token random prompt and 4 canvases of 256 (N = 48, adaptive), every
+    forward over all 4 canvases.  One decode of all canvases from the cached
+    prompts, timed with CUDA events on the model's stream (after one untimed
+    decode that captures the graphs)."""
+    import torch
+    from discrete_diffusion_block_gb300 import synth
+    cfg = dgp.full_config(max_context=PROMPT + CANVASES * C, max_requests=BATCH)
+    scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1, sample_seed=60_000)
+    m = dgp.dg_init_model(cfg, scfg, stream=stream)
+    prompts = [synth.prompt_ids(PROMPT, cfg.vocab, seed=3000 + b) for b in range(BATCH)]
+
+    def decode():
+        dgp.dg_prefill_batch(m, prompts)
+        Ns = []
+        for k in range(CANVASES):
+            Ns.append(dgp.dg_denoise_canvas_batch(m))
+            if k < CANVASES - 1:
+                dgp.dg_commit_canvas_batch(m)
+        return Ns
+    decode()
+    dgp.dg_prefill_batch(m, prompts)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    Ns = []
+    for k in range(CANVASES):
+        Ns.append(dgp.dg_denoise_canvas_batch(m))
+        if k < CANVASES - 1:
+            dgp.dg_commit_canvas_batch(m)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    m.close()
+    del m
+    torch.cuda.empty_cache()
+    steps = sum(sum(n) for n in Ns)                 # per-request steps (Eq. 8 summed over requests)
+    forwards = sum(max(n) for n in Ns)              # lockstep forwards over all 4 canvases
+    tokens = BATCH * CANVASES * C
+    return {"workload": (f"{BATCH} requests in lockstep on the same decoder, each a {PROMPT}-token random "
+                         f"prompt and {CANVASES} canvases of {C}, N={BUDGET}, adaptive"),
+            "requests": BATCH, "decode_ms": round(ms, 1),
+            "denoise_steps_per_s": round(steps / (ms / 1e3), 2),
+            "output_tokens_per_s": round(tokens / (ms / 1e3), 1),
+            "batched_forwards": forwards, "ms_per_batched_step": round(ms / (forwards + CANVASES - 1), 3),
+            "N_k_per_request": [[n[b] for n in Ns] for b in range(BATCH)],
+            "note": "requests' steps summed; a batched forward serves every request's canvas"}
 
 
 def micro(args):
@@ -643,6 +726,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the micro-op and long-context sections of the JSON line")
     ap.add_argument("--micro-reps", type=int, default=10)
+    ap.add_argument("--section", default=None, choices=["long", "batched"],
+                    help="run one extra section of the JSON line alone and print it")
     ap.add_argument("--micro", default=None,
                     choices=["moe", "lmhead", "sampler", "attention", "kv_append", "all"],
                     help="kernel micro-benchmarks at the micro-op shapes instead of the decoder")
@@ -651,6 +736,17 @@ def main():
     args = ap.parse_args()
     if args.micro:
         return micro(args)
+    if args.section:
+        import torch
+        import discrete_diffusion_block_gb300 as dgp
+        from discrete_diffusion_block_gb300 import build
+        torch.cuda.set_device(0)
+        build.build()
+        dgp.load()
+        stream = torch.cuda.Stream(device=torch.device("cuda", 0))
+        out = long_context(dgp, stream, peaks()[1]) if args.section == "long" else batched(dgp, stream)
+        print(json.dumps(out), flush=True)
+        return 0
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

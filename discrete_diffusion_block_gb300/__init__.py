@@ -31,7 +31,7 @@ class DgError(RuntimeError):
 class dg_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_layers", "d_model", "n_q_heads", "n_kv_heads", "head_dim", "n_experts", "top_k",
-        "d_ff", "vocab", "page_size", "max_context")] + [
+        "d_ff", "vocab", "page_size", "max_context", "max_requests")] + [
         ("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float), ("init_std", ctypes.c_float),
         ("weight_seed", ctypes.c_uint64)]
 
@@ -67,6 +67,7 @@ class Config:
     vocab: int
     page_size: int = 128
     max_context: int = 4096
+    max_requests: int = 1
     rope_base: float = 10000.0
     rms_eps: float = 1e-6
     init_std: float = 0.02
@@ -125,6 +126,10 @@ _SIGS = {
     "dg_prefill": (_I, [_P, _P, _I]),
     "dg_denoise_step": (_I, [_P, _P]),
     "dg_denoise_canvas": (_I, [_P, _P]),
+    "dg_prefill_batch": (_I, [_P, _P, _P]),
+    "dg_denoise_canvas_batch": (_I, [_P, _P]),
+    "dg_commit_canvas_batch": (_I, [_P, _P, _P]),
+    "dg_generate_batch": (_I, [_P, _P, _P, _I, _P, _P]),
     "dg_commit_canvas": (_I, [_P, _P, _P]),
     "dg_generate": (_I, [_P, _P, _I, _I, _P, ctypes.POINTER(dg_stats)]),
     "dg_set_sampler": (_I, [_P, ctypes.POINTER(dg_sampler_config)]),
@@ -153,6 +158,7 @@ _SIGS = {
     "dg_op_lm_head_partials": (_I, [_P, _P, _P, _I, _I, _I, _U64, _I, _I, _F, _P, _P, _P]),
     "dg_op_logits_partials": (_I, [_P, _I, _I, _U64, _I, _I, _F, _P, _P]),
     "dg_op_gumbel_noise": (_I, [_P, _P, _U64, _P]),
+    "dg_op_fill_tiled_weights": (_I, [_P, _I, _I, _U64, ctypes.c_uint32, _F, _P]),
     "dg_op_sampler_update": (_I, [_P, _I, _I, _I, ctypes.POINTER(dg_sampler_config), _P, _P, _P,
                                   _P, _P, _P, _P, _P, _P]),
     "dg_op_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -300,6 +306,57 @@ def dg_generate(m, prompt, K_max):
                  canvas_loop_syncs=st.canvas_loop_syncs,
                  N_k=Nk[:K].tolist(), C_k=Ck[:K].tolist())
     return out[:K], stats
+
+
+def _prompt_arrays(prompts):
+    ps = [_i32(p) for p in prompts]
+    ptrs = (ctypes.c_void_p * len(ps))(*[p.ctypes.data if len(p) else None for p in ps])
+    lens = np.array([len(p) for p in ps], np.int32)
+    return ps, ptrs, lens
+
+
+def dg_prefill_batch(m, prompts):
+    ps, ptrs, lens = _prompt_arrays(prompts)
+    _check(load().dg_prefill_batch(m.handle, ptrs, _ptr(lens)))
+
+
+def dg_denoise_canvas_batch(m):
+    """Steps at which each request's canvas finished."""
+    n = np.zeros(m.cfg.max_requests or 1, np.int32)
+    _check(load().dg_denoise_canvas_batch(m.handle, _ptr(n)))
+    return n.tolist()
+
+
+def dg_commit_canvas_batch(m):
+    B = m.cfg.max_requests or 1
+    ids = np.zeros((B, m.scfg.canvas_len), np.int32)
+    valid = np.zeros(B, np.int32)
+    _check(load().dg_commit_canvas_batch(m.handle, _ptr(ids), _ptr(valid)))
+    return ids, valid.tolist()
+
+
+def dg_generate_batch(m, prompts, K_max):
+    """(ids [B][K_max][C] (canvases past a request's K are not reported), per-request stats)."""
+    B = m.cfg.max_requests or 1
+    assert len(prompts) == B
+    ps, ptrs, lens = _prompt_arrays(prompts)
+    out = np.zeros((B, K_max, m.scfg.canvas_len), np.int32)
+    Nk, Ck = np.zeros((B, K_max), np.int32), np.zeros((B, K_max), np.int32)
+    sts = (dg_stats * B)()
+    for b in range(B):
+        sts[b].N_k = Nk[b].ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        sts[b].C_k = Ck[b].ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    _check(load().dg_generate_batch(m.handle, ptrs, _ptr(lens), K_max, _ptr(out), sts))
+    stats = []
+    for b in range(B):
+        st = sts[b]
+        stats.append(dict(K=st.K, total_tokens=st.total_tokens, total_steps=st.total_steps,
+                          n_forwards=st.n_forwards, effective_steps=st.effective_steps, tpf=st.tpf,
+                          prefill_seconds=st.prefill_seconds, decode_seconds=st.decode_seconds,
+                          steps_per_s=st.steps_per_s, tokens_per_s=st.tokens_per_s,
+                          canvas_loop_syncs=st.canvas_loop_syncs, N_k=Nk[b][:st.K].tolist(),
+                          C_k=Ck[b][:st.K].tolist()))
+    return out, stats
 
 
 def dg_set_sampler(m, scfg):
@@ -457,6 +514,29 @@ def dg_op_lm_head_partials(xn, w_out, rows, d, V, seed, canvas, step, partials, 
 def dg_op_logits_partials(logits, rows, V, seed, canvas, step, partials, stream=None, inv_tau=1.0):
     _check(load().dg_op_logits_partials(_ptr(logits), rows, V, seed, canvas, step, inv_tau, _ptr(partials),
                                         _stream(stream)))
+
+
+def dg_op_fill_tiled_weights(dst, rows, cols, seed, tensor_id, std=0.02, stream=None):
+    _check(load().dg_op_fill_tiled_weights(_ptr(dst), rows, cols, seed, tensor_id, std, _stream(stream)))
+
+
+def to_operand_tiles(x):
+    """Row-major [rows][cols] numpy array (cols a multiple of 64) -> the
+    library's operand-tile order (128-row blocks, the last one partial; per
+    block cols/64 tiles of (block rows) x 64, the 16-byte chunk c of row r at
+    chunk position c ^ (r % 8)), flattened.  Host-side layout marshalling."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    out = []
+    for b0 in range(0, rows, 128):
+        blk = x[b0:b0 + 128]
+        n = blk.shape[0]
+        t = blk.reshape(n, cols // 64, 8, 8).transpose(1, 0, 2, 3)          # [kt][row][chunk][8]
+        pos = np.arange(8)[None, :] ^ (np.arange(n)[:, None] % 8)           # stored position of chunk c
+        o = np.empty_like(t)
+        o[:, np.arange(n)[:, None], pos, :] = t
+        out.append(o.reshape(-1))
+    return np.concatenate(out)
 
 
 def dg_op_gumbel_noise(words, out, stream=None):

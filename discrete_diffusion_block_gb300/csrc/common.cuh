@@ -219,9 +219,13 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch.  Kernels of a denoising step are launched
-// with programmatic stream serialization (launch_pdl), so a kernel's blocks
-// may be resident while its predecessor in the stream is still running.
+// Programmatic dependent launch, opt-in (DG_PDL=1).  With it, the kernels of
+// a denoising step are launched with programmatic stream serialization
+// (launch_pdl), so a kernel's blocks may be resident while its predecessor in
+// the stream is still running.  It is off by default: with it on, steps over
+// long prefixes (32k tokens) and multi-request steps stalled on the GB300
+// (a bounded wait of the attention gave up, and some runs did not return)
+// while the same launches without it ran to the end; the cause is not known.
 // Every such kernel calls pdl_wait() before it reads or writes anything an
 // earlier kernel touches (griddepcontrol.wait returns once the preceding grid
 // has completed and its memory is visible; it is a no-op for an ordinary
@@ -230,7 +234,8 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
-bool pdl_enabled();  // host: on unless DG_PDL=0 is set in the environment
+bool pdl_enabled();  // host: on only when DG_PDL=1 is set in the environment and it is not suspended
+void pdl_suspend(bool suspended);  // host: this thread's launches without programmatic dependence
 
 // Operand tiles of a row-major [rows][cols] bf16 matrix (cols a multiple of
 // 64), the layout every tensor-core operand of the decoder is stored in: row

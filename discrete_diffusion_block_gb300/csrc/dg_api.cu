@@ -48,8 +48,10 @@ int fail(int code, const char *fmt, ...) {
 #define CK(call)                                                                          \
   do {                                                                                    \
     cudaError_t e_ = (call);                                                              \
-    if (e_ != cudaSuccess)                                                                \
+    if (e_ != cudaSuccess) {                                                              \
+      cudaGetLastError(); /* a failed launch must not be reported again by a later call */ \
       return fail(DG_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));              \
+    }                                                                                     \
   } while (0)
 
 #define CKR(call)                                                                         \
@@ -97,6 +99,7 @@ struct dg_model {
   bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr,
        *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
+  int *route_bar = nullptr;                  // device, 2 ints: grid barrier of the fused routing + scatter
   float *gates = nullptr, *y = nullptr;
   float *xchg = nullptr;  // split-K partial exchange of the projection GEMMs
   int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
@@ -113,6 +116,13 @@ struct dg_model {
   float *conf = nullptr;
   int *done_host = nullptr;  // pinned, 2 ints (done, error word)
   int prompt_len = 0, prefix_len = 0, canvas_index = 0, step = 0;
+  // Lockstep batching: B requests, each with n_pages_req KV pages (request b
+  // owns physical pages b * n_pages_req ...), its own prompt and prefix, and
+  // its canvas at rows [b C, b C + C) of every per-position array.  With
+  // B = 1 the request's lengths are also prompt_len / prefix_len above.
+  int B = 1, n_pages_req = 0;
+  std::vector<int> prompt_lens, prefix_lens;
+  int *req_done = nullptr, *req_nk = nullptr, *batch_counter = nullptr;  // device, BatchCtl
   bool prefilled = false, canvas_active = false, canvas_done = false;
   // profiling: launch counts always, event-timed device ms when prof_on
   bool prof_on = false;
@@ -262,8 +272,10 @@ void prof_collect(dg_model *m) {
     cudaEvent_t a_ = prof_begin(m);                                                       \
     cudaError_t e_ = (call);                                                              \
     prof_end(m, (cls), (nk), a_);                                                         \
-    if (e_ != cudaSuccess)                                                                \
+    if (e_ != cudaSuccess) {                                                              \
+      cudaGetLastError();                                                                 \
       return fail(DG_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));              \
+    }                                                                                     \
   } while (0)
 
 #define SYNC(m)                                                                           \
@@ -288,6 +300,8 @@ int validate(const dg_config *c, const dg_sampler_config *s) {
   if (c->vocab < 256 || c->vocab % 256) return fail(DG_EINVAL, "vocab must be a positive multiple of 256");
   if (c->page_size < 64 || c->page_size % 64)
     return fail(DG_EINVAL, "page_size must be a positive multiple of 64");
+  if (c->max_requests < 0 || c->max_requests > dg::kMaxRequests)
+    return fail(DG_EINVAL, "max_requests must be in [0, %d]", dg::kMaxRequests);
   if (s->canvas_len < 1 || s->canvas_len > 1024) return fail(DG_EINVAL, "canvas_len must be in [1, 1024]");
   if (c->max_context < s->canvas_len) return fail(DG_EINVAL, "max_context smaller than one canvas");
   if (s->budget_N < 1 || s->budget_N > 65535) return fail(DG_EINVAL, "budget_N must be in [1, 65535]");
@@ -297,10 +311,12 @@ int validate(const dg_config *c, const dg_sampler_config *s) {
   return DG_OK;
 }
 
-// All layers over T tokens already embedded in m->h at positions pos0..;
-// K/V go to the cache at those positions.  kv_only_last: the last layer only
-// needs its K/V (KV-append and prefill).
-int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
+// All layers over T tokens already embedded in m->h, at the positions of
+// `rows` (one request's tokens from pos0[0], or n_req requests' rows, see
+// dg::RowSet); K/V go to the cache at those positions through page table
+// `ptab` (the request's slice, or the whole table with rows.n_req > 1).
+// kv_only_last: the last layer only needs its K/V (KV-append and prefill).
+int run_layers(dg_model *m, int T, const dg::RowSet &rows, const int *ptab, int causal, bool kv_only_last) {
   const dg_config &c = m->cfg;
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim;
   cudaStream_t st = m->stream;
@@ -309,24 +325,27 @@ int run_layers(dg_model *m, int T, int pos0, int causal, bool kv_only_last) {
     const Layer &W = m->layers[L];
     if (L == 0 || !fuse_norm)
       KL(DG_K_RMSNORM, 1, dg::rmsnorm_rows(m->xq, m->h, W.attn_norm, T, d, c.rms_eps, st, nullptr, true));
-    dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), m->page_table, pos0, c.page_size,
+    dg::QkvOut qo{m->q, m->kpool(L), m->vpool(L), ptab, rows, c.page_size,
                   c.n_q_heads, c.n_kv_heads, c.head_dim, m->cos_t, m->sin_t};
     int *err = m->done_dev + 1;
     KL(DG_K_QKV_ROPE, 1, dg::gemm_qkv(m->xq, W.wqkv, T, d, qo, err, m->xchg, st));
     if (kv_only_last && L == c.n_layers - 1) break;
-    dg::AttnShape as{pos0, T, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, causal, m->n_pages};
+    dg::AttnShape as{rows.pos0[0], rows.n_req > 1 ? rows.rows_per_req : T, c.n_q_heads, c.n_kv_heads,
+                     c.head_dim, c.page_size, causal, m->n_pages};
+    as.n_req = rows.n_req;
+    as.pages_per_req = rows.pages_per_req;
+    for (int b = 0; b < rows.n_req; ++b) as.req_prefix[b] = rows.pos0[b];
     KL(DG_K_ATTENTION, dg::attention_launch_count(as),
-       dg::attention(m->q, m->kpool(L), m->vpool(L), m->page_table, as, m->o, m->attn_ws,
+       dg::attention(m->q, m->kpool(L), m->vpool(L), ptab, as, m->o, m->attn_ws,
                      m->attn_ws_bytes, st, err, true));
     KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, m->xchg, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
-    KL(DG_K_ROUTE, 1,
-       dg::moe_norm_route(m->h, W.moe_norm, c.rms_eps, m->xn, W.wr, T, d, c.n_experts, c.top_k, topk, m->gates,
-                          m->slot_row, m->gcount, err, st));
-    KL(DG_K_ROUTE, 1,
-       dg::moe_scatter(m->xn, topk, m->gcount, m->slot_row, T, d, c.n_experts, c.top_k, dg::kExpertTileRows,
-                       m->x_tiles, m->offs, m->work, m->n_work, m->max_work, st, m->moe_stats));
+    int nl = 0;  // routing and scatter: one launch, or two when the routing grid exceeds the machine
+    KL(DG_K_ROUTE, nl,
+       dg::moe_route_scatter(m->h, W.moe_norm, c.rms_eps, m->xn, W.wr, T, d, c.n_experts, c.top_k, topk,
+                             m->gates, m->slot_row, m->gcount, m->x_tiles, m->offs, m->work, m->n_work,
+                             m->max_work, m->route_bar, err, st, m->moe_stats, &nl));
     const int rows = T * c.top_k;
     KL(DG_K_EXPERT_FFN, 1,
        dg::moe_ffn(m->x_tiles, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
@@ -349,7 +368,7 @@ int fill_model_weights(dg_model *m) {
   const float sd = c.init_std;
   cudaStream_t st = m->stream;
   CK(dg::fill_weights(m->embed, (uint64_t)c.vocab * d, s, 1, 0, sd, st));
-  CK(dg::fill_weights(m->lm_head, (uint64_t)c.vocab * d, s, 2, 0, sd, st));
+  CK(dg::fill_tiled_weights(m->lm_head, c.vocab, d, c.vocab, c.vocab, 2, 2, 2, s, sd, st));
   CK(dg::fill_const(m->final_norm, d, 1.0f, st));
   for (int L = 0; L < c.n_layers; ++L) {
     const uint32_t b = 100u + 16u * (uint32_t)L;
@@ -402,7 +421,8 @@ int alloc_model(dg_model *m, const void *const *weights) {
       CKR(m->alloc(&W.moe_norm, d));
     }
   }
-  m->n_pages = dg::ceil_div(c.max_context, c.page_size);
+  m->n_pages_req = dg::ceil_div(c.max_context, c.page_size);
+  m->n_pages = m->B * m->n_pages_req;
   m->layer_pool_elems = (size_t)m->n_pages * kd * c.page_size;
   CKR(m->alloc(&m->k_pool, m->layer_pool_elems * c.n_layers));
   CKR(m->alloc(&m->v_pool, m->layer_pool_elems * c.n_layers));
@@ -412,17 +432,20 @@ int alloc_model(dg_model *m, const void *const *weights) {
   CK(cudaMemset(m->v_pool, 0, m->layer_pool_elems * c.n_layers * sizeof(bf16)));
   CKR(m->alloc(&m->page_table, m->n_pages));
   m->page_table_host.resize(m->n_pages);
-  for (int i = 0; i < m->n_pages; ++i) m->page_table_host[i] = i;  // single request: in order
+  for (int i = 0; i < m->n_pages; ++i) m->page_table_host[i] = i;  // request b: its own range, in order
   CKR(m->alloc(&m->cos_t, (size_t)c.max_context * c.head_dim / 2));
   CKR(m->alloc(&m->sin_t, (size_t)c.max_context * c.head_dim / 2));
 
-  const int T = m->Tmax = C > kPrefillChunk ? C : kPrefillChunk;
+  const int BC = m->B * C;  // rows of a batched canvas forward
+  const int T = m->Tmax = BC > kPrefillChunk ? BC : kPrefillChunk;
   CKR(m->alloc(&m->ids, T));
   CKR(m->alloc(&m->h, (size_t)T * d));
   CKR(m->alloc(&m->xn, (size_t)T * d));
   CKR(m->alloc(&m->xq, (size_t)T * d));
-  CKR(m->alloc(&m->xn_lo, (size_t)C * d));
+  CKR(m->alloc(&m->xn_lo, (size_t)BC * d));
   CKR(m->alloc(&m->moe_stats, 2));
+  CKR(m->alloc(&m->route_bar, 2));
+  CK(cudaMemset(m->route_bar, 0, 2 * sizeof(int)));
   CKR(m->alloc(&m->q, (size_t)T * qd));
   CKR(m->alloc(&m->o, (size_t)T * qd));
   CKR(m->alloc(&m->xchg, dg::gemm_xchg_bytes() / sizeof(float)));
@@ -448,17 +471,21 @@ int alloc_model(dg_model *m, const void *const *weights) {
   }
   m->attn_ws_bytes = ws;
   CKR(m->alloc((unsigned char **)&m->attn_ws, ws));
-  CKR(m->alloc((unsigned char **)&m->partials, (size_t)C * (c.vocab / dg::kVocabTile) * 20));
-  CKR(m->alloc(&m->x, C));
-  CKR(m->alloc(&m->last, C));
-  CKR(m->alloc(&m->stable, C));
-  CKR(m->alloc(&m->argmax, C));
-  CKR(m->alloc(&m->gumbel, C));
+  CKR(m->alloc((unsigned char **)&m->partials, (size_t)BC * (c.vocab / dg::kVocabTile) * 20));
+  CKR(m->alloc(&m->x, BC));
+  CKR(m->alloc(&m->last, BC));
+  CKR(m->alloc(&m->stable, BC));
+  CKR(m->alloc(&m->argmax, BC));
+  CKR(m->alloc(&m->gumbel, BC));
+  CKR(m->alloc(&m->req_done, m->B));
+  CKR(m->alloc(&m->req_nk, m->B));
+  CKR(m->alloc(&m->batch_counter, 1));
+  CK(cudaMemset(m->batch_counter, 0, sizeof(int)));
   // [0] canvas done, [1] error word of bounded device waits, [2] bad page index
   CKR(m->alloc(&m->done_dev, 3));
   CK(cudaMemset(m->done_dev, 0, 3 * sizeof(int)));
-  CKR(m->alloc(&m->committed, C));
-  CKR(m->alloc(&m->conf, C));
+  CKR(m->alloc(&m->committed, BC));
+  CKR(m->alloc(&m->conf, BC));
   if (cudaMallocHost(&m->done_host, 2 * sizeof(int)) != cudaSuccess ||
       cudaMallocHost(&m->dyn_host, sizeof(dg::StepParams)) != cudaSuccess) {
     cudaGetLastError();
@@ -473,7 +500,22 @@ int check_model(dg_model *m) {
   return DG_OK;
 }
 
-int prefill_impl(dg_model *m, const int32_t *prompt, int32_t n) {
+// Synchronise the stream and report a bounded device-side wait that gave up
+// in the work since the last check (the error word is then cleared).
+int sync_check(dg_model *m) {
+  CK(cudaMemcpyAsync(m->done_host, m->done_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+  SYNC(m);
+  if (m->done_host[1]) {
+    const int code = m->done_host[1];
+    CK(cudaMemsetAsync(m->done_dev + 1, 0, sizeof(int), m->stream));
+    SYNC(m);
+    return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", code);
+  }
+  return DG_OK;
+}
+
+// Check request b's prompt (host) against the vocabulary and its KV capacity.
+int check_prompt(dg_model *m, const int32_t *prompt, int32_t n) {
   const dg_config &c = m->cfg;
   if (n < 0 || (n > 0 && !prompt)) return fail(DG_EINVAL, "bad prompt");
   if (n + m->sc.canvas_len > c.max_context)
@@ -481,29 +523,69 @@ int prefill_impl(dg_model *m, const int32_t *prompt, int32_t n) {
                 c.max_context);
   for (int i = 0; i < n; ++i)
     if (prompt[i] < 0 || prompt[i] >= c.vocab) return fail(DG_EINVAL, "prompt id %d out of range", prompt[i]);
+  return DG_OK;
+}
+
+// Encode request b's prompt into its KV pages (causal), in chunks of Tmax.
+// Its launches go without programmatic dependent launch even when DG_PDL=1
+// asks for it: with it, encoding long prompts (chunks of 2048 tokens after a
+// prefix of tens of thousands) stalled on the GB300 (one bounded wait of the
+// attention gave up, and one run did not return).
+int encode_prompt(dg_model *m, int b, const int32_t *prompt, int32_t n) {
+  struct PdlOff {
+    PdlOff() { dg::pdl_suspend(true); }
+    ~PdlOff() { dg::pdl_suspend(false); }
+  } pdl_off;
+  const dg_config &c = m->cfg;
+  const int *ptab = m->page_table + (size_t)b * m->n_pages_req;
   for (int p0 = 0; p0 < n; p0 += m->Tmax) {
     const int T = n - p0 < m->Tmax ? n - p0 : m->Tmax;
     CK(cudaMemcpyAsync(m->ids, prompt + p0, sizeof(int) * T, cudaMemcpyHostToDevice, m->stream));
     KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->ids, T, c.d_model, m->stream));
-    CKR(run_layers(m, T, p0, 1, true));
-    SYNC(m);  // the host prompt buffer and m->ids are reused by the next chunk
+    dg::RowSet rows;
+    rows.pos0[0] = p0;
+    CKR(run_layers(m, T, rows, ptab, 1, true));
+    CKR(sync_check(m));  // the host prompt buffer and m->ids are reused by the next chunk
   }
-  m->prompt_len = m->prefix_len = n;
-  m->canvas_index = 0;
-  m->prefilled = true;
-  m->canvas_active = m->canvas_done = false;
   return DG_OK;
 }
 
-// Denoising forward of the current canvas up to the final norm (in m->xn).
+void reset_generation(dg_model *m) {
+  m->prompt_len = m->prefix_len = m->prompt_lens[0];
+  m->prefix_lens = m->prompt_lens;
+  m->canvas_index = 0;
+  m->prefilled = true;
+  m->canvas_active = m->canvas_done = false;
+}
+
+int prefill_impl(dg_model *m, const int32_t *prompt, int32_t n) {
+  CKR(check_prompt(m, prompt, n));
+  CKR(encode_prompt(m, 0, prompt, n));
+  m->prompt_lens.assign(1, n);
+  reset_generation(m);
+  return DG_OK;
+}
+
+// The rows of the current canvases: one request's canvas after its prefix,
+// or (B > 1) every request's canvas after its own prefix.
+dg::RowSet canvas_rows(dg_model *m) {
+  dg::RowSet rows;
+  rows.n_req = m->B;
+  rows.rows_per_req = m->B > 1 ? m->sc.canvas_len : 0;
+  rows.pages_per_req = m->B > 1 ? m->n_pages_req : 0;
+  for (int b = 0; b < m->B; ++b) rows.pos0[b] = m->prefix_lens[b];
+  return rows;
+}
+
+// Denoising forward of the current canvas(es) up to the final norm (in m->xn).
 int canvas_forward(dg_model *m) {
   const dg_config &c = m->cfg;
-  const int C = m->sc.canvas_len;
-  KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, C, c.d_model, m->stream));
-  CKR(run_layers(m, C, m->prefix_len, 0, false));
-  // final norm kept to ~16 bits (hi + lo bf16) for the LM head
+  const int T = m->B * m->sc.canvas_len;
+  KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, T, c.d_model, m->stream));
+  CKR(run_layers(m, T, canvas_rows(m), m->page_table, 0, false));
+  // final norm kept to ~16 bits (hi + lo bf16), as the LM head's operand tiles
   KL(DG_K_RMSNORM, 1,
-     dg::rmsnorm_rows(m->xn, m->h, m->final_norm, C, c.d_model, c.rms_eps, m->stream, m->xn_lo));
+     dg::rmsnorm_rows(m->xn, m->h, m->final_norm, T, c.d_model, c.rms_eps, m->stream, m->xn_lo, true));
   return DG_OK;
 }
 
@@ -518,12 +600,14 @@ int begin_canvas(dg_model *m) {
   if (!m->prefilled) return fail(DG_ESTATE, "dg_prefill must come first");
   if (m->canvas_done) return fail(DG_ESTATE, "canvas finished: call dg_commit_canvas");
   if (!m->canvas_active) {
-    if (m->prefix_len + m->sc.canvas_len > m->cfg.max_context)
-      return fail(DG_ECAPACITY, "no room for another canvas (prefix %d, max_context %d)",
-                  m->prefix_len, m->cfg.max_context);
+    for (int b = 0; b < m->B; ++b)
+      if (m->prefix_lens[b] + m->sc.canvas_len > m->cfg.max_context)
+        return fail(DG_ECAPACITY, "no room for another canvas (prefix %d, max_context %d)",
+                    m->prefix_lens[b], m->cfg.max_context);
     KL(DG_K_CANVAS_INIT, 1,
        dg::canvas_init(m->x, m->committed, m->last, m->stable, m->sc.canvas_len, m->cfg.vocab,
-                       m->sc.sample_seed, m->canvas_index, m->stream));
+                       m->sc.sample_seed, m->canvas_index, m->stream, m->B));
+    if (m->B > 1) CK(cudaMemsetAsync(m->req_nk, 0, sizeof(int) * m->B, m->stream));
     m->step = 0;
     m->canvas_active = true;
   }
@@ -536,20 +620,26 @@ int begin_canvas(dg_model *m) {
 int step_launches(dg_model *m) {
   const dg_config &c = m->cfg;
   const dg_sampler_config &s = m->sc;
-  const int C = s.canvas_len;
+  const int C = s.canvas_len, T = m->B * C;
   CKR(canvas_forward(m));
   KL(DG_K_LM_HEAD, 1,
-     dg::gemm_lm_head_partials(m->xn, m->xn_lo, m->lm_head, C, c.d_model, c.vocab, s.sample_seed,
+     dg::gemm_lm_head_partials(m->xn, m->xn_lo, m->lm_head, T, c.d_model, c.vocab, s.sample_seed,
                                m->canvas_index, m->step, 1.0f, m->partials, m->done_dev + 1, m->stream,
-                               m->dyn_dev));
+                               m->dyn_dev, nullptr, m->B > 1 ? C : 0));
   KL(DG_K_SAMPLER_MERGE, 1,
-     dg::sampler_merge(m->partials, C, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
+     dg::sampler_merge(m->partials, T, c.vocab, m->argmax, m->conf, m->gumbel, m->stream));
+  dg::BatchCtl bt;
+  if (m->B > 1) bt = dg::BatchCtl{m->B, m->req_done, m->req_nk, m->batch_counter};
   KL(DG_K_SAMPLER_RULE, 1,
      dg::sampler_rule(m->argmax, m->conf, m->gumbel, C, m->step, s.budget_N, s.stable_steps,
                       s.adaptive, s.conf_threshold, m->x, m->committed, m->last, m->stable,
-                      m->done_dev, m->stream, m->dyn_dev, m->loop_ctl));
+                      m->done_dev, m->stream, m->dyn_dev, m->loop_ctl, bt));
   return DG_OK;
 }
+
+// Graphs of a step are valid for one set of prefix lengths: a single
+// request's prefix, or (B > 1, requests advancing together) the canvas index.
+int graph_key(const dg_model *m) { return m->B > 1 ? -1 - m->canvas_index : m->prefix_len; }
 
 // Capture step_launches() into a graph for the current prefix length.
 int capture_step(dg_model *m, dg_model::StepGraph *g) {
@@ -592,7 +682,7 @@ int denoise_impl(dg_model *m, int32_t *done) {
     CKR(step_launches(m));
     m->eager_step_done = true;
   } else {
-    const auto key = std::make_pair(m->prefix_len, m->prof_on ? 1 : 0);
+    const auto key = std::make_pair(graph_key(m), m->prof_on ? 1 : 0);
     auto it = m->graphs.find(key);
     if (it == m->graphs.end()) {
       dg_model::StepGraph g;
@@ -679,11 +769,11 @@ int denoise_canvas_impl(dg_model *m, int32_t *n_steps) {
       return DG_OK;
     }
   }
-  auto it = m->loop_graphs.find(m->prefix_len);
+  auto it = m->loop_graphs.find(graph_key(m));
   if (it == m->loop_graphs.end()) {
     dg_model::LoopGraph lg;
     CKR(capture_loop(m, &lg));
-    it = m->loop_graphs.emplace(m->prefix_len, lg).first;
+    it = m->loop_graphs.emplace(graph_key(m), lg).first;
   }
   CKR(put_step_params(m, m->step + 1));
   CK(cudaGraphLaunch(it->second.exec, m->stream));
@@ -710,22 +800,43 @@ int valid_tokens(const int32_t *ids, int C, int eos) {
   return C;
 }
 
+// Finish the current canvas(es): ids to out_ids (host, B * C), C_k of each
+// request to out_valid (host, B), then (append) the one KV-append forward of
+// every request's canvas, each after its own prefix.
 int commit_impl(dg_model *m, int32_t *out_ids, int32_t *out_valid, bool append) {
   if (!m->canvas_active || !m->canvas_done) return fail(DG_ESTATE, "canvas not finished");
-  const int C = m->sc.canvas_len;
-  std::vector<int32_t> ids(C);
-  CK(cudaMemcpyAsync(ids.data(), m->x, sizeof(int) * C, cudaMemcpyDeviceToHost, m->stream));
+  const int C = m->sc.canvas_len, T = m->B * C;
+  std::vector<int32_t> ids(T);
+  CK(cudaMemcpyAsync(ids.data(), m->x, sizeof(int) * T, cudaMemcpyDeviceToHost, m->stream));
   SYNC(m);
-  if (out_ids) memcpy(out_ids, ids.data(), sizeof(int) * C);
-  if (out_valid) *out_valid = valid_tokens(ids.data(), C, m->sc.eos_id);
+  if (out_ids) memcpy(out_ids, ids.data(), sizeof(int) * T);
+  if (out_valid)
+    for (int b = 0; b < m->B; ++b) out_valid[b] = valid_tokens(ids.data() + (size_t)b * C, C, m->sc.eos_id);
   if (append) {
-    KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, C, m->cfg.d_model, m->stream));
-    CKR(run_layers(m, C, m->prefix_len, m->sc.commit_causal ? 1 : 0, true));
-    SYNC(m);
-    m->prefix_len += C;
+    KL(DG_K_EMBED, 1, dg::embed_rows(m->h, m->embed, m->x, T, m->cfg.d_model, m->stream));
+    CKR(run_layers(m, T, canvas_rows(m), m->page_table, m->sc.commit_causal ? 1 : 0, true));
+    CKR(sync_check(m));
+    for (int b = 0; b < m->B; ++b) m->prefix_lens[b] += C;
+    m->prefix_len = m->prefix_lens[0];
     m->canvas_index += 1;
     m->canvas_active = m->canvas_done = false;
   }
+  return DG_OK;
+}
+
+// Per-request step counts of the canvases just finished (B > 1: the step at
+// which each request's canvas finished; B = 1: the steps taken).
+int read_request_steps(dg_model *m, std::vector<int> &nk) {
+  nk.assign(m->B, m->step);
+  if (m->B > 1) {
+    CK(cudaMemcpyAsync(nk.data(), m->req_nk, sizeof(int) * m->B, cudaMemcpyDeviceToHost, m->stream));
+    SYNC(m);
+  }
+  return DG_OK;
+}
+
+int single_only(dg_model *m) {
+  if (m->B != 1) return fail(DG_EINVAL, "the model holds %d requests: use the batch calls", m->B);
   return DG_OK;
 }
 
@@ -743,6 +854,9 @@ int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, const voi
   dg_model *m = new dg_model();
   m->cfg = *cfg;
   m->sc = *scfg;
+  m->B = cfg->max_requests > 1 ? cfg->max_requests : 1;
+  m->prompt_lens.assign(m->B, 0);
+  m->prefix_lens.assign(m->B, 0);
   if (const char *f = getenv("DG_FAULT_ALLOC")) m->fail_alloc_at = atoi(f);
   if (cuda_stream) {
     m->stream = (cudaStream_t)cuda_stream;
@@ -790,27 +904,114 @@ void dg_free_model(dg_model *m) {
 
 int dg_prefill(dg_model *m, const int32_t *prompt_ids, int32_t n) {
   CKR(check_model(m));
+  CKR(single_only(m));
   return prefill_impl(m, prompt_ids, n);
 }
 
 int dg_denoise_step(dg_model *m, int32_t *done) {
   CKR(check_model(m));
+  CKR(single_only(m));
   return denoise_impl(m, done);
 }
 
 int dg_denoise_canvas(dg_model *m, int32_t *n_steps) {
   CKR(check_model(m));
+  CKR(single_only(m));
   return denoise_canvas_impl(m, n_steps);
 }
 
 int dg_commit_canvas(dg_model *m, int32_t *out_ids, int32_t *out_valid) {
   CKR(check_model(m));
+  CKR(single_only(m));
   return commit_impl(m, out_ids, out_valid, true);
+}
+
+int dg_prefill_batch(dg_model *m, const int32_t *const *prompts, const int32_t *lens) {
+  CKR(check_model(m));
+  if (!prompts || !lens) return fail(DG_EINVAL, "null prompts");
+  for (int b = 0; b < m->B; ++b) CKR(check_prompt(m, prompts[b], lens[b]));
+  for (int b = 0; b < m->B; ++b) CKR(encode_prompt(m, b, prompts[b], lens[b]));
+  m->prompt_lens.assign(lens, lens + m->B);
+  reset_generation(m);
+  return DG_OK;
+}
+
+int dg_denoise_canvas_batch(dg_model *m, int32_t *n_steps) {
+  CKR(check_model(m));
+  int32_t n = 0;
+  CKR(denoise_canvas_impl(m, &n));
+  std::vector<int> nk;
+  CKR(read_request_steps(m, nk));
+  if (n_steps) memcpy(n_steps, nk.data(), sizeof(int) * m->B);
+  return DG_OK;
+}
+
+int dg_commit_canvas_batch(dg_model *m, int32_t *out_ids, int32_t *out_valid) {
+  CKR(check_model(m));
+  return commit_impl(m, out_ids, out_valid, true);
+}
+
+int dg_generate_batch(dg_model *m, const int32_t *const *prompts, const int32_t *lens, int32_t K_max,
+                      int32_t *out_ids, dg_stats *stats) {
+  CKR(check_model(m));
+  if (K_max < 1 || !out_ids) return fail(DG_EINVAL, "K_max >= 1 and out_ids required");
+  const int B = m->B, C = m->sc.canvas_len;
+  const double t0 = now_s();
+  CKR(dg_prefill_batch(m, prompts, lens));
+  const double t1 = now_s();
+  std::vector<std::vector<int>> Ns(B), Cs(B);
+  std::vector<char> active(B, 1);
+  std::vector<int32_t> ids((size_t)B * C), valid(B);
+  const int64_t syncs0 = m->host_syncs;
+  for (int k = 0; k < K_max; ++k) {
+    int32_t n = 0;
+    CKR(denoise_canvas_impl(m, &n));
+    std::vector<int> nk;
+    CKR(read_request_steps(m, nk));
+    CKR(commit_impl(m, ids.data(), valid.data(), false));
+    bool any = false;
+    for (int b = 0; b < B; ++b) {
+      if (!active[b]) continue;
+      memcpy(out_ids + ((size_t)b * K_max + k) * C, ids.data() + (size_t)b * C, sizeof(int32_t) * C);
+      Ns[b].push_back(nk[b]);
+      Cs[b].push_back(valid[b]);
+      if (valid[b] < C) active[b] = 0;  // its generation ends with the canvas holding its first EOS
+      any = any || active[b];
+    }
+    if (!any || k == K_max - 1) break;
+    CKR(commit_impl(m, nullptr, nullptr, true));
+  }
+  const double t2 = now_s();
+  for (int b = 0; stats && b < B; ++b) {
+    dg_stats &st = stats[b];
+    const int K = (int)Ns[b].size();
+    long long tok = 0, steps = 0, wsum = 0;
+    for (int i = 0; i < K; ++i) {
+      tok += Cs[b][i];
+      steps += Ns[b][i];
+      wsum += (long long)Ns[b][i] * Cs[b][i];
+      if (st.N_k) st.N_k[i] = Ns[b][i];
+      if (st.C_k) st.C_k[i] = Cs[b][i];
+    }
+    st.K = K;
+    st.total_tokens = (int)tok;
+    st.total_steps = (int)steps;
+    st.n_forwards = (int)(steps + K - 1);
+    st.effective_steps = tok ? (double)wsum / (double)tok : 0.0;
+    st.tpf = (double)tok / (double)(steps + K - 1);
+    st.prefill_seconds = t1 - t0;
+    st.decode_seconds = t2 - t1;
+    st.steps_per_s = t2 > t1 ? (double)steps / (t2 - t1) : 0.0;
+    st.tokens_per_s = t2 > t1 ? (double)tok / (t2 - t1) : 0.0;
+    st.canvas_loop_syncs = (int32_t)(m->host_syncs - syncs0);
+  }
+  return DG_OK;
 }
 
 int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_max,
                 int32_t *out_ids, dg_stats *stats) {
   CKR(check_model(m));
+  CKR(single_only(m));
   if (K_max < 1 || !out_ids) return fail(DG_EINVAL, "K_max >= 1 and out_ids required");
   const int C = m->sc.canvas_len;
   const double t0 = now_s();
@@ -872,11 +1073,12 @@ int dg_set_sampler(dg_model *m, const dg_sampler_config *scfg) {
 
 int dg_rewind(dg_model *m, int32_t n_prefix) {
   CKR(check_model(m));
+  CKR(single_only(m));
   if (!m->prefilled) return fail(DG_ESTATE, "nothing cached");
   if (n_prefix < m->prompt_len || n_prefix > m->prefix_len ||
       (n_prefix - m->prompt_len) % m->sc.canvas_len)
     return fail(DG_EINVAL, "n_prefix must be the prompt plus whole committed canvases");
-  m->prefix_len = n_prefix;
+  m->prefix_len = m->prefix_lens[0] = n_prefix;
   m->canvas_index = (n_prefix - m->prompt_len) / m->sc.canvas_len;
   m->canvas_active = m->canvas_done = false;
   return DG_OK;
@@ -902,6 +1104,7 @@ int dg_write_canvas(dg_model *m, const int32_t *ids, const uint8_t *committed,
                     const int32_t *last_argmax, const int32_t *stable, int32_t step,
                     int32_t canvas_index) {
   CKR(check_model(m));
+  CKR(single_only(m));
   if (!m->prefilled) return fail(DG_ESTATE, "dg_prefill must come first");
   if (!ids || !committed || !last_argmax || !stable || step < 0 || canvas_index < 0)
     return fail(DG_EINVAL, "all state arrays are required");
@@ -932,6 +1135,7 @@ int dg_read_step_outputs(dg_model *m, int32_t *argmax, float *conf, int32_t *gum
 
 int dg_canvas_logits(dg_model *m, float *logits_dev) {
   CKR(check_model(m));
+  CKR(single_only(m));
   if (!logits_dev) return fail(DG_EINVAL, "null logits");
   CKR(begin_canvas(m));
   CKR(canvas_forward(m));
@@ -1201,6 +1405,7 @@ struct MoeWs {
   int *offs, *gcount, *slot_row, *work, *n_work;
   bf16 *act, *x_tiles;
   float *y_rows;
+  int *bar;
   size_t bytes;
   int max_work;
 };
@@ -1222,6 +1427,7 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.act = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, F) * 2);
   w.x_tiles = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, d) * 2);
   w.y_rows = (float *)take((size_t)T * k * d * 4);
+  w.bar = (int *)take(2 * 4);
   w.bytes = off;
   return w;
 }
@@ -1249,10 +1455,10 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   cudaStream_t st = (cudaStream_t)stream;
   int *status = nullptr;
   CKR(op_status_ptr(&status));
-  CK(dg::moe_route((const bf16 *)xn, (const bf16 *)w_router, T, d, n_experts, top_k, expert_ids, gates,
-                   w.slot_row, w.gcount, status, st));
-  CK(dg::moe_scatter((const bf16 *)xn, expert_ids, w.gcount, w.slot_row, T, d, n_experts, top_k,
-                     dg::kExpertTileRows, w.x_tiles, w.offs, w.work, w.n_work, w.max_work, st));
+  CK(cudaMemsetAsync(w.bar, 0, 2 * sizeof(int), st));
+  CK(dg::moe_route_scatter(nullptr, nullptr, 0.0f, const_cast<bf16 *>((const bf16 *)xn), (const bf16 *)w_router, T,
+                           d, n_experts, top_k, expert_ids, gates, w.slot_row, w.gcount, w.x_tiles, w.offs, w.work,
+                           w.n_work, w.max_work, w.bar, status, st));
   const int rows = T * top_k;
   CK(dg::moe_ffn(w.x_tiles, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
                  w.max_work, n_experts, d, d_ff, w.act, w.y_rows, status, st));
@@ -1290,6 +1496,14 @@ int dg_op_logits_partials(const float *logits, int32_t rows, int32_t V, uint64_t
     return fail(DG_EINVAL, "bad arguments");
   CK(dg::logits_partials(logits, rows, V, sample_seed, canvas, step, inv_tau, partials,
                          (cudaStream_t)stream));
+  return DG_OK;
+}
+
+int dg_op_fill_tiled_weights(uint16_t *dst, int32_t rows, int32_t cols, uint64_t seed,
+                             uint32_t tensor_id, float std_dev, void *stream) {
+  if (!dst || rows < 1 || cols < 64 || cols % 64) return fail(DG_EINVAL, "bad arguments");
+  CK(dg::fill_tiled_weights((bf16 *)dst, rows, cols, rows, rows, tensor_id, tensor_id, tensor_id, seed, std_dev,
+                            (cudaStream_t)stream));
   return DG_OK;
 }
 

@@ -20,11 +20,12 @@ cudaError_t fill_moe_weights(bf16 *wr, bf16 *wgu, bf16 *wd, int d, int E, int F,
 cudaError_t fill_const(float *dst, size_t n, float v, cudaStream_t st);
 cudaError_t rope_table(float *cos_t, float *sin_t, int max_pos, int head_dim, float base,
                        cudaStream_t st);
+// n_req canvases of C positions (request b: sample seed + b), arrays [n_req C].
 cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
-                        uint64_t seed, int canvas, cudaStream_t st);
+                        uint64_t seed, int canvas, cudaStream_t st, int n_req = 1);
 cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st);
 // out = RMSNorm(h) * gain (bf16), row-major, or as operand tiles (tiled_index)
-// when `tiled` (then out_lo must be null).
+// when `tiled`; out_lo (optional) the bf16 rounding of the remainder, same layout.
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
                          cudaStream_t st, bf16 *out_lo = nullptr, bool tiled = false);
 // Routing of one MoE layer (kernels_route.cu), two launches.
@@ -58,6 +59,15 @@ cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k
 cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
                         int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
                         cudaStream_t st, unsigned long long *stats = nullptr);
+// moe_norm_route (h != null) or moe_route, then moe_scatter, as one launch
+// when the routing grid fits the machine (the scatter then runs in the
+// routing kernel after a grid-wide barrier on bar, 2 zeroed ints), else as
+// two; *launches (optional) receives 1 or 2.  slot_row serves as the rank
+// array in between.
+cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
+                              int E, int k, int *ids, float *gates, int *slot_row, int *gcount, bf16 *x_tiles,
+                              int *offs, int *work, int *n_work, int max_work, int *bar, int *err, cudaStream_t st,
+                              unsigned long long *stats = nullptr, int *launches = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
 size_t moe_work_ints(int T, int k, int E, int tile_rows);
 // Routed experts of one layer (kernels_moe.cu): act = SwiGLU(X Wg^T, X Wu^T),
@@ -81,11 +91,26 @@ cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *
                       int pg, cudaStream_t st);
 
 // ---- GEMM-based layer pieces (kernels_gemm.cu) -----------------------------
+constexpr int kMaxRequests = 8;  // requests decoded together in one forward
+// Rows of a forward that belong to several requests (multi-request batching):
+// rows [b R, (b + 1) R) are request b's, its first at absolute position
+// pos0[b] of that request, its K/V pages at page_table[b * pages_per_req ...].
+// n_req = 1: one request, rows at pos0[0] + row.
+struct RowSet {
+  int n_req = 1, rows_per_req = 0, pages_per_req = 0;
+  int pos0[kMaxRequests] = {};
+  __host__ __device__ int req(int row) const { return n_req > 1 ? row / rows_per_req : 0; }
+  __host__ __device__ int pos(int row) const {
+    const int b = req(row);
+    return pos0[b] + row - b * rows_per_req;
+  }
+};
 struct QkvOut {
   bf16 *q;                // [T][Hq*hd]
   bf16 *k_pool, *v_pool;  // layer slice [n_pages][Hkv][pg][hd]
   const int *page_table;
-  int pos0, pg, Hq, Hkv, hd;
+  RowSet rows;            // positions and page-table slices of the rows
+  int pg, Hq, Hkv, hd;
   const float *cos_t, *sin_t;  // [max_pos][hd/2]
 };
 // `err`: device error word set by a tensor-core GEMM whose bounded wait gave up.
@@ -107,7 +132,8 @@ constexpr int kExpertTileRows = 128;  // token rows per expert work item (MMA N 
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, uint64_t seed, int canvas, int step, float inv_tau,
                                   void *partials, int *err, cudaStream_t st,
-                                  const StepParams *dyn = nullptr, float *logits = nullptr);
+                                  const StepParams *dyn = nullptr, float *logits = nullptr,
+                                  int rows_per_req = 0);
 cudaError_t gemm_lm_head_logits(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                 int V, float *logits, int *err, cudaStream_t st);
 
@@ -133,17 +159,32 @@ struct LoopCtl {
   float temp_start, temp_end;         // re-noise temperature schedule
   const int *err;                     // error word of the step's bounded waits
 };
+// Lockstep batching of n_req requests (canvases of C positions each, one rule
+// block per request): req_done[b] this step's per-request decision, req_nk[b]
+// the step at which request b's canvas finished (0: not yet; zeroed at canvas
+// start), counter a zeroed int the blocks count themselves on.
+struct BatchCtl {
+  int n_req = 1;
+  int *req_done = nullptr, *req_nk = nullptr, *counter = nullptr;
+};
 // dyn (optional, device): the step number is taken from dyn->step (and, in a
-// loop, the next step's words are written back to it).
+// loop, the next step's words are written back to it).  *done: the step's
+// canvas (every request's canvas) is finished.
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
                          int budget_N, int stable_steps, int adaptive, float conf_threshold,
                          int *x, uint8_t *committed, int *last, int *stable, int *done,
-                         cudaStream_t st, StepParams *dyn = nullptr, LoopCtl loop = LoopCtl{});
+                         cudaStream_t st, StepParams *dyn = nullptr, LoopCtl loop = LoopCtl{},
+                         BatchCtl bt = BatchCtl{});
 
 // ---- attention (kernels_attn.cu) -------------------------------------------
 struct AttnShape {
   int n_prefix, n_new, Hq, Hkv, hd, pg, causal;
   int n_pages = 0;  // physical pages of the pools when known (0: unknown)
+  // several requests of n_new rows each (q and out hold n_req * n_new rows):
+  // request b's keys start after req_prefix[b] cached ones, its pages at
+  // page_table[b * pages_per_req ...]; n_req = 1: n_prefix, the whole table
+  int n_req = 1, pages_per_req = 0;
+  int req_prefix[kMaxRequests] = {};
 };
 // Device scratch the call needs (none: split-KV states merge on chip); ws and
 // ws_bytes of attention() are accepted and unused.

@@ -15,31 +15,29 @@
 // a 64- or 128-key K or V operand tile is one contiguous bulk copy.
 //
 // The kernel is a tcgen05 tensor-core kernel with one pass over the block's
-// key range and an online softmax.  A block holds two 128-row query tiles
-// that share every K and V tile and run in ping-pong, so that the softmax of
-// one tile overlaps the tensor work of the other.  Per 128-key tile j and
-// query tile t: S_t = Q_t K_j^T (TMEM), the row maximum, P = 2^(S*scale - m)
-// written back over S's first 64 columns as bf16 pairs, row sum l in fp32,
-// O_t += P_t V_j (TMEM, P read from tensor memory as the A operand, V the
-// N-contiguous "MN-major" B operand).  The running maximum m is raised
-// lazily: only a row whose maximum grows by more than 2^8 moves to the new
-// reference and rescales its accumulator row in TMEM (read, scale, write
-// back) after the previous tile's P V has landed; below that P stays <= 2^8
-// and the final O / l does not depend on which reference was used.  Roles
-// (384 threads): warp 0 streams the two query tiles once (TMA through a 4-D
-// map that packs the G heads of a token as consecutive rows) and the K tiles
-// through a two-slot ring; warp 2 streams the V tiles through their own
-// two-slot ring (both as bulk copies of the pool's pre-swizzled pages, from a
-// page list resolved before the dependency wait); warp 1 issues the MMAs in
-// the order P V_0(j), S_0(j+1), P V_1(j), S_1(j+1); warps 4-7 and 8-11 do
-// the softmax of query tiles 0 and 1 (thread = query row, all 128 keys of a
-// tile, two passes over S in tensor memory).  TMEM: 256 columns per query
-// tile (S/P, then O).  With the key range split over several blocks, the
-// blocks of a query tile pair form a cluster: each stages its unnormalised
-// output rows and softmax states (m, l) in shared memory, and each block
-// reads the slice of rows it owns from every peer through distributed shared
-// memory, merges them (weights 2^(m_s - m*)) and writes them; no device
-// scratch is used.
+// key range and an online softmax: per 128-key tile, S = Q K^T (TMEM), the
+// tile's raw-score maximum, P = 2^(S*scale - m) as bf16 into shared memory,
+// row sum l in fp32, O += P V (TMEM).  The running maximum m is raised lazily:
+// only a row whose maximum grows by more than 2^8 moves to the new reference
+// and rescales its accumulator row in TMEM (read, scale, write back) after the
+// previous tile's P V has landed; below that P stays <= 2^8 and the final
+// O / l does not depend on which reference was used.  Roles (352 threads):
+// warp 0 streams Q once (TMA through a 4-D map that packs the G heads of a
+// token as consecutive rows) and the K tiles through a three-slot ring; warp
+// 6 streams the V tiles through their own three-slot ring (both as bulk
+// copies of the pool's pre-swizzled pages, from a page list resolved before
+// the dependency wait); warp 1 issues the MMAs, S of tile i + 1 before P V of
+// tile i, with two S accumulators and two P tiles so the softmax of one tile
+// overlaps the tensor work of the next (P is written to tensor memory by the
+// softmax threads and read from there as the A operand of P V; V is the
+// N-contiguous "MN-major" B operand); warps 2-5 and 7-10 do the softmax, two
+// warps per TMEM lane quarter (thread = query row), each on half of a tile's
+// keys, exchanging their halves' maxima per tile.  With the key range split
+// over several blocks, the blocks of one query tile form a
+// cluster: each stages its unnormalised output rows and softmax state (m, l)
+// in shared memory, pushes to every peer the slice of rows that peer owns
+// (bulk shared-to-shared copies), and each block merges its slice (weights
+// 2^(m_s - m*)) and writes it; no device scratch is used.
 #include <cuda.h>
 
 #include <cudaTypedefs.h>
@@ -54,7 +52,7 @@ namespace dg {
 
 namespace {
 
-constexpr int kRowsPerBlock = 128;  // query rows (token, head) per query tile: the MMA M
+constexpr int kRowsPerBlock = 128;  // query rows (token, head) per block: the MMA M
 constexpr int kKeysPerTile = 128;   // keys per S tile: the MMA N of Q K^T, the K of P V
 
 struct AttnParams {
@@ -68,7 +66,13 @@ struct AttnParams {
   int *err;        // device error words, may be null: [0] a bounded wait gave up, [1] a bad page index
   int n_pages;     // physical pages of the pools, 0 when unknown
   bf16 *final_out; // split launches: where the cluster's merge writes the output
-  int out_tiles;   // outputs as operand tiles over [n_new][Hq hd] (the o-projection operand)
+  int out_tiles;   // outputs as operand tiles over [n_req n_new][Hq hd] (the o-projection operand)
+  // several requests (blockIdx.z = request * splits + split): request b's
+  // n_new rows follow b * n_new rows of q / out, its keys start after
+  // req_prefix[b] cached ones, its pages at page_table[b * pages_per_req ...]
+  int n_req, splits, pages_per_req;
+  int req_prefix[kMaxRequests];
+  int req_kps[kMaxRequests];  // keys per split of each request (its own plan; trailing splits empty)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -77,36 +81,35 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 
-constexpr int kQTiles = 2;          // query tiles of 128 rows per block, in ping-pong
-constexpr int kBlockRows = kQTiles * kRowsPerBlock;
-constexpr int kAttnThreads = 384;   // warp 0: Q and K copies; 1: MMAs; 2: V copies; 4-7, 8-11: softmax of tiles 0, 1
+constexpr int kAttnThreads = 352;  // warps 0, 1, 6: copies and MMAs; 2-5 and 7-10: softmax
 constexpr int kAttnPages = 64;  // 64-key halves whose physical page is looked up before the key loop
 constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one 8 KB copy)
 
-// Shared memory (bytes from a 1024-aligned base): the two query tiles
-// [HB][128 rows][64]; a 2-slot K ring and a 2-slot V ring of 128-key tiles
-// [HB][128 keys][64] (each tile feeds both query tiles, so two slots keep the
-// tensor core fed); the rows' softmax states; the page list; barriers.  After
-// the key loop the K and V rings hold the block's fp32 output rows [256][HD]
-// (read by the peers of a split query tile through distributed shared
-// memory) and the query tiles the merge weights.
+// Shared memory (bytes from a 1024-aligned base): Q [HB][128 rows][64]; a
+// 3-slot K ring and a 3-slot V ring of 128-key tiles [HB][128 keys][64] (the
+// P tiles live in tensor memory, which leaves room for the third slots: the
+// key loop is bound by copy latency times ring depth); the page list;
+// barriers.  After the key loop the K ring holds the fp32 output rows
+// [128][HD] on their way out; with split keys the V ring holds the rows'
+// softmax states and merge weights (first 8 KB) and receives the peers'
+// partial rows (from 8 KB on).
 template <int HD>
 struct AttnSmem {
   static constexpr int HB = HD / 64;                       // 64-wide hd blocks
-  static constexpr int kK = 2, kV = 2;                     // ring depths
-  static constexpr size_t tile = (size_t)HB * 16384;       // one 128-row tile of keys, values or queries
+  static constexpr int kK = 3, kV = 3;                     // ring depths
+  static constexpr size_t tile = (size_t)HB * 16384;       // one 128-key K or V tile, or Q
   static constexpr size_t q = 0;
-  static constexpr size_t kring = q + kQTiles * tile;
+  static constexpr size_t kring = q + tile;
   static constexpr size_t vring = kring + kK * tile;
-  static constexpr size_t stage = kring;                   // after the key loop: fp32 rows [256][HD]
-  static constexpr size_t ml = vring + kV * tile;          // [256] (m, l) of the rows (split merge)
-  static constexpr size_t pages = ml + kBlockRows * 8;     // physical page per 64-key half (ints)
-  static constexpr size_t bars = pages + kAttnPages * 4;
-  // q_full, k_full[kK], k_empty[kK], v_full[kV], v_empty[kV], s_full[2], p_full[2], pv_done[2], o_full
-  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 2 + 2 + 2 + 1;
+  static constexpr size_t recv = vring + 8192;             // split merge: the peers' partial rows
+  static constexpr size_t pages = vring + kV * tile;       // physical page per 64-key half (ints)
+  static constexpr size_t xch = pages + kAttnPages * 4;    // [2 halves][128 rows] fp32: the softmax pairs' exchange
+  static constexpr size_t bars = xch + 2 * 128 * 4;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty[2], o_full,
+  // r_full (peer partials received)
+  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 4 + 1;
   static constexpr size_t bytes = bars + n_bars * 8 + 16 + 1024;
-  static_assert((size_t)kBlockRows * HD * 4 <= (kK + kV) * tile, "output staging fits the K and V rings");
-  static_assert((size_t)kBlockRows * 8 * 4 + kBlockRows * 8 <= kQTiles * tile, "merge tables fit the Q tiles");
+  static_assert((size_t)128 * HD * 4 <= (kK + kV) * tile, "output staging fits the K and V rings");
 };
 
 // One 64-key half of a K or V operand tile, all zero (keys past the end).
@@ -164,12 +167,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-
 // Rows whose running maximum grows by more than this (log2 units) rescale
 // their accumulated output; otherwise P = 2^(s - m) stays <= 2^8 and the
 // stale maximum is kept (the final O / l does not depend on m).
@@ -186,27 +183,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t *q_full = (uint64_t *)(base + S::bars);
   uint64_t *k_full = q_full + 1, *k_empty = k_full + KK;
   uint64_t *v_full = k_empty + KK, *v_empty = v_full + KV;
-  uint64_t *s_full = v_empty + KV, *p_full = s_full + 2, *pv_done = p_full + 2, *o_full = pv_done + 2;
-  uint32_t *tmem_slot = (uint32_t *)(o_full + 1);
+  uint64_t *s_full = v_empty + KV, *s_empty = s_full + 2;
+  uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1, *o_full = p_empty + 2, *r_full = o_full + 1;
+  uint32_t *tmem_slot = (uint32_t *)(r_full + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
   int *pages = (int *)(base + S::pages);
-  auto q_tile = [&](int t) { return base + S::q + (size_t)t * S::tile; };
   auto k_tile = [&](int slot) { return base + S::kring + (size_t)slot * S::tile; };
   auto v_tile = [&](int slot) { return base + S::vring + (size_t)slot * S::tile; };
 
-  const int g = blockIdx.y, split = blockIdx.z;
+  const int g = blockIdx.y, b_req = blockIdx.z / p.splits, split = blockIdx.z - b_req * p.splits;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_total = p.G * p.n_new;
-  const int r_cta = blockIdx.x * kBlockRows;
-  const int n_q = min(kQTiles, ceil_div(rows_total - r_cta, kRowsPerBlock));  // query tiles holding rows
-  const int n_keys = p.n_prefix + p.n_new;
-  const int k_begin = split * p.keys_per_split;
-  int k_end = min(n_keys, k_begin + p.keys_per_split);
-  if (p.causal) {  // keys past the block's last query token are hidden from every row
-    const int t_max = min(p.n_new - 1, (min(r_cta + kBlockRows, rows_total) - 1) / p.G);
-    k_end = min(k_end, p.n_prefix + t_max + 1);
+  const int r_cta = blockIdx.x * 128;
+  const int n_prefix = p.n_req > 1 ? p.req_prefix[b_req] : p.n_prefix;
+  const int *page_table = p.page_table + (size_t)b_req * p.pages_per_req;
+  const int tok0 = b_req * p.n_new;  // the request's first row of q and out
+  const int n_keys = n_prefix + p.n_new;
+  const int kps = p.n_req > 1 ? p.req_kps[b_req] : p.keys_per_split;
+  const int k_begin = split * kps;
+  int k_end = min(n_keys, k_begin + kps);
+  if (p.causal) {
+    const int t_max = min(p.n_new - 1, (r_cta + 127) / p.G);
+    k_end = min(k_end, n_prefix + t_max + 1);
   }
-  const int n_kt = k_end > k_begin ? ceil_div(k_end - k_begin, kKeysPerTile) : 0;
+  const int n_kt = k_end > k_begin ? ceil_div(k_end - k_begin, 128) : 0;
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -221,10 +221,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(s_full + i, 1);
-      tc::mbar_init(p_full + i, 4);  // one arrival per softmax warp of the tile
-      tc::mbar_init(pv_done + i, 1);
+      tc::mbar_init(s_empty + i, 8);  // one arrival per softmax warp
     }
+    tc::mbar_init(p_full, 8);
+    tc::mbar_init(p_empty, 1);
+    tc::mbar_init(p_empty + 1, 1);
     tc::mbar_init(o_full, 1);
+    tc::mbar_init(r_full, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     for (int i = lane; i < n_halves; i += 32) {
       const int key = k_begin + 64 * i;
-      int pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
+      int pg_i = key < k_end ? page_table[key / p.pg] : -1;
       if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) {
         if (p.err) atomicExch(p.err + 1, 39);  // reported, not an abort: later blocks still run
         pg_i = -1;
@@ -269,10 +272,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  // per query tile t: S (fp32, 128 key columns) at 256 t, its P (bf16 pairs)
-  // written over S's first 64 columns, O at 256 t + 128
-  auto t_s = [&](int t) { return tmem + 256u * (uint32_t)t; };
-  auto t_o = [&](int t) { return tmem + 256u * (uint32_t)t + 128u; };
+  // S double buffer: columns [0,128) [128,256); O: [256, 256+HD); P double
+  // buffer (bf16 pairs): [384, 448) [448, 512)
+  const uint32_t t_s = tmem, t_o = tmem + 256, t_p = tmem + 384;
 
   // One 128-key K or V tile: per 64-key half, the page's hd sub-blocks; two
   // halves of one page that follow each other move as one copy; a half past
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (hi < kAttnPages) {
         pg_i = pages[hi];
       } else {
-        pg_i = key < k_end ? p.page_table[key / p.pg] : -1;
+        pg_i = key < k_end ? page_table[key / p.pg] : -1;
         if (pg_i >= 0 && p.n_pages > 0 && pg_i >= p.n_pages) pg_i = -1;
       }
       pgs[h] = pg_i;
@@ -311,18 +313,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   };
 
-  if (warp == 0) {  // the query tiles, then the K ring (S of a tile needs only its K)
+  if (warp == 0) {  // Q, then the K ring (S of a tile needs only its K)
     if (lane == 0 && n_kt > 0) {
-      tc::mbar_expect_tx(q_full, (uint32_t)(n_q * HB * 16384));
-      for (int t = 0; t < n_q; ++t)
-        for (int b = 0; b < HB; ++b) {
-          asm volatile(
-              "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
-              "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(tc::smem_u32(q_tile(t) + (size_t)b * 16384)),
-              "l"((uint64_t)&tq), "r"(64 * b), "r"(0), "r"(g), "r"((r_cta + kRowsPerBlock * t) / p.G),
-              "r"(tc::smem_u32(q_full))
-              : "memory");
-        }
+      tc::mbar_expect_tx(q_full, (uint32_t)(HB * 16384));
+      for (int b = 0; b < HB; ++b) {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(tc::smem_u32(base + S::q + (size_t)b * 16384)),
+            "l"((uint64_t)&tq), "r"(64 * b), "r"(0), "r"(g), "r"(tok0 + r_cta / p.G), "r"(tc::smem_u32(q_full))
+            : "memory");
+      }
       int nk = 0;
       for (; nk < n_kt; ++nk) {
         const int slot = nk % KK;
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (*abort) drain(k_full, nk, KK);
     }
-  } else if (warp == 2) {  // the V ring
+  } else if (warp == 6) {  // the V ring
     if (lane == 0 && n_kt > 0) {
       int nv = 0;
       for (; nv < n_kt; ++nv) {
@@ -344,179 +344,175 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (*abort) drain(v_full, nv, KV);
     }
   } else if (warp == 1) {
-    // Tensor-core order per key tile j (tile 1's steps only when it holds rows):
-    //   P V of tile 0 (j), S of tile 0 (j + 1), P V of tile 1 (j), S of tile 1 (j + 1)
-    // so that while one tile's softmax runs the tensor core works for the
-    // other.  S of a tile overwrites its P columns only after the P V that
-    // reads them (the MMAs of a CTA execute in issue order).
     if (lane == 0 && n_kt > 0) {
       const uint32_t idesc_s = tc::idesc_bf16(128, 128);
       const uint32_t idesc_o = tc::idesc_bf16(128, HD) | (1u << 16);  // B (V) N-contiguous
       tc::mbar_wait(q_full, 0, p.err, 32, abort);
-      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-        const int slot = j % KK;
+      auto issue_s = [&](int i) {  // S[i & 1] = Q K_i^T
+        const int slot = i % KK, buf = i & 1;
+        if (i >= 2) tc::mbar_wait(s_empty + buf, ((i >> 1) - 1) & 1, p.err, 33, abort);
+        tc::mbar_wait(k_full + slot, (i / KK) & 1, p.err, 34, abort);
+        tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t adesc = tc::sw128_desc(tc::smem_u32(q_tile(t) + (size_t)(kk >> 2) * 16384)) + 2 * (kk & 3);
+          const uint64_t adesc = tc::sw128_desc(tc::smem_u32(base + S::q + (size_t)(kk >> 2) * 16384)) + 2 * (kk & 3);
           const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(k_tile(slot) + (size_t)(kk >> 2) * 16384)) + 2 * (kk & 3);
-          tc::mma_bf16(t_s(t), adesc, bdesc, idesc_s, kk ? 1u : 0u);
+          tc::mma_bf16(t_s + buf * 128, adesc, bdesc, idesc_s, kk ? 1u : 0u);
         }
-        tc::mma_commit(s_full + t);
+        tc::mma_commit(s_full + buf);
+        tc::mma_commit(k_empty + slot);
       };
-      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j
-        const int slot = j % KV;
+      issue_s(0);
+      for (int i = 0; i < n_kt; ++i) {
+        if (i + 1 < n_kt) issue_s(i + 1);
+        const int slot = i % KV;
+        tc::mbar_wait(p_full, i & 1, p.err, 35, abort);
+        tc::mbar_wait(v_full + slot, (i / KV) & 1, p.err, 29, abort);
+        tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 (8 columns of P) per MMA
           const uint64_t bdesc = mn_desc(tc::smem_u32(v_tile(slot))) + (uint64_t)kk * (2048 >> 4);
-          mma_bf16_tmem_a(t_o(t), t_s(t) + 8 * kk, bdesc, idesc_o, (j | kk) ? 1u : 0u);
+          mma_bf16_tmem_a(t_o, t_p + 64 * (i & 1) + 8 * kk, bdesc, idesc_o, (i | kk) ? 1u : 0u);
         }
-        tc::mma_commit(pv_done + t);
-      };
-      tc::mbar_wait(k_full, 0, p.err, 34, abort);
-      tc::fence_after();
-      for (int t = 0; t < n_q; ++t) issue_s(t, 0);
-      tc::mma_commit(k_empty);
-      for (int j = 0; j < n_kt; ++j) {
-        const bool nxt = j + 1 < n_kt;
-        tc::mbar_wait(v_full + j % KV, (j / KV) & 1, p.err, 29, abort);
-        for (int t = 0; t < n_q; ++t) {
-          tc::mbar_wait(p_full + t, j & 1, p.err, 35, abort);
-          tc::fence_after();
-          issue_pv(t, j);
-          if (nxt) {
-            if (t == 0) {
-              tc::mbar_wait(k_full + (j + 1) % KK, ((j + 1) / KK) & 1, p.err, 34, abort);
-              tc::fence_after();
-            }
-            issue_s(t, j + 1);
-          }
-        }
-        tc::mma_commit(v_empty + j % KV);
-        if (nxt) tc::mma_commit(k_empty + (j + 1) % KK);
+        tc::mma_commit(p_empty + (i & 1));
+        tc::mma_commit(v_empty + slot);
       }
       tc::mma_commit(o_full);
     }
-  } else if (warp >= 4) {
-    // ---- softmax: warps 4-7 tile 0, 8-11 tile 1; thread = query row, all
-    // 128 keys of a tile; two passes over S in tensor memory (maximum, then
-    // P = 2^(s scale - m) written over S's first 64 columns as bf16 pairs)
-    const int t = (warp - 4) >> 2, q4 = warp & 3;
-    const int row = kRowsPerBlock * t + 32 * q4 + lane, r = r_cta + row;
+  } else {
+    // ---- softmax warps: two per TMEM lane quarter (warps 2-5: keys 0-63 of a
+    // tile, warps 7-10: keys 64-127); thread = query row; the pair exchanges
+    // its halves' maxima through shared memory (named barrier 1 + quarter)
+    const int half = warp >= 7 ? 1 : 0;
+    const int q4 = warp & 3, row = 32 * q4 + lane, r = r_cta + row;
     const bool ok = r < rows_total;
-    const int lim = p.causal ? p.n_prefix + (ok ? r / p.G : 0) : n_keys - 1;
+    const int lim = p.causal ? n_prefix + (ok ? r / p.G : 0) : n_keys - 1;
     const int last = min(k_end - 1, lim);  // last key this row sees in the block's range
     const float NEG = __int_as_float(0xff800000);
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    float m = NEG, l = 0.0f;
-    if (t < n_q) {
-      for (int j = 0; j < n_kt; ++j) {
-        tc::mbar_wait(s_full + t, j & 1, p.err, 36, abort);
-        tc::fence_after();
-        const int nvalid = min(128, last - (k_begin + 128 * j) + 1);  // <= 0: none
-        // pass 1: the maximum of the raw scores (the scale is positive)
-        float a0 = NEG, a1 = NEG, a2 = NEG, a3 = NEG;
+    float *xch = (float *)(base + S::xch);  // [2 halves][128 rows]
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;\n" ::"r"(1 + q4) : "memory"); };
+    float m = NEG, l = 0.0f;  // l: this half's share of the row sum
+    for (int i = 0; i < n_kt; ++i) {
+      const int buf = i & 1;
+      tc::mbar_wait(s_full + buf, (i >> 1) & 1, p.err, 36, abort);
+      tc::fence_after();
+      const int key_base = k_begin + 128 * i + 64 * half;
+      uint32_t x[2][32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t x[2][32];
+      for (int c = 0; c < 2; ++c) tc::tmem_ld32(t_s + buf * 128 + lane_off + 64 * half + 32 * c, x[c]);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) tc::tmem_ld32(t_s(t) + lane_off + 64 * h + 32 * c, x[c]);
+      for (int c = 0; c < 2; ++c) tc::tmem_ld_wait(x[c]);  // ties every loaded register to the wait
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) attn_arrive(s_empty + buf);
+      // keys this row must not see are -inf (only in a half that holds some)
+      const int nvalid = min(64, last - key_base + 1);  // <= 0: none
+      if (nvalid < 64) {
 #pragma unroll
-          for (int c = 0; c < 2; ++c) tc::tmem_ld_wait(x[c]);
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 4) {
-              const int k0 = 64 * h + 32 * c + jj;
-              a0 = fmaxf(a0, k0 < nvalid ? __uint_as_float(x[c][jj]) : NEG);
-              a1 = fmaxf(a1, k0 + 1 < nvalid ? __uint_as_float(x[c][jj + 1]) : NEG);
-              a2 = fmaxf(a2, k0 + 2 < nvalid ? __uint_as_float(x[c][jj + 2]) : NEG);
-              a3 = fmaxf(a3, k0 + 3 < nvalid ? __uint_as_float(x[c][jj + 3]) : NEG);
-            }
-        }
-        const float tmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.scale_log2;
-        const float m_new = fmaxf(m, tmax);
-        const bool grow = m_new > m + kRescaleLog2;  // false while both are -inf
-        const float m_old = m;
-        if (grow) m = m_new;
-        // rows whose maximum grew: O to the new reference, O <- O 2^(m_old - m),
-        // once P V of the previous tile has landed
-        float f = 1.0f;
-        if (__any_sync(0xffffffffu, grow) && j > 0) {
-          tc::mbar_wait(pv_done + t, (j - 1) & 1, p.err, 40, abort);
-          tc::fence_after();
-          f = grow ? ex2(m_old - m) : 1.0f;  // m_old = -inf: 0 (O holds zeros)
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(t_o(t) + lane_off + 32 * c, o);
-            tc::tmem_ld_wait(o);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * f);
-            tmem_st32(t_o(t) + lane_off + 32 * c, o);
-          }
-        }
-        // pass 2: P = 2^(x scale - m), one FMA and one ex2 per key, -inf keys 0;
-        // 64-key halves, each written (32 columns of bf16 pairs) over S columns
-        // this thread has already read
-        const float nmu = m == NEG ? 0.0f : -m;
-        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t x[2][32];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) tc::tmem_ld32(t_s(t) + lane_off + 64 * h + 32 * c, x[c]);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) tc::tmem_ld_wait(x[c]);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 2) {
-              const int k0 = 64 * h + 32 * c + jj;
-              const float p0 = k0 < nvalid ? ex2(fmaf(__uint_as_float(x[c][jj]), p.scale_log2, nmu)) : 0.0f;
-              const float p1 = k0 + 1 < nvalid ? ex2(fmaf(__uint_as_float(x[c][jj + 1]), p.scale_log2, nmu)) : 0.0f;
-              if ((jj & 6) == 0) s0 += p0 + p1;
-              else if ((jj & 6) == 2) s1 += p0 + p1;
-              else if ((jj & 6) == 4) s2 += p0 + p1;
-              else s3 += p0 + p1;
-              pk[jj >> 1] = pack_bf16(p0, p1);
-            }
-            tmem_st16(t_s(t) + lane_off + 32 * h + 16 * c, pk);
-          }
-        }
-        l = l * f + ((s0 + s1) + (s2 + s3));
-        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");  // P (and O) written before the release
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) attn_arrive(p_full + t);
+          for (int j = 0; j < 32; ++j)
+            if (32 * c + j >= nvalid) x[c][j] = 0xff800000u;
       }
+      // maximum of the raw scores of this half (the scale is positive), four
+      // chains, then the pair's maximum
+      float a0 = __int_as_float(0xff800000), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          a0 = fmaxf(a0, __uint_as_float(x[c][j]));
+          a1 = fmaxf(a1, __uint_as_float(x[c][j + 1]));
+          a2 = fmaxf(a2, __uint_as_float(x[c][j + 2]));
+          a3 = fmaxf(a3, __uint_as_float(x[c][j + 3]));
+        }
+      const float hmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      xch[half * 128 + row] = hmax;
+      pair_sync();
+      const float tmax = fmaxf(hmax, xch[(half ^ 1) * 128 + row]) * p.scale_log2;
+      pair_sync();  // both read before the next tile's maxima overwrite the slots
+      const float m_new = fmaxf(m, tmax);
+      const bool grow = m_new > m + kRescaleLog2;  // false while both are -inf; the same in both halves
+      // P tile i & 1 is free once P V of tile i - 2 is done
+      if (i >= 2) tc::mbar_wait(p_empty + (i & 1), ((i >> 1) - 1) & 1, p.err, 37, abort);
+      const float m_old = m;
+      if (grow) m = m_new;
+      // P = 2^(x scale - m): one FMA and one ex2 per key; -inf keys give 0.
+      // Each 32-key group goes to the row's P columns in tensor memory as
+      // soon as it is packed (this half: columns 32 half .. 32 half + 31).
+      const float nmu = m == NEG ? 0.0f : -m;
+      float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+      const uint32_t prow = t_p + 64 * (i & 1) + 32 * half + lane_off;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(x[c][j]), p.scale_log2, nmu));
+          const float p1 = ex2(fmaf(__uint_as_float(x[c][j + 1]), p.scale_log2, nmu));
+          if ((j & 6) == 0) s0 += p0 + p1;
+          else if ((j & 6) == 2) s1 += p0 + p1;
+          else if ((j & 6) == 4) s2 += p0 + p1;
+          else s3 += p0 + p1;
+          pk[j >> 1] = pack_bf16(p0, p1);
+        }
+        tmem_st16(prow + 16 * c, pk);
+      }
+      // rows whose maximum grew: O (and l) to the new reference, O <- O 2^(m_old - m);
+      // each half rescales its half of the O columns
+      float f = 1.0f;
+      if (__any_sync(0xffffffffu, grow) && i > 0) {
+        // O must hold P V of every earlier tile: wait for tile i - 1's
+        tc::mbar_wait(p_empty + ((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, 40, abort);
+        tc::fence_after();
+        f = grow ? ex2(m_old - m) : 1.0f;  // m_old = -inf: 0 (O holds zeros)
+#pragma unroll 1
+        for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(t_o + lane_off + 32 * c, o);
+          tc::tmem_ld_wait(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st32(t_o + lane_off + 32 * c, o);
+        }
+      }
+      l = l * f + ((s0 + s1) + (s2 + s3));
+      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");  // P (and O) written before the release
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) attn_arrive(p_full);
     }
-    // ---- output: TMEM -> shared rows (fp32, float4 slots rotated by row) ----
-    if (n_kt > 0 && t < n_q) {
+    // the row sum of both halves
+    xch[half * 128 + row] = l;
+    pair_sync();
+    const float lt = half ? xch[row] + l : l + xch[128 + row];  // keys 0-63 first
+    // ---- output: TMEM -> shared rows -> coalesced stores --------------------
+    if (n_kt > 0) {
       tc::mbar_wait(o_full, 0, p.err, 38, abort);
       tc::fence_after();
     }
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    float *orow = (float *)(base + S::stage) + (size_t)row * HD;
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+    float *orow = (float *)(base + S::kring) + (size_t)row * HD;  // the K and V rings are idle now
 #pragma unroll 1
-    for (int c = 0; c < HD / 32; ++c) {
+    for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
       uint32_t v[32];
-      if (n_kt > 0 && t < n_q) {
-        tc::tmem_ld32(t_o(t) + lane_off + 32 * c, v);
+      if (n_kt > 0) {
+        tc::tmem_ld32(t_o + lane_off + 32 * c, v);
         tc::tmem_ld_wait(v);
       } else {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) v[jj] = 0u;
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
       }
       const float sc = p.out ? inv : 1.0f;  // split blocks keep the unnormalised sum
 #pragma unroll
-      for (int jj = 0; jj < 32; jj += 4) {
-        const int qd = ((32 * c + jj) >> 2) ^ (row & 7);
-        *(float4 *)(orow + 4 * qd) = make_float4(__uint_as_float(v[jj]) * sc, __uint_as_float(v[jj + 1]) * sc,
-                                                 __uint_as_float(v[jj + 2]) * sc, __uint_as_float(v[jj + 3]) * sc);
+      for (int j = 0; j < 32; j += 4) {  // float4 slot rotated by row: conflict-free
+        const int q = ((32 * c + j) >> 2) ^ (row & 7);
+        *(float4 *)(orow + 4 * q) = make_float4(__uint_as_float(v[j]) * sc, __uint_as_float(v[j + 1]) * sc,
+                                                __uint_as_float(v[j + 2]) * sc, __uint_as_float(v[j + 3]) * sc);
       }
     }
-    if (!p.out) ((float2 *)(base + S::ml))[row] = make_float2(m, l);  // split blocks: the row's softmax state
+    if (!p.out && half == 0) ((float2 *)(base + S::vring))[row] = make_float2(m, lt);  // split blocks: the row's softmax state
   }
   __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
@@ -525,45 +521,77 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(512u));
   }
-  const float *stage = (const float *)(base + S::stage);
   if (p.out) {
     // Rows out of shared memory, one warp per row, lanes along hd.
-    for (int rr = warp; rr < kBlockRows; rr += kAttnThreads / 32) {
+    const float *stage = (const float *)(base + S::kring);
+    for (int rr = warp; rr < 128; rr += kAttnThreads / 32) {
       const int r = r_cta + rr;
       if (r >= rows_total) break;
-      const int tk = r / p.G, h = g * p.G + r % p.G;
+      const int t = tok0 + r / p.G, h = g * p.G + r % p.G;
       for (int c4 = lane; c4 < HD / 4; c4 += 32) {
         const float4 v = *(const float4 *)(stage + (size_t)rr * HD + 4 * (c4 ^ (rr & 7)));
         uint2 w;
         w.x = pack_bf16(v.x, v.y);
         w.y = pack_bf16(v.z, v.w);
-        *(uint2 *)(p.out + (p.out_tiles ? tiled_index(p.n_new, p.Hq * HD, tk, h * HD + 4 * c4)
-                                        : ((size_t)tk * p.Hq + h) * HD + 4 * c4)) = w;
+        *(uint2 *)(p.out + (p.out_tiles ? tiled_index(p.n_req * p.n_new, p.Hq * HD, t, h * HD + 4 * c4)
+                                        : ((size_t)t * p.Hq + h) * HD + 4 * c4)) = w;
       }
     }
     return;
   }
-  // Split-KV merge inside the cluster of this query tile pair's blocks.
-  // Block z owns rows [z n, z n + n), n = ceil(256 / NS); it reads the
-  // partial rows and softmax states of those rows from every peer's shared
-  // memory (distributed shared memory loads) and merges them (weights
-  // 2^(m_s - m*)); a closing cluster barrier keeps every block's shared
-  // memory alive until its peers have read it.
-  const int NS = gridDim.z;
-  const int n_own = (kBlockRows + NS - 1) / NS;
+  // Split-KV merge inside the cluster of this query tile's blocks.  Block z
+  // owns rows [z n, z n + n), n = ceil(128 / NS) rounded up to even (16-byte
+  // aligned softmax-state rows); every block sends its staged
+  // output rows and softmax states of those rows to their owner with bulk
+  // shared-to-shared copies (into the owner's idle V ring past its first
+  // 8 KB), and the owner merges the NS partials (weights 2^(m_s - m*)) in
+  // shared memory.
+  const int NS = p.splits;
+  const int n_own = (((128 + NS - 1) / NS) + 1) & ~1;
+  const uint32_t o_slot = (uint32_t)n_own * HD * 4, ml_slot = (uint32_t)n_own * 8;
+  const uint32_t slot_bytes = o_slot + ml_slot;
+  const float *stage = (const float *)(base + S::kring);
+  const float2 *ml_stage = (const float2 *)(base + S::vring);
+  unsigned char *recv = base + S::recv;           // (NS - 1) slots: O rows, then (m, l) pairs
+  uint64_t *rbar = r_full;
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the copies read the staged rows
   __syncwarp();
-  tc::cluster_sync();  // every block's rows and states are staged (release / acquire)
-  const int z = split, r0 = z * n_own, n_mine = max(0, min(kBlockRows, r0 + n_own) - r0);
+  tc::cluster_sync();  // every block staged; every block's V ring is idle
+  const int z = split, r0 = z * n_own, n_mine = max(0, min(128, r0 + n_own) - r0);
+  if (threadIdx.x == 0) {
+    tc::mbar_expect_tx(rbar, (uint32_t)(NS - 1) * ((uint32_t)n_mine * HD * 4 + (uint32_t)((n_mine + 1) & ~1) * 8));
+    for (int q = 1; q < NS; ++q) {
+      const int j = (z + q) % NS, jr0 = j * n_own, nj = max(0, min(128, jr0 + n_own) - jr0);
+      if (nj == 0) continue;
+      const int slot = z < j ? z : z - 1;
+      const uint32_t dst = tc::cluster_addr(tc::smem_u32(recv) + slot * slot_bytes, (uint32_t)j);
+      const uint32_t bar = tc::cluster_addr(tc::smem_u32(rbar), (uint32_t)j);
+      tc::bulk_copy_to_peer(dst, tc::smem_u32(stage + (size_t)jr0 * HD), (uint32_t)nj * HD * 4, bar);
+      tc::bulk_copy_to_peer(dst + o_slot, tc::smem_u32(ml_stage + jr0), (uint32_t)((nj + 1) & ~1) * 8, bar);
+    }
+  }
+  if (n_mine > 0) tc::mbar_wait(rbar, 0, p.err, 41, abort);
+  // Once per owned row: the partials' weights 2^(m_s - m*) (0 for a split
+  // that saw no key), 1 / L and the output row (token, head), into the idle
+  // V ring past the staged softmax states; then every thread merges float4
+  // columns with them.
   const float NEG = __int_as_float(0xff800000);
-  float *wtab = (float *)(base + S::q);       // [n_own][8] weights, then [n_own] 1 / L (the Q tiles are idle)
-  int *otab = (int *)(wtab + 9 * n_own);      // [n_own] (token << 12) | head, -1 past the rows
-  const uint32_t stage_sa = tc::smem_u32(stage), ml_sa = tc::smem_u32(base + S::ml);
+  float *wtab = (float *)(base + S::vring + 2048);  // [n_own][8] weights, then [n_own] 1 / L
+  int *otab = (int *)(wtab + 9 * n_own);            // [n_own] (token << 12) | head, -1 past the rows
   for (int lr = threadIdx.x; lr < n_mine; lr += kAttnThreads) {
     const int rr = r0 + lr, r = r_cta + rr;
     float2 ml[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      ml[q] = q < NS ? ld_cluster_f2(tc::cluster_addr(ml_sa + (uint32_t)rr * 8, (uint32_t)q)) : make_float2(NEG, 0.0f);
+    for (int q = 0; q < 8; ++q) {
+      if (q >= NS) {
+        ml[q] = make_float2(NEG, 0.0f);
+      } else if (q == z) {
+        ml[q] = ml_stage[rr];
+      } else {
+        const unsigned char *sl = recv + (size_t)(q < z ? q : q - 1) * slot_bytes;
+        ml[q] = ((const float2 *)(sl + o_slot))[lr];
+      }
+    }
     float mx = NEG;
 #pragma unroll
     for (int q = 0; q < 8; ++q) mx = fmaxf(mx, ml[q].x);
@@ -578,47 +606,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       wtab[lr * 8 + q] = w;
     }
     wtab[8 * n_own + lr] = L > 0.0f ? 1.0f / L : 0.0f;
-    otab[lr] = r < rows_total ? ((r / p.G) << 12) | (g * p.G + r % p.G) : -1;
+    otab[lr] = r < rows_total ? ((tok0 + r / p.G) << 12) | (g * p.G + r % p.G) : -1;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < n_mine * (HD / 4); idx += kAttnThreads) {
     const int lr = idx / (HD / 4), c4 = idx - lr * (HD / 4), rr = r0 + lr;
     const int th = otab[lr];
     if (th < 0) continue;
-    const uint32_t off = ((uint32_t)rr * HD + 4 * (c4 ^ (rr & 7))) * 4;  // the staging order travels with the rows
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const float w = q < NS ? wtab[lr * 8 + q] : 0.0f;
       if (w == 0.0f) continue;
-      const float4 o = tc::ld_cluster_f4(tc::cluster_addr(stage_sa + off, (uint32_t)q));
+      const float *rows = q == z ? stage + (size_t)rr * HD
+                                 : (const float *)(recv + (size_t)(q < z ? q : q - 1) * slot_bytes) + (size_t)lr * HD;
+      const float4 o = *(const float4 *)(rows + 4 * (c4 ^ (rr & 7)));  // the staging order travels with the rows
       acc.x += w * o.x;
       acc.y += w * o.y;
       acc.z += w * o.z;
       acc.w += w * o.w;
     }
     const float invL = wtab[8 * n_own + lr];
-    const int tk = th >> 12, h = th & 4095;
+    const int t = th >> 12, h = th & 4095;
     uint2 v;
     v.x = pack_bf16(acc.x * invL, acc.y * invL);
     v.y = pack_bf16(acc.z * invL, acc.w * invL);
-    *(uint2 *)(p.final_out + (p.out_tiles ? tiled_index(p.n_new, p.Hq * HD, tk, h * HD + 4 * c4)
-                                          : ((size_t)tk * p.Hq + h) * HD + 4 * c4)) = v;
+    *(uint2 *)(p.final_out + (p.out_tiles ? tiled_index(p.n_req * p.n_new, p.Hq * HD, t, h * HD + 4 * c4)
+                                          : ((size_t)t * p.Hq + h) * HD + 4 * c4)) = v;
   }
   __syncwarp();
-  tc::cluster_sync();  // every peer has read this block's rows
+  tc::cluster_sync();  // every copy out of this block's shared memory has landed
 }
 
 struct SplitPlan {
   int splits, keys_per_split;
 };
 
-SplitPlan plan_splits(const AttnShape &s) {
+// Key splits of one request with n_prefix cached keys (a batch of requests
+// uses each request's own plan, so that its results do not depend on the
+// others': the batch's grid has the largest split count, and a request's
+// splits past its own are empty).
+SplitPlan plan_splits(const AttnShape &s, int n_prefix) {
   const int G = s.Hq / s.Hkv;
-  const int base = s.Hkv * ceil_div(G * s.n_new, kBlockRows);
-  const int n_keys = s.n_prefix + s.n_new;
+  const int base = s.Hkv * ceil_div(G * s.n_new, kRowsPerBlock);
+  const int n_keys = n_prefix + s.n_new;
   const int n_kb = ceil_div(n_keys, kKeysPerTile);
-  int splits = 148 / base;  // about one wave: one ~196 KB block per SM
+  int splits = 148 / base;  // about one wave: one 192 KB block per SM
   if (splits > 8) splits = 8;  // the blocks of a query tile form one (portable) cluster
   if (splits > n_kb) splits = n_kb;
   if (splits < 1) splits = 1;
@@ -703,6 +736,7 @@ cudaError_t attn_map(CUtensorMap *map, const void *ptr, int rank, const uint64_t
 
 template <int HD>
 cudaError_t launch_attn(const CUtensorMap &tq, const AttnParams &p, dim3 grid, cudaStream_t st) {
+  // the key splits of one request's query tile form a cluster (grid.z = requests x splits)
   using S = AttnSmem<HD>;
   static_assert(S::bytes <= 232448, "shared memory of the attention kernel");
   static unsigned long long attr_set = 0;
@@ -726,11 +760,11 @@ cudaError_t launch_attn(const CUtensorMap &tq, const AttnParams &p, dim3 grid, c
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (grid.z > 1) {  // the key splits of a query tile: one cluster
+  if (p.splits > 1) {  // the key splits of a query tile: one cluster
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = 1;
     attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = grid.z;
+    attr[na].val.clusterDim.z = p.splits;
     ++na;
   }
   cfg.attrs = attr;
@@ -748,7 +782,16 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
     return cudaErrorInvalidValue;
   const int G = s.Hq / s.Hkv;
   if (128 % G) return cudaErrorInvalidValue;
-  const SplitPlan pl = plan_splits(s);
+  SplitPlan pl = plan_splits(s, s.n_prefix);
+  int req_kps[kMaxRequests] = {};
+  if (s.n_req > 1) {
+    pl.splits = 1;
+    for (int b = 0; b < s.n_req; ++b) {
+      const SplitPlan pb = plan_splits(s, s.req_prefix[b]);
+      req_kps[b] = pb.keys_per_split;
+      pl.splits = max(pl.splits, pb.splits);
+    }
+  }
   AttnParams p;
   p.q = q;
   p.k_pool = k_pool;
@@ -756,6 +799,14 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   p.page_table = page_table;
   p.n_prefix = s.n_prefix;
   p.n_new = s.n_new;
+  if (s.n_req < 1 || s.n_req > kMaxRequests) return cudaErrorInvalidValue;
+  p.n_req = s.n_req;
+  p.splits = pl.splits;
+  p.pages_per_req = s.pages_per_req;
+  for (int b = 0; b < kMaxRequests; ++b) {
+    p.req_prefix[b] = b < s.n_req ? s.req_prefix[b] : 0;
+    p.req_kps[b] = req_kps[b];
+  }
   p.Hq = s.Hq;
   p.Hkv = s.Hkv;
   p.G = G;
@@ -776,13 +827,20 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
   // lands as 128 rows (token, head of the group) of 128 bytes.
   CUtensorMap tq;
   {
-    const uint64_t dims[4] = {(uint64_t)s.hd, (uint64_t)G, (uint64_t)s.Hkv, (uint64_t)s.n_new};
+    const uint64_t dims[4] = {(uint64_t)s.hd, (uint64_t)G, (uint64_t)s.Hkv, (uint64_t)s.n_new * s.n_req};
     const uint64_t strides[3] = {(uint64_t)s.hd * 2, (uint64_t)G * s.hd * 2, (uint64_t)s.Hq * s.hd * 2};
     const uint32_t box[4] = {64, (uint32_t)G, 1, (uint32_t)(128 / G)};
     cudaError_t e = attn_map(&tq, q, 4, dims, strides, box);
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid(ceil_div(rows_total, kBlockRows), s.Hkv, pl.splits);
+  if (pl.splits > 1) {  // the peers' partial rows fit the V ring past its first 8 KB
+    const size_t n_own = (size_t)(((128 + pl.splits - 1) / pl.splits) + 1) & ~(size_t)1;
+    const size_t need = (size_t)(pl.splits - 1) * (n_own * s.hd * 4 + n_own * 8);
+    const size_t room = (s.hd == 128 ? AttnSmem<128>::pages - AttnSmem<128>::recv
+                                     : AttnSmem<64>::pages - AttnSmem<64>::recv);
+    if (need > room) return cudaErrorInvalidValue;
+  }
+  const dim3 grid(ceil_div(rows_total, kRowsPerBlock), s.Hkv, pl.splits * s.n_req);
   return s.hd == 128 ? launch_attn<128>(tq, p, grid, st) : launch_attn<64>(tq, p, grid, st);
 }
 

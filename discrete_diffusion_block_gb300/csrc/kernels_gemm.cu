@@ -15,9 +15,10 @@ namespace dg {
 
 namespace {
 
-// q/k/v projection: RoPE (rotate-half pairs (j, j+hd/2)) on q and k at
-// absolute position pos0 + token; q to [T][Hq*hd]; k and v straight into the
-// paged pool slice of this layer.  The tile holds whole heads (128 rows are
+// q/k/v projection: RoPE (rotate-half pairs (j, j+hd/2)) on q and k at each
+// row's absolute position (its request's first position + the row's index
+// within the request); q to [T][Hq*hd]; k and v straight into the paged pool
+// slice of this layer, through the row's request's page-table slice.  The tile holds whole heads (128 rows are
 // one head of 128 or two of 64).  Tokens are taken 64 at a time: their
 // cos/sin rows and page slots are staged in shared memory, then each thread
 // rotates two adjacent pairs (j, j+1) and (j+hd/2, j+1+hd/2) of one token and
@@ -34,8 +35,9 @@ struct EpiQkv {
     float *cs = (float *)extra;
     float *sn = cs + kTok * kMaxHalf;
     long long *slot = (long long *)(sn + kTok * kMaxHalf);
-    const int ps = o.pos0 + c.n0 + t0 + tid;
-    const long long page = tid < nt ? (long long)o.page_table[ps / o.pg] : 0;
+    const int rw = c.n0 + t0 + tid, ps = o.rows.pos(rw);
+    const long long page =
+        tid < nt ? (long long)o.page_table[o.rows.req(rw) * o.rows.pages_per_req + ps / o.pg] : 0;
     for (int i0 = 0; i0 < n4; i0 += 8 * nthr) {
       float4 rc[8], rs[8];
 #pragma unroll
@@ -43,7 +45,7 @@ struct EpiQkv {
         const int i = i0 + tid + nthr * u;
         if (i < n4) {
           const int t = i / q4, j4 = i - t * q4;
-          const size_t p = (size_t)(o.pos0 + c.n0 + t0 + t);
+          const size_t p = (size_t)o.rows.pos(c.n0 + t0 + t);
           rc[u] = ((const float4 *)(o.cos_t + p * half))[j4];
           rs[u] = ((const float4 *)(o.sin_t + p * half))[j4];
         }
@@ -131,7 +133,7 @@ struct EpiQkv {
               *(__nv_bfloat162 *)dst = __floats2bfloat162_rn(lo0, lo1);
               *(__nv_bfloat162 *)(dst + half) = __floats2bfloat162_rn(hi0, hi1);
             } else {  // pool: feature f of slot s in sub-block f/64, chunk ((f%64)/8) ^ (s%8)
-              const int s7 = (o.pos0 + c.n0 + t0 + t) & 7;
+              const int s7 = o.rows.pos(c.n0 + t0 + t) & 7;
               bf16 *row = base_kv + slot[t];
               const int f0 = j, f1 = j + half;
               *(__nv_bfloat162 *)(row + (size_t)(f0 >> 6) * o.pg * 64 + ((((f0 & 63) >> 3) ^ s7) << 3) + (f0 & 7)) =

@@ -6,10 +6,12 @@
 // vocab tile u / m_tiles and row block u % m_tiles, so the CTAs that share a
 // vocab tile run it at the same time and its weights are read from HBM once.
 //
-//   warp 0 (one thread)  TMA producer: per 64-wide K step the 128-row A box
+//   warp 0 (one thread)  producer: per 64-wide K step the 128-row A tile
 //                        (normalised rows, and the low half of their hi/lo
-//                        split) and the 256-row B box (W_out rows) into a
-//                        3-stage ring;
+//                        split) and the two 128-row tiles of 256 W_out rows
+//                        into a 3-stage ring; all operands are stored as
+//                        operand tiles (tiled_index), so each is one
+//                        contiguous bulk copy;
 //   warp 1 (one thread)  allocates all 512 TMEM columns (two 128 x 256 fp32
 //                        accumulators) and issues tcgen05.mma, unit n into
 //                        accumulator n & 1;
@@ -60,11 +62,15 @@ struct TmemRowSrc {
 };
 
 struct LmArgs {
+  const bf16 *xn, *xn_lo;   // normalised rows (hi, lo) as operand tiles of [T][K]
+  const bf16 *w;            // W_out as operand tiles of [V][K]
   int T, V, K;              // token rows, vocabulary, model width
   PartialPlanes P;          // partials planes [T][V/256] (modes 0, 2)
   float *logits;            // [T][V] fp32 (modes 1, 2)
   uint32_t ctr2, key0, key1;
   float inv_tau;            // 1 / temperature of the re-noise keys
+  int rows_per_req;         // > 0: row r is position r % rows_per_req of request r / rows_per_req,
+                            // whose Gumbel stream is keyed by the sample seed + request
   const StepParams *dyn;    // when set, the stream words and inv_tau come from device memory
   int *err;
 };
@@ -72,9 +78,7 @@ struct LmArgs {
 // MODE 0: sampler partials; MODE 1: fp32 logits; MODE 2: both, from the same
 // accumulator (so that the partials can be checked on the logits they came from).
 template <int NA, int MODE>
-__global__ void __launch_bounds__(kLmThreads, 1)
-    lm_head_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap ta2,
-                   const __grid_constant__ CUtensorMap tb, LmArgs g) {
+__global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(LmArgs g) {
   using S = LmSmem<NA>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -119,15 +123,29 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const uint32_t tmem = *tmem_slot;
   auto a_tile = [&](int s, int h) { return base + (size_t)s * S::stage_bytes + h * kLmABytes; };
   auto b_tile = [&](int s) { return base + (size_t)s * S::stage_bytes + NA * kLmABytes; };
+  // A tile of row block mt (the last block may be partial: its rows past T
+  // stay stale in shared memory, and their accumulator rows are never
+  // stored); the 256 W_out rows of vocab tile v as two full 128-row tiles.
+  auto a_bytes = [&](int mt) { return (uint32_t)min(128, g.T - 128 * mt) * 128; };
+  auto load_a = [&](int s, int mt, int kt) {
+    tc::bulk_load(a_tile(s, 0), g.xn + tiled_index(g.T, g.K, 128 * mt, 64 * kt), a_bytes(mt), full + s);
+    if (NA == 2)
+      tc::bulk_load(a_tile(s, 1), g.xn_lo + tiled_index(g.T, g.K, 128 * mt, 64 * kt), a_bytes(mt), full + s);
+  };
+  auto load_b = [&](int s, int v, int kt) {
+    for (int h = 0; h < 2; ++h)
+      tc::bulk_load(b_tile(s) + h * 16384, g.w + tiled_index(g.V, g.K, kVocabTile * v + 128 * h, 64 * kt), 16384u,
+                    full + s);
+  };
 
-  // The weights never change: the first unit's W_out boxes are requested
+  // The weights never change: the first unit's W_out tiles are requested
   // before waiting for the kernel that produced the normalised rows.
   const int pre = min(kLmStages, KT);
   if (warp == 0 && lane == 0) {
-    const int v = blockIdx.x / m_tiles;
+    const int v = blockIdx.x / m_tiles, mt = blockIdx.x - v * m_tiles;
     for (int i = 0; i < pre; ++i) {
-      tc::mbar_expect_tx(full + i, S::stage_bytes);
-      tc::tma_load_2d(b_tile(i), &tb, i * tc::kBK, v * kVocabTile, full + i);
+      tc::mbar_expect_tx(full + i, NA * a_bytes(mt) + kLmBBytes);
+      load_b(i, v, i);
     }
   }
   pdl_wait();
@@ -144,11 +162,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 11, abort);
           if (*abort) break;
           if (it >= pre) {
-            tc::mbar_expect_tx(full + s, S::stage_bytes);
-            tc::tma_load_2d(b_tile(s), &tb, kt * tc::kBK, v * kVocabTile, full + s);
+            tc::mbar_expect_tx(full + s, NA * a_bytes(mt) + kLmBBytes);
+            load_b(s, v, kt);
           }
-          tc::tma_load_2d(a_tile(s, 0), &ta, kt * tc::kBK, mt * 128, full + s);
-          if (NA == 2) tc::tma_load_2d(a_tile(s, 1), &ta2, kt * tc::kBK, mt * 128, full + s);
+          load_a(s, mt, kt);
         }
         if (*abort) break;
       }
@@ -226,7 +243,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       Partial p{};
       if (MODE != 1) {
         TmemRowSrc src{taddr};
-        p = row_tile_partial(src, v, (uint32_t)pos, c2, k0, k1, gbound, inv_tau);
+        const int b = g.rows_per_req > 0 ? pos / g.rows_per_req : 0;
+        const uint64_t seed = (((uint64_t)k1 << 32) | k0) + (uint64_t)b;
+        p = row_tile_partial(src, v, (uint32_t)(pos - b * g.rows_per_req), c2, (uint32_t)seed,
+                             (uint32_t)(seed >> 32), gbound, inv_tau);
       }
       // the accumulator is free for unit n + 2
       tc::fence_before();
@@ -265,8 +285,7 @@ int lm_num_sms() {
 }
 
 template <int NA, int MODE>
-cudaError_t launch_lm_head(const CUtensorMap &ta, const CUtensorMap &ta2, const CUtensorMap &tb,
-                           const LmArgs &g, cudaStream_t st) {
+cudaError_t launch_lm_head(const LmArgs &g, cudaStream_t st) {
   using S = LmSmem<NA>;
   static_assert(S::bytes <= 232448, "shared memory of the LM head");
   auto kern = lm_head_kernel<NA, MODE>;
@@ -285,39 +304,33 @@ cudaError_t launch_lm_head(const CUtensorMap &ta, const CUtensorMap &ta2, const 
   int grid = lm_num_sms() / m_tiles * m_tiles;
   if (grid < m_tiles) grid = m_tiles;
   if (grid > units) grid = units;
-  return launch_pdl(kern, dim3(grid), dim3(kLmThreads), S::bytes, st, ta, ta2, tb, g);
+  return launch_pdl(kern, dim3(grid), dim3(kLmThreads), S::bytes, st, g);
 }
 
 }  // namespace
-
-cudaError_t tmap_bf16_cached(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
-                             uint32_t box);
 
 static cudaError_t lm_head_launch(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, LmArgs &g, int mode, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (d % tc::kBK || V % kVocabTile) return cudaErrorInvalidValue;
-  CUtensorMap ta, ta2, tb;
-  cudaError_t e;
-  if ((e = tmap_bf16_cached(&ta, xn, T, d, 128)) != cudaSuccess) return e;
-  if ((e = tmap_bf16_cached(&ta2, xn_lo ? xn_lo : xn, T, d, 128)) != cudaSuccess) return e;
-  if ((e = tmap_bf16_cached(&tb, w_out, V, d, 256)) != cudaSuccess) return e;
+  g.xn = xn;
+  g.xn_lo = xn_lo;
+  g.w = w_out;
   g.T = T;
   g.V = V;
   g.K = d;
-  if (mode == 0)
-    return xn_lo ? launch_lm_head<2, 0>(ta, ta2, tb, g, st) : launch_lm_head<1, 0>(ta, ta2, tb, g, st);
-  if (mode == 2)
-    return xn_lo ? launch_lm_head<2, 2>(ta, ta2, tb, g, st) : launch_lm_head<1, 2>(ta, ta2, tb, g, st);
-  return xn_lo ? launch_lm_head<2, 1>(ta, ta2, tb, g, st) : launch_lm_head<1, 1>(ta, ta2, tb, g, st);
+  if (mode == 0) return xn_lo ? launch_lm_head<2, 0>(g, st) : launch_lm_head<1, 0>(g, st);
+  if (mode == 2) return xn_lo ? launch_lm_head<2, 2>(g, st) : launch_lm_head<1, 2>(g, st);
+  return xn_lo ? launch_lm_head<2, 1>(g, st) : launch_lm_head<1, 1>(g, st);
 }
 
 cudaError_t gemm_lm_head_partials(const bf16 *xn, const bf16 *xn_lo, const bf16 *w_out, int T, int d,
                                   int V, uint64_t seed, int canvas, int step, float inv_tau,
                                   void *partials, int *err, cudaStream_t st, const StepParams *dyn,
-                                  float *logits) {
+                                  float *logits, int rows_per_req) {
   LmArgs g{};
   g.inv_tau = inv_tau;
+  g.rows_per_req = rows_per_req;
   g.P = PartialPlanes::at(partials, T, V / kVocabTile);
   g.logits = logits;
   g.ctr2 = gumbel_ctr2(canvas, step);

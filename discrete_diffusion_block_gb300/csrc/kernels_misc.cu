@@ -131,13 +131,15 @@ __global__ void rope_table_kernel(float *ct, float *stt, int max_pos, int half, 
 }
 
 // x_1 ~ Unif(V^C): id = floor(word0 * V / 2^32), word0 of Philox at (i, 0, k, 2).
+// Request b (blockIdx.y) of a lockstep batch draws with sample seed + b.
 __global__ void canvas_init_kernel(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
-                                   uint32_t k0, uint32_t k1, int canvas) {
+                                   uint64_t seed, int canvas) {
   pdl_wait();
   pdl_trigger();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= C) return;
-  const U4 w = philox10((uint32_t)i, 0u, (uint32_t)canvas, kTagInit, k0, k1);
+  const int p = blockIdx.x * blockDim.x + threadIdx.x, b = blockIdx.y, i = b * C + p;
+  if (p >= C) return;
+  const uint64_t s = seed + (uint64_t)b;
+  const U4 w = philox10((uint32_t)p, 0u, (uint32_t)canvas, kTagInit, (uint32_t)s, (uint32_t)(s >> 32));
   x[i] = (int)(((uint64_t)w.w[0] * (uint64_t)V) >> 32);
   committed[i] = 0;
   last[i] = -1;
@@ -207,9 +209,16 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *
       o2[2 * c] = h01;
       o2[2 * c + 1] = h23;
     }
-    if (l2) {
-      l2[2 * c] = __floats2bfloat162_rn(y0 - __low2float(h01), y1 - __high2float(h01));
-      l2[2 * c + 1] = __floats2bfloat162_rn(y2 - __low2float(h23), y3 - __high2float(h23));
+    if (out_lo) {
+      const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - __low2float(h01), y1 - __high2float(h01));
+      const __nv_bfloat162 l23 = __floats2bfloat162_rn(y2 - __low2float(h23), y3 - __high2float(h23));
+      if (tiled_rows > 0) {
+        *(uint2 *)(out_lo + tiled_index(tiled_rows, d, t, 4 * c)) =
+            make_uint2(*(const uint32_t *)&l01, *(const uint32_t *)&l23);
+      } else {
+        l2[2 * c] = l01;
+        l2[2 * c + 1] = l23;
+      }
     }
   }
 }
@@ -344,14 +353,20 @@ __global__ void kv_append_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *
 
 }  // namespace
 
+namespace {
+thread_local bool t_pdl_suspended = false;
+}
+
 bool pdl_enabled() {
   static int on = -1;
   if (on < 0) {
     const char *v = getenv("DG_PDL");
-    on = (v && v[0] == '0') ? 0 : 1;
+    on = (v && v[0] == '1') ? 1 : 0;
   }
-  return on == 1;
+  return on == 1 && !t_pdl_suspended;
 }
+
+void pdl_suspend(bool suspended) { t_pdl_suspended = suspended; }
 
 static float weight_scale(float std_dev) {
   return (float)((double)std_dev * sqrt(3.0) / 8388608.0);
@@ -403,9 +418,9 @@ cudaError_t rope_table(float *ct, float *stt, int max_pos, int hd, float base, c
 }
 
 cudaError_t canvas_init(int *x, uint8_t *committed, int *last, int *stable, int C, int V,
-                        uint64_t seed, int canvas, cudaStream_t st) {
-  return launch_pdl(canvas_init_kernel, dim3(ceil_div(C, 256)), dim3(256), 0, st, x, committed, last, stable, C, V,
-                    (uint32_t)seed, (uint32_t)(seed >> 32), canvas);
+                        uint64_t seed, int canvas, cudaStream_t st, int n_req) {
+  return launch_pdl(canvas_init_kernel, dim3(ceil_div(C, 256), n_req), dim3(256), 0, st, x, committed, last, stable,
+                    C, V, seed, canvas);
 }
 
 cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d, cudaStream_t st) {
@@ -416,7 +431,7 @@ cudaError_t embed_rows(float *h, const bf16 *table, const int *ids, int T, int d
 cudaError_t rmsnorm_rows(bf16 *out, const float *h, const float *gain, int T, int d, float eps,
                          cudaStream_t st, bf16 *out_lo, bool tiled) {
   if (T == 0) return cudaSuccess;
-  if (d % 4 || (tiled && (d % 64 || out_lo))) return cudaErrorInvalidValue;
+  if (d % 4 || (tiled && d % 64)) return cudaErrorInvalidValue;
   return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, out, out_lo, h, gain, d, eps,
                     tiled ? T : 0);
 }

@@ -53,6 +53,163 @@ constexpr int kNormRegs = 12;
 constexpr int kPairIters = kRouteTok * 16 / kRouteThreads;  // pairs per thread at most (k <= 16)  // float4 columns per thread held in registers by the norm
 constexpr int kSmemBudget = 200 * 1024;  // dynamic; the expert sort adds 11 KB of static shared memory
 
+// ---------------------------------------------------------------------------
+// Placement of the routed pairs and copy of their token rows.
+// ---------------------------------------------------------------------------
+constexpr int kScatThreads = 256;
+
+inline size_t scatter_smem_ints(int ng, int E, int per) { return (size_t)ng * E + 2 * E + 2 * (size_t)per; }
+
+struct ScatArgs {
+  const bf16 *xn;
+  const int *ids, *gcount;
+  int *slot_row;  // in: rank within the token group; out: sorted row
+  bf16 *x_tiles;  // [item][d/64] tiles of 128 rows x 64 columns, swizzled
+  int T, d, E, k, tile_rows, ng;
+  int per;        // pairs per block
+  int *offs, *work, *n_work, *sync;
+  int max_work;
+  unsigned long long *stats;
+};
+
+// Exclusive prefix sum over the block of one value per thread (kScatThreads
+// threads); returns the prefix and stores the block total in *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncwarp();
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kScatThreads / 32; ++w) {
+    const int c = warp_tot[w];
+    before += w < warp ? c : 0;
+    all += c;
+  }
+  __syncwarp();
+  __syncthreads();  // warp_tot may be reused by the next scan
+  *total = all;
+  return before + x - v;
+}
+
+// The scatter work of block `blk` (kScatThreads threads): its share of the
+// pairs, and (blk 0) the expert segments, the work list and the FFN's
+// counters.  tab: shared memory of scatter_smem_ints() ints.
+__device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *tab, int *warp_tot) {
+  // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]; then
+  // the expert and group rank of each of this block's pairs
+  const int E = a.E, ng = a.ng, n = ng * E;
+  int *soffs = tab + n, *stoff = soffs + E, *s_ex = stoff + E, *s_rk = s_ex + a.per;
+  const int TK = a.T * a.k;
+  const int p0 = blk * a.per, p1 = min(TK, p0 + a.per);
+  // the block's pairs and the group counts: all loads in flight together
+  for (int i = threadIdx.x; i < p1 - p0; i += kScatThreads) {
+    s_ex[i] = a.ids[p0 + i];
+    s_rk[i] = a.slot_row[p0 + i];
+  }
+  for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
+  __syncwarp();
+  __syncthreads();
+  const int e = threadIdx.x;  // E <= kScatThreads
+  int tot = 0;
+  if (e < E)
+    for (int g = 0; g < ng; ++g) {
+      const int c = tab[g * E + e];
+      tab[g * E + e] = tot;
+      tot += c;
+    }
+  int total, n_items;
+  const int off = block_exclusive_scan(tot, warp_tot, &total);
+  const int tiles = e < E ? (tot + a.tile_rows - 1) / a.tile_rows : 0;
+  const int toff = block_exclusive_scan(tiles, warp_tot, &n_items);
+  if (e < E) {
+    soffs[e] = off;
+    stoff[e] = toff;
+  }
+  if (blk == 0) {  // the expert segments and the work list of the expert FFN
+    int touched;
+    block_exclusive_scan(e < E && tot > 0 ? 1 : 0, warp_tot, &touched);
+    if (e < E) {
+      a.offs[e] = off;
+      for (int j = 0; j < tiles; ++j) {
+        a.work[2 * (toff + j)] = e;
+        a.work[2 * (toff + j) + 1] = j * a.tile_rows;
+      }
+    }
+    if (threadIdx.x == 0) {
+      a.offs[E] = total;
+      *a.n_work = n_items;
+      if (a.stats) {  // experts whose weights the expert FFN streams, and their rows
+        atomicAdd(&a.stats[0], (unsigned long long)touched);
+        atomicAdd(&a.stats[1], (unsigned long long)total);
+      }
+    }
+    for (int i = threadIdx.x; i <= a.max_work; i += kScatThreads) a.sync[i] = 0;  // FFN counters
+  }
+  __syncwarp();
+  __syncthreads();
+  // Pairs of this block: one warp per pair, two pairs at a time; the warp
+  // copies the token's row into row r of its item's tiles (16-byte chunk c of
+  // k-tile kt at chunk position c ^ (r % 8): the tensor core's swizzled
+  // operand order), both rows' loads in flight before any store.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
+  constexpr int NW = kScatThreads / 32, U = 12;
+  for (int pb = p0 + warp; pb < p1; pb += 2 * NW) {
+    const uint4 *src[2];
+    uint4 *dst[2];
+    int rr[2];
+    bool ok[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int p = pb + q * NW;
+      ok[q] = p < p1;
+      src[q] = nullptr;
+      dst[q] = nullptr;
+      rr[q] = 0;
+      if (ok[q]) {
+        const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
+        const int within = tab[g * E + ex] + s_rk[p - p0];  // rank among the expert's rows
+        if (lane == 0) a.slot_row[p] = soffs[ex] + within;
+        const int item = stoff[ex] + within / a.tile_rows;
+        rr[q] = within % a.tile_rows;
+        src[q] = (const uint4 *)(a.xn + (size_t)t * a.d);
+        dst[q] = (uint4 *)(a.x_tiles + (size_t)item * KT * (128 * 64)) + rr[q] * 8;
+      }
+    }
+    for (int c0 = 0; c0 < vec; c0 += 32 * U) {
+      uint4 v[2][U];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (ok[q] && c < vec) v[q][u] = src[q][c];
+        }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (ok[q] && c < vec) dst[q][(c >> 3) * 1024 + ((c & 7) ^ (rr[q] & 7))] = v[q][u];
+        }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
+  extern __shared__ int tab[];
+  __shared__ int warp_tot[kScatThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  scatter_block(a, blockIdx.x, tab, warp_tot);
+}
+
 struct RouteArgs {
   const float *h;      // norm: input rows fp32 [T][d]
   const float *gain;   // norm: RMSNorm gain [d]
@@ -66,6 +223,11 @@ struct RouteArgs {
   int *rank;           // [T*k] rank of each pair among its group's pairs of the same expert
   int *gcount;         // [ceil(T/32)][E] pairs per (token group, expert)
   int *err;
+  // fused scatter: after a grid-wide barrier (bar: count, generation), every
+  // CTA runs its share of the scatter (sc, with sc.per pairs per CTA)
+  int fuse;
+  int *bar;
+  ScatArgs sc;
 };
 
 struct RouteSmem {
@@ -104,6 +266,12 @@ __device__ __forceinline__ void load_w_tile(const bf16 *wr, int E, int KT, int m
     const int rows = min(128, E - 128 * mt);
     bulk_load(stage + mt * kWBox, wr + ((size_t)128 * KT * mt + (size_t)rows * kt) * 64, (uint32_t)rows * 128, bar);
   }
+}
+
+__device__ __forceinline__ int ld_acquire_s32(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
@@ -257,7 +425,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
   }
   pdl_wait();
-  pdl_trigger();
+  if (!a.fuse) pdl_trigger();  // fused: the expert FFN may launch only once the scatter's barrier is passed
   if (threadIdx.x == 0 && a.err && *(volatile int *)a.err) *abort = 1;  // an earlier timeout
 
   if (NORM) {
@@ -488,6 +656,42 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncwarp();
   tc::cluster_sync();  // peers' counts stay alive until every read is done
+  if (!a.fuse) return;
+  // ---- fused scatter ------------------------------------------------------
+  // Every token group's counts and ranks are in global memory once all CTAs
+  // pass a grid-wide barrier (the launch is cooperative: all CTAs are
+  // resident).  Self-resetting: each CTA reads the generation word, then
+  // arrives; the last to arrive zeroes the count and bumps the generation,
+  // which the others wait for (bounded).  Then this CTA's share of the
+  // scatter reuses its shared memory.
+  __syncthreads();
+  __shared__ int passed;
+  if (threadIdx.x == 0) {
+    int *gen = a.bar + 1;
+    const int g0 = ld_acquire_s32(gen);
+    __threadfence();  // this CTA's counts and ranks before its arrival
+    passed = 1;
+    if (atomicAdd(a.bar, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.bar, 0);
+      __threadfence();
+      atomicExch(gen, g0 + 1);
+    } else {
+      const long long c0 = clock64();
+      while (ld_acquire_s32(gen) == g0) {
+        if (clock64() - c0 > tc::kWaitCycles) {
+          if (a.err) atomicExch(a.err, 55);
+          passed = 0;  // counts may be incomplete: leave the scatter undone
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  pdl_trigger();
+  if (!passed) return;
+  __shared__ int warp_tot[kScatThreads / 32];
+  scatter_block(a.sc, blockIdx.x, (int *)base, warp_tot);
 }
 
 template <bool NORM>
@@ -511,7 +715,7 @@ cudaError_t launch_route(const CUtensorMap &tx, RouteArgs a, cudaStream_t st) {
   cfg.blockDim = dim3(kRouteThreads, 1, 1);
   cfg.dynamicSmemBytes = L.bytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
   if (pdl_enabled()) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -523,14 +727,21 @@ cudaError_t launch_route(const CUtensorMap &tx, RouteArgs a, cudaStream_t st) {
   attr[na].val.clusterDim.y = 1;
   attr[na].val.clusterDim.z = 1;
   ++na;
+  if (a.fuse) {  // the CTAs wait on one another at the scatter's barrier: all must be resident
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, tx, a);
 }
 
+int num_sms_route();
+
 cudaError_t route_common(bool norm, const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr,
                          int T, int d, int E, int k, int *ids, float *gates, int *rank, int *gcount, int *err,
-                         cudaStream_t st) {
+                         cudaStream_t st, const ScatArgs *fused = nullptr, int *bar = nullptr) {
   if (T < 0 || d < 64 || d % 64 || E < 1 || E > 256 || k < 1 || k > 16 || k > E) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
   RouteArgs a = {};
@@ -556,160 +767,21 @@ cudaError_t route_common(bool norm, const float *h, const float *gain, float eps
   a.gcount = gcount;
   a.err = err;
   a.wr = wr;
+  if (fused) {
+    a.fuse = 1;
+    a.bar = bar;
+    a.sc = *fused;
+    const int grid = ceil_div(T, kRouteTok) * a.S;
+    a.sc.per = ceil_div(T * k, grid);
+    const RouteSmem full = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
+    if (scatter_smem_ints(a.sc.ng, E, a.sc.per) * sizeof(int) > full.bytes - 1024) return cudaErrorInvalidValue;
+  }
   CUtensorMap tx{};  // the norm path writes the B operand itself
   if (norm) return launch_route<true>(tx, a, st);
   cudaError_t e;
   e = tmap_bf16_cached(&tx, xn, (uint64_t)T, (uint64_t)d, kRouteTok);
   if (e != cudaSuccess) return e;
   return launch_route<false>(tx, a, st);
-}
-
-// ---------------------------------------------------------------------------
-// Placement of the routed pairs and copy of their token rows.
-// ---------------------------------------------------------------------------
-constexpr int kScatThreads = 256;
-
-struct ScatArgs {
-  const bf16 *xn;
-  const int *ids, *gcount;
-  int *slot_row;  // in: rank within the token group; out: sorted row
-  bf16 *x_tiles;  // [item][d/64] tiles of 128 rows x 64 columns, swizzled
-  int T, d, E, k, tile_rows, ng;
-  int per;        // pairs per block
-  int *offs, *work, *n_work, *sync;
-  int max_work;
-  unsigned long long *stats;
-};
-
-// Exclusive prefix sum over the block of one value per thread (kScatThreads
-// threads); returns the prefix and stores the block total in *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncwarp();
-  __syncthreads();
-  int before = 0, all = 0;
-#pragma unroll
-  for (int w = 0; w < kScatThreads / 32; ++w) {
-    const int c = warp_tot[w];
-    before += w < warp ? c : 0;
-    all += c;
-  }
-  __syncwarp();
-  __syncthreads();  // warp_tot may be reused by the next scan
-  *total = all;
-  return before + x - v;
-}
-
-__global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
-  // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]; then
-  // the expert and group rank of each of this block's pairs
-  extern __shared__ int tab[];
-  __shared__ int warp_tot[kScatThreads / 32];
-  pdl_wait();
-  pdl_trigger();
-  const int E = a.E, ng = a.ng, n = ng * E;
-  int *soffs = tab + n, *stoff = soffs + E, *s_ex = stoff + E, *s_rk = s_ex + a.per;
-  const int TK = a.T * a.k;
-  const int p0 = blockIdx.x * a.per, p1 = min(TK, p0 + a.per);
-  // the block's pairs and the group counts: all loads in flight together
-  for (int i = threadIdx.x; i < p1 - p0; i += kScatThreads) {
-    s_ex[i] = a.ids[p0 + i];
-    s_rk[i] = a.slot_row[p0 + i];
-  }
-  for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
-  __syncwarp();
-  __syncthreads();
-  const int e = threadIdx.x;  // E <= kScatThreads
-  int tot = 0;
-  if (e < E)
-    for (int g = 0; g < ng; ++g) {
-      const int c = tab[g * E + e];
-      tab[g * E + e] = tot;
-      tot += c;
-    }
-  int total, n_items;
-  const int off = block_exclusive_scan(tot, warp_tot, &total);
-  const int tiles = e < E ? (tot + a.tile_rows - 1) / a.tile_rows : 0;
-  const int toff = block_exclusive_scan(tiles, warp_tot, &n_items);
-  if (e < E) {
-    soffs[e] = off;
-    stoff[e] = toff;
-  }
-  if (blockIdx.x == 0) {  // the expert segments and the work list of the expert FFN
-    int touched;
-    block_exclusive_scan(e < E && tot > 0 ? 1 : 0, warp_tot, &touched);
-    if (e < E) {
-      a.offs[e] = off;
-      for (int j = 0; j < tiles; ++j) {
-        a.work[2 * (toff + j)] = e;
-        a.work[2 * (toff + j) + 1] = j * a.tile_rows;
-      }
-    }
-    if (threadIdx.x == 0) {
-      a.offs[E] = total;
-      *a.n_work = n_items;
-      if (a.stats) {  // experts whose weights the expert FFN streams, and their rows
-        atomicAdd(&a.stats[0], (unsigned long long)touched);
-        atomicAdd(&a.stats[1], (unsigned long long)total);
-      }
-    }
-    for (int i = threadIdx.x; i <= a.max_work; i += kScatThreads) a.sync[i] = 0;  // FFN counters
-  }
-  __syncwarp();
-  __syncthreads();
-  // Pairs of this block: one warp per pair, two pairs at a time; the warp
-  // copies the token's row into row r of its item's tiles (16-byte chunk c of
-  // k-tile kt at chunk position c ^ (r % 8): the tensor core's swizzled
-  // operand order), both rows' loads in flight before any store.
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
-  constexpr int NW = kScatThreads / 32, U = 12;
-  for (int pb = p0 + warp; pb < p1; pb += 2 * NW) {
-    const uint4 *src[2];
-    uint4 *dst[2];
-    int rr[2];
-    bool ok[2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int p = pb + q * NW;
-      ok[q] = p < p1;
-      src[q] = nullptr;
-      dst[q] = nullptr;
-      rr[q] = 0;
-      if (ok[q]) {
-        const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
-        const int within = tab[g * E + ex] + s_rk[p - p0];  // rank among the expert's rows
-        if (lane == 0) a.slot_row[p] = soffs[ex] + within;
-        const int item = stoff[ex] + within / a.tile_rows;
-        rr[q] = within % a.tile_rows;
-        src[q] = (const uint4 *)(a.xn + (size_t)t * a.d);
-        dst[q] = (uint4 *)(a.x_tiles + (size_t)item * KT * (128 * 64)) + rr[q] * 8;
-      }
-    }
-    for (int c0 = 0; c0 < vec; c0 += 32 * U) {
-      uint4 v[2][U];
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + lane + 32 * u;
-          if (ok[q] && c < vec) v[q][u] = src[q][c];
-        }
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + lane + 32 * u;
-          if (ok[q] && c < vec) dst[q][(c >> 3) * 1024 + ((c & 7) ^ (rr[q] & 7))] = v[q][u];
-        }
-    }
-  }
 }
 
 int num_sms_route() {
@@ -740,12 +812,13 @@ cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k
                       gcount, err, st);
 }
 
-cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
-                        int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
-                        cudaStream_t st, unsigned long long *stats) {
+namespace {
+
+cudaError_t scatter_args(ScatArgs &a, const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T,
+                         int d, int E, int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work,
+                         int max_work, unsigned long long *stats) {
   if (T < 0 || d % 64 || E < 1 || E > kScatThreads || k < 1 || tile_rows != 128) return cudaErrorInvalidValue;
   if ((size_t)max_work < moe_max_work(T, k, E, tile_rows)) return cudaErrorInvalidValue;
-  ScatArgs a;
   a.xn = xn;
   a.ids = ids;
   a.gcount = gcount;
@@ -763,14 +836,26 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
   a.sync = work + 2 * max_work;
   a.max_work = max_work;
   a.stats = stats;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
+                        int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
+                        cudaStream_t st, unsigned long long *stats) {
+  ScatArgs a;
+  cudaError_t e = scatter_args(a, xn, ids, gcount, slot_row, T, d, E, k, tile_rows, x_tiles, offs, work, n_work,
+                               max_work, stats);
+  if (e != cudaSuccess) return e;
   const int TK = T * k;
   const int grid = max(1, min(ceil_div(TK, 2 * (kScatThreads / 32)), 2 * num_sms_route()));
   a.per = ceil_div(TK, grid);
-  const size_t smem = ((size_t)a.ng * E + 2 * E + 2 * (size_t)a.per) * sizeof(int);
+  const size_t smem = scatter_smem_ints(a.ng, E, a.per) * sizeof(int);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static unsigned long long attr_set = 0;
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
     e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -778,6 +863,32 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
     if (dev < 64) attr_set |= 1ull << dev;
   }
   return launch_pdl(scatter_kernel, dim3(grid), dim3(kScatThreads), smem, st, a);
+}
+
+cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
+                              int E, int k, int *ids, float *gates, int *slot_row, int *gcount, bf16 *x_tiles,
+                              int *offs, int *work, int *n_work, int max_work, int *bar, int *err, cudaStream_t st,
+                              unsigned long long *stats, int *launches) {
+  const bool norm = h != nullptr;
+  const int S = (d / 64) >= 8 ? 8 : (d / 64) >= 4 ? 4 : (d / 64) >= 2 ? 2 : 1;
+  const int grid = ceil_div(T, kRouteTok) * S;
+  if (bar && grid <= num_sms_route()) {  // one CTA per SM: every routing CTA can be resident
+    ScatArgs a;
+    cudaError_t e = scatter_args(a, xn, ids, gcount, slot_row, T, d, E, k, kExpertTileRows, x_tiles, offs, work,
+                                 n_work, max_work, stats);
+    if (e != cudaSuccess) return e;
+    e = route_common(norm, h, gain, eps, xn, wr, T, d, E, k, ids, gates, slot_row, gcount, err, st, &a, bar);
+    if (e != cudaErrorCooperativeLaunchTooLarge) {
+      if (launches) *launches = 1;
+      return e;
+    }
+    cudaGetLastError();  // not resident together after all: two launches
+  }
+  cudaError_t e = route_common(norm, h, gain, eps, xn, wr, T, d, E, k, ids, gates, slot_row, gcount, err, st);
+  if (e != cudaSuccess) return e;
+  if (launches) *launches = 2;
+  return moe_scatter(xn, ids, gcount, slot_row, T, d, E, k, kExpertTileRows, x_tiles, offs, work, n_work, max_work,
+                     st, stats);
 }
 
 }  // namespace dg

@@ -121,16 +121,23 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(PartialPlanes P, i
   }
 }
 
+// One block per request (positions [b C, b C + C)).  With several requests
+// (lockstep batching) a request whose canvas is finished (req_nk[b] > 0)
+// keeps its state; req_nk[b] records the step at which its canvas finished,
+// and the step is done when every request's canvas is; the last block to
+// finish (a counter in global memory, fenced) takes that decision, continues
+// a device loop and resets the counter.
 __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum, int C, int step,
                             int budget_N, int stable_steps, int adaptive, float thr, int *x,
                             uint8_t *committed, int *last, int *stable, int *done,
-                            StepParams *dyn, LoopCtl loop) {
+                            StepParams *dyn, LoopCtl loop, BatchCtl bt) {
   pdl_wait();
   pdl_trigger();
-  const int i = threadIdx.x;
+  const int b = blockIdx.x, i = b * C + threadIdx.x;
   if (dyn) step = dyn->step;
+  const bool finished = bt.req_nk && bt.req_nk[b] > 0;
   bool com = true;
-  if (i < C) {
+  if (threadIdx.x < C && !finished) {
     com = committed[i] != 0;
     if (!com) {
       const int a = argmax[i];
@@ -147,21 +154,30 @@ __global__ void rule_kernel(const int *argmax, const float *conf, const int *gum
     }
   }
   const int n_free = __syncthreads_count(!com);
-  if (i == 0) {
-    const int d = (step >= budget_N || (adaptive && n_free == 0)) ? 1 : 0;
-    *done = d;
-    if (loop.active) {
-      const bool stop = d || (loop.err && *(volatile const int *)loop.err);
-      if (!stop && dyn) {  // the next step's words (the same schedule as the host's, in double)
-        const int nx = step + 1;
-        double tau = loop.temp_start;
-        if (budget_N > 1) tau += ((double)loop.temp_end - (double)loop.temp_start) * (nx - 1) / (budget_N - 1);
-        dyn->step = nx;
-        dyn->ctr2 = (dyn->ctr2 & 0xFFFF0000u) | (uint32_t)nx;
-        dyn->inv_tau = (float)(1.0 / tau);
-      }
-      cudaGraphSetConditional(loop.handle, stop ? 0u : 1u);
+  if (threadIdx.x != 0) return;
+  const int d_req = (finished || step >= budget_N || (adaptive && n_free == 0)) ? 1 : 0;
+  int d = d_req;
+  if (gridDim.x > 1) {
+    bt.req_done[b] = d_req;
+    if (d_req && !finished) bt.req_nk[b] = step;
+    __threadfence();
+    if (atomicAdd(bt.counter, 1) != (int)gridDim.x - 1) return;  // not the last block
+    __threadfence();
+    for (int r = 0; r < (int)gridDim.x; ++r) d &= *(volatile int *)(bt.req_done + r);
+    *bt.counter = 0;
+  }
+  *done = d;
+  if (loop.active) {
+    const bool stop = d || (loop.err && *(volatile const int *)loop.err);
+    if (!stop && dyn) {  // the next step's words (the same schedule as the host's, in double)
+      const int nx = step + 1;
+      double tau = loop.temp_start;
+      if (budget_N > 1) tau += ((double)loop.temp_end - (double)loop.temp_start) * (nx - 1) / (budget_N - 1);
+      dyn->step = nx;
+      dyn->ctr2 = (dyn->ctr2 & 0xFFFF0000u) | (uint32_t)nx;
+      dyn->inv_tau = (float)(1.0 / tau);
     }
+    cudaGraphSetConditional(loop.handle, stop ? 0u : 1u);
   }
 }
 
@@ -200,11 +216,12 @@ cudaError_t sampler_merge(const void *partials, int C, int V, int *argmax, float
 cudaError_t sampler_rule(const int *argmax, const float *conf, const int *gumbel, int C, int step,
                          int budget_N, int stable_steps, int adaptive, float conf_threshold,
                          int *x, uint8_t *committed, int *last, int *stable, int *done,
-                         cudaStream_t st, StepParams *dyn, LoopCtl loop) {
-  if (C > 1024) return cudaErrorInvalidValue;
+                         cudaStream_t st, StepParams *dyn, LoopCtl loop, BatchCtl bt) {
+  if (C > 1024 || bt.n_req < 1 || (bt.n_req > 1 && (!bt.req_done || !bt.req_nk || !bt.counter)))
+    return cudaErrorInvalidValue;
   const int threads = ((C + 31) / 32) * 32;
-  return launch_pdl(rule_kernel, dim3(1), dim3(threads), 0, st, argmax, conf, gumbel, C, step, budget_N,
-                    stable_steps, adaptive, conf_threshold, x, committed, last, stable, done, dyn, loop);
+  return launch_pdl(rule_kernel, dim3(bt.n_req), dim3(threads), 0, st, argmax, conf, gumbel, C, step, budget_N,
+                    stable_steps, adaptive, conf_threshold, x, committed, last, stable, done, dyn, loop, bt);
 }
 
 }  // namespace dg

@@ -67,7 +67,9 @@ typedef struct dg_config {
     int32_t d_ff;          /* expert SwiGLU width F                          */
     int32_t vocab;
     int32_t page_size;     /* tokens per KV page (a multiple of 64)          */
-    int32_t max_context;   /* KV pool capacity in tokens (prompt + canvases) */
+    int32_t max_context;   /* KV pool capacity in tokens (prompt + canvases), per request */
+    int32_t max_requests;  /* requests decoded together (0 or 1: one; at most 8), see
+                              dg_generate_batch                                */
     float rope_base;       /* RoPE theta base (10000)                        */
     float rms_eps;         /* RMSNorm epsilon (1e-6)                         */
     float init_std;        /* std of the seeded random-init weights (0.02)   */
@@ -183,6 +185,46 @@ int dg_generate(dg_model *m, const int32_t *prompt, int32_t n_prompt, int32_t K_
 
 /* ---- helpers: state access for replay tests and benchmarking ------------ */
 
+/* ---- multi-request batching (lockstep) ------------------------------------
+ * A model created with cfg->max_requests = B > 1 holds B requests, each with
+ * its own prompt, KV pages (max_context tokens each) and canvas, and runs
+ * every denoising forward and every KV-append forward over all B canvases at
+ * once (B * canvas_len rows through the projections, the expert FFN and the
+ * LM head: the expert weights streamed per step serve B requests; blog, on
+ * serving throughput under concurrency).  Requests advance in lockstep: a
+ * canvas step runs until every request's canvas is finished, a request whose
+ * canvas finished earlier keeps it unchanged, and all requests commit
+ * together.  Request b samples with sample_seed + b; given that seed, its
+ * tokens, step counts and Eq. 7-10 are those of a single-request model.
+ * The single-request calls above (dg_prefill, dg_denoise_step,
+ * dg_denoise_canvas, dg_commit_canvas, dg_generate, dg_rewind,
+ * dg_write_canvas, dg_canvas_logits) return DG_EINVAL on such a model; the
+ * state readers report request 0. */
+
+/* Encode prompts[b][0 .. lens[b]) (host) of every request b < B into its own
+ * KV pages, as dg_prefill does for one. */
+int dg_prefill_batch(dg_model *m, const int32_t *const *prompts, const int32_t *lens);
+
+/* Denoise the current canvases until every request's is finished, as
+ * dg_denoise_canvas (one device-side loop, one host synchronisation);
+ * n_steps (host, B entries, may be NULL) receives, per request, the step at
+ * which its canvas finished. */
+int dg_denoise_canvas_batch(dg_model *m, int32_t *n_steps);
+
+/* Finish the current canvases: ids to out_ids (host, B * canvas_len, may be
+ * NULL), each request's C_k to out_valid (host, B, may be NULL), then one
+ * KV-append forward of all B canvases (each after its own prefix). */
+int dg_commit_canvas_batch(dg_model *m, int32_t *out_ids, int32_t *out_valid);
+
+/* dg_generate for B requests in lockstep: out_ids (host, B * K_max *
+ * canvas_len; request b's canvas k at (b K_max + k) canvas_len) and stats
+ * (host, B entries, may be NULL; per request, its own N_k / C_k arrays).
+ * A request's generation ends with its canvas holding the first EOS (its
+ * later canvases are computed with the others and not reported); the batch
+ * ends when every request has ended or after K_max canvases. */
+int dg_generate_batch(dg_model *m, const int32_t *const *prompts, const int32_t *lens, int32_t K_max,
+                      int32_t *out_ids, dg_stats *stats);
+
 /* Replace the sampler configuration (e.g. a new sample_seed). */
 int dg_set_sampler(dg_model *m, const dg_sampler_config *scfg);
 
@@ -228,7 +270,8 @@ int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t
 
 /* Device pointer and size of a weight tensor.  which: DG_W_* below; layer is
  * ignored for the embedding, LM head and final norm.  Physical layouts:
- *   EMBED, LM_HEAD   [V][d]
+ *   EMBED            [V][d]
+ *   LM_HEAD          operand tiles of [V][d]
  *   WQKV             operand tiles of         rows: W_q, then W_k, then W_v
  *                    [(Hq + 2 Hkv) * hd][d]
  *   WO               operand tiles of [d][Hq * hd]
@@ -256,11 +299,13 @@ int dg_get_weight(dg_model *m, int32_t which, int32_t layer, void **dev_ptr, siz
 /* ---- profiling --------------------------------------------------------- */
 
 /* Kernel classes of the decoder, for per-class timing and launch counts.
- * DG_K_ROUTE counts two launches per MoE layer: the routing kernel (the MoE
- * RMSNorm, router logits, top-k and gates, and each routed pair's rank among
- * its token group's pairs of the same expert) and the scatter kernel (the
- * stable sort of the routed pairs by expert, the gather of their rows into
- * the expert FFN's operand tiles, and its work list). */
+ * DG_K_ROUTE covers the routing (the MoE RMSNorm, router logits, top-k and
+ * gates, and each routed pair's rank among its token group's pairs of the
+ * same expert) and the scatter (the stable sort of the routed pairs by
+ * expert, the gather of their rows into the expert FFN's operand tiles, and
+ * its work list): one launch per MoE layer when the routing kernel's grid
+ * fits the machine (the scatter then runs in its tail, after a grid-wide
+ * barrier), else two. */
 enum {
     DG_K_EMBED = 0, DG_K_RMSNORM, DG_K_QKV_ROPE, DG_K_ATTENTION, DG_K_O_PROJ,
     DG_K_ROUTE, DG_K_EXPERT_FFN, DG_K_COMBINE, DG_K_LM_HEAD,
@@ -412,10 +457,12 @@ int dg_op_fill_moe_weights(uint16_t *w_router, uint16_t *w_gate_up, uint16_t *w_
  * Layout of `partials` (device, rows * V/256 * 20 bytes): 5 planes of
  * [rows][V/256]: m (f32), a (i32), s (f32), gk (f32), gi (i32).
  * dg_op_lm_head_partials computes logits = (xn + xn_lo) W_out^T with fp32
- * accumulation in tensor memory (xn_lo, device bf16 [rows][d], may be NULL:
- * the low half of a hi/lo split of fp32 rows, as the decoder's final norm
- * writes it) and reduces them with the decoder's own LM-head epilogue, the
- * logits never leaving the chip; when `logits` (device fp32 [rows][V]) is not
+ * accumulation in tensor memory and reduces them with the decoder's own
+ * LM-head epilogue, the logits never leaving the chip.  xn and xn_lo (may be
+ * NULL: the low half of a hi/lo split of fp32 rows, as the decoder's final
+ * norm writes it) are device bf16 operand tiles of [rows][d], w_out device
+ * bf16 operand tiles of [V][d] (layout of dg_get_weight; see
+ * dg_op_fill_tiled_weights).  When `logits` (device fp32 [rows][V]) is not
  * NULL the same launch also writes the logits the partials were reduced from.
  * dg_op_logits_partials runs the same per-(row, tile) reduction code on
  * given fp32 logits [rows][V] (device): the injected-logit entry of the
@@ -427,6 +474,12 @@ int dg_op_lm_head_partials(const uint16_t *xn, const uint16_t *xn_lo, const uint
 int dg_op_logits_partials(const float *logits, int32_t rows, int32_t V, uint64_t sample_seed,
                           int32_t canvas, int32_t step, float inv_tau, void *partials,
                           void *stream);
+
+/* dst (device, bf16, rows * cols elements; cols a multiple of 64) = the
+ * operand tiles (layout of dg_get_weight) of the logical [rows][cols] tensor
+ * `tensor_id` of the seeded weights (elements as dg_op_fill_weights). */
+int dg_op_fill_tiled_weights(uint16_t *dst, int32_t rows, int32_t cols, uint64_t seed,
+                             uint32_t tensor_id, float std_dev, void *stream);
 
 /* The sampler's Gumbel noise transform: out[i] = -dg_log(-dg_log(u)),
  * u = (2 (words[i] >> 9) + 1) 2^-24 (device uint32 in, device fp32 out, n

@@ -40,6 +40,13 @@ def new_partials(rows, V):
     return torch.zeros(dgp.partials_bytes(rows, V) // 4, dtype=torch.int32, device=dev())
 
 
+def tiles_dev(t):
+    """A row-major bf16 CPU tensor [rows][cols] as a device tensor in the
+    library's operand-tile order (the LM head's operand layout)."""
+    bits = t.contiguous().view(torch.int16).numpy()
+    return torch.from_numpy(dgp.to_operand_tiles(bits)).view(torch.bfloat16).to(dev())
+
+
 def top2_gap(x):
     s = np.sort(np.asarray(x, np.float64), axis=-1)
     return s[..., -1] - s[..., -2]

@@ -5,7 +5,7 @@ import torch
 
 import discrete_diffusion_block_gb300 as dgp
 from discrete_diffusion_block_gb300 import synth
-from gpu_util import bf16_to_f32, dev, new_partials, partial_planes, rel_err, top2_gap
+from gpu_util import bf16_to_f32, dev, new_partials, partial_planes, rel_err, tiles_dev, top2_gap
 from oracle import dgmath, model as om, philox, sampler as osamp, weights as ow
 
 pytestmark = pytest.mark.gpu
@@ -196,9 +196,9 @@ def test_sampler_rule_branches_over_scripted_steps():
 @pytest.mark.parametrize("rows,d,V,sample", [(256, 256, 1024, None), (256, 2816, 262144, [0, 63, 64, 130, 255])])
 def test_lm_head_partials_against_fp64_logits(rows, d, V, sample):
     xf, xt = synth.normal_bf16((rows, d), seed=2)
-    xn = xt.to(dev())
+    xn = tiles_dev(xt)
     w = torch.empty(V * d, dtype=torch.bfloat16, device=dev())
-    dgp.dg_op_fill_weights(w, 0, 2, 0, 0.02)
+    dgp.dg_op_fill_tiled_weights(w, V, d, 0, 2, 0.02)
     part = new_partials(rows, V)
     dgp.dg_op_lm_head_partials(xn, w, rows, d, V, 3, 1, 2, part)
     got = partial_planes(part, rows, V)
@@ -243,7 +243,7 @@ def _lm_head_rows(C, d, seed, split):
     xt = torch.from_numpy(x)
     hi = xt.to(torch.bfloat16)
     lo = (xt - hi.float()).to(torch.bfloat16) if split else None
-    return hi.to(dev()), (lo.to(dev()) if split else None)
+    return tiles_dev(hi), (tiles_dev(lo) if split else None)
 
 
 @pytest.mark.parametrize("split,canvas,step,seed,rows,inv_tau", [
@@ -257,7 +257,7 @@ def test_lm_head_epilogue_partials_bit_exact_on_its_own_logits(split, canvas, st
     launch the decoder runs must equal them too."""
     C, d, V = 256, 2816, 262144
     w = torch.empty(V * d, dtype=torch.bfloat16, device=dev())
-    dgp.dg_op_fill_weights(w, 0, 2, 0, 0.02)
+    dgp.dg_op_fill_tiled_weights(w, V, d, 0, 2, 0.02)
     hi, lo = _lm_head_rows(C, d, 31 + step, split)
     logits = torch.empty(C, V, dtype=torch.float32, device=dev())
     inv_tau = np.float32(inv_tau)

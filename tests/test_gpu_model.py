@@ -201,6 +201,7 @@ def test_profile_counts_launches():
     dgp.dg_denoise_step(m)
     prof = dgp.dg_profile_read(m)
     assert prof["expert_ffn"][1] == 2 and prof["lm_head"][1] == 1
+    assert prof["route"][1] == 2          # routing and scatter fused: one launch per MoE layer
     assert all(ms >= 0 for ms, _ in prof.values()) and prof["expert_ffn"][0] > 0
     m.close()
 
@@ -227,7 +228,8 @@ def test_projection_weights_are_operand_tiles_of_the_logical_matrices(oracle_wei
     d, qd, kd = cfg.d_model, cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
     for which, rows, cols, ref in [
             (dgp.DG_W_WQKV, qd + 2 * kd, d, lambda W: np.vstack([W["wq"], W["wk"], W["wv"]])),
-            (dgp.DG_W_WO, d, qd, lambda W: W["wo"])]:
+            (dgp.DG_W_WO, d, qd, lambda W: W["wo"]),
+            (dgp.DG_W_LM_HEAD, cfg.vocab, d, lambda W: oracle_weights.lm_head)]:
         ptr, nbytes = dgp.dg_get_weight(m, which, 1)
         assert nbytes == rows * cols * 2
         host = np.zeros(rows * cols, np.uint16)
