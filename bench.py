@@ -279,7 +279,7 @@ def gpu_arm(args):
     hbm, tf_burst, tf_sust, peak_src = peaks()
 
     stream = torch.cuda.Stream(device=dev)
-    cfg = dgp.full_config(max_context=PROMPT + CANVASES * C)
+    cfg = dgp.full_config(max_context=PROMPT + CANVASES * C, n_layers=args.layers)
     scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1)
     m = dgp.dg_init_model(cfg, scfg, stream=stream)
     log("model initialised")
@@ -416,7 +416,8 @@ def gpu_arm(args):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic: seeded random-init weights, uniform random prompt ids",
-                "config": {"workload": WORKLOAD,
+                "config": {"workload": WORKLOAD if args.layers == 30 else
+                           WORKLOAD.replace("30 layers", f"{args.layers} layers (profiling case, not the headline)"),
                            "step": "decode of 4 canvases (all denoising steps + 3 KV-append forwards), prompt cached",
                            "l2": (f"inputs larger than L2 (129 MB): {expert_gb:.1f} GB of expert weights "
                                   f"({touched / n_moe:.1f} experts touched per MoE launch, measured) and "
@@ -731,6 +732,8 @@ def main():
     ap.add_argument("--micro", default=None,
                     choices=["moe", "lmhead", "sampler", "attention", "kv_append", "all"],
                     help="kernel micro-benchmarks at the micro-op shapes instead of the decoder")
+    ap.add_argument("--layers", type=int, default=30,
+                    help="decoder depth; fewer layers give a small case of the same kernels for ncu captures")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if measured for the current binaries")
     args = ap.parse_args()

@@ -231,6 +231,29 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 // has completed and its memory is visible; it is a no-op for an ordinary
 // launch) and pdl_trigger() once its own successor may be scheduled.
 // ---------------------------------------------------------------------------
+// Codes >= kShapeErrorBase in a device error word mean that a kernel found
+// itself launched without the cluster shape it was built for (it returned
+// before any cluster operation); lower codes are bounded waits that gave up.
+constexpr int kShapeErrorBase = 200;
+
+// The device error word of bounded waits, loaded at a kernel's start so that
+// its latency overlaps the setup (a kernel that finds it set skips its waits:
+// an earlier one already gave up).  Under programmatic dependent launch the
+// load may precede the previous kernel's last write; a missed record only
+// costs bounded waits that give up again.
+__device__ __forceinline__ int ld_err_word(const int *p) {
+  int v = 0;
+  if (p) asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// CTAs in this CTA's cluster (1 for a launch without clusters).
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(n));
+  return n;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 

@@ -495,6 +495,15 @@ int alloc_model(dg_model *m, const void *const *weights) {
   return DG_OK;
 }
 
+// A nonzero device error word: a bounded wait that gave up, or (codes from
+// kShapeErrorBase on) a kernel that found itself launched without its
+// cluster shape and returned before doing anything.
+int device_fail(int code) {
+  if (code >= dg::kShapeErrorBase)
+    return fail(DG_ECUDA, "a kernel ran without the cluster shape it was launched with (code %d)", code);
+  return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", code);
+}
+
 int check_model(dg_model *m) {
   if (!m) return fail(DG_EINVAL, "null model");
   return DG_OK;
@@ -509,7 +518,7 @@ int sync_check(dg_model *m) {
     const int code = m->done_host[1];
     CK(cudaMemsetAsync(m->done_dev + 1, 0, sizeof(int), m->stream));
     SYNC(m);
-    return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", code);
+    return device_fail(code);
   }
   return DG_OK;
 }
@@ -704,7 +713,7 @@ int denoise_impl(dg_model *m, int32_t *done) {
   m->host_syncs += 1;
   if (used) prof_collect_graph(m, *used);
   if (m->done_host[1])
-    return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", m->done_host[1]);
+    return device_fail(m->done_host[1]);
   m->canvas_done = m->done_host[0] != 0;
   if (done) *done = m->canvas_done ? 1 : 0;
   return DG_OK;
@@ -782,7 +791,7 @@ int denoise_canvas_impl(dg_model *m, int32_t *n_steps) {
   SYNC(m);
   m->host_syncs += 1;
   if (m->done_host[1])
-    return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", m->done_host[1]);
+    return device_fail(m->done_host[1]);
   const int steps = m->dyn_host->step - start;  // the loop leaves dyn at its last step
   const int loop_steps = m->dyn_host->step - m->step;
   for (int i = 0; i < DG_K_CLASSES; ++i) m->prof_launches[i] += it->second.launches[i] * loop_steps;
@@ -1340,7 +1349,7 @@ int dg_op_status(void *stream) {
   CK(cudaMemcpy(v, st, sizeof(v), cudaMemcpyDeviceToHost));
   if (v[0] == 0 && v[1] == 0) return DG_OK;
   CK(cudaMemset(st, 0, sizeof(v)));
-  if (v[0]) return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", v[0]);
+  if (v[0]) return device_fail(v[0]);
   return fail(DG_EINVAL, "a page table entry was outside the pools (its keys were skipped)");
 }
 

@@ -8,7 +8,7 @@
 // Both operands are stored as operand tiles (tiled_index in common.cuh): 128
 // rows x 64 columns per tile, already in the 128-byte swizzled order of a
 // K-major shared-memory operand, so one contiguous bulk copy stages a tile.
-// Roles inside a GEMM CTA (128 threads):
+// Roles inside a GEMM CTA (256 threads):
 //   warp 0, one thread  -- producer: per 64-wide K step the weight tile (A,
 //                          <= 16 KB) and the activation tiles of up to 256
 //                          token rows (B) into a 4-stage shared-memory ring;
@@ -17,8 +17,9 @@
 //   warp 1, one thread  -- allocates the TMEM accumulator and issues
 //                          tcgen05.mma (M = 128, N <= 256, K = 16) per stage,
 //                          releasing each stage with tcgen05.commit;
-//   warps 0-3           -- read the accumulator out of TMEM (each warp its
-//                          32-lane quarter) and run the fused epilogue.
+//   warps 0-7           -- read the accumulator out of TMEM (warp w its
+//                          32-lane quarter w % 4, the 32-column chunks of
+//                          parity w / 4) and run the fused epilogue.
 // Split-K: the SPLIT CTAs of a cluster own 1/SPLIT of K each; after the main
 // loop every CTA stores the slices of its fp32 partial tile that its peers
 // own to a global exchange buffer (it stays in L2), and CTA j adds the SPLIT
@@ -234,6 +235,7 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 constexpr int kSkBN = 256;           // B rows per tile (MMA N upper bound)
+constexpr int kSkThreads = 256;      // two warps per TMEM lane quarter in the epilogue
 constexpr int kSkStages = 4;
 constexpr uint32_t kBChunkBytes = 64 * 128;  // one 64-row B box
 
@@ -269,7 +271,7 @@ inline size_t split_k_xchg_bytes(int n_ctas) { return (size_t)n_ctas * 128 * kSk
 }  // namespace tc
 
 template <int SPLIT, class Epi>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(tc::kSkThreads, 1)
     tc_gemm_sk_kernel(TcArgs g, Epi epi) {
   using S = tc::SkSmem<SPLIT, Epi>;
   constexpr int STAGES = tc::kSkStages, W = S::W;
@@ -285,6 +287,12 @@ __global__ void __launch_bounds__(128, 1)
   // (the SPLIT CTAs blockIdx.x = c * SPLIT + z, one per K range) takes units
   // c, c + n_clusters, ..., so the grid is sized to the machine and the
   // units spread evenly over it.
+  // Every CTA of the launch sees the same cluster size: a launch without the
+  // SPLIT-CTA clusters this kernel exchanges partials in returns at once.
+  if (cluster_ctas() != (uint32_t)SPLIT) {
+    if (threadIdx.x == 0 && g.err) atomicExch(g.err, kShapeErrorBase + 1);
+    return;
+  }
   const int n_items = ceil_div(g.N, tc::kSkBN);
   const int m_tiles = ceil_div(g.M, 128);
   const int n_units = n_items * m_tiles;
@@ -292,6 +300,7 @@ __global__ void __launch_bounds__(128, 1)
   if (cluster >= n_units) return;  // every CTA of a cluster decides alike
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int err_seen = threadIdx.x == 64 ? ld_err_word(g.err) : 0;
   const int z = SPLIT > 1 ? (int)(blockIdx.x % SPLIT) : 0;
   const int KT = g.K / tc::kBK;
   const int kb = (int)((long long)KT * z / SPLIT), ke = (int)((long long)KT * (z + 1) / SPLIT);
@@ -372,14 +381,17 @@ __global__ void __launch_bounds__(128, 1)
   // (Warps 2-3 only: the producer and MMA threads go straight on.)
   if (S::prep && Epi::kPrepEarly && warp >= 2) {
     const TileCtx sub = slice_ctx(unit_ctx(cluster));
-    if (sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x - 64, 64);
+    if (sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x - 64, tc::kSkThreads - 64);
   }
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;  // an earlier timeout: do not wait again
+  // An earlier timeout: do not wait again.  Loaded at the start by an
+  // epilogue thread, off the producer's path (its loops check the flag
+  // before every copy).
+  if (threadIdx.x == 64 && err_seen) *abort = 1;
   if (S::prep && !Epi::kPrepEarly && warp >= 2) {
     const TileCtx sub = slice_ctx(unit_ctx(cluster));
-    if (sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x - 64, 64);
+    if (sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x - 64, tc::kSkThreads - 64);
   }
 
   int it = 0;     // ring position: k-tiles issued (producer) / consumed (MMA) so far
@@ -431,14 +443,14 @@ __global__ void __launch_bounds__(128, 1)
 
     tc::mbar_wait(accb, tiles & 1, g.err, 3, abort);
     tc::fence_after();
-    const int row = warp * 32 + lane;
+    const int row = (warp & 3) * 32 + lane, hc = warp >> 2;  // TMEM lane; parity of this warp's chunks
     const int nchunks = (ctx.n_valid + 31) >> 5;  // 32-column TMEM chunks holding valid outputs
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     unsigned char *extra = base + S::mine + S::red;
     if (SPLIT == 1) {
       float *red = (float *)base;
 #pragma unroll 1
-      for (int c = 0; c < nchunks; ++c) {
+      for (int c = hc; c < nchunks; c += 2) {
         uint32_t v[32];
         tc::tmem_ld32(trow + 32 * c, v);
         tc::tmem_ld_wait(v);
@@ -462,7 +474,7 @@ __global__ void __launch_bounds__(128, 1)
       float *xc = g.xchg + (size_t)(blockIdx.x - z) * SPLIT * slice_elems;  // this cluster's [z][j] slices
       const TileCtx sub = slice_ctx(ctx);
 #pragma unroll 1
-      for (int c = 0; c < nchunks; ++c) {
+      for (int c = hc; c < nchunks; c += 2) {
         const int sl = (32 * c) / W, o = 32 * c - sl * W;
         if (sl == z) continue;
         uint32_t v[32];
@@ -473,12 +485,12 @@ __global__ void __launch_bounds__(128, 1)
         for (int j = 0; j < 32; ++j) dst[(size_t)j * 128] = __uint_as_float(v[j]);
       }
       // a later unit's epilogue inputs load while the stores drain
-      if (S::prep && unit != cluster && sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x, 128);
+      if (S::prep && unit != cluster && sub.n_valid > 0) epi.prepare(sub, base + S::pre_off, threadIdx.x, tc::kSkThreads);
       tc::cluster_sync();  // every CTA's partials are in L2
       float *mine = (float *)base;
       if (sub.n_valid > 0 && !*abort) {
 #pragma unroll 1
-        for (int c = 0; c < W / 32; ++c) {
+        for (int c = hc; c < W / 32; c += 2) {
           if (32 * c >= sub.n_valid) break;
           uint32_t own[32];
           tc::tmem_ld32(trow + z * W + 32 * c, own);
@@ -555,7 +567,7 @@ cudaError_t launch_tc_sk(const TcArgs &g, const Epi &epi, int n_clusters, cudaSt
   if (n_clusters <= 0 || g.M <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_clusters * SPLIT, 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(tc::kSkThreads, 1, 1);
   cfg.dynamicSmemBytes = S::bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];

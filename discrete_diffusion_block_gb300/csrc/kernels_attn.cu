@@ -191,6 +191,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto k_tile = [&](int slot) { return base + S::kring + (size_t)slot * S::tile; };
   auto v_tile = [&](int slot) { return base + S::vring + (size_t)slot * S::tile; };
 
+  // Split blocks merge through distributed shared memory: a launch without
+  // the splits-CTA clusters returns at once (every block sees the same size).
+  if (p.splits > 1 && cluster_ctas() != (uint32_t)p.splits) {
+    if (threadIdx.x == 0 && p.err) atomicExch(p.err, kShapeErrorBase + 2);
+    return;
+  }
   const int g = blockIdx.y, b_req = blockIdx.z / p.splits, split = blockIdx.z - b_req * p.splits;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_total = p.G * p.n_new;
@@ -208,6 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   const int n_kt = k_end > k_begin ? ceil_div(k_end - k_begin, 128) : 0;
 
+  const int err_seen = threadIdx.x == 0 ? ld_err_word(p.err) : 0;
   if (threadIdx.x == 0) {
     *abort = 0;
     tc::mbar_init(q_full, 1);
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0 && p.err && *(volatile int *)p.err) *abort = 1;
+  if (threadIdx.x == 0 && err_seen) *abort = 1;
   __syncwarp();  // lone-thread roles above: reconverge before the CTA-wide barrier
   tc::fence_before();
   __syncthreads();

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(LmArgs g) {
   const int n_units = m_tiles * tiles, KT = g.K / tc::kBK;
   if ((int)blockIdx.x >= n_units) return;
 
+  const int err_seen = threadIdx.x == 0 ? ld_err_word(g.err) : 0;
   if (threadIdx.x == 0) {
     *abort = 0;
     for (int s = 0; s < kLmStages; ++s) {
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(LmArgs g) {
   }
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;
+  if (threadIdx.x == 0 && err_seen) *abort = 1;
 
   if (warp == 0) {
     if (lane == 0) {

@@ -13,8 +13,8 @@
 // W_down), again two accumulators sharing one staged act tile.  Sharing the
 // B operand between two weight blocks halves the re-reads of the item's rows,
 // which are as many bytes as the weights themselves.  All units sit in one
-// list, phase A first; CTAs (one per SM) take the next unit from a global
-// counter.  A phase B unit needs the whole act row block of its item: its
+// list, phase A first; CTA b (one per SM) starts with unit b and then takes
+// the next unit from a global counter.  A phase B unit needs the whole act row block of its item: its
 // producer first requests the unit's leading weight tiles, then waits
 // (bounded) until the item's phase A units have all published their outputs
 // (per-item counter, release/acquire, then a proxy fence before the copies
@@ -52,6 +52,11 @@ namespace dg {
 namespace {
 
 constexpr int kFfnStages = 4;
+// 128-row blocks of W_down per down unit (two accumulators sharing one
+// staged act tile).  Measured: with one block a down unit's k-step took as
+// long as with two (the ring's four stages in flight, not the bytes per
+// stage, set the pace), so two blocks do twice the work per k-step.
+constexpr int kDownBlocks = 2;
 constexpr int kFfnEpiWarps = 8;
 constexpr int kFfnEpiThreads = 32 * kFfnEpiWarps;
 constexpr int kFfnThreads = kFfnEpiThreads + 64;
@@ -68,7 +73,7 @@ struct UnitInfo {
   int phase;    // 0: gate/up, 1: down
   int item, mt, b_row, n_valid, e;
   int a_rows;   // valid rows of each weight tile (phase A: features in the block)
-  int n_acc;    // weight blocks (accumulators) of the unit: 2, or 1 for an odd last block of W_down
+  int n_acc;    // weight blocks (accumulators) of the unit: 2 (gate, up), or kDownBlocks or fewer (down)
   int pad[3];
 };
 
@@ -142,6 +147,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   volatile int *abort = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int err_seen = threadIdx.x == 0 ? ld_err_word(g.err) : 0;
   if (threadIdx.x == 0) {
     *abort = 0;
     for (int s = 0; s < kFfnStages; ++s) {
@@ -172,10 +178,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the work list and the gathered rows come from earlier kernels
   pdl_trigger();
-  if (threadIdx.x == 0 && g.err && *(volatile int *)g.err) *abort = 1;
+  if (threadIdx.x == 0 && err_seen) *abort = 1;
 
   const int n_items = *g.n_work;
-  const int mA = (g.F + 127) / 128, mB = (g.d + 255) / 256;
+  const int mA = (g.F + 127) / 128, mB = (g.d + 128 * kDownBlocks - 1) / (128 * kDownBlocks);
   const int nA = n_items * mA, n_units = nA + n_items * mB;
   const int KTA = g.d / tc::kBK, KTB = g.F / tc::kBK;
   auto a_tile = [&](int s, int j) { return base + (size_t)s * kFfnStageBytes + (size_t)j * kFfnATileBytes; };
@@ -187,7 +193,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
       for (int n = 0;; ++n) {
         const int q = n % kFfnQueue;
         if (n >= kFfnQueue) tc::mbar_wait(q_empty + q, ((n / kFfnQueue) - 1) & 1, g.err, 21, abort);
-        const int u = *abort ? n_units : atomicAdd(g.next, 1);
+        // the first unit of every CTA is its block index (no atomic on the
+        // way to the first copies); the counter hands out the rest
+        const int u = *abort ? n_units : n == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(g.next, 1);
         UnitInfo inf;
         inf.u = u < n_units ? u : -1;
         if (inf.u >= 0) {
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           inf.n_valid = min(kFfnBN, g.offs[e + 1] - e0 - n0);
           inf.e = e;
           inf.a_rows = inf.phase ? 128 : min(128, g.F - 128 * inf.mt);
-          inf.n_acc = inf.phase ? min(2, g.d / 128 - 2 * inf.mt) : 2;
+          inf.n_acc = inf.phase ? min(kDownBlocks, g.d / 128 - kDownBlocks * inf.mt) : 2;
         }
         queue[q] = inf;
         mbar_arrive(q_full + q);  // release: the entry is visible to the waiting roles
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         const bf16 *a0;
         size_t a_blk;
         if (inf.phase) {
-          a0 = g.wd + (size_t)inf.e * g.d * g.F + (size_t)(2 * inf.mt) * 128 * g.F;
+          a0 = g.wd + (size_t)inf.e * g.d * g.F + (size_t)(kDownBlocks * inf.mt) * 128 * g.F;
           a_blk = (size_t)128 * g.F;
         } else {
           a0 = g.wgu + (size_t)inf.e * 2 * g.F * g.d + (size_t)128 * g.d * inf.mt;
@@ -226,6 +234,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           for (int j = 0; j < inf.n_acc; ++j)
             tc::bulk_load(a_tile(s, j), a0 + j * a_blk + kt * a_kt, a_bytes, full + s);
         };
+
         // Phase B: the first stages' weight tiles go out before the wait on act.
         const int pre = inf.phase ? min(KT, kFfnStages) : 0;
         for (int kt = 0; kt < pre; ++kt) {
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         // token the warp stores 32 consecutive features (128 bytes).
 #pragma unroll 1
         for (int a = 0; a < inf.n_acc; ++a) {
-          float *dst = g.y + (size_t)inf.b_row * g.d + 256 * inf.mt + 128 * a + lrow;
+          float *dst = g.y + (size_t)inf.b_row * g.d + 128 * (kDownBlocks * inf.mt + a) + lrow;
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             const int col0 = 64 * half + 32 * c;

@@ -34,6 +34,8 @@
 // the same cluster barriers whatever happened, so no CTA can be left waiting.
 #include <cuda.h>
 
+#include <cstdlib>
+
 #include "gemm_tc.cuh"
 #include "internal.h"
 
@@ -58,7 +60,9 @@ constexpr int kSmemBudget = 200 * 1024;  // dynamic; the expert sort adds 11 KB 
 // ---------------------------------------------------------------------------
 constexpr int kScatThreads = 256;
 
-inline size_t scatter_smem_ints(int ng, int E, int per) { return (size_t)ng * E + 2 * E + 2 * (size_t)per; }
+__host__ __device__ inline size_t scatter_smem_ints(int ng, int E, int per) { return (size_t)ng * E + 2 * E + 2 * (size_t)per; }
+// Bytes of the table above, rounded up to 16 (the staged rows follow it).
+__host__ __device__ inline size_t scatter_tab_bytes(int ng, int E, int per) { return (scatter_smem_ints(ng, E, per) * 4 + 15) & ~(size_t)15; }
 
 struct ScatArgs {
   const bf16 *xn;
@@ -67,6 +71,7 @@ struct ScatArgs {
   bf16 *x_tiles;  // [item][d/64] tiles of 128 rows x 64 columns, swizzled
   int T, d, E, k, tile_rows, ng;
   int per;        // pairs per block
+  int stage_bytes;  // shared memory after the table for the block's token rows (0: none)
   int *offs, *work, *n_work, *sync;
   int max_work;
   unsigned long long *stats;
@@ -100,8 +105,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
 
 // The scatter work of block `blk` (kScatThreads threads): its share of the
 // pairs, and (blk 0) the expert segments, the work list and the FFN's
-// counters.  tab: shared memory of scatter_smem_ints() ints.
-__device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *tab, int *warp_tot) {
+// counters.  tab: shared memory of scatter_smem_ints() ints; stage: shared
+// memory of stage_bytes bytes (16-byte aligned) for the block's token rows,
+// or null.
+__device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *tab, int *warp_tot,
+                                              unsigned char *stage, size_t stage_bytes) {
   // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]; then
   // the expert and group rank of each of this block's pairs
   const int E = a.E, ng = a.ng, n = ng * E;
@@ -154,12 +162,50 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
   }
   __syncwarp();
   __syncthreads();
-  // Pairs of this block: one warp per pair, two pairs at a time; the warp
-  // copies the token's row into row r of its item's tiles (16-byte chunk c of
+  // The block's pairs are consecutive, so their tokens are the few rows
+  // t_lo .. t_hi (k pairs each): when they fit, those rows are staged in
+  // shared memory once (every 16-byte load in flight together) and each pair
+  // is written from there.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
+  constexpr int NW = kScatThreads / 32;
+  const int t_lo = p0 / a.k, n_tok = p1 > p0 ? (p1 - 1) / a.k - t_lo + 1 : 0;
+  if (stage && (size_t)n_tok * a.d * 2 <= stage_bytes) {
+    const uint4 *src = (const uint4 *)(a.xn + (size_t)t_lo * a.d);  // rows t_lo .. t_hi are contiguous
+    uint4 *st4 = (uint4 *)stage;
+    const int n4 = n_tok * vec;
+    for (int i0 = 0; i0 < n4; i0 += 8 * kScatThreads) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + (int)threadIdx.x + u * kScatThreads;
+        if (i < n4) v[u] = src[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + (int)threadIdx.x + u * kScatThreads;
+        if (i < n4) st4[i] = v[u];
+      }
+    }
+    __syncthreads();
+    // One warp per pair: the token's row into row r of its item's tiles
+    // (16-byte chunk c of k-tile kt at chunk position c ^ (r % 8): the tensor
+    // core's swizzled operand order).
+    for (int p = p0 + warp; p < p1; p += NW) {
+      const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
+      const int within = tab[g * E + ex] + s_rk[p - p0];  // rank among the expert's rows
+      if (lane == 0) a.slot_row[p] = soffs[ex] + within;
+      const int item = stoff[ex] + within / a.tile_rows, rr = within % a.tile_rows;
+      const uint4 *row = st4 + (size_t)(t - t_lo) * vec;
+      uint4 *dst = (uint4 *)(a.x_tiles + (size_t)item * KT * (128 * 64)) + rr * 8;
+      for (int c = lane; c < vec; c += 32) dst[(c >> 3) * 1024 + ((c & 7) ^ (rr & 7))] = row[c];
+    }
+    return;
+  }
+  // Otherwise one warp per pair, two pairs at a time; the warp copies the
+  // token's row into row r of its item's tiles (16-byte chunk c of
   // k-tile kt at chunk position c ^ (r % 8): the tensor core's swizzled
   // operand order), both rows' loads in flight before any store.
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
-  constexpr int NW = kScatThreads / 32, U = 12;
+  constexpr int U = 12;
   for (int pb = p0 + warp; pb < p1; pb += 2 * NW) {
     const uint4 *src[2];
     uint4 *dst[2];
@@ -207,7 +253,9 @@ __global__ void __launch_bounds__(kScatThreads) scatter_kernel(ScatArgs a) {
   __shared__ int warp_tot[kScatThreads / 32];
   pdl_wait();
   pdl_trigger();
-  scatter_block(a, blockIdx.x, tab, warp_tot);
+  scatter_block(a, blockIdx.x, tab, warp_tot,
+                a.stage_bytes ? (unsigned char *)tab + scatter_tab_bytes(a.ng, a.E, a.per) : nullptr,
+                (size_t)a.stage_bytes);
 }
 
 struct RouteArgs {
@@ -226,6 +274,7 @@ struct RouteArgs {
   // fused scatter: after a grid-wide barrier (bar: count, generation), every
   // CTA runs its share of the scatter (sc, with sc.per pairs per CTA)
   int fuse;
+  int grid;  // fused: CTAs of the launch
   int *bar;
   ScatArgs sc;
 };
@@ -339,6 +388,47 @@ __device__ __forceinline__ void topk_warp(const float *lrow, int E, int k, int l
   }
 }
 
+// ---- fused scatter ---------------------------------------------------------
+// Every token group's counts and ranks are in global memory once all CTAs
+// pass a grid-wide barrier (the launch is cooperative: all CTAs are
+// resident).  Self-resetting: each CTA reads the generation word, then
+// arrives; the last to arrive zeroes the count and bumps the generation,
+// which the others wait for (bounded).  Then this CTA's share of the scatter
+// reuses its shared memory (base: the CTA's dynamic shared memory, 1024-byte
+// aligned).
+__device__ __forceinline__ void fused_scatter_tail(const RouteArgs &a, unsigned char *base) {
+  __syncthreads();
+  __shared__ int passed;
+  if (threadIdx.x == 0) {
+    int *gen = a.bar + 1;
+    const int g0 = ld_acquire_s32(gen);
+    __threadfence();  // this CTA's counts and ranks before its arrival
+    passed = 1;
+    if (atomicAdd(a.bar, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.bar, 0);
+      __threadfence();
+      atomicExch(gen, g0 + 1);
+    } else {
+      const long long c0 = clock64();
+      while (ld_acquire_s32(gen) == g0) {
+        if (clock64() - c0 > tc::kWaitCycles) {
+          if (a.err) atomicExch(a.err, 55);
+          passed = 0;  // counts may be incomplete: leave the scatter undone
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  pdl_trigger();
+  if (!passed) return;
+  __shared__ int warp_tot[kScatThreads / 32];
+  scatter_block(a.sc, blockIdx.x, (int *)base, warp_tot,
+                a.sc.stage_bytes ? base + scatter_tab_bytes(a.sc.ng, a.sc.E, a.sc.per) : nullptr,
+                (size_t)a.sc.stage_bytes);
+}
+
 template <bool NORM>
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const __grid_constant__ CUtensorMap tx, RouteArgs a) {
@@ -359,6 +449,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   int *cnt = (int *)(base + L.cnt_off);  // this CTA's pairs per expert
   int *pid = (int *)(base + L.pid_off);  // this CTA's pairs' experts
 
+  // The S CTAs of a token group exchange through distributed shared memory:
+  // a launch without S-CTA clusters returns at once (every CTA sees the same
+  // size), leaving the scatter and the grid barrier untouched.
+  if (cluster_ctas() != (uint32_t)a.S) {
+    if (threadIdx.x == 0 && a.err) atomicExch(a.err, kShapeErrorBase + 3);
+    return;
+  }
   const int S = a.S, z = (int)(blockIdx.x % S), grp = (int)(blockIdx.x / S);
   const int t0 = grp * kRouteTok, ep = a.m_tiles * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -373,6 +470,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   const uint32_t tcols = a.m_tiles * kAcc * kRouteTok;
   for (int e = threadIdx.x; e < ep; e += kRouteThreads) cnt[e] = 0;
 
+  const int err_seen = threadIdx.x == 0 ? ld_err_word(a.err) : 0;
   if (threadIdx.x == 0) {
     *abort = 0;
     for (int s = 0; s < stages; ++s) {
@@ -426,7 +524,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   pdl_wait();
   if (!a.fuse) pdl_trigger();  // fused: the expert FFN may launch only once the scatter's barrier is passed
-  if (threadIdx.x == 0 && a.err && *(volatile int *)a.err) *abort = 1;  // an earlier timeout
+  if (threadIdx.x == 0 && err_seen) *abort = 1;  // an earlier timeout
 
   if (NORM) {
     const float4 *row = (const float4 *)(a.h + (size_t)(tn < a.T ? tn : 0) * a.d);
@@ -656,62 +754,71 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncwarp();
   tc::cluster_sync();  // peers' counts stay alive until every read is done
-  if (!a.fuse) return;
-  // ---- fused scatter ------------------------------------------------------
-  // Every token group's counts and ranks are in global memory once all CTAs
-  // pass a grid-wide barrier (the launch is cooperative: all CTAs are
-  // resident).  Self-resetting: each CTA reads the generation word, then
-  // arrives; the last to arrive zeroes the count and bumps the generation,
-  // which the others wait for (bounded).  Then this CTA's share of the
-  // scatter reuses its shared memory.
-  __syncthreads();
-  __shared__ int passed;
-  if (threadIdx.x == 0) {
-    int *gen = a.bar + 1;
-    const int g0 = ld_acquire_s32(gen);
-    __threadfence();  // this CTA's counts and ranks before its arrival
-    passed = 1;
-    if (atomicAdd(a.bar, 1) == (int)gridDim.x - 1) {
-      atomicExch(a.bar, 0);
-      __threadfence();
-      atomicExch(gen, g0 + 1);
-    } else {
-      const long long c0 = clock64();
-      while (ld_acquire_s32(gen) == g0) {
-        if (clock64() - c0 > tc::kWaitCycles) {
-          if (a.err) atomicExch(a.err, 55);
-          passed = 0;  // counts may be incomplete: leave the scatter undone
-          break;
-        }
-      }
-    }
-    __threadfence();
+  if (a.fuse) fused_scatter_tail(a, base);
+}
+
+template <bool NORM>
+cudaError_t route_attributes() {
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(route_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(route_kernel<NORM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set |= 1ull << dev;
   }
-  __syncthreads();
-  pdl_trigger();
-  if (!passed) return;
-  __shared__ int warp_tot[kScatThreads / 32];
-  scatter_block(a.sc, blockIdx.x, (int *)base, warp_tot);
+  return cudaSuccess;
+}
+
+// Clusters of S CTAs (smem bytes of dynamic shared memory each) that can be
+// resident at once: the cap on a cooperative launch, which must be decided
+// before the launch (a refused launch would end a CUDA graph capture).
+template <bool NORM>
+int route_max_clusters(int S, uint32_t smem) {
+  struct Entry {
+    int dev, S;
+    uint32_t smem;
+    int n;
+  };
+  static Entry cache[16];
+  static int n_cache = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].dev == dev && cache[i].S == S && cache[i].smem == smem) return cache[i].n;
+  if (route_attributes<NORM>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, 1, 1);
+  cfg.blockDim = dim3(kRouteThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, route_kernel<NORM>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (n_cache < 16) cache[n_cache++] = Entry{dev, S, smem, n};
+  return n;
 }
 
 template <bool NORM>
 cudaError_t launch_route(const CUtensorMap &tx, RouteArgs a, cudaStream_t st) {
   const RouteSmem L = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
   auto kern = route_kernel<NORM>;
-  static unsigned long long attr_set = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = route_attributes<NORM>();
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set |= 1ull << dev;
-  }
   const int groups = ceil_div(a.T, kRouteTok);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(groups * a.S, 1, 1);
+  cfg.gridDim = dim3(a.fuse ? a.grid : groups * a.S, 1, 1);
   cfg.blockDim = dim3(kRouteThreads, 1, 1);
   cfg.dynamicSmemBytes = L.bytes;
   cfg.stream = st;
@@ -771,10 +878,18 @@ cudaError_t route_common(bool norm, const float *h, const float *gain, float eps
     a.fuse = 1;
     a.bar = bar;
     a.sc = *fused;
-    const int grid = ceil_div(T, kRouteTok) * a.S;
-    a.sc.per = ceil_div(T * k, grid);
     const RouteSmem full = route_smem(a.S, a.nk_max, a.stages, a.m_tiles);
-    if (scatter_smem_ints(a.sc.ng, E, a.sc.per) * sizeof(int) > full.bytes - 1024) return cudaErrorInvalidValue;
+    // The routing clusters must all be resident together; if they cannot
+    // be, the launch is not fused (decided here: a refused launch would end
+    // a CUDA graph capture).
+    const int max_clusters = norm ? route_max_clusters<true>(a.S, full.bytes) : route_max_clusters<false>(a.S, full.bytes);
+    const int groups = ceil_div(T, kRouteTok);
+    if (groups > max_clusters) return cudaErrorCooperativeLaunchTooLarge;
+    a.grid = a.S * groups;
+    a.sc.per = ceil_div(T * k, a.grid);
+    const size_t tab = scatter_tab_bytes(a.sc.ng, E, a.sc.per), usable = full.bytes - 1024;
+    if (tab > usable) return cudaErrorInvalidValue;
+    a.sc.stage_bytes = (int)(usable - tab);
   }
   CUtensorMap tx{};  // the norm path writes the B operand itself
   if (norm) return launch_route<true>(tx, a, st);
@@ -836,6 +951,7 @@ cudaError_t scatter_args(ScatArgs &a, const bf16 *xn, const int *ids, const int 
   a.sync = work + 2 * max_work;
   a.max_work = max_work;
   a.stats = stats;
+  a.stage_bytes = 0;
   return cudaSuccess;
 }
 
@@ -851,8 +967,12 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
   const int TK = T * k;
   const int grid = max(1, min(ceil_div(TK, 2 * (kScatThreads / 32)), 2 * num_sms_route()));
   a.per = ceil_div(TK, grid);
-  const size_t smem = scatter_smem_ints(a.ng, E, a.per) * sizeof(int);
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  const size_t tab = scatter_tab_bytes(a.ng, E, a.per);
+  if (tab > 200 * 1024) return cudaErrorInvalidValue;
+  // room for the block's token rows (at most per / k + 2 of them), if it fits
+  const size_t stage = (size_t)(a.per / k + 2) * d * 2;
+  a.stage_bytes = tab + stage <= 200 * 1024 ? (int)stage : 0;
+  const size_t smem = tab + a.stage_bytes;
   static unsigned long long attr_set = 0;
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -872,7 +992,14 @@ cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16
   const bool norm = h != nullptr;
   const int S = (d / 64) >= 8 ? 8 : (d / 64) >= 4 ? 4 : (d / 64) >= 2 ? 2 : 1;
   const int grid = ceil_div(T, kRouteTok) * S;
-  if (bar && grid <= num_sms_route()) {  // one CTA per SM: every routing CTA can be resident
+  // DG_FUSE_ROUTE=0 keeps the two launches (for profilers that replay one
+  // kernel at a time: an Nsight Compute capture of the cooperative fused
+  // launch faulted on the GB300).
+  static const bool fuse_allowed = [] {
+    const char *v = getenv("DG_FUSE_ROUTE");
+    return !(v && v[0] == '0');
+  }();
+  if (fuse_allowed && bar && grid <= num_sms_route()) {  // one CTA per SM: every routing CTA can be resident
     ScatArgs a;
     cudaError_t e = scatter_args(a, xn, ids, gcount, slot_row, T, d, E, k, kExpertTileRows, x_tiles, offs, work,
                                  n_work, max_work, stats);
@@ -882,7 +1009,7 @@ cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16
       if (launches) *launches = 1;
       return e;
     }
-    cudaGetLastError();  // not resident together after all: two launches
+    cudaGetLastError();  // too few clusters resident together for the routing: two launches
   }
   cudaError_t e = route_common(norm, h, gain, eps, xn, wr, T, d, E, k, ids, gates, slot_row, gcount, err, st);
   if (e != cudaSuccess) return e;

@@ -349,9 +349,11 @@ int dg_op_fill_weights(uint16_t *dst, uint64_t n, uint64_t seed, uint32_t tensor
  * that gives up (about a second; the kernel then skips its remaining work and
  * its outputs are not valid), or an attention page-table entry outside the
  * pools, is recorded in a per-device status word that this call reads.  It
- * synchronises `stream`, returns DG_ETIMEOUT (a wait gave up) or DG_EINVAL (a
- * bad page index) when a kernel-level call since the last dg_op_status
- * recorded one, and clears the record; DG_OK otherwise.  The record is
+ * synchronises `stream`, returns DG_ETIMEOUT (a wait gave up), DG_ECUDA (a
+ * kernel found itself launched without the thread-block cluster shape it
+ * exchanges partial results in, and returned before touching anything) or
+ * DG_EINVAL (a bad page index) when a kernel-level call since the last
+ * dg_op_status recorded one, and clears the record; DG_OK otherwise.  The record is
  * shared by every kernel-level call on the device, and while it is set later
  * kernel-level kernels skip their waits (their outputs are not valid). */
 int dg_op_status(void *stream);
