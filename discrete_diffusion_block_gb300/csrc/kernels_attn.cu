@@ -245,10 +245,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
   // Physical page of every 64-key half of the block's range (-1 past the
-  // last key or on a bad index), and those pages' K and V into L2, before the
-  // wait on the previous kernel: the page table was written before it started,
-  // cached prefix keys do not depend on it, and L2 is coherent with the
-  // canvas keys it writes.
+  // last key or on a bad index), before the wait on the previous kernel: the
+  // page table was written before it started.  (Requesting those pages' K
+  // and V into L2 here as well delayed the first K tile: the prefetches go
+  // through the same bulk-copy path as the ring's loads.)
   const int n_halves = 2 * n_kt;
   if (warp == 0) {
     for (int i = lane; i < n_halves; i += 32) {
@@ -259,16 +259,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         pg_i = -1;
       }
       if (i < kAttnPages) pages[i] = pg_i;
-      if (pg_i < 0) continue;
-      const size_t off = ((size_t)pg_i * p.Hkv + g) * p.pg * HD + (size_t)(key % p.pg) * 64;
-      for (int b = 0; b < HB; ++b) {
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.k_pool + off + (size_t)b * p.pg * 64),
-                     "r"((uint32_t)kAttnSlotHalfBytes)
-                     : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.v_pool + off + (size_t)b * p.pg * 64),
-                     "r"((uint32_t)kAttnSlotHalfBytes)
-                     : "memory");
-      }
     }
   }
   pdl_wait();
