@@ -16,21 +16,22 @@
 //
 // The kernel is a tcgen05 tensor-core kernel with one pass over the block's
 // key range and an online softmax: per 128-key tile, S = Q K^T (TMEM), the
-// tile's raw-score maximum, P = 2^(S*scale - m) as bf16 into shared memory,
+// tile's raw-score maximum, P = 2^(S*scale - m) as bf16 into tensor memory,
 // row sum l in fp32, O += P V (TMEM).  The running maximum m is raised lazily:
 // only a row whose maximum grows by more than 2^8 moves to the new reference
 // and rescales its accumulator row in TMEM (read, scale, write back) after the
 // previous tile's P V has landed; below that P stays <= 2^8 and the final
-// O / l does not depend on which reference was used.  Roles (352 threads):
+// O / l does not depend on which reference was used.  Roles (384 threads):
 // warp 0 streams Q once (TMA through a 4-D map that packs the G heads of a
 // token as consecutive rows) and the K tiles through a three-slot ring; warp
 // 6 streams the V tiles through their own three-slot ring (both as bulk
 // copies of the pool's pre-swizzled pages, from a page list resolved before
-// the dependency wait); warp 1 issues the MMAs, S of tile i + 1 before P V of
-// tile i, with two S accumulators and two P tiles so the softmax of one tile
-// overlaps the tensor work of the next (P is written to tensor memory by the
-// softmax threads and read from there as the A operand of P V; V is the
-// N-contiguous "MN-major" B operand); warps 2-5 and 7-10 do the softmax, two
+// the dependency wait); warp 1 issues the S = Q K^T MMAs and warp 11 the
+// P V MMAs, each from its own thread, so that S of the next tiles never waits
+// behind this tile's softmax; two S accumulators and two P tiles let the
+// softmax of one tile overlap the tensor work of the next (P is written to
+// tensor memory by the softmax threads and read from there as the A operand
+// of P V; V is the N-contiguous "MN-major" B operand); warps 2-5 and 7-10 do the softmax, two
 // warps per TMEM lane quarter (thread = query row), each on half of a tile's
 // keys, exchanging their halves' maxima per tile.  With the key range split
 // over several blocks, the blocks of one query tile form a
@@ -81,7 +82,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 
-constexpr int kAttnThreads = 352;  // warps 0, 1, 6: copies and MMAs; 2-5 and 7-10: softmax
+constexpr int kAttnThreads = 384;  // warps 0, 6: copies; 1, 11: MMAs; 2-5 and 7-10: softmax
+constexpr int kAttnPvWarp = 11;
 constexpr int kAttnPages = 64;  // 64-key halves whose physical page is looked up before the key loop
 constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one 8 KB copy)
 
@@ -343,7 +345,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && n_kt > 0) {
       const uint32_t idesc_s = tc::idesc_bf16(128, 128);
-      const uint32_t idesc_o = tc::idesc_bf16(128, HD) | (1u << 16);  // B (V) N-contiguous
       tc::mbar_wait(q_full, 0, p.err, 32, abort);
       auto issue_s = [&](int i) {  // S[i & 1] = Q K_i^T
         const int slot = i % KK, buf = i & 1;
@@ -359,9 +360,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc::mma_commit(s_full + buf);
         tc::mma_commit(k_empty + slot);
       };
-      issue_s(0);
+      for (int i = 0; i < n_kt; ++i) issue_s(i);
+    }
+  } else if (warp == kAttnPvWarp) {
+    // P V of every tile, from its own thread: issuing S of the next tiles
+    // does not wait for this tile's softmax (each thread's commits track the
+    // MMAs it issued).
+    if (lane == 0 && n_kt > 0) {
+      const uint32_t idesc_o = tc::idesc_bf16(128, HD) | (1u << 16);  // B (V) N-contiguous
       for (int i = 0; i < n_kt; ++i) {
-        if (i + 1 < n_kt) issue_s(i + 1);
         const int slot = i % KV;
         tc::mbar_wait(p_full, i & 1, p.err, 35, abort);
         tc::mbar_wait(v_full + slot, (i / KV) & 1, p.err, 29, abort);
