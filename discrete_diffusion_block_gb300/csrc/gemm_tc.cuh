@@ -30,9 +30,18 @@
 #pragma once
 #include <cuda.h>
 
-#include "gemm_mma.cuh"
+#include "common.cuh"
 
 namespace dg {
+
+// Context handed to a GEMM epilogue.
+struct TileCtx {
+  int m0, n0;      // tile origin in (M, N)
+  int m_valid;     // rows of the tile inside M
+  int n_valid;     // columns of the tile inside N
+  int swz;         // tile layout: element (f, t) at f * ldc + (t ^ (f & swz)); 0 or 31
+  int prepared;    // the epilogue's prepare() already staged its inputs in its scratch
+};
 
 struct TcArgs {
   int M, N, K;             // D[M][N] = A[M][K] . B[N][K]^T
