@@ -35,6 +35,8 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
+from . import fp8
+
 
 @dataclass(frozen=True)
 class ModelConfig:
@@ -51,6 +53,7 @@ class ModelConfig:
     rms_eps: float = 1e-6
     init_std: float = 0.02
     weight_seed: int = 0
+    expert_fp8: bool = False   # gate/up weights and their input rows in e4m3 (oracle/fp8.py)
 
     def with_(self, **kw):
         return replace(self, **kw)
@@ -159,23 +162,39 @@ def routing_margin(y, wr, forced):
     return np.take_along_axis(r, np.asarray(forced, np.int64), axis=1).min(axis=1) - kth, np.abs(r).max(axis=1)
 
 
-def expert_ffn(x, wg, wu, wd):
-    """SwiGLU expert on rows x [n, d]."""
+def expert_ffn(x, wg, wu, wd, fp8_gate_up=False):
+    """SwiGLU expert on rows x [n, d].
+
+    fp8_gate_up: the gate/up products take e4m3 operands (oracle/fp8.py):
+    each weight row (output feature) and each input row, rounded to bf16 as
+    the decoder hands it over, scaled by its own power of two."""
     wg, wu, wd = (np.asarray(w, np.float64) for w in (wg, wu, wd))
+    if fp8_gate_up:
+        x = fp8.dequantize_rows(*fp8.quantize_rows(bf16_round(x)))
+        wg = fp8.dequantize_rows(*fp8.quantize_rows(wg))
+        wu = fp8.dequantize_rows(*fp8.quantize_rows(wu))
     return (silu(x @ wg.T) * (x @ wu.T)) @ wd.T
 
 
-def moe_given_routing(y, ids, gates, W):
+def bf16_round(x):
+    """Round to the nearest bf16 value, ties to even (float64 in and out)."""
+    f = np.asarray(x, np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def moe_given_routing(y, ids, gates, W, fp8_gate_up=False):
     out = np.zeros_like(y)
     for e in np.unique(ids):
         tok, slot = np.nonzero(ids == e)
-        out[tok] += gates[tok, slot][:, None] * expert_ffn(y[tok], W["wg"][e], W["wu"][e], W["wd"][e])
+        out[tok] += gates[tok, slot][:, None] * expert_ffn(y[tok], W["wg"][e], W["wu"][e], W["wd"][e], fp8_gate_up)
     return out
 
 
-def moe(y, W, k, forced=None, rel_tol=None):
+def moe(y, W, k, forced=None, rel_tol=None, fp8_gate_up=False):
     ids, gates, r = route(y, W["wr"], k, forced, rel_tol=rel_tol)
-    return moe_given_routing(y, ids, gates, W), ids, gates, r
+    return moe_given_routing(y, ids, gates, W, fp8_gate_up), ids, gates, r
 
 
 def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=None, routing_rel_tol=None):
@@ -199,7 +218,7 @@ def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=N
     o = attention(q, K, V, visibility(prefix_k.shape[0], T, mode))
     h = h + o.reshape(T, Hq * hd) @ np.asarray(W["wo"], np.float64).T
     n2 = rmsnorm(h, W["moe_norm"], cfg.rms_eps)
-    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing, routing_rel_tol)
+    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing, routing_rel_tol, cfg.expert_fp8)
     if trace is not None:
         trace.append(dict(n=n, q=q, k=k, v=v, o=o, n2=n2, ids=ids, gates=gates, router=r, y=y))
     return h + y, k, v
