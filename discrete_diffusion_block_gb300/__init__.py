@@ -31,7 +31,7 @@ class DgError(RuntimeError):
 class dg_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_layers", "d_model", "n_q_heads", "n_kv_heads", "head_dim", "n_experts", "top_k",
-        "d_ff", "vocab", "page_size", "max_context", "max_requests")] + [
+        "d_ff", "vocab", "page_size", "max_context", "max_requests", "expert_fp8")] + [
         ("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float), ("init_std", ctypes.c_float),
         ("weight_seed", ctypes.c_uint64)]
 
@@ -68,6 +68,7 @@ class Config:
     page_size: int = 128
     max_context: int = 4096
     max_requests: int = 1
+    expert_fp8: int = 0
     rope_base: float = 10000.0
     rms_eps: float = 1e-6
     init_std: float = 0.02
@@ -158,6 +159,7 @@ _SIGS = {
     "dg_op_lm_head_partials": (_I, [_P, _P, _P, _I, _I, _I, _U64, _I, _I, _F, _P, _P, _P]),
     "dg_op_logits_partials": (_I, [_P, _I, _I, _U64, _I, _I, _F, _P, _P]),
     "dg_op_gumbel_noise": (_I, [_P, _P, _U64, _P]),
+    "dg_op_quantize_rows_e4m3": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "dg_op_fill_tiled_weights": (_I, [_P, _I, _I, _U64, ctypes.c_uint32, _F, _P]),
     "dg_op_sampler_update": (_I, [_P, _I, _I, _I, ctypes.POINTER(dg_sampler_config), _P, _P, _P,
                                   _P, _P, _P, _P, _P, _P]),
@@ -541,6 +543,13 @@ def to_operand_tiles(x):
 
 def dg_op_gumbel_noise(words, out, stream=None):
     _check(load().dg_op_gumbel_noise(_ptr(words), _ptr(out), words.numel(), _stream(stream)))
+
+
+def dg_op_quantize_rows_e4m3(src_tiles, n_mat, rows, cols, dst, exps, stream=None):
+    """bf16 operand tiles of n_mat [rows][cols] matrices -> e4m3 operand tiles
+    (dst: rows * cols bytes each) and row scale exponents (exps int32)."""
+    _check(load().dg_op_quantize_rows_e4m3(_ptr(src_tiles), n_mat, rows, cols, _ptr(dst), _ptr(exps),
+                                           _stream(stream)))
 
 
 def dg_op_sampler_update(partials, C, V, step, scfg, x, committed, last, stable, argmax, conf,

@@ -273,6 +273,32 @@ __host__ __device__ inline size_t tiled_index(int rows, int cols, int r, int c) 
   return (size_t)128 * cols * b + (size_t)rows_b * 64 * kt + (size_t)rr * 64 + (size_t)((((cc >> 3) ^ (rr & 7)) << 3) | (cc & 7));
 }
 
+// ---- e4m3 (FP8) expert path -------------------------------------------------
+// A row (an output feature of W_gate / W_up, or a token row of the expert
+// input) is stored as e4m3(row * 2^-k) with k the smallest integer such that
+// max|row| <= 448 * 2^k; conversion rounds to nearest even and saturates.
+// An e4m3 matrix [R][C] in operand tiles occupies the bytes of a bf16 matrix
+// [R][C/2] in operand tiles: 128-row blocks of 128-byte rows (128 elements
+// per k-tile), 16-element chunk j of row r at chunk position j ^ (r % 8).
+__device__ __forceinline__ int e4m3_scale_exp(float absmax) {
+  if (!(absmax > 0.0f)) return 0;
+  int e;
+  const float m = frexpf(absmax, &e);  // absmax = m 2^e, 448 * 2^(e-9) = 0.875 * 2^e
+  return m <= 0.875f ? e - 9 : e - 8;
+}
+
+// Two e4m3 codes: `lo` in the low byte (the lower address), `hi` in the high.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Byte offset of e4m3 element (r, c), c a multiple of 16, in operand tiles of [rows][cols].
+__host__ __device__ inline size_t tiled_index_e4m3(int rows, int cols, int r, int c) {
+  return 2 * tiled_index(rows, cols / 2, r, c / 2);
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args &&...args) {

@@ -64,6 +64,8 @@ constexpr int kPrefillChunk = 2048;
 
 struct Layer {
   bf16 *wqkv = nullptr, *wo = nullptr, *wr = nullptr, *wgu = nullptr, *wd = nullptr;
+  uint8_t *wgu8 = nullptr;  // expert_fp8: W_gate / W_up as e4m3 operand tiles
+  int *kw = nullptr;        // expert_fp8: their rows' scale exponents [E][2][F]
   float *attn_norm = nullptr, *moe_norm = nullptr;
 };
 
@@ -100,6 +102,7 @@ struct dg_model {
        *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   int *route_bar = nullptr;                  // device, 2 ints: grid barrier of the fused routing + scatter
+  int *kx = nullptr;                         // expert_fp8: scale exponents of the expert input rows
   float *gates = nullptr, *y = nullptr;
   float *xchg = nullptr;  // split-K partial exchange of the projection GEMMs
   int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
@@ -302,6 +305,8 @@ int validate(const dg_config *c, const dg_sampler_config *s) {
     return fail(DG_EINVAL, "page_size must be a positive multiple of 64");
   if (c->max_requests < 0 || c->max_requests > dg::kMaxRequests)
     return fail(DG_EINVAL, "max_requests must be in [0, %d]", dg::kMaxRequests);
+  if (c->expert_fp8 != 0 && c->expert_fp8 != 1) return fail(DG_EINVAL, "expert_fp8 must be 0 or 1");
+  if (c->expert_fp8 && c->d_model % 128) return fail(DG_EINVAL, "expert_fp8 needs d_model a multiple of 128");
   if (s->canvas_len < 1 || s->canvas_len > 1024) return fail(DG_EINVAL, "canvas_len must be in [1, 1024]");
   if (c->max_context < s->canvas_len) return fail(DG_EINVAL, "max_context smaller than one canvas");
   if (s->budget_N < 1 || s->budget_N > 65535) return fail(DG_EINVAL, "budget_N must be in [1, 65535]");
@@ -342,14 +347,16 @@ int run_layers(dg_model *m, int T, const dg::RowSet &rows, const int *ptab, int 
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
     int nl = 0;  // routing and scatter: one launch, or two when the routing grid exceeds the machine
+    const dg::Fp8Experts fx{W.wgu8, W.kw, m->kx};
     KL(DG_K_ROUTE, nl,
        dg::moe_route_scatter(m->h, W.moe_norm, c.rms_eps, m->xn, W.wr, T, d, c.n_experts, c.top_k, topk,
                              m->gates, m->slot_row, m->gcount, m->x_tiles, m->offs, m->work, m->n_work,
-                             m->max_work, m->route_bar, err, st, m->moe_stats, &nl));
+                             m->max_work, m->route_bar, err, st, m->moe_stats, &nl,
+                             c.expert_fp8 ? &fx : nullptr));
     const int rows = T * c.top_k;
     KL(DG_K_EXPERT_FFN, 1,
        dg::moe_ffn(m->x_tiles, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
-                   c.n_experts, d, c.d_ff, m->act, m->y, err, st));
+                   c.n_experts, d, c.d_ff, m->act, m->y, err, st, c.expert_fp8 ? &fx : nullptr));
     if (fuse_norm && L + 1 < c.n_layers) {
       KL(DG_K_COMBINE, 1,
          dg::moe_combine_norm(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, m->layers[L + 1].attn_norm,
@@ -456,6 +463,7 @@ int alloc_model(dg_model *m, const void *const *weights) {
   CKR(m->alloc(&m->offs, E + 1));
   CKR(m->alloc(&m->gcount, dg::moe_group_count_ints(T, E)));
   CKR(m->alloc(&m->slot_row, (size_t)T * k));
+  if (c.expert_fp8) CKR(m->alloc(&m->kx, (size_t)T * k));
   CKR(m->alloc(&m->work, dg::moe_work_ints(T, k, E, dg::kExpertTileRows)));
   CKR(m->alloc(&m->n_work, 1));
   CKR(m->alloc(&m->act, dg::moe_item_tile_elems(m->max_work, F)));
@@ -502,6 +510,19 @@ int device_fail(int code) {
   if (code >= dg::kShapeErrorBase)
     return fail(DG_ECUDA, "a kernel ran without the cluster shape it was launched with (code %d)", code);
   return fail(DG_ETIMEOUT, "a bounded device-side wait gave up (code %d)", code);
+}
+
+// expert_fp8: the e4m3 copy of every layer's W_gate / W_up and their rows'
+// scale exponents, made from the bf16 weights (seeded or borrowed).
+int quantize_expert_weights(dg_model *m) {
+  const dg_config &c = m->cfg;
+  const int E = c.n_experts, F = c.d_ff, d = c.d_model;
+  for (auto &W : m->layers) {
+    CKR(m->alloc(&W.wgu8, (size_t)E * 2 * F * d));
+    CKR(m->alloc(&W.kw, (size_t)E * 2 * F));
+    CK(dg::quantize_rows_e4m3(W.wgu, W.wgu8, W.kw, 2 * E, F, d, m->stream));
+  }
+  return DG_OK;
 }
 
 int check_model(dg_model *m) {
@@ -879,6 +900,7 @@ int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, const voi
   }
   int r = alloc_model(m, weights);
   if (r == DG_OK && !weights) r = fill_model_weights(m);
+  if (r == DG_OK && cfg->expert_fp8) r = quantize_expert_weights(m);
   if (r == DG_OK) {
     cudaError_t e = dg::rope_table(m->cos_t, m->sin_t, cfg->max_context, cfg->head_dim,
                                    cfg->rope_base, m->stream);
@@ -1519,6 +1541,14 @@ int dg_op_fill_tiled_weights(uint16_t *dst, int32_t rows, int32_t cols, uint64_t
 int dg_op_gumbel_noise(const uint32_t *words, float *out, uint64_t n, void *stream) {
   if ((!words || !out) && n) return fail(DG_EINVAL, "null pointer");
   CK(dg::gumbel_noise(words, out, (size_t)n, (cudaStream_t)stream));
+  return DG_OK;
+}
+
+int dg_op_quantize_rows_e4m3(const uint16_t *src, int32_t n_mat, int32_t rows, int32_t cols, uint8_t *dst,
+                             int32_t *exps, void *stream) {
+  if (n_mat < 0 || rows < 0 || cols < 128 || cols % 128) return fail(DG_EINVAL, "cols must be a positive multiple of 128");
+  if ((!src || !dst || !exps) && n_mat && rows) return fail(DG_EINVAL, "null pointer");
+  CK(dg::quantize_rows_e4m3((const bf16 *)src, dst, exps, n_mat, rows, cols, (cudaStream_t)stream));
   return DG_OK;
 }
 

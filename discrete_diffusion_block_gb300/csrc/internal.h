@@ -56,9 +56,10 @@ cudaError_t moe_norm_route(const float *h, const float *gain, float eps, bf16 *x
                            cudaStream_t st);
 cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k, int *ids, float *gates,
                       int *rank, int *gcount, int *err, cudaStream_t st);
+struct Fp8Experts;
 cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
                         int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
-                        cudaStream_t st, unsigned long long *stats = nullptr);
+                        cudaStream_t st, unsigned long long *stats = nullptr, const Fp8Experts *fp8 = nullptr);
 // moe_norm_route (h != null) or moe_route, then moe_scatter, as one launch
 // when the routing grid fits the machine (the scatter then runs in the
 // routing kernel after a grid-wide barrier on bar, 2 zeroed ints), else as
@@ -67,7 +68,8 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
 cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
                               int E, int k, int *ids, float *gates, int *slot_row, int *gcount, bf16 *x_tiles,
                               int *offs, int *work, int *n_work, int max_work, int *bar, int *err, cudaStream_t st,
-                              unsigned long long *stats = nullptr, int *launches = nullptr);
+                              unsigned long long *stats = nullptr, int *launches = nullptr,
+                              const Fp8Experts *fp8 = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
 size_t moe_work_ints(int T, int k, int E, int tile_rows);
 // Routed experts of one layer (kernels_moe.cu): act = SwiGLU(X Wg^T, X Wu^T),
@@ -75,9 +77,22 @@ size_t moe_work_ints(int T, int k, int E, int tile_rows);
 // X: the item tiles of moe_scatter; wgu / wd: expert weights as operand tiles
 // (the fill kernels' layout); act_tiles: moe_item_tile_elems(max_work, F)
 // elements of scratch; y: [rows][d] fp32, row = sorted pair row.
+// The e4m3 expert path (kernels_moe.cu): gate/up weights as e4m3 operand
+// tiles (the bytes of bf16 tiles [E][2][F][d/2]) with their rows' scale
+// exponents kw [E][2][F]; the scatter writes the token rows as e4m3 tiles and
+// their exponents kx [rows].
+struct Fp8Experts {
+  const uint8_t *wgu8;
+  const int *kw;
+  int *kx;
+};
+// Rows of n_mat bf16 operand-tile matrices [R][C] to e4m3 operand tiles and
+// scale exponents [n_mat][R] (C a multiple of 128).
+cudaError_t quantize_rows_e4m3(const bf16 *src, uint8_t *dst, int *exps, int n_mat, int R, int C,
+                               cudaStream_t st);
 cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
-                    float *y, int *err, cudaStream_t st);
+                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8 = nullptr);
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
 // h[t] += sum_s gate * y (as moe_combine with accumulate), then the RMSNorm of

@@ -92,7 +92,13 @@ struct FfnArgs {
   const int *work, *n_work, *offs;
   const bf16 *wgu;  // per expert: operand tiles of W_gate [F][d], then of W_up [F][d]
   const bf16 *wd;   // per expert: operand tiles of W_down [d][F]
-  const bf16 *x;    // [item][d/64] tiles: the item's token rows
+  const bf16 *x;    // [item][d/64] tiles: the item's token rows (fp8: [item][d/128] e4m3 tiles)
+  // fp8 != 0: the gate/up products take e4m3 operands: wgu8 holds W_gate /
+  // W_up as e4m3 operand tiles (same order as wgu), kw their rows' scale
+  // exponents [E][2][F], kx the exponents of the token rows [rows]
+  int fp8;
+  const uint8_t *wgu8;
+  const int *kw, *kx;
   int *done;   // [max_work] phase A units finished per item
   int *next;   // unit counter
   int E, d, F;
@@ -123,6 +129,22 @@ __device__ __forceinline__ bool epi_any(bool v) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(b)) : "memory");
+}
+
+// D (+)= A B^T with e4m3 A and B (kind::f8f6f4, K = 32 per instruction, the
+// same 128-byte swizzled operand rows as the bf16 MMAs: 128 elements a row).
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+}
+
+// Instruction descriptor: fp32 accumulator, e4m3 A and B (type code 0),
+// both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ float swiglu_f(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
@@ -183,7 +205,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   const int n_items = *g.n_work;
   const int mA = (g.F + 127) / 128, mB = (g.d + 128 * kDownBlocks - 1) / (128 * kDownBlocks);
   const int nA = n_items * mA, n_units = nA + n_items * mB;
-  const int KTA = g.d / tc::kBK, KTB = g.F / tc::kBK;
+  // gate/up k-steps: 64 bf16 or 128 e4m3 elements (128 bytes a row either way)
+  const int KTA = g.fp8 ? g.d / 128 : g.d / tc::kBK, KTB = g.F / tc::kBK;
   auto a_tile = [&](int s, int j) { return base + (size_t)s * kFfnStageBytes + (size_t)j * kFfnATileBytes; };
   auto b_tile = [&](int s) { return base + (size_t)s * kFfnStageBytes + 2 * kFfnATileBytes; };
 
@@ -221,6 +244,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         if (inf.phase) {
           a0 = g.wd + (size_t)inf.e * g.d * g.F + (size_t)(kDownBlocks * inf.mt) * 128 * g.F;
           a_blk = (size_t)128 * g.F;
+        } else if (g.fp8) {  // e4m3 tiles: the bytes of bf16 tiles of half the columns
+          const int dh = g.d / 2;
+          a0 = (const bf16 *)g.wgu8 + (size_t)inf.e * 2 * g.F * dh + (size_t)128 * dh * inf.mt;
+          a_blk = (size_t)g.F * dh;
         } else {
           a0 = g.wgu + (size_t)inf.e * 2 * g.F * g.d + (size_t)128 * g.d * inf.mt;
           a_blk = (size_t)g.F * g.d;
@@ -297,7 +324,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         if (n >= 2) tc::mbar_wait(acc_empty + buf, ((n >> 1) - 1) & 1, g.err, 25, abort);
         tc::fence_after();
         const uint32_t d0 = tmem + buf * kFfnPairCols, d1 = d0 + kFfnBN;
-        const uint32_t idesc = tc::idesc_bf16(128, max(16, (inf.n_valid + 15) & ~15));
+        const int n_mma = max(16, (inf.n_valid + 15) & ~15);
+        const bool f8 = g.fp8 && inf.phase == 0;
+        const uint32_t idesc = f8 ? idesc_e4m3(128, n_mma) : tc::idesc_bf16(128, n_mma);
         const int KT = inf.phase ? KTB : KTA;
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int s = it % kFfnStages, r = it / kFfnStages;
@@ -306,10 +335,18 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           const uint64_t adesc0 = tc::sw128_desc(tc::smem_u32(a_tile(s, 0)));
           const uint64_t adesc1 = tc::sw128_desc(tc::smem_u32(a_tile(s, 1)));
           const uint64_t bdesc = tc::sw128_desc(tc::smem_u32(b_tile(s)));
+          if (f8) {
 #pragma unroll
-          for (int kk = 0; kk < tc::kBK / 16; ++kk) {
-            tc::mma_bf16(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
-            if (inf.n_acc > 1) tc::mma_bf16(d1, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {  // 32 e4m3 elements (32 bytes) per MMA
+              mma_e4m3(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+              mma_e4m3(d1, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < tc::kBK / 16; ++kk) {
+              tc::mma_bf16(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+              if (inf.n_acc > 1) tc::mma_bf16(d1, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
+            }
           }
           tc::mma_commit(empty + s);
         }
@@ -338,6 +375,12 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         // (features f, f + 1) of one token row into the act tile.
         const bool fok = lrow < inf.a_rows;
         const int fb = 128 * inf.mt + (lrow & ~1), cc = fb & 63;
+        // fp8: this feature's gate and up exponents (the token rows' come per column)
+        int kwg = 0, kwu = 0;
+        if (g.fp8 && fok) {
+          kwg = g.kw[((size_t)inf.e * 2) * g.F + 128 * inf.mt + lrow];
+          kwu = g.kw[((size_t)inf.e * 2 + 1) * g.F + 128 * inf.mt + lrow];
+        }
         unsigned char *blk =
             (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + (fb >> 6)) * kTileElems);
 #pragma unroll 1
@@ -347,8 +390,17 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           uint32_t gv[32], uv[32];
           tc::tmem_ld32(tp + col0, gv);
           tc::tmem_ld32(tp + kFfnBN + col0, uv);
+          const int kx_lane = g.fp8 && col0 + lane < inf.n_valid ? g.kx[inf.b_row + col0 + lane] : 0;
           tc::tmem_ld_wait(gv);
           tc::tmem_ld_wait(uv);
+          if (g.fp8) {  // back to the rows' scales: exact powers of two
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int kx = __shfl_sync(0xffffffffu, kx_lane, j);
+              gv[j] = __float_as_uint(ldexpf(__uint_as_float(gv[j]), kwg + kx));
+              uv[j] = __float_as_uint(ldexpf(__uint_as_float(uv[j]), kwu + kx));
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float a0 = swiglu_f(__uint_as_float(gv[2 * j]), __uint_as_float(uv[2 * j]));
@@ -400,6 +452,46 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   }
 }
 
+// Rows of n_mat bf16 operand-tile matrices [R][C] (contiguous, R * C
+// elements each) to e4m3 operand tiles (R * C bytes each) and their scale
+// exponents [n_mat][R]: one warp per row, the row read twice (its maximum,
+// then 16 elements per lane and step).
+__global__ void quantize_rows_e4m3_kernel(const bf16 *src, uint8_t *dst, int *exps, int n_mat, int R, int C) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= (long long)n_mat * R) return;
+  const int m = (int)(gw / R), r = (int)(gw - (long long)m * R);
+  const bf16 *A = src + (size_t)m * R * C;
+  uint8_t *B = dst + (size_t)m * R * C;
+  float amax = 0.0f;
+  for (int c = 8 * lane; c < C; c += 256) {
+    const uint4 v = *(const uint4 *)(A + tiled_index(R, C, r, c));
+    const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)&v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(p2[i]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const int k = e4m3_scale_exp(amax);
+  for (int c = 16 * lane; c < C; c += 512) {
+    uint4 v[2];
+    v[0] = *(const uint4 *)(A + tiled_index(R, C, r, c));
+    v[1] = *(const uint4 *)(A + tiled_index(R, C, r, c + 8));
+    const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)v;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __bfloat1622float2(p2[2 * i]), b = __bfloat1622float2(p2[2 * i + 1]);
+      w[i] = cvt_e4m3x2(ldexpf(a.x, -k), ldexpf(a.y, -k)) | (cvt_e4m3x2(ldexpf(b.x, -k), ldexpf(b.y, -k)) << 16);
+    }
+    *(uint4 *)(B + tiled_index_e4m3(R, C, r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (lane == 0) exps[(size_t)m * R + r] = k;
+}
+
 int ffn_num_sms() {
   static int cached[64] = {0};
   int dev = 0;
@@ -414,9 +506,18 @@ int ffn_num_sms() {
 
 }  // namespace
 
+cudaError_t quantize_rows_e4m3(const bf16 *src, uint8_t *dst, int *exps, int n_mat, int R, int C,
+                               cudaStream_t st) {
+  if (n_mat <= 0 || R <= 0) return cudaSuccess;
+  if (C <= 0 || C % 128) return cudaErrorInvalidValue;
+  const long long threads = (long long)n_mat * R * 32;
+  quantize_rows_e4m3_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(src, dst, exps, n_mat, R, C);
+  return cudaGetLastError();
+}
+
 cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
-                    float *y, int *err, cudaStream_t st) {
+                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8) {
   if (rows <= 0) return cudaSuccess;
   if (d % 128 || F % 64) return cudaErrorInvalidValue;
   static_assert(FfnSmem::bytes <= 232448, "shared memory of the expert FFN");
@@ -444,6 +545,12 @@ cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *
   g.act = act_tiles;
   g.y = y;
   g.err = err;
+  if (fp8) {
+    g.fp8 = 1;
+    g.wgu8 = fp8->wgu8;
+    g.kw = fp8->kw;
+    g.kx = fp8->kx;
+  }
   return launch_pdl(moe_ffn_kernel, dim3(ffn_num_sms()), dim3(kFfnThreads), FfnSmem::bytes, st, g);
 }
 

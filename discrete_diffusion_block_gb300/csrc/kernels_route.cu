@@ -72,6 +72,8 @@ struct ScatArgs {
   int T, d, E, k, tile_rows, ng;
   int per;        // pairs per block
   int stage_bytes;  // shared memory after the table for the block's token rows (0: none)
+  int fp8;        // rows written as e4m3 operand tiles ([item][d/128], 16 KB each) with exponents kx
+  int *kx;        // fp8: scale exponent of every sorted row
   int *offs, *work, *n_work, *sync;
   int max_work;
   unsigned long long *stats;
@@ -187,6 +189,47 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
       }
     }
     __syncthreads();
+    if (a.fp8) {
+      // One warp per pair: the row's scale exponent from its maximum, then
+      // 16 e4m3 elements per lane and step into row r of the item's e4m3
+      // tiles (128 elements a k-tile; chunk j at position j ^ (r % 8)).
+      for (int p = p0 + warp; p < p1; p += NW) {
+        const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
+        const int within = tab[g * E + ex] + s_rk[p - p0];
+        if (lane == 0) a.slot_row[p] = soffs[ex] + within;
+        const int item = stoff[ex] + within / a.tile_rows, rr = within % a.tile_rows;
+        const uint4 *row = st4 + (size_t)(t - t_lo) * vec;
+        float amax = 0.0f;
+        for (int c = lane; c < vec; c += 32) {
+          const uint4 v = row[c];
+          const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)&v;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(p2[i]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const int kexp = e4m3_scale_exp(amax);
+        unsigned char *dst8 = (unsigned char *)a.x_tiles + (size_t)item * (a.d / 128) * 16384 + (size_t)rr * 128;
+        for (int j = lane; j < a.d / 16; j += 32) {
+          uint4 v[2] = {row[2 * j], row[2 * j + 1]};
+          const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)v;
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 x0 = __bfloat1622float2(p2[2 * i]), x1 = __bfloat1622float2(p2[2 * i + 1]);
+            w[i] = cvt_e4m3x2(ldexpf(x0.x, -kexp), ldexpf(x0.y, -kexp)) |
+                   (cvt_e4m3x2(ldexpf(x1.x, -kexp), ldexpf(x1.y, -kexp)) << 16);
+          }
+          const int kt = j >> 3, ch = j & 7;
+          *(uint4 *)(dst8 + (size_t)kt * 16384 + ((ch ^ (rr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (lane == 0) a.kx[soffs[ex] + within] = kexp;
+      }
+      return;
+    }
     // One warp per pair: the token's row into row r of its item's tiles
     // (16-byte chunk c of k-tile kt at chunk position c ^ (r % 8): the tensor
     // core's swizzled operand order).
@@ -931,7 +974,8 @@ namespace {
 
 cudaError_t scatter_args(ScatArgs &a, const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T,
                          int d, int E, int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work,
-                         int max_work, unsigned long long *stats) {
+                         int max_work, unsigned long long *stats, const Fp8Experts *fp8) {
+  if (fp8 && (d % 128 || !fp8->kx)) return cudaErrorInvalidValue;
   if (T < 0 || d % 64 || E < 1 || E > kScatThreads || k < 1 || tile_rows != 128) return cudaErrorInvalidValue;
   if ((size_t)max_work < moe_max_work(T, k, E, tile_rows)) return cudaErrorInvalidValue;
   a.xn = xn;
@@ -952,6 +996,8 @@ cudaError_t scatter_args(ScatArgs &a, const bf16 *xn, const int *ids, const int 
   a.max_work = max_work;
   a.stats = stats;
   a.stage_bytes = 0;
+  a.fp8 = fp8 ? 1 : 0;
+  a.kx = fp8 ? fp8->kx : nullptr;
   return cudaSuccess;
 }
 
@@ -959,10 +1005,10 @@ cudaError_t scatter_args(ScatArgs &a, const bf16 *xn, const int *ids, const int 
 
 cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
                         int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,
-                        cudaStream_t st, unsigned long long *stats) {
+                        cudaStream_t st, unsigned long long *stats, const Fp8Experts *fp8) {
   ScatArgs a;
   cudaError_t e = scatter_args(a, xn, ids, gcount, slot_row, T, d, E, k, tile_rows, x_tiles, offs, work, n_work,
-                               max_work, stats);
+                               max_work, stats, fp8);
   if (e != cudaSuccess) return e;
   const int TK = T * k;
   const int grid = max(1, min(ceil_div(TK, 2 * (kScatThreads / 32)), 2 * num_sms_route()));
@@ -972,6 +1018,7 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
   // room for the block's token rows (at most per / k + 2 of them), if it fits
   const size_t stage = (size_t)(a.per / k + 2) * d * 2;
   a.stage_bytes = tab + stage <= 200 * 1024 ? (int)stage : 0;
+  if (a.fp8 && !a.stage_bytes) return cudaErrorInvalidValue;  // e4m3 rows are written from the staged rows
   const size_t smem = tab + a.stage_bytes;
   static unsigned long long attr_set = 0;
   int dev = 0;
@@ -988,7 +1035,7 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
 cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,
                               int E, int k, int *ids, float *gates, int *slot_row, int *gcount, bf16 *x_tiles,
                               int *offs, int *work, int *n_work, int max_work, int *bar, int *err, cudaStream_t st,
-                              unsigned long long *stats, int *launches) {
+                              unsigned long long *stats, int *launches, const Fp8Experts *fp8) {
   const bool norm = h != nullptr;
   const int S = (d / 64) >= 8 ? 8 : (d / 64) >= 4 ? 4 : (d / 64) >= 2 ? 2 : 1;
   const int grid = ceil_div(T, kRouteTok) * S;
@@ -1002,7 +1049,7 @@ cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16
   if (fuse_allowed && bar && grid <= num_sms_route()) {  // one CTA per SM: every routing CTA can be resident
     ScatArgs a;
     cudaError_t e = scatter_args(a, xn, ids, gcount, slot_row, T, d, E, k, kExpertTileRows, x_tiles, offs, work,
-                                 n_work, max_work, stats);
+                                 n_work, max_work, stats, fp8);
     if (e != cudaSuccess) return e;
     e = route_common(norm, h, gain, eps, xn, wr, T, d, E, k, ids, gates, slot_row, gcount, err, st, &a, bar);
     if (e != cudaErrorCooperativeLaunchTooLarge) {
@@ -1015,7 +1062,7 @@ cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16
   if (e != cudaSuccess) return e;
   if (launches) *launches = 2;
   return moe_scatter(xn, ids, gcount, slot_row, T, d, E, k, kExpertTileRows, x_tiles, offs, work, n_work, max_work,
-                     st, stats);
+                     st, stats, fp8);
 }
 
 }  // namespace dg

@@ -70,6 +70,15 @@ typedef struct dg_config {
     int32_t max_context;   /* KV pool capacity in tokens (prompt + canvases), per request */
     int32_t max_requests;  /* requests decoded together (0 or 1: one; at most 8), see
                               dg_generate_batch                                */
+    int32_t expert_fp8;    /* 1: the experts' gate/up products in FP8 e4m3 (blog
+                              "Test Conditions Behind 1,456 Tokens per Second":
+                              FP8 serving): each W_gate / W_up row and each
+                              expert input row stored as e4m3(row * 2^-k), k the
+                              smallest integer with max|row| <= 448 * 2^k
+                              (round to nearest even, saturating); W_down and
+                              the SwiGLU output stay bf16; d_model a multiple
+                              of 128.  The e4m3 copy is made from the bf16
+                              weights at init (seeded or borrowed).  0: bf16.  */
     float rope_base;       /* RoPE theta base (10000)                        */
     float rms_eps;         /* RMSNorm epsilon (1e-6)                         */
     float init_std;        /* std of the seeded random-init weights (0.02)   */
@@ -488,6 +497,18 @@ int dg_op_fill_tiled_weights(uint16_t *dst, int32_t rows, int32_t cols, uint64_t
  * entries).  Test hook: lets the transform be compared with a reference over
  * every distinct input. */
 int dg_op_gumbel_noise(const uint32_t *words, float *out, uint64_t n, void *stream);
+
+/* The FP8 expert path's weight quantizer (dg_config.expert_fp8): n_mat bf16
+ * matrices [rows][cols] in operand tiles (contiguous, rows * cols elements
+ * each; cols a multiple of 128) to e4m3 (fn) operand tiles (rows * cols bytes
+ * each: the bytes of bf16 tiles [rows][cols/2]; element (r, c) of a 128-row
+ * block at k-tile c / 128, 16-element chunk ((c % 128) / 16) ^ (r % 8)) and
+ * each row's scale exponent k (exps [n_mat][rows]): row = e4m3 row * 2^k, k
+ * the smallest integer with max|row| <= 448 * 2^k (0 for a zero row),
+ * conversion rounding to nearest even and saturating.  Device pointers; the
+ * caller owns them.  No counterpart in the paper beyond "FP8 weights". */
+int dg_op_quantize_rows_e4m3(const uint16_t *src, int32_t n_mat, int32_t rows, int32_t cols, uint8_t *dst,
+                             int32_t *exps, void *stream);
 
 /* Merge the partials of each row by a balanced binary tree over the tiles
  * (left = lower vocab range; M = max; S = sL*exp(mL-M) + sR*exp(mR-M);
