@@ -394,7 +394,7 @@ def gpu_arm(args):
     m.close()
     del m
 
-    micro_lines, long_ctx, batch = None, None, None
+    micro_lines, long_ctx, batch, fp8 = None, None, None, None
     if rank == 0 and not args.no_extra:
         micro_lines = micro_results(dgp, "all", args.micro_reps)
         log("micro-ops done")
@@ -402,6 +402,8 @@ def gpu_arm(args):
         log("long context done")
         batch = batched(dgp, stream)
         log("batched done")
+        fp8 = fp8_experts(dgp, stream, value)
+        log("fp8 experts done")
     expert_gb = touched / n_moe * 3 * cfg.d_ff * cfg.d_model * 2 * cfg.n_layers / 1e9
 
     cpu = None
@@ -428,6 +430,7 @@ def gpu_arm(args):
                 "experts_touched_per_moe_launch": round(touched / n_moe, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "prefill": prefill, "micro": micro_lines, "long_context": long_ctx, "batched": batch,
+                "fp8_experts": fp8,
                 "clocks": clk.summary(), "gpu_launches": launches}
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -653,6 +656,41 @@ def long_context(dgp, stream, tf_burst):
 BATCH = 4
 
 
+def fp8_experts(dgp, stream, bf16_value):
+    """The same workload as the value (2048-token prompt, 4 canvases of 256,
+    N = 48, adaptive) with the experts' gate/up products in FP8 e4m3
+    (dg_config.expert_fp8): two untimed decodes (graph capture, warm-up), then
+    two decodes timed with CUDA events on the model's stream.  Not the
+    headline: the value is the bf16 decoder's."""
+    import torch
+    from discrete_diffusion_block_gb300 import synth
+    cfg = dgp.full_config(max_context=PROMPT + CANVASES * C, expert_fp8=1)
+    scfg = dgp.SamplerConfig(budget_N=BUDGET, adaptive=1)
+    m = dgp.dg_init_model(cfg, scfg, stream=stream)
+    dgp.dg_prefill(m, synth.prompt_ids(PROMPT, cfg.vocab, seed=1000))
+    for w in range(2):
+        decode_all(dgp, m, 20_000 + w, scfg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    Ns = []
+    for s in range(2):
+        n, _ = decode_all(dgp, m, 30_000 + s, scfg)
+        Ns += n
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    m.close()
+    del m
+    torch.cuda.empty_cache()
+    value = sum(Ns) / (ms / 1e3)                 # counted like the value: denoising steps (Eq. 8)
+    return {"workload": WORKLOAD + "; expert gate/up products in FP8 e4m3 (per-row power-of-two scales)",
+            "denoise_steps_per_s": round(value, 2), "vs_bf16_experts": round(value / bf16_value, 3),
+            "decode_ms": round(ms, 1), "N_k": Ns,
+            "note": "W_down and the SwiGLU output stay bf16; timed like the value (all canvases of a "
+                    "decode, KV-append forwards included; denoising steps counted)"}
+
+
 def batched(dgp, stream):
     """Lockstep multi-request batching on the same decoder: 4 requests, each a
     2048-token random prompt and 4 canvases of 256 (N = 48, adaptive), every
@@ -727,7 +765,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the micro-op and long-context sections of the JSON line")
     ap.add_argument("--micro-reps", type=int, default=10)
-    ap.add_argument("--section", default=None, choices=["long", "batched"],
+    ap.add_argument("--section", default=None, choices=["long", "batched", "fp8"],
                     help="run one extra section of the JSON line alone and print it")
     ap.add_argument("--micro", default=None,
                     choices=["moe", "lmhead", "sampler", "attention", "kv_append", "all"],
@@ -747,7 +785,12 @@ def main():
         build.build()
         dgp.load()
         stream = torch.cuda.Stream(device=torch.device("cuda", 0))
-        out = long_context(dgp, stream, peaks()[1]) if args.section == "long" else batched(dgp, stream)
+        if args.section == "long":
+            out = long_context(dgp, stream, peaks()[1])
+        elif args.section == "batched":
+            out = batched(dgp, stream)
+        else:
+            out = fp8_experts(dgp, stream, float("nan"))
         print(json.dumps(out), flush=True)
         return 0
     if args.impl == "reference":

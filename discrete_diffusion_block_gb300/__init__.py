@@ -141,6 +141,7 @@ _SIGS = {
     "dg_canvas_logits": (_I, [_P, _P]),
     "dg_read_kv": (_I, [_P, _I, _I, _I, _P, _P]),
     "dg_read_routing": (_I, [_P, _I, _P, _I, _P]),
+    "dg_read_moe_input": (_I, [_P, _P, _I, _P, _P]),
     "dg_read_page_table": (_I, [_P, _P, _I, _P]),
     "dg_get_weight": (_I, [_P, _I, _I, ctypes.POINTER(_P), ctypes.POINTER(_SZ)]),
     "dg_kernel_class_name": (ctypes.c_char_p, [_I]),
@@ -404,6 +405,15 @@ def dg_read_kv(m, layer, pos0, n):
     k, v = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
     _check(load().dg_read_kv(m.handle, layer, pos0, n, _ptr(k), _ptr(v)))
     return k, v
+
+
+def dg_read_moe_input(m):
+    """(bf16 bits [rows][d_model] uint16, layer) of the last MoE input."""
+    n, L = ctypes.c_int32(), ctypes.c_int32()
+    _check(load().dg_read_moe_input(m.handle, None, 0, ctypes.byref(n), ctypes.byref(L)))
+    rows = np.zeros((n.value, m.cfg.d_model), np.uint16)
+    _check(load().dg_read_moe_input(m.handle, _ptr(rows), n.value, ctypes.byref(n), ctypes.byref(L)))
+    return rows, L.value
 
 
 def dg_read_routing(m, layer):

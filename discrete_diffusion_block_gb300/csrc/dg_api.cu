@@ -103,6 +103,7 @@ struct dg_model {
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   int *route_bar = nullptr;                  // device, 2 ints: grid barrier of the fused routing + scatter
   int *kx = nullptr;                         // expert_fp8: scale exponents of the expert input rows
+  int moe_input_rows = 0, moe_input_layer = -1;  // the rows xn holds: the last MoE input
   float *gates = nullptr, *y = nullptr;
   float *xchg = nullptr;  // split-K partial exchange of the projection GEMMs
   int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
@@ -346,6 +347,8 @@ int run_layers(dg_model *m, int T, const dg::RowSet &rows, const int *ptab, int 
     KL(DG_K_O_PROJ, 1, dg::gemm_residual(m->o, W.wo, T, qd, d, m->h, err, m->xchg, st));
     int *topk = m->topk + (size_t)L * m->Tmax * c.top_k;
     m->routing_rows[L] = T;
+    m->moe_input_rows = T;
+    m->moe_input_layer = L;
     int nl = 0;  // routing and scatter: one launch, or two when the routing grid exceeds the machine
     const dg::Fp8Experts fx{W.wgu8, W.kw, m->kx};
     KL(DG_K_ROUTE, nl,
@@ -616,6 +619,7 @@ int canvas_forward(dg_model *m) {
   // final norm kept to ~16 bits (hi + lo bf16), as the LM head's operand tiles
   KL(DG_K_RMSNORM, 1,
      dg::rmsnorm_rows(m->xn, m->h, m->final_norm, T, c.d_model, c.rms_eps, m->stream, m->xn_lo, true));
+  m->moe_input_rows = 0;  // xn now holds the final norm
   return DG_OK;
 }
 
@@ -1220,6 +1224,19 @@ int dg_read_routing(dg_model *m, int32_t layer, int32_t *ids, int32_t max_rows, 
     const int n = rows < max_rows ? rows : max_rows;
     CK(cudaMemcpyAsync(ids, m->topk + (size_t)layer * m->Tmax * m->cfg.top_k,
                        sizeof(int) * (size_t)n * m->cfg.top_k, cudaMemcpyDeviceToHost, m->stream));
+    SYNC(m);
+  }
+  return DG_OK;
+}
+
+int dg_read_moe_input(dg_model *m, uint16_t *rows, int32_t max_rows, int32_t *n_rows, int32_t *layer) {
+  CKR(check_model(m));
+  if (n_rows) *n_rows = m->moe_input_rows;
+  if (layer) *layer = m->moe_input_layer;
+  if (rows && m->moe_input_rows > 0) {
+    const int n = m->moe_input_rows < max_rows ? m->moe_input_rows : max_rows;
+    CK(cudaMemcpyAsync(rows, m->xn, sizeof(uint16_t) * (size_t)n * m->cfg.d_model, cudaMemcpyDeviceToHost,
+                       m->stream));
     SYNC(m);
   }
   return DG_OK;

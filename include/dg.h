@@ -273,6 +273,17 @@ int dg_read_kv(dg_model *m, int32_t layer, int32_t pos0, int32_t n, uint16_t *k_
  * where router logits are tied within rounding. */
 int dg_read_routing(dg_model *m, int32_t layer, int32_t *ids, int32_t max_rows, int32_t *n_rows);
 
+/* Expert input of the last MoE layer the last forward ran (the MoE RMSNorm's
+ * bf16 output rows, which the router and the experts read): rows (host,
+ * [rows][d_model] bf16 bits, up to max_rows rows), *n_rows = its rows,
+ * *layer = that layer.  After a prefill chunk that is the second-to-last
+ * layer (the last layer's MoE does not run: its output feeds no cached key);
+ * after a canvas forward there are none (*n_rows = 0: the final norm has
+ * replaced them).
+ * Lets a replay take the FP8 path's per-row quantization decisions on the
+ * same bf16 values as the kernels. */
+int dg_read_moe_input(dg_model *m, uint16_t *rows, int32_t max_rows, int32_t *n_rows, int32_t *layer);
+
 /* Page table (logical page -> physical page), host out, up to max_entries;
  * *n_pages = pages covering the prefix plus the current canvas. */
 int dg_read_page_table(dg_model *m, int32_t *table, int32_t max_entries, int32_t *n_pages);

@@ -162,15 +162,19 @@ def routing_margin(y, wr, forced):
     return np.take_along_axis(r, np.asarray(forced, np.int64), axis=1).min(axis=1) - kth, np.abs(r).max(axis=1)
 
 
-def expert_ffn(x, wg, wu, wd, fp8_gate_up=False):
+def expert_ffn(x, wg, wu, wd, fp8_gate_up=False, x_bf16=None):
     """SwiGLU expert on rows x [n, d].
 
     fp8_gate_up: the gate/up products take e4m3 operands (oracle/fp8.py):
     each weight row (output feature) and each input row, rounded to bf16 as
-    the decoder hands it over, scaled by its own power of two."""
+    the decoder hands it over, scaled by its own power of two.  x_bf16
+    (optional, [n, d] bf16 values): the input rows to quantize instead of
+    bf16(x) -- a replay passes the decoder's own rows so that both sides take
+    the integer quantization decisions on the same values."""
     wg, wu, wd = (np.asarray(w, np.float64) for w in (wg, wu, wd))
     if fp8_gate_up:
-        x = fp8.dequantize_rows(*fp8.quantize_rows(bf16_round(x)))
+        xb = bf16_round(x) if x_bf16 is None else np.asarray(x_bf16, np.float64)
+        x = fp8.dequantize_rows(*fp8.quantize_rows(xb))
         wg = fp8.dequantize_rows(*fp8.quantize_rows(wg))
         wu = fp8.dequantize_rows(*fp8.quantize_rows(wu))
     return (silu(x @ wg.T) * (x @ wu.T)) @ wd.T
@@ -184,25 +188,28 @@ def bf16_round(x):
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def moe_given_routing(y, ids, gates, W, fp8_gate_up=False):
+def moe_given_routing(y, ids, gates, W, fp8_gate_up=False, y_bf16=None):
     out = np.zeros_like(y)
     for e in np.unique(ids):
         tok, slot = np.nonzero(ids == e)
-        out[tok] += gates[tok, slot][:, None] * expert_ffn(y[tok], W["wg"][e], W["wu"][e], W["wd"][e], fp8_gate_up)
+        xb = None if y_bf16 is None else y_bf16[tok]
+        out[tok] += gates[tok, slot][:, None] * expert_ffn(y[tok], W["wg"][e], W["wu"][e], W["wd"][e],
+                                                           fp8_gate_up, xb)
     return out
 
 
-def moe(y, W, k, forced=None, rel_tol=None, fp8_gate_up=False):
+def moe(y, W, k, forced=None, rel_tol=None, fp8_gate_up=False, y_bf16=None):
     ids, gates, r = route(y, W["wr"], k, forced, rel_tol=rel_tol)
-    return moe_given_routing(y, ids, gates, W, fp8_gate_up), ids, gates, r
+    return moe_given_routing(y, ids, gates, W, fp8_gate_up, y_bf16), ids, gates, r
 
 
-def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=None, routing_rel_tol=None):
+def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=None, routing_rel_tol=None,
+          moe_input_bf16=None):
     """One decoder layer over new tokens h [T, d] at positions pos.
 
     prefix_k/v [S, Hkv, hd] are the cached (rotated) keys/values visible to
     every new token; forced_routing (optional [T, k]) and routing_rel_tol as
-    in route().
+    in route(); moe_input_bf16 (optional) as expert_ffn's x_bf16.
     Returns (h_out, k_new, v_new).
     """
     T = h.shape[0]
@@ -218,7 +225,7 @@ def block(h, pos, W, cfg, prefix_k, prefix_v, mode, trace=None, forced_routing=N
     o = attention(q, K, V, visibility(prefix_k.shape[0], T, mode))
     h = h + o.reshape(T, Hq * hd) @ np.asarray(W["wo"], np.float64).T
     n2 = rmsnorm(h, W["moe_norm"], cfg.rms_eps)
-    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing, routing_rel_tol, cfg.expert_fp8)
+    y, ids, gates, r = moe(n2, W, cfg.top_k, forced_routing, routing_rel_tol, cfg.expert_fp8, moe_input_bf16)
     if trace is not None:
         trace.append(dict(n=n, q=q, k=k, v=v, o=o, n2=n2, ids=ids, gates=gates, router=r, y=y))
     return h + y, k, v
