@@ -244,11 +244,13 @@ def decode_all(dgp, m, seed, scfg):
     return Ns, Cs
 
 
-# DRAM traffic / algorithmic bytes of the expert-FFN kernel, from one ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 128-expert MoE
-# layer shape of `--micro moe`; the decoder's launches touch fewer experts and
-# their traffic is this ratio times their algorithmic bytes.
-FFN_TRAFFIC_RATIO = 1.5642e9 / 1.5634e9
+# DRAM traffic / algorithmic bytes of the decoder's own expert-FFN launches:
+# dram__bytes_read.sum + dram__bytes_write.sum of all 30 launches of one eager
+# denoising step (ncu, 1 pass, `python bench.py --profile-step` with routing
+# and scatter unfused), over their algorithmic bytes from the same step's
+# experts touched (profiles/launch_list_full_decoder.md).  Below 1: the
+# weights stream once and part of the row, SwiGLU and output bytes stay in L2.
+FFN_TRAFFIC_RATIO = 7.958e9 / 8.705e9
 
 
 def expert_bytes(cfg, experts_per_launch, rows_per_launch):
@@ -369,7 +371,8 @@ def gpu_arm(args):
         traffic = args.traffic if args.traffic is not None else round(FFN_TRAFFIC_RATIO * per_launch[dom])
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
-                    "traffic_source": "ncu dram bytes of the 128-expert layer, scaled by experts touched",
+                    "traffic_source": ("ncu dram bytes / algorithmic bytes of the 30 expert-FFN launches of one "
+                                       "eager decoder step (0.914), times this launch's algorithmic bytes"),
                     "peak_source": f"{peak_src} hbm_gbs",
                     "algorithmic_bytes_per_launch": round(per_launch[dom]), "measured_in": measured_in}
 
@@ -741,6 +744,34 @@ def batched(dgp, stream):
             "note": "requests' steps summed; a batched forward serves every request's canvas"}
 
 
+def profile_step(args):
+    """--profile-step: the decoder of the value, its prompt encoded, then one
+    eager denoising step (every kernel of a step launched directly, none from
+    a graph) -- the command profilers capture; prints one short line."""
+    import torch
+    import discrete_diffusion_block_gb300 as dgp
+    from discrete_diffusion_block_gb300 import build, synth
+    torch.cuda.set_device(0)
+    build.build()
+    dgp.load()
+    stream = torch.cuda.Stream(device=torch.device("cuda", 0))
+    cfg = dgp.full_config(max_context=PROMPT + CANVASES * C, n_layers=args.layers)
+    m = dgp.dg_init_model(cfg, dgp.SamplerConfig(budget_N=BUDGET, adaptive=1), stream=stream)
+    dgp.dg_prefill(m, synth.prompt_ids(PROMPT, cfg.vocab, seed=1000))
+    torch.cuda.synchronize()
+    dgp.dg_denoise_step(m)
+    torch.cuda.synchronize()
+    import numpy as np
+    touched = [int(len(np.unique(dgp.dg_read_routing(m, L)))) for L in range(cfg.n_layers)]
+    per_expert = 3 * cfg.d_ff * cfg.d_model * 2
+    rows = C * cfg.top_k
+    fixed = rows * cfg.d_model * (2 + 4) + rows * cfg.d_ff * 2 * 2     # rows in, y out, SwiGLU out + in
+    print(json.dumps({"profile_step": "done", "layers": cfg.n_layers, "experts_touched": touched,
+                      "expert_ffn_algorithmic_bytes": [e * per_expert + fixed for e in touched]}), flush=True)
+    m.close()
+    return 0
+
+
 def micro(args):
     """--micro: the kernel micro-ops only, one JSON line per case."""
     import torch
@@ -774,7 +805,11 @@ def main():
                     help="decoder depth; fewer layers give a small case of the same kernels for ncu captures")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if measured for the current binaries")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="prefill + one eager denoising step of the decoder (for profiler captures)")
     args = ap.parse_args()
+    if args.profile_step:
+        return profile_step(args)
     if args.micro:
         return micro(args)
     if args.section:
