@@ -159,13 +159,19 @@ struct dg_model {
   dg::StepParams *dyn_dev = nullptr, *dyn_host = nullptr;  // per-step sampler words
 
   int alloc_count = 0;    // device allocations made by this model
-  int fail_alloc_at = 0;  // host-side fault injection: make allocation n (1-based) fail
+  // Host-side fault injection (DG_FAULT, read at dg_init_model; nothing is
+  // done to the GPU): allocation n (1-based) fails with DG_ENOMEM, kernel
+  // launch n fails with DG_ECUDA before it is made, or every KV capacity
+  // check reports a full pool (DG_ECAPACITY).
+  int fail_alloc_at = 0;
+  int launch_count = 0, fail_launch_at = 0;
+  bool fault_kvfull = false;
   template <class T>
   int alloc(T **p, size_t n) {
     void *v = nullptr;
     if (n == 0) n = 1;
     if (++alloc_count == fail_alloc_at)
-      return fail(DG_ENOMEM, "device allocation %d failed (injected by DG_FAULT_ALLOC)", alloc_count);
+      return fail(DG_ENOMEM, "device allocation %d failed (injected by DG_FAULT)", alloc_count);
     if (cudaMalloc(&v, n * sizeof(T)) != cudaSuccess) {
       cudaGetLastError();
       return fail(DG_ENOMEM, "cudaMalloc of %zu bytes failed", n * sizeof(T));
@@ -273,6 +279,8 @@ void prof_collect(dg_model *m) {
 // Launch `call` (one or more kernels of class `cls`) with profiling brackets.
 #define KL(cls, nk, call)                                                                 \
   do {                                                                                    \
+    if (m->fail_launch_at && ++m->launch_count == m->fail_launch_at)                      \
+      return fail(DG_ECUDA, "launch %d failed (injected by DG_FAULT=badcall)", m->launch_count); \
     cudaEvent_t a_ = prof_begin(m);                                                       \
     cudaError_t e_ = (call);                                                              \
     prof_end(m, (cls), (nk), a_);                                                         \
@@ -551,6 +559,7 @@ int sync_check(dg_model *m) {
 int check_prompt(dg_model *m, const int32_t *prompt, int32_t n) {
   const dg_config &c = m->cfg;
   if (n < 0 || (n > 0 && !prompt)) return fail(DG_EINVAL, "bad prompt");
+  if (m->fault_kvfull) return fail(DG_ECAPACITY, "KV pool full (injected by DG_FAULT=kvfull)");
   if (n + m->sc.canvas_len > c.max_context)
     return fail(DG_ECAPACITY, "prompt of %d tokens plus a canvas exceeds max_context %d", n,
                 c.max_context);
@@ -634,6 +643,7 @@ int begin_canvas(dg_model *m) {
   if (!m->prefilled) return fail(DG_ESTATE, "dg_prefill must come first");
   if (m->canvas_done) return fail(DG_ESTATE, "canvas finished: call dg_commit_canvas");
   if (!m->canvas_active) {
+    if (m->fault_kvfull) return fail(DG_ECAPACITY, "KV pool full (injected by DG_FAULT=kvfull)");
     for (int b = 0; b < m->B; ++b)
       if (m->prefix_lens[b] + m->sc.canvas_len > m->cfg.max_context)
         return fail(DG_ECAPACITY, "no room for another canvas (prefix %d, max_context %d)",
@@ -892,6 +902,11 @@ int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg, const voi
   m->prompt_lens.assign(m->B, 0);
   m->prefix_lens.assign(m->B, 0);
   if (const char *f = getenv("DG_FAULT_ALLOC")) m->fail_alloc_at = atoi(f);
+  if (const char *f = getenv("DG_FAULT")) {  // alloc:n | badcall:n | kvfull
+    if (!strncmp(f, "alloc:", 6)) m->fail_alloc_at = atoi(f + 6);
+    else if (!strncmp(f, "badcall:", 8)) m->fail_launch_at = atoi(f + 8);
+    else if (!strcmp(f, "kvfull")) m->fault_kvfull = true;
+  }
   if (cuda_stream) {
     m->stream = (cudaStream_t)cuda_stream;
   } else {

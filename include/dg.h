@@ -143,7 +143,12 @@ const char *dg_last_error(void);
  * `cuda_stream` (a cudaStream_t) orders all of the model's work; NULL
  * creates a private non-blocking stream.  On success *out owns everything
  * but borrowed weights until dg_free_model.  DG_ENOMEM if a device
- * allocation fails (everything allocated so far is released). */
+ * allocation fails (everything allocated so far is released).
+ * Host-side fault injection, read here from the environment (nothing is
+ * done to the GPU): DG_FAULT=alloc:n (or DG_FAULT_ALLOC=n) -- the model's
+ * n-th device allocation fails with DG_ENOMEM; DG_FAULT=badcall:n -- its
+ * n-th kernel launch fails with DG_ECUDA before it is made; DG_FAULT=kvfull --
+ * every KV capacity check fails with DG_ECAPACITY. */
 int dg_init_model(const dg_config *cfg, const dg_sampler_config *scfg,
                   const void *const *weights, void *cuda_stream, dg_model **out);
 void dg_free_model(dg_model *m);

@@ -297,6 +297,30 @@ def test_injected_allocation_failure_returns_enomem_and_releases(monkeypatch):
     m.close()
 
 
+def test_injected_kv_full_and_failed_launch_return_their_codes(monkeypatch):
+    # DG_FAULT=kvfull: every KV capacity check reports a full pool;
+    # DG_FAULT=badcall:n: the n-th kernel launch fails before it is made.
+    # Host-side only: nothing is done to the GPU.  The model can be freed and
+    # a model without the fault runs.
+    monkeypatch.setenv("DG_FAULT", "kvfull")
+    m = new_model()
+    with pytest.raises(dgp.DgError) as e:
+        dgp.dg_prefill(m, synth.prompt_ids(P, 1024))
+    assert e.value.code == dgp.DG_ECAPACITY and "injected" in str(e.value)
+    m.close()
+    monkeypatch.setenv("DG_FAULT", "badcall:3")
+    m = new_model()
+    with pytest.raises(dgp.DgError) as e:
+        dgp.dg_prefill(m, synth.prompt_ids(P, 1024))
+    assert e.value.code == dgp.DG_ECUDA and "injected" in str(e.value)
+    m.close()
+    monkeypatch.delenv("DG_FAULT")
+    m = new_model()
+    dgp.dg_prefill(m, synth.prompt_ids(P, 1024))
+    dgp.dg_denoise_step(m)
+    m.close()
+
+
 def test_annealed_re_noise_follows_the_oracle_schedule(oracle_weights):
     # Temperature annealing: step n's re-noise samples are drawn at tau_n
     # (linear from 1.5 to 0.5 over the budget); teacher-forced against the
