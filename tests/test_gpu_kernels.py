@@ -193,7 +193,12 @@ def test_sampler_rule_branches_over_scripted_steps():
 
 # ---- LM head fused with the vocab reduction -------------------------------------
 
-@pytest.mark.parametrize("rows,d,V,sample", [(256, 256, 1024, None), (256, 2816, 262144, [0, 63, 64, 130, 255])])
+@pytest.mark.parametrize("rows,d,V,sample", [
+    (256, 256, 1024, None),
+    (200, 256, 1024, None),                  # a last row block of 72 rows
+    (384, 320, 2048, None),                  # three row blocks sharing each vocab tile, five k-steps
+    (512, 256, 4096, None),                  # four row blocks
+    (256, 2816, 262144, [0, 63, 64, 130, 255])])
 def test_lm_head_partials_against_fp64_logits(rows, d, V, sample):
     xf, xt = synth.normal_bf16((rows, d), seed=2)
     xn = tiles_dev(xt)
