@@ -91,10 +91,11 @@ constexpr int kAttnSlotHalfBytes = 64 * 128;  // 64 keys x 64 hd bf16 (one 8 KB 
 // 3-slot K ring and a 3-slot V ring of 128-key tiles [HB][128 keys][64] (the
 // P tiles live in tensor memory, which leaves room for the third slots: the
 // key loop is bound by copy latency times ring depth); the page list;
-// barriers.  After the key loop the K ring holds the fp32 output rows
-// [128][HD] on their way out; with split keys the V ring holds the rows'
-// softmax states and merge weights (first 8 KB) and receives the peers'
-// partial rows (from 8 KB on).
+// barriers.  After the key loop the K ring holds the bf16 output rows
+// [128][HD] on their way out (unnormalised partial rows of a split block);
+// with split keys the V ring holds the rows' softmax states and the merge
+// weights (first 8 KB), and the owners of the rows read the peers' staged
+// rows and states from the peers' shared memory.
 template <int HD>
 struct AttnSmem {
   static constexpr int HB = HD / 64;                       // 64-wide hd blocks
@@ -103,19 +104,32 @@ struct AttnSmem {
   static constexpr size_t q = 0;
   static constexpr size_t kring = q + tile;
   static constexpr size_t vring = kring + kK * tile;
-  static constexpr size_t recv = vring + 8192;             // split merge: the peers' partial rows
   static constexpr size_t pages = vring + kV * tile;       // physical page per 64-key half (ints)
   static constexpr size_t xch = pages + kAttnPages * 4;    // [2 halves][128 rows] fp32: the softmax pairs' exchange
   static constexpr size_t bars = xch + 2 * 128 * 4;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, p_empty[2], o_full,
-  // r_full (peer partials received)
-  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 4 + 1;
+  // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], s_empty[2], p_full, p_empty[2], o_full
+  static constexpr int n_bars = 1 + 2 * kK + 2 * kV + 4 + 4;
   static constexpr size_t bytes = bars + n_bars * 8 + 16 + 1024;
-  static_assert((size_t)128 * HD * 4 <= (kK + kV) * tile, "output staging fits the K and V rings");
+  static_assert((size_t)128 * HD * 2 <= kK * tile, "output staging fits the K ring");
 };
 
 // One 64-key half of a K or V operand tile, all zero (keys past the end).
 __device__ __align__(128) unsigned char g_zero_half[kAttnSlotHalfBytes];
+
+__device__ __forceinline__ uint4 ld_cluster_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ void attn_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(b)) : "memory");
@@ -186,8 +200,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t *k_full = q_full + 1, *k_empty = k_full + KK;
   uint64_t *v_full = k_empty + KK, *v_empty = v_full + KV;
   uint64_t *s_full = v_empty + KV, *s_empty = s_full + 2;
-  uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1, *o_full = p_empty + 2, *r_full = o_full + 1;
-  uint32_t *tmem_slot = (uint32_t *)(r_full + 1);
+  uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1, *o_full = p_empty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(o_full + 1);
   volatile int *abort = (volatile int *)(tmem_slot + 1);
   int *pages = (int *)(base + S::pages);
   auto k_tile = [&](int slot) { return base + S::kring + (size_t)slot * S::tile; };
@@ -236,7 +250,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(p_empty, 1);
     tc::mbar_init(p_empty + 1, 1);
     tc::mbar_init(o_full, 1);
-    tc::mbar_init(r_full, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -497,7 +510,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::fence_after();
     }
     const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-    float *orow = (float *)(base + S::kring) + (size_t)row * HD;  // the K and V rings are idle now
+    uint4 *orow = (uint4 *)(base + S::kring) + (size_t)row * (HD / 8);  // the K ring is idle now
 #pragma unroll 1
     for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
       uint32_t v[32];
@@ -510,10 +523,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       const float sc = p.out ? inv : 1.0f;  // split blocks keep the unnormalised sum
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {  // float4 slot rotated by row: conflict-free
-        const int q = ((32 * c + j) >> 2) ^ (row & 7);
-        *(float4 *)(orow + 4 * q) = make_float4(__uint_as_float(v[j]) * sc, __uint_as_float(v[j + 1]) * sc,
-                                                __uint_as_float(v[j + 2]) * sc, __uint_as_float(v[j + 3]) * sc);
+      for (int j = 0; j < 32; j += 8) {  // bf16 chunk of 8 columns, slot rotated by row: conflict-free
+        const int q = ((32 * c + j) >> 3) ^ (row & 7);
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(v[j]) * sc, __uint_as_float(v[j + 1]) * sc);
+        w.y = pack_bf16(__uint_as_float(v[j + 2]) * sc, __uint_as_float(v[j + 3]) * sc);
+        w.z = pack_bf16(__uint_as_float(v[j + 4]) * sc, __uint_as_float(v[j + 5]) * sc);
+        w.w = pack_bf16(__uint_as_float(v[j + 6]) * sc, __uint_as_float(v[j + 7]) * sc);
+        orow[q] = w;
       }
     }
     if (!p.out && half == 0) ((float2 *)(base + S::vring))[row] = make_float2(m, lt);  // split blocks: the row's softmax state
@@ -527,58 +544,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (p.out) {
     // Rows out of shared memory, one warp per row, lanes along hd.
-    const float *stage = (const float *)(base + S::kring);
+    const uint4 *stage = (const uint4 *)(base + S::kring);
     for (int rr = warp; rr < 128; rr += kAttnThreads / 32) {
       const int r = r_cta + rr;
       if (r >= rows_total) break;
       const int t = tok0 + r / p.G, h = g * p.G + r % p.G;
-      for (int c4 = lane; c4 < HD / 4; c4 += 32) {
-        const float4 v = *(const float4 *)(stage + (size_t)rr * HD + 4 * (c4 ^ (rr & 7)));
-        uint2 w;
-        w.x = pack_bf16(v.x, v.y);
-        w.y = pack_bf16(v.z, v.w);
-        *(uint2 *)(p.out + (p.out_tiles ? tiled_index(p.n_req * p.n_new, p.Hq * HD, t, h * HD + 4 * c4)
-                                        : ((size_t)t * p.Hq + h) * HD + 4 * c4)) = w;
-      }
+      for (int c8 = lane; c8 < HD / 8; c8 += 32)
+        *(uint4 *)(p.out + (p.out_tiles ? tiled_index(p.n_req * p.n_new, p.Hq * HD, t, h * HD + 8 * c8)
+                                        : ((size_t)t * p.Hq + h) * HD + 8 * c8)) = stage[(size_t)rr * (HD / 8) + (c8 ^ (rr & 7))];
     }
     return;
   }
   // Split-KV merge inside the cluster of this query tile's blocks.  Block z
-  // owns rows [z n, z n + n), n = ceil(128 / NS) rounded up to even (16-byte
-  // aligned softmax-state rows); every block sends its staged
-  // output rows and softmax states of those rows to their owner with bulk
-  // shared-to-shared copies (into the owner's idle V ring past its first
-  // 8 KB), and the owner merges the NS partials (weights 2^(m_s - m*)) in
-  // shared memory.
+  // owns rows [z n, z n + n), n = ceil(128 / NS).  After a cluster barrier
+  // (every block has staged its unnormalised output rows and their softmax
+  // states) the owner reads the NS partials of its rows straight from the
+  // blocks' shared memory (distributed shared-memory loads, all of a column's
+  // in flight) and merges them with weights 2^(m_s - m*); a second barrier
+  // keeps each block's staged rows until its peers have read them.
   const int NS = p.splits;
-  const int n_own = (((128 + NS - 1) / NS) + 1) & ~1;
-  const uint32_t o_slot = (uint32_t)n_own * HD * 4, ml_slot = (uint32_t)n_own * 8;
-  const uint32_t slot_bytes = o_slot + ml_slot;
-  const float *stage = (const float *)(base + S::kring);
-  const float2 *ml_stage = (const float2 *)(base + S::vring);
-  unsigned char *recv = base + S::recv;           // (NS - 1) slots: O rows, then (m, l) pairs
-  uint64_t *rbar = r_full;
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the copies read the staged rows
+  const int n_own = (128 + NS - 1) / NS;
+  const uint32_t stage_sa = tc::smem_u32(base + S::kring), ml_sa = tc::smem_u32(base + S::vring);
   __syncwarp();
-  tc::cluster_sync();  // every block staged; every block's V ring is idle
+  tc::cluster_sync();  // every block staged its rows and states
   const int z = split, r0 = z * n_own, n_mine = max(0, min(128, r0 + n_own) - r0);
-  if (threadIdx.x == 0) {
-    tc::mbar_expect_tx(rbar, (uint32_t)(NS - 1) * ((uint32_t)n_mine * HD * 4 + (uint32_t)((n_mine + 1) & ~1) * 8));
-    for (int q = 1; q < NS; ++q) {
-      const int j = (z + q) % NS, jr0 = j * n_own, nj = max(0, min(128, jr0 + n_own) - jr0);
-      if (nj == 0) continue;
-      const int slot = z < j ? z : z - 1;
-      const uint32_t dst = tc::cluster_addr(tc::smem_u32(recv) + slot * slot_bytes, (uint32_t)j);
-      const uint32_t bar = tc::cluster_addr(tc::smem_u32(rbar), (uint32_t)j);
-      tc::bulk_copy_to_peer(dst, tc::smem_u32(stage + (size_t)jr0 * HD), (uint32_t)nj * HD * 4, bar);
-      tc::bulk_copy_to_peer(dst + o_slot, tc::smem_u32(ml_stage + jr0), (uint32_t)((nj + 1) & ~1) * 8, bar);
-    }
-  }
-  if (n_mine > 0) tc::mbar_wait(rbar, 0, p.err, 41, abort);
   // Once per owned row: the partials' weights 2^(m_s - m*) (0 for a split
-  // that saw no key), 1 / L and the output row (token, head), into the idle
-  // V ring past the staged softmax states; then every thread merges float4
-  // columns with them.
+  // that saw no key), 1 / L and the output row (token, head), into the V ring
+  // past the staged softmax states; then every thread merges float4 columns
+  // with them.
   const float NEG = __int_as_float(0xff800000);
   float *wtab = (float *)(base + S::vring + 2048);  // [n_own][8] weights, then [n_own] 1 / L
   int *otab = (int *)(wtab + 9 * n_own);            // [n_own] (token << 12) | head, -1 past the rows
@@ -586,16 +579,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int rr = r0 + lr, r = r_cta + rr;
     float2 ml[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (q >= NS) {
-        ml[q] = make_float2(NEG, 0.0f);
-      } else if (q == z) {
-        ml[q] = ml_stage[rr];
-      } else {
-        const unsigned char *sl = recv + (size_t)(q < z ? q : q - 1) * slot_bytes;
-        ml[q] = ((const float2 *)(sl + o_slot))[lr];
-      }
-    }
+    for (int q = 0; q < 8; ++q)
+      ml[q] = q < NS ? ld_cluster_f2(tc::cluster_addr(ml_sa + 8u * (uint32_t)rr, (uint32_t)q)) : make_float2(NEG, 0.0f);
     float mx = NEG;
 #pragma unroll
     for (int q = 0; q < 8; ++q) mx = fmaxf(mx, ml[q].x);
@@ -613,33 +598,59 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     otab[lr] = r < rows_total ? ((tok0 + r / p.G) << 12) | (g * p.G + r % p.G) : -1;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < n_mine * (HD / 4); idx += kAttnThreads) {
-    const int lr = idx / (HD / 4), c4 = idx - lr * (HD / 4), rr = r0 + lr;
-    const int th = otab[lr];
-    if (th < 0) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // Two 8-column chunks per thread at a time, the loads of both in flight
+  // before the sums; partials summed in split order.
+  const int n_items = n_mine * (HD / 8);
+  for (int i0 = threadIdx.x; i0 < n_items; i0 += 2 * kAttnThreads) {
+    float w[2][8];
+    uint4 o[2][8];
+    int th[2], c8s[2], lrs[2];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float w = q < NS ? wtab[lr * 8 + q] : 0.0f;
-      if (w == 0.0f) continue;
-      const float *rows = q == z ? stage + (size_t)rr * HD
-                                 : (const float *)(recv + (size_t)(q < z ? q : q - 1) * slot_bytes) + (size_t)lr * HD;
-      const float4 o = *(const float4 *)(rows + 4 * (c4 ^ (rr & 7)));  // the staging order travels with the rows
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
+    for (int u = 0; u < 2; ++u) {
+      const int idx = i0 + u * kAttnThreads;
+      th[u] = -1;
+      if (idx >= n_items) continue;
+      const int lr = idx / (HD / 8), c8 = idx - lr * (HD / 8), rr = r0 + lr;
+      th[u] = otab[lr];
+      c8s[u] = c8;
+      lrs[u] = lr;
+      // the staging order travels with the rows: chunk c8 of row rr sits at slot c8 ^ (rr & 7)
+      const uint32_t off = stage_sa + 16u * (uint32_t)(rr * (HD / 8) + (c8 ^ (rr & 7)));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        w[u][q] = (q < NS && th[u] >= 0) ? wtab[lr * 8 + q] : 0.0f;
+        if (w[u][q] != 0.0f) o[u][q] = ld_cluster_u4(tc::cluster_addr(off, (uint32_t)q));
+      }
     }
-    const float invL = wtab[8 * n_own + lr];
-    const int t = th >> 12, h = th & 4095;
-    uint2 v;
-    v.x = pack_bf16(acc.x * invL, acc.y * invL);
-    v.y = pack_bf16(acc.z * invL, acc.w * invL);
-    *(uint2 *)(p.final_out + (p.out_tiles ? tiled_index(p.n_req * p.n_new, p.Hq * HD, t, h * HD + 4 * c4)
-                                          : ((size_t)t * p.Hq + h) * HD + 4 * c4)) = v;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (th[u] < 0) continue;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (w[u][q] == 0.0f) continue;
+        const uint32_t wd[4] = {o[u][q].x, o[u][q].y, o[u][q].z, o[u][q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] += w[u][q] * __uint_as_float(wd[e] << 16);
+          acc[2 * e + 1] += w[u][q] * __uint_as_float(wd[e] & 0xffff0000u);
+        }
+      }
+      const float invL = wtab[8 * n_own + lrs[u]];
+      const int t = th[u] >> 12, h = th[u] & 4095, c8 = c8s[u];
+      uint4 v;
+      v.x = pack_bf16(acc[0] * invL, acc[1] * invL);
+      v.y = pack_bf16(acc[2] * invL, acc[3] * invL);
+      v.z = pack_bf16(acc[4] * invL, acc[5] * invL);
+      v.w = pack_bf16(acc[6] * invL, acc[7] * invL);
+      *(uint4 *)(p.final_out + (p.out_tiles ? tiled_index(p.n_req * p.n_new, p.Hq * HD, t, h * HD + 8 * c8)
+                                            : ((size_t)t * p.Hq + h) * HD + 8 * c8)) = v;
+    }
   }
   __syncwarp();
-  tc::cluster_sync();  // every copy out of this block's shared memory has landed
+  tc::cluster_sync();  // the peers have read this block's staged rows and states
 }
 
 struct SplitPlan {
@@ -836,13 +847,6 @@ cudaError_t attention(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, con
     const uint32_t box[4] = {64, (uint32_t)G, 1, (uint32_t)(128 / G)};
     cudaError_t e = attn_map(&tq, q, 4, dims, strides, box);
     if (e != cudaSuccess) return e;
-  }
-  if (pl.splits > 1) {  // the peers' partial rows fit the V ring past its first 8 KB
-    const size_t n_own = (size_t)(((128 + pl.splits - 1) / pl.splits) + 1) & ~(size_t)1;
-    const size_t need = (size_t)(pl.splits - 1) * (n_own * s.hd * 4 + n_own * 8);
-    const size_t room = (s.hd == 128 ? AttnSmem<128>::pages - AttnSmem<128>::recv
-                                     : AttnSmem<64>::pages - AttnSmem<64>::recv);
-    if (need > room) return cudaErrorInvalidValue;
   }
   const dim3 grid(ceil_div(rows_total, kRowsPerBlock), s.Hkv, pl.splits * s.n_req);
   return s.hd == 128 ? launch_attn<128>(tq, p, grid, st) : launch_attn<64>(tq, p, grid, st);
