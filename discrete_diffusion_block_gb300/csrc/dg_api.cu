@@ -101,7 +101,7 @@ struct dg_model {
   bf16 *xn = nullptr, *xn_lo = nullptr, *q = nullptr, *o = nullptr, *act = nullptr,
        *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
-  int *route_bar = nullptr;                  // device, 2 ints: grid barrier of the fused routing + scatter
+  int *route_bar = nullptr;                  // device, kGridBarInts: grid barrier of the fused routing + scatter
   int *kx = nullptr;                         // expert_fp8: scale exponents of the expert input rows
   int moe_input_rows = 0, moe_input_layer = -1;  // the rows xn holds: the last MoE input
   float *gates = nullptr, *y = nullptr;
@@ -462,8 +462,8 @@ int alloc_model(dg_model *m, const void *const *weights) {
   CKR(m->alloc(&m->xq, (size_t)T * d));
   CKR(m->alloc(&m->xn_lo, (size_t)BC * d));
   CKR(m->alloc(&m->moe_stats, 2));
-  CKR(m->alloc(&m->route_bar, 2));
-  CK(cudaMemset(m->route_bar, 0, 2 * sizeof(int)));
+  CKR(m->alloc(&m->route_bar, dg::kGridBarInts));
+  CK(cudaMemset(m->route_bar, 0, dg::kGridBarInts * sizeof(int)));
   CKR(m->alloc(&m->q, (size_t)T * qd));
   CKR(m->alloc(&m->o, (size_t)T * qd));
   CKR(m->alloc(&m->xchg, dg::gemm_xchg_bytes() / sizeof(float)));
@@ -1490,7 +1490,7 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.act = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, F) * 2);
   w.x_tiles = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, d) * 2);
   w.y_rows = (float *)take((size_t)T * k * d * 4);
-  w.bar = (int *)take(2 * 4);
+  w.bar = (int *)take(dg::kGridBarInts * 4);
   w.bytes = off;
   return w;
 }
@@ -1518,7 +1518,7 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
   cudaStream_t st = (cudaStream_t)stream;
   int *status = nullptr;
   CKR(op_status_ptr(&status));
-  CK(cudaMemsetAsync(w.bar, 0, 2 * sizeof(int), st));
+  CK(cudaMemsetAsync(w.bar, 0, dg::kGridBarInts * sizeof(int), st));
   CK(dg::moe_route_scatter(nullptr, nullptr, 0.0f, const_cast<bf16 *>((const bf16 *)xn), (const bf16 *)w_router, T,
                            d, n_experts, top_k, expert_ids, gates, w.slot_row, w.gcount, w.x_tiles, w.offs, w.work,
                            w.n_work, w.max_work, w.bar, status, st));

@@ -56,6 +56,11 @@ cudaError_t moe_norm_route(const float *h, const float *gain, float eps, bf16 *x
                            cudaStream_t st);
 cudaError_t moe_route(const bf16 *xn, const bf16 *wr, int T, int d, int E, int k, int *ids, float *gates,
                       int *rank, int *gcount, int *err, cudaStream_t st);
+// A grid-wide barrier's words: the arrival count at [0] and the generation
+// at [32], on its own 128-byte line (the arrivals' atomics do not share a
+// line with the CTAs polling the generation).  Zeroed before first use.
+constexpr int kGridBarInts = 64;
+
 struct Fp8Experts;
 cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *slot_row, int T, int d, int E,
                         int k, int tile_rows, bf16 *x_tiles, int *offs, int *work, int *n_work, int max_work,

@@ -118,12 +118,30 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
   int *soffs = tab + n, *stoff = soffs + E, *s_ex = stoff + E, *s_rk = s_ex + a.per;
   const int TK = a.T * a.k;
   const int p0 = blk * a.per, p1 = min(TK, p0 + a.per);
-  // the block's pairs and the group counts: all loads in flight together
-  for (int i = threadIdx.x; i < p1 - p0; i += kScatThreads) {
-    s_ex[i] = a.ids[p0 + i];
-    s_rk[i] = a.slot_row[p0 + i];
+  // the block's pairs and the group counts: every load of a round in
+  // flight before any store (each load waits an L2 round trip)
+  constexpr int kLoadU = 8;
+  for (int i0 = 0; i0 < max(p1 - p0, n); i0 += kLoadU * kScatThreads) {
+    int ex[kLoadU], rk[kLoadU], gc[kLoadU];
+#pragma unroll
+    for (int u = 0; u < kLoadU; ++u) {
+      const int i = i0 + (int)threadIdx.x + u * kScatThreads;
+      if (i < p1 - p0) {
+        ex[u] = a.ids[p0 + i];
+        rk[u] = a.slot_row[p0 + i];
+      }
+      if (i < n) gc[u] = a.gcount[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadU; ++u) {
+      const int i = i0 + (int)threadIdx.x + u * kScatThreads;
+      if (i < p1 - p0) {
+        s_ex[i] = ex[u];
+        s_rk[i] = rk[u];
+      }
+      if (i < n) tab[i] = gc[u];
+    }
   }
-  for (int i = threadIdx.x; i < n; i += kScatThreads) tab[i] = a.gcount[i];
   __syncwarp();
   __syncthreads();
   const int e = threadIdx.x;  // E <= kScatThreads
@@ -314,7 +332,7 @@ struct RouteArgs {
   int *rank;           // [T*k] rank of each pair among its group's pairs of the same expert
   int *gcount;         // [ceil(T/32)][E] pairs per (token group, expert)
   int *err;
-  // fused scatter: after a grid-wide barrier (bar: count, generation), every
+  // fused scatter: after a grid-wide barrier (bar: kGridBarInts words), every
   // CTA runs its share of the scatter (sc, with sc.per pairs per CTA)
   int fuse;
   int grid;  // fused: CTAs of the launch
@@ -364,6 +382,18 @@ __device__ __forceinline__ int ld_acquire_s32(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Arrival with release at gpu scope: the writes this thread has observed
+// (the CTA's, through the preceding CTA barrier) are visible before the count.
+__device__ __forceinline__ int atom_add_release_s32(int *p, int v) {
+  int old;
+  asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_release_s32(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
@@ -443,14 +473,15 @@ __device__ __forceinline__ void fused_scatter_tail(const RouteArgs &a, unsigned 
   __syncthreads();
   __shared__ int passed;
   if (threadIdx.x == 0) {
-    int *gen = a.bar + 1;
+    int *gen = a.bar + 32;
     const int g0 = ld_acquire_s32(gen);
-    __threadfence();  // this CTA's counts and ranks before its arrival
     passed = 1;
-    if (atomicAdd(a.bar, 1) == (int)gridDim.x - 1) {
-      atomicExch(a.bar, 0);
-      __threadfence();
-      atomicExch(gen, g0 + 1);
+    if (atom_add_release_s32(a.bar, 1) == (int)gridDim.x - 1) {  // releases this CTA's counts and ranks
+      // the last arrival: every CTA's writes are visible to it (the arrivals
+      // released them); reset the count, then release the generation
+      asm volatile("fence.acq_rel.gpu;\n" ::: "memory");
+      *(volatile int *)a.bar = 0;
+      st_release_s32(gen, g0 + 1);
     } else {
       const long long c0 = clock64();
       while (ld_acquire_s32(gen) == g0) {
@@ -461,7 +492,8 @@ __device__ __forceinline__ void fused_scatter_tail(const RouteArgs &a, unsigned 
         }
       }
     }
-    __threadfence();
+    // acquired: the generation by ld.acquire, or (the last arrival) by the
+    // fence after its count; the CTA barrier below passes it to the CTA
   }
   __syncthreads();
   pdl_trigger();
