@@ -361,9 +361,11 @@ cudaError_t gemm_qkv(const bf16 *x_tiles, const bf16 *wqkv, int T, int d, const 
   if (o.hd / 2 > EpiQkv::kMaxHalf || 128 % o.hd || d % 64) return cudaErrorInvalidValue;
   EpiQkv epi{o};
   const TcArgs g = targs(M, T, d, wqkv, x_tiles, err, xchg);
-  const int units = ceil_div(M, 128) * ceil_div(T, tc::kSkBN), kt = d / tc::kBK;
-  if (kt >= 4) return launch_tc_sk<4>(g, epi, plain_clusters(units, 4), st);
-  return launch_tc_sk<1>(g, epi, plain_clusters(units, 1), st);
+  const int units = ceil_div(M, 128) * ceil_div(T, tc::kSkBN);
+  // a canvas step (32 units at the full width) splits K four ways; a prompt
+  // chunk or a lockstep batch has units enough for every SM unsplit
+  const int split = pick_split(units, d / tc::kBK);
+  return launch_split(g, epi, plain_clusters(units, split), split, st);
 }
 
 cudaError_t gemm_residual(const bf16 *act_tiles, const bf16 *w, int T, int K, int N, float *h, int *err,
