@@ -63,6 +63,12 @@ constexpr int kScatThreads = 256;
 __host__ __device__ inline size_t scatter_smem_ints(int ng, int E, int per) { return (size_t)ng * E + 2 * E + 2 * (size_t)per; }
 // Bytes of the table above, rounded up to 16 (the staged rows follow it).
 __host__ __device__ inline size_t scatter_tab_bytes(int ng, int E, int per) { return (scatter_smem_ints(ng, E, per) * 4 + 15) & ~(size_t)15; }
+// Staging for n_tok token rows of width d: the bf16 rows, and with fp8 their
+// e4m3 codes (16-byte aligned) and scale exponents.
+__host__ __device__ inline size_t scatter_stage_bytes(int n_tok, int d, int fp8) {
+  const size_t rows = (size_t)n_tok * d * 2;
+  return fp8 ? rows + (((size_t)n_tok * d + 15) & ~(size_t)15) + (size_t)n_tok * 4 : rows;
+}
 
 struct ScatArgs {
   const bf16 *xn;
@@ -189,7 +195,7 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, vec = a.d / 8, KT = a.d / 64;
   constexpr int NW = kScatThreads / 32;
   const int t_lo = p0 / a.k, n_tok = p1 > p0 ? (p1 - 1) / a.k - t_lo + 1 : 0;
-  if (stage && (size_t)n_tok * a.d * 2 <= stage_bytes) {
+  if (stage && scatter_stage_bytes(n_tok, a.d, a.fp8) <= stage_bytes) {
     const uint4 *src = (const uint4 *)(a.xn + (size_t)t_lo * a.d);  // rows t_lo .. t_hi are contiguous
     uint4 *st4 = (uint4 *)stage;
     const int n4 = n_tok * vec;
@@ -208,15 +214,15 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
     }
     __syncthreads();
     if (a.fp8) {
-      // One warp per pair: the row's scale exponent from its maximum, then
-      // 16 e4m3 elements per lane and step into row r of the item's e4m3
-      // tiles (128 elements a k-tile; chunk j at position j ^ (r % 8)).
-      for (int p = p0 + warp; p < p1; p += NW) {
-        const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
-        const int within = tab[g * E + ex] + s_rk[p - p0];
-        if (lane == 0) a.slot_row[p] = soffs[ex] + within;
-        const int item = stoff[ex] + within / a.tile_rows, rr = within % a.tile_rows;
-        const uint4 *row = st4 + (size_t)(t - t_lo) * vec;
+      // Each token's row is quantized once (one warp per token): its scale
+      // exponent from the row maximum, then its e4m3 codes, in column order,
+      // into shared memory after the staged rows.  One warp per pair then
+      // copies its token's codes into row r of its item's e4m3 tiles (128
+      // elements a k-tile; chunk j at position j ^ (r % 8)).
+      unsigned char *q8 = stage + (size_t)n_tok * a.d * 2;
+      int *texp = (int *)(q8 + (((size_t)n_tok * a.d + 15) & ~(size_t)15));
+      for (int tt = warp; tt < n_tok; tt += NW) {
+        const uint4 *row = st4 + (size_t)tt * vec;
         float amax = 0.0f;
         for (int c = lane; c < vec; c += 32) {
           const uint4 v = row[c];
@@ -230,7 +236,7 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         const int kexp = e4m3_scale_exp(amax);
-        unsigned char *dst8 = (unsigned char *)a.x_tiles + (size_t)item * (a.d / 128) * 16384 + (size_t)rr * 128;
+        uint4 *dst = (uint4 *)(q8 + (size_t)tt * a.d);
         for (int j = lane; j < a.d / 16; j += 32) {
           uint4 v[2] = {row[2 * j], row[2 * j + 1]};
           const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)v;
@@ -241,10 +247,23 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
             w[i] = cvt_e4m3x2(ldexpf(x0.x, -kexp), ldexpf(x0.y, -kexp)) |
                    (cvt_e4m3x2(ldexpf(x1.x, -kexp), ldexpf(x1.y, -kexp)) << 16);
           }
-          const int kt = j >> 3, ch = j & 7;
-          *(uint4 *)(dst8 + (size_t)kt * 16384 + ((ch ^ (rr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        if (lane == 0) a.kx[soffs[ex] + within] = kexp;
+        if (lane == 0) texp[tt] = kexp;
+      }
+      __syncthreads();
+      for (int p = p0 + warp; p < p1; p += NW) {
+        const int ex = s_ex[p - p0], t = p / a.k, g = t / kRouteTok;
+        const int within = tab[g * E + ex] + s_rk[p - p0];
+        if (lane == 0) a.slot_row[p] = soffs[ex] + within;
+        const int item = stoff[ex] + within / a.tile_rows, rr = within % a.tile_rows;
+        const uint4 *src = (const uint4 *)(q8 + (size_t)(t - t_lo) * a.d);
+        unsigned char *dst8 = (unsigned char *)a.x_tiles + (size_t)item * (a.d / 128) * 16384 + (size_t)rr * 128;
+        for (int j = lane; j < a.d / 16; j += 32) {
+          const int kt = j >> 3, ch = j & 7;
+          *(uint4 *)(dst8 + (size_t)kt * 16384 + ((ch ^ (rr & 7)) << 4)) = src[j];
+        }
+        if (lane == 0) a.kx[soffs[ex] + within] = texp[t - t_lo];
       }
       return;
     }
@@ -965,6 +984,9 @@ cudaError_t route_common(bool norm, const float *h, const float *gain, float eps
     const size_t tab = scatter_tab_bytes(a.sc.ng, E, a.sc.per), usable = full.bytes - 1024;
     if (tab > usable) return cudaErrorInvalidValue;
     a.sc.stage_bytes = (int)(usable - tab);
+    // e4m3 rows are written from the staged rows only: without room, two launches
+    if (a.sc.fp8 && scatter_stage_bytes(a.sc.per / k + 2, d, 1) > (size_t)a.sc.stage_bytes)
+      return cudaErrorCooperativeLaunchTooLarge;
   }
   CUtensorMap tx{};  // the norm path writes the B operand itself
   if (norm) return launch_route<true>(tx, a, st);
@@ -1048,7 +1070,7 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
   const size_t tab = scatter_tab_bytes(a.ng, E, a.per);
   if (tab > 200 * 1024) return cudaErrorInvalidValue;
   // room for the block's token rows (at most per / k + 2 of them), if it fits
-  const size_t stage = (size_t)(a.per / k + 2) * d * 2;
+  const size_t stage = scatter_stage_bytes(a.per / k + 2, d, a.fp8);
   a.stage_bytes = tab + stage <= 200 * 1024 ? (int)stage : 0;
   if (a.fp8 && !a.stage_bytes) return cudaErrorInvalidValue;  // e4m3 rows are written from the staged rows
   const size_t smem = tab + a.stage_bytes;
