@@ -111,13 +111,41 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
   return before + x - v;
 }
 
+// The token rows t_lo .. t_lo + n_tok - 1 of a block's pairs (contiguous in
+// xn) into shared memory, every 16-byte load of a round in flight, read
+// through L2 (peers of the block may have written them).
+__device__ __forceinline__ void scatter_stage_rows(const ScatArgs &a, int t_lo, int n_tok, uint4 *st4) {
+  const uint4 *src = (const uint4 *)(a.xn + (size_t)t_lo * a.d);
+  const int n4 = n_tok * (a.d / 8);
+  for (int i0 = 0; i0 < n4; i0 += 8 * kScatThreads) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + (int)threadIdx.x + u * kScatThreads;
+      if (i < n4) v[u] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + (int)threadIdx.x + u * kScatThreads;
+      if (i < n4) st4[i] = v[u];
+    }
+  }
+}
+
+// The block's first token row and token count.
+__device__ __forceinline__ void scatter_tokens(const ScatArgs &a, int blk, int *t_lo, int *n_tok) {
+  const int p0 = blk * a.per, p1 = min(a.T * a.k, p0 + a.per);
+  *t_lo = p0 / a.k;
+  *n_tok = p1 > p0 ? (p1 - 1) / a.k - *t_lo + 1 : 0;
+}
+
 // The scatter work of block `blk` (kScatThreads threads): its share of the
 // pairs, and (blk 0) the expert segments, the work list and the FFN's
 // counters.  tab: shared memory of scatter_smem_ints() ints; stage: shared
 // memory of stage_bytes bytes (16-byte aligned) for the block's token rows,
 // or null.
 __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *tab, int *warp_tot,
-                                              unsigned char *stage, size_t stage_bytes) {
+                                              unsigned char *stage, size_t stage_bytes, bool rows_staged = false) {
   // [ng][E]: pairs of e in earlier groups; then offs[E], first item[E]; then
   // the expert and group rank of each of this block's pairs
   const int E = a.E, ng = a.ng, n = ng * E;
@@ -196,23 +224,11 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
   constexpr int NW = kScatThreads / 32;
   const int t_lo = p0 / a.k, n_tok = p1 > p0 ? (p1 - 1) / a.k - t_lo + 1 : 0;
   if (stage && scatter_stage_bytes(n_tok, a.d, a.fp8) <= stage_bytes) {
-    const uint4 *src = (const uint4 *)(a.xn + (size_t)t_lo * a.d);  // rows t_lo .. t_hi are contiguous
     uint4 *st4 = (uint4 *)stage;
-    const int n4 = n_tok * vec;
-    for (int i0 = 0; i0 < n4; i0 += 8 * kScatThreads) {
-      uint4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + (int)threadIdx.x + u * kScatThreads;
-        if (i < n4) v[u] = src[i];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + (int)threadIdx.x + u * kScatThreads;
-        if (i < n4) st4[i] = v[u];
-      }
+    if (!rows_staged) {  // (the fused kernel may have staged them before its grid barrier)
+      scatter_stage_rows(a, t_lo, n_tok, st4);
+      __syncthreads();
     }
-    __syncthreads();
     if (a.fp8) {
       // Each token's row is quantized once (one warp per token): its scale
       // exponent from the row maximum, then its e4m3 codes, in column order,
@@ -488,27 +504,42 @@ __device__ __forceinline__ void topk_warp(const float *lrow, int E, int k, int l
 // which the others wait for (bounded).  Then this CTA's share of the scatter
 // reuses its shared memory (base: the CTA's dynamic shared memory, 1024-byte
 // aligned).
-__device__ __forceinline__ void fused_scatter_tail(const RouteArgs &a, unsigned char *base) {
+__device__ __forceinline__ void fused_scatter_tail(const RouteArgs &a, unsigned char *base, int grp) {
   __syncthreads();
-  __shared__ int passed;
+  // Grid-wide barrier (self-resetting, bounded): thread 0 arrives; the last
+  // arrival resets the count and bumps the generation the others wait for.
+  // Between its arrival and that wait, the CTA stages its token rows when
+  // they are its own token group's (written by its cluster, visible since
+  // the cluster barrier that ended the routing).
+  __shared__ int passed, g0_s, last_s;
   if (threadIdx.x == 0) {
     int *gen = a.bar + 32;
     const int g0 = ld_acquire_s32(gen);
+    g0_s = g0;
     passed = 1;
-    if (atom_add_release_s32(a.bar, 1) == (int)gridDim.x - 1) {  // releases this CTA's counts and ranks
-      // the last arrival: every CTA's writes are visible to it (the arrivals
+    last_s = atom_add_release_s32(a.bar, 1) == (int)gridDim.x - 1;  // releases this CTA's counts and ranks
+    if (last_s) {
+      // every CTA's writes are visible to the last arrival (the arrivals
       // released them); reset the count, then release the generation
       asm volatile("fence.acq_rel.gpu;\n" ::: "memory");
       *(volatile int *)a.bar = 0;
       st_release_s32(gen, g0 + 1);
-    } else {
-      const long long c0 = clock64();
-      while (ld_acquire_s32(gen) == g0) {
-        if (clock64() - c0 > tc::kWaitCycles) {
-          if (a.err) atomicExch(a.err, 55);
-          passed = 0;  // counts may be incomplete: leave the scatter undone
-          break;
-        }
+    }
+  }
+  unsigned char *stage = a.sc.stage_bytes ? base + scatter_tab_bytes(a.sc.ng, a.sc.E, a.sc.per) : nullptr;
+  int t_lo, n_tok;
+  scatter_tokens(a.sc, blockIdx.x, &t_lo, &n_tok);
+  const bool early = stage && n_tok > 0 && t_lo / kRouteTok == grp && (t_lo + n_tok - 1) / kRouteTok == grp &&
+                     scatter_stage_bytes(n_tok, a.sc.d, a.sc.fp8) <= (size_t)a.sc.stage_bytes;
+  if (early) scatter_stage_rows(a.sc, t_lo, n_tok, (uint4 *)stage);
+  if (threadIdx.x == 0 && !last_s) {
+    const int *gen = a.bar + 32;
+    const long long c0 = clock64();
+    while (ld_acquire_s32(gen) == g0_s) {
+      if (clock64() - c0 > tc::kWaitCycles) {
+        if (a.err) atomicExch(a.err, 55);
+        passed = 0;  // counts may be incomplete: leave the scatter undone
+        break;
       }
     }
     // acquired: the generation by ld.acquire, or (the last arrival) by the
@@ -518,9 +549,7 @@ __device__ __forceinline__ void fused_scatter_tail(const RouteArgs &a, unsigned 
   pdl_trigger();
   if (!passed) return;
   __shared__ int warp_tot[kScatThreads / 32];
-  scatter_block(a.sc, blockIdx.x, (int *)base, warp_tot,
-                a.sc.stage_bytes ? base + scatter_tab_bytes(a.sc.ng, a.sc.E, a.sc.per) : nullptr,
-                (size_t)a.sc.stage_bytes);
+  scatter_block(a.sc, blockIdx.x, (int *)base, warp_tot, stage, (size_t)a.sc.stage_bytes, early);
 }
 
 template <bool NORM>
@@ -848,7 +877,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncwarp();
   tc::cluster_sync();  // peers' counts stay alive until every read is done
-  if (a.fuse) fused_scatter_tail(a, base);
+  if (a.fuse) fused_scatter_tail(a, base, grp);
 }
 
 template <bool NORM>
