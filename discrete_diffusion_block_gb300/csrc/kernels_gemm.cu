@@ -25,7 +25,8 @@ namespace {
 // stores them as bf16x2.
 struct EpiQkv {
   static constexpr int kTok = 64, kMaxHalf = 64;
-  static constexpr size_t extra_smem = (size_t)kTok * kMaxHalf * 2 * sizeof(float) + kTok * sizeof(long long);
+  static constexpr size_t extra_smem =
+      (size_t)kTok * kMaxHalf * 2 * sizeof(float) + kTok * sizeof(long long) + kTok * sizeof(int);
   QkvOut o;
   // Stage the cos/sin rows and page slots of tokens t0 .. t0 + nt - 1 of the
   // tile with threads tid of nthr (64 or 128; nt <= kTok <= nthr), all loads
@@ -60,7 +61,10 @@ struct EpiQkv {
         }
       }
     }
-    if (tid < nt) slot[tid] = page * o.Hkv * o.pg * o.hd + (long long)(ps % o.pg) * 64;
+    if (tid < nt) {
+      slot[tid] = page * o.Hkv * o.pg * o.hd + (long long)(ps % o.pg) * 64;
+      ((int *)(slot + kTok))[tid] = ps & 7;  // the pool row's chunk swizzle
+    }
   }
   // Split-K with slices of up to kTok tokens: the slice's cos/sin rows and
   // page slots are staged by prepare() into memory of their own, before the
@@ -80,6 +84,7 @@ struct EpiQkv {
     float *cs = (float *)extra;                           // [kTok][half]
     float *sn = cs + kTok * kMaxHalf;                     // [kTok][half]
     long long *slot = (long long *)(sn + kTok * kMaxHalf);  // element offset of (page, head 0) + 64 * slot
+    const int *pos7 = (const int *)(slot + kTok);             // position % 8 of each token
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t0 = 0; t0 < c.n_valid; t0 += kTok) {
       const int nt = min(kTok, c.n_valid - t0);
@@ -133,7 +138,7 @@ struct EpiQkv {
               *(__nv_bfloat162 *)dst = __floats2bfloat162_rn(lo0, lo1);
               *(__nv_bfloat162 *)(dst + half) = __floats2bfloat162_rn(hi0, hi1);
             } else {  // pool: feature f of slot s in sub-block f/64, chunk ((f%64)/8) ^ (s%8)
-              const int s7 = o.rows.pos(c.n0 + t0 + t) & 7;
+              const int s7 = pos7[t];
               bf16 *row = base_kv + slot[t];
               const int f0 = j, f1 = j + half;
               *(__nv_bfloat162 *)(row + (size_t)(f0 >> 6) * o.pg * 64 + ((((f0 & 63) >> 3) ^ s7) << 3) + (f0 & 7)) =
