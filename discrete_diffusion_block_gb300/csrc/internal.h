@@ -67,7 +67,7 @@ cudaError_t moe_scatter(const bf16 *xn, const int *ids, const int *gcount, int *
                         cudaStream_t st, unsigned long long *stats = nullptr, const Fp8Experts *fp8 = nullptr);
 // moe_norm_route (h != null) or moe_route, then moe_scatter, as one launch
 // when the routing grid fits the machine (the scatter then runs in the
-// routing kernel after a grid-wide barrier on bar, 2 zeroed ints), else as
+// routing kernel after a grid-wide barrier on bar, kGridBarInts zeroed ints), else as
 // two; *launches (optional) receives 1 or 2.  slot_row serves as the rank
 // array in between.
 cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16 *xn, const bf16 *wr, int T, int d,

@@ -35,10 +35,11 @@
 // warps per TMEM lane quarter (thread = query row), each on half of a tile's
 // keys, exchanging their halves' maxima per tile.  With the key range split
 // over several blocks, the blocks of one query tile form a
-// cluster: each stages its unnormalised output rows and softmax state (m, l)
-// in shared memory, pushes to every peer the slice of rows that peer owns
-// (bulk shared-to-shared copies), and each block merges its slice (weights
-// 2^(m_s - m*)) and writes it; no device scratch is used.
+// cluster: each stages its unnormalised output rows (bf16) and their softmax
+// state (m, l) in its own shared memory, and after a cluster barrier each
+// block reads the partials of the rows it owns from every block's shared
+// memory (distributed shared-memory loads), merges them (weights
+// 2^(m_s - m*)) and writes them; no device scratch is used.
 #include <cuda.h>
 
 #include <cudaTypedefs.h>
