@@ -102,6 +102,7 @@ struct dg_model {
        *x_tiles = nullptr;  // act and x_tiles: expert-FFN operand tiles per work item
   unsigned long long *moe_stats = nullptr;  // device: experts touched, rows routed
   int *route_bar = nullptr;                  // device, kGridBarInts: grid barrier of the fused routing + scatter
+  float *ffn_part = nullptr;                 // device: partial-sum slots of split gate/up units
   int *kx = nullptr;                         // expert_fp8: scale exponents of the expert input rows
   int moe_input_rows = 0, moe_input_layer = -1;  // the rows xn holds: the last MoE input
   float *gates = nullptr, *y = nullptr;
@@ -367,7 +368,8 @@ int run_layers(dg_model *m, int T, const dg::RowSet &rows, const int *ptab, int 
     const int rows = T * c.top_k;
     KL(DG_K_EXPERT_FFN, 1,
        dg::moe_ffn(m->x_tiles, rows, W.wgu, W.wd, m->offs, m->work, m->n_work, m->max_work,
-                   c.n_experts, d, c.d_ff, m->act, m->y, err, st, c.expert_fp8 ? &fx : nullptr));
+                   c.n_experts, d, c.d_ff, m->act, m->y, err, st, c.expert_fp8 ? &fx : nullptr, m->ffn_part,
+                   (int)dg::moe_ffn_part_slots()));
     if (fuse_norm && L + 1 < c.n_layers) {
       KL(DG_K_COMBINE, 1,
          dg::moe_combine_norm(m->h, m->y, m->gates, m->slot_row, T, c.top_k, d, m->layers[L + 1].attn_norm,
@@ -462,6 +464,7 @@ int alloc_model(dg_model *m, const void *const *weights) {
   CKR(m->alloc(&m->xq, (size_t)T * d));
   CKR(m->alloc(&m->xn_lo, (size_t)BC * d));
   CKR(m->alloc(&m->moe_stats, 2));
+  CKR(m->alloc(&m->ffn_part, dg::moe_ffn_part_slots() * (dg::kFfnPartSlotBytes / 4)));
   CKR(m->alloc(&m->route_bar, dg::kGridBarInts));
   CK(cudaMemset(m->route_bar, 0, dg::kGridBarInts * sizeof(int)));
   CKR(m->alloc(&m->q, (size_t)T * qd));
@@ -1469,6 +1472,7 @@ struct MoeWs {
   bf16 *act, *x_tiles;
   float *y_rows;
   int *bar;
+  float *part;
   size_t bytes;
   int max_work;
 };
@@ -1491,6 +1495,7 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.x_tiles = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, d) * 2);
   w.y_rows = (float *)take((size_t)T * k * d * 4);
   w.bar = (int *)take(dg::kGridBarInts * 4);
+  w.part = (float *)take(dg::moe_ffn_part_slots() * dg::kFfnPartSlotBytes);
   w.bytes = off;
   return w;
 }
@@ -1524,7 +1529,8 @@ int dg_op_moe(const uint16_t *xn, const uint16_t *w_router, const uint16_t *w_ga
                            w.n_work, w.max_work, w.bar, status, st));
   const int rows = T * top_k;
   CK(dg::moe_ffn(w.x_tiles, rows, (const bf16 *)w_gate_up, (const bf16 *)w_down, w.offs, w.work, w.n_work,
-                 w.max_work, n_experts, d, d_ff, w.act, w.y_rows, status, st));
+                 w.max_work, n_experts, d, d_ff, w.act, w.y_rows, status, st, nullptr, w.part,
+                 (int)dg::moe_ffn_part_slots()));
   CK(dg::moe_combine(y, w.y_rows, gates, w.slot_row, T, top_k, d, false, st));
   return DG_OK;
 }

@@ -76,12 +76,24 @@ cudaError_t moe_route_scatter(const float *h, const float *gain, float eps, bf16
                               unsigned long long *stats = nullptr, int *launches = nullptr,
                               const Fp8Experts *fp8 = nullptr);
 size_t moe_max_work(int T, int k, int E, int tile_rows);
+// Gate/up units of one expert-FFN launch that may run split along K (the
+// overflow past a whole number of waves); their part tickets follow the
+// work list's counters.
+constexpr int kFfnSplitUnits = 64;
+// Work list, per-item counters, the unit counter and the part tickets.
 size_t moe_work_ints(int T, int k, int E, int tile_rows);
+// Partial-sum slots of split gate/up units for moe_ffn: one per SM, 128 KB each.
+size_t moe_ffn_part_slots();
+constexpr size_t kFfnPartSlotBytes = (size_t)2 * 128 * 128 * 4;
 // Routed experts of one layer (kernels_moe.cu): act = SwiGLU(X Wg^T, X Wu^T),
 // y = act Wd^T, for every work item of moe_scatter; one persistent launch.
 // X: the item tiles of moe_scatter; wgu / wd: expert weights as operand tiles
 // (the fill kernels' layout); act_tiles: moe_item_tile_elems(max_work, F)
-// elements of scratch; y: [rows][d] fp32, row = sorted pair row.
+// elements of scratch; y: [rows][d] fp32, row = sorted pair row.  part_buf
+// (optional, part_slots slots of kFfnPartSlotBytes): when a launch's gate/up
+// units exceed a whole number of waves by a few (at most a quarter of the
+// SMs), those units run split along K, each part's sums summed in part order
+// by the last part (bf16 experts only).
 // The e4m3 expert path (kernels_moe.cu): gate/up weights as e4m3 operand
 // tiles (the bytes of bf16 tiles [E][2][F][d/2]) with their rows' scale
 // exponents kw [E][2][F]; the scatter writes the token rows as e4m3 tiles and
@@ -97,7 +109,8 @@ cudaError_t quantize_rows_e4m3(const bf16 *src, uint8_t *dst, int *exps, int n_m
                                cudaStream_t st);
 cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
-                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8 = nullptr);
+                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8 = nullptr,
+                    float *part_buf = nullptr, int part_slots = 0);
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
 // h[t] += sum_s gate * y (as moe_combine with accumulate), then the RMSNorm of

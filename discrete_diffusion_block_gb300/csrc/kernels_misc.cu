@@ -441,7 +441,9 @@ size_t moe_max_work(int T, int k, int E, int tile_rows) {
   return (size_t)(T * k + tile_rows - 1) / tile_rows + E;
 }
 
-size_t moe_work_ints(int T, int k, int E, int tile_rows) { return 3 * moe_max_work(T, k, E, tile_rows) + 1; }
+size_t moe_work_ints(int T, int k, int E, int tile_rows) {
+  return 3 * moe_max_work(T, k, E, tile_rows) + 1 + kFfnSplitUnits;
+}
 
 
 cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,

@@ -74,7 +74,11 @@ struct UnitInfo {
   int item, mt, b_row, n_valid, e;
   int a_rows;   // valid rows of each weight tile (phase A: features in the block)
   int n_acc;    // weight blocks (accumulators) of the unit: 2 (gate, up), or kDownBlocks or fewer (down)
-  int pad[3];
+  int kb, ke;   // the unit's k-steps
+  int part;     // a split gate/up unit: this part's index (its K range), else -1
+  int ov;       // a split gate/up unit: its index among the split units
+  int nparts;   // a split gate/up unit: its number of parts
+  int pad[2];
 };
 
 struct FfnSmem {
@@ -101,6 +105,13 @@ struct FfnArgs {
   const int *kw, *kx;
   int *done;   // [max_work] phase A units finished per item
   int *next;   // unit counter
+  // Split gate/up units (the overflow past a whole number of waves): each
+  // part stores its sums in a slot of part_buf ([2][128 token columns][128
+  // features] fp32) and takes a ticket from part_cnt[unit]; the last part
+  // sums the parts in part order and runs the SwiGLU epilogue.
+  float *part_buf;
+  int part_slots;
+  int *part_cnt;
   int E, d, F;
   bf16 *act;   // [item][F/64] tiles: SwiGLU output rows
   float *y;    // [rows][d]
@@ -204,7 +215,23 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
 
   const int n_items = *g.n_work;
   const int mA = (g.F + 127) / 128, mB = (g.d + 128 * kDownBlocks - 1) / (128 * kDownBlocks);
-  const int nA = n_items * mA, n_units = nA + n_items * mB;
+  const int nA = n_items * mA;
+  // Gate/up units past a whole number of waves, when only a few (at most a
+  // quarter of the grid), run split along K into S parts: the parts spread
+  // over the SMs instead of a nearly empty extra wave of whole units.
+  int n_ov = 0, S_ov = 1;
+  if (!g.fp8 && g.part_buf && nA > (int)gridDim.x) {
+    const int rem = nA % (int)gridDim.x;
+    if (rem > 0 && 4 * rem <= (int)gridDim.x && rem <= kFfnSplitUnits) {
+      const int s_try = 4;  // the last part reads every part's sums: more parts, more bytes
+      if (rem * s_try <= g.part_slots) {
+        n_ov = rem;
+        S_ov = s_try;
+      }
+    }
+  }
+  const int nA_full = nA - n_ov, nP = n_ov * S_ov;  // whole gate/up units first, then the parts
+  const int n_units = nA_full + nP + n_items * mB;
   // gate/up k-steps: 64 bf16 or 128 e4m3 elements (128 bytes a row either way)
   const int KTA = g.fp8 ? g.d / 128 : g.d / tc::kBK, KTB = g.F / tc::kBK;
   auto a_tile = [&](int s, int j) { return base + (size_t)s * kFfnStageBytes + (size_t)j * kFfnATileBytes; };
@@ -222,10 +249,26 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         UnitInfo inf;
         inf.u = u < n_units ? u : -1;
         if (inf.u >= 0) {
-          inf.phase = u >= nA;
-          const int v = inf.phase ? u - nA : u, per = inf.phase ? mB : mA;
+          inf.phase = u >= nA_full + nP;
+          inf.part = -1;
+          inf.ov = 0;
+          inf.nparts = 1;
+          int v, per = inf.phase ? mB : mA;
+          if (inf.phase) {
+            v = u - nA_full - nP;
+          } else if (u < nA_full) {
+            v = u;
+          } else {  // part (u - nA_full) % S_ov of split unit (u - nA_full) / S_ov
+            inf.ov = (u - nA_full) / S_ov;
+            inf.part = (u - nA_full) - inf.ov * S_ov;
+            inf.nparts = S_ov;
+            v = nA_full + inf.ov;
+          }
           inf.item = v / per;
           inf.mt = v - inf.item * per;
+          const int KTu = inf.phase ? KTB : KTA;
+          inf.kb = inf.part < 0 ? 0 : KTu * inf.part / S_ov;
+          inf.ke = inf.part < 0 ? KTu : KTu * (inf.part + 1) / S_ov;
           const int e = g.work[2 * inf.item], n0 = g.work[2 * inf.item + 1];
           const int e0 = g.offs[e];
           inf.b_row = e0 + n0;
@@ -285,9 +328,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           asm volatile("fence.proxy.async.global;\n" ::: "memory");
         }
         int issued = it;  // stages whose copies went out (for the drain below)
-        for (int kt = 0; kt < KT; ++kt) {
-          const int i = it + kt, s = i % kFfnStages, r = i / kFfnStages;
-          if (kt >= pre) {
+        const int nk = inf.ke - inf.kb;  // the unit's k-steps (a split part: its K range)
+        for (int kk = 0; kk < nk; ++kk) {
+          const int kt = inf.kb + kk, i = it + kk, s = i % kFfnStages, r = i / kFfnStages;
+          if (kk >= pre) {
             if (r > 0) tc::mbar_wait(empty + s, (r - 1) & 1, g.err, 23, abort);
             if (*abort) break;
             tc::mbar_expect_tx(full + s, tx);
@@ -309,7 +353,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
             }
           }
         }
-        it += KT;
+        it += nk;
       }
     }
   } else if (warp == kFfnMmaWarp) {
@@ -327,7 +371,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         const int n_mma = max(16, (inf.n_valid + 15) & ~15);
         const bool f8 = g.fp8 && inf.phase == 0;
         const uint32_t idesc = f8 ? idesc_e4m3(128, n_mma) : tc::idesc_bf16(128, n_mma);
-        const int KT = inf.phase ? KTB : KTA;
+        const int KT = inf.ke - inf.kb;  // the unit's k-steps (the first one starts the accumulators)
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int s = it % kFfnStages, r = it / kFfnStages;
           tc::mbar_wait(full + s, r & 1, g.err, 26, abort);
@@ -356,6 +400,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
     }
   } else {
     // ---- epilogue: warps 0-7; lane = accumulator row, 64 token columns per warp
+    __shared__ int split_last;  // written by thread 0, read by the epilogue after a barrier
     const int q4 = warp & 3, half = warp >> 2;
     const int lrow = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
@@ -369,20 +414,54 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
       tc::mbar_wait(acc_full + buf, (n >> 1) & 1, g.err, 28, abort);
       tc::fence_after();
       const uint32_t tp = tmem + buf * kFfnPairCols + lane_off;
-      if (inf.phase == 0) {
-        // SwiGLU of feature f = 128 mt + lrow for the warp's token columns;
-        // lanes 2i and 2i + 1 trade values so that each stores a bf16 pair
-        // (features f, f + 1) of one token row into the act tile.
-        const bool fok = lrow < inf.a_rows;
-        const int fb = 128 * inf.mt + (lrow & ~1), cc = fb & 63;
+      // SwiGLU of feature f = 128 mt + lrow for the warp's token columns;
+      // lanes 2i and 2i + 1 trade values so that each stores a bf16 pair
+      // (features f, f + 1) of one token row into the act tile.
+      const bool fok = lrow < inf.a_rows;
+      const int fb = 128 * inf.mt + (lrow & ~1), cc = fb & 63;
+      unsigned char *blk = inf.phase == 0
+                               ? (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + (fb >> 6)) * kTileElems)
+                               : nullptr;
+      auto store_act = [&](const uint32_t(&gv)[32], const uint32_t(&uv)[32], int col0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float a0 = swiglu_f(__uint_as_float(gv[2 * j]), __uint_as_float(uv[2 * j]));
+          const float a1 = swiglu_f(__uint_as_float(gv[2 * j + 1]), __uint_as_float(uv[2 * j + 1]));
+          const float recv = __shfl_xor_sync(0xffffffffu, (lane & 1) ? a0 : a1, 1);
+          const int t = col0 + 2 * j + (lane & 1);
+          const uint32_t w = (lane & 1) ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
+          if (fok && t < inf.n_valid)
+            *(uint32_t *)(blk + t * 128 + ((((cc >> 3) ^ (t & 7)) << 4) | ((cc & 7) << 1))) = w;
+        }
+      };
+      // a split unit's part slots: [2 (gate, up)][128 token columns][128 features] fp32
+      // (a warp's 32 features of one column: one 128-byte line)
+      float *const pslot = inf.part >= 0 ? g.part_buf + (size_t)inf.ov * inf.nparts * (kFfnPartSlotBytes / 4) : nullptr;
+      if (inf.phase == 0 && inf.part >= 0) {
+        // one K range of a split gate/up unit: its sums into its slot
+        float *pb = pslot + (size_t)inf.part * (kFfnPartSlotBytes / 4);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * half + 32 * c;
+          if (col0 >= inf.n_valid) break;
+          uint32_t gv[32], uv[32];
+          tc::tmem_ld32(tp + col0, gv);
+          tc::tmem_ld32(tp + kFfnBN + col0, uv);
+          tc::tmem_ld_wait(gv);
+          tc::tmem_ld_wait(uv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            pb[(size_t)(col0 + j) * 128 + lrow] = __uint_as_float(gv[j]);
+            pb[(size_t)(128 + col0 + j) * 128 + lrow] = __uint_as_float(uv[j]);
+          }
+        }
+      } else if (inf.phase == 0) {
         // fp8: this feature's gate and up exponents (the token rows' come per column)
         int kwg = 0, kwu = 0;
         if (g.fp8 && fok) {
           kwg = g.kw[((size_t)inf.e * 2) * g.F + 128 * inf.mt + lrow];
           kwu = g.kw[((size_t)inf.e * 2 + 1) * g.F + 128 * inf.mt + lrow];
         }
-        unsigned char *blk =
-            (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + (fb >> 6)) * kTileElems);
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * half + 32 * c;
@@ -401,16 +480,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
               uv[j] = __float_as_uint(ldexpf(__uint_as_float(uv[j]), kwu + kx));
             }
           }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float a0 = swiglu_f(__uint_as_float(gv[2 * j]), __uint_as_float(uv[2 * j]));
-            const float a1 = swiglu_f(__uint_as_float(gv[2 * j + 1]), __uint_as_float(uv[2 * j + 1]));
-            const float recv = __shfl_xor_sync(0xffffffffu, (lane & 1) ? a0 : a1, 1);
-            const int t = col0 + 2 * j + (lane & 1);
-            const uint32_t w = (lane & 1) ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
-            if (fok && t < inf.n_valid)
-              *(uint32_t *)(blk + t * 128 + ((((cc >> 3) ^ (t & 7)) << 4) | ((cc & 7) << 1))) = w;
-          }
+          store_act(gv, uv, col0);
         }
       } else {
         // y[row][256 mt + 128 a + lrow] for the warp's token columns: for each
@@ -438,7 +508,51 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
         __threadfence();
         asm volatile("fence.proxy.async.global;\n" ::: "memory");
         epi_sync();
-        if (threadIdx.x == 0) atomicAdd(g.done + inf.item, 1);  // publish after every thread's stores
+        bool publish = inf.part < 0;
+        if (inf.part >= 0) {
+          // the part's ticket; the last part (every other part's sums are
+          // stored: their tickets came first) sums the parts in part order
+          if (threadIdx.x == 0) split_last = atomicAdd(g.part_cnt + inf.ov, 1) == inf.nparts - 1;
+          epi_sync();
+          if (split_last) {
+            __threadfence();
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              const int col0 = 64 * half + 32 * c;
+              if (col0 >= inf.n_valid) break;
+              float sg[32], su[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) sg[j] = su[j] = 0.0f;
+#pragma unroll 1
+              for (int q = 0; q < inf.nparts; ++q) {  // part order: a fixed summation order
+                const float *pb = pslot + (size_t)q * (kFfnPartSlotBytes / 4) + (size_t)col0 * 128 + lrow;
+                float vg[32], vu[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  vg[j] = __ldcg(pb + (size_t)j * 128);
+                  vu[j] = __ldcg(pb + (size_t)(128 + j) * 128);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  sg[j] += vg[j];
+                  su[j] += vu[j];
+                }
+              }
+              uint32_t gv[32], uv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                gv[j] = __float_as_uint(sg[j]);
+                uv[j] = __float_as_uint(su[j]);
+              }
+              store_act(gv, uv, col0);
+            }
+            __threadfence();
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            epi_sync();
+            publish = true;
+          }
+        }
+        if (publish && threadIdx.x == 0) atomicAdd(g.done + inf.item, 1);  // publish after every thread's stores
       }
       if (lane == 0) mbar_arrive(q_empty + q);  // this warp is done with the queue entry
     }
@@ -515,9 +629,12 @@ cudaError_t quantize_rows_e4m3(const bf16 *src, uint8_t *dst, int *exps, int n_m
   return cudaGetLastError();
 }
 
+size_t moe_ffn_part_slots() { return (size_t)ffn_num_sms(); }
+
 cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
-                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8) {
+                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8, float *part_buf,
+                    int part_slots) {
   if (rows <= 0) return cudaSuccess;
   if (d % 128 || F % 64) return cudaErrorInvalidValue;
   static_assert(FfnSmem::bytes <= 232448, "shared memory of the expert FFN");
@@ -539,6 +656,9 @@ cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *
   g.x = x_tiles;
   g.done = const_cast<int *>(work) + 2 * max_work;  // zeroed by moe_scatter
   g.next = g.done + max_work;
+  g.part_cnt = g.next + 1;  // kFfnSplitUnits tickets, zeroed by moe_scatter
+  g.part_buf = part_buf;
+  g.part_slots = part_buf ? part_slots : 0;
   g.E = E;
   g.d = d;
   g.F = F;

@@ -212,7 +212,7 @@ __device__ __forceinline__ void scatter_block(const ScatArgs &a, int blk, int *t
         atomicAdd(&a.stats[1], (unsigned long long)total);
       }
     }
-    for (int i = threadIdx.x; i <= a.max_work; i += kScatThreads) a.sync[i] = 0;  // FFN counters
+    for (int i = threadIdx.x; i <= a.max_work + kFfnSplitUnits; i += kScatThreads) a.sync[i] = 0;  // FFN counters
   }
   __syncwarp();
   __syncthreads();

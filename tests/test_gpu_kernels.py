@@ -392,6 +392,45 @@ def test_moe_against_fp64(T, d, E, k, F):
     assert rel_err(y.cpu().numpy(), y_ref) <= TOL
 
 
+def test_moe_split_overflow_gate_up_units_against_fp64():
+    """Gate/up units just past a whole number of waves run split along K (the
+    last part sums the parts in order): a routing whose unit count exceeds the
+    SM count by at most a quarter of it, against the fp64 oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d, k, F = 512, 8, 704
+    mA = (F + 127) // 128
+    found = None
+    for E in (26, 28, 24, 30):
+        for T in (256, 240, 272, 224, 288):
+            wr = torch.empty(E * d, dtype=torch.bfloat16, device=dev())
+            wgu = torch.empty(E * 2 * F * d, dtype=torch.bfloat16, device=dev())
+            wd = torch.empty(E * d * F, dtype=torch.bfloat16, device=dev())
+            dgp.dg_op_fill_moe_weights(wr, wgu, wd, d, E, F, 0, 0, 0.02)
+            xf, xt = synth.normal_bf16((T, d), seed=5)
+            y = torch.empty(T, d, dtype=torch.float32, device=dev())
+            ids = torch.empty(T, k, dtype=torch.int32, device=dev())
+            gates = torch.empty(T, k, dtype=torch.float32, device=dev())
+            ws = torch.empty(dgp.dg_op_moe_workspace_bytes(T, d, E, k, F), dtype=torch.uint8, device=dev())
+            dgp.dg_op_moe(xt.to(dev()), wr, wgu, wd, T, d, E, k, F, y, ids, gates, ws)
+            gi = ids.cpu().numpy()
+            items = int(sum((c + 127) // 128 for c in np.bincount(gi.ravel(), minlength=E) if c > 0))
+            n_a = items * mA
+            if n_a > sms and 0 < n_a % sms <= sms // 4:
+                found = (T, E, xf, gi, gates.cpu().numpy(), y.cpu().numpy())
+                break
+        if found:
+            break
+    assert found, "no routing with a few gate/up units past a whole wave"
+    T, E, xf, gi, g_gpu, y_gpu = found
+    W = dict(wr=ow.tensor(0, 104, (E, d), 0.02), wg=ow.tensor(0, 105, (E, F, d), 0.02),
+             wu=ow.tensor(0, 106, (E, F, d), 0.02), wd=ow.tensor(0, 107, (E, d, F), 0.02))
+    x64 = xf.astype(np.float64)
+    _, g_ref, _ = om.route(x64, W["wr"], k, forced=gi)      # raises unless a valid top-k
+    assert np.abs(g_gpu - g_ref).max() <= TOL
+    y_ref = om.moe_given_routing(x64, gi, g_ref, W)
+    assert rel_err(y_gpu, y_ref) <= TOL
+
+
 # ---- KV append (bit-exact indexing) ----------------------------------------------
 
 def test_kv_append_bit_exact_with_shuffled_pages():
