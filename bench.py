@@ -258,10 +258,10 @@ def expert_bytes(cfg, experts_per_launch, rows_per_launch):
     down of every routed expert): the gate/up and down weights of every expert
     that received a row, once (the count is measured on the device by the
     routing kernel), the gathered token rows, the SwiGLU activations written
-    and read back, and the fp32 outputs."""
+    and read back, and the bf16 outputs."""
     d, F = cfg.d_model, cfg.d_ff
     e, r = experts_per_launch, rows_per_launch
-    return {"expert_ffn": e * 3 * F * d * 2 + r * d * 2 + 2 * r * F * 2 + r * d * 4}
+    return {"expert_ffn": e * 3 * F * d * 2 + r * d * 2 + 2 * r * F * 2 + r * d * 2}
 
 
 def gpu_arm(args):

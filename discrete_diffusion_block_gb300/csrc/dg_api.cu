@@ -105,7 +105,8 @@ struct dg_model {
   float *ffn_part = nullptr;                 // device: partial-sum slots of split gate/up units
   int *kx = nullptr;                         // expert_fp8: scale exponents of the expert input rows
   int moe_input_rows = 0, moe_input_layer = -1;  // the rows xn holds: the last MoE input
-  float *gates = nullptr, *y = nullptr;
+  float *gates = nullptr;
+  bf16 *y = nullptr;  // [T*k][d]: expert outputs per sorted pair row
   float *xchg = nullptr;  // split-K partial exchange of the projection GEMMs
   int *topk = nullptr, *offs = nullptr, *gcount = nullptr, *slot_row = nullptr, *work = nullptr,
       *n_work = nullptr;
@@ -1470,7 +1471,7 @@ namespace {
 struct MoeWs {
   int *offs, *gcount, *slot_row, *work, *n_work;
   bf16 *act, *x_tiles;
-  float *y_rows;
+  bf16 *y_rows;
   int *bar;
   float *part;
   size_t bytes;
@@ -1493,7 +1494,7 @@ MoeWs moe_layout(void *base, int T, int d, int E, int k, int F) {
   w.n_work = (int *)take(4);
   w.act = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, F) * 2);
   w.x_tiles = (bf16 *)take(dg::moe_item_tile_elems(w.max_work, d) * 2);
-  w.y_rows = (float *)take((size_t)T * k * d * 4);
+  w.y_rows = (bf16 *)take((size_t)T * k * d * 2);
   w.bar = (int *)take(dg::kGridBarInts * 4);
   w.part = (float *)take(dg::moe_ffn_part_slots() * dg::kFfnPartSlotBytes);
   w.bytes = off;

@@ -89,7 +89,7 @@ constexpr size_t kFfnPartSlotBytes = (size_t)2 * 128 * 128 * 4;
 // y = act Wd^T, for every work item of moe_scatter; one persistent launch.
 // X: the item tiles of moe_scatter; wgu / wd: expert weights as operand tiles
 // (the fill kernels' layout); act_tiles: moe_item_tile_elems(max_work, F)
-// elements of scratch; y: [rows][d] fp32, row = sorted pair row.  part_buf
+// elements of scratch; y: [rows][d] bf16, row = sorted pair row.  part_buf
 // (optional, part_slots slots of kFfnPartSlotBytes): when a launch's gate/up
 // units exceed a whole number of waves by a few (at most a quarter of the
 // SMs), those units run split along K, each part's sums summed in part order
@@ -109,14 +109,14 @@ cudaError_t quantize_rows_e4m3(const bf16 *src, uint8_t *dst, int *exps, int n_m
                                cudaStream_t st);
 cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
-                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8 = nullptr,
+                    bf16 *y, int *err, cudaStream_t st, const Fp8Experts *fp8 = nullptr,
                     float *part_buf = nullptr, int part_slots = 0);
-cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
+cudaError_t moe_combine(float *h, const bf16 *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st);
 // h[t] += sum_s gate * y (as moe_combine with accumulate), then the RMSNorm of
 // the updated row with `gain` into x_tiles (bf16 operand tiles, tiled_index
 // over [T][d]): the next layer's QKV input.  d <= 4096, a multiple of 64.
-cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const int *slot_row,
+cudaError_t moe_combine_norm(float *h, const bf16 *y, const float *gates, const int *slot_row,
                              int T, int k, int d, const float *gain, float eps, bf16 *x_tiles,
                              cudaStream_t st);
 cudaError_t kv_append(const bf16 *k_new, const bf16 *v_new, bf16 *k_pool, bf16 *v_pool,

@@ -228,10 +228,16 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(bf16 *out, bf16 *
 // An unordered logit (NaN) never wins a comparison but a still-unselected
 // expert is always taken over none, so every emitted id is in [0, E).
 
-// h[t] (+)= sum_s gate[t][s] * y[slot_row[t*k+s]], slots in ascending order.
-// The token's gates and rows are staged first; each thread then has all k
-// row loads of its float4 column in flight at once.
-__global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y, const float *gates,
+// Four bf16 values (one 8-byte load) to floats.
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xffff0000u));
+}
+
+// h[t] (+)= sum_s gate[t][s] * y[slot_row[t*k+s]] (y bf16), slots in
+// ascending order.  The token's gates and rows are staged first; each
+// thread then has all k row loads of its 4-column group in flight at once.
+__global__ void __launch_bounds__(256) combine_kernel(float4 *h, const uint2 *y, const float *gates,
                                                       const int *slot_row, int k, int d4,
                                                       int accumulate) {
   pdl_wait();
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
   }
   __syncthreads();
   for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-    float4 v[16];
+    uint2 v[16];
 #pragma unroll
     for (int s = 0; s < 16; ++s)
       if (s < k) v[s] = y[(size_t)r_s[s] * d4 + c];
@@ -254,10 +260,11 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
 #pragma unroll
     for (int s = 0; s < 16; ++s)
       if (s < k) {
-        mo.x += g_s[s] * v[s].x;
-        mo.y += g_s[s] * v[s].y;
-        mo.z += g_s[s] * v[s].z;
-        mo.w += g_s[s] * v[s].w;
+        const float4 f = bf16x4_to_float4(v[s]);
+        mo.x += g_s[s] * f.x;
+        mo.y += g_s[s] * f.y;
+        mo.z += g_s[s] * f.z;
+        mo.w += g_s[s] * f.w;
       }
     h[(size_t)t * d4 + c] = make_float4(acc.x + mo.x, acc.y + mo.y, acc.z + mo.z, acc.w + mo.w);
   }
@@ -265,10 +272,10 @@ __global__ void __launch_bounds__(256) combine_kernel(float4 *h, const float4 *y
 
 // combine_kernel followed by the RMSNorm of the updated row (the next
 // layer's input norm, same formula as rmsnorm_kernel): one block per token,
-// one float4 column per thread (d4 <= 1024), so that the h row, the gain and
-// all k expert rows of a column are in flight at once; the row stays in
-// registers between the two steps.
-__global__ void __launch_bounds__(1024, 2) combine_norm_kernel(float4 *h, const float4 *y, const float *gates,
+// one 4-column group per thread (d4 <= 1024), so that the h row and eight
+// expert rows of a column are in flight at once; the row stays in registers
+// between the two steps.
+__global__ void __launch_bounds__(1024, 2) combine_norm_kernel(float4 *h, const uint2 *y, const float *gates,
                                                             const int *slot_row, int k, int d4,
                                                             const float *gain, float eps, bf16 *x_tiles, int T) {
   pdl_wait();
@@ -280,7 +287,6 @@ __global__ void __launch_bounds__(1024, 2) combine_norm_kernel(float4 *h, const 
   __shared__ float red[32];
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4 acc = ok ? h[(size_t)t * d4 + c] : zero;
-  const float4 gg = ok ? ((const float4 *)gain)[c] : zero;
   if (threadIdx.x < k) {
     g_s[threadIdx.x] = gates[(size_t)t * k + threadIdx.x];
     r_s[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
@@ -289,26 +295,28 @@ __global__ void __launch_bounds__(1024, 2) combine_norm_kernel(float4 *h, const 
   float4 hv = zero;
   float ss = 0.0f;
   if (ok) {
-    float4 mo = zero;
-    for (int s0 = 0; s0 < k; s0 += 4) {  // four expert rows in flight at a time, summed in slot order
-      float4 v[4];
+    float4 mo = acc;  // h, then the gate-weighted expert rows in slot order
+    for (int s0 = 0; s0 < k; s0 += 8) {  // eight expert rows in flight at a time, summed in slot order
+      uint2 v[8];
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
+      for (int s = 0; s < 8; ++s)
         if (s0 + s < k) v[s] = y[(size_t)r_s[s0 + s] * d4 + c];
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
+      for (int s = 0; s < 8; ++s)
         if (s0 + s < k) {
           const float gs = g_s[s0 + s];
-          mo.x += gs * v[s].x;
-          mo.y += gs * v[s].y;
-          mo.z += gs * v[s].z;
-          mo.w += gs * v[s].w;
+          const float4 f = bf16x4_to_float4(v[s]);
+          mo.x += gs * f.x;
+          mo.y += gs * f.y;
+          mo.z += gs * f.z;
+          mo.w += gs * f.w;
         }
     }
-    hv = make_float4(acc.x + mo.x, acc.y + mo.y, acc.z + mo.z, acc.w + mo.w);
+    hv = mo;
     h[(size_t)t * d4 + c] = hv;
     ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
   }
+  const float4 gg = ok ? ((const float4 *)gain)[c] : zero;  // in flight during the sum of squares
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   const int nw = (blockDim.x + 31) >> 5;
@@ -446,20 +454,20 @@ size_t moe_work_ints(int T, int k, int E, int tile_rows) {
 }
 
 
-cudaError_t moe_combine(float *h, const float *y, const float *gates, const int *slot_row, int T,
+cudaError_t moe_combine(float *h, const bf16 *y, const float *gates, const int *slot_row, int T,
                         int k, int d, bool accumulate, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   if (k > 16 || d % 4) return cudaErrorInvalidValue;
-  return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const float4 *)y, gates, slot_row, k,
+  return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, st, (float4 *)h, (const uint2 *)y, gates, slot_row, k,
                     d / 4, accumulate ? 1 : 0);
 }
 
-cudaError_t moe_combine_norm(float *h, const float *y, const float *gates, const int *slot_row,
+cudaError_t moe_combine_norm(float *h, const bf16 *y, const float *gates, const int *slot_row,
                              int T, int k, int d, const float *gain, float eps, bf16 *x_tiles,
                              cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   if (k > 16 || d % 64 || d > 4 * 1024) return cudaErrorInvalidValue;
-  return launch_pdl(combine_norm_kernel, dim3(T), dim3((d / 4 + 31) & ~31), 0, st, (float4 *)h, (const float4 *)y,
+  return launch_pdl(combine_norm_kernel, dim3(T), dim3((d / 4 + 31) & ~31), 0, st, (float4 *)h, (const uint2 *)y,
                     gates, slot_row, k, d / 4, gain, eps, x_tiles, T);
 }
 

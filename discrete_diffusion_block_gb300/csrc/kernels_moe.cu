@@ -63,6 +63,7 @@ constexpr int kFfnThreads = kFfnEpiThreads + 64;
 constexpr int kFfnProducerWarp = kFfnEpiWarps, kFfnMmaWarp = kFfnEpiWarps + 1;
 constexpr int kFfnBN = kExpertTileRows;  // rows per item = MMA N upper bound
 constexpr int kFfnQueue = 4;
+constexpr int kFfnSplitParts = 4;  // K-range parts of a split gate/up unit
 constexpr uint32_t kFfnATileBytes = 128 * 128;  // one weight tile, up to 128 rows x 64
 constexpr uint32_t kFfnBBytes = kFfnBN * 128;
 constexpr uint32_t kFfnStageBytes = 2 * kFfnATileBytes + kFfnBBytes;
@@ -114,7 +115,7 @@ struct FfnArgs {
   int *part_cnt;
   int E, d, F;
   bf16 *act;   // [item][F/64] tiles: SwiGLU output rows
-  float *y;    // [rows][d]
+  bf16 *y;     // [rows][d]
   int *err;
 };
 
@@ -223,10 +224,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   if (!g.fp8 && g.part_buf && nA > (int)gridDim.x) {
     const int rem = nA % (int)gridDim.x;
     if (rem > 0 && 4 * rem <= (int)gridDim.x && rem <= kFfnSplitUnits) {
-      const int s_try = 4;  // the last part reads every part's sums: more parts, more bytes
-      if (rem * s_try <= g.part_slots) {
+      // the last part reads every part's sums: more parts, more bytes
+      if (rem * kFfnSplitParts <= g.part_slots) {
         n_ov = rem;
-        S_ov = s_try;
+        S_ov = kFfnSplitParts;
       }
     }
   }
@@ -422,9 +423,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
       unsigned char *blk = inf.phase == 0
                                ? (unsigned char *)(g.act + ((size_t)inf.item * (g.F / 64) + (fb >> 6)) * kTileElems)
                                : nullptr;
-      auto store_act = [&](const uint32_t(&gv)[32], const uint32_t(&uv)[32], int col0) {
+      // gv, uv: the gate and up sums of NC consecutive token columns from col0
+      auto store_act = [&](const auto &gv, const auto &uv, int col0) {
+        constexpr int NC = sizeof(gv) / sizeof(uint32_t);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < NC / 2; ++j) {
           const float a0 = swiglu_f(__uint_as_float(gv[2 * j]), __uint_as_float(uv[2 * j]));
           const float a1 = swiglu_f(__uint_as_float(gv[2 * j + 1]), __uint_as_float(uv[2 * j + 1]));
           const float recv = __shfl_xor_sync(0xffffffffu, (lane & 1) ? a0 : a1, 1);
@@ -434,8 +437,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
             *(uint32_t *)(blk + t * 128 + ((((cc >> 3) ^ (t & 7)) << 4) | ((cc & 7) << 1))) = w;
         }
       };
-      // a split unit's part slots: [2 (gate, up)][128 token columns][128 features] fp32
-      // (a warp's 32 features of one column: one 128-byte line)
+      // a split unit's part slots: [2 (gate, up)][32 groups of 4 token
+      // columns][128 features][4] fp32 (a warp's 32 features of 4 columns:
+      // 512 contiguous bytes, one 16-byte vector a lane)
       float *const pslot = inf.part >= 0 ? g.part_buf + (size_t)inf.ov * inf.nparts * (kFfnPartSlotBytes / 4) : nullptr;
       if (inf.phase == 0 && inf.part >= 0) {
         // one K range of a split gate/up unit: its sums into its slot
@@ -449,10 +453,14 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           tc::tmem_ld32(tp + kFfnBN + col0, uv);
           tc::tmem_ld_wait(gv);
           tc::tmem_ld_wait(uv);
+          float *const pg = pb + ((size_t)(col0 >> 2) * 128 + lrow) * 4;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            pb[(size_t)(col0 + j) * 128 + lrow] = __uint_as_float(gv[j]);
-            pb[(size_t)(128 + col0 + j) * 128 + lrow] = __uint_as_float(uv[j]);
+          for (int j = 0; j < 8; ++j) {
+            *(float4 *)(pg + 512 * j) = make_float4(__uint_as_float(gv[4 * j]), __uint_as_float(gv[4 * j + 1]),
+                                                    __uint_as_float(gv[4 * j + 2]), __uint_as_float(gv[4 * j + 3]));
+            *(float4 *)(pg + 128 * 128 + 512 * j) =
+                make_float4(__uint_as_float(uv[4 * j]), __uint_as_float(uv[4 * j + 1]), __uint_as_float(uv[4 * j + 2]),
+                            __uint_as_float(uv[4 * j + 3]));
           }
         }
       } else if (inf.phase == 0) {
@@ -483,11 +491,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           store_act(gv, uv, col0);
         }
       } else {
-        // y[row][256 mt + 128 a + lrow] for the warp's token columns: for each
-        // token the warp stores 32 consecutive features (128 bytes).
+        // y[row][256 mt + 128 a + lrow] (bf16) for the warp's token columns:
+        // lanes 2i and 2i + 1 trade values so that each stores the feature
+        // pair (f, f + 1) of one token row; per token column pair the warp
+        // writes two 64-byte runs.
 #pragma unroll 1
         for (int a = 0; a < inf.n_acc; ++a) {
-          float *dst = g.y + (size_t)inf.b_row * g.d + 128 * (kDownBlocks * inf.mt + a) + lrow;
+          bf16 *dst = g.y + (size_t)inf.b_row * g.d + 128 * (kDownBlocks * inf.mt + a) + (lrow & ~1);
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             const int col0 = 64 * half + 32 * c;
@@ -496,8 +506,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
             tc::tmem_ld32(tp + a * kFfnBN + col0, v);
             tc::tmem_ld_wait(v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < inf.n_valid) dst[(size_t)(col0 + j) * g.d] = __uint_as_float(v[j]);
+            for (int j = 0; j < 16; ++j) {
+              const float a0 = __uint_as_float(v[2 * j]), a1 = __uint_as_float(v[2 * j + 1]);
+              const float recv = __shfl_xor_sync(0xffffffffu, (lane & 1) ? a0 : a1, 1);
+              const int t = col0 + 2 * j + (lane & 1);
+              const uint32_t w = (lane & 1) ? pack_bf16x2(recv, a1) : pack_bf16x2(a0, recv);
+              if (t < inf.n_valid) *(uint32_t *)(dst + (size_t)t * g.d) = w;
+            }
           }
         }
       }
@@ -516,33 +531,35 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
           epi_sync();
           if (split_last) {
             __threadfence();
+            // 16 token columns a pass: every part's gate and up vectors of
+            // them in flight at once, then summed in part order
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-              const int col0 = 64 * half + 32 * c;
+            for (int c = 0; c < 4; ++c) {
+              const int col0 = 64 * half + 16 * c;
               if (col0 >= inf.n_valid) break;
-              float sg[32], su[32];
+              float4 vg[kFfnSplitParts][4], vu[kFfnSplitParts][4];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) sg[j] = su[j] = 0.0f;
-#pragma unroll 1
-              for (int q = 0; q < inf.nparts; ++q) {  // part order: a fixed summation order
-                const float *pb = pslot + (size_t)q * (kFfnPartSlotBytes / 4) + (size_t)col0 * 128 + lrow;
-                float vg[32], vu[32];
+              for (int q = 0; q < kFfnSplitParts; ++q) {
+                const float *pb = pslot + (size_t)q * (kFfnPartSlotBytes / 4) + ((size_t)(col0 >> 2) * 128 + lrow) * 4;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  vg[j] = __ldcg(pb + (size_t)j * 128);
-                  vu[j] = __ldcg(pb + (size_t)(128 + j) * 128);
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  sg[j] += vg[j];
-                  su[j] += vu[j];
+                for (int k = 0; k < 4; ++k) {
+                  vg[q][k] = __ldcg((const float4 *)(pb + 512 * k));
+                  vu[q][k] = __ldcg((const float4 *)(pb + 128 * 128 + 512 * k));
                 }
               }
-              uint32_t gv[32], uv[32];
+              uint32_t gv[16], uv[16];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                gv[j] = __float_as_uint(sg[j]);
-                uv[j] = __float_as_uint(su[j]);
+              for (int k = 0; k < 4; ++k) {
+                float4 sg = vg[0][k], su = vu[0][k];
+#pragma unroll
+                for (int q = 1; q < kFfnSplitParts; ++q) {
+                  sg.x += vg[q][k].x, sg.y += vg[q][k].y, sg.z += vg[q][k].z, sg.w += vg[q][k].w;
+                  su.x += vu[q][k].x, su.y += vu[q][k].y, su.z += vu[q][k].z, su.w += vu[q][k].w;
+                }
+                gv[4 * k] = __float_as_uint(sg.x), gv[4 * k + 1] = __float_as_uint(sg.y);
+                gv[4 * k + 2] = __float_as_uint(sg.z), gv[4 * k + 3] = __float_as_uint(sg.w);
+                uv[4 * k] = __float_as_uint(su.x), uv[4 * k + 1] = __float_as_uint(su.y);
+                uv[4 * k + 2] = __float_as_uint(su.z), uv[4 * k + 3] = __float_as_uint(su.w);
               }
               store_act(gv, uv, col0);
             }
@@ -633,7 +650,7 @@ size_t moe_ffn_part_slots() { return (size_t)ffn_num_sms(); }
 
 cudaError_t moe_ffn(const bf16 *x_tiles, int rows, const bf16 *wgu, const bf16 *wd, const int *offs,
                     const int *work, const int *n_work, int max_work, int E, int d, int F, bf16 *act_tiles,
-                    float *y, int *err, cudaStream_t st, const Fp8Experts *fp8, float *part_buf,
+                    bf16 *y, int *err, cudaStream_t st, const Fp8Experts *fp8, float *part_buf,
                     int part_slots) {
   if (rows <= 0) return cudaSuccess;
   if (d % 128 || F % 64) return cudaErrorInvalidValue;

@@ -455,7 +455,10 @@ int dg_op_canvas_attention_noalloc(const uint16_t *q, const uint16_t *k_pool,
  * (device bf16 [T][d], already RMS-normalised),
  *   r = xn W_r^T; S = the top_k largest r (ties -> lower expert id);
  *   gates = softmax(r_S); y = sum_{e in S} gate_e W_down,e (silu(W_gate,e xn) * W_up,e xn)
- * Weights in the layouts of dg_get_weight (W_GATE_UP, W_DOWN).
+ * Weights in the layouts of dg_get_weight (W_GATE_UP, W_DOWN).  The SwiGLU
+ * activations and each expert's output row are rounded to bf16 (the bf16
+ * operands of the next product, and of the gate-weighted sum, which
+ * accumulates in fp32).
  * Outputs (device): y fp32 [T][d]; expert_ids int32 [T][top_k] (descending
  * router logit); gates fp32 [T][top_k].  workspace: dg_op_moe_workspace_bytes(). */
 size_t dg_op_moe_workspace_bytes(int32_t T, int32_t d, int32_t n_experts, int32_t top_k,
