@@ -250,7 +250,7 @@ def decode_all(dgp, m, seed, scfg):
 # and scatter unfused), over their algorithmic bytes from the same step's
 # experts touched (profiles/launch_list_full_decoder.md).  Below 1: the
 # weights stream once and part of the row, SwiGLU and output bytes stay in L2.
-FFN_TRAFFIC_RATIO = 7.937e9 / 8.681e9
+FFN_TRAFFIC_RATIO = 7.951e9 / 8.717e9
 
 
 def expert_bytes(cfg, experts_per_launch, rows_per_launch):
