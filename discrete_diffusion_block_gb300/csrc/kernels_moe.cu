@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) moe_ffn_kernel(FfnArgs g) {
   // quarter of the grid), run split along K into S parts: the parts spread
   // over the SMs instead of a nearly empty extra wave of whole units.
   int n_ov = 0, S_ov = 1;
-  if (!g.fp8 && g.part_buf && nA > (int)gridDim.x) {
+  // (only with at least one k-step per part)
+  if (!g.fp8 && g.part_buf && nA > (int)gridDim.x && g.d / tc::kBK >= kFfnSplitParts) {
     const int rem = nA % (int)gridDim.x;
     if (rem > 0 && 4 * rem <= (int)gridDim.x && rem <= kFfnSplitUnits) {
       // the last part reads every part's sums: more parts, more bytes

@@ -392,12 +392,14 @@ def test_moe_against_fp64(T, d, E, k, F):
     assert rel_err(y.cpu().numpy(), y_ref) <= TOL
 
 
-def test_moe_split_overflow_gate_up_units_against_fp64():
+@pytest.mark.parametrize("d", [512, 128])
+def test_moe_split_overflow_gate_up_units_against_fp64(d):
     """Gate/up units just past a whole number of waves run split along K (the
     last part sums the parts in order): a routing whose unit count exceeds the
-    SM count by at most a quarter of it, against the fp64 oracle."""
+    SM count by at most a quarter of it, against the fp64 oracle.  At d = 128
+    a unit has two k-steps, fewer than its four parts: it must run whole."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    d, k, F = 512, 8, 704
+    k, F = 8, 704
     mA = (F + 127) // 128
     found = None
     for E in (26, 28, 24, 30):
