@@ -51,5 +51,5 @@ def test_expert_bytes_formula():
     import discrete_diffusion_block_gb300 as dgp
     b = bench.expert_bytes(dgp.full_config(), 128, 2048)
     weights = 128 * (1408 * 2816 + 2816 * 704) * 2          # gate/up and down of 128 experts
-    rows = 2048 * 2816 * 2 + 2 * 2048 * 704 * 2 + 2048 * 2816 * 4  # x in, act out and in, y out
+    rows = 2048 * 2816 * 2 + 2 * 2048 * 704 * 2 + 2048 * 2816 * 2  # x in, act out and in, y out (bf16)
     assert b == {"expert_ffn": weights + rows}
