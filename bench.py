@@ -372,7 +372,7 @@ def gpu_arm(args):
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
                     "traffic_source": ("ncu dram bytes / algorithmic bytes of the 30 expert-FFN launches of one "
-                                       "eager decoder step (0.914), times this launch's algorithmic bytes"),
+                                       f"eager decoder step ({FFN_TRAFFIC_RATIO:.3f}), times this launch's algorithmic bytes"),
                     "peak_source": f"{peak_src} hbm_gbs",
                     "algorithmic_bytes_per_launch": round(per_launch[dom]), "measured_in": measured_in}
 
