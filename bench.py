@@ -552,15 +552,22 @@ def micro_results(dgp, which, reps):
         T, d, V = 256, 2816, 262144
         w = torch.empty(V * d, dtype=torch.bfloat16, device=dev)
         dgp.dg_op_fill_tiled_weights(w, V, d, 0, 2)
-        _, xt = synth.normal_bf16((T, d), seed=2)
-        x = torch.from_numpy(dgp.to_operand_tiles(xt.view(torch.int16).numpy())).view(torch.bfloat16).to(dev)
+        tiles = lambda t: torch.from_numpy(dgp.to_operand_tiles(t.view(torch.int16).numpy())).view(
+            torch.bfloat16).to(dev)
+        # the decoder's form first: an fp32 activation as a bf16 hi + lo pair
+        xf = torch.from_numpy(synth.normal((T, d), seed=2))
+        hi = xf.to(torch.bfloat16)
+        lo = (xf - hi.float()).to(torch.bfloat16)
+        x, x_lo = tiles(hi), tiles(lo)
         part = torch.empty(dgp.partials_bytes(T, V) // 4, dtype=torch.int32, device=dev)
-        sec = timed(lambda: dgp.dg_op_lm_head_partials(x, w, T, d, V, 1, 0, 1, part))
         fl = 2.0 * T * d * V
-        log("micro lm head")
-        out.append({"micro": "lm_head_partials", "shape": f"T={T} d={d} V={V} (single bf16 activation)",
-                    "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst,
-                    "GBps_weights": V * d * 2 / sec / 1e9})
+        for name, xl in (("hi + lo bf16 activation, the decoder's form: 2x the MMAs", x_lo),
+                         ("single bf16 activation", None)):
+            sec = timed(lambda: dgp.dg_op_lm_head_partials(x, w, T, d, V, 1, 0, 1, part, xn_lo=xl))
+            log("micro lm head")
+            out.append({"micro": "lm_head_partials", "shape": f"T={T} d={d} V={V} ({name})",
+                        "ms": sec * 1e3, "TFLOPs": fl / sec / 1e12, "frac_bf16": fl / sec / 1e12 / tf_burst,
+                        "GBps_weights": V * d * 2 / sec / 1e9})
         del w
     if which in ("sampler", "all"):
         C_, V = 256, 262144
