@@ -107,9 +107,10 @@ struct FfnArgs {
   int *done;   // [max_work] phase A units finished per item
   int *next;   // unit counter
   // Split gate/up units (the overflow past a whole number of waves): each
-  // part stores its sums in a slot of part_buf ([2][128 token columns][128
-  // features] fp32) and takes a ticket from part_cnt[unit]; the last part
-  // sums the parts in part order and runs the SwiGLU epilogue.
+  // part stores its sums in a slot of part_buf ([2 (gate, up)][32 groups of
+  // 4 token columns][128 features][4] fp32) and takes a ticket from
+  // part_cnt[unit]; the last part sums the parts in part order and runs the
+  // SwiGLU epilogue.
   float *part_buf;
   int part_slots;
   int *part_cnt;
