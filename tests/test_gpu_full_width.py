@@ -83,6 +83,12 @@ def test_full_width_layers_against_oracle(fp8):
     xn0 = bits_to_f32(xn_bits).astype(np.float64)
     logits = torch.empty(C, cfg.vocab, dtype=torch.float32, device=dev())
     dgp.dg_canvas_logits(m, logits)
+    # every cross-CTA reduction of the forward runs in a fixed order (split-K
+    # partials by rank, split-KV partials by split, router partials by rank,
+    # expert rows by slot): the same state gives the same bits
+    again = torch.empty_like(logits)
+    dgp.dg_canvas_logits(m, again)
+    assert torch.equal(logits.view(torch.int32), again.view(torch.int32))
     st = dgp.dg_read_canvas(m)
     route_canvas = [dgp.dg_read_routing(m, L) for L in range(nl)]
     kv_prompt = [dgp.dg_read_kv(m, L, 0, P) for L in range(nl)]

@@ -397,7 +397,9 @@ def test_moe_split_overflow_gate_up_units_against_fp64(d):
     """Gate/up units just past a whole number of waves run split along K (the
     last part sums the parts in order): a routing whose unit count exceeds the
     SM count by at most a quarter of it, against the fp64 oracle.  At d = 128
-    a unit has two k-steps, fewer than its four parts: it must run whole."""
+    a unit has two k-steps, fewer than its four parts: it must run whole.
+    The parts are summed in a fixed order, so a second launch on the same
+    inputs must give the same bits."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     k, F = 8, 704
     mA = (F + 127) // 128
@@ -418,6 +420,10 @@ def test_moe_split_overflow_gate_up_units_against_fp64(d):
             items = int(sum((c + 127) // 128 for c in np.bincount(gi.ravel(), minlength=E) if c > 0))
             n_a = items * mA
             if n_a > sms and 0 < n_a % sms <= sms // 4:
+                y2, ids2, gates2 = torch.empty_like(y), torch.empty_like(ids), torch.empty_like(gates)
+                dgp.dg_op_moe(xt.to(dev()), wr, wgu, wd, T, d, E, k, F, y2, ids2, gates2, ws)
+                assert torch.equal(ids, ids2) and torch.equal(gates, gates2)
+                assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
                 found = (T, E, xf, gi, gates.cpu().numpy(), y.cpu().numpy())
                 break
         if found:
