@@ -20,6 +20,16 @@
 // (per-item counter, release/acquire, then a proxy fence before the copies
 // read them).
 //
+// Overflow split.  When the phase A units exceed a whole number of waves by
+// at most a quarter of the grid, those last units would run as a nearly
+// empty extra wave of full units (a unit's k-steps are latency-bound, ~26 us
+// for d = 2816).  Instead each runs as four parts over a quarter of K on
+// separate SMs: a part stores its fp32 gate and up sums in a slot and takes
+// a ticket; the part whose ticket is last (every other part's sums already
+// stored) sums the four slots in part order -- the same bits whichever CTAs
+// ran the parts -- and writes and publishes the item's act tile like a
+// whole unit.  No part waits for another.
+//
 // Operands.  Expert weights and the item rows (gathered by moe_scatter, and
 // the SwiGLU output written here by phase A) are stored as 16 KB tiles of 128
 // rows x 64 columns already in the tensor core's swizzled shared-memory order,
@@ -37,9 +47,9 @@
 //   warps 0-7           -- epilogue straight from TMEM: warp w reads lane
 //                          quarter w % 4 and token columns 64 (w / 4) ..
 //                          64 (w / 4) + 63 of the pair, computes SwiGLU and
-//                          writes the act tile (A) or writes y rows (B) with
-//                          coalesced stores, while the tensor core already
-//                          works on the next unit.
+//                          writes the act tile (A) or writes bf16 y rows (B)
+//                          with coalesced stores, while the tensor core
+//                          already works on the next unit.
 // Every wait is bounded; a wait that gives up records an error word and makes
 // the CTA's later waits return at once.
 #include <cuda.h>
